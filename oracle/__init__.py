@@ -1,0 +1,187 @@
+"""CPU oracle for block-sparse KV-outer attention -- TEST INFRASTRUCTURE ONLY.
+
+A ctypes front end over ``mxsa_oracle.c`` (plain C, IEEE double).  Only the
+tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
+import this package; the product library never does, and shares no code
+with it.  See ``mxsa_oracle.c`` for the definitions and their sources.
+
+Functions whose parity is pinned by tests/test_oracle_pins.py:
+  attention_rows  -- dense-attention / masked-SDPA / closed-form pins
+  combine         -- partition-merge identity against a single softmax
+  build_index     -- brute-force per-key scan on small inputs
+  schedule        -- coverage / ordering / balance invariants
+  decode          -- every code against torch's own dtype conversions
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxsa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+
+DTYPE_CODE = {"bf16": 0, "fp16": 1, "fp8": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, pthreads)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class OracleProblem(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("total_q", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("topk", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+        ("causal", ctypes.c_int32), ("softmax_scale", ctypes.c_double), ("q_dtype", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        _lib.oracle_decode.restype = ctypes.c_double
+        _lib.oracle_decode.argtypes = [ctypes.c_int32, ctypes.c_uint32]
+        _lib.oracle_attention_rows.restype = ctypes.c_int
+        _lib.oracle_attention_rows.argtypes = [P] * 9 + [ctypes.c_int64, P, P, ctypes.c_int32]
+        _lib.oracle_combine.restype = None
+        _lib.oracle_combine.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P]
+        _lib.oracle_build_index.restype = ctypes.c_int
+        _lib.oracle_build_index.argtypes = [P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
+        _lib.oracle_schedule.restype = ctypes.c_int64
+        _lib.oracle_schedule.argtypes = [P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, P,
+                                         ctypes.c_int64, P, P]
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def problem(num_seqs, total_q, num_q_heads, num_kv_heads, topk, page_size, num_pages, max_pages_per_seq,
+            causal, q_dtype="bf16", kv_dtype="bf16", softmax_scale=0.0, head_dim=128) -> OracleProblem:
+    return OracleProblem(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, topk, page_size, num_pages,
+                         max_pages_per_seq, int(bool(causal)), float(softmax_scale), DTYPE_CODE[q_dtype],
+                         DTYPE_CODE[kv_dtype])
+
+
+def _bits(x) -> np.ndarray:
+    """Raw storage bits of a CPU torch tensor (or numpy array) as uint16/uint8."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.element_size() == 1:
+                return x.view(torch.uint8).numpy()
+            return x.view(torch.int16).numpy().view(np.uint16)
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x)
+
+
+def decode(dtype: str, bits: int) -> float:
+    return _load().oracle_decode(DTYPE_CODE[dtype], int(bits))
+
+
+def attention_rows(prob: OracleProblem, q, k_cache, v_cache, selected, block_tables, cu_seqlens_q,
+                   used_kv_lens, rows: Optional[np.ndarray] = None, nthreads: Optional[int] = None):
+    """(out [n, 128] float64, lse [n] float64) for rows t*Hq+h (None: all rows)."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
+    sel = _c(selected, np.int32)
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_seqlens_q, np.int64)
+    lens = _c(used_kv_lens, np.int32)
+    if rows is not None:
+        rows = _c(rows, np.int64)
+        n = len(rows)
+    else:
+        n = prob.total_q * prob.num_q_heads
+    out = np.zeros((n, prob.head_dim), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    nthreads = nthreads or os.cpu_count() or 1
+    rc = lib.oracle_attention_rows(ctypes.byref(prob), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(sel), _ptr(bt),
+                                   _ptr(cu), _ptr(lens), _ptr(rows) if rows is not None else None,
+                                   ctypes.c_int64(n), _ptr(out), _ptr(lse), nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_rows failed: {rc}")
+    return out, lse
+
+
+def combine(o_parts: np.ndarray, lse_parts: np.ndarray):
+    o = _c(o_parts, np.float64)
+    lse = _c(lse_parts, np.float64)
+    n, d = o.shape
+    out = np.zeros(d, dtype=np.float64)
+    lse_out = np.zeros(1, dtype=np.float64)
+    _load().oracle_combine(n, d, _ptr(o), _ptr(lse), _ptr(out), _ptr(lse_out))
+    return out, float(lse_out[0])
+
+
+def build_index(prob: OracleProblem, selected, cu_seqlens_q, used_kv_lens):
+    """Returns dict(nb, row_ptr, entries, slot_entry, flags)."""
+    lib = _load()
+    sel = _c(selected, np.int32)
+    cu = _c(cu_seqlens_q, np.int64)
+    lens = _c(used_kv_lens, np.int32)
+    cap_len = prob.max_pages_per_seq * prob.page_size
+    nb_cap = int(sum((min(max(int(L), 0), cap_len) + 127) // 128 for L in lens))
+    rp_cap = prob.num_kv_heads * nb_cap + 1
+    row_ptr = np.zeros(rp_cap, dtype=np.int32)
+    nslots = prob.total_q * prob.num_kv_heads * prob.topk
+    entries = np.zeros(max(nslots, 1), dtype=np.int32)
+    slot_entry = np.zeros(max(nslots, 1), dtype=np.int32)
+    nb = ctypes.c_int32(0)
+    nnz = ctypes.c_int32(0)
+    flags = ctypes.c_int32(0)
+    rc = lib.oracle_build_index(ctypes.byref(prob), _ptr(sel), _ptr(cu), _ptr(lens), ctypes.byref(nb),
+                                _ptr(row_ptr), ctypes.c_int64(rp_cap), _ptr(entries), _ptr(slot_entry),
+                                ctypes.byref(nnz), ctypes.byref(flags))
+    if rc != 0:
+        raise RuntimeError(f"oracle_build_index failed: {rc}")
+    nkeys = prob.num_kv_heads * nb.value
+    return dict(nb=nb.value, row_ptr=row_ptr[:nkeys + 1].copy(), entries=entries[:nnz.value].copy(),
+                slot_entry=slot_entry[:nslots].copy(), flags=flags.value)
+
+
+def schedule(prob: OracleProblem, used_kv_lens, index: dict, rows_per_item_tiles: int, num_ctas: int):
+    """Returns dict(items [n,4] int32, cost_prefix [n+1] int64, cta_ptr [P+1] int32)."""
+    lib = _load()
+    lens = _c(used_kv_lens, np.int32)
+    row_ptr = _c(index["row_ptr"], np.int32)
+    cap = max(int(row_ptr[-1]) + 1, 1)
+    items = np.zeros((cap, 4), dtype=np.int32)
+    cost = np.zeros(cap + 1, dtype=np.int64)
+    cta = np.zeros(num_ctas + 1, dtype=np.int32)
+    n = lib.oracle_schedule(ctypes.byref(prob), _ptr(lens), index["nb"], _ptr(row_ptr), rows_per_item_tiles,
+                            num_ctas, _ptr(items), ctypes.c_int64(cap), _ptr(cost), _ptr(cta))
+    if n < 0:
+        raise RuntimeError("oracle_schedule: item capacity exceeded")
+    return dict(items=items[:n].copy(), cost_prefix=cost[:n + 1].copy(), cta_ptr=cta)
+
+
+def problem_for(w, softmax_scale: float = 0.0) -> OracleProblem:
+    """The oracle problem struct of a generated workload."""
+    return problem(w.num_seqs, w.total_q, w.num_q_heads, w.num_kv_heads, w.topk, w.page_size, w.num_pages,
+                   w.max_pages_per_seq, w.causal, w.spec.q_dtype, w.spec.kv_dtype, softmax_scale)

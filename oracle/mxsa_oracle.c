@@ -1,0 +1,435 @@
+/*
+ * Oracle for block-sparse KV-outer attention -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU statement of what the GPU path
+ * computes.  Only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg may load this library; the product path never calls it.  It shares no
+ * code, header, table or constant with the CUDA library.
+ *
+ * Sources (fw-ai/minimax-kernels README):
+ *   - intro paragraph: a query attends only to the 128-token KV blocks it
+ *     selected; the KV-outer formulation loads a block once for every query
+ *     that selected it -- a reordering of the same sum, so the oracle loops
+ *     over queries instead;
+ *   - "Quick start": token-major q [Tq,Hq,128]; paged caches
+ *     [pages,Hkv,page_size,128] reached through block_tables; selections
+ *     [Tq,Hkv,topk] of 128-token logical blocks; cu_seqlens_q; used_kv_lens;
+ *     output [Tq,Hq,128] and FP32 lse [Hq,Tq];
+ *   - feature list under "Installation": BF16/FP16/FP8 inputs, head dim 128,
+ *     pages of 64 or 128 tokens, varlen batches, MHA/GQA/MQA, causal or not.
+ * Readings where the pages are silent (scale 1/sqrt(128), natural-log lse of
+ * the scaled scores, bottom-right causal alignment pos = L - Tq + i, GQA head
+ * h -> kv head h / G, -1 = no block, set semantics for repeated blocks,
+ * empty rows -> out 0 and lse -inf, unscaled e4m3fn) are listed in the
+ * design notes.
+ *
+ * All arithmetic is IEEE double.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_BF16 = 0, OR_FP16 = 1, OR_FP8_E4M3 = 2 };
+
+/* status bits shared in meaning (not in code) with the GPU library */
+enum {
+  OR_FLAG_SEL_RANGE = 1,   /* selection outside [-1, nblk) */
+  OR_FLAG_SEL_DUP = 2,     /* a block repeated within one (token, kv-head) row */
+  OR_FLAG_CAUSAL_LEN = 8,  /* causal with used_kv_len < Tq of the sequence */
+  OR_FLAG_LEN = 16,        /* used_kv_len < 0 or beyond the block-table capacity */
+  OR_FLAG_CU = 128         /* cu_seqlens_q not a valid partition of the tokens */
+};
+
+typedef struct {
+  int32_t num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, topk, page_size, num_pages,
+      max_pages_per_seq, causal;
+  double softmax_scale; /* 0 => 1/sqrt(head_dim) */
+  int32_t q_dtype, kv_dtype;
+} oracle_problem;
+
+/* ------------------------------------------------------------------ decode
+ * Exact decoding of the storage formats, written from the format
+ * definitions (IEEE-754 binary16; bfloat16 = upper half of binary32;
+ * OCP FP8 E4M3 "fn": bias 7, no infinities, S.1111.111 is NaN). */
+static double decode_bf16(uint32_t bits) {
+  uint32_t u = (bits & 0xFFFFu) << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static double decode_fp16(uint32_t bits) {
+  uint32_t s = (bits >> 15) & 1u, e = (bits >> 10) & 0x1Fu, m = bits & 0x3FFu;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24); /* subnormal: m/1024 * 2^-14 */
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp(1.0 + (double)m / 1024.0, (int)e - 15);
+  return s ? -v : v;
+}
+
+static double decode_e4m3(uint32_t bits) {
+  uint32_t s = (bits >> 7) & 1u, e = (bits >> 3) & 0xFu, m = bits & 0x7u;
+  double v;
+  if (e == 15 && m == 7)
+    return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9); /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+  return s ? -v : v;
+}
+
+double oracle_decode(int32_t dtype, uint32_t bits) {
+  switch (dtype) {
+    case OR_BF16: return decode_bf16(bits);
+    case OR_FP16: return decode_fp16(bits);
+    case OR_FP8_E4M3: return decode_e4m3(bits);
+    default: return NAN;
+  }
+}
+
+static double load_elem(const void* base, int32_t dtype, int64_t idx) {
+  if (dtype == OR_FP8_E4M3) return decode_e4m3(((const uint8_t*)base)[idx]);
+  return oracle_decode(dtype, ((const uint16_t*)base)[idx]);
+}
+
+/* sequence of token t: the s with cu[s] <= t < cu[s+1] (linear scan) */
+static int32_t seq_of_token(const int64_t* cu, int32_t B, int64_t t) {
+  for (int32_t s = 0; s < B; ++s)
+    if (cu[s] <= t && t < cu[s + 1]) return s;
+  return -1;
+}
+
+/* -------------------------------------------------------------- attention */
+typedef struct {
+  const oracle_problem* p;
+  const void *q, *k, *v;
+  const int32_t *sel, *bt, *lens;
+  const int64_t *cu, *rows;
+  int64_t nrows;
+  double *out, *lse;
+  int64_t next;
+  pthread_mutex_t mu;
+  int err;
+} attn_job;
+
+/* One output row (token t, query head h), straight from the definition:
+ *   K = union over selected blocks b of {p : 128 b <= p < min(128 b + 128, L)},
+ *       keeping p <= pos(t) when causal;
+ *   s_p = scale * q . k_p;  out = sum_p softmax(s)_p v_p;  lse = log sum_p exp(s_p). */
+static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double* lse_out) {
+  const oracle_problem* p = J->p;
+  const int32_t D = p->head_dim, Hq = p->num_q_heads, Hkv = p->num_kv_heads;
+  const int32_t G = Hq / Hkv, g = h / G, ps = p->page_size;
+  const double scale = p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)D);
+  for (int32_t d = 0; d < D; ++d) out[d] = 0.0;
+  *lse_out = -INFINITY;
+  int32_t s = seq_of_token(J->cu, p->num_seqs, t);
+  if (s < 0) return 0;
+  int64_t L = J->lens[s];
+  if (L < 0) L = 0;
+  if (L > (int64_t)p->max_pages_per_seq * ps) L = (int64_t)p->max_pages_per_seq * ps;
+  const int64_t Tq_s = J->cu[s + 1] - J->cu[s];
+  const int64_t pos = L - Tq_s + (t - J->cu[s]);
+  const int64_t nblk = (L + 127) / 128;
+
+  unsigned char* in_set = (unsigned char*)calloc((size_t)(L > 0 ? L : 1), 1);
+  double* qv = (double*)malloc(sizeof(double) * D);
+  double* sc = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  if (!in_set || !qv || !sc) {
+    free(in_set); free(qv); free(sc);
+    return -1;
+  }
+  for (int32_t k = 0; k < p->topk; ++k) {
+    int32_t b = J->sel[(t * Hkv + g) * p->topk + k];
+    if (b < 0 || b >= nblk) continue;
+    int64_t hi = 128 * (int64_t)b + 128 < L ? 128 * (int64_t)b + 128 : L;
+    for (int64_t pp = 128 * (int64_t)b; pp < hi; ++pp)
+      if (!p->causal || pp <= pos) in_set[pp] = 1;
+  }
+  for (int32_t d = 0; d < D; ++d) qv[d] = load_elem(J->q, p->q_dtype, (t * Hq + h) * (int64_t)D + d);
+
+  double m = -INFINITY;
+  int64_t count = 0;
+  for (int64_t pp = 0; pp < L; ++pp) {
+    if (!in_set[pp]) continue;
+    int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + pp / ps];
+    if (page < 0 || page >= p->num_pages) {
+      free(in_set); free(qv); free(sc);
+      return -2;
+    }
+    int64_t base = (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
+    double dot = 0.0;
+    for (int32_t d = 0; d < D; ++d) dot += qv[d] * load_elem(J->k, p->kv_dtype, base + d);
+    sc[pp] = scale * dot;
+    if (sc[pp] > m) m = sc[pp];
+    ++count;
+  }
+  if (count > 0) {
+    double l = 0.0;
+    for (int64_t pp = 0; pp < L; ++pp) {
+      if (!in_set[pp]) continue;
+      int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + pp / ps];
+      int64_t base = (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
+      double w = exp(sc[pp] - m);
+      l += w;
+      for (int32_t d = 0; d < D; ++d) out[d] += w * load_elem(J->v, p->kv_dtype, base + d);
+    }
+    for (int32_t d = 0; d < D; ++d) out[d] /= l;
+    *lse_out = m + log(l);
+  }
+  free(in_set); free(qv); free(sc);
+  return 0;
+}
+
+static void* attn_worker(void* arg) {
+  attn_job* J = (attn_job*)arg;
+  const int32_t D = J->p->head_dim, Hq = J->p->num_q_heads;
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    int64_t i = J->next++;
+    pthread_mutex_unlock(&J->mu);
+    if (i >= J->nrows) break;
+    int64_t r = J->rows ? J->rows[i] : i;
+    int rc = attn_row(J, r / Hq, (int32_t)(r % Hq), J->out + i * D, J->lse + i);
+    if (rc) {
+      pthread_mutex_lock(&J->mu);
+      J->err = rc;
+      pthread_mutex_unlock(&J->mu);
+    }
+  }
+  return NULL;
+}
+
+/* Attention for `nrows` rows given as flat indices t*Hq + h (rows == NULL:
+ * every row in order).  out: [nrows][head_dim] double; lse: [nrows] double.
+ * Returns 0, or -1 (out of memory) / -2 (a needed page id is invalid) /
+ * -3 (bad arguments). */
+int oracle_attention_rows(const oracle_problem* p, const void* q, const void* k, const void* v,
+                          const int32_t* sel, const int32_t* block_tables, const int64_t* cu_seqlens_q,
+                          const int32_t* used_kv_lens, const int64_t* rows, int64_t nrows, double* out,
+                          double* lse, int32_t nthreads) {
+  if (!p || p->num_kv_heads <= 0 || p->num_q_heads % p->num_kv_heads) return -3;
+  attn_job J;
+  memset(&J, 0, sizeof J);
+  J.p = p; J.q = q; J.k = k; J.v = v; J.sel = sel; J.bt = block_tables; J.cu = cu_seqlens_q;
+  J.lens = used_kv_lens; J.rows = rows; J.out = out; J.lse = lse;
+  J.nrows = rows ? nrows : (int64_t)p->total_q * p->num_q_heads;
+  pthread_mutex_init(&J.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, attn_worker, &J);
+  for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return J.err;
+}
+
+/* ---------------------------------------------------------------- combine
+ * Merge of n partial results (o_k, lse_k) of disjoint key subsets of one
+ * row into the softmax over their union:
+ *   M = max lse_k,  w_k = exp(lse_k - M),  out = sum w_k o_k / sum w_k,
+ *   lse = M + log sum w_k.
+ * Parts with lse = -inf (empty subsets) carry no weight; no part left gives
+ * out = 0 and lse = -inf. */
+void oracle_combine(int32_t n, int32_t d, const double* o, const double* lse, double* out, double* lse_out) {
+  double M = -INFINITY;
+  for (int32_t k = 0; k < n; ++k)
+    if (lse[k] > M) M = lse[k];
+  for (int32_t j = 0; j < d; ++j) out[j] = 0.0;
+  if (M == -INFINITY) {
+    *lse_out = -INFINITY;
+    return;
+  }
+  double W = 0.0;
+  for (int32_t k = 0; k < n; ++k) {
+    if (lse[k] == -INFINITY) continue;
+    double w = exp(lse[k] - M);
+    W += w;
+    for (int32_t j = 0; j < d; ++j) out[j] += w * o[(int64_t)k * d + j];
+  }
+  for (int32_t j = 0; j < d; ++j) out[j] /= W;
+  *lse_out = M + log(W);
+}
+
+/* ------------------------------------------------------------ block index
+ * The inverted index of the KV-outer formulation ("loads a selected KV
+ * block once and processes all queries that selected it"): for every
+ * (kv head g, sequence s, block b) the ordered list of the selection slots
+ * that chose it.
+ *
+ * Definition (exact, integer):
+ *   nblk_s  = ceil(L_s / 128) with L_s clamped to [0, max_pages * page_size];
+ *   blk_off = exclusive prefix sum of nblk;  NB = sum nblk;
+ *   slot    = (t * Hkv + g) * topk + k, taken in increasing order;
+ *   a slot is an entry unless its block is -1, out of [0, nblk_s) (flag 1),
+ *   equal to an earlier slot's block in the same (t, g) row (flag 2), or,
+ *   when causal, starts after the token's position (128 b > pos(t));
+ *   key(slot) = g * NB + blk_off[s] + b;
+ *   entries   = entry slots sorted by (key, slot);  row_ptr = CSR offsets
+ *               over the Hkv * NB keys;  slot_entry[slot] = position or -1.
+ * Outputs: row_ptr[Hkv*NB + 1] (capacity row_ptr_cap), entries[nnz],
+ * slot_entry[total_q*Hkv*topk].  Returns 0, or -1 (capacity / memory). */
+typedef struct {
+  int64_t key;
+  int64_t slot;
+} key_slot;
+
+static int cmp_key_slot(const void* a, const void* b) {
+  const key_slot* x = (const key_slot*)a;
+  const key_slot* y = (const key_slot*)b;
+  if (x->key != y->key) return x->key < y->key ? -1 : 1;
+  if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;
+  return 0;
+}
+
+int oracle_build_index(const oracle_problem* p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
+                       int32_t* nb_out, int32_t* row_ptr, int64_t row_ptr_cap, int32_t* entries,
+                       int32_t* slot_entry, int32_t* nnz_out, int32_t* flags_out) {
+  const int32_t B = p->num_seqs, Hkv = p->num_kv_heads, K = p->topk;
+  const int64_t cap_len = (int64_t)p->max_pages_per_seq * p->page_size;
+  int32_t flags = 0;
+  int64_t* nblk = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t* blk_off = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  const int64_t nslots = (int64_t)p->total_q * Hkv * K;
+  key_slot* ks = (key_slot*)malloc(sizeof(key_slot) * (size_t)(nslots > 0 ? nslots : 1));
+  if (!nblk || !blk_off || !ks) {
+    free(nblk); free(blk_off); free(ks);
+    return -1;
+  }
+  if (cu[0] != 0 || cu[B] != p->total_q) flags |= OR_FLAG_CU;
+  for (int32_t s = 0; s < B; ++s)
+    if (cu[s + 1] < cu[s]) flags |= OR_FLAG_CU;
+  int64_t NB = 0;
+  for (int32_t s = 0; s < B; ++s) {
+    int64_t L = lens[s];
+    if (L < 0 || L > cap_len) flags |= OR_FLAG_LEN;
+    if (L < 0) L = 0;
+    if (L > cap_len) L = cap_len;
+    if (p->causal && L < cu[s + 1] - cu[s]) flags |= OR_FLAG_CAUSAL_LEN;
+    nblk[s] = (L + 127) / 128;
+    blk_off[s] = NB;
+    NB += nblk[s];
+  }
+  const int64_t nkeys = (int64_t)Hkv * NB;
+  if (nkeys + 1 > row_ptr_cap) {
+    free(nblk); free(blk_off); free(ks);
+    return -1;
+  }
+  int64_t n = 0;
+  for (int64_t slot = 0; slot < nslots; ++slot) slot_entry[slot] = -1;
+  for (int64_t t = 0; t < p->total_q; ++t) {
+    int32_t s = seq_of_token(cu, B, t);
+    for (int32_t g = 0; g < Hkv; ++g) {
+      for (int32_t k = 0; k < K; ++k) {
+        int64_t slot = (t * Hkv + g) * K + k;
+        int32_t b = sel[slot];
+        if (b == -1 || s < 0) continue;
+        if (b < -1 || b >= nblk[s]) {
+          flags |= OR_FLAG_SEL_RANGE;
+          continue;
+        }
+        int dup = 0;
+        for (int32_t k2 = 0; k2 < k; ++k2)
+          if (sel[(t * Hkv + g) * K + k2] == b) dup = 1;
+        if (dup) {
+          flags |= OR_FLAG_SEL_DUP;
+          continue;
+        }
+        if (p->causal) {
+          int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
+          int64_t pos = L - (cu[s + 1] - cu[s]) + (t - cu[s]);
+          if (128 * (int64_t)b > pos) continue;
+        }
+        ks[n].key = g * NB + blk_off[s] + b;
+        ks[n].slot = slot;
+        ++n;
+      }
+    }
+  }
+  qsort(ks, (size_t)n, sizeof(key_slot), cmp_key_slot);
+  for (int64_t key = 0; key <= nkeys; ++key) row_ptr[key] = 0;
+  for (int64_t i = 0; i < n; ++i) row_ptr[ks[i].key + 1] += 1;
+  for (int64_t key = 0; key < nkeys; ++key) row_ptr[key + 1] += row_ptr[key];
+  for (int64_t i = 0; i < n; ++i) {
+    entries[i] = (int32_t)ks[i].slot;
+    slot_entry[ks[i].slot] = (int32_t)i;
+  }
+  *nb_out = (int32_t)NB;
+  *nnz_out = (int32_t)n;
+  *flags_out = flags;
+  free(nblk); free(blk_off); free(ks);
+  return 0;
+}
+
+/* --------------------------------------------------------------- schedule
+ * Load-balancing schedule over the index ("load-balancing scheduler" in the
+ * README's test list; the splitting rule and cost model are this library's).
+ *
+ * Definition (exact, integer):
+ *   G = Hq / Hkv;  E = rows_per_item_tiles * max(1, 128 / G) entries per item;
+ *   for each key with cnt > 0, in key order: n = ceil(cnt / E) items, item i
+ *     covering entries [row_ptr[key] + i*cnt/n, row_ptr[key] + (i+1)*cnt/n);
+ *   cost(item) = valid_tokens(key) * kv_weight + tiles(item) * 256 + rows(item) * 2
+ *     with valid_tokens = min(128, L_s - 128 b), kv_weight = 2 (16-bit caches)
+ *     or 1 (FP8), tiles = ceil(entries / max(1, 128 / G)), rows = entries * G;
+ *   prefix = exclusive prefix sum of cost over items, C = total;
+ *   cta_ptr[c] = #{items i : prefix[i] < floor(c * C / P)}  for c = 0..P.
+ * items[4*i..] = {key, entry_begin, n_entries, 0}.  Returns the item count,
+ * or -1 when `items_cap` is too small. */
+int64_t oracle_schedule(const oracle_problem* p, const int32_t* lens, int32_t nb, const int32_t* row_ptr,
+                        int32_t rows_per_item_tiles, int32_t num_ctas, int32_t* items, int64_t items_cap,
+                        int64_t* cost_prefix, int32_t* cta_ptr) {
+  const int32_t B = p->num_seqs, Hkv = p->num_kv_heads;
+  const int32_t G = p->num_q_heads / Hkv;
+  const int32_t per_tile = 128 / G > 0 ? 128 / G : 1;
+  const int64_t E = (int64_t)rows_per_item_tiles * per_tile;
+  const int32_t kvw = p->kv_dtype == OR_FP8_E4M3 ? 1 : 2;
+  const int64_t cap_len = (int64_t)p->max_pages_per_seq * p->page_size;
+  int64_t n_items = 0, C = 0;
+  for (int64_t key = 0; key < (int64_t)Hkv * nb; ++key) {
+    int64_t cnt = row_ptr[key + 1] - row_ptr[key];
+    if (cnt <= 0) continue;
+    /* (g, s, b) of the key: key = g*NB + blk_off[s] + b */
+    int64_t r = key % nb;
+    int32_t s = 0;
+    int64_t off = 0;
+    for (s = 0; s < B; ++s) {
+      int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
+      int64_t nblk = (L + 127) / 128;
+      if (r < off + nblk) break;
+      off += nblk;
+    }
+    int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
+    int64_t b = r - off;
+    int64_t valid = L - 128 * b < 128 ? L - 128 * b : 128;
+    int64_t n = (cnt + E - 1) / E;
+    for (int64_t i = 0; i < n; ++i) {
+      int64_t e0 = i * cnt / n, e1 = (i + 1) * cnt / n;
+      if (n_items >= items_cap) return -1;
+      int64_t ne = e1 - e0;
+      items[4 * n_items + 0] = (int32_t)key;
+      items[4 * n_items + 1] = (int32_t)(row_ptr[key] + e0);
+      items[4 * n_items + 2] = (int32_t)ne;
+      items[4 * n_items + 3] = 0;
+      int64_t cost = valid * kvw + ((ne + per_tile - 1) / per_tile) * 256 + ne * G * 2;
+      cost_prefix[n_items] = C;
+      C += cost;
+      ++n_items;
+    }
+  }
+  cost_prefix[n_items] = C;
+  for (int32_t c = 0; c <= num_ctas; ++c) {
+    int64_t target = (int64_t)c * C / num_ctas;
+    int64_t cnt = 0;
+    for (int64_t i = 0; i < n_items; ++i)
+      if (cost_prefix[i] < target) ++cnt;
+    cta_ptr[c] = (int32_t)cnt;
+  }
+  return n_items;
+}
