@@ -1,0 +1,267 @@
+"""Block-sparse KV-outer attention for GB300: thin Python binding of libmxsa.
+
+Argument marshalling only -- every step runs in the library's CUDA kernels;
+PyTorch provides device memory and streams.  The entry points mirror the C
+ABI in include/mxsa.h (build_index, schedule, kvouter_fwd, combine,
+read_status), plus ``kvouter_attention`` with the call shape of the
+fw-ai/minimax-kernels README's Quick start and ``SparseAttention`` which
+keeps the workspaces of one problem shape for repeated calls.
+
+There is no fallback: the first call into the library raises ImportError
+when libmxsa.so has not been built, and every library error is raised as
+``MxsaError``.  (The package itself imports without the library so that the
+build script and the input generator stay usable.)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libmxsa.so")
+
+BF16, FP16, FP8_E4M3 = 0, 1, 2
+_DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16, torch.float8_e4m3fn: FP8_E4M3}
+_CODE_DTYPE = {v: k for k, v in _DTYPE_CODE.items()}
+
+FLAG_NAMES = {1: "SEL_RANGE", 2: "SEL_DUP", 4: "PAGE", 8: "CAUSAL_LEN", 16: "LEN", 32: "TIMEOUT",
+              64: "SCHEDULE", 128: "CU"}
+STATUS_NAMES = {0: "MXSA_OK", 1: "MXSA_ERR_INVALID_ARG", 2: "MXSA_ERR_UNSUPPORTED", 3: "MXSA_ERR_WORKSPACE",
+                4: "MXSA_ERR_CUDA", 5: "MXSA_ERR_DATA"}
+EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_build_index", "mxsa_schedule",
+            "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
+            "mxsa_sched_layout_query"]
+
+
+class MxsaError(RuntimeError):
+    def __init__(self, status: int, what: str, flags: int = 0):
+        self.status = status
+        self.flags = flags
+        names = [n for b, n in FLAG_NAMES.items() if flags & b]
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}" + (f" flags={names}" if names else ""))
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_q", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+    def key(self):
+        return tuple(getattr(self, f) for f, _ in self._fields_)
+
+
+class IndexLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "seq_info", "token_seq", "slot_entry", "bitmap", "kmap",
+                                               "counts", "row_ptr", "entries", "active_keys", "active_valid",
+                                               "lookback", "total")] + \
+               [(n, ctypes.c_int64) for n in ("keys_cap", "nslots", "bitmap_words_cap", "kmap_bytes_cap",
+                                              "tiles_cap")]
+
+
+class SchedLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "items", "cost_prefix", "cta_ptr", "lookback", "total")] + \
+               [(n, ctypes.c_int64) for n in ("items_cap", "tiles_cap")]
+
+
+def _load_library() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmxsa is not built ({LIB_PATH} missing); run __graft_entry__.build() or "
+                          f"python -m block_sparse_attention_builder_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    lib.mxsa_version.restype = ctypes.c_int32
+    lib.mxsa_status_string.restype = ctypes.c_char_p
+    lib.mxsa_status_string.argtypes = [ctypes.c_int]
+    sig = {
+        "mxsa_workspace_size": [P, P, P, P],
+        "mxsa_build_index": [P, P, P, P, P, S, P],
+        "mxsa_schedule": [P, P, S, ctypes.c_int32, P, S, P],
+        "mxsa_kvouter_fwd": [P, P, P, P, P, P, S, P, S, ctypes.c_int32, P, S, P],
+        "mxsa_combine": [P, P, S, P, S, P, P, P],
+        "mxsa_read_status": [P, P, P],
+        "mxsa_index_layout_query": [P, P],
+        "mxsa_sched_layout_query": [P, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = args
+    return lib
+
+
+_lib_handle: Optional[ctypes.CDLL] = None
+
+
+def library() -> ctypes.CDLL:
+    global _lib_handle
+    if _lib_handle is None:
+        _lib_handle = _load_library()
+    return _lib_handle
+
+
+class _LazyLib:
+    def __getattr__(self, name):
+        return getattr(library(), name)
+
+
+_lib = _LazyLib()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MxsaError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_problem(num_seqs, total_q, num_q_heads, num_kv_heads, topk, page_size, num_pages, max_pages_per_seq,
+                 causal=False, softmax_scale=0.0, q_dtype=torch.bfloat16, kv_dtype=None, head_dim=128) -> Problem:
+    kv_dtype = q_dtype if kv_dtype is None else kv_dtype
+    return Problem(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, topk, page_size, num_pages,
+                   max_pages_per_seq, int(bool(causal)), float(softmax_scale or 0.0), _DTYPE_CODE[q_dtype],
+                   _DTYPE_CODE[kv_dtype])
+
+
+def workspace_size(prob: Problem) -> Tuple[int, int, int]:
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.mxsa_workspace_size(ctypes.byref(prob), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+           "mxsa_workspace_size")
+    return a.value, b.value, c.value
+
+
+def index_layout(prob: Problem) -> IndexLayout:
+    L = IndexLayout()
+    _check(_lib.mxsa_index_layout_query(ctypes.byref(prob), ctypes.byref(L)), "mxsa_index_layout_query")
+    return L
+
+
+def sched_layout(prob: Problem) -> SchedLayout:
+    L = SchedLayout()
+    _check(_lib.mxsa_sched_layout_query(ctypes.byref(prob), ctypes.byref(L)), "mxsa_sched_layout_query")
+    return L
+
+
+def build_index(prob, sel, cu_seqlens_q, used_kv_lens, index_ws, stream=None):
+    _check(_lib.mxsa_build_index(ctypes.byref(prob), _ptr(sel), _ptr(cu_seqlens_q), _ptr(used_kv_lens),
+                                 _ptr(index_ws), index_ws.numel() * index_ws.element_size(), _stream(stream)),
+           "mxsa_build_index")
+
+
+def schedule(prob, index_ws, sched_ws, num_ctas=0, stream=None):
+    _check(_lib.mxsa_schedule(ctypes.byref(prob), _ptr(index_ws), index_ws.numel() * index_ws.element_size(),
+                              int(num_ctas), _ptr(sched_ws), sched_ws.numel() * sched_ws.element_size(),
+                              _stream(stream)), "mxsa_schedule")
+
+
+def kvouter_fwd(prob, q, k_cache, v_cache, block_tables, index_ws, sched_ws, partial_ws, num_ctas=0, stream=None):
+    _check(_lib.mxsa_kvouter_fwd(ctypes.byref(prob), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                 _ptr(index_ws), index_ws.numel() * index_ws.element_size(), _ptr(sched_ws),
+                                 sched_ws.numel() * sched_ws.element_size(), int(num_ctas), _ptr(partial_ws),
+                                 partial_ws.numel() * partial_ws.element_size(), _stream(stream)),
+           "mxsa_kvouter_fwd")
+
+
+def combine(prob, index_ws, partial_ws, out, lse=None, stream=None):
+    _check(_lib.mxsa_combine(ctypes.byref(prob), _ptr(index_ws), index_ws.numel() * index_ws.element_size(),
+                             _ptr(partial_ws), partial_ws.numel() * partial_ws.element_size(), _ptr(out), _ptr(lse),
+                             _stream(stream)), "mxsa_combine")
+
+
+def read_status(index_ws, stream=None) -> int:
+    flags = ctypes.c_int32(0)
+    st = _lib.mxsa_read_status(_ptr(index_ws), _stream(stream), ctypes.byref(flags))
+    if st not in (0, 5):
+        raise MxsaError(st, "mxsa_read_status")
+    return flags.value
+
+
+@dataclass
+class Workspaces:
+    index: torch.Tensor
+    sched: torch.Tensor
+    partial: torch.Tensor
+
+
+def allocate_workspaces(prob: Problem, device) -> Workspaces:
+    ib, sb, pb = workspace_size(prob)
+    return Workspaces(torch.empty(ib, dtype=torch.uint8, device=device),
+                      torch.empty(sb, dtype=torch.uint8, device=device),
+                      torch.empty(pb, dtype=torch.uint8, device=device))
+
+
+class SparseAttention:
+    """The four steps for one problem shape, with workspaces kept across calls."""
+
+    def __init__(self, prob: Problem, device="cuda", num_ctas: int = 0):
+        self.prob = prob
+        self.device = torch.device(device)
+        self.ws = allocate_workspaces(prob, self.device)
+        self.num_ctas = num_ctas
+
+    def __call__(self, q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, out=None,
+                 lse=None, return_lse=True, stream=None):
+        p = self.prob
+        if out is None:
+            out = torch.empty(p.total_q, p.num_q_heads, 128, dtype=q.dtype, device=q.device)
+        if return_lse and lse is None:
+            lse = torch.empty(p.num_q_heads, p.total_q, dtype=torch.float32, device=q.device)
+        build_index(p, selected, cu_seqlens_q, used_kv_lens, self.ws.index, stream)
+        schedule(p, self.ws.index, self.ws.sched, self.num_ctas, stream)
+        kvouter_fwd(p, q, k_cache, v_cache, block_tables, self.ws.index, self.ws.sched, self.ws.partial,
+                    self.num_ctas, stream)
+        combine(p, self.ws.index, self.ws.partial, out, lse if return_lse else None, stream)
+        return out, (lse if return_lse else None)
+
+    def status(self, stream=None) -> int:
+        return read_status(self.ws.index, stream)
+
+
+def kvouter_attention(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, page_size,
+                      causal=False, softmax_scale=None, return_lse=False, num_ctas=0, check=True):
+    """Block-sparse KV-outer attention with the README Quick-start call shape.
+
+    q [Tq, Hq, 128] bf16/fp16; k_cache/v_cache [pages, Hkv, page_size, 128]
+    (q's dtype or float8_e4m3fn); selected int32 [Tq, Hkv, topk]; block_tables
+    int32 [B, max_pages]; cu_seqlens_q int64 [B+1]; used_kv_lens int32 [B].
+    Returns (output [Tq, Hq, 128], lse [Hq, Tq] float32 or None).  With
+    check=True the device status word is read (one stream sync) and data
+    errors are raised.
+    """
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("selected", selected),
+                    ("block_tables", block_tables), ("cu_seqlens_q", cu_seqlens_q), ("used_kv_lens", used_kv_lens)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if selected.dtype != torch.int32 or block_tables.dtype != torch.int32 or used_kv_lens.dtype != torch.int32:
+        raise ValueError("selected, block_tables and used_kv_lens must be int32")
+    if cu_seqlens_q.dtype != torch.int64:
+        raise ValueError("cu_seqlens_q must be int64")
+    Tq, Hq, D = q.shape
+    pages, Hkv, ps, D2 = k_cache.shape
+    if k_cache.shape != v_cache.shape or D2 != D or ps != page_size:
+        raise ValueError("k_cache / v_cache shapes disagree with q or page_size")
+    prob = make_problem(len(used_kv_lens), Tq, Hq, Hkv, selected.shape[2], page_size, pages,
+                        block_tables.shape[1], causal, softmax_scale or 0.0, q.dtype, k_cache.dtype, head_dim=D)
+    attn = SparseAttention(prob, q.device, num_ctas)
+    out, lse = attn(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, return_lse=return_lse)
+    if check:
+        flags = attn.status()
+        if flags:
+            raise MxsaError(5, "kvouter_attention", flags)
+    return out, lse

@@ -1,0 +1,297 @@
+// C-ABI entry points of libmxsa: argument validation, workspace layout and
+// the launches of the four steps (index builder, scheduler, KV-outer
+// forward, combine).  Nothing here allocates memory.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+
+namespace mxsa {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+int64_t max_blocks_per_seq(const mxsa_problem& p) {
+  return ((int64_t)p.max_pages_per_seq * p.page_size + 127) / 128;
+}
+
+mxsa_status validate_problem(const mxsa_problem& p) {
+  if (p.num_seqs < 1 || p.total_q < 0 || p.num_q_heads < 1 || p.num_kv_heads < 1 || p.topk < 1 ||
+      p.num_pages < 1 || p.max_pages_per_seq < 1 || (p.causal != 0 && p.causal != 1) ||
+      !(p.softmax_scale >= 0.f) || !std::isfinite(p.softmax_scale))
+    return MXSA_ERR_INVALID_ARG;
+  if (p.num_q_heads % p.num_kv_heads != 0) return MXSA_ERR_INVALID_ARG;
+  if (p.head_dim != 128) return MXSA_ERR_UNSUPPORTED;
+  if (p.num_q_heads / p.num_kv_heads > 128) return MXSA_ERR_UNSUPPORTED;
+  if (p.topk > 256) return MXSA_ERR_UNSUPPORTED;
+  if (p.page_size != 64 && p.page_size != 128) return MXSA_ERR_UNSUPPORTED;
+  if (p.q_dtype != MXSA_BF16 && p.q_dtype != MXSA_FP16) return MXSA_ERR_UNSUPPORTED;
+  if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3) return MXSA_ERR_UNSUPPORTED;
+  const int64_t nslots = (int64_t)p.total_q * p.num_kv_heads * p.topk;
+  if (nslots >= (1ll << 26)) return MXSA_ERR_UNSUPPORTED;  // slot ids and packed scan fields
+  const int64_t keys_cap = (int64_t)p.num_kv_heads * p.num_seqs * max_blocks_per_seq(p);
+  if (keys_cap >= (1ll << 31) - 1) return MXSA_ERR_UNSUPPORTED;
+  if ((int64_t)p.num_pages * p.num_kv_heads >= (1ll << 31)) return MXSA_ERR_UNSUPPORTED;
+  if ((int64_t)p.max_pages_per_seq * p.page_size >= (1ll << 30)) return MXSA_ERR_UNSUPPORTED;
+  return MXSA_OK;
+}
+
+mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L) {
+  mxsa_status s = validate_problem(p);
+  if (s != MXSA_OK) return s;
+  std::memset(L, 0, sizeof(*L));
+  const int64_t B = p.num_seqs, Tq = p.total_q, Hkv = p.num_kv_heads;
+  const int64_t mb = max_blocks_per_seq(p);
+  L->keys_cap = Hkv * B * mb;
+  L->nslots = Tq * Hkv * p.topk;
+  L->bitmap_words_cap = Hkv * mb * ((Tq + 31) / 32 + B);
+  L->kmap_bytes_cap = Hkv * mb * Tq;
+  L->tiles_cap = (L->keys_cap + kScanTile - 1) / kScanTile;
+  const int64_t act = L->keys_cap < L->nslots ? L->keys_cap : L->nslots;
+  size_t o = 0;
+  L->header = o;       o = align_up(o + kHdrInts * 4);
+  L->seq_info = o;     o = align_up(o + (size_t)B * sizeof(SeqInfo));
+  L->token_seq = o;    o = align_up(o + (size_t)Tq * 4);
+  L->slot_entry = o;   o = align_up(o + (size_t)L->nslots * 4);
+  L->bitmap = o;       o = align_up(o + (size_t)L->bitmap_words_cap * 4);
+  L->kmap = o;         o = align_up(o + (size_t)L->kmap_bytes_cap);
+  L->counts = o;       o = align_up(o + (size_t)L->keys_cap * 4);
+  L->row_ptr = o;      o = align_up(o + (size_t)(L->keys_cap + 1) * 4);
+  L->entries = o;      o = align_up(o + (size_t)L->nslots * 4);
+  L->active_keys = o;  o = align_up(o + (size_t)act * 4);
+  L->active_valid = o; o = align_up(o + (size_t)act * 4);
+  L->lookback = o;     o = align_up(o + (size_t)L->tiles_cap * 8);
+  L->total = o;
+  return MXSA_OK;
+}
+
+mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L) {
+  mxsa_index_layout il;
+  mxsa_status s = index_layout(p, &il);
+  if (s != MXSA_OK) return s;
+  std::memset(L, 0, sizeof(*L));
+  L->items_cap = il.nslots > 0 ? il.nslots : 1;
+  const int64_t act = il.keys_cap < il.nslots ? il.keys_cap : il.nslots;
+  L->tiles_cap = (act + kScanTile - 1) / kScanTile;
+  size_t o = 0;
+  L->header = o;      o = align_up(o + kSchInts * 4);
+  L->items = o;       o = align_up(o + (size_t)L->items_cap * 16);
+  L->cost_prefix = o; o = align_up(o + (size_t)(L->items_cap + 1) * 8);
+  L->cta_ptr = o;     o = align_up(o + (size_t)(MXSA_MAX_CTAS + 1) * 4);
+  L->lookback = o;    o = align_up(o + (size_t)(L->tiles_cap > 0 ? L->tiles_cap : 1) * 8);
+  L->total = o;
+  return MXSA_OK;
+}
+
+static void partial_layout(const mxsa_problem& p, size_t* o_off, size_t* lse_off, size_t* total) {
+  const int64_t nslots = (int64_t)p.total_q * p.num_kv_heads * p.topk;
+  const int64_t G = p.num_q_heads / p.num_kv_heads;
+  *o_off = 0;
+  *lse_off = align_up((size_t)nslots * G * 128 * 4);
+  *total = align_up(*lse_off + (size_t)nslots * G * 4);
+  if (*total == 0) *total = kAlign;
+}
+
+IndexPtrs index_ptrs(const mxsa_problem& p, void* ws) {
+  mxsa_index_layout L;
+  index_layout(p, &L);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  IndexPtrs x;
+  x.hdr = reinterpret_cast<int32_t*>(b + L.header);
+  x.seq = reinterpret_cast<SeqInfo*>(b + L.seq_info);
+  x.token_seq = reinterpret_cast<int32_t*>(b + L.token_seq);
+  x.slot_entry = reinterpret_cast<int32_t*>(b + L.slot_entry);
+  x.bitmap = reinterpret_cast<uint32_t*>(b + L.bitmap);
+  x.kmap = b + L.kmap;
+  x.counts = reinterpret_cast<int32_t*>(b + L.counts);
+  x.row_ptr = reinterpret_cast<int32_t*>(b + L.row_ptr);
+  x.entries = reinterpret_cast<int32_t*>(b + L.entries);
+  x.active = reinterpret_cast<int32_t*>(b + L.active_keys);
+  x.active_valid = reinterpret_cast<int32_t*>(b + L.active_valid);
+  x.lookback = reinterpret_cast<unsigned long long*>(b + L.lookback);
+  return x;
+}
+
+SchedPtrs sched_ptrs(const mxsa_problem& p, void* ws) {
+  mxsa_sched_layout L;
+  sched_layout(p, &L);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  SchedPtrs x;
+  x.hdr = reinterpret_cast<int32_t*>(b + L.header);
+  x.items = reinterpret_cast<int4*>(b + L.items);
+  x.cost_prefix = reinterpret_cast<long long*>(b + L.cost_prefix);
+  x.cta_ptr = reinterpret_cast<int32_t*>(b + L.cta_ptr);
+  x.lookback = reinterpret_cast<unsigned long long*>(b + L.lookback);
+  return x;
+}
+
+static mxsa_status resolve_ctas(int32_t num_ctas, int* out) {
+  int n = num_ctas;
+  if (n == 0) n = sm_count();
+  if (n < 1 || n > MXSA_MAX_CTAS) return MXSA_ERR_INVALID_ARG;
+  *out = n;
+  return MXSA_OK;
+}
+
+}  // namespace mxsa
+
+using namespace mxsa;
+
+extern "C" {
+
+int32_t mxsa_version(void) { return (1 << 16) | 0; }
+
+const char* mxsa_status_string(mxsa_status s) {
+  switch (s) {
+    case MXSA_OK: return "MXSA_OK";
+    case MXSA_ERR_INVALID_ARG: return "MXSA_ERR_INVALID_ARG";
+    case MXSA_ERR_UNSUPPORTED: return "MXSA_ERR_UNSUPPORTED";
+    case MXSA_ERR_WORKSPACE: return "MXSA_ERR_WORKSPACE";
+    case MXSA_ERR_CUDA: return "MXSA_ERR_CUDA";
+    case MXSA_ERR_DATA: return "MXSA_ERR_DATA";
+  }
+  return "unknown mxsa_status";
+}
+
+mxsa_status mxsa_workspace_size(const mxsa_problem* problem, size_t* index_bytes, size_t* sched_bytes,
+                                size_t* partial_bytes) {
+  if (!problem || !index_bytes || !sched_bytes || !partial_bytes) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout il;
+  mxsa_sched_layout sl;
+  mxsa_status s = index_layout(*problem, &il);
+  if (s != MXSA_OK) return s;
+  sched_layout(*problem, &sl);
+  size_t po, pl, pt;
+  partial_layout(*problem, &po, &pl, &pt);
+  *index_bytes = il.total;
+  *sched_bytes = sl.total;
+  *partial_bytes = pt;
+  return MXSA_OK;
+}
+
+mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layout* layout) {
+  if (!problem || !layout) return MXSA_ERR_INVALID_ARG;
+  return index_layout(*problem, layout);
+}
+
+mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layout* layout) {
+  if (!problem || !layout) return MXSA_ERR_INVALID_ARG;
+  return sched_layout(*problem, layout);
+}
+
+mxsa_status mxsa_build_index(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
+                             const int32_t* used_kv_lens, void* index_ws, size_t index_bytes, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout L;
+  mxsa_status s = index_layout(*problem, &L);
+  if (s != MXSA_OK) return s;
+  if (!cu_seqlens_q || !used_kv_lens || !index_ws || (problem->total_q > 0 && !sel)) return MXSA_ERR_INVALID_ARG;
+  if (!aligned(sel, 4) || !aligned(cu_seqlens_q, 8) || !aligned(used_kv_lens, 4) || !aligned(index_ws, 16))
+    return MXSA_ERR_INVALID_ARG;
+  if (index_bytes < L.total) return MXSA_ERR_WORKSPACE;
+  IndexPtrs ix = index_ptrs(*problem, index_ws);
+  cudaError_t e = launch_build_index(*problem, sel, cu_seqlens_q, used_kv_lens, ix, L,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
+mxsa_status mxsa_schedule(const mxsa_problem* problem, const void* index_ws, size_t index_bytes, int32_t num_ctas,
+                          void* sched_ws, size_t sched_bytes, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout il;
+  mxsa_sched_layout sl;
+  mxsa_status s = index_layout(*problem, &il);
+  if (s != MXSA_OK) return s;
+  sched_layout(*problem, &sl);
+  if (!index_ws || !sched_ws || !aligned(index_ws, 16) || !aligned(sched_ws, 16)) return MXSA_ERR_INVALID_ARG;
+  if (index_bytes < il.total || sched_bytes < sl.total) return MXSA_ERR_WORKSPACE;
+  int ctas = 0;
+  s = resolve_ctas(num_ctas, &ctas);
+  if (s != MXSA_OK) return s;
+  IndexPtrs ix = index_ptrs(*problem, const_cast<void*>(index_ws));
+  SchedPtrs sc = sched_ptrs(*problem, sched_ws);
+  cudaError_t e = launch_schedule(*problem, ix, sc, sl, ctas, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
+mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const void* index_ws, size_t index_bytes,
+                             const void* sched_ws, size_t sched_bytes, int32_t num_ctas, void* partial_ws,
+                             size_t partial_bytes, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout il;
+  mxsa_sched_layout sl;
+  mxsa_status s = index_layout(*problem, &il);
+  if (s != MXSA_OK) return s;
+  sched_layout(*problem, &sl);
+  if (!k_cache || !v_cache || !block_tables || !index_ws || !sched_ws || !partial_ws ||
+      (problem->total_q > 0 && !q))
+    return MXSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_tables, 4) ||
+      !aligned(index_ws, 16) || !aligned(sched_ws, 16) || !aligned(partial_ws, 16))
+    return MXSA_ERR_INVALID_ARG;
+  size_t po, pl, pt;
+  partial_layout(*problem, &po, &pl, &pt);
+  if (index_bytes < il.total || sched_bytes < sl.total || partial_bytes < pt) return MXSA_ERR_WORKSPACE;
+  int ctas = 0;
+  s = resolve_ctas(num_ctas, &ctas);
+  if (s != MXSA_OK) return s;
+  IndexPtrs ix = index_ptrs(*problem, const_cast<void*>(index_ws));
+  SchedPtrs sc = sched_ptrs(*problem, const_cast<void*>(sched_ws));
+  uint8_t* pb = static_cast<uint8_t*>(partial_ws);
+  int detail = 0;
+  cudaError_t e = launch_fwd(*problem, q, k_cache, v_cache, block_tables, ix, sc, ctas,
+                             reinterpret_cast<float*>(pb + po), reinterpret_cast<float*>(pb + pl),
+                             static_cast<cudaStream_t>(stream), &detail);
+  if (e != cudaSuccess) return detail ? MXSA_ERR_INVALID_ARG : MXSA_ERR_CUDA;
+  return MXSA_OK;
+}
+
+mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
+                         const void* partial_ws, size_t partial_bytes, void* out, float* lse, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout il;
+  mxsa_status s = index_layout(*problem, &il);
+  if (s != MXSA_OK) return s;
+  if (!index_ws || !partial_ws || (problem->total_q > 0 && !out)) return MXSA_ERR_INVALID_ARG;
+  if (!aligned(index_ws, 16) || !aligned(partial_ws, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return MXSA_ERR_INVALID_ARG;
+  size_t po, pl, pt;
+  partial_layout(*problem, &po, &pl, &pt);
+  if (index_bytes < il.total || partial_bytes < pt) return MXSA_ERR_WORKSPACE;
+  IndexPtrs ix = index_ptrs(*problem, const_cast<void*>(index_ws));
+  const uint8_t* pb = static_cast<const uint8_t*>(partial_ws);
+  cudaError_t e = launch_combine(*problem, ix, reinterpret_cast<const float*>(pb + po),
+                                 reinterpret_cast<const float*>(pb + pl), out, lse,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
+mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device_flags) {
+  if (!index_ws || !device_flags || !aligned(index_ws, 16)) return MXSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t flags = 0;
+  if (cudaMemcpyAsync(&flags, static_cast<const uint8_t*>(index_ws) + kHdrFlags * 4, 4, cudaMemcpyDeviceToHost,
+                      st) != cudaSuccess)
+    return MXSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MXSA_ERR_CUDA;
+  *device_flags = flags;
+  return flags ? MXSA_ERR_DATA : MXSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// Combine: LSE-weighted merge of the per-block partials of every (token,
+// head) row ("combine" kernel in the test list of the fw-ai/minimax-kernels
+// README; output [Tq, Hq, 128] and FP32 lse [Hq, Tq] from its Quick start).
+//
+//   M = max_k lse_k,  w_k = exp(lse_k - M),
+//   out = sum_k w_k o_k / sum_k w_k   (rounded to nearest-even, q dtype),
+//   lse = M + log(sum_k w_k);  no partial: out = 0, lse = -inf.
+//
+// One warp per row; lane j owns columns 4j..4j+3 (one float4 of every
+// 512-byte partial row, so each partial is read as one coalesced 512-byte
+// transaction).  The row's slot -> entry map and lses are read once per
+// 32 slots with one load per lane.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mxsa {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    k_combine(const int32_t* slot_entry, const float* part_o, const float* part_lse, uint8_t* out, float* lse_out,
+              int total_q, int Hq, int Hkv, int topk, int out_bf16) {
+  const int lane = threadIdx.x & 31;
+  const int G = Hq / Hkv;
+  const long long n_rows = (long long)total_q * Hq;
+  constexpr float kLog2e = 1.4426950408889634f;
+  for (long long row = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); row < n_rows;
+       row += (long long)gridDim.x * kWarpsPerBlock) {
+    const int t = (int)(row / Hq), h = (int)(row % Hq);
+    const int g = h / G, j = h % G;
+    const int32_t* se = slot_entry + ((long long)t * Hkv + g) * topk;
+    // pass 1: max lse over the row's partials
+    float M = -INFINITY;
+    for (int k0 = 0; k0 < topk; k0 += 32) {
+      const int k = k0 + lane;
+      float l = -INFINITY;
+      if (k < topk) {
+        const int e = se[k];
+        if (e >= 0) l = part_lse[(long long)e * G + j];
+      }
+      M = fmaxf(M, l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    if (M != -INFINITY) {
+      const float M2 = M * kLog2e;
+      for (int k0 = 0; k0 < topk; k0 += 32) {
+        const int k = k0 + lane;
+        int e = -1;
+        float w = 0.f;
+        if (k < topk) {
+          e = se[k];
+          if (e >= 0) {
+            const float l = part_lse[(long long)e * G + j];
+            w = l == -INFINITY ? 0.f : ex2_approx(fmaf(l, kLog2e, -M2));
+          }
+        }
+        unsigned live = __ballot_sync(0xffffffffu, w > 0.f);
+        while (live) {
+          const int src = __ffs(live) - 1;
+          live &= live - 1;
+          const int es = __shfl_sync(0xffffffffu, e, src);
+          const float ws = __shfl_sync(0xffffffffu, w, src);
+          const float4 v = reinterpret_cast<const float4*>(part_o + ((long long)es * G + j) * 128)[lane];
+          acc.x = fmaf(ws, v.x, acc.x);
+          acc.y = fmaf(ws, v.y, acc.y);
+          acc.z = fmaf(ws, v.z, acc.z);
+          acc.w = fmaf(ws, v.w, acc.w);
+          W += ws;
+        }
+      }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    uint2 packed;
+    if (out_bf16) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      packed = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    } else {
+      __half2 a = __floats2half2_rn(acc.x * inv, acc.y * inv);
+      __half2 b = __floats2half2_rn(acc.z * inv, acc.w * inv);
+      packed = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    }
+    reinterpret_cast<uint2*>(out + row * 256)[lane] = packed;
+    if (lse_out && lane == 0)
+      lse_out[(long long)h * total_q + t] = W > 0.f ? M + lg2_approx(W) * 0.69314718055994530942f : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
+                           const float* part_lse, void* out, float* lse, cudaStream_t st) {
+  const long long rows = (long long)p.total_q * p.num_q_heads;
+  if (rows == 0) return cudaSuccess;
+  int sms = 148, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
+  k_combine<<<(int)blocks, kWarpsPerBlock * 32, 0, st>>>(ix.slot_entry, part_o, part_lse,
+                                                         static_cast<uint8_t*>(out), lse, p.total_q,
+                                                         p.num_q_heads, p.num_kv_heads, p.topk,
+                                                         p.q_dtype == MXSA_BF16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace mxsa

@@ -1,0 +1,148 @@
+// Internal declarations shared by the library's translation units:
+// workspace layouts, per-sequence metadata and the kernel launchers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mxsa.h"
+
+namespace mxsa {
+
+// index workspace header (int32 words)
+enum : int {
+  kHdrFlags = 0,
+  kHdrNB = 1,        // blocks over all sequences
+  kHdrNnz = 2,       // entries
+  kHdrActive = 3,    // keys with at least one entry
+  kHdrKeys = 4,      // Hkv * NB
+  kHdrBMW = 5,       // bitmap words per kv head
+  kHdrKMW = 6,       // kmap bytes per kv head
+  kHdrTileCtr = 7,   // dynamic tile counter of the key scan
+  kHdrInts = 16
+};
+
+// schedule workspace header (int32 words)
+enum : int {
+  kSchItems = 0,
+  kSchCtas = 1,
+  kSchCostLo = 2,
+  kSchCostHi = 3,
+  kSchTileCtr = 4,
+  kSchInts = 16
+};
+
+// Per-sequence metadata written by the index builder.
+struct SeqInfo {
+  int32_t L;        // used_kv_len clamped to [0, max_pages * page_size]
+  int32_t nblk;     // ceil(L / 128)
+  int32_t blk_off;  // exclusive prefix of nblk
+  int32_t tq;       // new query tokens
+  int32_t q_begin;  // cu_seqlens_q[s]
+  int32_t bm_off;   // bitmap word offset of the sequence within one kv head
+  int32_t km_off;   // kmap byte offset of the sequence within one kv head
+  int32_t words;    // ceil(tq / 32): bitmap words per key row
+};
+
+struct IndexPtrs {
+  int32_t* hdr;
+  SeqInfo* seq;
+  int32_t* token_seq;
+  int32_t* slot_entry;
+  uint32_t* bitmap;
+  uint8_t* kmap;
+  int32_t* counts;
+  int32_t* row_ptr;
+  int32_t* entries;
+  int32_t* active;
+  int32_t* active_valid;
+  unsigned long long* lookback;
+};
+
+struct SchedPtrs {
+  int32_t* hdr;
+  int4* items;
+  long long* cost_prefix;
+  int32_t* cta_ptr;
+  unsigned long long* lookback;
+};
+
+constexpr int kScanThreads = 256;
+constexpr int kScanPerThread = 4;
+constexpr int kScanTile = kScanThreads * kScanPerThread;  // keys per look-back tile
+
+// wall-clock limit of every on-device wait (ns)
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+int64_t max_blocks_per_seq(const mxsa_problem& p);
+mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L);
+mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L);
+IndexPtrs index_ptrs(const mxsa_problem& p, void* ws);
+SchedPtrs sched_ptrs(const mxsa_problem& p, void* ws);
+mxsa_status validate_problem(const mxsa_problem& p);
+
+// launchers (return cudaGetLastError())
+cudaError_t launch_build_index(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
+                               const IndexPtrs& ix, const mxsa_index_layout& lay, cudaStream_t st);
+cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc,
+                            const mxsa_sched_layout& lay, int num_ctas, cudaStream_t st);
+cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
+                       float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
+cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
+                           const float* part_lse, void* out, float* lse, cudaStream_t st);
+
+// ------------------------------------------------------------------------
+// device helpers shared by the scan kernels
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long dev_globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Decoupled look-back (single-pass chained scan) over 62-bit payloads:
+// bits 63..62 = status (0 none, 1 tile aggregate, 2 inclusive prefix).
+// Called by one thread per tile; returns the exclusive prefix of `tile`.
+// Payload addition must not carry across the packed fields (callers keep
+// every field below its capacity).  A wait beyond the limit sets
+// MXSA_FLAG_TIMEOUT and returns what was accumulated so far.
+__device__ __forceinline__ unsigned long long lookback_exclusive(unsigned long long* state, int tile,
+                                                                 unsigned long long aggregate, int* flags) {
+  constexpr unsigned long long kAgg = 1ull << 62, kInc = 2ull << 62, kMask = (1ull << 62) - 1;
+  if (tile == 0) {
+    st_release_u64(&state[0], kInc | aggregate);
+    return 0;
+  }
+  st_release_u64(&state[tile], kAgg | aggregate);
+  unsigned long long excl = 0;
+  int j = tile - 1;
+  const unsigned long long t0 = dev_globaltimer();
+  while (j >= 0) {
+    unsigned long long v = ld_acquire_u64(&state[j]);
+    unsigned long long st = v >> 62;
+    if (st == 0) {
+      if (dev_globaltimer() - t0 > kWaitLimitNs) {
+        atomicOr(flags, MXSA_FLAG_TIMEOUT);
+        break;
+      }
+      continue;
+    }
+    excl += v & kMask;
+    if (st == 2) break;
+    --j;
+  }
+  st_release_u64(&state[tile], kInc | (excl + aggregate));
+  return excl;
+}
+#endif
+
+}  // namespace mxsa

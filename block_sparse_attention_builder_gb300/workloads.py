@@ -104,6 +104,12 @@ def generate_values(numel: int, key: int, dtype: str, device, start: int = 0, ch
     return out.view(TORCH_DTYPE[dtype])
 
 
+def generate_at(idx: torch.Tensor, key: int, dtype: str) -> torch.Tensor:
+    """Elements at the int64 flat indices `idx` of the stream `key` (raw storage bits)."""
+    table = _quantile_table(dtype).to(idx.device)
+    return table[(_hash_index(idx, key) >> 16) & 0xFFFF]
+
+
 # --------------------------------------------------------------------------
 # workload specification
 # --------------------------------------------------------------------------
@@ -234,10 +240,17 @@ class Workload:
         """Pages `pages` of the K (2) or V (3) cache, generated on the CPU."""
         per_page = self.num_kv_heads * self.page_size * HEAD_DIM
         key = stream_key(self.spec.seed, tensor_id)
-        out = [generate_values(per_page, key, self.spec.kv_dtype, "cpu", start=int(p) * per_page) for p in pages]
-        if not out:
-            return torch.empty(0, self.num_kv_heads, self.page_size, HEAD_DIM, dtype=TORCH_DTYPE[self.spec.kv_dtype])
-        return torch.stack(out).view(len(pages), self.num_kv_heads, self.page_size, HEAD_DIM)
+        pages = torch.as_tensor(np.asarray(pages, dtype=np.int64))
+        raw = _quantile_table(self.spec.kv_dtype)
+        out = torch.empty(len(pages) * per_page, dtype=raw.dtype)
+        step = max(1, (1 << 24) // per_page)
+        ar = torch.arange(per_page, dtype=torch.int64)
+        for i in range(0, len(pages), step):
+            grp = pages[i:i + step]
+            idx = (grp[:, None] * per_page + ar[None, :]).reshape(-1)
+            out[i * per_page:(i + len(grp)) * per_page] = generate_at(idx, key, self.spec.kv_dtype)
+        return out.view(TORCH_DTYPE[self.spec.kv_dtype]).view(len(pages), self.num_kv_heads, self.page_size,
+                                                                 HEAD_DIM)
 
     def compact_cache_for_rows(self, rows: np.ndarray):
         """A small cache holding only the pages that rows (flat t*Hq+h) can reach.

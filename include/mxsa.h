@@ -1,0 +1,193 @@
+/*
+ * mxsa -- block-sparse KV-outer attention over a paged KV cache, for one
+ * GB300 (sm_103a).  C ABI: plain pointers and sizes, no C++ or torch types.
+ *
+ * The operation (fw-ai/minimax-kernels README, intro and "Quick start"):
+ * every query token t of sequence s attends, per KV head g, only to the
+ * 128-token logical KV blocks listed in selected[t, g, :] (-1 = none).  In
+ * the KV-outer (KV-stationary) formulation each selected block is loaded
+ * from HBM once and used for every (query, GQA query head) row that selected
+ * it, producing per-row partial outputs and log-sum-exps that a combine step
+ * merges.  The call sequence is
+ *
+ *     mxsa_build_index -> mxsa_schedule -> mxsa_kvouter_fwd -> mxsa_combine
+ *
+ * all asynchronous on the caller's CUDA stream, followed optionally by
+ * mxsa_read_status.  For token t of sequence s (offset i = t - cu[s]) the
+ * result is, with L = used_kv_lens[s], Tq_s = cu[s+1] - cu[s], pos(t) =
+ * L - Tq_s + i, G = Hq / Hkv and g = h / G:
+ *
+ *     K(t,g)   = { p : p in a selected block b (128 b <= p < 128 b + 128),
+ *                  p < L, and p <= pos(t) when causal }
+ *     s_p      = softmax_scale * q[t,h,:] . k_p
+ *     out[t,h] = sum_p softmax(s)_p * v_p            (0 when K(t,g) is empty)
+ *     lse[h,t] = log sum_p exp(s_p)   (natural log; -inf when K is empty)
+ *
+ * Key p lives at k_cache[block_tables[s][p / page_size], g, p % page_size, :].
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer; the library allocates nothing (no
+ *     cudaMalloc, no host allocation) and keeps no state between calls.
+ *   - "device" pointers must point to GPU memory of the current device;
+ *     all must be 16-byte aligned and densely packed in the stated layout.
+ *   - Host-side argument errors return synchronously with a status code; the
+ *     library never falls back to another implementation silently.
+ *   - Data errors found on the device (a selection outside [-1, nblk), a
+ *     repeated block in one row, a bad page id, ...) set bits in a status
+ *     word inside the index workspace and skip the offending slot or page;
+ *     they never trap.  mxsa_read_status returns that word.
+ *   - Calls on one workspace set must be ordered on one stream.
+ */
+#ifndef MXSA_H_
+#define MXSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXSA_OK = 0,
+  MXSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, inconsistent shape */
+  MXSA_ERR_UNSUPPORTED = 2, /* head_dim != 128, page_size not 64/128, G > 128, ... */
+  MXSA_ERR_WORKSPACE = 3,   /* a workspace is smaller than mxsa_workspace_size says */
+  MXSA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  MXSA_ERR_DATA = 5         /* mxsa_read_status: the device flagged bad input data */
+} mxsa_status;
+
+typedef enum { MXSA_BF16 = 0, MXSA_FP16 = 1, MXSA_FP8_E4M3 = 2 } mxsa_dtype;
+
+/* Bits of the device status word (mxsa_read_status). */
+#define MXSA_FLAG_SEL_RANGE 1   /* selected block outside [-1, ceil(L/128)) : slot ignored */
+#define MXSA_FLAG_SEL_DUP 2     /* block repeated in one (token, kv head) row: later slot ignored */
+#define MXSA_FLAG_PAGE 4        /* a needed block_tables entry outside [0, num_pages): page skipped */
+#define MXSA_FLAG_CAUSAL_LEN 8  /* causal with used_kv_len < new tokens of the sequence */
+#define MXSA_FLAG_LEN 16        /* used_kv_len < 0 or > max_pages_per_seq * page_size: clamped */
+#define MXSA_FLAG_TIMEOUT 32    /* an on-device wait gave up (result undefined) */
+#define MXSA_FLAG_SCHEDULE 64   /* schedule and forward disagree on the CTA count */
+#define MXSA_FLAG_CU 128        /* cu_seqlens_q is not a non-decreasing partition of total_q */
+
+/* Problem description (sizes and flags of one call).  The sources: the
+ * Quick-start signature and the supported-feature list of the
+ * fw-ai/minimax-kernels README. */
+typedef struct {
+  int32_t num_seqs;          /* B >= 1 */
+  int32_t total_q;           /* Tq = cu_seqlens_q[B] >= 0 */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 and G = Hq / Hkv <= 128 */
+  int32_t head_dim;          /* must be 128 */
+  int32_t topk;              /* selection slots per (token, kv head), 1..256 */
+  int32_t page_size;         /* 64 or 128 tokens */
+  int32_t num_pages;         /* physical pages in k_cache / v_cache */
+  int32_t max_pages_per_seq; /* row stride of block_tables */
+  int32_t causal;            /* 0 or 1 (bottom-right aligned: pos(t) = L - Tq_s + i) */
+  float softmax_scale;       /* 0 means 1/sqrt(128) */
+  int32_t q_dtype;           /* MXSA_BF16 or MXSA_FP16; the output has this dtype */
+  int32_t kv_dtype;          /* q_dtype, or MXSA_FP8_E4M3 (unscaled e4m3fn) */
+} mxsa_problem;
+
+/* Library version, (major << 16) | minor. */
+int32_t mxsa_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* mxsa_status_string(mxsa_status status);
+
+/* Workspace sizes (bytes) for a problem: upper bounds computed from the
+ * shapes alone, so one allocation serves any selections / lengths of that
+ * shape.  index: inverted block index + device status word; sched: work
+ * items and the per-CTA partition; partial: FP32 partial outputs and lses
+ * (one 128-float row + one lse per (selected block, query head) pair).
+ * Returns MXSA_ERR_INVALID_ARG / MXSA_ERR_UNSUPPORTED for bad problems. */
+mxsa_status mxsa_workspace_size(const mxsa_problem* problem, size_t* index_bytes, size_t* sched_bytes,
+                                size_t* partial_bytes);
+
+/* Step 1 -- index builder ("index builder" in the README's test list; the
+ * algorithm is this library's): inverts the query -> block selections into
+ * block -> (token, head group) lists.  Keys are (kv head g, sequence s,
+ * block b) in that order; within a key the entries are the selection slots
+ * (t * Hkv + g) * topk + k in increasing t (bit-exact, deterministic).
+ *   sel           device int32 [total_q, Hkv, topk], -1 = none
+ *   cu_seqlens_q  device int64 [B + 1]
+ *   used_kv_lens  device int32 [B]
+ *   index_ws      device, index_bytes from mxsa_workspace_size (written)
+ * Asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream). */
+mxsa_status mxsa_build_index(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
+                             const int32_t* used_kv_lens, void* index_ws, size_t index_bytes, void* stream);
+
+/* Step 2 -- load-balancing scheduler ("load-balancing scheduler" in the
+ * README's test list; the split rule and cost model are this library's):
+ * splits each key's entries into work items of at most 4 tiles of 128
+ * (token, head) rows and partitions the items into `num_ctas` contiguous
+ * ranges of near-equal integer cost.
+ *   index_ws   device, written by mxsa_build_index on the same stream
+ *   num_ctas   persistent CTAs of the forward; 0 = one per SM of the
+ *              current device; at most 4096
+ *   sched_ws   device, sched_bytes from mxsa_workspace_size (written) */
+mxsa_status mxsa_schedule(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
+                          int32_t num_ctas, void* sched_ws, size_t sched_bytes, void* stream);
+
+/* Step 3 -- KV-outer forward (the README's intro): every work item TMA-loads
+ * its KV block (through block_tables) into shared memory once, gathers the
+ * q rows of every (token, head) that selected it, and runs q k^T and p v on
+ * the tcgen05 tensor cores with FP32 accumulators in tensor memory and the
+ * softmax in registers.  Writes one FP32 partial row o = sum softmax * v
+ * over the block's keys and its lse per (entry, head) into partial_ws.
+ *   q             device [total_q, Hq, 128] of q_dtype
+ *   k_cache/v_cache device [num_pages, Hkv, page_size, 128] of kv_dtype
+ *   block_tables  device int32 [B, max_pages_per_seq]
+ *   num_ctas      must equal the value given to mxsa_schedule (0 = #SMs)
+ *   partial_ws    device, partial_bytes from mxsa_workspace_size (written) */
+mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_tables, const void* index_ws,
+                             size_t index_bytes, const void* sched_ws, size_t sched_bytes, int32_t num_ctas,
+                             void* partial_ws, size_t partial_bytes, void* stream);
+
+/* Step 4 -- combine: for each (t, h) merges the partials of the row's
+ * selected blocks with LSE weights: M = max lse_k, w_k = exp(lse_k - M),
+ * out = sum w_k o_k / sum w_k (rounded to nearest-even into q_dtype),
+ * lse = M + log sum w_k.  A row with no partial gets out 0 and lse -inf.
+ *   out   device [total_q, Hq, 128] of q_dtype (written)
+ *   lse   device float [Hq, total_q] (written), or NULL to skip it */
+mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
+                         const void* partial_ws, size_t partial_bytes, void* out, float* lse, void* stream);
+
+/* Synchronises `stream`, then copies the device status word (MXSA_FLAG_*
+ * bits) of index_ws into *device_flags.  Returns MXSA_ERR_DATA when any bit
+ * is set, MXSA_OK otherwise. */
+mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device_flags);
+
+/* Byte offsets of the arrays inside the index workspace, for inspection
+ * (tests compare them bit-exactly with an independent CPU statement).
+ * header: int32[16] = {flags, NB (blocks over all sequences), nnz (entries),
+ *   n_active (keys with entries), n_keys (Hkv * NB), ...};
+ * row_ptr: int32 [n_keys + 1]; entries: int32 [nnz] slot ids;
+ * slot_entry: int32 [total_q * Hkv * topk], position in entries or -1;
+ * active_keys: int32 [n_active], keys with entries in increasing order. */
+typedef struct {
+  size_t header, seq_info, token_seq, slot_entry, bitmap, kmap, counts, row_ptr, entries, active_keys,
+      active_valid, lookback, total;
+  int64_t keys_cap, nslots, bitmap_words_cap, kmap_bytes_cap, tiles_cap;
+} mxsa_index_layout;
+mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layout* layout);
+
+/* Byte offsets inside the schedule workspace.  header: int32[16] =
+ * {n_items, num_ctas, total cost low 32 bits, total cost high 32 bits, ...};
+ * items: int32[4] per item = {key, entry_begin, n_entries, 0};
+ * cost_prefix: int64 [n_items + 1]; cta_ptr: int32 [num_ctas + 1]. */
+typedef struct {
+  size_t header, items, cost_prefix, cta_ptr, lookback, total;
+  int64_t items_cap, tiles_cap;
+} mxsa_sched_layout;
+mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layout* layout);
+
+/* Entries per work item tile and tiles per work item used by the scheduler. */
+#define MXSA_TILE_ROWS 128
+#define MXSA_ITEM_TILES 4
+#define MXSA_MAX_CTAS 4096
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXSA_H_ */

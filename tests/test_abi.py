@@ -1,0 +1,110 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU and
+exports every symbol include/mxsa.h declares; host-side validation and
+workspace sizing behave as documented (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import block_sparse_attention_builder_gb300 as mx
+from block_sparse_attention_builder_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return mx.library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "mxsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxsa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert "mxsa_kvouter_fwd" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(mx.EXPORTED) | set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mxsa_version() >> 16 == 1
+    for code, name in mx.STATUS_NAMES.items():
+        assert lib.mxsa_status_string(code).decode() == name
+
+
+def _prob(**kw):
+    base = dict(num_seqs=2, total_q=4, num_q_heads=16, num_kv_heads=2, topk=8, page_size=64, num_pages=100,
+                max_pages_per_seq=40, causal=False)
+    base.update(kw)
+    return mx.make_problem(**base)
+
+
+def test_workspace_sizes_are_shape_upper_bounds(lib):
+    p = _prob()
+    ib, sb, pb = mx.workspace_size(p)
+    L = mx.index_layout(p)
+    assert ib == L.total and L.nslots == 4 * 2 * 8
+    assert L.keys_cap == 2 * 2 * 20  # Hkv * B * ceil(40 * 64 / 128)
+    assert pb >= L.nslots * 8 * 516
+    S = mx.sched_layout(p)
+    assert sb == S.total and S.items_cap == L.nslots
+    offs = [L.header, L.seq_info, L.token_seq, L.slot_entry, L.bitmap, L.kmap, L.counts, L.row_ptr, L.entries,
+            L.active_keys, L.active_valid, L.lookback, L.total]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), 2), (dict(page_size=32), 2), (dict(num_q_heads=12, num_kv_heads=5), 1),
+    (dict(num_q_heads=256, num_kv_heads=1), 2), (dict(topk=300), 2), (dict(topk=0), 1), (dict(num_seqs=0), 1),
+    (dict(num_pages=0), 1), (dict(causal=2), 1), (dict(softmax_scale=-1.0), 1),
+])
+def test_invalid_problems_are_rejected(lib, kw, status):
+    p = _prob()
+    for k, v in kw.items():
+        setattr(p, k, v)
+    with pytest.raises(mx.MxsaError) as ei:
+        mx.workspace_size(p)
+    assert ei.value.status == status
+
+
+def test_unsupported_dtype_pairs(lib):
+    p = _prob(q_dtype=torch.bfloat16, kv_dtype=torch.float16)
+    with pytest.raises(mx.MxsaError) as ei:
+        mx.workspace_size(p)
+    assert ei.value.status == 2
+    p = _prob(q_dtype=torch.float16, kv_dtype=torch.float8_e4m3fn)
+    assert mx.workspace_size(p)[0] > 0
+
+
+def test_null_and_small_workspace_rejected_before_any_launch(lib):
+    p = _prob()
+    ib, sb, pb = mx.workspace_size(p)
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: validation fails first
+    assert lib.mxsa_build_index(ctypes.byref(p), fake, None, fake, fake, ib, None) == 1
+    assert lib.mxsa_build_index(ctypes.byref(p), fake, fake, fake, fake, ib - 1, None) == 3
+    assert lib.mxsa_build_index(ctypes.byref(p), P((1 << 20) + 2), fake, fake, fake, ib, None) == 1
+    assert lib.mxsa_schedule(ctypes.byref(p), fake, ib, 0, fake, sb - 256, None) == 3
+    assert lib.mxsa_schedule(ctypes.byref(p), fake, ib, 5000, fake, sb, None) == 1
+    assert lib.mxsa_kvouter_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, ib, fake, sb, 1, fake, pb - 1,
+                                None) == 3
+    assert lib.mxsa_combine(ctypes.byref(p), fake, ib, fake, pb, P((1 << 20) + 8), None, None) == 1
+    assert lib.mxsa_read_status(None, None, None) == 1
+    assert lib.mxsa_workspace_size(None, None, None, None) == 1
+
+
+def test_package_has_no_cpu_fallback():
+    import block_sparse_attention_builder_gb300 as pkg
+    src = open(pkg.__file__).read()
+    assert "import oracle" not in src and "from oracle" not in src
+    for f in os.listdir(os.path.join(ROOT, "block_sparse_attention_builder_gb300", "csrc")):
+        text = open(os.path.join(ROOT, "block_sparse_attention_builder_gb300", "csrc", f)).read()
+        assert "oracle" not in text.lower() or f.endswith(".md")
