@@ -1,0 +1,432 @@
+"""Benchmark of block-sparse KV-outer attention on GB300.
+
+One step = the whole hot path (index builder, scheduler, KV-outer forward,
+combine) over one batch of the synthetic workload, inputs resident in HBM.
+Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
+on the launching stream with an L2 flush (a 256 MiB write) between steps
+outside the events; device time summed over the K steps; max over ranks.
+Per-kernel durations come from events recorded between the four calls on the
+same stream.  Multi-GPU (torchrun): every rank runs its own batch of the
+same workload recipe (independent sequences, no collective on the data
+path); value = tokens of all ranks / max-over-ranks time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn tokens/s, TFLOP/s and unique-KV GB/s vs roofline, 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 10  # k_seq k_zero k_mark k_scan k_emit | k_sched_init k_sched_scan k_partition | k_fwd | k_combine
+DEFAULT_WORKLOAD = "gqa_decode"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, src="fallback")
+
+
+def fwd_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("fwd.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "block_sparse_attention_builder_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per forward launch from a committed ncu summary, if it was
+    taken on the current forward-kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "k_fwd_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("fwd_source_hash") != fwd_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workload
+def load_workload(name: str, rank: int):
+    from block_sparse_attention_builder_gb300 import workloads as W
+    spec = W.WORKLOADS[name]
+    if rank:
+        import dataclasses
+        spec = dataclasses.replace(spec, seed=spec.seed + 7919 * rank)
+    return W.make_workload(spec)
+
+
+def workload_config(w, stats, name):
+    return {"workload": name, "description": w.spec.description, "num_seqs": w.num_seqs, "total_q": w.total_q,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": 128,
+            "page_size": w.page_size, "topk": w.topk, "causal": bool(w.causal), "q_dtype": w.spec.q_dtype,
+            "kv_dtype": w.spec.kv_dtype, "unique_kv_blocks": stats["unique_blocks"],
+            "block_visits": stats["block_visits"], "l2": "flushed between timed steps (256 MiB write); "
+            "the step's unique KV also exceeds L2", "kv_cache": "resident in HBM (model state)"}
+
+
+def algorithmic(w, stats):
+    kv_elem = 1 if w.spec.kv_dtype == "fp8" else 2
+    unique_kv_bytes = stats["unique_tokens"] * 128 * 2 * kv_elem
+    flops = 4 * 128 * stats["visit_keys"] * (w.num_q_heads // w.num_kv_heads)
+    io_bytes = (w.total_q * w.num_q_heads * 128 * 2 * 2 + w.total_q * w.num_q_heads * 4 + w.selected.nbytes
+                + w.block_tables.nbytes + w.cu_seqlens_q.nbytes + w.used_kv_lens.nbytes)
+    partial_bytes = stats["block_visits"] * (w.num_q_heads // w.num_kv_heads) * (128 + 1) * 4 * 2
+    return unique_kv_bytes, flops, io_bytes, partial_bytes
+
+
+# ------------------------------------------------------------ CPU oracle
+def _gen_device():
+    return "cuda" if torch.cuda.is_available() else "cpu"
+
+
+def oracle_sample(w, target_rows: int, seed: int = 0):
+    """A bounded sample of the workload for the oracle: every head of
+    randomly chosen (token, kv head) pairs (all pairs when target_rows covers
+    the workload), with a compact cache of the pages they reach.  The pages
+    come from the seeded generator (run on the GPU when there is one, for
+    speed; the bits are device-independent), never from the CUDA path."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    G = w.num_q_heads // w.num_kv_heads
+    n_all = w.total_q * w.num_kv_heads
+    n_pairs = max(1, min(n_all, target_rows // G))
+    pairs = np.arange(n_all) if n_pairs == n_all else np.sort(rng.choice(n_all, size=n_pairs, replace=False))
+    rows = (((pairs // w.num_kv_heads) * w.num_q_heads + (pairs % w.num_kv_heads) * G)[:, None]
+            + np.arange(G)).reshape(-1)
+    kc, vc, bt = w.compact_cache_for_rows(rows, _gen_device())
+    prob = oracle.problem_for(w)
+    prob.num_pages = max(1, kc.shape[0])
+    return prob, w.q(), kc, vc, bt, rows
+
+
+def time_oracle(w, sample, nthreads):
+    import oracle
+    prob, q, kc, vc, bt, rows = sample
+    t0 = time.perf_counter()
+    oracle.attention_rows(prob, q, kc, vc, w.selected, bt, w.cu_seqlens_q, w.used_kv_lens, rows=rows,
+                          nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def _sample_rows(w, nthreads, seconds):
+    """Rows the oracle finishes in about `seconds` (capped at the workload)."""
+    calib = oracle_sample(w, 64)
+    per_row = time_oracle(w, calib, nthreads) / len(calib[-1])
+    return int(max(64, min(seconds / max(per_row, 1e-9), 16384)))
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The oracle as it stands, timed on the host cores: repeated passes over
+    a bounded sample until about `budget_s` seconds of CPU work."""
+    import oracle  # noqa: F401  (built by __graft_entry__.build)
+    nthreads = os.cpu_count() or 1
+    sample = oracle_sample(w, _sample_rows(w, nthreads, budget_s), seed=1)
+    rows = len(sample[-1])
+    total, passes = 0.0, 0
+    while total < budget_s and passes < 50:
+        total += time_oracle(w, sample, nthreads)
+        passes += 1
+    tok_s = rows * passes / w.num_q_heads / total
+    G = w.num_q_heads // w.num_kv_heads
+    whole = rows == w.total_q * w.num_q_heads
+    what = "the whole workload" if whole else f"every head of {rows // G} random (token, kv-head) pairs"
+    return {"value": tok_s, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{rows} (token, head) rows of {w.spec.name} ({what}), {passes} passes, {total:.1f} s "
+                      f"on {nthreads} threads; tokens/s = rows / Hq / time"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = load_workload(args.workload, 0)
+    nthreads = os.cpu_count() or 1
+    per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    sample = oracle_sample(w, _sample_rows(w, nthreads, per_step_budget), seed=1)
+    rows = len(sample[-1])
+    for _ in range(args.warmup):
+        time_oracle(w, sample, nthreads)
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(w, sample, nthreads)
+    tokens = rows / w.num_q_heads
+    value = tokens * args.steps / total
+    stats = _stats(w)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, stats, args.workload),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                             "sample": f"{rows} (token, head) rows of {w.spec.name} per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _stats(w):
+    from block_sparse_attention_builder_gb300 import workloads as W
+    return W.selected_blocks_tokens(w)
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "mine" else "gloo")
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import block_sparse_attention_builder_gb300 as mx
+    from block_sparse_attention_builder_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    w = load_workload(args.workload, rank)
+    stats = _stats(w)
+    unique_kv_bytes, flops, io_bytes, partial_bytes = algorithmic(w, stats)
+    log(f"[bench] {args.workload}: {stats}")
+
+    # inputs resident in HBM
+    q, k, v = w.q(dev), w.k_cache(dev), w.v_cache(dev)
+    sel = torch.from_numpy(w.selected).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
+    lens = torch.from_numpy(w.used_kv_lens).to(dev)
+    prob = mx.make_problem(w.num_seqs, w.total_q, w.num_q_heads, w.num_kv_heads, w.topk, w.page_size,
+                           w.num_pages, w.max_pages_per_seq, w.causal, 0.0, q.dtype, k.dtype)
+    attn = mx.SparseAttention(prob, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.num_q_heads, w.total_q, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        mx.build_index(prob, sel, cu, lens, attn.ws.index, stream)
+        if ev:
+            ev[1].record(stream)
+        mx.schedule(prob, attn.ws.index, attn.ws.sched, 0, stream)
+        if ev:
+            ev[2].record(stream)
+        mx.kvouter_fwd(prob, q, k, v, bt, attn.ws.index, attn.ws.sched, attn.ws.partial, 0, stream)
+        if ev:
+            ev[3].record(stream)
+        mx.combine(prob, attn.ws.index, attn.ws.partial, out, lse, stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = mx.read_status(attn.ws.index, stream)
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    step_ms = per.sum(axis=1)
+    total_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = w.total_q
+    value = tokens_per_step * world * args.steps / (total_ms / 1e3)
+    fwd_ms = float(per[:, 2].mean())
+    peaks = measured_peaks()
+
+    # ---------------------------------------------------------- e2e (public API, host buffers)
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_sel, h_bt, h_cu, h_lens = pin(q), pin(sel), pin(bt), pin(cu), pin(lens)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_sel, d_bt, d_cu, d_lens = (torch.empty_like(x) for x in (q, sel, bt, cu, lens))
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_sel, h_bt, h_cu, h_lens))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        for d_, h_ in ((d_q, h_q), (d_sel, h_sel), (d_bt, h_bt), (d_cu, h_cu), (d_lens, h_lens)):
+            d_.copy_(h_, non_blocking=True)
+        o, l = attn(d_q, k, v, d_sel, d_bt, d_cu, d_lens, out=out, lse=lse, stream=stream)
+        h_out.copy_(o, non_blocking=True)
+        h_lse.copy_(l, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens_per_step * world * args.steps / (e2e_ms / 1e3)
+    assert torch.equal(h_out.to(dev), out)
+
+    if rank == 0:
+        kv_gbs = unique_kv_bytes / (ms_per_step / 1e3) / 1e9
+        tflops = flops / (ms_per_step / 1e3) / 1e12
+        fwd_gbs = unique_kv_bytes / (fwd_ms / 1e3) / 1e9
+        fwd_tflops = flops / (fwd_ms / 1e3) / 1e12
+        bound = "hbm" if w.spec.name in ("gqa_decode", "skewed_decode", "tiny_decode") else "tensor"
+        if bound == "hbm":
+            roof = {"bound": "hbm", "achieved": fwd_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": fwd_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),
+                    "kernel": "k_fwd", "algorithmic_bytes_per_launch": unique_kv_bytes,
+                    "peak_source": peaks["src"]}
+        else:
+            pk = peaks["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": pk, "unit": "TFLOP/s",
+                    "frac": fwd_tflops / pk, "traffic": recorded_traffic(args.workload), "kernel": "k_fwd",
+                    "algorithmic_flops_per_launch": flops, "peak_source": peaks["src"] + " bf16 burst"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.spec.kv_dtype if w.spec.kv_dtype != "fp8" else "fp8-e4m3 kv, bf16 q",
+            "data": "synthetic (seeded counter-based N(0,1) values; selections per the workload recipe)",
+            "config": workload_config(w, stats, args.workload),
+            "tflops": tflops, "unique_kv_gbs": kv_gbs,
+            "kernel_ms": {"index": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
+                          "fwd": fwd_ms, "combine": float(per[:, 3].mean())},
+            "fwd_unique_kv_gbs": fwd_gbs, "fwd_tflops": fwd_tflops,
+            "bytes": {"unique_kv": unique_kv_bytes, "io": io_bytes, "partials_overhead": partial_bytes},
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / args.steps,
+                    "note": "q, selections, block tables, cu_seqlens_q, used_kv_lens copied H2D from pinned "
+                            "memory and out + lse copied D2H every step; the KV cache is resident model state"},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

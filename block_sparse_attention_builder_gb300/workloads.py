@@ -236,23 +236,24 @@ class Workload:
     def v_cache(self, device="cpu") -> torch.Tensor:
         return self._cache(3, device)
 
-    def cache_pages(self, tensor_id: int, pages: np.ndarray) -> torch.Tensor:
-        """Pages `pages` of the K (2) or V (3) cache, generated on the CPU."""
+    def cache_pages(self, tensor_id: int, pages: np.ndarray, device="cpu") -> torch.Tensor:
+        """Pages `pages` of the K (2) or V (3) cache as a CPU tensor.  The
+        values are generated on `device` (identical bits on any device)."""
         per_page = self.num_kv_heads * self.page_size * HEAD_DIM
         key = stream_key(self.spec.seed, tensor_id)
-        pages = torch.as_tensor(np.asarray(pages, dtype=np.int64))
+        pages = torch.as_tensor(np.asarray(pages, dtype=np.int64)).to(device)
         raw = _quantile_table(self.spec.kv_dtype)
         out = torch.empty(len(pages) * per_page, dtype=raw.dtype)
         step = max(1, (1 << 24) // per_page)
-        ar = torch.arange(per_page, dtype=torch.int64)
+        ar = torch.arange(per_page, dtype=torch.int64, device=device)
         for i in range(0, len(pages), step):
             grp = pages[i:i + step]
             idx = (grp[:, None] * per_page + ar[None, :]).reshape(-1)
-            out[i * per_page:(i + len(grp)) * per_page] = generate_at(idx, key, self.spec.kv_dtype)
+            out[i * per_page:(i + len(grp)) * per_page] = generate_at(idx, key, self.spec.kv_dtype).cpu()
         return out.view(TORCH_DTYPE[self.spec.kv_dtype]).view(len(pages), self.num_kv_heads, self.page_size,
                                                                  HEAD_DIM)
 
-    def compact_cache_for_rows(self, rows: np.ndarray):
+    def compact_cache_for_rows(self, rows: np.ndarray, device="cpu"):
         """A small cache holding only the pages that rows (flat t*Hq+h) can reach.
 
         Returns (k_cache, v_cache, block_tables) on the CPU: the physical page
@@ -280,7 +281,7 @@ class Workload:
         bt = np.full_like(self.block_tables, -1)
         for (s, lp), p in need.items():
             bt[s, lp] = remap[p]
-        return self.cache_pages(2, phys), self.cache_pages(3, phys), bt
+        return self.cache_pages(2, phys, device), self.cache_pages(3, phys, device), bt
 
 
 def _draw_selection(spec: WorkloadSpec, rng: np.random.Generator, lens: np.ndarray, tq: List[int]) -> np.ndarray:
@@ -376,16 +377,26 @@ def selected_blocks_tokens(w: Workload) -> Dict[str, float]:
     uniq = set()
     visits = 0
     tokens_unique = 0
+    visit_keys = 0  # sum over (token, kv head, selected block) of the keys the token may use
     for s in range(w.num_seqs):
         L = int(w.used_kv_lens[s])
         nblk = (L + BLOCK - 1) // BLOCK
-        for t in range(int(w.cu_seqlens_q[s]), int(w.cu_seqlens_q[s + 1])):
+        t0, t1 = int(w.cu_seqlens_q[s]), int(w.cu_seqlens_q[s + 1])
+        for t in range(t0, t1):
+            pos = L - (t1 - t0) + (t - t0)
             for g in range(Hkv):
                 for b in w.selected[t, g]:
                     if 0 <= b < nblk:
+                        n_keys = min(BLOCK, L - BLOCK * int(b))
+                        if w.causal:
+                            n_keys = min(n_keys, pos - BLOCK * int(b) + 1)
+                        if n_keys <= 0:
+                            continue
                         visits += 1
+                        visit_keys += n_keys
                         key = (s, g, int(b))
                         if key not in uniq:
                             uniq.add(key)
                             tokens_unique += min(BLOCK, L - BLOCK * int(b))
-    return {"unique_blocks": len(uniq), "unique_tokens": tokens_unique, "block_visits": visits}
+    return {"unique_blocks": len(uniq), "unique_tokens": tokens_unique, "block_visits": visits,
+            "visit_keys": visit_keys}
