@@ -391,7 +391,7 @@ def main():
         tflops = flops / (ms_per_step / 1e3) / 1e12
         fwd_gbs = unique_kv_bytes / (fwd_ms / 1e3) / 1e9
         fwd_tflops = flops / (fwd_ms / 1e3) / 1e12
-        bound = "hbm" if w.spec.name in ("gqa_decode", "skewed_decode", "tiny_decode") else "tensor"
+        bound = "hbm" if "decode" in w.spec.name else "tensor"
         if bound == "hbm":
             roof = {"bound": "hbm", "achieved": fwd_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": fwd_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),

@@ -170,6 +170,13 @@ WORKLOADS: Dict[str, WorkloadSpec] = {
         description="256 seqs, Tq=1, Hq64/Hkv8, L log-U[1K,256K], ps64, top-64, 8 hot groups"),
 }
 
+# Smaller copies of the recipes for profiler captures (a few GB on the device
+# at most, unique KV still larger than L2).
+WORKLOADS["gqa_decode_p16"] = WorkloadSpec(
+    name="gqa_decode_p16", tq=[1] * 16, kv_lens=_uniform_int(4096, 32768), num_q_heads=64, num_kv_heads=8,
+    page_size=64, topk=16, causal=False, selection="uniform_last", seed=1012,
+    description="profiling copy of gqa_decode with 16 sequences")
+
 # The order of the five workloads as the problem statement lists them.
 WORKLOAD_ORDER = ["tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode"]
 
