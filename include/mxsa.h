@@ -182,6 +182,28 @@ typedef struct {
 } mxsa_sched_layout;
 mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layout* layout);
 
+/* The whole call (index, schedule, forward, combine) without any
+ * caller-provided workspace.  The pages describe no such entry point; it
+ * exists for callers that may not allocate device memory themselves, such as
+ * plug-ins of a host runtime that plans every buffer up front, or hot loops
+ * that must not risk the device-wide synchronisation a cudaMalloc/cudaFree
+ * can cause.  The caller passes inputs and outputs exactly as for the four
+ * steps (same layouts and dtypes; lse may be NULL); all scratch lives in one
+ * fixed 16 MiB device array inside the library, which every GPU that loads
+ * the library keeps reserved until the process exits.  Problems whose three
+ * workspaces (mxsa_workspace_size) add up to more than 16 MiB are rejected
+ * with MXSA_ERR_WORKSPACE before anything runs.  Nothing is allocated.
+ * The first call on a device looks up the array's device address (make that
+ * first call before any stream capture).  Calls share the array: calls that
+ * overlap on the GPU race and must be serialised by the caller.  Device-side
+ * data errors are not reported by this entry point (the status word lives
+ * in the shared array); use the four steps to read them.  Asynchronous on
+ * `stream`. */
+mxsa_status mxsa_attention_noalloc(const mxsa_problem* problem, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* sel, const int32_t* block_tables,
+                                   const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, void* out, float* lse,
+                                   void* stream);
+
 /* Entries per work item tile and tiles per work item used by the scheduler. */
 #define MXSA_TILE_ROWS 128
 #define MXSA_ITEM_TILES 4
