@@ -66,7 +66,8 @@ class IndexLayout(ctypes.Structure):
 
 
 class SchedLayout(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "items", "cost_prefix", "cta_ptr", "lookback", "total")] + \
+    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "items", "cost_prefix", "cta_ptr", "items_dec",
+                                               "cost_prefix_dec", "cta_ptr_dec", "lookback", "total")] + \
                [(n, ctypes.c_int64) for n in ("items_cap", "tiles_cap")]
 
 

@@ -89,11 +89,14 @@ mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L) {
   const int64_t act = il.keys_cap < il.nslots ? il.keys_cap : il.nslots;
   L->tiles_cap = (act + kScanTile - 1) / kScanTile;
   size_t o = 0;
-  L->header = o;      o = align_up(o + kSchInts * 4);
-  L->items = o;       o = align_up(o + (size_t)L->items_cap * 16);
-  L->cost_prefix = o; o = align_up(o + (size_t)(L->items_cap + 1) * 8);
-  L->cta_ptr = o;     o = align_up(o + (size_t)(MXSA_MAX_CTAS + 1) * 4);
-  L->lookback = o;    o = align_up(o + (size_t)(L->tiles_cap > 0 ? L->tiles_cap : 1) * 8);
+  L->header = o;          o = align_up(o + kSchInts * 4);
+  L->items = o;           o = align_up(o + (size_t)L->items_cap * 16);
+  L->cost_prefix = o;     o = align_up(o + (size_t)(L->items_cap + 1) * 8);
+  L->cta_ptr = o;         o = align_up(o + (size_t)(MXSA_MAX_CTAS + 1) * 4);
+  L->items_dec = o;       o = align_up(o + (size_t)L->items_cap * 16);
+  L->cost_prefix_dec = o; o = align_up(o + (size_t)(L->items_cap + 1) * 8);
+  L->cta_ptr_dec = o;     o = align_up(o + (size_t)(MXSA_MAX_CTAS + 1) * 4);
+  L->lookback = o;        o = align_up(o + (size_t)(L->tiles_cap > 0 ? L->tiles_cap : 1) * 16);
   L->total = o;
   return MXSA_OK;
 }
@@ -136,6 +139,9 @@ SchedPtrs sched_ptrs(const mxsa_problem& p, void* ws) {
   x.items = reinterpret_cast<int4*>(b + L.items);
   x.cost_prefix = reinterpret_cast<long long*>(b + L.cost_prefix);
   x.cta_ptr = reinterpret_cast<int32_t*>(b + L.cta_ptr);
+  x.items_dec = reinterpret_cast<int4*>(b + L.items_dec);
+  x.cost_prefix_dec = reinterpret_cast<long long*>(b + L.cost_prefix_dec);
+  x.cta_ptr_dec = reinterpret_cast<int32_t*>(b + L.cta_ptr_dec);
   x.lookback = reinterpret_cast<unsigned long long*>(b + L.lookback);
   return x;
 }

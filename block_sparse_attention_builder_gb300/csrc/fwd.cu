@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int it_begin = a.cta_ptr[blockIdx.x], it_end = a.cta_ptr[blockIdx.x + 1];
+  if (it_begin >= it_end) return;  // uniform: nothing to do, nothing allocated
 
   if (tid == 0) {
     mbar_init(&c.kv_full[0], a.kv_fp8 ? 128 : 1);
@@ -474,6 +475,11 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
     *err_detail = 1;
     return cudaErrorInvalidValue;
   }
+  // decode work items (runs of single-token keys) first, then the
+  // KV-stationary items; each kernel's CTAs without items exit at once
+  cudaError_t de = launch_fwd_decode(p, q, tmk, tmv, block_tables, ix, sc, num_ctas, part_o, part_lse, st,
+                                     err_detail);
+  if (de != cudaSuccess) return de;
   const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
   const size_t smem = fwd_smem_bytes(fp8);
   static std::once_flag once;

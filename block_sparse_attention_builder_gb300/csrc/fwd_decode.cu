@@ -1,0 +1,661 @@
+// KV-outer forward for decode work items (fw-ai/minimax-kernels README,
+// intro: a selected KV block is loaded once for the queries that selected
+// it).  In a sequence with one new token every selected block of a KV head
+// is selected by that one token, so the scheduler hands this kernel runs of
+// up to 8 such blocks; each block is still loaded from HBM exactly once,
+// and the run's partial results are merged on chip by an online softmax,
+// leaving one partial (o, lse) per run instead of one per block.
+//
+// With only G (<= 16) query rows per block, the products are computed
+// transposed so that the 128 keys fill the MMA's M dimension:
+//   S^T = K Q^T   (M = 128 keys, N = rows padded to 16, K = 128)
+//   O^T += V^T P^T (M = 128 head dims, N = rows, K = 128 keys)
+// Accumulators live in tensor memory; softmax thread k owns key k of S^T
+// and head dim k of O^T.  The row maximum m is only raised when a block's
+// score exceeds it by more than 2^8 (then O^T and the per-thread sums are
+// rescaled), so most blocks need no cross-thread reduction.
+//
+// Persistent kernel, 192 threads: warps 0-3 softmax/epilogue (and FP8
+// widening), warp 4 TMA producer (q rows of the item; K and V pages of each
+// block into a 2-3 stage ring), warp 5 TMEM owner and MMA issuer.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mxsa {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kKVTile = 32768;  // 128 keys x 128 x 16-bit
+constexpr uint32_t kStage = 2 * kKVTile;
+constexpr int kMaxStages = 3;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct BlockInfo {
+  int32_t valid, pad0, pad1, pad2;
+};
+
+struct Ctrl {
+  uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
+  uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
+  uint64_t stg_full, stg_empty, done;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  BlockInfo info[kMaxStages];
+};
+
+struct DecArgs {
+  const int32_t* block_tables;
+  const SeqInfo* seq;
+  const int32_t* active;
+  const int32_t* row_ptr;
+  const int4* items;
+  const int32_t* cta_ptr;
+  const int32_t* idx_hdr;
+  const int32_t* sch_hdr;
+  float* part_o;
+  float* part_lse;
+  int32_t* flags;
+  int32_t num_seqs, Hq, Hkv, G, page_size, max_pages, num_pages, kv_fp8, ab_bf16, ns;
+  float scale_log2;
+};
+
+struct Layout {
+  uint32_t q, p, stg, red, ctrl, total;
+};
+
+template <int N>
+__host__ __device__ constexpr Layout smem_layout(int ns, int fp8) {
+  Layout L{};
+  L.q = (uint32_t)ns * kStage;
+  L.p = L.q + 2u * N * 256u;
+  L.stg = L.p + 2u * N * 256u;
+  L.red = L.stg + (fp8 ? kKVTile : 0u);
+  L.ctrl = L.red + 4u * N * 4u;
+  L.total = L.ctrl + (uint32_t)sizeof(Ctrl);
+  return L;
+}
+
+template <int N>
+constexpr int stages_for(int fp8) {
+  return fp8 ? 2 : (N <= 32 ? 3 : 2);
+}
+
+__device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (seq[mid].blk_off <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t swz_kv(uint32_t row, uint32_t chunk16) {
+  return (chunk16 >> 3) * 16384u + row * 128u + (((chunk16 & 7u) ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  if (!bf16) return h2;
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  float2 f = __half22float2(h);
+  return pack2(f.x, f.y, 1);
+}
+
+// named barrier 1 over the 128 softmax threads
+__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool wg_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool wg_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
+  if constexpr (N == 16) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) tmem_ld32(taddr + c * 32, v + c * 32);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float* v) {
+#pragma unroll
+  for (int c = 0; c < N / 16; ++c) {
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[c * 16 + i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr + c * 16),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// per-row maximum / sum over the 128 softmax threads (result in every thread)
+template <int N, bool kMax>
+__device__ __forceinline__ void wg_reduce(float* v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float x = __shfl_xor_sync(0xffffffffu, v[r], o);
+      v[r] = kMax ? fmaxf(v[r], x) : v[r] + x;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < N; ++r) red[warp * N + r] = v[r];
+  }
+  wg_sync();
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    const float a = red[r], b = red[N + r], c = red[2 * N + r], d = red[3 * N + r];
+    v[r] = kMax ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
+  }
+  wg_sync();
+}
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_fwd_dec(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+              const __grid_constant__ CUtensorMap tmq, DecArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(sm + L.ctrl);
+  float* red = reinterpret_cast<float*>(sm + L.red);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = a.ns;
+
+  if (a.sch_hdr[kSchCtas] != (int)gridDim.x) {
+    if (tid == 0 && blockIdx.x == 0) atomicOr(a.flags, MXSA_FLAG_SCHEDULE);
+    return;
+  }
+  const int it_begin = a.cta_ptr[blockIdx.x], it_end = a.cta_ptr[blockIdx.x + 1];
+  if (it_begin >= it_end) return;  // uniform: nothing to do, nothing allocated
+
+  constexpr uint32_t kTmemCols = N <= 8 ? 32 : (N == 16 ? 64 : (N == 32 ? 128 : 256));
+  if (tid == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(&c.kv_full[i], a.kv_fp8 ? 128 : 1);
+      mbar_init(&c.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.q_full[i], 1);
+      mbar_init(&c.q_empty[i], 1);
+      mbar_init(&c.s_full[i], 1);
+      mbar_init(&c.p_full[i], 128);
+      mbar_init(&c.p_empty[i], 1);
+      mbar_init(&c.o_full[i], 1);
+      mbar_init(&c.o_empty[i], 128);
+    }
+    mbar_init(&c.stg_full, 1);
+    mbar_init(&c.stg_empty, 128);
+    mbar_init(&c.done, 1);
+    c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&c.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  volatile int* abort_flag = &c.abort_flag;
+  const uint32_t sbase = smem_u32(sm);
+  const int NB = a.idx_hdr[kHdrNB];
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      tma_prefetch_desc(&tmq);
+      const int ps = a.page_size;
+      const int npg = ps == 128 ? 1 : 2;
+      int blk = 0, n_it = 0;
+      bool ok = true;
+      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+        const int4 itm = a.items[it];
+        const int ib = n_it & 1, ui = n_it >> 1;
+        ok = mbar_wait(&c.q_empty[ib], (ui & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        if (!ok) break;
+        // q rows of the item's token: rows t*Hq + g*G .. + N (rows past G are
+        // padding; rows past the tensor end read as zero)
+        const int key0 = a.active[itm.x];
+        const int g = key0 / NB;
+        const int s = seq_of_block(a.seq, a.num_seqs, key0 - g * NB);
+        const int t = a.seq[s].q_begin;
+        const int row0 = t * a.Hq + g * a.G;
+        uint8_t* qdst = sm + L.q + ib * (N * 256);
+        mbar_arrive_expect_tx(&c.q_full[ib], (uint32_t)N * 256u);
+        tma_load_2d(qdst, &tmq, &c.q_full[ib], 0, row0);
+        tma_load_2d(qdst + N * 128, &tmq, &c.q_full[ib], 64, row0);
+        for (int j = 0; j < itm.w && ok; ++j, ++blk) {
+          const int st = blk % ns, us = blk / ns;
+          ok = mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          if (!ok) break;
+          const int key = a.active[itm.x + j];
+          const int r = key - g * NB;
+          const SeqInfo si = a.seq[s];
+          const int b = r - si.blk_off;
+          const int valid = min(128, si.L - 128 * b);
+          int pages[2] = {-1, -1};
+          for (int pg = 0; pg < npg; ++pg) {
+            if (pg * 64 >= valid) continue;
+            const int lp = ps == 128 ? b : 2 * b + pg;
+            const int phys = a.block_tables[(size_t)s * a.max_pages + lp];
+            if (phys < 0 || phys >= a.num_pages) {
+              atomicOr(a.flags, MXSA_FLAG_PAGE);
+              continue;
+            }
+            pages[pg] = phys;
+          }
+          c.info[st].valid = valid;
+          const int present = (pages[0] >= 0) + (pages[1] >= 0);
+          if (!a.kv_fp8) {
+            uint8_t* kdst = sm + st * kStage;
+            uint8_t* vdst = kdst + kKVTile;
+            mbar_arrive_expect_tx(&c.kv_full[st], (uint32_t)present * (uint32_t)ps * 512u);
+            for (int pg = 0; pg < npg; ++pg) {
+              if (pages[pg] < 0) continue;
+              const int z = pages[pg] * a.Hkv + g;
+              for (int h = 0; h < 2; ++h) {
+                tma_load_3d(kdst + h * 16384 + pg * 8192, &tmk, &c.kv_full[st], h * 64, 0, z);
+                tma_load_3d(vdst + h * 16384 + pg * 8192, &tmv, &c.kv_full[st], h * 64, 0, z);
+              }
+            }
+          } else {
+            ok = mbar_wait(&c.stg_empty, (blk & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (!ok) break;
+            uint8_t* stg = sm + L.stg;
+            mbar_arrive_expect_tx(&c.stg_full, (uint32_t)present * (uint32_t)ps * 256u);
+            for (int pg = 0; pg < npg; ++pg) {
+              if (pages[pg] < 0) continue;
+              const int z = pages[pg] * a.Hkv + g;
+              tma_load_3d(stg + pg * 8192, &tmk, &c.stg_full, 0, 0, z);
+              tma_load_3d(stg + 16384 + pg * 8192, &tmv, &c.stg_full, 0, 0, z);
+            }
+          }
+        }
+      }
+      // drain the loads in flight before the CTA may exit
+      for (int k = std::max(0, blk - ns); k < blk; ++k) {
+        if (a.kv_fp8) {
+          if (k == blk - 1) mbar_wait(&c.stg_full, k & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        } else {
+          mbar_wait(&c.kv_full[k % ns], (k / ns) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        }
+      }
+      if (n_it > 0)
+        mbar_wait(&c.q_full[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                  kWaitLimitNs);
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(128, N, (uint32_t)a.ab_bf16, 0, 0);
+      const uint32_t id_o = idesc_f16(128, N, (uint32_t)a.ab_bf16, 1, 0);
+      int blk = 0, n_it = 0;
+      bool ok = true;
+      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+        const int nk = a.items[it].w;
+        const int ib = n_it & 1, ui = n_it >> 1;
+        const uint32_t q_s = sbase + L.q + ib * (N * 256);
+        const uint32_t tO = tmem + 2 * N + ib * N;
+        ok = mbar_wait(&c.q_full[ib], ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs) &&
+             mbar_wait(&c.o_empty[ib], (ui & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        if (!ok) break;
+        const int first = blk;
+        for (int j = 0; j <= nk && ok; ++j) {
+          if (j < nk) {  // S^T of block blk
+            const int st = (blk + j) % ns, us = (blk + j) / ns, sb = (blk + j) & 1;
+            ok = mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t k_s = sbase + st * kStage;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t off_k = (ks >> 2) * 16384u + (ks & 3) * 32u;
+              const uint32_t off_q = (ks >> 2) * (uint32_t)(N * 128) + (ks & 3) * 32u;
+              mma_f16_ss(tmem + sb * N, smem_desc_sw128(k_s + off_k, 0, 1024), smem_desc_sw128(q_s + off_q, 0, 1024),
+                         id_s, ks > 0);
+            }
+            mma_commit(&c.s_full[sb]);
+            if (j == nk - 1) mma_commit(&c.q_empty[ib]);
+          }
+          if (j > 0) {  // O^T += V^T P^T of the previous block
+            const int pb = blk + j - 1;
+            const int st = pb % ns, sb = pb & 1, ub = pb >> 1;
+            ok = mbar_wait(&c.p_full[sb], ub & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t v_s = sbase + st * kStage + kKVTile;
+            const uint32_t p_s = sbase + L.p + sb * (N * 256);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t off_p = (ks >> 2) * (uint32_t)(N * 128) + (ks & 3) * 32u;
+              mma_f16_ss(tO, smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), smem_desc_sw128(p_s + off_p, 0, 1024),
+                         id_o, (pb != first || ks > 0) ? 1u : 0u);
+            }
+            mma_commit(&c.p_empty[sb]);
+            mma_commit(&c.kv_empty[st]);
+            if (j == nk) mma_commit(&c.o_full[ib]);
+          }
+        }
+        blk += nk;
+      }
+      mma_commit(&c.done);
+      mbar_wait(&c.done, 0, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------ softmax group
+    const int k = tid;  // key of S^T / head dim of O^T / TMEM lane
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    const int bf16 = a.ab_bf16;
+    const float c2 = a.scale_log2;
+    int blk = 0, n_it = 0;
+    bool ok = true;
+    float m[N], lsum[N];
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+      const int4 itm = a.items[it];
+      const int nk = itm.w;
+      const int ib = n_it & 1, ui = n_it >> 1;
+      const uint32_t tO = tmem + lane_addr + 2 * N + ib * N;
+      for (int j = 0; j < nk && ok; ++j, ++blk) {
+        const int st = blk % ns, us = blk / ns, sb = blk & 1, ub = blk >> 1;
+        uint8_t* kst = sm + st * kStage;
+        uint8_t* vst = kst + kKVTile;
+        int valid;
+        if (a.kv_fp8) {
+          ok = wg_all(mbar_wait(&c.stg_full, blk & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+          if (!ok) break;
+          valid = c.info[st].valid;
+          const uint8_t* stg = sm + L.stg;
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t* src = stg + kv * 16384 + k * 128;
+            const uint32_t dst = smem_u32(kv ? vst : kst);
+            for (int cc = 0; cc < 8; ++cc) {
+              const int c8 = (cc + k) & 7;
+              uint4 raw = make_uint4(0, 0, 0, 0);
+              if (k < valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
+              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                o[2 * i] = widen_e4m3x2((uint16_t)(w[i] & 0xffffu), bf16);
+                o[2 * i + 1] = widen_e4m3x2((uint16_t)(w[i] >> 16), bf16);
+              }
+              st_shared_v4(dst + swz_kv(k, 2 * c8), o[0], o[1], o[2], o[3]);
+              st_shared_v4(dst + swz_kv(k, 2 * c8 + 1), o[4], o[5], o[6], o[7]);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&c.stg_empty);
+          mbar_arrive(&c.kv_full[st]);
+        } else {
+          ok = wg_all(mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+          if (!ok) break;
+          valid = c.info[st].valid;
+          if (k >= valid) {
+            // keys past the sequence end must not bring stale values into P V
+            for (int ch = 0; ch < 16; ++ch) st_shared_v4(smem_u32(vst) + swz_kv(k, ch), 0, 0, 0, 0);
+          }
+        }
+        // ---- scores of key k for every row
+        ok = wg_all(mbar_wait(&c.s_full[sb], ub & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        if (!ok) break;
+        tc_fence_after();
+        float x[N];
+        tmem_ld_n<N>(tmem + lane_addr + sb * N, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int r = 0; r < N; ++r) x[r] = (k < valid && r < a.G) ? x[r] * c2 : -INFINITY;
+        if (j == 0) {
+#pragma unroll
+          for (int r = 0; r < N; ++r) m[r] = x[r];
+          wg_reduce<N, true>(m, red);
+#pragma unroll
+          for (int r = 0; r < N; ++r) {
+            if (m[r] == -INFINITY) m[r] = 0.f;  // padding rows
+            lsum[r] = 0.f;
+          }
+        } else {
+          bool exceed = false;
+#pragma unroll
+          for (int r = 0; r < N; ++r) exceed |= x[r] > m[r] + kRescaleThreshold;
+          if (wg_any(exceed)) {
+            // raise m: wait until the previous P V finished, rescale O^T
+            float mb[N];
+#pragma unroll
+            for (int r = 0; r < N; ++r) mb[r] = x[r];
+            wg_reduce<N, true>(mb, red);
+            const int pb = blk - 1;
+            ok = wg_all(mbar_wait(&c.p_empty[pb & 1], (pb >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                  kWaitLimitNs));
+            if (!ok) break;
+            tc_fence_after();
+            float alpha[N], o[N];
+#pragma unroll
+            for (int r = 0; r < N; ++r) {
+              const float mn = fmaxf(m[r], mb[r]);
+              alpha[r] = ex2_approx(m[r] - mn);
+              m[r] = mn;
+              lsum[r] *= alpha[r];
+            }
+            tmem_ld_n<N>(tO, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int r = 0; r < N; ++r) o[r] *= alpha[r];
+            tmem_st_n<N>(tO, o);
+          }
+        }
+        // ---- P^T of key k into the [rows][keys] operand tile
+        ok = wg_all(mbar_wait(&c.p_empty[sb], (ub & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        if (!ok) break;
+        float p[N];
+#pragma unroll
+        for (int r = 0; r < N; ++r) {
+          p[r] = x[r] == -INFINITY ? 0.f : ex2_approx(x[r] - m[r]);
+          lsum[r] += p[r];
+        }
+        {
+          uint8_t* pbuf = sm + L.p + sb * (N * 256);
+          const uint32_t half = (uint32_t)(k >> 6) * (uint32_t)(N * 128);
+          const uint32_t kk = (uint32_t)(k & 63);
+          const bool odd = k & 1;
+#pragma unroll
+          for (int r = 0; r < N; ++r) {
+            const float other = __shfl_xor_sync(0xffffffffu, p[r], 1);
+            // even keys store rows 0,2,4,..; odd keys rows 1,3,5,..: one
+            // 4-byte pair (key & ~1, key | 1) per store
+            if ((r & 1) == (int)odd) {
+              const float lo = odd ? other : p[r], hi = odd ? p[r] : other;
+              const uint32_t kp = kk & ~1u;
+              const uint32_t off = half + (uint32_t)r * 128u + ((((kp >> 3) ^ (uint32_t)(r & 7)) << 4) | ((kp & 7u) * 2u));
+              *reinterpret_cast<uint32_t*>(pbuf + off) = pack2(lo, hi, bf16);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&c.p_full[sb]);
+      }
+      if (!ok) break;
+      // ---- epilogue of the item: o = O / l, lse = (m + log2 l) ln 2
+      ok = wg_all(mbar_wait(&c.o_full[ib], ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+      if (!ok) break;
+      tc_fence_after();
+      float o[N];
+      tmem_ld_n<N>(tO, o);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&c.o_empty[ib]);
+      wg_reduce<N, false>(lsum, red);
+      const int e0 = itm.y;
+      const int G = a.G;
+      float* dst = a.part_o + (size_t)e0 * G * 128 + k;
+#pragma unroll
+      for (int r = 0; r < N; ++r)
+        if (r < G) dst[(size_t)r * 128] = lsum[r] > 0.f ? o[r] / lsum[r] : 0.f;
+      if (k < G) {
+        float lv = -INFINITY, mv = 0.f;
+#pragma unroll
+        for (int r = 0; r < N; ++r)
+          if (r == k) {
+            lv = lsum[r];
+            mv = m[r];
+          }
+        a.part_lse[(size_t)e0 * G + k] = lv > 0.f ? (mv + lg2_approx(lv)) * 0.69314718055994530942f : -INFINITY;
+      }
+      // the other keys of the run carry no weight of their own
+      for (int idx = k; idx < (nk - 1) * G; idx += 128) {
+        const int jj = 1 + idx / G, rr = idx % G;
+        const int e = a.row_ptr[a.active[itm.x + jj]];
+        a.part_lse[(size_t)e * G + rr] = -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_q_map(CUtensorMap* m, const void* q, const mxsa_problem& p, int n_rows_box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)p.total_q * p.num_q_heads};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, (cuuint32_t)n_rows_box};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapDataType dt = p.q_dtype == MXSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, dt, 2, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int N>
+cudaError_t launch_n(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq, DecArgs a,
+                     int num_ctas, cudaStream_t st) {
+  a.ns = stages_for<N>(a.kv_fp8);
+  const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
+  const size_t smem = L.total + 1024;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    const Layout l16 = smem_layout<N>(stages_for<N>(0), 0), l8 = smem_layout<N>(stages_for<N>(1), 1);
+    attr_err = cudaFuncSetAttribute(k_fwd_dec<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(std::max(l16.total, l8.total) + 1024));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  k_fwd_dec<N><<<num_ctas, kThreads, smem, st>>>(tmk, tmv, tmq, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_decode(const mxsa_problem& p, const void* q, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
+                              float* part_o, float* part_lse, cudaStream_t st, int* err_detail) {
+  const int G = p.num_q_heads / p.num_kv_heads;
+  if (G > kDecodeMaxG || p.total_q == 0) return cudaSuccess;  // no decode items exist
+  constexpr int N = 16;
+  CUtensorMap tmq;
+  if (!make_q_map(&tmq, q, p, N)) {
+    *err_detail = 1;
+    return cudaErrorInvalidValue;
+  }
+  DecArgs a;
+  a.block_tables = block_tables;
+  a.seq = ix.seq;
+  a.active = ix.active;
+  a.row_ptr = ix.row_ptr;
+  a.items = sc.items_dec;
+  a.cta_ptr = sc.cta_ptr_dec;
+  a.idx_hdr = ix.hdr;
+  a.sch_hdr = sc.hdr;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.flags = ix.hdr + kHdrFlags;
+  a.num_seqs = p.num_seqs;
+  a.Hq = p.num_q_heads;
+  a.Hkv = p.num_kv_heads;
+  a.G = G;
+  a.page_size = p.page_size;
+  a.max_pages = p.max_pages_per_seq;
+  a.num_pages = p.num_pages;
+  a.kv_fp8 = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 0;
+  a.ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
+  a.ns = 0;
+  const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_n<N>(tmk, tmv, tmq, a, num_ctas, st);
+}
+
+}  // namespace mxsa

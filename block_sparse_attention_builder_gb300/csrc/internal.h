@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mxsa.h"
@@ -24,13 +25,22 @@ enum : int {
 
 // schedule workspace header (int32 words)
 enum : int {
-  kSchItems = 0,
+  kSchItems = 0,     // normal (KV-stationary) items
   kSchCtas = 1,
   kSchCostLo = 2,
   kSchCostHi = 3,
   kSchTileCtr = 4,
+  kSchDecItems = 5,  // merged decode items
+  kSchDecCostLo = 6,
+  kSchDecCostHi = 7,
   kSchInts = 16
 };
+
+// keys of one single-token sequence and kv head are merged into decode items
+// of at most this many blocks; decode items need G <= kDecodeMaxG (the rows
+// of one token fill one 16-wide MMA N dimension)
+constexpr int kDecodeBlocks = 8;
+constexpr int kDecodeMaxG = 16;
 
 // Per-sequence metadata written by the index builder.
 struct SeqInfo {
@@ -61,10 +71,13 @@ struct IndexPtrs {
 
 struct SchedPtrs {
   int32_t* hdr;
-  int4* items;
+  int4* items;              // normal items {key, entry_begin, n_entries, 0}
   long long* cost_prefix;
   int32_t* cta_ptr;
-  unsigned long long* lookback;
+  int4* items_dec;          // decode items {active_pos, entry, 1, n_keys}
+  long long* cost_prefix_dec;
+  int32_t* cta_ptr_dec;
+  unsigned long long* lookback;  // 2 words per tile: normal, decode
 };
 
 constexpr int kScanThreads = 256;
@@ -89,6 +102,10 @@ cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const Sc
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
                        float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
+// decode work list (merged single-token runs), launched by launch_fwd
+cudaError_t launch_fwd_decode(const mxsa_problem& p, const void* q, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
+                              float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
 cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
                            const float* part_lse, void* out, float* lse, cudaStream_t st);
 

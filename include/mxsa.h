@@ -173,11 +173,17 @@ typedef struct {
 mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layout* layout);
 
 /* Byte offsets inside the schedule workspace.  header: int32[16] =
- * {n_items, num_ctas, total cost low 32 bits, total cost high 32 bits, ...};
- * items: int32[4] per item = {key, entry_begin, n_entries, 0};
- * cost_prefix: int64 [n_items + 1]; cta_ptr: int32 [num_ctas + 1]. */
+ * {n_items, num_ctas, total cost low, total cost high, (scan counter),
+ *  n_dec_items, decode cost low, decode cost high, ...};
+ * Two lists, each with int64 exclusive cost prefixes [n + 1] and its own
+ * partition cta_ptr int32 [num_ctas + 1]:
+ *   items:     int32[4] = {key, entry_begin, n_entries, 0}, keys of
+ *              sequences with several new tokens (KV-stationary tiles);
+ *   items_dec: int32[4] = {position in active_keys, entry, 1, n_keys}, runs
+ *              of up to 8 keys of one single-token sequence and kv head
+ *              (every one of those keys holds that token's one entry). */
 typedef struct {
-  size_t header, items, cost_prefix, cta_ptr, lookback, total;
+  size_t header, items, cost_prefix, cta_ptr, items_dec, cost_prefix_dec, cta_ptr_dec, lookback, total;
   int64_t items_cap, tiles_cap;
 } mxsa_sched_layout;
 mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layout* layout);
@@ -204,9 +210,11 @@ mxsa_status mxsa_attention_noalloc(const mxsa_problem* problem, const void* q, c
                                    const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, void* out, float* lse,
                                    void* stream);
 
-/* Entries per work item tile and tiles per work item used by the scheduler. */
+/* Rows per tile, tiles per normal work item and blocks per decode work item
+ * used by the scheduler. */
 #define MXSA_TILE_ROWS 128
 #define MXSA_ITEM_TILES 4
+#define MXSA_DECODE_BLOCKS 8
 #define MXSA_MAX_CTAS 4096
 
 #ifdef __cplusplus

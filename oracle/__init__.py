@@ -65,9 +65,9 @@ def _load():
         _lib.oracle_combine.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P]
         _lib.oracle_build_index.restype = ctypes.c_int
         _lib.oracle_build_index.argtypes = [P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
-        _lib.oracle_schedule.restype = ctypes.c_int64
-        _lib.oracle_schedule.argtypes = [P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, P,
-                                         ctypes.c_int64, P, P]
+        _lib.oracle_schedule.restype = ctypes.c_int
+        _lib.oracle_schedule.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int64, P]
     return _lib
 
 
@@ -165,20 +165,31 @@ def build_index(prob: OracleProblem, selected, cu_seqlens_q, used_kv_lens):
                 slot_entry=slot_entry[:nslots].copy(), flags=flags.value)
 
 
-def schedule(prob: OracleProblem, used_kv_lens, index: dict, rows_per_item_tiles: int, num_ctas: int):
-    """Returns dict(items [n,4] int32, cost_prefix [n+1] int64, cta_ptr [P+1] int32)."""
+def schedule(prob: OracleProblem, used_kv_lens, cu_seqlens_q, index: dict, rows_per_item_tiles: int,
+             decode_blocks: int, num_ctas: int):
+    """Returns dict(items, cost_prefix, cta_ptr) for the normal list and
+    dict(items_dec, cost_prefix_dec, cta_ptr_dec) for the decode list."""
     lib = _load()
     lens = _c(used_kv_lens, np.int32)
+    cu = _c(cu_seqlens_q, np.int64)
     row_ptr = _c(index["row_ptr"], np.int32)
     cap = max(int(row_ptr[-1]) + 1, 1)
-    items = np.zeros((cap, 4), dtype=np.int32)
-    cost = np.zeros(cap + 1, dtype=np.int64)
-    cta = np.zeros(num_ctas + 1, dtype=np.int32)
-    n = lib.oracle_schedule(ctypes.byref(prob), _ptr(lens), index["nb"], _ptr(row_ptr), rows_per_item_tiles,
-                            num_ctas, _ptr(items), ctypes.c_int64(cap), _ptr(cost), _ptr(cta))
-    if n < 0:
+    items_n = np.zeros((cap, 4), dtype=np.int32)
+    cost_n = np.zeros(cap + 1, dtype=np.int64)
+    cta_n = np.zeros(num_ctas + 1, dtype=np.int32)
+    items_d = np.zeros((cap, 4), dtype=np.int32)
+    cost_d = np.zeros(cap + 1, dtype=np.int64)
+    cta_d = np.zeros(num_ctas + 1, dtype=np.int32)
+    counts = np.zeros(2, dtype=np.int64)
+    rc = lib.oracle_schedule(ctypes.byref(prob), _ptr(lens), _ptr(cu), index["nb"], _ptr(row_ptr),
+                             rows_per_item_tiles, decode_blocks, num_ctas, _ptr(items_n), _ptr(cost_n),
+                             _ptr(cta_n), _ptr(items_d), _ptr(cost_d), _ptr(cta_d), ctypes.c_int64(cap),
+                             _ptr(counts))
+    if rc != 0:
         raise RuntimeError("oracle_schedule: item capacity exceeded")
-    return dict(items=items[:n].copy(), cost_prefix=cost[:n + 1].copy(), cta_ptr=cta)
+    nn, nd = int(counts[0]), int(counts[1])
+    return dict(items=items_n[:nn].copy(), cost_prefix=cost_n[:nn + 1].copy(), cta_ptr=cta_n,
+                items_dec=items_d[:nd].copy(), cost_prefix_dec=cost_d[:nd + 1].copy(), cta_ptr_dec=cta_d)
 
 
 def problem_for(w, softmax_scale: float = 0.0) -> OracleProblem:

@@ -266,7 +266,9 @@ void oracle_combine(int32_t n, int32_t d, const double* o, const double* lse, do
  * Definition (exact, integer):
  *   nblk_s  = ceil(L_s / 128) with L_s clamped to [0, max_pages * page_size];
  *   blk_off = exclusive prefix sum of nblk;  NB = sum nblk;
- *   slot    = (t * Hkv + g) * topk + k, taken in increasing order;
+ *   slot    = (t * Hkv + g) * topk + k, taken in increasing order (none
+ *             when cu_seqlens_q is not a non-decreasing partition of
+ *             [0, total_q]: flag 128, nothing indexed);
  *   a slot is an entry unless its block is -1, out of [0, nblk_s) (flag 1),
  *   equal to an earlier slot's block in the same (t, g) row (flag 2), or,
  *   when causal, starts after the token's position (128 b > pos(t));
@@ -323,7 +325,9 @@ int oracle_build_index(const oracle_problem* p, const int32_t* sel, const int64_
   }
   int64_t n = 0;
   for (int64_t slot = 0; slot < nslots; ++slot) slot_entry[slot] = -1;
-  for (int64_t t = 0; t < p->total_q; ++t) {
+  /* an invalid cu_seqlens_q defines no token -> sequence map: nothing is indexed */
+  const int64_t t_end = (flags & OR_FLAG_CU) ? 0 : p->total_q;
+  for (int64_t t = 0; t < t_end; ++t) {
     int32_t s = seq_of_token(cu, B, t);
     for (int32_t g = 0; g < Hkv; ++g) {
       for (int32_t k = 0; k < K; ++k) {
@@ -369,67 +373,145 @@ int oracle_build_index(const oracle_problem* p, const int32_t* sel, const int64_
 
 /* --------------------------------------------------------------- schedule
  * Load-balancing schedule over the index ("load-balancing scheduler" in the
- * README's test list; the splitting rule and cost model are this library's).
+ * README's test list; the splitting rule, the decode merge and the cost
+ * model are this library's).
  *
- * Definition (exact, integer):
- *   G = Hq / Hkv;  E = rows_per_item_tiles * max(1, 128 / G) entries per item;
- *   for each key with cnt > 0, in key order: n = ceil(cnt / E) items, item i
- *     covering entries [row_ptr[key] + i*cnt/n, row_ptr[key] + (i+1)*cnt/n);
- *   cost(item) = valid_tokens(key) * kv_weight + tiles(item) * 256 + rows(item) * 2
- *     with valid_tokens = min(128, L_s - 128 b), kv_weight = 2 (16-bit caches)
- *     or 1 (FP8), tiles = ceil(entries / max(1, 128 / G)), rows = entries * G;
- *   prefix = exclusive prefix sum of cost over items, C = total;
- *   cta_ptr[c] = #{items i : prefix[i] < floor(c * C / P)}  for c = 0..P.
- * items[4*i..] = {key, entry_begin, n_entries, 0}.  Returns the item count,
- * or -1 when `items_cap` is too small. */
-int64_t oracle_schedule(const oracle_problem* p, const int32_t* lens, int32_t nb, const int32_t* row_ptr,
-                        int32_t rows_per_item_tiles, int32_t num_ctas, int32_t* items, int64_t items_cap,
-                        int64_t* cost_prefix, int32_t* cta_ptr) {
-  const int32_t B = p->num_seqs, Hkv = p->num_kv_heads;
+ * Definition (exact, integer), keys with cnt > 0 taken in key order:
+ *   G = Hq / Hkv;  a key (g, s, b) is a DECODE key when the sequence has
+ *   exactly one new token (Tq_s == 1) and G <= 16; otherwise it is NORMAL.
+ *   NORMAL: E = rows_per_item_tiles * max(1, 128 / G) entries per item;
+ *     n = ceil(cnt / E) items, item i covering entries
+ *     [row_ptr[key] + i*cnt/n, row_ptr[key] + (i+1)*cnt/n);
+ *     cost = valid_tokens(key) * kv_weight + tiles * 256 + rows * 2 with
+ *     tiles = ceil(entries / max(1, 128 / G)), rows = entries * G.
+ *   DECODE: a run is a maximal sequence of consecutive active keys with the
+ *     same (g, s) (all hold the same single entry: the one token of s);
+ *     a run of len keys becomes n = ceil(len / decode_blocks) items, item i
+ *     covering run positions [i*len/n, (i+1)*len/n);  item = {position of
+ *     its first key in the active-key list, entry of that key, 1, nkeys};
+ *     cost = sum over its keys of valid_tokens * kv_weight + nkeys * 64 + 256.
+ *   valid_tokens = min(128, L_s - 128 b); kv_weight = 2 (16-bit) or 1 (FP8).
+ *   Each list (normal, decode) gets its own exclusive cost prefix (total C)
+ *   and its own partition: cta_ptr[c] = #{items i : prefix[i] < floor(c*C/P)}.
+ * items rows: {key, entry_begin, n_entries, 0} (normal);
+ *             {active_pos, entry, 1, nkeys} (decode).
+ * out_counts[0] = normal items, out_counts[1] = decode items.
+ * Returns 0, or -1 when a capacity is too small. */
+static int64_t seq_len_clamped(const oracle_problem* p, const int32_t* lens, int32_t s) {
+  const int64_t cap_len = (int64_t)p->max_pages_per_seq * p->page_size;
+  return lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
+}
+
+static void key_to_gsb(const oracle_problem* p, const int32_t* lens, int32_t nb, int64_t key, int32_t* g,
+                       int32_t* s, int64_t* b) {
+  *g = (int32_t)(key / nb);
+  int64_t r = key % nb, off = 0;
+  int32_t ss;
+  for (ss = 0; ss < p->num_seqs; ++ss) {
+    int64_t nblk = (seq_len_clamped(p, lens, ss) + 127) / 128;
+    if (r < off + nblk) break;
+    off += nblk;
+  }
+  *s = ss;
+  *b = r - off;
+}
+
+static void partition(int64_t n_items, const int64_t* prefix, int32_t num_ctas, int32_t* cta_ptr) {
+  const int64_t C = prefix[n_items];
+  for (int32_t c = 0; c <= num_ctas; ++c) {
+    int64_t target = (int64_t)c * C / num_ctas, cnt = 0;
+    for (int64_t i = 0; i < n_items; ++i)
+      if (prefix[i] < target) ++cnt;
+    cta_ptr[c] = (int32_t)cnt;
+  }
+}
+
+int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t* cu, int32_t nb,
+                    const int32_t* row_ptr, int32_t rows_per_item_tiles, int32_t decode_blocks, int32_t num_ctas,
+                    int32_t* items_n, int64_t* cost_n, int32_t* cta_n, int32_t* items_d, int64_t* cost_d,
+                    int32_t* cta_d, int64_t items_cap, int64_t* out_counts) {
+  const int32_t Hkv = p->num_kv_heads;
   const int32_t G = p->num_q_heads / Hkv;
   const int32_t per_tile = 128 / G > 0 ? 128 / G : 1;
   const int64_t E = (int64_t)rows_per_item_tiles * per_tile;
   const int32_t kvw = p->kv_dtype == OR_FP8_E4M3 ? 1 : 2;
-  const int64_t cap_len = (int64_t)p->max_pages_per_seq * p->page_size;
-  int64_t n_items = 0, C = 0;
-  for (int64_t key = 0; key < (int64_t)Hkv * nb; ++key) {
-    int64_t cnt = row_ptr[key + 1] - row_ptr[key];
-    if (cnt <= 0) continue;
-    /* (g, s, b) of the key: key = g*NB + blk_off[s] + b */
-    int64_t r = key % nb;
-    int32_t s = 0;
-    int64_t off = 0;
-    for (s = 0; s < B; ++s) {
-      int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
-      int64_t nblk = (L + 127) / 128;
-      if (r < off + nblk) break;
-      off += nblk;
+  const int64_t nkeys = (int64_t)Hkv * nb;
+  /* the active keys, in key order */
+  int64_t n_active = 0;
+  for (int64_t key = 0; key < nkeys; ++key)
+    if (row_ptr[key + 1] > row_ptr[key]) ++n_active;
+  int64_t* active = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_active > 0 ? n_active : 1));
+  if (!active) return -1;
+  n_active = 0;
+  for (int64_t key = 0; key < nkeys; ++key)
+    if (row_ptr[key + 1] > row_ptr[key]) active[n_active++] = key;
+  int64_t nn = 0, nd = 0, Cn = 0, Cd = 0;
+  for (int64_t a = 0; a < n_active; ++a) {
+    int32_t g, s;
+    int64_t b;
+    key_to_gsb(p, lens, nb, active[a], &g, &s, &b);
+    const int64_t L = seq_len_clamped(p, lens, s);
+    const int64_t Tq_s = cu[s + 1] - cu[s];
+    const int dec = Tq_s == 1 && G <= 16;
+    if (!dec) {
+      const int64_t key = active[a];
+      const int64_t cnt = row_ptr[key + 1] - row_ptr[key];
+      const int64_t valid = L - 128 * b < 128 ? L - 128 * b : 128;
+      const int64_t n = (cnt + E - 1) / E;
+      for (int64_t i = 0; i < n; ++i) {
+        const int64_t e0 = i * cnt / n, e1 = (i + 1) * cnt / n, ne = e1 - e0;
+        if (nn >= items_cap) { free(active); return -1; }
+        items_n[4 * nn + 0] = (int32_t)key;
+        items_n[4 * nn + 1] = (int32_t)(row_ptr[key] + e0);
+        items_n[4 * nn + 2] = (int32_t)ne;
+        items_n[4 * nn + 3] = 0;
+        cost_n[nn] = Cn;
+        Cn += valid * kvw + ((ne + per_tile - 1) / per_tile) * 256 + ne * G * 2;
+        ++nn;
+      }
+      continue;
     }
-    int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
-    int64_t b = r - off;
-    int64_t valid = L - 128 * b < 128 ? L - 128 * b : 128;
-    int64_t n = (cnt + E - 1) / E;
+    /* decode: only the first key of a run emits; the run ends where (g, s) changes */
+    if (a > 0) {
+      int32_t g2, s2;
+      int64_t b2;
+      key_to_gsb(p, lens, nb, active[a - 1], &g2, &s2, &b2);
+      if (g2 == g && s2 == s) continue;
+    }
+    int64_t len = 1;
+    while (a + len < n_active) {
+      int32_t g2, s2;
+      int64_t b2;
+      key_to_gsb(p, lens, nb, active[a + len], &g2, &s2, &b2);
+      if (g2 != g || s2 != s) break;
+      ++len;
+    }
+    const int64_t n = (len + decode_blocks - 1) / decode_blocks;
     for (int64_t i = 0; i < n; ++i) {
-      int64_t e0 = i * cnt / n, e1 = (i + 1) * cnt / n;
-      if (n_items >= items_cap) return -1;
-      int64_t ne = e1 - e0;
-      items[4 * n_items + 0] = (int32_t)key;
-      items[4 * n_items + 1] = (int32_t)(row_ptr[key] + e0);
-      items[4 * n_items + 2] = (int32_t)ne;
-      items[4 * n_items + 3] = 0;
-      int64_t cost = valid * kvw + ((ne + per_tile - 1) / per_tile) * 256 + ne * G * 2;
-      cost_prefix[n_items] = C;
-      C += cost;
-      ++n_items;
+      const int64_t k0 = i * len / n, k1 = (i + 1) * len / n;
+      if (nd >= items_cap) { free(active); return -1; }
+      items_d[4 * nd + 0] = (int32_t)(a + k0);
+      items_d[4 * nd + 1] = row_ptr[active[a + k0]];
+      items_d[4 * nd + 2] = 1;
+      items_d[4 * nd + 3] = (int32_t)(k1 - k0);
+      cost_d[nd] = Cd;
+      int64_t c = (k1 - k0) * 64 + 256;
+      for (int64_t k = k0; k < k1; ++k) {
+        int32_t g2, s2;
+        int64_t b2;
+        key_to_gsb(p, lens, nb, active[a + k], &g2, &s2, &b2);
+        c += (L - 128 * b2 < 128 ? L - 128 * b2 : 128) * kvw;
+      }
+      Cd += c;
+      ++nd;
     }
   }
-  cost_prefix[n_items] = C;
-  for (int32_t c = 0; c <= num_ctas; ++c) {
-    int64_t target = (int64_t)c * C / num_ctas;
-    int64_t cnt = 0;
-    for (int64_t i = 0; i < n_items; ++i)
-      if (cost_prefix[i] < target) ++cnt;
-    cta_ptr[c] = (int32_t)cnt;
-  }
-  return n_items;
+  cost_n[nn] = Cn;
+  cost_d[nd] = Cd;
+  partition(nn, cost_n, num_ctas, cta_n);
+  partition(nd, cost_d, num_ctas, cta_d);
+  out_counts[0] = nn;
+  out_counts[1] = nd;
+  free(active);
+  return 0;
 }

@@ -10,6 +10,7 @@ import oracle
 
 TORCH = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8": torch.float8_e4m3fn}
 ITEM_TILES = 4
+DECODE_BLOCKS = 8
 
 
 def device_inputs(w, device="cuda"):
@@ -48,11 +49,21 @@ def read_sched(attn, num_ctas):
     L = mx.sched_layout(attn.prob)
     ws = attn.ws.sched.cpu().numpy()
     hdr = ws[L.header:L.header + 64].view(np.int32)
-    n = int(hdr[0])
+    n, nd = int(hdr[0]), int(hdr[5])
     items = ws[L.items:L.items + 16 * n].view(np.int32).reshape(n, 4).copy()
     cost = ws[L.cost_prefix:L.cost_prefix + 8 * (n + 1)].view(np.int64).copy()
     cta = ws[L.cta_ptr:L.cta_ptr + 4 * (num_ctas + 1)].view(np.int32).copy()
-    return dict(items=items, cost_prefix=cost, cta_ptr=cta, num_ctas=int(hdr[1]))
+    items_d = ws[L.items_dec:L.items_dec + 16 * nd].view(np.int32).reshape(nd, 4).copy()
+    cost_d = ws[L.cost_prefix_dec:L.cost_prefix_dec + 8 * (nd + 1)].view(np.int64).copy()
+    cta_d = ws[L.cta_ptr_dec:L.cta_ptr_dec + 4 * (num_ctas + 1)].view(np.int32).copy()
+    return dict(items=items, cost_prefix=cost, cta_ptr=cta, items_dec=items_d, cost_prefix_dec=cost_d,
+                cta_ptr_dec=cta_d, num_ctas=int(hdr[1]))
+
+
+def oracle_schedule(w, num_ctas):
+    prob = oracle.problem_for(w)
+    idx = oracle.build_index(prob, w.selected, w.cu_seqlens_q, w.used_kv_lens)
+    return oracle.schedule(prob, w.used_kv_lens, w.cu_seqlens_q, idx, ITEM_TILES, DECODE_BLOCKS, num_ctas)
 
 
 def read_partials(attn):

@@ -67,30 +67,45 @@ def test_index_bit_exact(name, small_runs):
 def test_schedule_bit_exact(name, small_runs):
     w = SMALL[name]
     attn = small_runs[name][0]
-    prob = oracle.problem_for(w)
-    ref_idx = oracle.build_index(prob, w.selected, w.cu_seqlens_q, w.used_kv_lens)
-    ref = oracle.schedule(prob, w.used_kv_lens, ref_idx, U.ITEM_TILES, NUM_SMS)
+    ref = U.oracle_schedule(w, NUM_SMS)
     got = U.read_sched(attn, NUM_SMS)
     assert got["num_ctas"] == NUM_SMS
-    assert np.array_equal(got["items"], ref["items"])
-    assert np.array_equal(got["cost_prefix"], ref["cost_prefix"])
-    assert np.array_equal(got["cta_ptr"], ref["cta_ptr"])
+    for k in ("items", "cost_prefix", "cta_ptr", "items_dec", "cost_prefix_dec", "cta_ptr_dec"):
+        assert np.array_equal(got[k], ref[k]), k
 
 
 @pytest.mark.parametrize("name", list(SMALL))
 def test_forward_partials_match_oracle(name, small_runs):
+    """Partials straight out of the forward kernels.  Entries of normal items
+    hold one block each; a decode item holds the merge of its run of blocks
+    at its first entry (checked against the oracle's LSE merge of the run's
+    per-block results) and -inf lse at the others."""
     w = SMALL[name]
     attn = small_runs[name][0]
     G = w.num_q_heads // w.num_kv_heads
     idx = U.read_index(attn)
+    sch = U.read_sched(attn, NUM_SMS)
     o_gpu, l_gpu = U.read_partials(attn)
     o_ref, l_ref = U.oracle_slot_partials(w)
-    slots = np.nonzero(idx["slot_entry"] >= 0)[0]
-    e = idx["slot_entry"][slots]
-    rows_gpu = (e[:, None] * G + np.arange(G)).reshape(-1)
+    # normal entries: one block per partial
+    ents = np.concatenate([np.arange(e0, e0 + n) for _, e0, n, _ in sch["items"]]) if len(sch["items"]) else \
+        np.zeros(0, np.int64)
+    slots = idx["entries"][ents]
+    rows_gpu = (ents[:, None] * G + np.arange(G)).reshape(-1)
     rows_ref = (slots[:, None] * G + np.arange(G)).reshape(-1)
     U.assert_close_out(o_gpu[rows_gpu], o_ref[rows_ref], U.out_tol(w), f"{name} partial o")
     U.assert_close_lse(l_gpu[rows_gpu], l_ref[rows_ref], 2e-3, f"{name} partial lse")
+    # decode items: merged partial at the first entry, -inf elsewhere
+    for a0, e0, _, nk in sch["items_dec"]:
+        keys = idx["active"][a0:a0 + nk]
+        es = idx["row_ptr"][keys]
+        assert es[0] == e0
+        sl = idx["entries"][es]
+        for j in range(G):
+            mo, ml = oracle.combine(o_ref[sl * G + j], l_ref[sl * G + j])
+            U.assert_close_out(o_gpu[e0 * G + j], mo, U.out_tol(w), f"{name} decode partial o")
+            U.assert_close_lse([l_gpu[e0 * G + j]], [ml], 2e-3, f"{name} decode partial lse")
+            assert np.all(l_gpu[es[1:] * G + j] == -np.inf)
 
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -233,10 +248,10 @@ def test_full_size_workload(name):
     assert np.array_equal(got["row_ptr"], ref_idx["row_ptr"])
     assert np.array_equal(got["entries"], ref_idx["entries"])
     assert np.array_equal(got["slot_entry"], ref_idx["slot_entry"])
-    ref_s = oracle.schedule(prob, w.used_kv_lens, ref_idx, U.ITEM_TILES, NUM_SMS)
+    ref_s = U.oracle_schedule(w, NUM_SMS)
     got_s = U.read_sched(attn, NUM_SMS)
-    assert np.array_equal(got_s["items"], ref_s["items"])
-    assert np.array_equal(got_s["cta_ptr"], ref_s["cta_ptr"])
+    for k in ("items", "cost_prefix", "cta_ptr", "items_dec", "cost_prefix_dec", "cta_ptr_dec"):
+        assert np.array_equal(got_s[k], ref_s[k]), k
     # output on sampled rows: every head of ~2048 / (topk * 2) sampled
     # (token, kv head) pairs, always including the first and the last token
     rng = np.random.default_rng(0)

@@ -391,6 +391,13 @@ def test_index_matches_brute_force_scan(causal):
     assert (se >= 0).sum() == len(ent)
 
 
+def test_index_invalid_cu_indexes_nothing():
+    sel = np.zeros((3, 1, 1), np.int32)
+    prob = oracle.problem(2, 3, 1, 1, 1, 64, 4, 4, False)
+    idx = oracle.build_index(prob, sel, np.array([0, 2, 1], np.int64), np.array([200, 200], np.int32))
+    assert idx["flags"] & 128 and len(idx["entries"]) == 0 and np.all(idx["slot_entry"] == -1)
+
+
 def test_index_flags_len_and_causal():
     sel = np.zeros((2, 1, 1), np.int32)
     cu = np.array([0, 2], np.int64)
@@ -403,50 +410,87 @@ def test_index_flags_len_and_causal():
 
 # ------------------------------------------------------------- schedule pins
 def test_schedule_split_worked_example():
-    # one key with 10 entries, G = 32 -> 4 entries per tile, 1 tile per item:
-    # n = ceil(10 / 4) = 3 items with boundaries floor(i*10/3) = 0, 3, 6, 10
+    # one key with 10 entries (a 10-token sequence: normal list), G = 32 ->
+    # 4 entries per tile, 1 tile per item: n = ceil(10 / 4) = 3 items with
+    # boundaries floor(i*10/3) = 0, 3, 6, 10
     sel = np.zeros((10, 1, 1), np.int32)
     cu = np.array([0, 10], np.int64)
     prob = oracle.problem(1, 10, 32, 1, 1, 128, 1, 1, False)
     idx = oracle.build_index(prob, sel, cu, np.array([100], np.int32))
-    sch = oracle.schedule(prob, [100], idx, 1, 2)
+    sch = oracle.schedule(prob, [100], cu, idx, 1, 16, 2)
     assert sch["items"][:, 1].tolist() == [0, 3, 6] and sch["items"][:, 2].tolist() == [3, 3, 4]
     # cost = 100 tokens * 2 + 1 tile * 256 + rows * 2, rows = entries * 32:
     # 200 + 256 + 192 = 648 (3 entries) and 200 + 256 + 256 = 712 (4 entries)
     assert sch["cost_prefix"].tolist() == [0, 648, 1296, 2008]
     # targets floor(c * 2008 / 2) = 0, 1004, 2008 -> items with prefix below them
     assert sch["cta_ptr"].tolist() == [0, 2, 3]
+    assert len(sch["items_dec"]) == 0 and sch["cta_ptr_dec"].tolist() == [0, 0, 0]
 
 
-@pytest.mark.parametrize("name", ["tiny_decode", "shared_prefill_small", "varlen_small"])
+def test_schedule_decode_run_worked_example():
+    # one decode token (Tq = 1), G = 8, selecting 20 of the 25 blocks of a
+    # 3100-token sequence: one run of 20 keys -> ceil(20 / 16) = 2 items of
+    # run positions [0, 10) and [10, 20); the last block (24) holds 3100 - 3072
+    # = 28 tokens.  cost = sum valid * 2 + 10 * 64 + 256
+    blocks = np.array([24, 0, 3, 5, 7, 9, 11, 13, 15, 17, 19, 21, 23, 1, 2, 4, 6, 8, 10, 12], np.int32)
+    sel = blocks.reshape(1, 1, 20)
+    cu = np.array([0, 1], np.int64)
+    prob = oracle.problem(1, 1, 8, 1, 20, 64, 49, 49, False)
+    idx = oracle.build_index(prob, sel, cu, np.array([3100], np.int32))
+    sch = oracle.schedule(prob, [3100], cu, idx, 4, 16, 3)
+    assert len(sch["items"]) == 0
+    d = sch["items_dec"]
+    assert d[:, 0].tolist() == [0, 10] and d[:, 3].tolist() == [10, 10] and d[:, 2].tolist() == [1, 1]
+    # entries follow key order (block order): the first key of item 1 is the
+    # 11th smallest selected block
+    assert d[:, 1].tolist() == [0, 10]
+    first = 10 * 128 * 2 + 10 * 64 + 256
+    second = (9 * 128 + 28) * 2 + 10 * 64 + 256
+    assert sch["cost_prefix_dec"].tolist() == [0, first, first + second]
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "shared_prefill_small", "varlen_small", "skewed_small"])
 def test_schedule_invariants(name):
     if name == "shared_prefill_small":
         w = W.custom(name, [256], [2048], 16, 1, 128, 8, True, "zipf_diag", 3)
     elif name == "varlen_small":
-        w = W.custom(name, [1, 8, 64, 3], [3000, 900, 2000, 5000], 32, 4, 128, 6, True, "uniform_drop10", 4)
+        w = W.custom(name, [1, 8, 64, 3, 1], [3000, 900, 2000, 5000, 700], 32, 4, 128, 6, True, "uniform_drop10", 4)
+    elif name == "skewed_small":
+        w = W.custom(name, [1] * 16, [200, 700, 1500, 9000] * 4, 64, 8, 64, 64, False, "hot_groups", 104)
     else:
         w = W.workload(name)
     prob = oracle.problem_for(w)
     idx = oracle.build_index(prob, w.selected, w.cu_seqlens_q, w.used_kv_lens)
     G = w.num_q_heads // w.num_kv_heads
-    for R in (1, 4):
+    rp = idx["row_ptr"]
+    active = np.nonzero(np.diff(rp))[0]
+    tq = np.diff(w.cu_seqlens_q)
+    for R, D in ((1, 16), (4, 8)):
         for P in (1, 7, 152):
-            sch = oracle.schedule(prob, w.used_kv_lens, idx, R, P)
-            items = sch["items"]
-            # every entry covered exactly once, in order, each item inside one key
+            sch = oracle.schedule(prob, w.used_kv_lens, w.cu_seqlens_q, idx, R, D, P)
             covered = []
-            for key, e0, n, _ in items:
-                assert idx["row_ptr"][key] <= e0 and e0 + n <= idx["row_ptr"][key + 1]
+            for key, e0, n, _ in sch["items"]:
+                assert rp[key] <= e0 and e0 + n <= rp[key + 1]
                 assert 1 <= n <= R * max(1, 128 // G)
                 covered.extend(range(e0, e0 + n))
-            assert covered == list(range(len(idx["entries"])))
-            cp = sch["cta_ptr"]
-            assert cp[0] == 0 and cp[-1] == len(items) and np.all(np.diff(cp) >= 0)
-            cost = np.diff(sch["cost_prefix"])
-            C = sch["cost_prefix"][-1]
-            for c in range(P):
-                assert cost[cp[c]:cp[c + 1]].sum() <= C / P + cost.max() + 1
-            sch2 = oracle.schedule(prob, w.used_kv_lens, idx, R, P)
+            for a0, e, one, nk in sch["items_dec"]:
+                assert one == 1 and 1 <= nk <= D and e == rp[active[a0]]
+                keys = active[a0:a0 + nk]
+                assert np.all(np.diff(rp)[keys] == 1)  # one entry per decode key
+                covered.extend(rp[keys].tolist())
+                # a decode item stays within one (kv head, sequence): same token for all its keys
+                toks = {int(idx["entries"][rp[k]]) // (w.num_kv_heads * w.topk) for k in keys}
+                assert len(toks) == 1 and tq[np.searchsorted(w.cu_seqlens_q, toks.pop(), side="right") - 1] == 1
+            assert sorted(covered) == list(range(len(idx["entries"])))
+            for it, cp, cost in (("items", "cta_ptr", "cost_prefix"), ("items_dec", "cta_ptr_dec", "cost_prefix_dec")):
+                c = sch[cp]
+                assert c[0] == 0 and c[-1] == len(sch[it]) and np.all(np.diff(c) >= 0)
+                if len(sch[it]):
+                    costs = np.diff(sch[cost])
+                    C = sch[cost][-1]
+                    for k in range(P):
+                        assert costs[c[k]:c[k + 1]].sum() <= C / P + costs.max() + 1
+            sch2 = oracle.schedule(prob, w.used_kv_lens, w.cu_seqlens_q, idx, R, D, P)
             assert all(np.array_equal(sch[k], sch2[k]) for k in sch)
 
 
