@@ -60,14 +60,14 @@ class Problem(ctypes.Structure):
 class IndexLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("header", "seq_info", "token_seq", "slot_entry", "bitmap", "kmap",
                                                "counts", "row_ptr", "entries", "active_keys", "active_valid",
-                                               "lookback", "total")] + \
+                                               "row_nnz", "cta_sums", "total")] + \
                [(n, ctypes.c_int64) for n in ("keys_cap", "nslots", "bitmap_words_cap", "kmap_bytes_cap",
                                               "tiles_cap")]
 
 
 class SchedLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("header", "items", "cost_prefix", "cta_ptr", "items_dec",
-                                               "cost_prefix_dec", "cta_ptr_dec", "lookback", "total")] + \
+                                               "cost_prefix_dec", "cta_ptr_dec", "cta_sums", "total")] + \
                [(n, ctypes.c_int64) for n in ("items_cap", "tiles_cap")]
 
 

@@ -75,7 +75,8 @@ mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L) {
   L->entries = o;      o = align_up(o + (size_t)L->nslots * 4);
   L->active_keys = o;  o = align_up(o + (size_t)act * 4);
   L->active_valid = o; o = align_up(o + (size_t)act * 4);
-  L->lookback = o;     o = align_up(o + (size_t)L->tiles_cap * 8);
+  L->row_nnz = o;      o = align_up(o + (size_t)Tq * Hkv * 4);
+  L->cta_sums = o;     o = align_up(o + (size_t)kMaxCoopCtas * 8);
   L->total = o;
   return MXSA_OK;
 }
@@ -96,7 +97,7 @@ mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L) {
   L->items_dec = o;       o = align_up(o + (size_t)L->items_cap * 16);
   L->cost_prefix_dec = o; o = align_up(o + (size_t)(L->items_cap + 1) * 8);
   L->cta_ptr_dec = o;     o = align_up(o + (size_t)(MXSA_MAX_CTAS + 1) * 4);
-  L->lookback = o;        o = align_up(o + (size_t)(L->tiles_cap > 0 ? L->tiles_cap : 1) * 16);
+  L->cta_sums = o;        o = align_up(o + (size_t)kMaxCoopCtas * 16);
   L->total = o;
   return MXSA_OK;
 }
@@ -126,7 +127,8 @@ IndexPtrs index_ptrs(const mxsa_problem& p, void* ws) {
   x.entries = reinterpret_cast<int32_t*>(b + L.entries);
   x.active = reinterpret_cast<int32_t*>(b + L.active_keys);
   x.active_valid = reinterpret_cast<int32_t*>(b + L.active_valid);
-  x.lookback = reinterpret_cast<unsigned long long*>(b + L.lookback);
+  x.row_nnz = reinterpret_cast<int32_t*>(b + L.row_nnz);
+  x.cta_sums = reinterpret_cast<unsigned long long*>(b + L.cta_sums);
   return x;
 }
 
@@ -142,7 +144,7 @@ SchedPtrs sched_ptrs(const mxsa_problem& p, void* ws) {
   x.items_dec = reinterpret_cast<int4*>(b + L.items_dec);
   x.cost_prefix_dec = reinterpret_cast<long long*>(b + L.cost_prefix_dec);
   x.cta_ptr_dec = reinterpret_cast<int32_t*>(b + L.cta_ptr_dec);
-  x.lookback = reinterpret_cast<unsigned long long*>(b + L.lookback);
+  x.cta_sums = reinterpret_cast<unsigned long long*>(b + L.cta_sums);
   return x;
 }
 

@@ -8,14 +8,21 @@
 // never depends on atomics: each (key, token) pair owns one bit of a per-key
 // token bitmap, and the emission walks the set bits in order.
 //
-//   k_seq    (1 CTA)  per-sequence scan: L, nblk, block / bitmap / kmap offsets
-//   k_zero   (grid)   clears counters, bitmap and scan state; token -> sequence
-//   k_mark   (grid)   one warp per (token, kv head) row: validate, dedupe,
-//                     set the token's bit in each selected key row, record k
-//   k_scan   (grid)   decoupled look-back scan of per-key counts: row_ptr and
-//                     the compacted list of keys with entries
-//   k_emit   (grid)   each active key enumerates its bitmap row in order and
-//                     writes entries[] and the inverse map slot_entry[]
+// One cooperative launch (all CTAs resident) runs five phases separated by a
+// bounded grid barrier:
+//   seq    CTA 0: per-sequence scan (L, nblk, block / bitmap / kmap offsets);
+//          every CTA: token -> sequence map
+//   zero   clears counters, bitmap and scan state
+//   mark   one warp per (token, kv head) row: validate, dedupe, set the
+//          token's bit in each selected key row, record k
+//   reduce the keys are cut into one contiguous chunk per CTA; each CTA
+//          sums the entry counts of its chunk
+//   scan   each CTA adds the sums of the chunks before it, scans its chunk
+//          (row_ptr, the compacted list of keys with entries) and walks the
+//          bitmap rows of its keys in order, writing entries[] and the
+//          inverse map slot_entry[]
+#include <mutex>
+
 #include "internal.h"
 
 namespace mxsa {
@@ -55,9 +62,8 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* tmp, T* total) {
   return r;
 }
 
-__global__ void __launch_bounds__(1024) k_seq(IndexPtrs ix, const int64_t* cu, const int32_t* lens, int B,
-                                              int total_q, int Hkv, int cap_len, int causal) {
-  __shared__ long long tmp[33];
+__device__ void phase_seq(const IndexPtrs& ix, const int64_t* cu, const int32_t* lens, int B, int total_q, int Hkv,
+                          int cap_len, int causal, long long* tmp) {
   __shared__ int cu_bad;
   long long carry_blk = 0, carry_bm = 0, carry_km = 0;
   int flags = 0;
@@ -116,7 +122,7 @@ __global__ void __launch_bounds__(1024) k_seq(IndexPtrs ix, const int64_t* cu, c
   if ((threadIdx.x & 31) == 0 && f) atomicOr(&fl, f);
   __syncthreads();
   if (threadIdx.x == 0) {
-    ix.hdr[kHdrFlags] = fl;
+    if (fl) atomicOr(&ix.hdr[kHdrFlags], fl);
     ix.hdr[kHdrNB] = (int)carry_blk;
     ix.hdr[kHdrNnz] = 0;
     ix.hdr[kHdrActive] = 0;
@@ -128,15 +134,18 @@ __global__ void __launch_bounds__(1024) k_seq(IndexPtrs ix, const int64_t* cu, c
   }
 }
 
-__global__ void k_zero(IndexPtrs ix, const int64_t* cu, int B, int total_q, int Hkv) {
+__device__ void phase_zero(const IndexPtrs& ix, int Hkv) {
   const long long n_keys = ix.hdr[kHdrKeys];
   const long long n_bm = (long long)ix.hdr[kHdrBMW] * Hkv;
-  const long long n_tiles = (n_keys + kScanTile - 1) / kScanTile;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   for (long long i = tid; i < n_keys; i += stride) ix.counts[i] = 0;
   for (long long i = tid; i < n_bm; i += stride) ix.bitmap[i] = 0u;
-  for (long long i = tid; i < n_tiles; i += stride) ix.lookback[i] = 0ull;
+}
+
+__device__ void phase_token_seq(const IndexPtrs& ix, const int64_t* cu, int B, int total_q) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   for (long long t = tid; t < total_q; t += stride) {
     // last s with cu[s] <= t (sequences of zero tokens are skipped naturally)
     int lo = 0, hi = B - 1;
@@ -151,14 +160,13 @@ __global__ void k_zero(IndexPtrs ix, const int64_t* cu, int B, int total_q, int 
 
 constexpr int kMarkWarps = 8;
 
-__global__ void __launch_bounds__(kMarkWarps * 32) k_mark(IndexPtrs ix, const int32_t* sel, int total_q, int Hkv,
-                                                         int topk, int causal) {
-  __shared__ int32_t rowbuf[kMarkWarps][256];
+__device__ void phase_mark(const IndexPtrs& ix, const int32_t* sel, int total_q, int Hkv, int topk, int causal,
+                           int32_t (*rowbuf)[256]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int NB = ix.hdr[kHdrNB];
   const size_t BMW = (size_t)ix.hdr[kHdrBMW], KMW = (size_t)ix.hdr[kHdrKMW];
   const long long n_rows = (long long)total_q * Hkv;
-  int flags = 0;
+  int flags = 0, made = 0;
   for (long long row = (long long)blockIdx.x * kMarkWarps + w; row < n_rows; row += (long long)gridDim.x * kMarkWarps) {
     const int t = (int)(row / Hkv), g = (int)(row % Hkv);
     const int32_t* srow = sel + row * topk;
@@ -189,52 +197,15 @@ __global__ void __launch_bounds__(kMarkWarps * 32) k_mark(IndexPtrs ix, const in
       atomicOr(&ix.bitmap[word], 1u << (i & 31));
       ix.kmap[(size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq + i] = (uint8_t)k;
       atomicAdd(&ix.counts[(long long)g * NB + si.blk_off + b], 1);
+      ++made;
     }
+    made = __reduce_add_sync(0xffffffffu, made);
+    if (lane == 0) ix.row_nnz[row] = made;
+    made = 0;
     __syncwarp();
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && flags) atomicOr(&ix.hdr[kHdrFlags], flags);
-}
-
-// Look-back scan over keys; payload = (entry count << 31) | active count.
-__global__ void __launch_bounds__(kScanThreads) k_scan(IndexPtrs ix) {
-  __shared__ int tile_s;
-  __shared__ unsigned long long tmp[33];
-  __shared__ unsigned long long excl_s;
-  const int n_keys = ix.hdr[kHdrKeys];
-  const int n_tiles = (n_keys + kScanTile - 1) / kScanTile;
-  if (threadIdx.x == 0) tile_s = atomicAdd(&ix.hdr[kHdrTileCtr], 1);
-  __syncthreads();
-  const int tile = tile_s;
-  if (tile >= n_tiles) return;
-  const long long k0 = (long long)tile * kScanTile + threadIdx.x * kScanPerThread;
-  int c[kScanPerThread];
-  unsigned long long local = 0;
-#pragma unroll
-  for (int j = 0; j < kScanPerThread; ++j) {
-    c[j] = (k0 + j < n_keys) ? ix.counts[k0 + j] : 0;
-    local += ((unsigned long long)c[j] << 31) | (c[j] > 0 ? 1ull : 0ull);
-  }
-  unsigned long long tot;
-  unsigned long long ex = block_exclusive_scan(local, tmp, &tot);
-  if (threadIdx.x == 0) excl_s = lookback_exclusive(ix.lookback, tile, tot, &ix.hdr[kHdrFlags]);
-  __syncthreads();
-  unsigned long long run = excl_s + ex;
-  const unsigned long long kLow = (1ull << 31) - 1;
-#pragma unroll
-  for (int j = 0; j < kScanPerThread; ++j) {
-    if (k0 + j < n_keys) {
-      ix.row_ptr[k0 + j] = (int)(run >> 31);
-      if (c[j] > 0) ix.active[run & kLow] = (int)(k0 + j);
-    }
-    run += ((unsigned long long)c[j] << 31) | (c[j] > 0 ? 1ull : 0ull);
-  }
-  if (tile == n_tiles - 1 && threadIdx.x == kScanThreads - 1) {
-    const unsigned long long all = excl_s + tot;
-    ix.row_ptr[n_keys] = (int)(all >> 31);
-    ix.hdr[kHdrNnz] = (int)(all >> 31);
-    ix.hdr[kHdrActive] = (int)(all & kLow);
-  }
 }
 
 __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
@@ -245,6 +216,36 @@ __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
     else hi = mid - 1;
   }
   return lo;
+}
+
+template <typename T>
+__device__ __forceinline__ T block_sum(T v, T* tmp) {
+  T total;
+  block_exclusive_scan(v, tmp, &total);
+  return total;
+}
+
+// Keys are cut into gridDim.x contiguous chunks; CTA c owns chunk c.
+__device__ __forceinline__ void key_chunk(int n_keys, int* lo, int* hi) {
+  const long long chunk = ((long long)n_keys + gridDim.x - 1) / gridDim.x;
+  const long long a = (long long)blockIdx.x * chunk, b = a + chunk;
+  *lo = (int)(a < n_keys ? a : n_keys);
+  *hi = (int)(b < n_keys ? b : n_keys);
+}
+
+// payload of one key in the scans: (entries << 31) | (key has entries)
+__device__ __forceinline__ unsigned long long key_payload(int c) {
+  return ((unsigned long long)c << 31) | (c > 0 ? 1ull : 0ull);
+}
+
+// reduce: per-CTA sum of the payloads of its chunk
+__device__ void phase_key_reduce(const IndexPtrs& ix, unsigned long long* tmp) {
+  int lo, hi;
+  key_chunk(ix.hdr[kHdrKeys], &lo, &hi);
+  unsigned long long v = 0;
+  for (int k = lo + threadIdx.x; k < hi; k += blockDim.x) v += key_payload(ix.counts[k]);
+  v = block_sum(v, tmp);
+  if (threadIdx.x == 0) ix.cta_sums[blockIdx.x] = v;
 }
 
 // Writes the entries of one bitmap row: `n_words` words starting at `bm`,
@@ -268,94 +269,188 @@ __device__ __forceinline__ void emit_row_serial(const IndexPtrs& ix, const uint3
   }
 }
 
-__global__ void __launch_bounds__(256) k_emit(IndexPtrs ix, int B, int Hkv, int topk) {
+// One warp writes the entries of a long bitmap row, 32 words at a time
+// with a prefix over the words' popcounts.
+__device__ __forceinline__ void emit_row_warp(const IndexPtrs& ix, const uint32_t* bm, int n_words,
+                                              const uint8_t* km, int q_begin, int g, int Hkv, int topk, int base) {
   const int lane = threadIdx.x & 31;
-  const int n_active = ix.hdr[kHdrActive];
+  int run = base;
+  for (int w0 = 0; w0 < n_words; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t bits = w < n_words ? bm[w] : 0u;
+    const int cnt = __popc(bits);
+    const int inc = warp_inclusive_scan(cnt);
+    int j = run + inc - cnt;
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const int i = w * 32 + bit;
+      const int k = km[i];
+      const int slot = ((q_begin + i) * Hkv + g) * topk + k;
+      ix.entries[j] = slot;
+      ix.slot_entry[slot] = j;
+      ++j;
+    }
+    run += __shfl_sync(0xffffffffu, inc, 31);
+  }
+}
+
+// scan + emit: each CTA adds the sums of the chunks before its own, scans
+// its chunk in tiles (row_ptr, the list of keys with entries and their valid
+// token counts) and writes the entries of its keys: rows of at most two
+// bitmap words one lane per key, longer rows one warp per key.
+__device__ void phase_key_scan_emit(const IndexPtrs& ix, int B, int Hkv, int topk, unsigned long long* tmp) {
+  __shared__ int long_key[kScanTile];
+  __shared__ int long_base[kScanTile];
+  __shared__ int n_long;
+  const int n_keys = ix.hdr[kHdrKeys];
   const int NB = ix.hdr[kHdrNB];
   const size_t BMW = (size_t)ix.hdr[kHdrBMW], KMW = (size_t)ix.hdr[kHdrKMW];
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  for (int grp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); grp * 32 < n_active; grp += warps_total) {
-    const int a = grp * 32 + lane;
-    bool have = a < n_active;
-    int key = 0, g = 0, s = 0, b = 0, words = 0, base = 0;
-    SeqInfo si{};
-    if (have) {
-      key = ix.active[a];
-      g = key / NB;
-      const int r = key - g * NB;
-      s = seq_of_block(ix.seq, B, r);
-      si = ix.seq[s];
-      b = r - si.blk_off;
-      words = si.words;
-      base = ix.row_ptr[key];
-      const int valid = si.L - 128 * b;
-      ix.active_valid[a] = valid < 128 ? valid : 128;
-    }
-    const uint32_t* bm = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * words;
-    const uint8_t* km = ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq;
-    // short rows (<= 2 words): one lane per key
-    const bool is_long = have && words > 2;
-    if (have && !is_long) emit_row_serial(ix, bm, words, km, si.q_begin, g, Hkv, topk, base);
-    // long rows: the warp walks 32 words at a time with a prefix over popcounts
-    unsigned long_mask = __ballot_sync(0xffffffffu, is_long);
-    while (long_mask) {
-      const int src = __ffs(long_mask) - 1;
-      long_mask &= long_mask - 1;
-      const int L_words = __shfl_sync(0xffffffffu, words, src);
-      const int L_base = __shfl_sync(0xffffffffu, base, src);
-      const int L_g = __shfl_sync(0xffffffffu, g, src);
-      const int L_q0 = __shfl_sync(0xffffffffu, si.q_begin, src);
-      const unsigned long long bm_addr = __shfl_sync(0xffffffffu, (unsigned long long)bm, src);
-      const unsigned long long km_addr = __shfl_sync(0xffffffffu, (unsigned long long)km, src);
-      const uint32_t* lbm = reinterpret_cast<const uint32_t*>(bm_addr);
-      const uint8_t* lkm = reinterpret_cast<const uint8_t*>(km_addr);
-      int run = L_base;
-      for (int w0 = 0; w0 < L_words; w0 += 32) {
-        const int w = w0 + lane;
-        uint32_t bits = w < L_words ? lbm[w] : 0u;
-        const int cnt = __popc(bits);
-        const int inc = warp_inclusive_scan(cnt);
-        int j = run + inc - cnt;
-        while (bits) {
-          const int bit = __ffs(bits) - 1;
-          bits &= bits - 1;
-          const int i = w * 32 + bit;
-          const int k = lkm[i];
-          const int slot = ((L_q0 + i) * Hkv + L_g) * topk + k;
-          ix.entries[j] = slot;
-          ix.slot_entry[slot] = j;
-          ++j;
-        }
-        run += __shfl_sync(0xffffffffu, inc, 31);
-      }
-    }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  unsigned long long pre = 0, all = 0;
+  for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+    const unsigned long long v = ix.cta_sums[c];
+    all += v;
+    if (c < (int)blockIdx.x) pre += v;
   }
+  pre = block_sum(pre, tmp);
+  all = block_sum(all, tmp);
+  const unsigned long long kLow = (1ull << 31) - 1;
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    ix.row_ptr[n_keys] = (int)(all >> 31);
+    ix.hdr[kHdrNnz] = (int)(all >> 31);
+    ix.hdr[kHdrActive] = (int)(all & kLow);
+  }
+  int lo, hi;
+  key_chunk(n_keys, &lo, &hi);
+  unsigned long long carry = pre;
+  for (int t0 = lo; t0 < hi; t0 += kScanTile) {
+    const int k0 = t0 + threadIdx.x * kScanPerThread;
+    int c[kScanPerThread];
+    unsigned long long local = 0;
+#pragma unroll
+    for (int j = 0; j < kScanPerThread; ++j) {
+      c[j] = (k0 + j < hi) ? ix.counts[k0 + j] : 0;
+      local += key_payload(c[j]);
+    }
+    if (threadIdx.x == 0) n_long = 0;
+    unsigned long long tot;
+    unsigned long long run = carry + block_exclusive_scan(local, tmp, &tot);
+#pragma unroll
+    for (int j = 0; j < kScanPerThread; ++j) {
+      const int key = k0 + j;
+      if (key < hi) {
+        const int base = (int)(run >> 31);
+        ix.row_ptr[key] = base;
+        if (c[j] > 0) {
+          const int pos = (int)(run & kLow);
+          ix.active[pos] = key;
+          const int g = key / NB, r = key - g * NB;
+          const SeqInfo si = ix.seq[seq_of_block(ix.seq, B, r)];
+          const int b = r - si.blk_off;
+          const int valid = si.L - 128 * b;
+          ix.active_valid[pos] = valid < 128 ? valid : 128;
+          if (si.words <= 2) {
+            emit_row_serial(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
+                            ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv,
+                            topk, base);
+          } else {
+            const int at = atomicAdd(&n_long, 1);
+            long_key[at] = key;
+            long_base[at] = base;
+          }
+        }
+      }
+      run += key_payload(c[j]);
+    }
+    __syncthreads();
+    for (int i = warp; i < n_long; i += n_warps) {
+      const int key = long_key[i];
+      const int g = key / NB, r = key - g * NB;
+      const SeqInfo si = ix.seq[seq_of_block(ix.seq, B, r)];
+      const int b = r - si.blk_off;
+      emit_row_warp(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
+                    ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv, topk,
+                    long_base[i]);
+    }
+    (void)lane;
+    __syncthreads();
+    carry += tot;
+  }
+}
+
+struct IndexArgs {
+  IndexPtrs ix;
+  const int32_t* sel;
+  const int64_t* cu;
+  const int32_t* lens;
+  int B, total_q, Hkv, topk, cap_len, causal;
+};
+
+constexpr int kIndexThreads = 256;
+static_assert(kIndexThreads == kScanThreads && kIndexThreads == kMarkWarps * 32, "phase block sizes");
+
+__global__ void __launch_bounds__(kIndexThreads) k_index(IndexArgs a) {
+  __shared__ unsigned long long tmp[33];
+  __shared__ int32_t rowbuf[kMarkWarps][256];
+  int* bar = a.ix.hdr + kHdrBarCount;
+  int* flags = a.ix.hdr + kHdrFlags;
+  const unsigned nb = gridDim.x;
+  if (blockIdx.x == 0)
+    phase_seq(a.ix, a.cu, a.lens, a.B, a.total_q, a.Hkv, a.cap_len, a.causal, reinterpret_cast<long long*>(tmp));
+  phase_token_seq(a.ix, a.cu, a.B, a.total_q);
+  grid_barrier(bar, flags, nb);
+  phase_zero(a.ix, a.Hkv);
+  grid_barrier(bar, flags, nb);
+  phase_mark(a.ix, a.sel, a.total_q, a.Hkv, a.topk, a.causal, rowbuf);
+  grid_barrier(bar, flags, nb);
+  phase_key_reduce(a.ix, tmp);
+  grid_barrier(bar, flags, nb);
+  phase_key_scan_emit(a.ix, a.B, a.Hkv, a.topk, tmp);
 }
 
 }  // namespace
 
+// CTAs of a cooperative launch: at most 2 per SM (all must be resident at
+// once); 0 when the device cannot launch cooperatively.  Cached per device.
+int coop_grid(const void* kernel, int threads) {
+  constexpr int kMaxDev = 64, kMaxKernels = 4;
+  static std::mutex mu;
+  static const void* keys[kMaxDev][kMaxKernels] = {};
+  static int vals[kMaxDev][kMaxKernels] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < kMaxKernels; ++i)
+    if (keys[dev][i] == kernel) return vals[dev][i];
+  int sms = 0, per_sm = 0, coop = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess) per_sm = 0;
+  int g = (coop && sms > 0 && per_sm > 0) ? sms * (per_sm < 2 ? per_sm : 2) : 0;
+  if (g > kMaxCoopCtas) g = kMaxCoopCtas;
+  for (int i = 0; i < kMaxKernels; ++i)
+    if (!keys[dev][i]) {
+      keys[dev][i] = kernel;
+      vals[dev][i] = g;
+      break;
+    }
+  return g;
+}
+
 cudaError_t launch_build_index(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
                                const IndexPtrs& ix, const mxsa_index_layout& lay, cudaStream_t st) {
-  const int cap_len = p.max_pages_per_seq * p.page_size;
-  k_seq<<<1, 1024, 0, st>>>(ix, cu, lens, p.num_seqs, p.total_q, p.num_kv_heads, cap_len, p.causal);
-  int sms = 148;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  k_zero<<<sms * 4, 256, 0, st>>>(ix, cu, p.num_seqs, p.total_q, p.num_kv_heads);
-  const long long rows = (long long)p.total_q * p.num_kv_heads;
-  if (rows > 0) {
-    long long g = (rows + kMarkWarps - 1) / kMarkWarps;
-    if (g > sms * 16) g = sms * 16;
-    k_mark<<<(int)g, kMarkWarps * 32, 0, st>>>(ix, sel, p.total_q, p.num_kv_heads, p.topk, p.causal);
-  }
-  if (lay.tiles_cap > 0) k_scan<<<(unsigned)lay.tiles_cap, kScanThreads, 0, st>>>(ix);
-  long long groups = (std::min<long long>(lay.keys_cap, lay.nslots) + 31) / 32;
-  long long eg = (groups + 7) / 8;
-  if (eg > sms * 8) eg = sms * 8;
-  if (eg < 1) eg = 1;
-  k_emit<<<(int)eg, 256, 0, st>>>(ix, p.num_seqs, p.num_kv_heads, p.topk);
-  return cudaGetLastError();
+  (void)lay;
+  IndexArgs a{ix, sel, cu, lens, p.num_seqs, p.total_q, p.num_kv_heads, p.topk,
+              p.max_pages_per_seq * p.page_size, p.causal};
+  const int grid = coop_grid(reinterpret_cast<const void*>(k_index), kIndexThreads);
+  if (grid <= 0) return cudaErrorNotSupported;
+  // header words: flags, sizes, counters and the grid barrier start at zero
+  cudaError_t e = cudaMemsetAsync(ix.hdr, 0, kHdrInts * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&a};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_index), dim3(grid), dim3(kIndexThreads), args,
+                                     0, st);
 }
 
 }  // namespace mxsa

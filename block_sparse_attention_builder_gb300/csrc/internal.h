@@ -20,6 +20,9 @@ enum : int {
   kHdrBMW = 5,       // bitmap words per kv head
   kHdrKMW = 6,       // kmap bytes per kv head
   kHdrTileCtr = 7,   // dynamic tile counter of the key scan
+  kHdrBarCount = 8,  // grid barrier: arrivals (cleared before each launch)
+  kHdrAbort = 9,     // grid barrier: set when a barrier wait gave up
+  kHdrBarGen = 10,   // grid barrier: generation
   kHdrInts = 16
 };
 
@@ -33,6 +36,9 @@ enum : int {
   kSchDecItems = 5,  // merged decode items
   kSchDecCostLo = 6,
   kSchDecCostHi = 7,
+  kSchBarCount = 8,  // grid barrier (as in the index header)
+  kSchAbort = 9,
+  kSchBarGen = 10,
   kSchInts = 16
 };
 
@@ -66,8 +72,12 @@ struct IndexPtrs {
   int32_t* entries;
   int32_t* active;
   int32_t* active_valid;
-  unsigned long long* lookback;
+  int32_t* row_nnz;                // entries made per (token, kv head) row
+  unsigned long long* cta_sums;    // per-CTA sums of the cooperative scans
 };
+
+// CTAs of the cooperative launches (index, schedule) never exceed this
+constexpr int kMaxCoopCtas = 1024;
 
 struct SchedPtrs {
   int32_t* hdr;
@@ -77,7 +87,7 @@ struct SchedPtrs {
   int4* items_dec;          // decode items {active_pos, entry, 1, n_keys}
   long long* cost_prefix_dec;
   int32_t* cta_ptr_dec;
-  unsigned long long* lookback;  // 2 words per tile: normal, decode
+  unsigned long long* cta_sums;  // 2 words per CTA: normal, decode
 };
 
 constexpr int kScanThreads = 256;
@@ -126,40 +136,38 @@ __device__ __forceinline__ unsigned long long dev_globaltimer() {
   return t;
 }
 
-// Decoupled look-back (single-pass chained scan) over 62-bit payloads:
-// bits 63..62 = status (0 none, 1 tile aggregate, 2 inclusive prefix).
-// Called by one thread per tile; returns the exclusive prefix of `tile`.
-// Payload addition must not carry across the packed fields (callers keep
-// every field below its capacity).  A wait beyond the limit sets
-// MXSA_FLAG_TIMEOUT and returns what was accumulated so far.
-__device__ __forceinline__ unsigned long long lookback_exclusive(unsigned long long* state, int tile,
-                                                                 unsigned long long aggregate, int* flags) {
-  constexpr unsigned long long kAgg = 1ull << 62, kInc = 2ull << 62, kMask = (1ull << 62) - 1;
-  if (tile == 0) {
-    st_release_u64(&state[0], kInc | aggregate);
-    return 0;
-  }
-  st_release_u64(&state[tile], kAgg | aggregate);
-  unsigned long long excl = 0;
-  int j = tile - 1;
-  const unsigned long long t0 = dev_globaltimer();
-  while (j >= 0) {
-    unsigned long long v = ld_acquire_u64(&state[j]);
-    unsigned long long st = v >> 62;
-    if (st == 0) {
-      if (dev_globaltimer() - t0 > kWaitLimitNs) {
-        atomicOr(flags, MXSA_FLAG_TIMEOUT);
-        break;
+// Grid-wide barrier for kernels launched cooperatively (all CTAs
+// co-resident).  bar[0] counts arrivals and must be 0 at launch, bar[1] is
+// the abort word (0 at launch), bar[2] the generation.  The wait is bounded:
+// past the limit it sets MXSA_FLAG_TIMEOUT and the abort word, and every
+// later barrier of the launch returns at once.
+__device__ __forceinline__ void grid_barrier(int* bar, int* flags, unsigned nblocks) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* vgen = bar + 2;
+    volatile int* vabort = bar + 1;
+    const int g = *vgen;
+    __threadfence();
+    const int arrived = atomicAdd(bar, 1) + 1;
+    if (arrived == (int)nblocks) {
+      atomicExch(bar, 0);
+      __threadfence();
+      atomicAdd(bar + 2, 1);
+    } else {
+      const unsigned long long t0 = dev_globaltimer();
+      while (*vgen == g && !*vabort) {
+        if (dev_globaltimer() - t0 > kWaitLimitNs) {
+          atomicOr(flags, MXSA_FLAG_TIMEOUT);
+          atomicExch(bar + 1, 1);
+          break;
+        }
       }
-      continue;
     }
-    excl += v & kMask;
-    if (st == 2) break;
-    --j;
+    __threadfence();
   }
-  st_release_u64(&state[tile], kInc | (excl + aggregate));
-  return excl;
+  __syncthreads();
 }
+
 #endif
 
 }  // namespace mxsa

@@ -19,10 +19,17 @@
 // lies in [target_c, target_{c+1}), so no CTA exceeds C / num_ctas by more
 // than one item.
 //
-//   k_sched_init   clears the look-back state
-//   k_sched_scan   look-back scans over active keys (one per list), then
-//                  writes the items and their cost prefixes
-//   k_partition    one thread per CTA boundary and list: binary search
+// Every per-key and per-item quantity has a closed form (item sizes take
+// two values, q = cnt / n and q + 1, and the first i items hold
+// floor(i * cnt / n) entries), so the work per key and per item is O(1).
+// One cooperative launch, two phases separated by a bounded grid barrier:
+//   reduce  the active keys are cut into one contiguous chunk per CTA; each
+//           CTA sums the item counts and costs of its chunk (both lists)
+//   scan    each CTA adds the sums of the chunks before it, scans its chunk
+//           in tiles and writes the tile's items in parallel; an item with
+//           exclusive prefix p and cost w sets cta_ptr[c] = item + 1 for
+//           every boundary c whose target lies in (p, p + w], which is the
+//           partition rule above without a search
 #include <algorithm>
 
 #include "internal.h"
@@ -32,6 +39,9 @@ namespace mxsa {
 namespace {
 
 constexpr int kItemBits = 26;  // payload: (cost << 26) | items
+constexpr int kSchThreads = 256;
+constexpr int kSchPerThread = 2;
+constexpr int kSchTile = kSchThreads * kSchPerThread;
 
 __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v) {
   const int lane = threadIdx.x & 31;
@@ -62,17 +72,6 @@ __device__ __forceinline__ unsigned long long block_excl_u64(unsigned long long 
   return r;
 }
 
-struct KeyWork {
-  int key, begin, cnt, n_items;  // normal key; n_items = 0 when not emitting
-  long long cost;
-  int dec_len, dec_items;        // decode run start: run length and items
-  long long dec_cost;
-};
-
-__device__ __forceinline__ long long item_cost(int ne, int valid, int kvw, int per_tile, int G) {
-  return (long long)valid * kvw + (long long)((ne + per_tile - 1) / per_tile) * 256 + (long long)ne * G * 2;
-}
-
 __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
@@ -83,178 +82,281 @@ __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
   return lo;
 }
 
-// decode run of `len` keys starting at active position a: cost of its
-// chunk [k0, k1)
-__device__ __forceinline__ long long dec_chunk_cost(const IndexPtrs& ix, int a, int k0, int k1, int kvw) {
-  long long c = (long long)(k1 - k0) * 64 + 256;
-  for (int k = k0; k < k1; ++k) c += (long long)ix.active_valid[a + k] * kvw;
-  return c;
+struct Params {
+  int B, Hkv, G, kvw, per_tile, E, num_ctas;
+};
+
+// What one active key contributes.  kind 0: nothing (inside a decode run),
+// 1: a normal key, 2: the first key of a decode run.
+struct KeyWork {
+  int kind;
+  int a;      // active position
+  int key;    // normal: key id
+  int begin;  // normal: first entry
+  int cnt;    // normal: entries; decode: run length (keys)
+  int valid;  // normal: valid tokens of the block
+  int adj;    // decode: cost removed from the run's last item (partial last block)
+  int n;      // items
+  long long cost;
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// exclusive cost prefix of item i within a normal key, and item i's cost
+__device__ __forceinline__ void normal_item(const KeyWork& k, const Params& P, int i, int* e0, int* ne,
+                                            long long* pre, long long* cost) {
+  const int q = k.cnt / k.n;
+  const long long fl = (long long)i * k.cnt / k.n, fl1 = (long long)(i + 1) * k.cnt / k.n;
+  const long long m = fl - (long long)i * q;  // items before i with q + 1 entries
+  const long long t_q = ceil_div(q, P.per_tile), t_q1 = ceil_div(q + 1, P.per_tile);
+  *e0 = (int)fl;
+  *ne = (int)(fl1 - fl);
+  *pre = (long long)i * k.valid * P.kvw + ((i - m) * t_q + m * t_q1) * 256 + fl * P.G * 2;
+  *cost = (long long)k.valid * P.kvw + (long long)ceil_div(*ne, P.per_tile) * 256 + (long long)(*ne) * P.G * 2;
 }
 
-__global__ void k_sched_init(SchedPtrs sc, long long tiles_cap, int num_ctas) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * tiles_cap; i += stride)
-    sc.lookback[i] = 0ull;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    sc.hdr[kSchItems] = 0;
-    sc.hdr[kSchCtas] = num_ctas;
-    sc.hdr[kSchCostLo] = 0;
-    sc.hdr[kSchCostHi] = 0;
-    sc.hdr[kSchTileCtr] = 0;
-    sc.hdr[kSchDecItems] = 0;
-    sc.hdr[kSchDecCostLo] = 0;
-    sc.hdr[kSchDecCostHi] = 0;
-    sc.cost_prefix[0] = 0;
-    sc.cost_prefix_dec[0] = 0;
-  }
+__device__ __forceinline__ void decode_item(const KeyWork& k, const Params& P, int i, int* k0, int* nk,
+                                            long long* pre, long long* cost) {
+  const long long per_key = 64 + 128LL * P.kvw;
+  const int a0 = (int)((long long)i * k.cnt / k.n), a1 = (int)((long long)(i + 1) * k.cnt / k.n);
+  *k0 = a0;
+  *nk = a1 - a0;
+  *pre = (long long)a0 * per_key + (long long)i * 256;
+  *cost = (long long)(a1 - a0) * per_key + 256 - (i == k.n - 1 ? k.adj : 0);
 }
 
-__global__ void __launch_bounds__(kScanThreads) k_sched_scan(IndexPtrs ix, SchedPtrs sc, long long tiles_cap,
-                                                              int B, int G, int kvw, int per_tile, int E) {
-  __shared__ int tile_s;
-  __shared__ unsigned long long tmp[33];
-  __shared__ unsigned long long excl_n, excl_d;
-  const int n_active = ix.hdr[kHdrActive];
-  const int NB = ix.hdr[kHdrNB];
-  const int n_tiles = (n_active + kScanTile - 1) / kScanTile;
-  if (threadIdx.x == 0) tile_s = atomicAdd(&sc.hdr[kSchTileCtr], 1);
-  __syncthreads();
-  const int tile = tile_s;
-  if (tile >= n_tiles) return;
-  const bool dec_ok = G <= kDecodeMaxG;
-  const int a0 = tile * kScanTile + threadIdx.x * kScanPerThread;
-  KeyWork kw[kScanPerThread];
-  unsigned long long local_n = 0, local_d = 0;
-#pragma unroll
-  for (int j = 0; j < kScanPerThread; ++j) {
-    const int a = a0 + j;
-    kw[j] = KeyWork{0, 0, 0, 0, 0, 0, 0, 0};
-    if (a >= n_active) continue;
-    const int key = ix.active[a];
-    const int g = key / NB, r = key - g * NB;
-    const SeqInfo si = ix.seq[seq_of_block(ix.seq, B, r)];
-    if (!(dec_ok && si.tq == 1)) {
-      const int b0 = ix.row_ptr[key], b1 = ix.row_ptr[key + 1];
-      const int cnt = b1 - b0;
-      const int n = (cnt + E - 1) / E;
-      const int valid = ix.active_valid[a];
-      long long cost = 0;
-      for (int i = 0; i < n; ++i) {
-        const int ne = (int)(((long long)(i + 1) * cnt) / n - ((long long)i * cnt) / n);
-        cost += item_cost(ne, valid, kvw, per_tile, G);
-      }
-      kw[j].key = key;
-      kw[j].begin = b0;
-      kw[j].cnt = cnt;
-      kw[j].n_items = n;
-      kw[j].cost = cost;
-      local_n += ((unsigned long long)cost << kItemBits) | (unsigned long long)n;
-    } else {
-      const int lo = g * NB + si.blk_off, hi = lo + si.nblk;  // keys of this (g, s)
-      if (a > 0 && ix.active[a - 1] >= lo) continue;          // not the first key of its run
-      int len = 1;
-      while (a + len < n_active && ix.active[a + len] < hi) ++len;
-      const int n = (len + kDecodeBlocks - 1) / kDecodeBlocks;
-      long long cost = 0;
-      for (int i = 0; i < n; ++i) cost += dec_chunk_cost(ix, a, (i * len) / n, ((i + 1) * len) / n, kvw);
-      kw[j].dec_len = len;
-      kw[j].dec_items = n;
-      kw[j].dec_cost = cost;
-      local_d += ((unsigned long long)cost << kItemBits) | (unsigned long long)n;
-    }
+__device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const Params& P, int NB, int n_active, int a) {
+  KeyWork w{};
+  w.a = a;
+  if (a >= n_active) return w;
+  const int key = ix.active[a];
+  const int g = key / NB, r = key - g * NB;
+  const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+  if (P.G <= kDecodeMaxG && si.tq == 1) {
+    const int lo = g * NB + si.blk_off;
+    if (a > 0 && ix.active[a - 1] >= lo) return w;  // inside a run
+    const int len = ix.row_nnz[si.q_begin * P.Hkv + g];  // entries of the token's row = keys of the run
+    const int b_last = ix.active[a + len - 1] - lo;
+    const int v_last = si.L - 128 * b_last;
+    w.kind = 2;
+    w.cnt = len;
+    w.n = ceil_div(len, kDecodeBlocks);
+    w.adj = (b_last == si.nblk - 1 && v_last < 128) ? (128 - v_last) * P.kvw : 0;
+    w.cost = (long long)len * (64 + 128LL * P.kvw) + (long long)w.n * 256 - w.adj;
+    return w;
   }
-  unsigned long long tot_n, tot_d;
-  const unsigned long long ex_n = block_excl_u64(local_n, tmp, &tot_n);
-  const unsigned long long ex_d = block_excl_u64(local_d, tmp, &tot_d);
+  w.kind = 1;
+  w.key = key;
+  w.begin = ix.row_ptr[key];
+  w.cnt = ix.row_ptr[key + 1] - w.begin;
+  w.valid = ix.active_valid[a];
+  w.n = ceil_div(w.cnt, P.E);
+  const int q = w.cnt / w.n, rem = w.cnt % w.n;
+  w.cost = (long long)w.n * w.valid * P.kvw +
+           ((long long)(w.n - rem) * ceil_div(q, P.per_tile) + (long long)rem * ceil_div(q + 1, P.per_tile)) * 256 +
+           (long long)w.cnt * P.G * 2;
+  return w;
+}
+
+__device__ __forceinline__ unsigned long long pack(long long cost, int n) {
+  return ((unsigned long long)cost << kItemBits) | (unsigned long long)n;
+}
+
+__device__ __forceinline__ void active_chunk(int n_active, int* lo, int* hi) {
+  const long long chunk = ((long long)n_active + gridDim.x - 1) / gridDim.x;
+  const long long a = (long long)blockIdx.x * chunk, b = a + chunk;
+  *lo = (int)(a < n_active ? a : n_active);
+  *hi = (int)(b < n_active ? b : n_active);
+}
+
+// number of boundaries c in [0, P] whose target floor(c * C / P) is <= x
+__device__ __forceinline__ int boundaries_at_or_below(long long x, long long C, int P) {
+  if (C <= 0) return P + 1;
+  const long long n = ((x + 1) * P - 1) / C + 1;
+  return (int)(n < P + 1 ? n : P + 1);
+}
+
+__device__ void phase_reduce(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P, unsigned long long* tmp) {
+  const int n_active = ix.hdr[kHdrActive], NB = ix.hdr[kHdrNB];
+  int lo, hi;
+  active_chunk(n_active, &lo, &hi);
+  unsigned long long vn = 0, vd = 0;
+  for (int a = lo + threadIdx.x; a < hi; a += blockDim.x) {
+    const KeyWork w = key_work(ix, P, NB, hi, a);
+    if (w.kind == 1) vn += pack(w.cost, w.n);
+    if (w.kind == 2) vd += pack(w.cost, w.n);
+  }
+  unsigned long long tn, td;
+  block_excl_u64(vn, tmp, &tn);
+  block_excl_u64(vd, tmp, &td);
   if (threadIdx.x == 0) {
-    excl_n = lookback_exclusive(sc.lookback, tile, tot_n, &ix.hdr[kHdrFlags]);
-    excl_d = lookback_exclusive(sc.lookback + tiles_cap, tile, tot_d, &ix.hdr[kHdrFlags]);
+    sc.cta_sums[2 * blockIdx.x] = tn;
+    sc.cta_sums[2 * blockIdx.x + 1] = td;
   }
-  __syncthreads();
+}
+
+__device__ void phase_scan_emit(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P, unsigned long long* tmp) {
+  __shared__ KeyWork s_w[kSchTile];
+  __shared__ int s_nb[kSchTile], s_db[kSchTile];           // tile-relative item bases
+  __shared__ long long s_nc[kSchTile], s_dc[kSchTile];     // global cost bases
+  __shared__ int s_tot_n, s_tot_d;
+  const int n_active = ix.hdr[kHdrActive], NB = ix.hdr[kHdrNB];
   const unsigned long long kLow = (1ull << kItemBits) - 1;
-  unsigned long long run_n = excl_n + ex_n, run_d = excl_d + ex_d;
-#pragma unroll
-  for (int j = 0; j < kScanPerThread; ++j) {
-    const int a = a0 + j;
-    if (a >= n_active) break;
-    if (kw[j].n_items > 0) {
-      const int valid = ix.active_valid[a];
-      long long item = (long long)(run_n & kLow);
-      long long cost = (long long)(run_n >> kItemBits);
-      const int n = kw[j].n_items, cnt = kw[j].cnt;
-      for (int i = 0; i < n; ++i) {
-        const int e0 = (int)(((long long)i * cnt) / n), e1 = (int)(((long long)(i + 1) * cnt) / n);
-        sc.items[item] = make_int4(kw[j].key, kw[j].begin + e0, e1 - e0, 0);
-        sc.cost_prefix[item] = cost;
-        cost += item_cost(e1 - e0, valid, kvw, per_tile, G);
-        ++item;
-      }
-      run_n += ((unsigned long long)kw[j].cost << kItemBits) | (unsigned long long)n;
-    }
-    if (kw[j].dec_items > 0) {
-      long long item = (long long)(run_d & kLow);
-      long long cost = (long long)(run_d >> kItemBits);
-      const int n = kw[j].dec_items, len = kw[j].dec_len;
-      for (int i = 0; i < n; ++i) {
-        const int k0 = (i * len) / n, k1 = ((i + 1) * len) / n;
-        sc.items_dec[item] = make_int4(a + k0, ix.row_ptr[ix.active[a + k0]], 1, k1 - k0);
-        sc.cost_prefix_dec[item] = cost;
-        cost += dec_chunk_cost(ix, a, k0, k1, kvw);
-        ++item;
-      }
-      run_d += ((unsigned long long)kw[j].dec_cost << kItemBits) | (unsigned long long)n;
+  // prefix of the chunks before this CTA's, and the totals
+  unsigned long long pre_n = 0, pre_d = 0, all_n = 0, all_d = 0;
+  for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+    const unsigned long long vn = sc.cta_sums[2 * c], vd = sc.cta_sums[2 * c + 1];
+    all_n += vn;
+    all_d += vd;
+    if (c < (int)blockIdx.x) {
+      pre_n += vn;
+      pre_d += vd;
     }
   }
-  if (tile == n_tiles - 1 && threadIdx.x == kScanThreads - 1) {
-    const unsigned long long all_n = excl_n + tot_n, all_d = excl_d + tot_d;
-    const long long nn = (long long)(all_n & kLow), Cn = (long long)(all_n >> kItemBits);
-    const long long nd = (long long)(all_d & kLow), Cd = (long long)(all_d >> kItemBits);
-    sc.hdr[kSchItems] = (int)nn;
+  unsigned long long t;
+  block_excl_u64(pre_n, tmp, &t); pre_n = t;
+  block_excl_u64(pre_d, tmp, &t); pre_d = t;
+  block_excl_u64(all_n, tmp, &t); all_n = t;
+  block_excl_u64(all_d, tmp, &t); all_d = t;
+  const long long Cn = (long long)(all_n >> kItemBits), Cd = (long long)(all_d >> kItemBits);
+  const int Nn = (int)(all_n & kLow), Nd = (int)(all_d & kLow);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    sc.hdr[kSchItems] = Nn;
+    sc.hdr[kSchCtas] = P.num_ctas;
     sc.hdr[kSchCostLo] = (int)(Cn & 0xffffffffll);
     sc.hdr[kSchCostHi] = (int)(Cn >> 32);
-    sc.cost_prefix[nn] = Cn;
-    sc.hdr[kSchDecItems] = (int)nd;
+    sc.hdr[kSchDecItems] = Nd;
     sc.hdr[kSchDecCostLo] = (int)(Cd & 0xffffffffll);
     sc.hdr[kSchDecCostHi] = (int)(Cd >> 32);
-    sc.cost_prefix_dec[nd] = Cd;
+    sc.cost_prefix[Nn] = Cn;
+    sc.cost_prefix_dec[Nd] = Cd;
+    // boundaries whose target is 0 (at least c = 0) start at item 0
+    for (int c = 0, e = boundaries_at_or_below(0, Cn, P.num_ctas); c < e; ++c) sc.cta_ptr[c] = 0;
+    for (int c = 0, e = boundaries_at_or_below(0, Cd, P.num_ctas); c < e; ++c) sc.cta_ptr_dec[c] = 0;
+  }
+  int lo, hi;
+  active_chunk(n_active, &lo, &hi);
+  unsigned long long carry_n = pre_n, carry_d = pre_d;
+  for (int t0 = lo; t0 < hi; t0 += kSchTile) {
+    unsigned long long vn = 0, vd = 0;
+    KeyWork w[kSchPerThread];
+#pragma unroll
+    for (int j = 0; j < kSchPerThread; ++j) {
+      const int a = t0 + threadIdx.x * kSchPerThread + j;
+      w[j] = key_work(ix, P, NB, hi, a);
+      if (w[j].kind == 1) vn += pack(w[j].cost, w[j].n);
+      if (w[j].kind == 2) vd += pack(w[j].cost, w[j].n);
+    }
+    unsigned long long tn, td;
+    unsigned long long en = block_excl_u64(vn, tmp, &tn);
+    unsigned long long ed = block_excl_u64(vd, tmp, &td);
+#pragma unroll
+    for (int j = 0; j < kSchPerThread; ++j) {
+      const int slot = threadIdx.x * kSchPerThread + j;
+      s_w[slot] = w[j];
+      s_nb[slot] = (int)(en & kLow);
+      s_db[slot] = (int)(ed & kLow);
+      s_nc[slot] = (long long)((carry_n + en) >> kItemBits);
+      s_dc[slot] = (long long)((carry_d + ed) >> kItemBits);
+      if (w[j].kind == 1) en += pack(w[j].cost, w[j].n);
+      if (w[j].kind == 2) ed += pack(w[j].cost, w[j].n);
+    }
+    if (threadIdx.x == 0) {
+      s_tot_n = (int)(tn & kLow);
+      s_tot_d = (int)(td & kLow);
+    }
+    __syncthreads();
+    const int base_n = (int)(carry_n & kLow), base_d = (int)(carry_d & kLow);
+    // normal items of the tile
+    for (int x = threadIdx.x; x < s_tot_n; x += blockDim.x) {
+      int l = 0, h = kSchTile - 1;  // last slot with base <= x holding a normal key
+      while (l < h) {
+        const int mid = (l + h + 1) >> 1;
+        if (s_nb[mid] <= x) l = mid;
+        else h = mid - 1;
+      }
+      while (l > 0 && (s_w[l].kind != 1 || s_nb[l] + s_w[l].n <= x)) --l;
+      const KeyWork& k = s_w[l];
+      const int i = x - s_nb[l];
+      int e0, ne;
+      long long pre, cost;
+      normal_item(k, P, i, &e0, &ne, &pre, &cost);
+      const long long p = s_nc[l] + pre;
+      const int item = base_n + x;
+      sc.items[item] = make_int4(k.key, k.begin + e0, ne, 0);
+      sc.cost_prefix[item] = p;
+      for (int c = boundaries_at_or_below(p, Cn, P.num_ctas), e = boundaries_at_or_below(p + cost, Cn, P.num_ctas);
+           c < e; ++c)
+        sc.cta_ptr[c] = item + 1;
+    }
+    // decode items of the tile
+    for (int x = threadIdx.x; x < s_tot_d; x += blockDim.x) {
+      int l = 0, h = kSchTile - 1;
+      while (l < h) {
+        const int mid = (l + h + 1) >> 1;
+        if (s_db[mid] <= x) l = mid;
+        else h = mid - 1;
+      }
+      while (l > 0 && (s_w[l].kind != 2 || s_db[l] + s_w[l].n <= x)) --l;
+      const KeyWork& k = s_w[l];
+      const int i = x - s_db[l];
+      int k0, nk;
+      long long pre, cost;
+      decode_item(k, P, i, &k0, &nk, &pre, &cost);
+      const long long p = s_dc[l] + pre;
+      const int item = base_d + x;
+      sc.items_dec[item] = make_int4(k.a + k0, ix.row_ptr[ix.active[k.a + k0]], 1, nk);
+      sc.cost_prefix_dec[item] = p;
+      for (int c = boundaries_at_or_below(p, Cd, P.num_ctas), e = boundaries_at_or_below(p + cost, Cd, P.num_ctas);
+           c < e; ++c)
+        sc.cta_ptr_dec[c] = item + 1;
+    }
+    __syncthreads();
+    carry_n += tn;
+    carry_d += td;
   }
 }
 
-__global__ void k_partition(SchedPtrs sc, int num_ctas) {
-  for (int c2 = blockIdx.x * blockDim.x + threadIdx.x; c2 < 2 * (num_ctas + 1); c2 += gridDim.x * blockDim.x) {
-    const bool dec = c2 > num_ctas;
-    const int c = dec ? c2 - (num_ctas + 1) : c2;
-    const int n_items = sc.hdr[dec ? kSchDecItems : kSchItems];
-    const long long C = (long long)(unsigned)sc.hdr[dec ? kSchDecCostLo : kSchCostLo] |
-                        ((long long)sc.hdr[dec ? kSchDecCostHi : kSchCostHi] << 32);
-    const long long* prefix = dec ? sc.cost_prefix_dec : sc.cost_prefix;
-    const long long target = (long long)c * C / num_ctas;
-    // number of items with cost_prefix < target (prefix is non-decreasing)
-    int lo = 0, hi = n_items;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] < target) lo = mid + 1;
-      else hi = mid;
-    }
-    (dec ? sc.cta_ptr_dec : sc.cta_ptr)[c] = lo;
-  }
+struct SchedArgs {
+  IndexPtrs ix;
+  SchedPtrs sc;
+  Params P;
+};
+
+__global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
+  __shared__ unsigned long long tmp[33];
+  int* bar = a.sc.hdr + kSchBarCount;
+  int* flags = a.ix.hdr + kHdrFlags;
+  phase_reduce(a.ix, a.sc, a.P, tmp);
+  grid_barrier(bar, flags, gridDim.x);
+  phase_scan_emit(a.ix, a.sc, a.P, tmp);
 }
 
 }  // namespace
 
+int coop_grid(const void* kernel, int threads);
+
 cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc,
                             const mxsa_sched_layout& lay, int num_ctas, cudaStream_t st) {
+  (void)lay;
   const int G = p.num_q_heads / p.num_kv_heads;
-  const int per_tile = std::max(1, MXSA_TILE_ROWS / G);
-  const int E = MXSA_ITEM_TILES * per_tile;
-  const int kvw = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
-  const long long tiles = std::max<long long>(lay.tiles_cap, 1);
-  k_sched_init<<<(int)std::min<long long>((2 * tiles + 255) / 256, 1024), 256, 0, st>>>(sc, tiles, num_ctas);
-  if (lay.tiles_cap > 0)
-    k_sched_scan<<<(unsigned)lay.tiles_cap, kScanThreads, 0, st>>>(ix, sc, tiles, p.num_seqs, G, kvw, per_tile,
-                                                                     E);
-  k_partition<<<(2 * (num_ctas + 1) + 255) / 256, 256, 0, st>>>(sc, num_ctas);
-  return cudaGetLastError();
+  SchedArgs a;
+  a.ix = ix;
+  a.sc = sc;
+  a.P.B = p.num_seqs;
+  a.P.Hkv = p.num_kv_heads;
+  a.P.G = G;
+  a.P.kvw = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
+  a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
+  a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
+  a.P.num_ctas = num_ctas;
+  const int grid = coop_grid(reinterpret_cast<const void*>(k_schedule), kSchThreads);
+  if (grid <= 0) return cudaErrorNotSupported;
+  cudaError_t e = cudaMemsetAsync(sc.hdr, 0, kSchInts * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&a};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_schedule), dim3(grid), dim3(kSchThreads), args,
+                                     0, st);
 }
 
 }  // namespace mxsa

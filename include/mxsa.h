@@ -167,7 +167,7 @@ mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device
  * active_keys: int32 [n_active], keys with entries in increasing order. */
 typedef struct {
   size_t header, seq_info, token_seq, slot_entry, bitmap, kmap, counts, row_ptr, entries, active_keys,
-      active_valid, lookback, total;
+      active_valid, row_nnz, cta_sums, total;
   int64_t keys_cap, nslots, bitmap_words_cap, kmap_bytes_cap, tiles_cap;
 } mxsa_index_layout;
 mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layout* layout);
@@ -183,7 +183,7 @@ mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layo
  *              of up to 8 keys of one single-token sequence and kv head
  *              (every one of those keys holds that token's one entry). */
 typedef struct {
-  size_t header, items, cost_prefix, cta_ptr, items_dec, cost_prefix_dec, cta_ptr_dec, lookback, total;
+  size_t header, items, cost_prefix, cta_ptr, items_dec, cost_prefix_dec, cta_ptr_dec, cta_sums, total;
   int64_t items_cap, tiles_cap;
 } mxsa_sched_layout;
 mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layout* layout);
