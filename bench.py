@@ -1,7 +1,8 @@
 """Benchmark of block-sparse KV-outer attention on GB300.
 
-One step = the whole hot path (index builder, scheduler, KV-outer forward,
-combine) over one batch of the synthetic workload, inputs resident in HBM.
+One step = the whole hot path (index builder and scheduler in one launch,
+KV-outer forward, combine) over one batch of the synthetic workload, inputs
+resident in HBM.
 Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -10,8 +11,8 @@ Prints ONE JSON line (rank 0).
 Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
 on the launching stream with an L2 flush (a 256 MiB write) between steps
 outside the events; device time summed over the K steps; max over ranks.
-Per-kernel durations come from events recorded between the four calls on the
-same stream.  Multi-GPU (torchrun): every rank runs its own batch of the
+Per-kernel durations come from events recorded between the calls (plan =
+index + schedule in one launch, forward, combine) on the same stream.  Multi-GPU (torchrun): every rank runs its own batch of the
 same workload recipe (independent sequences, no collective on the data
 path); value = tokens of all ranks / max-over-ranks time ("weak" scaling).
 """
@@ -36,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn tokens/s, TFLOP/s and unique-KV GB/s vs roofline, 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 10  # k_seq k_zero k_mark k_scan k_emit | k_sched_init k_sched_scan k_partition | k_fwd | k_combine
+KERNELS_PER_STEP = 4  # k_plan (index + schedule) | k_fwd_dec, k_fwd | k_combine
 DEFAULT_WORKLOAD = "gqa_decode"
 
 
@@ -57,7 +58,7 @@ def measured_peaks():
 
 def fwd_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("fwd.cu", "ptx.cuh", "internal.h"):
+    for f in ("fwd.cu", "fwd_decode.cu", "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "block_sparse_attention_builder_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -305,18 +306,15 @@ def main():
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        mx.build_index(prob, sel, cu, lens, attn.ws.index, stream)
+        mx.plan(prob, sel, cu, lens, attn.ws.index, attn.ws.sched, 0, stream)  # index + schedule, one launch
         if ev:
             ev[1].record(stream)
-        mx.schedule(prob, attn.ws.index, attn.ws.sched, 0, stream)
-        if ev:
-            ev[2].record(stream)
         mx.kvouter_fwd(prob, q, k, v, bt, attn.ws.index, attn.ws.sched, attn.ws.partial, 0, stream)
         if ev:
-            ev[3].record(stream)
+            ev[2].record(stream)
         mx.combine(prob, attn.ws.index, attn.ws.partial, out, lse, stream)
         if ev:
-            ev[4].record(stream)
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -325,7 +323,7 @@ def main():
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} after warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -338,7 +336,7 @@ def main():
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(3)] for i in range(args.steps)])
     step_ms = per.sum(axis=1)
     total_ms = float(step_ms.sum())
     if world > 1:
@@ -348,7 +346,7 @@ def main():
     ms_per_step = total_ms / args.steps
     tokens_per_step = w.total_q
     value = tokens_per_step * world * args.steps / (total_ms / 1e3)
-    fwd_ms = float(per[:, 2].mean())
+    fwd_ms = float(per[:, 1].mean())
     peaks = measured_peaks()
 
     # ---------------------------------------------------------- e2e (public API, host buffers)
@@ -395,8 +393,8 @@ def main():
         if bound == "hbm":
             roof = {"bound": "hbm", "achieved": fwd_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": fwd_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),
-                    "kernel": "k_fwd", "algorithmic_bytes_per_launch": unique_kv_bytes,
-                    "peak_source": peaks["src"]}
+                    "kernel": "k_fwd_dec (+ k_fwd, which has no items here)",
+                    "algorithmic_bytes_per_launch": unique_kv_bytes, "peak_source": peaks["src"]}
         else:
             pk = peaks["bf16_tflops"]
             roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": pk, "unit": "TFLOP/s",
@@ -409,8 +407,8 @@ def main():
             "data": "synthetic (seeded counter-based N(0,1) values; selections per the workload recipe)",
             "config": workload_config(w, stats, args.workload),
             "tflops": tflops, "unique_kv_gbs": kv_gbs,
-            "kernel_ms": {"index": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
-                          "fwd": fwd_ms, "combine": float(per[:, 3].mean())},
+            "kernel_ms": {"plan (index + schedule)": float(per[:, 0].mean()), "fwd": fwd_ms,
+                          "combine": float(per[:, 2].mean())},
             "fwd_unique_kv_gbs": fwd_gbs, "fwd_tflops": fwd_tflops,
             "bytes": {"unique_kv": unique_kv_bytes, "io": io_bytes, "partials_overhead": partial_bytes},
             "roofline": roof,

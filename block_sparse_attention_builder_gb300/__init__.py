@@ -34,6 +34,7 @@ FLAG_NAMES = {1: "SEL_RANGE", 2: "SEL_DUP", 4: "PAGE", 8: "CAUSAL_LEN", 16: "LEN
 STATUS_NAMES = {0: "MXSA_OK", 1: "MXSA_ERR_INVALID_ARG", 2: "MXSA_ERR_UNSUPPORTED", 3: "MXSA_ERR_WORKSPACE",
                 4: "MXSA_ERR_CUDA", 5: "MXSA_ERR_DATA"}
 EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_build_index", "mxsa_schedule",
+            "mxsa_plan",
             "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
             "mxsa_sched_layout_query"]
 
@@ -60,7 +61,7 @@ class Problem(ctypes.Structure):
 class IndexLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("header", "seq_info", "token_seq", "slot_entry", "bitmap", "kmap",
                                                "counts", "row_ptr", "entries", "active_keys", "active_valid",
-                                               "row_nnz", "cta_sums", "total")] + \
+                                               "row_nnz", "row_minb", "row_maxb", "cta_sums", "total")] + \
                [(n, ctypes.c_int64) for n in ("keys_cap", "nslots", "bitmap_words_cap", "kmap_bytes_cap",
                                               "tiles_cap")]
 
@@ -84,6 +85,7 @@ def _load_library() -> ctypes.CDLL:
         "mxsa_workspace_size": [P, P, P, P],
         "mxsa_build_index": [P, P, P, P, P, S, P],
         "mxsa_schedule": [P, P, S, ctypes.c_int32, P, S, P],
+        "mxsa_plan": [P, P, P, P, P, S, ctypes.c_int32, P, S, P],
         "mxsa_kvouter_fwd": [P, P, P, P, P, P, S, P, S, ctypes.c_int32, P, S, P],
         "mxsa_combine": [P, P, S, P, S, P, P, P],
         "mxsa_read_status": [P, P, P],
@@ -169,6 +171,13 @@ def schedule(prob, index_ws, sched_ws, num_ctas=0, stream=None):
                               _stream(stream)), "mxsa_schedule")
 
 
+def plan(prob, sel, cu_seqlens_q, used_kv_lens, index_ws, sched_ws, num_ctas=0, stream=None):
+    """build_index + schedule in one launch (identical workspaces)."""
+    _check(_lib.mxsa_plan(ctypes.byref(prob), _ptr(sel), _ptr(cu_seqlens_q), _ptr(used_kv_lens), _ptr(index_ws),
+                          index_ws.numel() * index_ws.element_size(), int(num_ctas), _ptr(sched_ws),
+                          sched_ws.numel() * sched_ws.element_size(), _stream(stream)), "mxsa_plan")
+
+
 def kvouter_fwd(prob, q, k_cache, v_cache, block_tables, index_ws, sched_ws, partial_ws, num_ctas=0, stream=None):
     _check(_lib.mxsa_kvouter_fwd(ctypes.byref(prob), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                  _ptr(index_ws), index_ws.numel() * index_ws.element_size(), _ptr(sched_ws),
@@ -221,8 +230,7 @@ class SparseAttention:
             out = torch.empty(p.total_q, p.num_q_heads, 128, dtype=q.dtype, device=q.device)
         if return_lse and lse is None:
             lse = torch.empty(p.num_q_heads, p.total_q, dtype=torch.float32, device=q.device)
-        build_index(p, selected, cu_seqlens_q, used_kv_lens, self.ws.index, stream)
-        schedule(p, self.ws.index, self.ws.sched, self.num_ctas, stream)
+        plan(p, selected, cu_seqlens_q, used_kv_lens, self.ws.index, self.ws.sched, self.num_ctas, stream)
         kvouter_fwd(p, q, k_cache, v_cache, block_tables, self.ws.index, self.ws.sched, self.ws.partial,
                     self.num_ctas, stream)
         combine(p, self.ws.index, self.ws.partial, out, lse if return_lse else None, stream)

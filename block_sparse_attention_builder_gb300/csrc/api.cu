@@ -76,7 +76,9 @@ mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L) {
   L->active_keys = o;  o = align_up(o + (size_t)act * 4);
   L->active_valid = o; o = align_up(o + (size_t)act * 4);
   L->row_nnz = o;      o = align_up(o + (size_t)Tq * Hkv * 4);
-  L->cta_sums = o;     o = align_up(o + (size_t)kMaxCoopCtas * 8);
+  L->row_minb = o;     o = align_up(o + (size_t)Tq * Hkv * 4);
+  L->row_maxb = o;     o = align_up(o + (size_t)Tq * Hkv * 4);
+  L->cta_sums = o;     o = align_up(o + (size_t)kMaxCoopCtas * 3 * 8);
   L->total = o;
   return MXSA_OK;
 }
@@ -128,6 +130,8 @@ IndexPtrs index_ptrs(const mxsa_problem& p, void* ws) {
   x.active = reinterpret_cast<int32_t*>(b + L.active_keys);
   x.active_valid = reinterpret_cast<int32_t*>(b + L.active_valid);
   x.row_nnz = reinterpret_cast<int32_t*>(b + L.row_nnz);
+  x.row_minb = reinterpret_cast<int32_t*>(b + L.row_minb);
+  x.row_maxb = reinterpret_cast<int32_t*>(b + L.row_maxb);
   x.cta_sums = reinterpret_cast<unsigned long long*>(b + L.cta_sums);
   return x;
 }
@@ -234,6 +238,30 @@ mxsa_status mxsa_schedule(const mxsa_problem* problem, const void* index_ws, siz
   IndexPtrs ix = index_ptrs(*problem, const_cast<void*>(index_ws));
   SchedPtrs sc = sched_ptrs(*problem, sched_ws);
   cudaError_t e = launch_schedule(*problem, ix, sc, sl, ctas, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
+mxsa_status mxsa_plan(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
+                      const int32_t* used_kv_lens, void* index_ws, size_t index_bytes, int32_t num_ctas,
+                      void* sched_ws, size_t sched_bytes, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout il;
+  mxsa_sched_layout sl;
+  mxsa_status s = index_layout(*problem, &il);
+  if (s != MXSA_OK) return s;
+  sched_layout(*problem, &sl);
+  if (!cu_seqlens_q || !used_kv_lens || !index_ws || !sched_ws || (problem->total_q > 0 && !sel))
+    return MXSA_ERR_INVALID_ARG;
+  if (!aligned(sel, 4) || !aligned(cu_seqlens_q, 8) || !aligned(used_kv_lens, 4) || !aligned(index_ws, 16) ||
+      !aligned(sched_ws, 16))
+    return MXSA_ERR_INVALID_ARG;
+  if (index_bytes < il.total || sched_bytes < sl.total) return MXSA_ERR_WORKSPACE;
+  int ctas = 0;
+  s = resolve_ctas(num_ctas, &ctas);
+  if (s != MXSA_OK) return s;
+  IndexPtrs ix = index_ptrs(*problem, index_ws);
+  SchedPtrs sc = sched_ptrs(*problem, sched_ws);
+  cudaError_t e = launch_plan(*problem, sel, cu_seqlens_q, used_kv_lens, ix, sc, ctas, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
 }
 

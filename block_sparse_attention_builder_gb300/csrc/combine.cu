@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int lane = threadIdx.x & 31;
   const int G = Hq / Hkv;
   const long long n_rows = (long long)total_q * Hq;
+  pdl_wait();  // the forward's partials are complete
   constexpr float kLog2e = 1.4426950408889634f;
   for (long long row = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); row < n_rows;
        row += (long long)gridDim.x * kWarpsPerBlock) {
@@ -105,11 +106,9 @@ cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const flo
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
-  k_combine<<<(int)blocks, kWarpsPerBlock * 32, 0, st>>>(ix.slot_entry, part_o, part_lse,
-                                                         static_cast<uint8_t*>(out), lse, p.total_q,
-                                                         p.num_q_heads, p.num_kv_heads, p.topk,
-                                                         p.q_dtype == MXSA_BF16 ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, st,
+                    (const int32_t*)ix.slot_entry, part_o, part_lse, static_cast<uint8_t*>(out), lse, p.total_q,
+                    p.num_q_heads, p.num_kv_heads, p.topk, p.q_dtype == MXSA_BF16 ? 1 : 0);
 }
 
 }  // namespace mxsa

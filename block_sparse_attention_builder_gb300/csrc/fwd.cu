@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();
+  pdl_wait();  // the schedule (and the previous forward) are complete
 
   if (a.sch_hdr[kSchCtas] != (int)gridDim.x) {
     if (tid == 0 && blockIdx.x == 0) atomicOr(a.flags, MXSA_FLAG_SCHEDULE);
@@ -515,8 +517,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  k_fwd<<<num_ctas, kThreads, smem, st>>>(tmk, tmv, a);
-  return cudaGetLastError();
+  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, a);
 }
 
 }  // namespace mxsa

@@ -215,6 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* red = reinterpret_cast<float*>(sm + L.red);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ns = a.ns;
+  pdl_launch_dependents();
+  pdl_wait();  // the schedule (and the previous forward) are complete
 
   if (a.sch_hdr[kSchCtas] != (int)gridDim.x) {
     if (tid == 0 && blockIdx.x == 0) atomicOr(a.flags, MXSA_FLAG_SCHEDULE);
@@ -614,8 +616,7 @@ cudaError_t launch_n(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUten
                                     (int)(std::max(l16.total, l8.total) + 1024));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  k_fwd_dec<N><<<num_ctas, kThreads, smem, st>>>(tmk, tmv, tmq, a);
-  return cudaGetLastError();
+  return launch_pdl(k_fwd_dec<N>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, a);
 }
 
 }  // namespace

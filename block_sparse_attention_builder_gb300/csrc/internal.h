@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -73,7 +74,9 @@ struct IndexPtrs {
   int32_t* active;
   int32_t* active_valid;
   int32_t* row_nnz;                // entries made per (token, kv head) row
-  unsigned long long* cta_sums;    // per-CTA sums of the cooperative scans
+  int32_t* row_minb;               // smallest / largest block of those entries
+  int32_t* row_maxb;
+  unsigned long long* cta_sums;    // per-CTA sums of the cooperative scans (3 per CTA)
 };
 
 // CTAs of the cooperative launches (index, schedule) never exceed this
@@ -107,6 +110,8 @@ mxsa_status validate_problem(const mxsa_problem& p);
 // launchers (return cudaGetLastError())
 cudaError_t launch_build_index(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
                                const IndexPtrs& ix, const mxsa_index_layout& lay, cudaStream_t st);
+cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
+                        const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas, cudaStream_t st);
 cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc,
                             const mxsa_sched_layout& lay, int num_ctas, cudaStream_t st);
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
@@ -119,9 +124,37 @@ cudaError_t launch_fwd_decode(const mxsa_problem& p, const void* q, const CUtens
 cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
                            const float* part_lse, void* out, float* lse, cudaStream_t st);
 
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it waits for that
+// kernel's results with griddepcontrol.wait before reading them.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------------------
 // device helpers shared by the scan kernels
 #ifdef __CUDACC__
+// wait until the previous kernel on the stream (a programmatic dependency)
+// has completed and its writes are visible; a no-op without one
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// let the next kernel on the stream be scheduled early
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

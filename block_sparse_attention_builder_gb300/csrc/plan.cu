@@ -1,0 +1,318 @@
+// Index build and schedule fused into one cooperative launch (mxsa_plan).
+// The result is the same index as mxsa_build_index and the same two work
+// lists as mxsa_schedule; the schedule is folded into the index's own scan:
+//
+//   seq + zero   every CTA recomputes the per-sequence scan (B <= 1024; one
+//                CTA and a barrier otherwise), CTA 0 stores it; every CTA
+//                fills its share of the token map and clears counters and
+//                bitmap rows                                   -> barrier
+//   mark         one warp per (token, kv head) row, as in the index build;
+//                it also records the row's entry count and its smallest and
+//                largest selected block                        -> barrier
+//   reduce       one contiguous chunk of keys per CTA; each key adds to
+//                three sums: (entries, key active), (normal items, cost),
+//                (decode items, cost).  A decode key (single-token sequence)
+//                contributes its whole run when its block is the row's
+//                smallest; the run length is the row's entry count and the
+//                partial-last-block adjustment applies when the row's
+//                largest block is the sequence's last      -> barrier
+//   scan + emit  each CTA adds the sums of the chunks before it; per tile of
+//                256 keys: row_ptr, the active-key list, the entries (bitmap
+//                walk), and the items of both lists with their cost prefixes
+//                and CTA boundaries.  A decode run's keys each hold one
+//                entry, so the entry of its k-th key is the first key's + k.
+#include <algorithm>
+
+#include "index_phases.cuh"
+#include "sched_common.cuh"
+
+namespace mxsa {
+
+namespace {
+
+using namespace sch;
+
+constexpr int kPlanThreads = 256;
+constexpr int kPlanTile = 256;  // keys per scan tile: one per thread
+constexpr int kRedundantSeqMax = 1024;
+static_assert(kPlanThreads == ixp::kIndexThreads, "index phases run with the same block size");
+
+struct PlanArgs {
+  ixp::IndexArgs ia;
+  SchedPtrs sc;
+  Params P;
+};
+
+// schedule contribution of key `key` with `c` entries (kind 0: none)
+__device__ __forceinline__ KeyWork plan_key_work(const IndexPtrs& ix, const Params& P, int NB, int key, int c) {
+  KeyWork w{};
+  if (c == 0) return w;
+  const int g = key / NB, r = key - g * NB;
+  const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+  const int b = r - si.blk_off;
+  if (P.G <= kDecodeMaxG && si.tq == 1) {
+    const int row = si.q_begin * P.Hkv + g;
+    if (b != ix.row_minb[row]) return w;  // not the first key of its run
+    const int len = ix.row_nnz[row];
+    const int bmax = ix.row_maxb[row];
+    const int v_last = si.L - 128 * bmax;
+    w.kind = 2;
+    w.cnt = len;
+    w.n = ceil_div(len, kDecodeBlocks);
+    w.adj = (bmax == si.nblk - 1 && v_last < 128) ? (128 - v_last) * P.kvw : 0;
+    w.cost = (long long)len * (64 + 128LL * P.kvw) + (long long)w.n * 256 - w.adj;
+    return w;
+  }
+  w.kind = 1;
+  w.key = key;
+  w.cnt = c;
+  const int valid = si.L - 128 * b;
+  w.valid = valid < 128 ? valid : 128;
+  w.n = ceil_div(c, P.E);
+  const int q = c / w.n, rem = c % w.n;
+  w.cost = (long long)w.n * w.valid * P.kvw +
+           ((long long)(w.n - rem) * ceil_div(q, P.per_tile) + (long long)rem * ceil_div(q + 1, P.per_tile)) * 256 +
+           (long long)c * P.G * 2;
+  return w;
+}
+
+__device__ __forceinline__ void plan_reduce(const IndexPtrs& ix, const Params& P, unsigned long long* tmp) {
+  const int n_keys = ix.hdr[kHdrKeys], NB = ix.hdr[kHdrNB];
+  int lo, hi;
+  ixp::key_chunk(n_keys, &lo, &hi);
+  unsigned long long vi = 0, vn = 0, vd = 0;
+  for (int k = lo + threadIdx.x; k < hi; k += blockDim.x) {
+    const int c = ix.counts[k];
+    vi += ixp::key_payload(c);
+    const KeyWork w = plan_key_work(ix, P, NB, k, c);
+    if (w.kind == 1) vn += pack(w.cost, w.n);
+    if (w.kind == 2) vd += pack(w.cost, w.n);
+  }
+  U3 tot;
+  block_excl_u64x3(U3{vi, vn, vd}, tmp, &tot);
+  if (threadIdx.x == 0) {
+    ix.cta_sums[3 * blockIdx.x] = tot.x;
+    ix.cta_sums[3 * blockIdx.x + 1] = tot.y;
+    ix.cta_sums[3 * blockIdx.x + 2] = tot.z;
+  }
+}
+
+__device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P, int Hkv,
+                                               int topk, unsigned long long* tmp) {
+  __shared__ KeyWork s_w[kPlanTile];
+  __shared__ int s_nb[kPlanTile], s_db[kPlanTile];
+  __shared__ long long s_nc[kPlanTile], s_dc[kPlanTile];
+  __shared__ int s_long_key[kPlanTile], s_long_base[kPlanTile];
+  __shared__ int s_n_long, s_tot_n, s_tot_d;
+  const int n_keys = ix.hdr[kHdrKeys], NB = ix.hdr[kHdrNB];
+  const size_t BMW = (size_t)ix.hdr[kHdrBMW], KMW = (size_t)ix.hdr[kHdrKMW];
+  const int warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  const unsigned long long kLow31 = (1ull << 31) - 1, kLow = (1ull << kItemBits) - 1;
+  // prefixes of the chunks before this CTA and the totals, all three sums
+  unsigned long long pi = 0, pn = 0, pd = 0, ai = 0, an = 0, ad = 0;
+  for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+    const unsigned long long vi = ix.cta_sums[3 * c], vn = ix.cta_sums[3 * c + 1], vd = ix.cta_sums[3 * c + 2];
+    ai += vi;
+    an += vn;
+    ad += vd;
+    if (c < (int)blockIdx.x) {
+      pi += vi;
+      pn += vn;
+      pd += vd;
+    }
+  }
+  U3 t3;
+  block_excl_u64x3(U3{pi, pn, pd}, tmp, &t3);
+  pi = t3.x;
+  pn = t3.y;
+  pd = t3.z;
+  block_excl_u64x3(U3{ai, an, ad}, tmp, &t3);
+  ai = t3.x;
+  an = t3.y;
+  ad = t3.z;
+  const long long Cn = (long long)(an >> kItemBits), Cd = (long long)(ad >> kItemBits);
+  const int Nn = (int)(an & kLow), Nd = (int)(ad & kLow);
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    ix.row_ptr[n_keys] = (int)(ai >> 31);
+    ix.hdr[kHdrNnz] = (int)(ai >> 31);
+    ix.hdr[kHdrActive] = (int)(ai & kLow31);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    sc.hdr[kSchItems] = Nn;
+    sc.hdr[kSchCtas] = P.num_ctas;
+    sc.hdr[kSchCostLo] = (int)(Cn & 0xffffffffll);
+    sc.hdr[kSchCostHi] = (int)(Cn >> 32);
+    sc.hdr[kSchDecItems] = Nd;
+    sc.hdr[kSchDecCostLo] = (int)(Cd & 0xffffffffll);
+    sc.hdr[kSchDecCostHi] = (int)(Cd >> 32);
+    sc.cost_prefix[Nn] = Cn;
+    sc.cost_prefix_dec[Nd] = Cd;
+    for (int c = 0, e = boundaries_at_or_below(0, Cn, P.num_ctas); c < e; ++c) sc.cta_ptr[c] = 0;
+    for (int c = 0, e = boundaries_at_or_below(0, Cd, P.num_ctas); c < e; ++c) sc.cta_ptr_dec[c] = 0;
+  }
+  int lo, hi;
+  ixp::key_chunk(n_keys, &lo, &hi);
+  unsigned long long ci = pi, cn = pn, cd = pd;
+  for (int t0 = lo; t0 < hi; t0 += kPlanTile) {
+    const int key = t0 + threadIdx.x;
+    const int c = key < hi ? ix.counts[key] : 0;
+    KeyWork w = plan_key_work(ix, P, NB, key, c);
+    if (threadIdx.x == 0) s_n_long = 0;
+    U3 tt;
+    const U3 ex = block_excl_u64x3(U3{ixp::key_payload(c), w.kind == 1 ? pack(w.cost, w.n) : 0ull,
+                                      w.kind == 2 ? pack(w.cost, w.n) : 0ull},
+                                   tmp, &tt);
+    const unsigned long long ei = ex.x, en = ex.y, ed = ex.z;
+    const unsigned long long ti = tt.x, tn = tt.y, td = tt.z;
+    const unsigned long long run = ci + ei;
+    if (key < hi) {
+      const int base = (int)(run >> 31);
+      ix.row_ptr[key] = base;
+      w.begin = base;
+      if (c > 0) {
+        const int pos = (int)(run & kLow31);
+        w.a = pos;
+        ix.active[pos] = key;
+        const int g = key / NB, r = key - g * NB;
+        const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+        const int b = r - si.blk_off;
+        const int valid = si.L - 128 * b;
+        ix.active_valid[pos] = valid < 128 ? valid : 128;
+        if (si.words <= 2) {
+          ixp::emit_row_serial(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
+                               ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g,
+                               Hkv, topk, base);
+        } else {
+          const int at = atomicAdd(&s_n_long, 1);
+          s_long_key[at] = key;
+          s_long_base[at] = base;
+        }
+      }
+    }
+    s_w[threadIdx.x] = w;
+    s_nb[threadIdx.x] = (int)(en & kLow);
+    s_db[threadIdx.x] = (int)(ed & kLow);
+    s_nc[threadIdx.x] = (long long)((cn + en) >> kItemBits);
+    s_dc[threadIdx.x] = (long long)((cd + ed) >> kItemBits);
+    if (threadIdx.x == 0) {
+      s_tot_n = (int)(tn & kLow);
+      s_tot_d = (int)(td & kLow);
+    }
+    __syncthreads();
+    // long bitmap rows: one warp per key
+    for (int i = warp; i < s_n_long; i += n_warps) {
+      const int k2 = s_long_key[i];
+      const int g = k2 / NB, r = k2 - g * NB;
+      const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+      const int b = r - si.blk_off;
+      ixp::emit_row_warp(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
+                         ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv,
+                         topk, s_long_base[i]);
+    }
+    const int base_n = (int)(cn & kLow), base_d = (int)(cd & kLow);
+    for (int x = threadIdx.x; x < s_tot_n; x += blockDim.x) {
+      int l = 0, h = kPlanTile - 1;  // last slot whose item base is <= x
+      while (l < h) {
+        const int mid = (l + h + 1) >> 1;
+        if (s_nb[mid] <= x) l = mid;
+        else h = mid - 1;
+      }
+      while (l > 0 && (s_w[l].kind != 1 || s_nb[l] + s_w[l].n <= x)) --l;
+      const KeyWork& k = s_w[l];
+      const int i = x - s_nb[l];
+      int e0, ne;
+      long long pre, cost;
+      normal_item(k, P, i, &e0, &ne, &pre, &cost);
+      const long long p = s_nc[l] + pre;
+      const int item = base_n + x;
+      sc.items[item] = make_int4(k.key, k.begin + e0, ne, 0);
+      sc.cost_prefix[item] = p;
+      for (int c2 = boundaries_at_or_below(p, Cn, P.num_ctas), e = boundaries_at_or_below(p + cost, Cn, P.num_ctas);
+           c2 < e; ++c2)
+        sc.cta_ptr[c2] = item + 1;
+    }
+    for (int x = threadIdx.x; x < s_tot_d; x += blockDim.x) {
+      int l = 0, h = kPlanTile - 1;
+      while (l < h) {
+        const int mid = (l + h + 1) >> 1;
+        if (s_db[mid] <= x) l = mid;
+        else h = mid - 1;
+      }
+      while (l > 0 && (s_w[l].kind != 2 || s_db[l] + s_w[l].n <= x)) --l;
+      const KeyWork& k = s_w[l];
+      const int i = x - s_db[l];
+      int k0, nk;
+      long long pre, cost;
+      decode_item(k, P, i, &k0, &nk, &pre, &cost);
+      const long long p = s_dc[l] + pre;
+      const int item = base_d + x;
+      sc.items_dec[item] = make_int4(k.a + k0, k.begin + k0, 1, nk);
+      sc.cost_prefix_dec[item] = p;
+      for (int c2 = boundaries_at_or_below(p, Cd, P.num_ctas), e = boundaries_at_or_below(p + cost, Cd, P.num_ctas);
+           c2 < e; ++c2)
+        sc.cta_ptr_dec[c2] = item + 1;
+    }
+    __syncthreads();
+    ci += ti;
+    cn += tn;
+    cd += td;
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
+  __shared__ unsigned long long tmp[3 * 33];
+  __shared__ int32_t rowbuf[ixp::kMarkWarps][256];
+  pdl_launch_dependents();
+  const ixp::IndexArgs& ia = a.ia;
+  int* bar = ia.ix.hdr + kHdrBarCount;
+  int* flags = ia.ix.hdr + kHdrFlags;
+  const unsigned nb = gridDim.x;
+  ixp::SeqTotals tot;
+  if (ia.B <= kRedundantSeqMax) {
+    tot = ixp::phase_seq(ia.ix, ia.cu, ia.lens, ia.B, ia.total_q, ia.Hkv, ia.cap_len, ia.causal,
+                         reinterpret_cast<long long*>(tmp), blockIdx.x == 0);
+  } else {
+    if (blockIdx.x == 0)
+      ixp::phase_seq(ia.ix, ia.cu, ia.lens, ia.B, ia.total_q, ia.Hkv, ia.cap_len, ia.causal,
+                     reinterpret_cast<long long*>(tmp));
+    grid_barrier(bar, flags, nb);
+    tot = ixp::SeqTotals{ia.ix.hdr[kHdrNB], ia.ix.hdr[kHdrBMW], ia.ix.hdr[kHdrKMW]};
+  }
+  ixp::phase_token_seq(ia.ix, ia.cu, ia.B, ia.total_q);
+  ixp::phase_zero(ia.ix, ia.Hkv, tot);
+  grid_barrier(bar, flags, nb);
+  ixp::phase_mark(ia.ix, ia.sel, ia.total_q, ia.Hkv, ia.topk, ia.causal, rowbuf);
+  grid_barrier(bar, flags, nb);
+  plan_reduce(ia.ix, a.P, tmp);
+  grid_barrier(bar, flags, nb);
+  plan_scan_emit(ia.ix, a.sc, a.P, ia.Hkv, ia.topk, tmp);
+}
+
+}  // namespace
+
+int coop_grid(const void* kernel, int threads);
+
+cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
+                        const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas, cudaStream_t st) {
+  PlanArgs a;
+  a.ia = ixp::IndexArgs{ix, sel, cu, lens, p.num_seqs, p.total_q, p.num_kv_heads, p.topk,
+                        p.max_pages_per_seq * p.page_size, p.causal};
+  a.sc = sc;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  a.P.B = p.num_seqs;
+  a.P.Hkv = p.num_kv_heads;
+  a.P.G = G;
+  a.P.kvw = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
+  a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
+  a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
+  a.P.num_ctas = num_ctas;
+  const int grid = coop_grid(reinterpret_cast<const void*>(k_plan), kPlanThreads);
+  if (grid <= 0) return cudaErrorNotSupported;
+  cudaError_t e = cudaMemsetAsync(ix.hdr, 0, kHdrInts * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&a};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_plan), dim3(grid), dim3(kPlanThreads), args, 0,
+                                     st);
+}
+
+}  // namespace mxsa

@@ -22,7 +22,9 @@
 // Every per-key and per-item quantity has a closed form (item sizes take
 // two values, q = cnt / n and q + 1, and the first i items hold
 // floor(i * cnt / n) entries), so the work per key and per item is O(1).
-// One cooperative launch, two phases separated by a bounded grid barrier:
+// One cooperative launch, two phases separated by a bounded grid barrier
+// (the fused plan kernel in plan.cu computes the same schedule inside the
+// index build):
 //   reduce  the active keys are cut into one contiguous chunk per CTA; each
 //           CTA sums the item counts and costs of its chunk (both lists)
 //   scan    each CTA adds the sums of the chunks before it, scans its chunk
@@ -32,98 +34,14 @@
 //           partition rule above without a search
 #include <algorithm>
 
-#include "internal.h"
+#include "index_phases.cuh"
+#include "sched_common.cuh"
 
 namespace mxsa {
 
 namespace {
 
-constexpr int kItemBits = 26;  // payload: (cost << 26) | items
-constexpr int kSchThreads = 256;
-constexpr int kSchPerThread = 2;
-constexpr int kSchTile = kSchThreads * kSchPerThread;
-
-__device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    unsigned long long n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long block_excl_u64(unsigned long long v, unsigned long long* tmp,
-                                                             unsigned long long* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  unsigned long long inc = warp_incl_u64(v);
-  if (lane == 31) tmp[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long w = lane < nw ? tmp[lane] : 0ull;
-    unsigned long long wi = warp_incl_u64(w);
-    if (lane < nw) tmp[lane] = wi - w;
-    if (lane == nw - 1) tmp[32] = wi;
-  }
-  __syncthreads();
-  unsigned long long r = tmp[warp] + inc - v;
-  *total = tmp[32];
-  __syncthreads();
-  return r;
-}
-
-__device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (seq[mid].blk_off <= r) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
-struct Params {
-  int B, Hkv, G, kvw, per_tile, E, num_ctas;
-};
-
-// What one active key contributes.  kind 0: nothing (inside a decode run),
-// 1: a normal key, 2: the first key of a decode run.
-struct KeyWork {
-  int kind;
-  int a;      // active position
-  int key;    // normal: key id
-  int begin;  // normal: first entry
-  int cnt;    // normal: entries; decode: run length (keys)
-  int valid;  // normal: valid tokens of the block
-  int adj;    // decode: cost removed from the run's last item (partial last block)
-  int n;      // items
-  long long cost;
-};
-
-__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
-
-// exclusive cost prefix of item i within a normal key, and item i's cost
-__device__ __forceinline__ void normal_item(const KeyWork& k, const Params& P, int i, int* e0, int* ne,
-                                            long long* pre, long long* cost) {
-  const int q = k.cnt / k.n;
-  const long long fl = (long long)i * k.cnt / k.n, fl1 = (long long)(i + 1) * k.cnt / k.n;
-  const long long m = fl - (long long)i * q;  // items before i with q + 1 entries
-  const long long t_q = ceil_div(q, P.per_tile), t_q1 = ceil_div(q + 1, P.per_tile);
-  *e0 = (int)fl;
-  *ne = (int)(fl1 - fl);
-  *pre = (long long)i * k.valid * P.kvw + ((i - m) * t_q + m * t_q1) * 256 + fl * P.G * 2;
-  *cost = (long long)k.valid * P.kvw + (long long)ceil_div(*ne, P.per_tile) * 256 + (long long)(*ne) * P.G * 2;
-}
-
-__device__ __forceinline__ void decode_item(const KeyWork& k, const Params& P, int i, int* k0, int* nk,
-                                            long long* pre, long long* cost) {
-  const long long per_key = 64 + 128LL * P.kvw;
-  const int a0 = (int)((long long)i * k.cnt / k.n), a1 = (int)((long long)(i + 1) * k.cnt / k.n);
-  *k0 = a0;
-  *nk = a1 - a0;
-  *pre = (long long)a0 * per_key + (long long)i * 256;
-  *cost = (long long)(a1 - a0) * per_key + 256 - (i == k.n - 1 ? k.adj : 0);
-}
+using namespace sch;
 
 __device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const Params& P, int NB, int n_active, int a) {
   KeyWork w{};
@@ -156,24 +74,6 @@ __device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const Params& P
            ((long long)(w.n - rem) * ceil_div(q, P.per_tile) + (long long)rem * ceil_div(q + 1, P.per_tile)) * 256 +
            (long long)w.cnt * P.G * 2;
   return w;
-}
-
-__device__ __forceinline__ unsigned long long pack(long long cost, int n) {
-  return ((unsigned long long)cost << kItemBits) | (unsigned long long)n;
-}
-
-__device__ __forceinline__ void active_chunk(int n_active, int* lo, int* hi) {
-  const long long chunk = ((long long)n_active + gridDim.x - 1) / gridDim.x;
-  const long long a = (long long)blockIdx.x * chunk, b = a + chunk;
-  *lo = (int)(a < n_active ? a : n_active);
-  *hi = (int)(b < n_active ? b : n_active);
-}
-
-// number of boundaries c in [0, P] whose target floor(c * C / P) is <= x
-__device__ __forceinline__ int boundaries_at_or_below(long long x, long long C, int P) {
-  if (C <= 0) return P + 1;
-  const long long n = ((x + 1) * P - 1) / C + 1;
-  return (int)(n < P + 1 ? n : P + 1);
 }
 
 __device__ void phase_reduce(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P, unsigned long long* tmp) {
@@ -325,6 +225,7 @@ struct SchedArgs {
 
 __global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
   __shared__ unsigned long long tmp[33];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int* bar = a.sc.hdr + kSchBarCount;
   int* flags = a.ix.hdr + kHdrFlags;
   phase_reduce(a.ix, a.sc, a.P, tmp);
@@ -332,13 +233,13 @@ __global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
   phase_scan_emit(a.ix, a.sc, a.P, tmp);
 }
 
+
+
 }  // namespace
 
 int coop_grid(const void* kernel, int threads);
 
-cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc,
-                            const mxsa_sched_layout& lay, int num_ctas, cudaStream_t st) {
-  (void)lay;
+static SchedArgs sched_args(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas) {
   const int G = p.num_q_heads / p.num_kv_heads;
   SchedArgs a;
   a.ix = ix;
@@ -350,6 +251,13 @@ cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const Sc
   a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
   a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
   a.P.num_ctas = num_ctas;
+  return a;
+}
+
+cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc,
+                            const mxsa_sched_layout& lay, int num_ctas, cudaStream_t st) {
+  (void)lay;
+  SchedArgs a = sched_args(p, ix, sc, num_ctas);
   const int grid = coop_grid(reinterpret_cast<const void*>(k_schedule), kSchThreads);
   if (grid <= 0) return cudaErrorNotSupported;
   cudaError_t e = cudaMemsetAsync(sc.hdr, 0, kSchInts * sizeof(int32_t), st);

@@ -128,6 +128,13 @@ mxsa_status mxsa_build_index(const mxsa_problem* problem, const int32_t* sel, co
 mxsa_status mxsa_schedule(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
                           int32_t num_ctas, void* sched_ws, size_t sched_bytes, void* stream);
 
+/* Steps 1 and 2 in one launch: the same index and schedule as
+ * mxsa_build_index followed by mxsa_schedule (bit-identical workspaces),
+ * with one kernel launch instead of two.  Arguments as for those calls. */
+mxsa_status mxsa_plan(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
+                      const int32_t* used_kv_lens, void* index_ws, size_t index_bytes, int32_t num_ctas,
+                      void* sched_ws, size_t sched_bytes, void* stream);
+
 /* Step 3 -- KV-outer forward (the README's intro): every work item TMA-loads
  * its KV block (through block_tables) into shared memory once, gathers the
  * q rows of every (token, head) that selected it, and runs q k^T and p v on
@@ -167,7 +174,7 @@ mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device
  * active_keys: int32 [n_active], keys with entries in increasing order. */
 typedef struct {
   size_t header, seq_info, token_seq, slot_entry, bitmap, kmap, counts, row_ptr, entries, active_keys,
-      active_valid, row_nnz, cta_sums, total;
+      active_valid, row_nnz, row_minb, row_maxb, cta_sums, total;
   int64_t keys_cap, nslots, bitmap_words_cap, kmap_bytes_cap, tiles_cap;
 } mxsa_index_layout;
 mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layout* layout);

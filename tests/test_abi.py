@@ -57,7 +57,7 @@ def test_workspace_sizes_are_shape_upper_bounds(lib):
     S = mx.sched_layout(p)
     assert sb == S.total and S.items_cap == L.nslots
     offs = [L.header, L.seq_info, L.token_seq, L.slot_entry, L.bitmap, L.kmap, L.counts, L.row_ptr, L.entries,
-            L.active_keys, L.active_valid, L.row_nnz, L.cta_sums, L.total]
+            L.active_keys, L.active_valid, L.row_nnz, L.row_minb, L.row_maxb, L.cta_sums, L.total]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
 
 

@@ -147,6 +147,28 @@ def test_combine_with_oracle_partials():
     U.assert_close_lse(lse.cpu().numpy().T.reshape(-1), full_l, 1e-5, "combine lse")
 
 
+@pytest.mark.parametrize("name", ["fp8_varlen_small", "skewed_small", "edges"])
+def test_plan_equals_separate_index_and_schedule(name):
+    """mxsa_plan (one launch) leaves the same index and schedule as
+    mxsa_build_index followed by mxsa_schedule."""
+    import block_sparse_attention_builder_gb300 as mx
+    w = _edge_workload() if name == "edges" else SMALL[name]
+    inp = U.device_inputs(w)
+    prob = U.problem(w)
+    a = mx.SparseAttention(prob, "cuda")
+    b = mx.SparseAttention(prob, "cuda")
+    mx.plan(prob, inp["sel"], inp["cu"], inp["lens"], a.ws.index, a.ws.sched)
+    mx.build_index(prob, inp["sel"], inp["cu"], inp["lens"], b.ws.index)
+    mx.schedule(prob, b.ws.index, b.ws.sched)
+    torch.cuda.synchronize()
+    ia, ib = U.read_index(a), U.read_index(b)
+    for k in ia:
+        assert np.array_equal(np.asarray(ia[k]), np.asarray(ib[k])), k
+    sa, sb = U.read_sched(a, NUM_SMS), U.read_sched(b, NUM_SMS)
+    for k in sa:
+        assert np.array_equal(np.asarray(sa[k]), np.asarray(sb[k])), k
+
+
 @pytest.mark.parametrize("num_ctas", [1, 7, 300])
 def test_cta_count_does_not_change_result(num_ctas, small_runs):
     w = SMALL["prefill_small"]
