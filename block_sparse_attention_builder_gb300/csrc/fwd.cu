@@ -1,21 +1,28 @@
-// KV-outer forward (fw-ai/minimax-kernels README, intro: "loads a selected
-// KV block once and processes all queries that selected it").
+// KV-outer forward for KV-stationary work items (fw-ai/minimax-kernels
+// README, intro: "loads a selected KV block once and processes all queries
+// that selected it").  A work item is up to 4 tiles of 128 (entry, head)
+// rows of one key (kv head, sequence, block): the block's K and V pages are
+// TMA-loaded once per item and every tile of rows is multiplied against them.
 //
-// Persistent kernel, one CTA per SM, 192 threads:
-//   warps 0-3  softmax warpgroup: gathers the q rows of a tile into shared
-//              memory, turns S = q k^T (TMEM) into P = exp(S - m) (shared
-//              memory), and writes o = (P v) / l and lse per row; for FP8
-//              caches it also widens the staged e4m3 block to BF16/FP16.
-//   warp 4     TMA producer: decodes the work item (key -> kv head,
-//              sequence, block), walks the block table and loads the 1-2
-//              pages of K and V of the block into a double-buffered stage.
-//   warp 5     TMEM owner and MMA issuer (tcgen05.mma, cta_group::1,
-//              M = N = 128, K = 16 per instruction, FP32 accumulate):
-//              S = Q K^T into TMEM columns [0,128), O = P V into [128,256).
-//
-// Rows of a tile are (entry, head) pairs: up to 128 / G consecutive entries
-// of the item's key, each contributing its G query heads.  Row r of the
-// tile is TMEM lane r and is owned by softmax thread r.
+// Persistent kernel, one CTA per SM, 320 threads:
+//   warps 0-3, 4-7  two softmax warpgroups; the CTA's tiles alternate
+//              between them (tile j -> warpgroup j % 2) so that one group's
+//              softmax overlaps the other group's MMAs, loads and stores.
+//              Per tile a group gathers the tile's q rows into its buffer,
+//              turns S = q k^T (TMEM) into P = exp(S - m) written over the q
+//              rows (q is no longer needed once q k^T has run), and after
+//              O = P v writes o = O / l and lse per row.  Row r of a tile is
+//              thread r of its group and TMEM lane r.  For FP8 caches
+//              warpgroup n % 2 widens the staged e4m3 block of the CTA's
+//              n-th item to BF16/FP16 in the stage (exactly), whether or
+//              not it owns a tile of that item.
+//   warp 8     producer: decodes items (key -> kv head, sequence, block),
+//              walks the block table and TMA-loads the block's K and V pages
+//              into a double-buffered stage (FP8: into a staging tile).
+//   warp 9     TMEM owner (512 columns: S and O of each group) and MMA
+//              issuer (tcgen05.mma, cta_group::1, M = N = 128, K = 16 per
+//              instruction, FP32 accumulate), issuing q k^T of tile j + 1
+//              before p v of tile j.
 //
 // Shared-memory operands use the 128-byte swizzled K-major layout (q, K, P)
 // and the 128-byte swizzled MN-major layout (V as the B operand of P V).
@@ -34,16 +41,20 @@ namespace mxsa {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTileBytes = 32768;  // 128 rows x 128 x 16-bit
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
 
 struct ItemInfo {
-  int32_t g, s, b, valid, e0, n, L, tq, q_begin, absent, pad0, pad1, pad2, pad3, pad4, pad5;
+  int32_t g, s, b, valid, e0, n, L, tq, q_begin, pad0, pad1, pad2, pad3, pad4, pad5, pad6;
 };
 
 struct Ctrl {
-  uint64_t kv_full[2], kv_empty[2], stg_full, stg_empty, q_full, s_full, p_full, o_full, done;
+  // stg_full[n % 2]: item n staged.  One barrier per widening group, so
+  // that each group waits for every phase of its own barrier in order.
+  uint64_t kv_full[2], kv_empty[2], stg_full[2], stg_empty, q_full[2], s_full[2], p_full[2], o_full[2], done;
   uint32_t tmem_base;
   int32_t abort_flag;
   ItemInfo info[2];
@@ -66,12 +77,11 @@ struct FwdArgs {
 };
 
 // smem offsets from the 1024-aligned base
-constexpr uint32_t kOffKV = 0;                             // 2 stages x (K, V)
-constexpr uint32_t kOffQ = 2 * kStageBytes;                // 131072
-constexpr uint32_t kOffP = kOffQ + kTileBytes;             // 163840
-constexpr uint32_t kOffStg = kOffP + kTileBytes;           // 196608 (FP8 staging, 32 KB)
-constexpr uint32_t kCtrlBf16 = kOffStg;                    // control block without staging
-constexpr uint32_t kCtrlFp8 = kOffStg + kTileBytes;        // 229376
+constexpr uint32_t kOffKV = 0;                            // 2 stages x (K, V)
+constexpr uint32_t kOffQP = 2 * kStageBytes;              // 2 groups x (q, then p) tile
+constexpr uint32_t kOffStg = kOffQP + 2 * kTileBytes;     // FP8 staging (K, V e4m3), 32 KB
+constexpr uint32_t kCtrlBf16 = kOffStg;
+constexpr uint32_t kCtrlFp8 = kOffStg + kTileBytes;
 
 __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
   int lo = 0, hi = B - 1;
@@ -108,6 +118,25 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
   return pack2(f.x, f.y, 1);     // exact: e4m3 values are representable in bf16
 }
 
+// named barrier (id 1 + group) over the 128 threads of one softmax group
+__device__ __forceinline__ bool group_all(bool v, int grp) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + grp)
+      : "memory");
+  return r != 0;
+}
+
+// Per-row state a group keeps from a tile's softmax to its epilogue.
+struct RowState {
+  size_t orow;
+  float m2, l;
+  int live;  // row holds an (entry, head) pair
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -125,22 +154,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (it_begin >= it_end) return;  // uniform: nothing to do, nothing allocated
 
   if (tid == 0) {
-    mbar_init(&c.kv_full[0], a.kv_fp8 ? 128 : 1);
-    mbar_init(&c.kv_full[1], a.kv_fp8 ? 128 : 1);
-    mbar_init(&c.kv_empty[0], 1);
-    mbar_init(&c.kv_empty[1], 1);
-    mbar_init(&c.stg_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.kv_full[i], a.kv_fp8 ? 128 : 1);  // FP8: the widening group arrives
+      mbar_init(&c.kv_empty[i], 1);
+      mbar_init(&c.q_full[i], 128);
+      mbar_init(&c.s_full[i], 1);
+      mbar_init(&c.p_full[i], 128);
+      mbar_init(&c.o_full[i], 1);
+      mbar_init(&c.stg_full[i], 1);
+    }
     mbar_init(&c.stg_empty, 128);
-    mbar_init(&c.q_full, 128);
-    mbar_init(&c.s_full, 1);
-    mbar_init(&c.p_full, 128);
-    mbar_init(&c.o_full, 1);
     mbar_init(&c.done, 1);
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(&c.tmem_base, 256);
+  if (warp == kMmaWarp) {
+    tmem_alloc(&c.tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -149,14 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = c.tmem_base;
   volatile int* abort_flag = &c.abort_flag;
   const uint32_t sbase = smem_u32(sm);
+  const int per_tile = a.per_tile;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       const int NB = a.idx_hdr[kHdrNB];
       const int ps = a.page_size;
+      const int npg = ps == 128 ? 1 : 2;
       int n = 0;
       bool ok = true;
       for (int it = it_begin; it < it_end && ok; ++it, ++n) {
@@ -172,33 +203,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int valid = min(128, si.L - 128 * b);
         // physical pages of the block (1 for 128-token pages, 1-2 for 64)
         int pages[2] = {-1, -1};
-        int absent = 0;
-        const int npg = ps == 128 ? 1 : 2;
         for (int pg = 0; pg < npg; ++pg) {
-          const bool needed = pg * 64 < valid;
-          if (!needed) {
-            absent |= 1 << pg;
-            continue;
-          }
+          if (pg * 64 >= valid) continue;
           const int lp = ps == 128 ? b : 2 * b + pg;
           const int phys = a.block_tables[(size_t)s * a.max_pages + lp];
           if (phys < 0 || phys >= a.num_pages) {
             atomicOr(a.flags, MXSA_FLAG_PAGE);
-            absent |= 1 << pg;
             continue;
           }
           pages[pg] = phys;
         }
         ItemInfo inf;
         inf.g = g; inf.s = s; inf.b = b; inf.valid = valid; inf.e0 = itm.y; inf.n = itm.z;
-        inf.L = si.L; inf.tq = si.tq; inf.q_begin = si.q_begin; inf.absent = absent;
+        inf.L = si.L; inf.tq = si.tq; inf.q_begin = si.q_begin;
         c.info[st] = inf;
         const int present = (pages[0] >= 0) + (pages[1] >= 0);
         if (!a.kv_fp8) {
-          const uint32_t bytes = (uint32_t)present * (uint32_t)ps * 512u;  // K+V, both halves
           uint8_t* kdst = sm + kOffKV + st * kStageBytes;
           uint8_t* vdst = kdst + kTileBytes;
-          mbar_arrive_expect_tx(&c.kv_full[st], bytes);
+          mbar_arrive_expect_tx(&c.kv_full[st], (uint32_t)present * (uint32_t)ps * 512u);
           for (int pg = 0; pg < npg; ++pg) {
             if (pages[pg] < 0) continue;
             const int z = pages[pg] * a.Hkv + g;
@@ -208,227 +231,253 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
+          // FP8: into the staging tile once the previous block was widened
+          // out of it (stg_empty); the widening group fills the stage
           ok = mbar_wait(&c.stg_empty, (n & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
-          const uint32_t bytes = (uint32_t)present * (uint32_t)ps * 256u;
           uint8_t* stg = sm + kOffStg;
-          mbar_arrive_expect_tx(&c.stg_full, bytes);
+          uint64_t* sf = &c.stg_full[st];
+          mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
           for (int pg = 0; pg < npg; ++pg) {
             if (pages[pg] < 0) continue;
             const int z = pages[pg] * a.Hkv + g;
-            tma_load_3d(stg + pg * 8192, &tmk, &c.stg_full, 0, 0, z);
-            tma_load_3d(stg + 16384 + pg * 8192, &tmv, &c.stg_full, 0, 0, z);
+            tma_load_3d(stg + pg * 8192, &tmk, sf, 0, 0, z);
+            tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
           }
         }
       }
-      // drain: wait until every load this thread issued has landed
-      for (int k = std::max(0, n - 2); k < n; ++k) {
-        if (a.kv_fp8) {
-          if (k == n - 1) mbar_wait(&c.stg_full, k & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        } else {
-          mbar_wait(&c.kv_full[k & 1], (k >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        }
+      // drain: every load this thread issued has landed before the CTA may
+      // exit (FP8: staging item n - 1 needed item n - 2 widened, so landed)
+      if (!a.kv_fp8) {
+        for (int k = std::max(0, n - 2); k < n; ++k)
+          mbar_drain(&c.kv_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+      } else if (n > 0) {
+        mbar_drain(&c.stg_full[(n - 1) & 1], ((n - 1) >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 0);
       const uint32_t id_pv = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 1);
-      const uint32_t tS = tmem, tO = tmem + 128;
-      const uint32_t q_s = sbase + kOffQ, p_s = sbase + kOffP;
-      int n = 0;
-      uint32_t tile_ctr = 0;
+      int n = 0, j = 0;
       bool ok = true;
+      // the tile whose P V is still to be issued: index, stage, last of its item
+      int pj = -1, pst = 0, plast = 0;
+      auto issue_pv = [&]() -> bool {
+        const int w = pj & 1;
+        if (!mbar_wait(&c.p_full[w], (pj >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs))
+          return false;
+        tc_fence_after();
+        const uint32_t p_s = sbase + kOffQP + w * kTileBytes;
+        const uint32_t v_s = sbase + kOffKV + pst * kStageBytes + kTileBytes;
+        const uint32_t tO = tmem + w * 256 + 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
+          mma_f16_ss(tO, smem_desc_sw128(p_s + off, 0, 1024), smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), id_pv,
+                     ks > 0);
+        }
+        mma_commit(&c.o_full[w]);
+        if (plast) mma_commit(&c.kv_empty[pst]);
+        pj = -1;
+        return true;
+      };
       for (int it = it_begin; it < it_end && ok; ++it, ++n) {
         const int st = n & 1, use = n >> 1;
         ok = mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        const int n_entries = c.info[st].n;
-        const int ntiles = (n_entries + a.per_tile - 1) / a.per_tile;
-        const uint32_t k_s = sbase + kOffKV + st * kStageBytes, v_s = k_s + kTileBytes;
-        for (int j = 0; j < ntiles; ++j, ++tile_ctr) {
-          ok = mbar_wait(&c.q_full, tile_ctr & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        const int ntiles = (c.info[st].n + per_tile - 1) / per_tile;
+        const uint32_t k_s = sbase + kOffKV + st * kStageBytes;
+        for (int t = 0; t < ntiles && ok; ++t, ++j) {
+          const int w = j & 1;
+          ok = mbar_wait(&c.q_full[w], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t q_s = sbase + kOffQP + w * kTileBytes;
+          const uint32_t tS = tmem + w * 256;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
-            mma_f16_ss(tS, smem_desc_sw128(q_s + off, 0, 1024), smem_desc_sw128(k_s + off, 0, 1024), id_qk,
-                       ks > 0);
+            mma_f16_ss(tS, smem_desc_sw128(q_s + off, 0, 1024), smem_desc_sw128(k_s + off, 0, 1024), id_qk, ks > 0);
           }
-          mma_commit(&c.s_full);
-          ok = mbar_wait(&c.p_full, tile_ctr & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
-            mma_f16_ss(tO, smem_desc_sw128(p_s + off, 0, 1024),
-                       smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), id_pv, ks > 0);
-          }
-          mma_commit(&c.o_full);
+          mma_commit(&c.s_full[w]);
+          if (pj >= 0) ok = issue_pv();
+          pj = j;
+          pst = st;
+          plast = t == ntiles - 1;
         }
-        mma_commit(&c.kv_empty[st]);
       }
+      if (ok && pj >= 0) issue_pv();
       // drain: all MMAs issued by this thread complete before TMEM is freed
       mma_commit(&c.done);
-      mbar_wait(&c.done, 0, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+      mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
   } else {
-    // ------------------------------------------------------ softmax group
-    const int r = tid;  // tile row == TMEM lane
-    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------ softmax groups
+    const int grp = warp >> 2;     // 0 or 1
+    const int r = tid & 127;       // tile row == TMEM lane
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + grp * 256 + lane_addr, tO = tS + 128;
+    const uint32_t qp = sbase + kOffQP + grp * kTileBytes;
     const int bf16 = a.ab_bf16;
-    int n = 0;
-    uint32_t tile_ctr = 0;
+    int n = 0, j = 0;
     bool ok = true;
+    RowState pend{0, -INFINITY, 0.f, 0};
+    int pend_j = -1;
+    // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l) ln 2
+    auto epilogue = [&]() {
+      const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
+      float4* dst = reinterpret_cast<float4*>(a.part_o + pend.orow * 128);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        float ov[32];
+        tmem_ld32(tO + cb * 32, ov);
+        tmem_ld_wait();
+        if (pend.live) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[cb * 8 + i] =
+                make_float4(ov[4 * i] * inv_l, ov[4 * i + 1] * inv_l, ov[4 * i + 2] * inv_l, ov[4 * i + 3] * inv_l);
+        }
+      }
+      if (pend.live)
+        a.part_lse[pend.orow] = pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY;
+      tc_fence_before();
+    };
     for (int it = it_begin; it < it_end && ok; ++it, ++n) {
       const int st = n & 1, use = n >> 1;
-      uint8_t* kst = sm + kOffKV + st * kStageBytes;
-      uint8_t* vst = kst + kTileBytes;
-      ItemInfo inf;
-      if (a.kv_fp8) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&c.stg_full, n & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                                                kWaitLimitNs));
+      const int ntiles = (a.items[it].z + per_tile - 1) / per_tile;
+      if (a.kv_fp8 && st == grp) {
+        // widen the staged e4m3 block (row r of K and V) into the stage;
+        // rows past the valid tokens become zero.  The producer staged this
+        // block only after kv_empty of the stage, so the stage is free.
+        ok = group_all(mbar_wait(&c.stg_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
+                       grp);
         if (!ok) break;
-        inf = c.info[st];
-        // widen row r of the staged K and V (e4m3, 128 B per row) into the
-        // swizzled 16-bit operand tiles; rows past the valid tokens become 0
+        const int valid = c.info[st].valid;
         const uint8_t* stg = sm + kOffStg;
         for (int kv = 0; kv < 2; ++kv) {
           const uint8_t* src = stg + kv * 16384 + r * 128;
-          uint8_t* dst = kv ? vst : kst;
+          const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
+#pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const int c8 = (cc + r) & 7;  // rotate to spread banks
             uint4 raw = make_uint4(0, 0, 0, 0);
-            if (r < inf.valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            uint32_t o[8];
+            if (r < valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
+            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t o8[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              o[2 * i] = widen_e4m3x2((uint16_t)(w[i] & 0xffffu), bf16);
-              o[2 * i + 1] = widen_e4m3x2((uint16_t)(w[i] >> 16), bf16);
+              o8[2 * i] = widen_e4m3x2((uint16_t)(w4[i] & 0xffffu), bf16);
+              o8[2 * i + 1] = widen_e4m3x2((uint16_t)(w4[i] >> 16), bf16);
             }
-            // 16 fp8 -> 16 x 16-bit = chunks 2*c8 and 2*c8+1 of the row
-            st_shared_v4(smem_u32(dst) + swz(r, 2 * c8), o[0], o[1], o[2], o[3]);
-            st_shared_v4(smem_u32(dst) + swz(r, 2 * c8 + 1), o[4], o[5], o[6], o[7]);
+            st_shared_v4(dst + swz(r, 2 * c8), o8[0], o8[1], o8[2], o8[3]);
+            st_shared_v4(dst + swz(r, 2 * c8 + 1), o8[4], o8[5], o8[6], o8[7]);
           }
         }
         fence_proxy_async_smem();
         mbar_arrive(&c.stg_empty);
         mbar_arrive(&c.kv_full[st]);
-      } else {
-        ok = __all_sync(0xffffffffu, mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags,
-                                                MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-        if (!ok) break;
-        inf = c.info[st];
-        if (r >= inf.valid) {
-          // keys past the sequence end (or of a skipped page) must not carry
-          // stale values into P V: zero row r of V
-          for (int ch = 0; ch < 16; ++ch) st_shared_v4(smem_u32(vst) + swz(r, ch), 0, 0, 0, 0);
-        }
       }
-      const int ntiles = (inf.n + a.per_tile - 1) / a.per_tile;
-      for (int j = 0; j < ntiles; ++j, ++tile_ctr) {
-        const int et0 = inf.e0 + j * a.per_tile;
-        const int ne = min(a.per_tile, inf.n - j * a.per_tile);
+      for (int t = 0; t < ntiles && ok; ++t, ++j) {
+        if ((j & 1) != grp) continue;
+        ok = group_all(mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
+        if (!ok) break;
+        const ItemInfo inf = c.info[st];
+        // this group's buffer is free once its previous tile's P V is done
+        if (pend_j >= 0) {
+          ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                   kWaitLimitNs),
+                         grp);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // ---- gather this tile's q rows (loads first, then the previous
+        // tile's epilogue, then the shared-memory stores)
+        const int et0 = inf.e0 + t * per_tile;
+        const int ne = min(per_tile, inf.n - t * per_tile);
         const int rows = ne * a.G;
-        // ---- gather q rows into the swizzled Q tile
         int lim = 0;
         size_t orow = 0;
+        uint4 v[16];
         if (r < rows) {
           const int e = et0 + r / a.G, hh = r % a.G;
           const int slot = a.entries[e];
-          const int t = slot / (a.Hkv * a.topk);
+          const int tok = slot / (a.Hkv * a.topk);
           const int h = inf.g * a.G + hh;
-          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)t * a.Hq + h) * 256);
-          uint4 v[16];
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)tok * a.Hq + h) * 256);
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) v[ch] = __ldg(src + ch);
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) st_shared_v4(sbase + kOffQ + swz(r, ch), v[ch].x, v[ch].y, v[ch].z, v[ch].w);
-          const int pos = inf.L - inf.tq + (t - inf.q_begin);
+          const int pos = inf.L - inf.tq + (tok - inf.q_begin);
           lim = inf.valid;
           if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
           orow = (size_t)e * a.G + hh;
         } else {
 #pragma unroll
-          for (int ch = 0; ch < 16; ++ch) st_shared_v4(sbase + kOffQ + swz(r, ch), 0, 0, 0, 0);
+          for (int ch = 0; ch < 16; ++ch) v[ch] = make_uint4(0, 0, 0, 0);
+        }
+        if (pend_j >= 0) epilogue();
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) st_shared_v4(qp + swz(r, ch), v[ch].x, v[ch].y, v[ch].z, v[ch].w);
+        if (t == 0 && !a.kv_fp8 && r >= inf.valid) {
+          // keys past the sequence end must not bring stale values into P V
+          const uint32_t vs = sbase + kOffKV + st * kStageBytes + kTileBytes;
+          for (int ch = 0; ch < 16; ++ch) st_shared_v4(vs + swz(r, ch), 0, 0, 0, 0);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&c.q_full);
+        mbar_arrive(&c.q_full[grp]);
         // ---- softmax of the row
-        ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full, tile_ctr & 1, abort_flag, a.flags,
-                                                MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        ok = group_all(mbar_wait(&c.s_full[grp], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
+                       grp);
         if (!ok) break;
         tc_fence_after();
         float m2 = -INFINITY, l = 0.f;
-        if (warp * 32 < rows) {
+        {
           float sv[128];
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb) tmem_ld32(tmem + lane_addr + cb * 32, sv + cb * 32);
+          for (int cb = 0; cb < 4; ++cb) tmem_ld32(tS + cb * 32, sv + cb * 32);
           tmem_ld_wait();
-          if (r < rows) {
-            float m = -INFINITY;
+          float m = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < 128; ++k)
-              if (k < lim) m = fmaxf(m, sv[k]);
-            m2 = m * a.scale_log2;
+          for (int k = 0; k < 128; ++k)
+            if (k < lim) m = fmaxf(m, sv[k]);
+          m2 = m * a.scale_log2;
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-              uint32_t pk[4];
+          for (int ch = 0; ch < 16; ++ch) {
+            uint32_t pk[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int k0 = ch * 8 + 2 * i;
-                const float p0 = k0 < lim ? ex2_approx(fmaf(sv[k0], a.scale_log2, -m2)) : 0.f;
-                const float p1 = k0 + 1 < lim ? ex2_approx(fmaf(sv[k0 + 1], a.scale_log2, -m2)) : 0.f;
-                l += p0 + p1;
-                pk[i] = pack2(p0, p1, bf16);
-              }
-              st_shared_v4(sbase + kOffP + swz(r, ch), pk[0], pk[1], pk[2], pk[3]);
+            for (int i = 0; i < 4; ++i) {
+              const int k0 = ch * 8 + 2 * i;
+              const float p0 = k0 < lim ? ex2_approx(fmaf(sv[k0], a.scale_log2, -m2)) : 0.f;
+              const float p1 = k0 + 1 < lim ? ex2_approx(fmaf(sv[k0 + 1], a.scale_log2, -m2)) : 0.f;
+              l += p0 + p1;
+              pk[i] = pack2(p0, p1, bf16);
             }
+            st_shared_v4(qp + swz(r, ch), pk[0], pk[1], pk[2], pk[3]);
           }
-        }
-        if (r >= rows) {
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) st_shared_v4(sbase + kOffP + swz(r, ch), 0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&c.p_full);
-        // ---- epilogue: o = O / l, lse = (m2 + log2 l) * ln 2
-        ok = __all_sync(0xffffffffu, mbar_wait(&c.o_full, tile_ctr & 1, abort_flag, a.flags,
-                                                MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-        if (!ok) break;
+        mbar_arrive(&c.p_full[grp]);
+        pend = RowState{orow, m2, l, r < rows ? 1 : 0};
+        pend_j = j;
+      }
+    }
+    if (ok && pend_j >= 0) {
+      ok = group_all(
+          mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
+      if (ok) {
         tc_fence_after();
-        if (warp * 32 < rows) {
-          // every indexed row has at least one key; l == 0 only on corrupt input
-          const float inv_l = l > 0.f ? 1.f / l : 0.f;
-          float4* dst = reinterpret_cast<float4*>(a.part_o + orow * 128);
-#pragma unroll
-          for (int cb = 0; cb < 4; ++cb) {
-            float ov[32];
-            tmem_ld32(tmem + lane_addr + 128 + cb * 32, ov);
-            tmem_ld_wait();
-            if (r < rows) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[cb * 8 + i] = make_float4(ov[4 * i] * inv_l, ov[4 * i + 1] * inv_l, ov[4 * i + 2] * inv_l,
-                                              ov[4 * i + 3] * inv_l);
-            }
-          }
-          if (r < rows) a.part_lse[orow] = l > 0.f ? (m2 + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
-        }
-        tc_fence_before();
+        epilogue();
       }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 256);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

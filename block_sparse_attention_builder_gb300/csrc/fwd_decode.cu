@@ -335,14 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain the loads in flight before the CTA may exit
       for (int k = std::max(0, blk - ns); k < blk; ++k) {
         if (a.kv_fp8) {
-          if (k == blk - 1) mbar_wait(&c.stg_full, k & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          if (k == blk - 1) mbar_drain(&c.stg_full, k & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         } else {
-          mbar_wait(&c.kv_full[k % ns], (k / ns) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          mbar_drain(&c.kv_full[k % ns], (k / ns) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         }
       }
       if (n_it > 0)
-        mbar_wait(&c.q_full[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                  kWaitLimitNs);
+        mbar_drain(&c.q_full[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------- MMA issuer
@@ -399,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         blk += nk;
       }
       mma_commit(&c.done);
-      mbar_wait(&c.done, 0, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+      mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------ softmax group

@@ -73,6 +73,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait that ignores the abort flag, for the drains before a CTA
+// exits: TMA copies and MMAs this thread issued complete on their own, so
+// their barriers are waited for even after another role gave up.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, int* status, int err_bit,
+                                           uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(status, err_bit);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
