@@ -89,12 +89,25 @@ constexpr int stages_for(int fp8) {
   return fp8 ? 2 : (N <= 32 ? 3 : 2);
 }
 
-__device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (seq[mid].blk_off <= r) lo = mid;
-    else hi = mid - 1;
+// One item's look-ups as the producer warp holds them: uniform fields, and
+// per lane j < nk the valid keys, physical pages and entry of block j.
+struct BlockDesc {
+  int nk, g, row0, valid, page0, page1, entry;
+};
+
+// Largest s with seq[s].blk_off <= r, found by the whole warp: each round
+// probes 32 evenly spaced sequences, so a batch of up to 1024 sequences
+// takes two dependent reads.
+__device__ __forceinline__ int warp_seq_of_block(const SeqInfo* seq, int B, int r, int lane) {
+  int lo = 0, hi = B;  // seq[lo].blk_off <= r always holds (blk_off[0] = 0)
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && seq[idx].blk_off <= r;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int last = m ? 31 - __clz((int)m) : 0;
+    lo += last * step;
+    hi = min(hi, lo + step);
   }
   return lo;
 }
@@ -259,79 +272,116 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NB = a.idx_hdr[kHdrNB];
 
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------- producer warp
+    // The whole warp looks an item's blocks up one item ahead (lane j:
+    // block j), so the dependent index reads (key, sequence, block table)
+    // never sit between a stage becoming free and its copy; lane 0 issues
+    // the TMA copies.
     if (lane == 0) {
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       tma_prefetch_desc(&tmq);
-      const int ps = a.page_size;
-      const int npg = ps == 128 ? 1 : 2;
-      int blk = 0, n_it = 0;
-      bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-        const int4 itm = a.items[it];
-        const int ib = n_it & 1, ui = n_it >> 1;
-        ok = mbar_wait(&c.q_empty[ib], (ui & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        if (!ok) break;
-        // q rows of the item's token: rows t*Hq + g*G .. + N (rows past G are
-        // padding; rows past the tensor end read as zero)
-        const int key0 = a.active[itm.x];
-        const int g = key0 / NB;
-        const int s = seq_of_block(a.seq, a.num_seqs, key0 - g * NB);
-        const int t = a.seq[s].q_begin;
-        const int row0 = t * a.Hq + g * a.G;
+    }
+    const int ps = a.page_size;
+    const int npg = ps == 128 ? 1 : 2;
+    const int G = a.G;
+    auto lookup = [&](int it) -> BlockDesc {
+      BlockDesc d;
+      const int4 itm = a.items[it];
+      d.nk = itm.w;
+      const int key = lane < itm.w ? a.active[itm.x + lane] : 0;
+      const int key0 = __shfl_sync(0xffffffffu, key, 0);
+      d.g = key0 / NB;
+      const int s = warp_seq_of_block(a.seq, a.num_seqs, key0 - d.g * NB, lane);
+      const SeqInfo si = a.seq[s];
+      d.row0 = si.q_begin * a.Hq + d.g * G;  // q rows t*Hq + g*G .. + N (past G: padding)
+      d.valid = 0;
+      d.page0 = -1;
+      d.page1 = -1;
+      d.entry = -1;
+      if (lane < itm.w) {
+        const int b = key - d.g * NB - si.blk_off;
+        d.valid = min(128, si.L - 128 * b);
+        for (int pg = 0; pg < npg; ++pg) {
+          if (pg * 64 >= d.valid) continue;
+          const int lp = ps == 128 ? b : 2 * b + pg;
+          const int phys = a.block_tables[(size_t)s * a.max_pages + lp];
+          if (phys < 0 || phys >= a.num_pages) {
+            atomicOr(a.flags, MXSA_FLAG_PAGE);
+            continue;
+          }
+          if (pg == 0) d.page0 = phys;
+          else d.page1 = phys;
+        }
+        if (lane > 0) d.entry = a.row_ptr[key];
+      }
+      return d;
+    };
+    BlockDesc cur = lookup(it_begin);
+    int blk = 0, n_it = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+      const int ib = n_it & 1, ui = n_it >> 1;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&c.q_empty[ib], (ui & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+      if (!ok) break;
+      if (lane == 0) {
         uint8_t* qdst = sm + L.q + ib * (N * 256);
         mbar_arrive_expect_tx(&c.q_full[ib], (uint32_t)N * 256u);
-        tma_load_2d(qdst, &tmq, &c.q_full[ib], 0, row0);
-        tma_load_2d(qdst + N * 128, &tmq, &c.q_full[ib], 64, row0);
-        for (int j = 0; j < itm.w && ok; ++j, ++blk) {
-          const int st = blk % ns, us = blk / ns;
-          ok = mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (!ok) break;
-          const int key = a.active[itm.x + j];
-          const int r = key - g * NB;
-          const SeqInfo si = a.seq[s];
-          const int b = r - si.blk_off;
-          const int valid = min(128, si.L - 128 * b);
-          int pages[2] = {-1, -1};
-          for (int pg = 0; pg < npg; ++pg) {
-            if (pg * 64 >= valid) continue;
-            const int lp = ps == 128 ? b : 2 * b + pg;
-            const int phys = a.block_tables[(size_t)s * a.max_pages + lp];
-            if (phys < 0 || phys >= a.num_pages) {
-              atomicOr(a.flags, MXSA_FLAG_PAGE);
-              continue;
-            }
-            pages[pg] = phys;
-          }
+        tma_load_2d(qdst, &tmq, &c.q_full[ib], 0, cur.row0);
+        tma_load_2d(qdst + N * 128, &tmq, &c.q_full[ib], 64, cur.row0);
+      }
+      BlockDesc nxt = cur;
+      for (int j = 0; j < cur.nk && ok; ++j, ++blk) {
+        const int st = blk % ns, us = blk / ns;
+        ok = __all_sync(0xffffffffu, mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags,
+                                               MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        if (ok && a.kv_fp8)
+          ok = __all_sync(0xffffffffu, mbar_wait(&c.stg_empty, (blk & 1) ^ 1, abort_flag, a.flags,
+                                                 MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        if (!ok) break;
+        const int valid = __shfl_sync(0xffffffffu, cur.valid, j);
+        const int pg0 = __shfl_sync(0xffffffffu, cur.page0, j);
+        const int pg1 = __shfl_sync(0xffffffffu, cur.page1, j);
+        if (lane == 0) {
           c.info[st].valid = valid;
-          const int present = (pages[0] >= 0) + (pages[1] >= 0);
+          const int pages[2] = {pg0, pg1};
+          const int present = (pg0 >= 0) + (pg1 >= 0);
           if (!a.kv_fp8) {
             uint8_t* kdst = sm + st * kStage;
             uint8_t* vdst = kdst + kKVTile;
             mbar_arrive_expect_tx(&c.kv_full[st], (uint32_t)present * (uint32_t)ps * 512u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
-              const int z = pages[pg] * a.Hkv + g;
+              const int z = pages[pg] * a.Hkv + cur.g;
               for (int h = 0; h < 2; ++h) {
                 tma_load_3d(kdst + h * 16384 + pg * 8192, &tmk, &c.kv_full[st], h * 64, 0, z);
                 tma_load_3d(vdst + h * 16384 + pg * 8192, &tmv, &c.kv_full[st], h * 64, 0, z);
               }
             }
           } else {
-            ok = mbar_wait(&c.stg_empty, (blk & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-            if (!ok) break;
             uint8_t* stg = sm + L.stg;
             mbar_arrive_expect_tx(&c.stg_full, (uint32_t)present * (uint32_t)ps * 256u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
-              const int z = pages[pg] * a.Hkv + g;
+              const int z = pages[pg] * a.Hkv + cur.g;
               tma_load_3d(stg + pg * 8192, &tmk, &c.stg_full, 0, 0, z);
               tma_load_3d(stg + 16384 + pg * 8192, &tmv, &c.stg_full, 0, 0, z);
             }
           }
         }
+        if (j == 0) {
+          // the next item's look-ups overlap this item's copies
+          if (it + 1 < it_end) nxt = lookup(it + 1);
+          // the other keys of this run carry no weight of their own (the
+          // run's merged partial sits at its first entry)
+          if (cur.entry >= 0)
+            for (int r = 0; r < G; ++r) a.part_lse[(size_t)cur.entry * G + r] = -INFINITY;
+        }
       }
+      cur = nxt;
+    }
+    if (lane == 0) {
       // drain the loads in flight before the CTA may exit
       for (int k = std::max(0, blk - ns); k < blk; ++k) {
         if (a.kv_fp8) {
@@ -348,135 +398,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(128, N, (uint32_t)a.ab_bf16, 0, 0);
       const uint32_t id_o = idesc_f16(128, N, (uint32_t)a.ab_bf16, 1, 0);
-      int blk = 0, n_it = 0;
-      bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-        const int nk = a.items[it].w;
-        const int ib = n_it & 1, ui = n_it >> 1;
-        const uint32_t q_s = sbase + L.q + ib * (N * 256);
-        const uint32_t tO = tmem + 2 * N + ib * N;
-        ok = mbar_wait(&c.q_full[ib], ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs) &&
-             mbar_wait(&c.o_empty[ib], (ui & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        if (!ok) break;
-        const int first = blk;
-        for (int j = 0; j <= nk && ok; ++j) {
-          if (j < nk) {  // S^T of block blk
-            const int st = (blk + j) % ns, us = (blk + j) / ns, sb = (blk + j) & 1;
-            ok = mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-            if (!ok) break;
+      // Two cursors over the CTA's blocks, each issued as soon as its inputs
+      // are there: S^T of block bs (its K landed; at an item start its q;
+      // the S buffer it reuses was read, i.e. bs <= bp + 1) and O^T += V^T P^T
+      // of block bp (its P written; at an item start the O buffer it reuses
+      // was read out).  P V of a block never waits for the next block's load,
+      // so a stage is released as soon as its block is consumed.
+      int its = it_begin, js = 0, ns_it = 0, nks = a.items[it_begin].w, bs = 0;
+      int itp = it_begin, jp = 0, np_it = 0, nkp = nks, bp = 0;
+      uint64_t t_last = globaltimer_ns();
+      while (itp < it_end) {
+        bool progressed = false;
+        if (its < it_end && bs <= bp + 1) {
+          const int ib = ns_it & 1, st = bs % ns;
+          if ((js > 0 || mbar_test(&c.q_full[ib], (ns_it >> 1) & 1)) && mbar_test(&c.kv_full[st], (bs / ns) & 1)) {
             tc_fence_after();
             const uint32_t k_s = sbase + st * kStage;
+            const uint32_t q_s = sbase + L.q + ib * (N * 256);
+            const uint32_t tS = tmem + (bs & 1) * N;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off_k = (ks >> 2) * 16384u + (ks & 3) * 32u;
               const uint32_t off_q = (ks >> 2) * (uint32_t)(N * 128) + (ks & 3) * 32u;
-              mma_f16_ss(tmem + sb * N, smem_desc_sw128(k_s + off_k, 0, 1024), smem_desc_sw128(q_s + off_q, 0, 1024),
-                         id_s, ks > 0);
+              mma_f16_ss(tS, smem_desc_sw128(k_s + off_k, 0, 1024), smem_desc_sw128(q_s + off_q, 0, 1024), id_s,
+                         ks > 0);
             }
-            mma_commit(&c.s_full[sb]);
-            if (j == nk - 1) mma_commit(&c.q_empty[ib]);
+            mma_commit(&c.s_full[bs & 1]);
+            ++bs;
+            if (++js == nks) {
+              mma_commit(&c.q_empty[ib]);
+              js = 0;
+              ++ns_it;
+              if (++its < it_end) nks = a.items[its].w;
+            }
+            progressed = true;
           }
-          if (j > 0) {  // O^T += V^T P^T of the previous block
-            const int pb = blk + j - 1;
-            const int st = pb % ns, sb = pb & 1, ub = pb >> 1;
-            ok = mbar_wait(&c.p_full[sb], ub & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-            if (!ok) break;
+        }
+        if (bp < bs) {
+          const int ib = np_it & 1, st = bp % ns, sb = bp & 1;
+          if (mbar_test(&c.p_full[sb], (bp >> 1) & 1) &&
+              (jp > 0 || mbar_test(&c.o_empty[ib], ((np_it >> 1) & 1) ^ 1))) {
             tc_fence_after();
             const uint32_t v_s = sbase + st * kStage + kKVTile;
             const uint32_t p_s = sbase + L.p + sb * (N * 256);
+            const uint32_t tO = tmem + 2 * N + ib * N;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off_p = (ks >> 2) * (uint32_t)(N * 128) + (ks & 3) * 32u;
               mma_f16_ss(tO, smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), smem_desc_sw128(p_s + off_p, 0, 1024),
-                         id_o, (pb != first || ks > 0) ? 1u : 0u);
+                         id_o, (jp > 0 || ks > 0) ? 1u : 0u);
             }
             mma_commit(&c.p_empty[sb]);
             mma_commit(&c.kv_empty[st]);
-            if (j == nk) mma_commit(&c.o_full[ib]);
+            ++bp;
+            if (++jp == nkp) {
+              mma_commit(&c.o_full[ib]);
+              jp = 0;
+              ++np_it;
+              if (++itp < it_end) nkp = a.items[itp].w;
+            }
+            progressed = true;
           }
         }
-        blk += nk;
+        if (progressed) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(a.flags, MXSA_FLAG_TIMEOUT);
+            break;
+          }
+        }
       }
       mma_commit(&c.done);
       mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------ softmax group
+    // Each thread waits on the barriers itself; the four warps vote once per
+    // block (an abort, or a score above the running maximum anywhere), so
+    // every named barrier below is reached by all 128 threads or by none.
     const int k = tid;  // key of S^T / head dim of O^T / TMEM lane
     const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
     const int bf16 = a.ab_bf16;
     const float c2 = a.scale_log2;
+    const int G = a.G;
+    const uint32_t kk = (uint32_t)(k & 63);
+    // byte offset of key k in row r of a [rows][keys] P^T tile: 128-byte
+    // swizzled K-major, two halves of 64 keys
+    const uint32_t p_key = (uint32_t)(k >> 6) * (uint32_t)(N * 128) + (kk & 7u) * 2u;
     int blk = 0, n_it = 0;
     bool ok = true;
     float m[N], lsum[N];
+    int4 itm_next = a.items[it_begin];
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
-      const int4 itm = a.items[it];
+      const int4 itm = itm_next;
+      if (it + 1 < it_end) itm_next = a.items[it + 1];  // its latency hides behind this item
       const int nk = itm.w;
       const int ib = n_it & 1, ui = n_it >> 1;
       const uint32_t tO = tmem + lane_addr + 2 * N + ib * N;
-      for (int j = 0; j < nk && ok; ++j, ++blk) {
+      for (int j = 0; j < nk; ++j, ++blk) {
         const int st = blk % ns, us = blk / ns, sb = blk & 1, ub = blk >> 1;
         uint8_t* kst = sm + st * kStage;
         uint8_t* vst = kst + kKVTile;
-        int valid;
+        int valid = 0;
+        bool okb;
         if (a.kv_fp8) {
-          ok = wg_all(mbar_wait(&c.stg_full, blk & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-          if (!ok) break;
-          valid = c.info[st].valid;
-          const uint8_t* stg = sm + L.stg;
-          for (int kv = 0; kv < 2; ++kv) {
-            const uint8_t* src = stg + kv * 16384 + k * 128;
-            const uint32_t dst = smem_u32(kv ? vst : kst);
-            for (int cc = 0; cc < 8; ++cc) {
-              const int c8 = (cc + k) & 7;
-              uint4 raw = make_uint4(0, 0, 0, 0);
-              if (k < valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
-              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-              uint32_t o[8];
+          okb = mbar_wait(&c.stg_full, blk & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          if (okb) {
+            valid = c.info[st].valid;
+            const uint8_t* stg = sm + L.stg;
+            for (int kv = 0; kv < 2; ++kv) {
+              const uint8_t* src = stg + kv * 16384 + k * 128;
+              const uint32_t dst = smem_u32(kv ? vst : kst);
+              for (int cc = 0; cc < 8; ++cc) {
+                const int c8 = (cc + k) & 7;
+                uint4 raw = make_uint4(0, 0, 0, 0);
+                if (k < valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t o[8];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                o[2 * i] = widen_e4m3x2((uint16_t)(w[i] & 0xffffu), bf16);
-                o[2 * i + 1] = widen_e4m3x2((uint16_t)(w[i] >> 16), bf16);
+                for (int i = 0; i < 4; ++i) {
+                  o[2 * i] = widen_e4m3x2((uint16_t)(w[i] & 0xffffu), bf16);
+                  o[2 * i + 1] = widen_e4m3x2((uint16_t)(w[i] >> 16), bf16);
+                }
+                st_shared_v4(dst + swz_kv(k, 2 * c8), o[0], o[1], o[2], o[3]);
+                st_shared_v4(dst + swz_kv(k, 2 * c8 + 1), o[4], o[5], o[6], o[7]);
               }
-              st_shared_v4(dst + swz_kv(k, 2 * c8), o[0], o[1], o[2], o[3]);
-              st_shared_v4(dst + swz_kv(k, 2 * c8 + 1), o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&c.stg_empty);
+            mbar_arrive(&c.kv_full[st]);
+          }
+        } else {
+          okb = mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          if (okb) {
+            valid = c.info[st].valid;
+            if (k >= valid) {
+              // keys past the sequence end must not bring stale values into P V
+              for (int ch = 0; ch < 16; ++ch) st_shared_v4(smem_u32(vst) + swz_kv(k, ch), 0, 0, 0, 0);
             }
           }
-          fence_proxy_async_smem();
-          mbar_arrive(&c.stg_empty);
-          mbar_arrive(&c.kv_full[st]);
-        } else {
-          ok = wg_all(mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-          if (!ok) break;
-          valid = c.info[st].valid;
-          if (k >= valid) {
-            // keys past the sequence end must not bring stale values into P V
-            for (int ch = 0; ch < 16; ++ch) st_shared_v4(smem_u32(vst) + swz_kv(k, ch), 0, 0, 0, 0);
-          }
         }
-        // ---- scores of key k for every row
-        ok = wg_all(mbar_wait(&c.s_full[sb], ub & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-        if (!ok) break;
-        tc_fence_after();
+        // ---- scores of key k for every row (tcgen05.ld is warp-collective)
+        okb = __all_sync(0xffffffffu,
+                         okb && mbar_wait(&c.s_full[sb], ub & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         float x[N];
-        tmem_ld_n<N>(tmem + lane_addr + sb * N, x);
-        tmem_ld_wait();
+        if (okb) {
+          tc_fence_after();
+          tmem_ld_n<N>(tmem + lane_addr + sb * N, x);
+          tmem_ld_wait();
+        }
 #pragma unroll
-        for (int r = 0; r < N; ++r) x[r] = (k < valid && r < a.G) ? x[r] * c2 : -INFINITY;
-        if (j == 0) {
-#pragma unroll
-          for (int r = 0; r < N; ++r) m[r] = x[r];
-          wg_reduce<N, true>(m, red);
-#pragma unroll
-          for (int r = 0; r < N; ++r) {
-            if (m[r] == -INFINITY) m[r] = 0.f;  // padding rows
-            lsum[r] = 0.f;
-          }
-        } else {
-          bool exceed = false;
+        for (int r = 0; r < N; ++r) x[r] = (okb && k < valid && r < G) ? x[r] * c2 : -INFINITY;
+        bool exceed = false;
+        if (j > 0) {
 #pragma unroll
           for (int r = 0; r < N; ++r) exceed |= x[r] > m[r] + kRescaleThreshold;
-          if (wg_any(exceed)) {
+        }
+        okb = okb && mbar_wait(&c.p_empty[sb], (ub & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        if (j == 0 || wg_any(exceed || !okb)) {
+          if (!wg_all(okb)) {
+            ok = false;
+            break;
+          }
+          if (j == 0) {
+#pragma unroll
+            for (int r = 0; r < N; ++r) m[r] = x[r];
+            wg_reduce<N, true>(m, red);
+#pragma unroll
+            for (int r = 0; r < N; ++r) {
+              if (m[r] == -INFINITY) m[r] = 0.f;  // padding rows
+              lsum[r] = 0.f;
+            }
+          } else {
             // raise m: wait until the previous P V finished, rescale O^T
             float mb[N];
 #pragma unroll
@@ -503,31 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // ---- P^T of key k into the [rows][keys] operand tile
-        ok = wg_all(mbar_wait(&c.p_empty[sb], (ub & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-        if (!ok) break;
-        float p[N];
+        const uint32_t pbuf = smem_u32(sm + L.p + sb * (N * 256)) + p_key;
 #pragma unroll
         for (int r = 0; r < N; ++r) {
-          p[r] = x[r] == -INFINITY ? 0.f : ex2_approx(x[r] - m[r]);
-          lsum[r] += p[r];
-        }
-        {
-          uint8_t* pbuf = sm + L.p + sb * (N * 256);
-          const uint32_t half = (uint32_t)(k >> 6) * (uint32_t)(N * 128);
-          const uint32_t kk = (uint32_t)(k & 63);
-          const bool odd = k & 1;
-#pragma unroll
-          for (int r = 0; r < N; ++r) {
-            const float other = __shfl_xor_sync(0xffffffffu, p[r], 1);
-            // even keys store rows 0,2,4,..; odd keys rows 1,3,5,..: one
-            // 4-byte pair (key & ~1, key | 1) per store
-            if ((r & 1) == (int)odd) {
-              const float lo = odd ? other : p[r], hi = odd ? p[r] : other;
-              const uint32_t kp = kk & ~1u;
-              const uint32_t off = half + (uint32_t)r * 128u + ((((kp >> 3) ^ (uint32_t)(r & 7)) << 4) | ((kp & 7u) * 2u));
-              *reinterpret_cast<uint32_t*>(pbuf + off) = pack2(lo, hi, bf16);
-            }
-          }
+          const float pr = x[r] == -INFINITY ? 0.f : ex2_approx(x[r] - m[r]);
+          lsum[r] += pr;
+          const uint16_t h = bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(pr)) : __half_as_ushort(__float2half_rn(pr));
+          st_shared_u16(pbuf + (uint32_t)r * 128u + (((kk >> 3) ^ (uint32_t)(r & 7)) << 4), h);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -535,21 +613,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue of the item: o = O / l, lse = (m + log2 l) ln 2
-      ok = wg_all(mbar_wait(&c.o_full[ib], ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-      if (!ok) break;
-      tc_fence_after();
+      bool oko = __all_sync(0xffffffffu,
+                            mbar_wait(&c.o_full[ib], ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
       float o[N];
-      tmem_ld_n<N>(tO, o);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&c.o_empty[ib]);
+      if (oko) {
+        tc_fence_after();
+        tmem_ld_n<N>(tO, o);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&c.o_empty[ib]);
+      }
+      ok = wg_all(oko);
+      if (!ok) break;
       wg_reduce<N, false>(lsum, red);
       const int e0 = itm.y;
-      const int G = a.G;
       float* dst = a.part_o + (size_t)e0 * G * 128 + k;
 #pragma unroll
       for (int r = 0; r < N; ++r)
-        if (r < G) dst[(size_t)r * 128] = lsum[r] > 0.f ? o[r] / lsum[r] : 0.f;
+        if (r < G) dst[(size_t)r * 128] = lsum[r] > 0.f ? o[r] * __frcp_rn(lsum[r]) : 0.f;
       if (k < G) {
         float lv = -INFINITY, mv = 0.f;
 #pragma unroll
@@ -559,12 +640,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mv = m[r];
           }
         a.part_lse[(size_t)e0 * G + k] = lv > 0.f ? (mv + lg2_approx(lv)) * 0.69314718055994530942f : -INFINITY;
-      }
-      // the other keys of the run carry no weight of their own
-      for (int idx = k; idx < (nk - 1) * G; idx += 128) {
-        const int jj = 1 + idx / G, rr = idx % G;
-        const int e = a.row_ptr[a.active[itm.x + jj]];
-        a.part_lse[(size_t)e * G + rr] = -INFINITY;
       }
     }
   }
