@@ -47,9 +47,46 @@ struct SeqTotals {
 
 // Sequence scan over the B sequences by one CTA.  Every CTA that runs it
 // gets the totals; only the writer stores seq_info, flags and the header.
+// Per-sequence facts a CTA keeps in shared memory (batches of up to
+// kSeqTab sequences): block offset, bitmap offset, kmap offset, first
+// token, clamped KV length and new tokens.  `find` maps a block row r to
+// its sequence (largest s with blk_off <= r) and `get` returns the
+// sequence's SeqInfo, from the table when it holds the batch, else from
+// global memory.
+constexpr int kSeqTab = 512;
+struct SeqTab {
+  const SeqInfo* g;
+  const int (*t)[kSeqTab];
+  int B;
+  __device__ __forceinline__ bool local() const { return t != nullptr; }
+  __device__ __forceinline__ int find(int r) const {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      const int off = local() ? t[0][mid] : g[mid].blk_off;
+      if (off <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  }
+  __device__ __forceinline__ SeqInfo get(int s) const {
+    if (!local()) return g[s];
+    SeqInfo si;
+    si.blk_off = t[0][s];
+    si.bm_off = t[1][s];
+    si.km_off = t[2][s];
+    si.q_begin = t[3][s];
+    si.L = t[4][s];
+    si.tq = t[5][s];
+    si.nblk = (si.L + 127) / 128;
+    si.words = (si.tq + 31) / 32;
+    return si;
+  }
+};
+
 __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_t* cu, const int32_t* lens, int B,
                                                int total_q, int Hkv, int cap_len, int causal, long long* tmp,
-                                               bool writer = true) {
+                                               bool writer = true, int (*tab)[kSeqTab] = nullptr) {
   __shared__ int cu_bad;
   long long carry_blk = 0, carry_bm = 0, carry_km = 0;
   int flags = 0;
@@ -84,6 +121,14 @@ __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_
     long long eb = block_exclusive_scan(nblk, tmp, &tb);
     long long ebm = block_exclusive_scan(bmw, tmp, &tbm);
     long long ekm = block_exclusive_scan(kmw, tmp, &tkm);
+    if (tab != nullptr && s < B && B <= kSeqTab) {
+      tab[0][s] = (int)(carry_blk + eb);
+      tab[1][s] = (int)(carry_bm + ebm);
+      tab[2][s] = (int)(carry_km + ekm);
+      tab[3][s] = q0;
+      tab[4][s] = L;
+      tab[5][s] = tq;
+    }
     if (s < B && writer) {
       SeqInfo si;
       si.L = L;
@@ -121,12 +166,14 @@ __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_
   return SeqTotals{carry_blk, carry_bm, carry_km};
 }
 
-__device__ __forceinline__ void phase_zero(const IndexPtrs& ix, int Hkv, const SeqTotals& tot) {
+__device__ __forceinline__ void phase_zero(const IndexPtrs& ix, int Hkv, const SeqTotals& tot,
+                                           bool zero_counts = true) {
   const long long n_keys = tot.nb * Hkv;
   const long long n_bm = tot.bmw * Hkv;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  for (long long i = tid; i < n_keys; i += stride) ix.counts[i] = 0;
+  if (zero_counts)
+    for (long long i = tid; i < n_keys; i += stride) ix.counts[i] = 0;
   for (long long i = tid; i < n_bm; i += stride) ix.bitmap[i] = 0u;
 }
 
@@ -147,8 +194,10 @@ __device__ __forceinline__ void phase_token_seq(const IndexPtrs& ix, const int64
 
 constexpr int kMarkWarps = 8;
 
+// count = false leaves counts alone (the caller derives them from the
+// bitmap rows), so popular blocks cost no contended atomics.
 __device__ __forceinline__ void phase_mark(const IndexPtrs& ix, const int32_t* sel, int total_q, int Hkv, int topk, int causal,
-                           int32_t (*rowbuf)[256]) {
+                           int32_t (*rowbuf)[256], bool count = true) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int NB = ix.hdr[kHdrNB];
   const size_t BMW = (size_t)ix.hdr[kHdrBMW], KMW = (size_t)ix.hdr[kHdrKMW];
@@ -183,7 +232,7 @@ __device__ __forceinline__ void phase_mark(const IndexPtrs& ix, const int32_t* s
       const size_t word = (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words + (i >> 5);
       atomicOr(&ix.bitmap[word], 1u << (i & 31));
       ix.kmap[(size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq + i] = (uint8_t)k;
-      atomicAdd(&ix.counts[(long long)g * NB + si.blk_off + b], 1);
+      if (count) atomicAdd(&ix.counts[(long long)g * NB + si.blk_off + b], 1);
       ++made;
       bmin = min(bmin, b);
       bmax = max(bmax, b);
@@ -393,18 +442,19 @@ struct IndexArgs {
 __device__ __forceinline__ void build_index_phases(const IndexArgs& a, unsigned long long* tmp,
                                                    int32_t (*rowbuf)[256]) {
   int* bar = a.ix.hdr + kHdrBarCount;
+  int epoch = 0;
   int* flags = a.ix.hdr + kHdrFlags;
   const unsigned nb = gridDim.x;
   if (blockIdx.x == 0)
     phase_seq(a.ix, a.cu, a.lens, a.B, a.total_q, a.Hkv, a.cap_len, a.causal, reinterpret_cast<long long*>(tmp));
   phase_token_seq(a.ix, a.cu, a.B, a.total_q);
-  grid_barrier(bar, flags, nb);
+  grid_barrier(bar, flags, nb, epoch);
   phase_zero(a.ix, a.Hkv, SeqTotals{a.ix.hdr[kHdrNB], a.ix.hdr[kHdrBMW], a.ix.hdr[kHdrKMW]});
-  grid_barrier(bar, flags, nb);
+  grid_barrier(bar, flags, nb, epoch);
   phase_mark(a.ix, a.sel, a.total_q, a.Hkv, a.topk, a.causal, rowbuf);
-  grid_barrier(bar, flags, nb);
+  grid_barrier(bar, flags, nb, epoch);
   phase_key_reduce(a.ix, tmp);
-  grid_barrier(bar, flags, nb);
+  grid_barrier(bar, flags, nb, epoch);
   phase_key_scan_emit(a.ix, a.B, a.Hkv, a.topk, tmp);
 }
 

@@ -23,7 +23,7 @@ enum : int {
   kHdrTileCtr = 7,   // dynamic tile counter of the key scan
   kHdrBarCount = 8,  // grid barrier: arrivals (cleared before each launch)
   kHdrAbort = 9,     // grid barrier: set when a barrier wait gave up
-  kHdrBarGen = 10,   // grid barrier: generation
+  kHdrReserved10 = 10,
   kHdrInts = 16
 };
 
@@ -39,7 +39,7 @@ enum : int {
   kSchDecCostHi = 7,
   kSchBarCount = 8,  // grid barrier (as in the index header)
   kSchAbort = 9,
-  kSchBarGen = 10,
+  kSchReserved10 = 10,
   kSchInts = 16
 };
 
@@ -170,30 +170,32 @@ __device__ __forceinline__ unsigned long long dev_globaltimer() {
 }
 
 // Grid-wide barrier for kernels launched cooperatively (all CTAs
-// co-resident).  bar[0] counts arrivals and must be 0 at launch, bar[1] is
-// the abort word (0 at launch), bar[2] the generation.  The wait is bounded:
-// past the limit it sets MXSA_FLAG_TIMEOUT and the abort word, and every
-// later barrier of the launch returns at once.
-__device__ __forceinline__ void grid_barrier(int* bar, int* flags, unsigned nblocks) {
+// co-resident).  bar[0] counts arrivals since the launch and must be 0 at
+// launch; the n-th barrier of a launch (n = ++epoch, the same in every CTA)
+// completes when it reaches n * nblocks, so no reset or generation word is
+// needed and the last arrival releases everyone.  bar[1] is the abort word
+// (0 at launch).  The wait is bounded: past the limit it sets
+// MXSA_FLAG_TIMEOUT and the abort word, and every later barrier of the
+// launch returns at once.
+__device__ __forceinline__ void grid_barrier(int* bar, int* flags, unsigned nblocks, int& epoch) {
   __syncthreads();
+  const int target = ++epoch * (int)nblocks;
   if (threadIdx.x == 0) {
-    volatile int* vgen = bar + 2;
     volatile int* vabort = bar + 1;
-    const int g = *vgen;
     __threadfence();
-    const int arrived = atomicAdd(bar, 1) + 1;
-    if (arrived == (int)nblocks) {
-      atomicExch(bar, 0);
-      __threadfence();
-      atomicAdd(bar + 2, 1);
-    } else {
+    int seen;
+    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], 1;" : "=r"(seen) : "l"(bar) : "memory");
+    if (seen + 1 < target) {
       const unsigned long long t0 = dev_globaltimer();
-      while (*vgen == g && !*vabort) {
+      while (true) {
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(bar) : "memory");
+        if (seen >= target || *vabort) break;
         if (dev_globaltimer() - t0 > kWaitLimitNs) {
           atomicOr(flags, MXSA_FLAG_TIMEOUT);
           atomicExch(bar + 1, 1);
           break;
         }
+        __nanosleep(64);
       }
     }
     __threadfence();

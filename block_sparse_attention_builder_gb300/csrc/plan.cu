@@ -43,13 +43,12 @@ struct PlanArgs {
   Params P;
 };
 
-// schedule contribution of key `key` with `c` entries (kind 0: none)
-__device__ __forceinline__ KeyWork plan_key_work(const IndexPtrs& ix, const Params& P, int NB, int key, int c) {
+// schedule contribution of key `key` (kv head g, block b of the sequence
+// si) with `c` entries (kind 0: none)
+__device__ __forceinline__ KeyWork plan_key_work(const IndexPtrs& ix, const Params& P, int key, int g,
+                                                 const SeqInfo& si, int b, int c) {
   KeyWork w{};
   if (c == 0) return w;
-  const int g = key / NB, r = key - g * NB;
-  const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
-  const int b = r - si.blk_off;
   if (P.G <= kDecodeMaxG && si.tq == 1) {
     const int row = si.q_begin * P.Hkv + g;
     if (b != ix.row_minb[row]) return w;  // not the first key of its run
@@ -76,15 +75,25 @@ __device__ __forceinline__ KeyWork plan_key_work(const IndexPtrs& ix, const Para
   return w;
 }
 
-__device__ __forceinline__ void plan_reduce(const IndexPtrs& ix, const Params& P, unsigned long long* tmp) {
+// reduce: each key's entry count is the population of its bitmap row (the
+// mark phase does not count), stored for the scan; then the three sums
+__device__ __forceinline__ void plan_reduce(const IndexPtrs& ix, const Params& P, const ixp::SeqTab& tab,
+                                            unsigned long long* tmp) {
   const int n_keys = ix.hdr[kHdrKeys], NB = ix.hdr[kHdrNB];
+  const size_t BMW = (size_t)ix.hdr[kHdrBMW];
   int lo, hi;
   ixp::key_chunk(n_keys, &lo, &hi);
   unsigned long long vi = 0, vn = 0, vd = 0;
   for (int k = lo + threadIdx.x; k < hi; k += blockDim.x) {
-    const int c = ix.counts[k];
+    const int g = k / NB, r = k - g * NB;
+    const SeqInfo si = tab.get(tab.find(r));
+    const int b = r - si.blk_off;
+    const uint32_t* row = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
+    int c = 0;
+    for (int w = 0; w < si.words; ++w) c += __popc(row[w]);
+    ix.counts[k] = c;
     vi += ixp::key_payload(c);
-    const KeyWork w = plan_key_work(ix, P, NB, k, c);
+    const KeyWork w = plan_key_work(ix, P, k, g, si, b, c);
     if (w.kind == 1) vn += pack(w.cost, w.n);
     if (w.kind == 2) vd += pack(w.cost, w.n);
   }
@@ -98,7 +107,7 @@ __device__ __forceinline__ void plan_reduce(const IndexPtrs& ix, const Params& P
 }
 
 __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P, int Hkv,
-                                               int topk, unsigned long long* tmp) {
+                                               int topk, const ixp::SeqTab& tab, unsigned long long* tmp) {
   __shared__ KeyWork s_w[kPlanTile];
   __shared__ int s_nb[kPlanTile], s_db[kPlanTile];
   __shared__ long long s_nc[kPlanTile], s_dc[kPlanTile];
@@ -156,7 +165,11 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
   for (int t0 = lo; t0 < hi; t0 += kPlanTile) {
     const int key = t0 + threadIdx.x;
     const int c = key < hi ? ix.counts[key] : 0;
-    KeyWork w = plan_key_work(ix, P, NB, key, c);
+    const int g = key / NB, r = key - g * NB;
+    SeqInfo si{};
+    if (c > 0) si = tab.get(tab.find(r));
+    const int b = r - si.blk_off;
+    KeyWork w = plan_key_work(ix, P, key, g, si, b, c);
     if (threadIdx.x == 0) s_n_long = 0;
     U3 tt;
     const U3 ex = block_excl_u64x3(U3{ixp::key_payload(c), w.kind == 1 ? pack(w.cost, w.n) : 0ull,
@@ -173,9 +186,6 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
         const int pos = (int)(run & kLow31);
         w.a = pos;
         ix.active[pos] = key;
-        const int g = key / NB, r = key - g * NB;
-        const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
-        const int b = r - si.blk_off;
         const int valid = si.L - 128 * b;
         ix.active_valid[pos] = valid < 128 ? valid : 128;
         if (si.words <= 2) {
@@ -203,7 +213,7 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
     for (int i = warp; i < s_n_long; i += n_warps) {
       const int k2 = s_long_key[i];
       const int g = k2 / NB, r = k2 - g * NB;
-      const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+      const SeqInfo si = tab.get(tab.find(r));
       const int b = r - si.blk_off;
       ixp::emit_row_warp(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
                          ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv,
@@ -262,30 +272,33 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
 __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   __shared__ unsigned long long tmp[3 * 33];
   __shared__ int32_t rowbuf[ixp::kMarkWarps][256];
+  __shared__ int s_tab[6][ixp::kSeqTab];
   pdl_launch_dependents();
   const ixp::IndexArgs& ia = a.ia;
   int* bar = ia.ix.hdr + kHdrBarCount;
+  int epoch = 0;
   int* flags = ia.ix.hdr + kHdrFlags;
   const unsigned nb = gridDim.x;
   ixp::SeqTotals tot;
   if (ia.B <= kRedundantSeqMax) {
     tot = ixp::phase_seq(ia.ix, ia.cu, ia.lens, ia.B, ia.total_q, ia.Hkv, ia.cap_len, ia.causal,
-                         reinterpret_cast<long long*>(tmp), blockIdx.x == 0);
+                         reinterpret_cast<long long*>(tmp), blockIdx.x == 0, s_tab);
   } else {
     if (blockIdx.x == 0)
       ixp::phase_seq(ia.ix, ia.cu, ia.lens, ia.B, ia.total_q, ia.Hkv, ia.cap_len, ia.causal,
                      reinterpret_cast<long long*>(tmp));
-    grid_barrier(bar, flags, nb);
+    grid_barrier(bar, flags, nb, epoch);
     tot = ixp::SeqTotals{ia.ix.hdr[kHdrNB], ia.ix.hdr[kHdrBMW], ia.ix.hdr[kHdrKMW]};
   }
   ixp::phase_token_seq(ia.ix, ia.cu, ia.B, ia.total_q);
-  ixp::phase_zero(ia.ix, ia.Hkv, tot);
-  grid_barrier(bar, flags, nb);
-  ixp::phase_mark(ia.ix, ia.sel, ia.total_q, ia.Hkv, ia.topk, ia.causal, rowbuf);
-  grid_barrier(bar, flags, nb);
-  plan_reduce(ia.ix, a.P, tmp);
-  grid_barrier(bar, flags, nb);
-  plan_scan_emit(ia.ix, a.sc, a.P, ia.Hkv, ia.topk, tmp);
+  ixp::phase_zero(ia.ix, ia.Hkv, tot, false);
+  grid_barrier(bar, flags, nb, epoch);
+  ixp::phase_mark(ia.ix, ia.sel, ia.total_q, ia.Hkv, ia.topk, ia.causal, rowbuf, false);
+  const ixp::SeqTab tab{ia.ix.seq, ia.B <= ixp::kSeqTab ? s_tab : nullptr, ia.B};
+  grid_barrier(bar, flags, nb, epoch);
+  plan_reduce(ia.ix, a.P, tab, tmp);
+  grid_barrier(bar, flags, nb, epoch);
+  plan_scan_emit(ia.ix, a.sc, a.P, ia.Hkv, ia.topk, tab, tmp);
 }
 
 }  // namespace

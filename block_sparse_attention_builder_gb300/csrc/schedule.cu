@@ -227,9 +227,10 @@ __global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
   __shared__ unsigned long long tmp[33];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int* bar = a.sc.hdr + kSchBarCount;
+  int epoch = 0;
   int* flags = a.ix.hdr + kHdrFlags;
   phase_reduce(a.ix, a.sc, a.P, tmp);
-  grid_barrier(bar, flags, gridDim.x);
+  grid_barrier(bar, flags, gridDim.x, epoch);
   phase_scan_emit(a.ix, a.sc, a.P, tmp);
 }
 
