@@ -130,12 +130,51 @@ __device__ __forceinline__ bool group_all(bool v, int grp) {
   return r != 0;
 }
 
-// Per-row state a group keeps from a tile's softmax to its epilogue.
+// Per-row state a group keeps from a tile's softmax to its epilogue.  The
+// rows of a tile are consecutive partial rows: row r is orow0 + r.
 struct RowState {
-  size_t orow;
+  size_t orow0;
   float m2, l;
-  int live;  // row holds an (entry, head) pair
+  int rows;  // rows of the tile that hold an (entry, head) pair
 };
+
+// P = exp2(S * scale_log2 - m2) of one row over 64 of the block's keys
+// (half h: keys 64h .. 64h + 63, S values in sv), packed to the MMA operand
+// type and written to the row's swizzled slots; returns the partial row sum.
+// kFull: every key is visible (no length or causal limit).
+template <bool kBf16, bool kFull>
+__device__ __forceinline__ float softmax_store_p(const float* sv, int h, float scale_log2, float m2, int lim,
+                                                 uint32_t qp, int r) {
+  float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+  for (int cl = 0; cl < 8; ++cl) {
+    const int ch = 8 * h + cl;
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int kl = cl * 8 + 2 * i, k0 = 64 * h + kl;
+      float p0 = ex2_approx(fmaf(sv[kl], scale_log2, -m2));
+      float p1 = ex2_approx(fmaf(sv[kl + 1], scale_log2, -m2));
+      if (!kFull) {
+        p0 = k0 < lim ? p0 : 0.f;
+        p1 = k0 + 1 < lim ? p1 : 0.f;
+      }
+      if (i == 0) l0 += p0 + p1;
+      if (i == 1) l1 += p0 + p1;
+      if (i == 2) l2 += p0 + p1;
+      if (i == 3) l3 += p0 + p1;
+      if (kBf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&h);
+      } else {
+        __half2 h = __floats2half2_rn(p0, p1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+    st_shared_v4(qp + swz(r, ch), pk[0], pk[1], pk[2], pk[3]);
+  }
+  return (l0 + l1) + (l2 + l3);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, FwdArgs a) {
@@ -324,26 +363,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bf16 = a.ab_bf16;
     int n = 0, j = 0;
     bool ok = true;
+    const int wl = tid & 31, wrow0 = (warp & 3) * 32;  // lane; the warp's first tile row
     RowState pend{0, -INFINITY, 0.f, 0};
     int pend_j = -1;
-    // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l) ln 2
+    // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l)
+    // ln 2.  Each 32-column slice goes through the warp's 4 KB of the group's
+    // (free) q/P buffer so that every store instruction writes four whole
+    // 128-byte row segments instead of 32 scattered 16-byte pieces.
     auto epilogue = [&]() {
       const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
-      float4* dst = reinterpret_cast<float4*>(a.part_o + pend.orow * 128);
+      const uint32_t stg = qp + (uint32_t)(warp & 3) * 4096u;
+      // a warp whose 32 rows are all padding has nothing to store
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 0; cb < 4 && wrow0 < pend.rows; ++cb) {
         float ov[32];
         tmem_ld32(tO + cb * 32, ov);
         tmem_ld_wait();
-        if (pend.live) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[cb * 8 + i] =
-                make_float4(ov[4 * i] * inv_l, ov[4 * i + 1] * inv_l, ov[4 * i + 2] * inv_l, ov[4 * i + 3] * inv_l);
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(stg + (uint32_t)wl * 128u + ((uint32_t)(c8 ^ (wl & 7)) << 4),
+                       __float_as_uint(ov[4 * c8] * inv_l), __float_as_uint(ov[4 * c8 + 1] * inv_l),
+                       __float_as_uint(ov[4 * c8 + 2] * inv_l), __float_as_uint(ov[4 * c8 + 3] * inv_l));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (wl >> 3), cc = wl & 7;
+          const uint4 val = ld_shared_v4(stg + (uint32_t)rr * 128u + ((uint32_t)(cc ^ (rr & 7)) << 4));
+          if (wrow0 + rr < pend.rows)
+            st_global_v4(a.part_o + (pend.orow0 + wrow0 + rr) * 128 + cb * 32 + cc * 4, val);
         }
+        __syncwarp();
       }
-      if (pend.live)
-        a.part_lse[pend.orow] = pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY;
+      if (r < pend.rows)
+        a.part_lse[pend.orow0 + r] =
+            pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY;
       tc_fence_before();
     };
     for (int it = it_begin; it < it_end && ok; ++it, ++n) {
@@ -399,28 +452,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et0 = inf.e0 + t * per_tile;
         const int ne = min(per_tile, inf.n - t * per_tile);
         const int rows = ne * a.G;
-        int lim = 0;
-        size_t orow = 0;
-        uint4 v[16];
+        // row r's q row (token, head) and key limit; -1: padding row
+        int lim = 0, qrow = -1;
         if (r < rows) {
           const int e = et0 + r / a.G, hh = r % a.G;
           const int slot = a.entries[e];
           const int tok = slot / (a.Hkv * a.topk);
-          const int h = inf.g * a.G + hh;
-          const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)tok * a.Hq + h) * 256);
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) v[ch] = __ldg(src + ch);
+          qrow = tok * a.Hq + inf.g * a.G + hh;
           const int pos = inf.L - inf.tq + (tok - inf.q_begin);
           lim = inf.valid;
           if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
-          orow = (size_t)e * a.G + hh;
-        } else {
+        }
+        // coalesced gather: in round i the two half-warps read whole 256-byte
+        // q rows (the warp's rows 2i and 2i + 1, one 16-byte chunk per lane)
+        uint4 v[16];
 #pragma unroll
-          for (int ch = 0; ch < 16; ++ch) v[ch] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i) {
+          const int src_row = __shfl_sync(0xffffffffu, qrow, 2 * i + (wl >> 4));
+          v[i] = src_row >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.q + (size_t)src_row * 256) + (wl & 15))
+                              : make_uint4(0, 0, 0, 0);
         }
         if (pend_j >= 0) epilogue();
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) st_shared_v4(qp + swz(r, ch), v[ch].x, v[ch].y, v[ch].z, v[ch].w);
+        for (int i = 0; i < 16; ++i)
+          st_shared_v4(qp + swz(wrow0 + 2 * i + (wl >> 4), wl & 15), v[i].x, v[i].y, v[i].z, v[i].w);
         if (t == 0 && !a.kv_fp8 && r >= inf.valid) {
           // keys past the sequence end must not bring stale values into P V
           const uint32_t vs = sbase + kOffKV + st * kStageBytes + kTileBytes;
@@ -435,33 +490,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float m2 = -INFINITY, l = 0.f;
         {
-          float sv[128];
+          // S is read from TMEM twice, 64 columns at a time (the maximum, then
+          // P), so that only 64 scores are live; four independent maxima and
+          // sums keep the dependency chains short
+          const bool full = __all_sync(0xffffffffu, lim >= 128);
+          // padding rows' P is never used (their output rows are not stored),
+          // so a warp of padding rows skips the softmax
+          const bool dead = wrow0 >= rows;
+          float m0 = -INFINITY, m1 = -INFINITY, m3 = -INFINITY, m4 = -INFINITY;
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb) tmem_ld32(tS + cb * 32, sv + cb * 32);
-          tmem_ld_wait();
-          float m = -INFINITY;
+          for (int h = 0; h < 2 && !dead; ++h) {
+            float sv[64];
+            tmem_ld32(tS + h * 64, sv);
+            tmem_ld32(tS + h * 64 + 32, sv + 32);
+            tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 128; ++k)
-            if (k < lim) m = fmaxf(m, sv[k]);
-          m2 = m * a.scale_log2;
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k0 = ch * 8 + 2 * i;
-              const float p0 = k0 < lim ? ex2_approx(fmaf(sv[k0], a.scale_log2, -m2)) : 0.f;
-              const float p1 = k0 + 1 < lim ? ex2_approx(fmaf(sv[k0 + 1], a.scale_log2, -m2)) : 0.f;
-              l += p0 + p1;
-              pk[i] = pack2(p0, p1, bf16);
+            for (int k = 0; k < 64; k += 4) {
+              const int kk = 64 * h + k;
+              m0 = fmaxf(m0, full || kk < lim ? sv[k] : -INFINITY);
+              m1 = fmaxf(m1, full || kk + 1 < lim ? sv[k + 1] : -INFINITY);
+              m3 = fmaxf(m3, full || kk + 2 < lim ? sv[k + 2] : -INFINITY);
+              m4 = fmaxf(m4, full || kk + 3 < lim ? sv[k + 3] : -INFINITY);
             }
-            st_shared_v4(qp + swz(r, ch), pk[0], pk[1], pk[2], pk[3]);
+          }
+          m2 = fmaxf(fmaxf(m0, m1), fmaxf(m3, m4)) * a.scale_log2;
+#pragma unroll
+          for (int h = 0; h < 2 && !dead; ++h) {
+            float sv[64];
+            tmem_ld32(tS + h * 64, sv);
+            tmem_ld32(tS + h * 64 + 32, sv + 32);
+            tmem_ld_wait();
+            if (bf16)
+              l += full ? softmax_store_p<true, true>(sv, h, a.scale_log2, m2, lim, qp, r)
+                        : softmax_store_p<true, false>(sv, h, a.scale_log2, m2, lim, qp, r);
+            else
+              l += full ? softmax_store_p<false, true>(sv, h, a.scale_log2, m2, lim, qp, r)
+                        : softmax_store_p<false, false>(sv, h, a.scale_log2, m2, lim, qp, r);
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&c.p_full[grp]);
-        pend = RowState{orow, m2, l, r < rows ? 1 : 0};
+        pend = RowState{(size_t)et0 * a.G, m2, l, rows};
         pend_j = j;
       }
     }
