@@ -130,6 +130,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over the ranks: a job of independent per-rank batches
+    takes as long as its slowest rank.  No-op for one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank_step: int, world: int, steps: int, total_ms: float) -> float:
+    """Tokens of all ranks per second, over the max-over-ranks time."""
+    return tokens_per_rank_step * world * steps / (total_ms / 1e3)
+
+
 # ------------------------------------------------------------- workload
 def load_workload(name: str, rank: int):
     from block_sparse_attention_builder_gb300 import workloads as W
@@ -338,14 +354,10 @@ def main():
         torch.distributed.barrier()
     per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(3)] for i in range(args.steps)])
     step_ms = per.sum(axis=1)
-    total_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(step_ms.sum()), world, dev)
     ms_per_step = total_ms / args.steps
     tokens_per_step = w.total_q
-    value = tokens_per_step * world * args.steps / (total_ms / 1e3)
+    value = whole_job_value(tokens_per_step, world, args.steps, total_ms)
     fwd_ms = float(per[:, 1].mean())
     peaks = measured_peaks()
 
@@ -377,11 +389,8 @@ def main():
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens_per_step * world * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = whole_job_value(tokens_per_step, world, args.steps, e2e_ms)
     assert torch.equal(h_out.to(dev), out)
 
     if rank == 0:

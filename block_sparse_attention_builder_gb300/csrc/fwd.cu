@@ -324,7 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int it = it_begin; it < it_end && ok; ++it, ++n) {
         const int st = n & 1, use = n >> 1;
-        ok = mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        // at an item boundary, the previous tile's p v goes first unless this
+        // item's block has already landed: it releases the previous stage,
+        // which the producer needs to load the item after this one
+        if (pj >= 0 && !mbar_test(&c.kv_full[st], use & 1)) ok = issue_pv();
+        ok = ok && mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
         const int ntiles = (c.info[st].n + per_tile - 1) / per_tile;

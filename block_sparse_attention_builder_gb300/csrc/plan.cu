@@ -69,9 +69,9 @@ __device__ __forceinline__ KeyWork plan_key_work(const IndexPtrs& ix, const Para
   w.valid = valid < 128 ? valid : 128;
   w.n = ceil_div(c, P.E);
   const int q = c / w.n, rem = c % w.n;
-  w.cost = (long long)w.n * w.valid * P.kvw +
+  w.cost = (long long)w.n * (kItemFixed + (long long)w.valid * P.kvw) +
            ((long long)(w.n - rem) * ceil_div(q, P.per_tile) + (long long)rem * ceil_div(q + 1, P.per_tile)) * 256 +
-           (long long)c * P.G * 2;
+           (long long)c * P.G * kRowCost;
   return w;
 }
 

@@ -117,6 +117,13 @@ struct KeyWork {
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // exclusive cost prefix of item i within a normal key, and item i's cost
+// Cost units where a 128-row tile costs 256: a normal item's fixed part
+// (its stage turnover: the block's load, and for FP8 its widening, before
+// its first tile) and the per-row part (gather, epilogue stores).  Chosen by
+// timing a mixed FP8 varlen batch over a sweep of both constants.
+constexpr long long kItemFixed = 384;
+constexpr long long kRowCost = 3;
+
 __device__ __forceinline__ void normal_item(const KeyWork& k, const Params& P, int i, int* e0, int* ne,
                                             long long* pre, long long* cost) {
   const int q = k.cnt / k.n;
@@ -125,8 +132,10 @@ __device__ __forceinline__ void normal_item(const KeyWork& k, const Params& P, i
   const long long t_q = ceil_div(q, P.per_tile), t_q1 = ceil_div(q + 1, P.per_tile);
   *e0 = (int)fl;
   *ne = (int)(fl1 - fl);
-  *pre = (long long)i * k.valid * P.kvw + ((i - m) * t_q + m * t_q1) * 256 + fl * P.G * 2;
-  *cost = (long long)k.valid * P.kvw + (long long)ceil_div(*ne, P.per_tile) * 256 + (long long)(*ne) * P.G * 2;
+  *pre = (long long)i * (kItemFixed + (long long)k.valid * P.kvw) + ((i - m) * t_q + m * t_q1) * 256 +
+         fl * P.G * kRowCost;
+  *cost = kItemFixed + (long long)k.valid * P.kvw + (long long)ceil_div(*ne, P.per_tile) * 256 +
+          (long long)(*ne) * P.G * kRowCost;
 }
 
 __device__ __forceinline__ void decode_item(const KeyWork& k, const Params& P, int i, int* k0, int* nk,

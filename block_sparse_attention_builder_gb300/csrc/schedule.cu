@@ -70,9 +70,9 @@ __device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const Params& P
   w.valid = ix.active_valid[a];
   w.n = ceil_div(w.cnt, P.E);
   const int q = w.cnt / w.n, rem = w.cnt % w.n;
-  w.cost = (long long)w.n * w.valid * P.kvw +
+  w.cost = (long long)w.n * (kItemFixed + (long long)w.valid * P.kvw) +
            ((long long)(w.n - rem) * ceil_div(q, P.per_tile) + (long long)rem * ceil_div(q + 1, P.per_tile)) * 256 +
-           (long long)w.cnt * P.G * 2;
+           (long long)w.cnt * P.G * kRowCost;
   return w;
 }
 

@@ -382,8 +382,9 @@ int oracle_build_index(const oracle_problem* p, const int32_t* sel, const int64_
  *   NORMAL: E = rows_per_item_tiles * max(1, 128 / G) entries per item;
  *     n = ceil(cnt / E) items, item i covering entries
  *     [row_ptr[key] + i*cnt/n, row_ptr[key] + (i+1)*cnt/n);
- *     cost = valid_tokens(key) * kv_weight + tiles * 256 + rows * 2 with
- *     tiles = ceil(entries / max(1, 128 / G)), rows = entries * G.
+ *     cost = 384 + valid_tokens(key) * kv_weight + tiles * 256 + rows * 3
+ *     with tiles = ceil(entries / max(1, 128 / G)), rows = entries * G
+ *     (the leading 384 is the item's fixed stage turnover).
  *   DECODE: a run is a maximal sequence of consecutive active keys with the
  *     same (g, s) (all hold the same single entry: the one token of s);
  *     a run of len keys becomes n = ceil(len / decode_blocks) items, item i
@@ -466,7 +467,7 @@ int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t*
         items_n[4 * nn + 2] = (int32_t)ne;
         items_n[4 * nn + 3] = 0;
         cost_n[nn] = Cn;
-        Cn += valid * kvw + ((ne + per_tile - 1) / per_tile) * 256 + ne * G * 2;
+        Cn += 384 + valid * kvw + ((ne + per_tile - 1) / per_tile) * 256 + ne * G * 3;
         ++nn;
       }
       continue;

@@ -419,10 +419,11 @@ def test_schedule_split_worked_example():
     idx = oracle.build_index(prob, sel, cu, np.array([100], np.int32))
     sch = oracle.schedule(prob, [100], cu, idx, 1, 16, 2)
     assert sch["items"][:, 1].tolist() == [0, 3, 6] and sch["items"][:, 2].tolist() == [3, 3, 4]
-    # cost = 100 tokens * 2 + 1 tile * 256 + rows * 2, rows = entries * 32:
-    # 200 + 256 + 192 = 648 (3 entries) and 200 + 256 + 256 = 712 (4 entries)
-    assert sch["cost_prefix"].tolist() == [0, 648, 1296, 2008]
-    # targets floor(c * 2008 / 2) = 0, 1004, 2008 -> items with prefix below them
+    # cost = 384 per item + 100 tokens * 2 + 1 tile * 256 + rows * 3, rows =
+    # entries * 32: 384 + 200 + 256 + 288 = 1128 (3 entries) and
+    # 384 + 200 + 256 + 384 = 1224 (4 entries)
+    assert sch["cost_prefix"].tolist() == [0, 1128, 2256, 3480]
+    # targets floor(c * 3480 / 2) = 0, 1740, 3480 -> items with prefix below them
     assert sch["cta_ptr"].tolist() == [0, 2, 3]
     assert len(sch["items_dec"]) == 0 and sch["cta_ptr_dec"].tolist() == [0, 0, 0]
 
