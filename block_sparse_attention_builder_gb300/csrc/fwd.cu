@@ -36,6 +36,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "fwd_decode.cuh"
 
 namespace mxsa {
 
@@ -176,21 +177,14 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
   return (l0 + l1) + (l2 + l3);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, FwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// Runs the CTA's KV-stationary items (all kThreads threads; 1024-aligned
+// shared memory `sm`; TMEM base `tmem` with 512 columns).
+__device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdArgs& a,
+                                                   uint8_t* sm, uint32_t tmem) {
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_launch_dependents();
-  pdl_wait();  // the schedule (and the previous forward) are complete
-
-  if (a.sch_hdr[kSchCtas] != (int)gridDim.x) {
-    if (tid == 0 && blockIdx.x == 0) atomicOr(a.flags, MXSA_FLAG_SCHEDULE);
-    return;
-  }
   const int it_begin = a.cta_ptr[blockIdx.x], it_end = a.cta_ptr[blockIdx.x + 1];
-  if (it_begin >= it_end) return;  // uniform: nothing to do, nothing allocated
+  if (it_begin >= it_end) return;  // uniform: nothing to do
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -207,14 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
-    tmem_alloc(&c.tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = c.tmem_base;
   volatile int* abort_flag = &c.abort_flag;
   const uint32_t sbase = smem_u32(sm);
   const int per_tile = a.per_tile;
@@ -551,27 +538,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
+// The forward: each CTA runs its decode items (decode_body, warps 0-5),
+// then its KV-stationary items (all warps), in one launch.  TMEM (512
+// columns) is allocated once for both phases.
+__global__ void __launch_bounds__(kThreads, 1)
+    k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+          const __grid_constant__ CUtensorMap tmq, FwdArgs a, dec::DecArgs d) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint32_t s_tmem;
+  const int warp = threadIdx.x >> 5;
+  pdl_launch_dependents();
+  pdl_wait();  // the schedule (and the previous step's combine) are complete
+  if (a.sch_hdr[kSchCtas] != (int)gridDim.x) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(a.flags, MXSA_FLAG_SCHEDULE);
+    return;
+  }
+  const int b = blockIdx.x;
+  const bool has_dec = d.cta_ptr != nullptr && d.cta_ptr[b] < d.cta_ptr[b + 1];
+  const bool has_kvs = a.cta_ptr[b] < a.cta_ptr[b + 1];
+  if (!has_dec && !has_kvs) return;  // uniform: nothing to do, nothing allocated
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  if (has_dec) dec::decode_body<16>(tmk, tmv, tmq, d, sm, tmem);
+  if (has_kvs) kv_stationary_body(tmk, tmv, a, sm, tmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // 3-D view of a cache [pages * Hkv][page_size][128]: box = one page, one
 // 128-byte column slab (64 x 16-bit, swizzled) or the full 128 e4m3 row.
 bool make_cache_map(CUtensorMap* m, const void* base, const mxsa_problem& p) {
-  auto fn = encode_fn();
+  auto fn = dec::encode_fn();
   if (!fn) return false;
   const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
   const cuuint64_t es = fp8 ? 1 : 2;
@@ -590,7 +598,10 @@ bool make_cache_map(CUtensorMap* m, const void* base, const mxsa_problem& p) {
 
 }  // namespace
 
-size_t fwd_smem_bytes(bool fp8) { return (fp8 ? kCtrlFp8 : kCtrlBf16) + sizeof(Ctrl) + 1024; }
+// dynamic shared memory of the forward: the larger of its two phases' needs
+size_t fwd_smem_bytes(bool fp8) {
+  return std::max((size_t)(fp8 ? kCtrlFp8 : kCtrlBf16) + sizeof(Ctrl) + 1024, dec::smem_bytes(fp8));
+}
 
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
@@ -600,11 +611,13 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
     *err_detail = 1;
     return cudaErrorInvalidValue;
   }
-  // decode work items (runs of single-token keys) first, then the
-  // KV-stationary items; each kernel's CTAs without items exit at once
-  cudaError_t de = launch_fwd_decode(p, q, tmk, tmv, block_tables, ix, sc, num_ctas, part_o, part_lse, st,
-                                     err_detail);
-  if (de != cudaSuccess) return de;
+  // one launch for both work lists (decode runs, KV-stationary tiles)
+  dec::DecArgs d;
+  CUtensorMap tmq;
+  if (!dec::make_args(p, q, block_tables, ix, sc, part_o, part_lse, &d, &tmq)) {
+    *err_detail = 1;
+    return cudaErrorInvalidValue;
+  }
   const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
   const size_t smem = fwd_smem_bytes(fp8);
   static std::once_flag once;
@@ -640,7 +653,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, a);
+  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, a, d);
 }
 
 }  // namespace mxsa

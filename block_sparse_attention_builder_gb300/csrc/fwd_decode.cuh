@@ -15,15 +15,20 @@
 // score exceeds it by more than 2^8 (then O^T and the per-thread sums are
 // rescaled), so most blocks need no cross-thread reduction.
 //
-// Persistent kernel, 192 threads: warps 0-3 softmax/epilogue (and FP8
-// widening), warp 4 TMA producer (q rows of the item; K and V pages of each
-// block into a 2-3 stage ring), warp 5 TMEM owner and MMA issuer.
+// The decode phase of the forward kernel (fwd.cu), run by each CTA on its
+// decode items before its KV-stationary items: warps 0-3 softmax/epilogue
+// (and FP8 widening), warp 4 TMA producer (q rows of the item; K and V pages
+// of each block into a 2-3 stage ring), warp 5 MMA issuer; the kernel's
+// other warps idle through this phase.  TMEM columns [0, 64) of the CTA's
+// allocation hold S^T and O^T.
+#pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -31,9 +36,8 @@
 
 namespace mxsa {
 
-namespace {
+namespace dec {
 
-constexpr int kThreads = 192;
 constexpr uint32_t kKVTile = 32768;  // 128 keys x 128 x 16-bit
 constexpr uint32_t kStage = 2 * kKVTile;
 constexpr int kMaxStages = 3;
@@ -217,28 +221,21 @@ __device__ __forceinline__ void wg_reduce(float* v, float* red) {
   wg_sync();
 }
 
+// Runs the CTA's decode items (called by all of the kernel's threads, with
+// 1024-aligned shared memory `sm` and the CTA's TMEM base `tmem`).  On
+// return every copy and MMA of the phase has completed and its mbarriers are
+// invalidated, so the shared memory is free for the next phase.
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_fwd_dec(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-              const __grid_constant__ CUtensorMap tmq, DecArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                                            const DecArgs& a, uint8_t* sm, uint32_t tmem) {
   const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + L.ctrl);
   float* red = reinterpret_cast<float*>(sm + L.red);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ns = a.ns;
-  pdl_launch_dependents();
-  pdl_wait();  // the schedule (and the previous forward) are complete
-
-  if (a.sch_hdr[kSchCtas] != (int)gridDim.x) {
-    if (tid == 0 && blockIdx.x == 0) atomicOr(a.flags, MXSA_FLAG_SCHEDULE);
-    return;
-  }
   const int it_begin = a.cta_ptr[blockIdx.x], it_end = a.cta_ptr[blockIdx.x + 1];
-  if (it_begin >= it_end) return;  // uniform: nothing to do, nothing allocated
+  if (it_begin >= it_end) return;  // uniform: nothing to do
 
-  constexpr uint32_t kTmemCols = N <= 8 ? 32 : (N == 16 ? 64 : (N == 32 ? 128 : 256));
   if (tid == 0) {
     for (int i = 0; i < ns; ++i) {
       mbar_init(&c.kv_full[i], a.kv_fp8 ? 128 : 1);
@@ -259,14 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(&c.tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = c.tmem_base;
   volatile int* abort_flag = &c.abort_flag;
   const uint32_t sbase = smem_u32(sm);
   const int NB = a.idx_hdr[kHdrNB];
@@ -474,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&c.done);
       mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------ softmax group
     // Each thread waits on the barriers itself; the four warps vote once per
     // block (an abort, or a score above the running maximum anywhere), so
@@ -646,10 +636,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0) {  // every barrier this phase initialised
+    for (int i = 0; i < ns; ++i) {
+      mbar_inval(&c.kv_full[i]);
+      mbar_inval(&c.kv_empty[i]);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_inval(&c.q_full[i]);
+      mbar_inval(&c.q_empty[i]);
+      mbar_inval(&c.s_full[i]);
+      mbar_inval(&c.p_full[i]);
+      mbar_inval(&c.p_empty[i]);
+      mbar_inval(&c.o_full[i]);
+      mbar_inval(&c.o_empty[i]);
+    }
+    mbar_inval(&c.stg_full);
+    mbar_inval(&c.stg_empty);
+    mbar_inval(&c.done);
+  }
+  __syncthreads();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -663,7 +671,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_q_map(CUtensorMap* m, const void* q, const mxsa_problem& p, int n_rows_box) {
+inline bool make_q_map(CUtensorMap* m, const void* q, const mxsa_problem& p, int n_rows_box) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {128, (cuuint64_t)p.total_q * p.num_q_heads};
@@ -676,61 +684,49 @@ bool make_q_map(CUtensorMap* m, const void* q, const mxsa_problem& p, int n_rows
          CUDA_SUCCESS;
 }
 
-template <int N>
-cudaError_t launch_n(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq, DecArgs a,
-                     int num_ctas, cudaStream_t st) {
-  a.ns = stages_for<N>(a.kv_fp8);
-  const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
-  const size_t smem = L.total + 1024;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    const Layout l16 = smem_layout<N>(stages_for<N>(0), 0), l8 = smem_layout<N>(stages_for<N>(1), 1);
-    attr_err = cudaFuncSetAttribute(k_fwd_dec<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(std::max(l16.total, l8.total) + 1024));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  return launch_pdl(k_fwd_dec<N>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, a);
-}
-
-}  // namespace
-
-cudaError_t launch_fwd_decode(const mxsa_problem& p, const void* q, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                              const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
-                              float* part_o, float* part_lse, cudaStream_t st, int* err_detail) {
-  const int G = p.num_q_heads / p.num_kv_heads;
-  if (G > kDecodeMaxG || p.total_q == 0) return cudaSuccess;  // no decode items exist
+// Smallest dynamic shared memory (plus 1024 for alignment) the decode
+// phase needs for the cache dtype.
+inline size_t smem_bytes(bool fp8) {
   constexpr int N = 16;
-  CUtensorMap tmq;
-  if (!make_q_map(&tmq, q, p, N)) {
-    *err_detail = 1;
-    return cudaErrorInvalidValue;
-  }
-  DecArgs a;
-  a.block_tables = block_tables;
-  a.seq = ix.seq;
-  a.active = ix.active;
-  a.row_ptr = ix.row_ptr;
-  a.items = sc.items_dec;
-  a.cta_ptr = sc.cta_ptr_dec;
-  a.idx_hdr = ix.hdr;
-  a.sch_hdr = sc.hdr;
-  a.part_o = part_o;
-  a.part_lse = part_lse;
-  a.flags = ix.hdr + kHdrFlags;
-  a.num_seqs = p.num_seqs;
-  a.Hq = p.num_q_heads;
-  a.Hkv = p.num_kv_heads;
-  a.G = G;
-  a.page_size = p.page_size;
-  a.max_pages = p.max_pages_per_seq;
-  a.num_pages = p.num_pages;
-  a.kv_fp8 = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 0;
-  a.ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
-  a.ns = 0;
-  const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
-  a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_n<N>(tmk, tmv, tmq, a, num_ctas, st);
+  return smem_layout<N>(stages_for<N>(fp8 ? 1 : 0), fp8 ? 1 : 0).total + 1024;
 }
+
+// Fills the decode phase's arguments and its q tensor map; false when the
+// tensor map cannot be made.
+inline bool make_args(const mxsa_problem& p, const void* q, const int32_t* block_tables, const IndexPtrs& ix,
+                      const SchedPtrs& sc, float* part_o, float* part_lse, DecArgs* a, CUtensorMap* tmq) {
+  constexpr int N = 16;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  *a = DecArgs{};
+  std::memset(tmq, 0, sizeof(*tmq));
+  if (G > kDecodeMaxG || p.total_q == 0) return true;  // no decode item can exist: phase off (cta_ptr null)
+  if (!make_q_map(tmq, q, p, N)) return false;
+  a->block_tables = block_tables;
+  a->seq = ix.seq;
+  a->active = ix.active;
+  a->row_ptr = ix.row_ptr;
+  a->items = sc.items_dec;
+  a->cta_ptr = sc.cta_ptr_dec;
+  a->idx_hdr = ix.hdr;
+  a->sch_hdr = sc.hdr;
+  a->part_o = part_o;
+  a->part_lse = part_lse;
+  a->flags = ix.hdr + kHdrFlags;
+  a->num_seqs = p.num_seqs;
+  a->Hq = p.num_q_heads;
+  a->Hkv = p.num_kv_heads;
+  a->G = G;
+  a->page_size = p.page_size;
+  a->max_pages = p.max_pages_per_seq;
+  a->num_pages = p.num_pages;
+  a->kv_fp8 = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 0;
+  a->ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
+  a->ns = stages_for<N>(a->kv_fp8);
+  const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
+  a->scale_log2 = scale * 1.4426950408889634f;
+  return true;
+}
+
+}  // namespace dec
 
 }  // namespace mxsa

@@ -117,10 +117,6 @@ cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const Sc
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
                        float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
-// decode work list (merged single-token runs), launched by launch_fwd
-cudaError_t launch_fwd_decode(const mxsa_problem& p, const void* q, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                              const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
-                              float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
 cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
                            const float* part_lse, void* out, float* lse, cudaStream_t st);
 
