@@ -269,7 +269,270 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
   }
 }
 
-__global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
+// ------------------------------------------------------------------------
+// All-decode batches (every sequence has at most one new token, G <= 16):
+// every selected key then holds exactly one entry, so entries, active keys
+// and decode runs all follow the (kv head, sequence) rows in key order and
+// the whole plan needs one grid barrier.  The result is the same index and
+// schedule as the general phases.
+//
+//   A  one warp per row (g, s) of the CTA's share: validate the row's
+//      selections (range, duplicates), rank the distinct blocks, park the
+//      ranked (block, slot) list in the row's own slot_entry range, and sum
+//      entries, decode items and cost per CTA               -> barrier
+//   B  CTA prefixes; per row: slot_entry, entries, active keys, row_ptr of
+//      every key of the row, and the row's decode items with their cost
+//      prefixes and CTA boundaries.
+constexpr int kFastRowsChunk = kPlanThreads;
+
+__device__ __forceinline__ void fast_rows(int n_rows, int* r0, int* r1) {
+  *r0 = (int)((long long)blockIdx.x * n_rows / gridDim.x);
+  *r1 = (int)((long long)(blockIdx.x + 1) * n_rows / gridDim.x);
+}
+
+// adj of a decode run: cost removed for the unread tail of a partial last block
+__device__ __forceinline__ int fast_adj(const SeqInfo& si, int bmax, int kvw) {
+  if (bmax < 0 || bmax != si.nblk - 1) return 0;
+  const int v_last = si.L - 128 * bmax;
+  return v_last < 128 ? (128 - v_last) * kvw : 0;
+}
+
+__device__ __forceinline__ void fast_phase_a(const IndexPtrs& ix, const int32_t* sel, const Params& P,
+                                             const ixp::SeqTab& tab, int topk, int32_t (*rowbuf)[256],
+                                             unsigned long long* tmp) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int n_rows = P.Hkv * P.B;
+  int r0, r1;
+  fast_rows(n_rows, &r0, &r1);
+  const long long per_key = 64 + 128LL * P.kvw;
+  unsigned long long se = 0, sit = 0, scost = 0;
+  int flags = 0;
+  for (int R = r0 + w; R < r1; R += nw) {
+    const int g = R / P.B, s = R - g * P.B;
+    const SeqInfo si = tab.get(s);
+    if (si.tq != 1) continue;  // uniform per warp
+    const int row = si.q_begin * P.Hkv + g;
+    const long long base_slot = (long long)row * topk;
+    for (int k = lane; k < topk; k += 32) rowbuf[w][k] = sel[base_slot + k];
+    __syncwarp();
+    // validity of each slot: a block of the sequence, not repeated earlier
+    // in the row (the first occurrence is kept)
+    bool ok[8];
+    int nv = 0, bmax = -1;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = lane + 32 * u;
+      ok[u] = false;
+      if (k >= topk) continue;
+      const int b = rowbuf[w][k];
+      if (b == -1) continue;
+      if (b < -1 || b >= si.nblk) {
+        flags |= MXSA_FLAG_SEL_RANGE;
+        continue;
+      }
+      bool dup = false;
+      for (int k2 = 0; k2 < k; ++k2) dup |= rowbuf[w][k2] == b;
+      if (dup) {
+        flags |= MXSA_FLAG_SEL_DUP;
+        continue;
+      }
+      ok[u] = true;
+      ++nv;
+      bmax = max(bmax, b);
+    }
+    __syncwarp();
+    // invalid slots out of the ranking
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = lane + 32 * u;
+      if (k < topk && !ok[u]) rowbuf[w][k] = 0x7fffffff;
+    }
+    __syncwarp();
+    // rank = distinct valid blocks below: the row's blocks in ascending order
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = lane + 32 * u;
+      if (k >= topk || !ok[u]) continue;
+      const int b = rowbuf[w][k];
+      int rank = 0;
+      for (int k2 = 0; k2 < topk; ++k2) rank += rowbuf[w][k2] < b;
+      ix.slot_entry[base_slot + rank] = (b << 8) | k;
+    }
+    const int nnz = __reduce_add_sync(0xffffffffu, nv);
+    bmax = __reduce_max_sync(0xffffffffu, bmax);
+    if (lane == 0) {
+      ix.row_nnz[row] = nnz;
+      ix.row_maxb[row] = bmax;
+      const int items = ceil_div(nnz, kDecodeBlocks);
+      se += nnz;
+      sit += items;
+      scost += nnz ? (unsigned long long)(nnz * per_key + (long long)items * 256 - fast_adj(si, bmax, P.kvw)) : 0ull;
+    }
+    __syncwarp();
+  }
+  flags = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && flags) atomicOr(&ix.hdr[kHdrFlags], flags);
+  U3 tot;
+  block_excl_u64x3(U3{se, sit, scost}, tmp, &tot);
+  if (threadIdx.x == 0) {
+    ix.cta_sums[3 * blockIdx.x] = tot.x;
+    ix.cta_sums[3 * blockIdx.x + 1] = tot.y;
+    ix.cta_sums[3 * blockIdx.x + 2] = tot.z;
+  }
+}
+
+__device__ __forceinline__ void fast_phase_b(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P,
+                                             const ixp::SeqTab& tab, int total_q, int topk, int32_t (*rowbuf)[256],
+                                             unsigned long long* tmp) {
+  __shared__ unsigned long long s_base[3][kFastRowsChunk];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int NB = ix.hdr[kHdrNB], n_keys = ix.hdr[kHdrKeys];
+  const int n_rows = P.Hkv * P.B;
+  // this CTA's prefixes and the totals
+  unsigned long long pe = 0, pit = 0, pc = 0, ae = 0, ait = 0, ac = 0;
+  for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+    const unsigned long long e = ix.cta_sums[3 * c], it = ix.cta_sums[3 * c + 1], co = ix.cta_sums[3 * c + 2];
+    ae += e;
+    ait += it;
+    ac += co;
+    if (c < (int)blockIdx.x) {
+      pe += e;
+      pit += it;
+      pc += co;
+    }
+  }
+  U3 t3;
+  block_excl_u64x3(U3{pe, pit, pc}, tmp, &t3);
+  pe = t3.x;
+  pit = t3.y;
+  pc = t3.z;
+  block_excl_u64x3(U3{ae, ait, ac}, tmp, &t3);
+  const int E = (int)t3.x, Nd = (int)t3.y;
+  const long long Cd = (long long)t3.z;
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    ix.row_ptr[n_keys] = E;
+    ix.hdr[kHdrNnz] = E;
+    ix.hdr[kHdrActive] = E;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    sc.hdr[kSchItems] = 0;
+    sc.hdr[kSchCtas] = P.num_ctas;
+    sc.hdr[kSchCostLo] = 0;
+    sc.hdr[kSchCostHi] = 0;
+    sc.hdr[kSchDecItems] = Nd;
+    sc.hdr[kSchDecCostLo] = (int)(Cd & 0xffffffffll);
+    sc.hdr[kSchDecCostHi] = (int)(Cd >> 32);
+    sc.cost_prefix[0] = 0;
+    sc.cost_prefix_dec[Nd] = Cd;
+    for (int c = 0; c <= P.num_ctas; ++c) sc.cta_ptr[c] = 0;
+    for (int c = 0, e = boundaries_at_or_below(0, Cd, P.num_ctas); c < e; ++c) sc.cta_ptr_dec[c] = 0;
+  }
+  // tokens outside every decode row (only when cu_seqlens_q was invalid):
+  // their slots index nothing
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total_q;
+       t += (long long)gridDim.x * blockDim.x) {
+    if (tab.get(ix.token_seq[t]).tq == 1) continue;
+    for (long long x = t * P.Hkv * topk; x < (t + 1) * P.Hkv * topk; ++x) ix.slot_entry[x] = -1;
+  }
+  int r0, r1;
+  fast_rows(n_rows, &r0, &r1);
+  unsigned long long ce = pe, cit = pit, cc = pc;
+  for (int c0 = r0; c0 < r1; c0 += kFastRowsChunk) {
+    // per-row bases of this chunk (rows in key order)
+    const int R = c0 + threadIdx.x;
+    unsigned long long ve = 0, vit = 0, vc = 0;
+    if (R < r1) {
+      const int g = R / P.B, s = R - g * P.B;
+      const SeqInfo si = tab.get(s);
+      if (si.tq == 1) {
+        const int row = si.q_begin * P.Hkv + g;
+        const int nnz = ix.row_nnz[row];
+        const int items = ceil_div(nnz, kDecodeBlocks);
+        ve = nnz;
+        vit = items;
+        vc = nnz ? (unsigned long long)(nnz * (64 + 128LL * P.kvw) + (long long)items * 256 -
+                                        fast_adj(si, ix.row_maxb[row], P.kvw))
+                 : 0ull;
+      }
+    }
+    U3 tt;
+    const U3 ex = block_excl_u64x3(U3{ve, vit, vc}, tmp, &tt);
+    s_base[0][threadIdx.x] = ce + ex.x;
+    s_base[1][threadIdx.x] = cit + ex.y;
+    s_base[2][threadIdx.x] = cc + ex.z;
+    __syncthreads();
+    const int nr = min(kFastRowsChunk, r1 - c0);
+    for (int rr = w; rr < nr; rr += nw) {
+      const int Rw = c0 + rr;
+      const int g = Rw / P.B, s = Rw - g * P.B;
+      const SeqInfo si = tab.get(s);
+      const int base_e = (int)s_base[0][rr];
+      const int base_it = (int)s_base[1][rr];
+      const long long base_c = (long long)s_base[2][rr];
+      const long long key0 = (long long)g * NB + si.blk_off;
+      int nnz = 0, bmax = -1;
+      if (si.tq == 1) {
+        const int row = si.q_begin * P.Hkv + g;
+        const long long base_slot = (long long)row * topk;
+        nnz = ix.row_nnz[row];
+        bmax = ix.row_maxb[row];
+        for (int j = lane; j < nnz; j += 32) rowbuf[w][j] = ix.slot_entry[base_slot + j];
+        __syncwarp();
+        for (int k = lane; k < topk; k += 32) ix.slot_entry[base_slot + k] = -1;
+        __syncwarp();
+        for (int j = lane; j < nnz; j += 32) {
+          const int v = rowbuf[w][j], b = v >> 8, k = v & 255;
+          const int pos = base_e + j;
+          ix.active[pos] = (int)(key0 + b);
+          ix.active_valid[pos] = min(128, si.L - 128 * b);
+          ix.entries[pos] = (int)(base_slot + k);
+          ix.slot_entry[base_slot + k] = pos;
+        }
+      }
+      __syncwarp();
+      // row_ptr of every key of the row: entries before it
+      for (int b = lane; b < si.nblk; b += 32) {
+        int lo = 0, hi = nnz;  // ranked blocks below b
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if ((rowbuf[w][mid] >> 8) < b) lo = mid + 1;
+          else hi = mid;
+        }
+        ix.row_ptr[key0 + b] = base_e + lo;
+      }
+      // the row's decode items
+      if (nnz > 0) {
+        KeyWork kw{};
+        kw.kind = 2;
+        kw.a = base_e;
+        kw.begin = base_e;
+        kw.cnt = nnz;
+        kw.n = ceil_div(nnz, kDecodeBlocks);
+        kw.adj = fast_adj(si, bmax, P.kvw);
+        for (int i = lane; i < kw.n; i += 32) {
+          int k0, nk;
+          long long pre, cost;
+          decode_item(kw, P, i, &k0, &nk, &pre, &cost);
+          const long long pfx = base_c + pre;
+          const int item = base_it + i;
+          sc.items_dec[item] = make_int4(kw.a + k0, kw.begin + k0, 1, nk);
+          sc.cost_prefix_dec[item] = pfx;
+          for (int c2 = boundaries_at_or_below(pfx, Cd, P.num_ctas),
+                   e = boundaries_at_or_below(pfx + cost, Cd, P.num_ctas);
+               c2 < e; ++c2)
+            sc.cta_ptr_dec[c2] = item + 1;
+        }
+      }
+      __syncwarp();
+    }
+    ce += tt.x;
+    cit += tt.y;
+    cc += tt.z;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 2) k_plan(PlanArgs a) {
   __shared__ unsigned long long tmp[3 * 33];
   __shared__ int32_t rowbuf[ixp::kMarkWarps][256];
   __shared__ int s_tab[6][ixp::kSeqTab];
@@ -291,6 +554,19 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     tot = ixp::SeqTotals{ia.ix.hdr[kHdrNB], ia.ix.hdr[kHdrBMW], ia.ix.hdr[kHdrKMW]};
   }
   ixp::phase_token_seq(ia.ix, ia.cu, ia.B, ia.total_q);
+  // (block << 8 | slot) of the ranked rows must fit an int: blocks < 2^23
+  if (ia.B <= ixp::kSeqTab && a.P.G <= kDecodeMaxG && ia.cap_len < (1 << 30)) {
+    // all-decode batch (every sequence at most one new token): one barrier
+    bool all_decode = true;
+    for (int s = threadIdx.x; s < ia.B; s += blockDim.x) all_decode &= s_tab[5][s] <= 1;
+    if (__syncthreads_and(all_decode)) {
+      const ixp::SeqTab tab{ia.ix.seq, s_tab, ia.B};
+      fast_phase_a(ia.ix, ia.sel, a.P, tab, ia.topk, rowbuf, tmp);
+      grid_barrier(bar, flags, nb, epoch);
+      fast_phase_b(ia.ix, a.sc, a.P, tab, ia.total_q, ia.topk, rowbuf, tmp);
+      return;
+    }
+  }
   ixp::phase_zero(ia.ix, ia.Hkv, tot, false);
   grid_barrier(bar, flags, nb, epoch);
   ixp::phase_mark(ia.ix, ia.sel, ia.total_q, ia.Hkv, ia.topk, ia.causal, rowbuf, false);

@@ -37,7 +37,25 @@ def small_cases():
                               q_dtype="fp16", kv_dtype="fp16"),
         "mha_fp16_fp8": W.custom("mha_fp16_fp8", [3, 4], [640, 1111], 4, 4, 128, 4, True, "uniform", 106,
                                  q_dtype="fp16", kv_dtype="fp8"),
+        "decode_edges": _decode_edge_workload(),
     }
+
+
+def _decode_edge_workload():
+    # An all-decode batch (every sequence has one new token or none), which
+    # the plan indexes in its one-barrier form: seq 0 has a token but L = 0
+    # (its selection is out of range, causal-length flag); seq 1 has no
+    # token; seq 2's token selects nothing; seq 3 has an out-of-range and a
+    # duplicate slot; seq 4 ends in a partial block; seq 5 is long.
+    w = W.custom("decode_edges", [1, 0, 1, 1, 1, 1], [0, 300, 700, 1000, 333, 5000], 8, 2, 64, 6, True,
+                 "uniform", 109)
+    sel = w.selected
+    sel[0] = -1
+    sel[0, 1, 2] = 0          # L = 0: no block exists
+    sel[1] = -1               # seq 2: nothing selected
+    sel[2, 0, 1] = 99         # out of range
+    sel[2, 1, 3] = sel[2, 1, 0]  # duplicate
+    return w
 
 
 SMALL = small_cases()
@@ -147,13 +165,15 @@ def test_combine_with_oracle_partials():
     U.assert_close_lse(lse.cpu().numpy().T.reshape(-1), full_l, 1e-5, "combine lse")
 
 
-@pytest.mark.parametrize("name", ["fp8_varlen_small", "skewed_small", "edges"])
+@pytest.mark.parametrize("name", ["fp8_varlen_small", "skewed_small", "edges", "decode_edges", "decode_bad_cu"])
 def test_plan_equals_separate_index_and_schedule(name):
     """mxsa_plan (one launch) leaves the same index and schedule as
     mxsa_build_index followed by mxsa_schedule."""
     import block_sparse_attention_builder_gb300 as mx
-    w = _edge_workload() if name == "edges" else SMALL[name]
+    w = _edge_workload() if name == "edges" else SMALL["decode_edges" if name == "decode_bad_cu" else name]
     inp = U.device_inputs(w)
+    if name == "decode_bad_cu":  # not a non-decreasing partition: nothing is indexed, CU flagged
+        inp["cu"] = torch.tensor([0, 2, 1, 3, 4, 5, 5], dtype=torch.int64, device="cuda")
     prob = U.problem(w)
     a = mx.SparseAttention(prob, "cuda")
     b = mx.SparseAttention(prob, "cuda")
@@ -167,6 +187,11 @@ def test_plan_equals_separate_index_and_schedule(name):
     sa, sb = U.read_sched(a, NUM_SMS), U.read_sched(b, NUM_SMS)
     for k in sa:
         assert np.array_equal(np.asarray(sa[k]), np.asarray(sb[k])), k
+    if name == "decode_bad_cu":
+        assert ia["flags"] & 128 and ia["nnz"] == 0
+        assert np.all(ia["slot_entry"] == -1)
+    if name == "decode_edges":
+        assert ia["flags"] & 1 and ia["flags"] & 2 and ia["flags"] & 8
 
 
 @pytest.mark.parametrize("num_ctas", [1, 7, 300])
