@@ -225,12 +225,26 @@ class SparseAttention:
 
     def __call__(self, q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, out=None,
                  lse=None, return_lse=True, stream=None):
+        """All four steps.  out / lse may be pinned host tensors: the combine
+        kernel then writes them directly (valid once the stream is synced)."""
+        self.prepare(selected, cu_seqlens_q, used_kv_lens, stream)
+        return self.attend(q, k_cache, v_cache, block_tables, out, lse, return_lse, stream)
+
+    def prepare(self, selected, cu_seqlens_q, used_kv_lens, stream=None):
+        """Index + schedule (one launch).  Needs only the selections and the
+        sequence lengths, so q and block_tables may still be in flight."""
+        plan(self.prob, selected, cu_seqlens_q, used_kv_lens, self.ws.index, self.ws.sched, self.num_ctas, stream)
+
+    def attend(self, q, k_cache, v_cache, block_tables, out=None, lse=None, return_lse=True, stream=None):
+        """Forward + combine over the last prepare()'s index and schedule."""
         p = self.prob
+        for name, t in (("out", out), ("lse", lse)):
+            if t is not None and not t.is_cuda and not t.is_pinned():
+                raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
         if out is None:
             out = torch.empty(p.total_q, p.num_q_heads, 128, dtype=q.dtype, device=q.device)
         if return_lse and lse is None:
             lse = torch.empty(p.num_q_heads, p.total_q, dtype=torch.float32, device=q.device)
-        plan(p, selected, cu_seqlens_q, used_kv_lens, self.ws.index, self.ws.sched, self.num_ctas, stream)
         kvouter_fwd(p, q, k_cache, v_cache, block_tables, self.ws.index, self.ws.sched, self.ws.partial,
                     self.num_ctas, stream)
         combine(p, self.ws.index, self.ws.partial, out, lse if return_lse else None, stream)

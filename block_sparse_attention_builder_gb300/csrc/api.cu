@@ -298,6 +298,22 @@ mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const v
   return MXSA_OK;
 }
 
+// Output pointers of the combine: device memory, or pinned host memory that
+// the GPU reaches at the same address (unified addressing; on a Grace-
+// Blackwell node the kernel's stores then cross NVLink-C2C directly, with no
+// device-to-host copy).  Pageable host memory and unknown pointers are
+// refused before any launch.
+static bool kernel_writable(const void* p) {
+  if (!p) return true;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the query recorded
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+  return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
                          const void* partial_ws, size_t partial_bytes, void* out, float* lse, void* stream) {
   if (!problem) return MXSA_ERR_INVALID_ARG;
@@ -307,6 +323,7 @@ mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size
   if (!index_ws || !partial_ws || (problem->total_q > 0 && !out)) return MXSA_ERR_INVALID_ARG;
   if (!aligned(index_ws, 16) || !aligned(partial_ws, 16) || !aligned(out, 16) || !aligned(lse, 4))
     return MXSA_ERR_INVALID_ARG;
+  if (!kernel_writable(out) || !kernel_writable(lse)) return MXSA_ERR_INVALID_ARG;
   size_t po, pl, pt;
   partial_layout(*problem, &po, &pl, &pt);
   if (index_bytes < il.total || partial_bytes < pt) return MXSA_ERR_WORKSPACE;

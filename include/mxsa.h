@@ -155,8 +155,12 @@ mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const v
  * selected blocks with LSE weights: M = max lse_k, w_k = exp(lse_k - M),
  * out = sum w_k o_k / sum w_k (rounded to nearest-even into q_dtype),
  * lse = M + log sum w_k.  A row with no partial gets out 0 and lse -inf.
- *   out   device [total_q, Hq, 128] of q_dtype (written)
- *   lse   device float [Hq, total_q] (written), or NULL to skip it */
+ *   out   [total_q, Hq, 128] of q_dtype (written): device memory, or pinned
+ *         host memory mapped at the same address (unified addressing), which
+ *         the kernel then writes directly over the host link
+ *   lse   float [Hq, total_q] (written), same memory rules, or NULL to skip it
+ * Pageable host memory or an unknown pointer for out/lse returns
+ * MXSA_ERR_INVALID_ARG before any launch. */
 mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
                          const void* partial_ws, size_t partial_bytes, void* out, float* lse, void* stream);
 

@@ -266,6 +266,29 @@ def test_quickstart_call_shape():
     U.assert_close_lse(lse.cpu().numpy().T.reshape(-1), l_ref, 2e-3, "quickstart lse")
 
 
+def test_pinned_host_outputs_and_pageable_refused():
+    """out / lse in pinned host memory are written by the combine kernel
+    directly (same values as device outputs); pageable host memory is refused
+    by the binding and by the library before any launch."""
+    import block_sparse_attention_builder_gb300 as mx
+    w = SMALL["gqa_decode_small"]
+    inp = U.device_inputs(w)
+    attn = mx.SparseAttention(U.problem(w), "cuda")
+    out_d, lse_d = attn(inp["q"], inp["k"], inp["v"], inp["sel"], inp["bt"], inp["cu"], inp["lens"])
+    h_out = torch.full(out_d.shape, 7.0, dtype=out_d.dtype).pin_memory()
+    h_lse = torch.full(lse_d.shape, 7.0, dtype=torch.float32).pin_memory()
+    attn.prepare(inp["sel"], inp["cu"], inp["lens"])
+    attn.attend(inp["q"], inp["k"], inp["v"], inp["bt"], out=h_out, lse=h_lse)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out, out_d.cpu()) and torch.equal(h_lse, lse_d.cpu())
+    pageable = torch.empty(out_d.shape, dtype=out_d.dtype)
+    with pytest.raises(ValueError):
+        attn.attend(inp["q"], inp["k"], inp["v"], inp["bt"], out=pageable)
+    with pytest.raises(mx.MxsaError) as ei:
+        mx.combine(attn.prob, attn.ws.index, attn.ws.partial, pageable)
+    assert ei.value.status == 1
+
+
 def test_bad_page_id_is_flagged_not_faulted():
     import block_sparse_attention_builder_gb300 as mx
     w = W.workload("tiny_decode")
