@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
           live &= live - 1;
           const int es = __shfl_sync(0xffffffffu, e, src);
           const float ws = __shfl_sync(0xffffffffu, w, src);
-          const float4 v = reinterpret_cast<const float4*>(part_o + ((long long)es * G + j) * 128)[lane];
+          const float4 v = __ldcs(reinterpret_cast<const float4*>(part_o + ((long long)es * G + j) * 128) + lane);
           acc.x = fmaf(ws, v.x, acc.x);
           acc.y = fmaf(ws, v.y, acc.y);
           acc.z = fmaf(ws, v.z, acc.z);

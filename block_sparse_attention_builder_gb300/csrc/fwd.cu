@@ -381,13 +381,13 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           const int rr = 4 * i + (wl >> 3), cc = wl & 7;
           const uint4 val = ld_shared_v4(stg + (uint32_t)rr * 128u + ((uint32_t)(cc ^ (rr & 7)) << 4));
           if (wrow0 + rr < pend.rows)
-            st_global_v4(a.part_o + (pend.orow0 + wrow0 + rr) * 128 + cb * 32 + cc * 4, val);
+            st_global_cs_v4(a.part_o + (pend.orow0 + wrow0 + rr) * 128 + cb * 32 + cc * 4, val);
         }
         __syncwarp();
       }
       if (r < pend.rows)
-        a.part_lse[pend.orow0 + r] =
-            pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY;
+        __stcs(&a.part_lse[pend.orow0 + r],
+               pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY);
       tc_fence_before();
     };
     for (int it = it_begin; it < it_end && ok; ++it, ++n) {

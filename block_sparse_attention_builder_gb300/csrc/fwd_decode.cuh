@@ -620,7 +620,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       float* dst = a.part_o + (size_t)e0 * G * 128 + k;
 #pragma unroll
       for (int r = 0; r < N; ++r)
-        if (r < G) dst[(size_t)r * 128] = lsum[r] > 0.f ? o[r] * __frcp_rn(lsum[r]) : 0.f;
+        if (r < G) __stcs(&dst[(size_t)r * 128], lsum[r] > 0.f ? o[r] * __frcp_rn(lsum[r]) : 0.f);
       if (k < G) {
         float lv = -INFINITY, mv = 0.f;
 #pragma unroll

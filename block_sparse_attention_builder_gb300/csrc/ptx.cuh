@@ -242,8 +242,11 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
   return v;
 }
 
-__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+// 16-byte global store with the evict-first (streaming) hint: for data
+// written once and read once later (the FP32 partials), so that it does not
+// push reused lines (gathered q rows) out of L2.
+__device__ __forceinline__ void st_global_cs_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 
