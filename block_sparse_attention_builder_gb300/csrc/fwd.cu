@@ -4,7 +4,7 @@
 // rows of one key (kv head, sequence, block): the block's K and V pages are
 // TMA-loaded once per item and every tile of rows is multiplied against them.
 //
-// Persistent kernel, one CTA per SM, 320 threads:
+// Persistent kernel, one CTA per SM, 352 threads (this phase's roles):
 //   warps 0-3, 4-7  two softmax warpgroups; the CTA's tiles alternate
 //              between them (tile j -> warpgroup j % 2) so that one group's
 //              softmax overlaps the other group's MMAs, loads and stores.
@@ -19,10 +19,10 @@
 //   warp 8     producer: decodes items (key -> kv head, sequence, block),
 //              walks the block table and TMA-loads the block's K and V pages
 //              into a double-buffered stage (FP8: into a staging tile).
-//   warp 9     TMEM owner (512 columns: S and O of each group) and MMA
-//              issuer (tcgen05.mma, cta_group::1, M = N = 128, K = 16 per
-//              instruction, FP32 accumulate), issuing q k^T of tile j + 1
-//              before p v of tile j.
+//   warps 9, 10  MMA issuers, one per softmax group (tcgen05.mma,
+//              cta_group::1, M = N = 128, K = 16 per instruction, FP32
+//              accumulate in TMEM: S and O of each group, 512 columns owned
+//              by warp 9): q k^T then p v of each of the group's tiles.
 //
 // Shared-memory operands use the 128-byte swizzled K-major layout (q, K, P)
 // and the 128-byte swizzled MN-major layout (V as the B operand of P V).
@@ -42,7 +42,7 @@ namespace mxsa {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTileBytes = 32768;  // 128 rows x 128 x 16-bit
@@ -189,7 +189,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.kv_full[i], a.kv_fp8 ? 128 : 1);  // FP8: the widening group arrives
-      mbar_init(&c.kv_empty[i], 1);
+      mbar_init(&c.kv_empty[i], 2);  // one arrival per MMA issuer
       mbar_init(&c.q_full[i], 128);
       mbar_init(&c.s_full[i], 1);
       mbar_init(&c.p_full[i], 128);
@@ -197,7 +197,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       mbar_init(&c.stg_full[i], 1);
     }
     mbar_init(&c.stg_empty, 128);
-    mbar_init(&c.done, 1);
+    mbar_init(&c.done, 2);
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -281,66 +281,55 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         mbar_drain(&c.stg_full[(n - 1) & 1], ((n - 1) >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (warp >= kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuers
+    // Warp 9 + g (lane 0) issues the MMAs of softmax group g (its tiles
+    // j = g, g + 2, ...):
+    // q k^T once the group gathered the tile's q, then p v once it wrote P.
+    // Each issuer waits only on its own group, so one group's MMAs never
+    // queue behind the other group's inputs; a stage is released after both
+    // issuers committed it (kv_empty counts two arrivals).
     if (lane == 0) {
+      const int g = warp - kMmaWarp;
       const uint32_t id_qk = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 0);
       const uint32_t id_pv = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 1);
+      const uint32_t q_s = sbase + kOffQP + g * kTileBytes;  // q, then P, of group g
+      const uint32_t tS = tmem + g * 256, tO = tS + 128;
       int n = 0, j = 0;
       bool ok = true;
-      // the tile whose P V is still to be issued: index, stage, last of its item
-      int pj = -1, pst = 0, plast = 0;
-      auto issue_pv = [&]() -> bool {
-        const int w = pj & 1;
-        if (!mbar_wait(&c.p_full[w], (pj >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t p_s = sbase + kOffQP + w * kTileBytes;
-        const uint32_t v_s = sbase + kOffKV + pst * kStageBytes + kTileBytes;
-        const uint32_t tO = tmem + w * 256 + 128;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
-          mma_f16_ss(tO, smem_desc_sw128(p_s + off, 0, 1024), smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), id_pv,
-                     ks > 0);
-        }
-        mma_commit(&c.o_full[w]);
-        if (plast) mma_commit(&c.kv_empty[pst]);
-        pj = -1;
-        return true;
-      };
       for (int it = it_begin; it < it_end && ok; ++it, ++n) {
         const int st = n & 1, use = n >> 1;
-        // at an item boundary, the previous tile's p v goes first unless this
-        // item's block has already landed: it releases the previous stage,
-        // which the producer needs to load the item after this one
-        if (pj >= 0 && !mbar_test(&c.kv_full[st], use & 1)) ok = issue_pv();
-        ok = ok && mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        ok = mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
         const int ntiles = (c.info[st].n + per_tile - 1) / per_tile;
-        const uint32_t k_s = sbase + kOffKV + st * kStageBytes;
+        const uint32_t k_s = sbase + kOffKV + st * kStageBytes, v_s = k_s + kTileBytes;
         for (int t = 0; t < ntiles && ok; ++t, ++j) {
-          const int w = j & 1;
-          ok = mbar_wait(&c.q_full[w], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          if ((j & 1) != g) continue;
+          ok = mbar_wait(&c.q_full[g], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t q_s = sbase + kOffQP + w * kTileBytes;
-          const uint32_t tS = tmem + w * 256;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
             mma_f16_ss(tS, smem_desc_sw128(q_s + off, 0, 1024), smem_desc_sw128(k_s + off, 0, 1024), id_qk, ks > 0);
           }
-          mma_commit(&c.s_full[w]);
-          if (pj >= 0) ok = issue_pv();
-          pj = j;
-          pst = st;
-          plast = t == ntiles - 1;
+          mma_commit(&c.s_full[g]);
+          ok = mbar_wait(&c.p_full[g], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
+            mma_f16_ss(tO, smem_desc_sw128(q_s + off, 0, 1024), smem_desc_sw128(v_s + ks * 2048u, 16384, 1024),
+                       id_pv, ks > 0);
+          }
+          mma_commit(&c.o_full[g]);
         }
+        if (ok) mma_commit(&c.kv_empty[st]);  // this issuer's share of the stage is done
       }
-      if (ok && pj >= 0) issue_pv();
-      // drain: all MMAs issued by this thread complete before TMEM is freed
+      // drain: all MMAs of both issuers complete before TMEM is freed (done
+      // counts two arrivals)
       mma_commit(&c.done);
       mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
@@ -430,16 +419,9 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         ok = group_all(mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
         if (!ok) break;
         const ItemInfo inf = c.info[st];
-        // this group's buffer is free once its previous tile's P V is done
-        if (pend_j >= 0) {
-          ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                                   kWaitLimitNs),
-                         grp);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // ---- gather this tile's q rows (loads first, then the previous
-        // tile's epilogue, then the shared-memory stores)
+        // ---- gather this tile's q rows: the loads go to registers first
+        // (their latency overlaps the wait for the previous tile's p v), then
+        // the previous tile's epilogue, then the shared-memory stores
         const int et0 = inf.e0 + t * per_tile;
         const int ne = min(per_tile, inf.n - t * per_tile);
         const int rows = ne * a.G;
@@ -462,6 +444,14 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           const int src_row = __shfl_sync(0xffffffffu, qrow, 2 * i + (wl >> 4));
           v[i] = src_row >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.q + (size_t)src_row * 256) + (wl & 15))
                               : make_uint4(0, 0, 0, 0);
+        }
+        // this group's buffer (and O) are free once its previous tile's p v is done
+        if (pend_j >= 0) {
+          ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                   kWaitLimitNs),
+                         grp);
+          if (!ok) break;
+          tc_fence_after();
         }
         if (pend_j >= 0) epilogue();
 #pragma unroll
