@@ -74,6 +74,7 @@ struct FwdArgs {
   float* part_lse;
   int32_t* flags;
   int32_t num_seqs, Hq, Hkv, G, topk, page_size, max_pages, num_pages, causal, kv_fp8, ab_bf16, per_tile;
+  int32_t tma_store;  // full tiles' partials go out by TMA (the partial map exists)
   float scale_log2;
 };
 
@@ -120,6 +121,10 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
 }
 
 // named barrier (id 1 + group) over the 128 threads of one softmax group
+__device__ __forceinline__ void group_sync(int grp) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
+}
+
 __device__ __forceinline__ bool group_all(bool v, int grp) {
   uint32_t r;
   asm volatile(
@@ -179,8 +184,9 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
 
 // Runs the CTA's KV-stationary items (all kThreads threads; 1024-aligned
 // shared memory `sm`; TMEM base `tmem` with 512 columns).
-__device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const FwdArgs& a,
-                                                   uint8_t* sm, uint32_t tmem) {
+__device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                                   const CUtensorMap& tmo, const FwdArgs& a, uint8_t* sm,
+                                                   uint32_t tmem) {
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int it_begin = a.cta_ptr[blockIdx.x], it_end = a.cta_ptr[blockIdx.x + 1];
@@ -344,6 +350,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     int n = 0, j = 0;
     bool ok = true;
     const int wl = tid & 31, wrow0 = (warp & 3) * 32;  // lane; the warp's first tile row
+    const uint64_t l2_policy = l2_policy_evict_first();
     RowState pend{0, -INFINITY, 0.f, 0};
     int pend_j = -1;
     // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l)
@@ -352,27 +359,60 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     // 128-byte row segments instead of 32 scattered 16-byte pieces.
     auto epilogue = [&]() {
       const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
-      const uint32_t stg = qp + (uint32_t)(warp & 3) * 4096u;
-      // a warp whose 32 rows are all padding has nothing to store
+      if (pend.rows == 128 && a.tma_store) {
+        // full tile: its 128 rows are one contiguous partial range, written
+        // by four TMA stores of 32-column slices staged (128B-swizzled) in
+        // the two halves of the group's q/P buffer
 #pragma unroll
-      for (int cb = 0; cb < 4 && wrow0 < pend.rows; ++cb) {
-        float ov[32];
-        tmem_ld32(tO + cb * 32, ov);
-        tmem_ld_wait();
+        for (int cb = 0; cb < 4; ++cb) {
+          const uint32_t stg = qp + (uint32_t)(cb & 1) * 16384u;
+          if (cb >= 2) {  // the slice staged two steps ago has been read out
+            if (r == 0) bulk_wait_group_read<1>();
+            group_sync(grp);
+          }
+          float ov[32];
+          tmem_ld32(tO + cb * 32, ov);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          st_shared_v4(stg + (uint32_t)wl * 128u + ((uint32_t)(c8 ^ (wl & 7)) << 4),
-                       __float_as_uint(ov[4 * c8] * inv_l), __float_as_uint(ov[4 * c8 + 1] * inv_l),
-                       __float_as_uint(ov[4 * c8 + 2] * inv_l), __float_as_uint(ov[4 * c8 + 3] * inv_l));
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + (wl >> 3), cc = wl & 7;
-          const uint4 val = ld_shared_v4(stg + (uint32_t)rr * 128u + ((uint32_t)(cc ^ (rr & 7)) << 4));
-          if (wrow0 + rr < pend.rows)
-            st_global_cs_v4(a.part_o + (pend.orow0 + wrow0 + rr) * 128 + cb * 32 + cc * 4, val);
+          for (int c8 = 0; c8 < 8; ++c8)
+            st_shared_v4(stg + (uint32_t)r * 128u + ((uint32_t)(c8 ^ (r & 7)) << 4),
+                         __float_as_uint(ov[4 * c8] * inv_l), __float_as_uint(ov[4 * c8 + 1] * inv_l),
+                         __float_as_uint(ov[4 * c8 + 2] * inv_l), __float_as_uint(ov[4 * c8 + 3] * inv_l));
+          fence_proxy_async_smem();
+          group_sync(grp);
+          if (r == 0) {
+            tma_store_2d(&tmo, stg, cb * 32, (int)pend.orow0, l2_policy);
+            bulk_commit_group();
+          }
         }
-        __syncwarp();
+        if (r == 0) bulk_wait_group_read<0>();
+        group_sync(grp);  // the buffer is free for the next tile's q rows
+      } else {
+        // partial tile: each 32-column slice goes through the warp's 4 KB of
+        // the group's (free) q/P buffer so that every store instruction
+        // writes four whole 128-byte row segments
+        const uint32_t stg = qp + (uint32_t)(warp & 3) * 4096u;
+        // a warp whose 32 rows are all padding has nothing to store
+#pragma unroll
+        for (int cb = 0; cb < 4 && wrow0 < pend.rows; ++cb) {
+          float ov[32];
+          tmem_ld32(tO + cb * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            st_shared_v4(stg + (uint32_t)wl * 128u + ((uint32_t)(c8 ^ (wl & 7)) << 4),
+                         __float_as_uint(ov[4 * c8] * inv_l), __float_as_uint(ov[4 * c8 + 1] * inv_l),
+                         __float_as_uint(ov[4 * c8 + 2] * inv_l), __float_as_uint(ov[4 * c8 + 3] * inv_l));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (wl >> 3), cc = wl & 7;
+            const uint4 val = ld_shared_v4(stg + (uint32_t)rr * 128u + ((uint32_t)(cc ^ (rr & 7)) << 4));
+            if (wrow0 + rr < pend.rows)
+              st_global_cs_v4(a.part_o + (pend.orow0 + wrow0 + rr) * 128 + cb * 32 + cc * 4, val);
+          }
+          __syncwarp();
+        }
       }
       if (r < pend.rows)
         __stcs(&a.part_lse[pend.orow0 + r],
@@ -524,6 +564,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         epilogue();
       }
     }
+    if (r == 0) bulk_wait_group_all();  // this group's partial stores are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -535,7 +576,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
 // columns) is allocated once for both phases.
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-          const __grid_constant__ CUtensorMap tmq, FwdArgs a, dec::DecArgs d) {
+          const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo, FwdArgs a,
+          dec::DecArgs d) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint32_t s_tmem;
@@ -559,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   if (has_dec) dec::decode_body<16>(tmk, tmv, tmq, d, sm, tmem);
-  if (has_kvs) kv_stationary_body(tmk, tmv, a, sm, tmem);
+  if (has_kvs) kv_stationary_body(tmk, tmv, tmo, a, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -568,6 +610,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // 3-D view of a cache [pages * Hkv][page_size][128]: box = one page, one
 // 128-byte column slab (64 x 16-bit, swizzled) or the full 128 e4m3 row.
+// 2-D view of the FP32 partial rows [rows][128]: box = 32 columns x 128
+// rows, 128B-swizzled (the epilogue's staging layout).
+bool make_partial_map(CUtensorMap* m, float* part_o, long long n_rows) {
+  auto fn = dec::encode_fn();
+  if (!fn || n_rows < 128) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)n_rows};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool make_cache_map(CUtensorMap* m, const void* base, const mxsa_problem& p) {
   auto fn = dec::encode_fn();
   if (!fn) return false;
@@ -627,6 +683,12 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.idx_hdr = ix.hdr;
   a.sch_hdr = sc.hdr;
   a.part_o = part_o;
+  CUtensorMap tmo;
+  std::memset(&tmo, 0, sizeof(tmo));
+  a.tma_store = make_partial_map(&tmo, part_o,
+                                 (long long)p.total_q * p.num_kv_heads * p.topk * (p.num_q_heads / p.num_kv_heads))
+                    ? 1
+                    : 0;
   a.part_lse = part_lse;
   a.flags = ix.hdr + kHdrFlags;
   a.num_seqs = p.num_seqs;
@@ -643,7 +705,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, a, d);
+  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmo, a, d);
 }
 
 }  // namespace mxsa
