@@ -75,6 +75,8 @@ struct FwdArgs {
   int32_t* flags;
   int32_t num_seqs, Hq, Hkv, G, topk, page_size, max_pages, num_pages, causal, kv_fp8, ab_bf16, per_tile;
   int32_t tma_store;  // full tiles' partials go out by TMA (the partial map exists)
+  int32_t* claim;     // schedule header word: next item to claim
+  int32_t* sch_hdr_mut;  // the schedule header (claim and exit counters)
   float scale_log2;
 };
 
@@ -189,13 +191,18 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
                                                    uint32_t tmem) {
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int it_begin = a.cta_ptr[blockIdx.x], it_end = a.cta_ptr[blockIdx.x + 1];
-  if (it_begin >= it_end) return;  // uniform: nothing to do
+  // Items are claimed dynamically (a global counter), in item order, by the
+  // producer, which publishes each one in its stage's info and ends with an
+  // item of no entries; every role follows that sequence.
+  const int n_items = a.sch_hdr[kSchItems];
+  if (n_items <= 0) return;  // uniform: nothing to do
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.kv_full[i], a.kv_fp8 ? 128 : 1);  // FP8: the widening group arrives
-      mbar_init(&c.kv_empty[i], 2);  // one arrival per MMA issuer
+      // a stage is refilled after both MMA issuers committed it and both
+      // softmax groups read its info (so no role lags two phases behind)
+      mbar_init(&c.kv_empty[i], 4);
       mbar_init(&c.q_full[i], 128);
       mbar_init(&c.s_full[i], 1);
       mbar_init(&c.p_full[i], 128);
@@ -221,11 +228,20 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       const int ps = a.page_size;
       const int npg = ps == 128 ? 1 : 2;
       int n = 0;
-      bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it, ++n) {
+      bool ok = true, ended = false;
+      int it = atomicAdd(a.claim, 1);
+      for (; ok; ++n) {
         const int st = n & 1, use = n >> 1;
         ok = mbar_wait(&c.kv_empty[st], (use & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         if (!ok) break;
+        if (it >= n_items) {  // no item left: publish the end
+          ItemInfo end{};
+          c.info[st] = end;
+          mbar_arrive(a.kv_fp8 ? &c.stg_full[st] : &c.kv_full[st]);
+          ended = true;
+          break;
+        }
+        const int next = atomicAdd(a.claim, 1);  // claimed one item ahead: its latency overlaps this item
         const int4 itm = a.items[it];
         const int key = itm.x;
         const int g = key / NB, r = key - g * NB;
@@ -277,15 +293,17 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
             tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
           }
         }
+        it = next;
       }
       // drain: every load this thread issued has landed before the CTA may
-      // exit (FP8: staging item n - 1 needed item n - 2 widened, so landed)
-      if (!a.kv_fp8) {
-        for (int k = std::max(0, n - 2); k < n; ++k)
-          mbar_drain(&c.kv_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-      } else if (n > 0) {
-        mbar_drain(&c.stg_full[(n - 1) & 1], ((n - 1) >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-      }
+      // exit.  After the end item (published on stage n % 2) item n - 2 has
+      // landed for sure (its stage was released for the end item), and its
+      // barrier has moved on, so only item n - 1 is waited for.  FP8:
+      // staging item n - 1 needed item n - 2 widened, so only n - 1.
+      const int k0 = (ended || a.kv_fp8) ? n - 1 : n - 2;
+      for (int k = std::max(0, k0); k < n; ++k)
+        mbar_drain(a.kv_fp8 ? &c.stg_full[k & 1] : &c.kv_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT,
+                   kWaitLimitNs);
     }
   } else if (warp >= kMmaWarp) {
     // ---------------------------------------------------------- MMA issuers
@@ -303,12 +321,14 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       const uint32_t tS = tmem + g * 256, tO = tS + 128;
       int n = 0, j = 0;
       bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it, ++n) {
+      for (; ok; ++n) {
         const int st = n & 1, use = n >> 1;
         ok = mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        const int ntiles = (c.info[st].n + per_tile - 1) / per_tile;
+        const int n_entries = c.info[st].n;
+        if (n_entries == 0) break;  // the end
+        const int ntiles = (n_entries + per_tile - 1) / per_tile;
         const uint32_t k_s = sbase + kOffKV + st * kStageBytes, v_s = k_s + kTileBytes;
         for (int t = 0; t < ntiles && ok; ++t, ++j) {
           if ((j & 1) != g) continue;
@@ -419,9 +439,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
                pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY);
       tc_fence_before();
     };
-    for (int it = it_begin; it < it_end && ok; ++it, ++n) {
+    for (; ok; ++n) {
       const int st = n & 1, use = n >> 1;
-      const int ntiles = (a.items[it].z + per_tile - 1) / per_tile;
       if (a.kv_fp8 && st == grp) {
         // widen the staged e4m3 block (row r of K and V) into the stage;
         // rows past the valid tokens become zero.  The producer staged this
@@ -429,7 +448,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         ok = group_all(mbar_wait(&c.stg_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
                        grp);
         if (!ok) break;
-        const int valid = c.info[st].valid;
+        const int valid = c.info[st].n > 0 ? c.info[st].valid : 0;  // the end item stages nothing
         const uint8_t* stg = sm + kOffStg;
         for (int kv = 0; kv < 2; ++kv) {
           const uint8_t* src = stg + kv * 16384 + r * 128;
@@ -451,14 +470,20 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&c.stg_empty);
+        if (c.info[st].n > 0) mbar_arrive(&c.stg_empty);
         mbar_arrive(&c.kv_full[st]);
       }
+      // every group reads every item's info (the tile count decides the
+      // groups' alternation), then lets the stage go
+      ok = group_all(mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
+      if (!ok) break;
+      const ItemInfo inf = c.info[st];
+      if (inf.n == 0) break;  // the end
+      group_sync(grp);  // all of the group read the info before the stage may be refilled
+      if (r == 0) mbar_arrive(&c.kv_empty[st]);
+      const int ntiles = (inf.n + per_tile - 1) / per_tile;
       for (int t = 0; t < ntiles && ok; ++t, ++j) {
         if ((j & 1) != grp) continue;
-        ok = group_all(mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
-        if (!ok) break;
-        const ItemInfo inf = c.info[st];
         // ---- gather this tile's q rows: the loads go to registers first
         // (their latency overlaps the wait for the previous tile's p v), then
         // the previous tile's epilogue, then the shared-memory stores
@@ -590,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int b = blockIdx.x;
   const bool has_dec = d.cta_ptr != nullptr && d.cta_ptr[b] < d.cta_ptr[b + 1];
-  const bool has_kvs = a.cta_ptr[b] < a.cta_ptr[b + 1];
+  const bool has_kvs = a.sch_hdr[kSchItems] > 0;  // claimed dynamically by every CTA
   if (!has_dec && !has_kvs) return;  // uniform: nothing to do, nothing allocated
   if (warp == kMmaWarp) {
     tmem_alloc(&s_tmem, 512);
@@ -606,6 +631,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  if (has_kvs && threadIdx.x == 0) {
+    // the last CTA to leave resets the claim counter for the next forward on
+    // the same schedule (every CTA has finished claiming by now)
+    __threadfence();
+    if (atomicAdd(a.sch_hdr_mut + kSchExit, 1) == (int)gridDim.x - 1) {
+      a.sch_hdr_mut[kSchClaim] = 0;
+      a.sch_hdr_mut[kSchExit] = 0;
+      __threadfence();
+    }
+  }
 }
 
 // 3-D view of a cache [pages * Hkv][page_size][128]: box = one page, one
@@ -682,6 +717,8 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.cta_ptr = sc.cta_ptr;
   a.idx_hdr = ix.hdr;
   a.sch_hdr = sc.hdr;
+  a.sch_hdr_mut = sc.hdr;
+  a.claim = sc.hdr + kSchClaim;
   a.part_o = part_o;
   CUtensorMap tmo;
   std::memset(&tmo, 0, sizeof(tmo));

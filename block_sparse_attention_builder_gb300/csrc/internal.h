@@ -40,6 +40,8 @@ enum : int {
   kSchBarCount = 8,  // grid barrier (as in the index header)
   kSchAbort = 9,
   kSchReserved10 = 10,
+  kSchClaim = 11,    // forward: next KV-stationary item to claim (0 after the plan)
+  kSchExit = 12,     // forward: CTAs that left (the last one resets both)
   kSchInts = 16
 };
 

@@ -149,6 +149,8 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     sc.hdr[kSchItems] = Nn;
     sc.hdr[kSchCtas] = P.num_ctas;
+    sc.hdr[kSchClaim] = 0;
+    sc.hdr[kSchExit] = 0;
     sc.hdr[kSchCostLo] = (int)(Cn & 0xffffffffll);
     sc.hdr[kSchCostHi] = (int)(Cn >> 32);
     sc.hdr[kSchDecItems] = Nd;
@@ -417,6 +419,8 @@ __device__ __forceinline__ void fast_phase_b(const IndexPtrs& ix, const SchedPtr
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     sc.hdr[kSchItems] = 0;
     sc.hdr[kSchCtas] = P.num_ctas;
+    sc.hdr[kSchClaim] = 0;
+    sc.hdr[kSchExit] = 0;
     sc.hdr[kSchCostLo] = 0;
     sc.hdr[kSchCostHi] = 0;
     sc.hdr[kSchDecItems] = Nd;

@@ -122,6 +122,8 @@ __device__ void phase_scan_emit(const IndexPtrs& ix, const SchedPtrs& sc, const 
   const int Nn = (int)(all_n & kLow), Nd = (int)(all_d & kLow);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     sc.hdr[kSchItems] = Nn;
+    sc.hdr[kSchClaim] = 0;
+    sc.hdr[kSchExit] = 0;
     sc.hdr[kSchCtas] = P.num_ctas;
     sc.hdr[kSchCostLo] = (int)(Cn & 0xffffffffll);
     sc.hdr[kSchCostHi] = (int)(Cn >> 32);

@@ -202,6 +202,25 @@ def test_cta_count_does_not_change_result(num_ctas, small_runs):
     assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
 
 
+@pytest.mark.parametrize("name", ["prefill_small", "fp8_varlen_small"])
+def test_repeated_forward_on_one_plan(name):
+    """The forward claims KV-stationary items from a counter in the schedule
+    header; the last CTA to leave resets it, so forwards repeated on one plan
+    see every item again and give bit-identical results."""
+    import block_sparse_attention_builder_gb300 as mx
+    w = SMALL[name]
+    inp = U.device_inputs(w)
+    attn = mx.SparseAttention(U.problem(w), "cuda")
+    attn.prepare(inp["sel"], inp["cu"], inp["lens"])
+    outs = [attn.attend(inp["q"], inp["k"], inp["v"], inp["bt"]) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert attn.status() == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    o_ref, l_ref = U.oracle_full(w)
+    U.assert_close_out(outs[-1][0].float().cpu().numpy().reshape(-1, 128), o_ref, U.out_tol(w), f"{name} out")
+
+
 def test_deterministic_repeat(small_runs):
     w = SMALL["skewed_small"]
     _, out0, lse0, inp = small_runs["skewed_small"]
