@@ -74,7 +74,6 @@ struct FwdArgs {
   float* part_lse;
   int32_t* flags;
   int32_t num_seqs, Hq, Hkv, G, topk, page_size, max_pages, num_pages, causal, kv_fp8, ab_bf16, per_tile;
-  int32_t tma_store;  // full tiles' partials go out by TMA (the partial map exists)
   int32_t* claim;     // schedule header word: next item to claim
   int32_t* sch_hdr_mut;  // the schedule header (claim and exit counters)
   float scale_log2;
@@ -187,8 +186,7 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
 // Runs the CTA's KV-stationary items (all kThreads threads; 1024-aligned
 // shared memory `sm`; TMEM base `tmem` with 512 columns).
 __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
-                                                   const CUtensorMap& tmo, const FwdArgs& a, uint8_t* sm,
-                                                   uint32_t tmem) {
+                                                   const FwdArgs& a, uint8_t* sm, uint32_t tmem) {
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Items are claimed dynamically (a global counter), in item order, by the
@@ -370,68 +368,37 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     int n = 0, j = 0;
     bool ok = true;
     const int wl = tid & 31, wrow0 = (warp & 3) * 32;  // lane; the warp's first tile row
-    const uint64_t l2_policy = l2_policy_evict_first();
     RowState pend{0, -INFINITY, 0.f, 0};
     int pend_j = -1;
     // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l)
-    // ln 2.  Each 32-column slice goes through the warp's 4 KB of the group's
-    // (free) q/P buffer so that every store instruction writes four whole
-    // 128-byte row segments instead of 32 scattered 16-byte pieces.
+    // ln 2.  O is read in the 16x256b shape, in which four consecutive lanes
+    // hold 8 consecutive columns of one row, so every store instruction
+    // writes eight whole 32-byte sectors (8 rows x 32 B) straight from
+    // registers; it runs while the next tile's q k^T is in flight.
     auto epilogue = [&]() {
       const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
-      if (pend.rows == 128 && a.tma_store) {
-        // full tile: its 128 rows are one contiguous partial range, written
-        // by four TMA stores of 32-column slices staged (128B-swizzled) in
-        // the two halves of the group's q/P buffer
+      if (wrow0 < pend.rows) {  // a warp of padding rows has nothing to store
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          const uint32_t stg = qp + (uint32_t)(cb & 1) * 16384u;
-          if (cb >= 2) {  // the slice staged two steps ago has been read out
-            if (r == 0) bulk_wait_group_read<1>();
-            group_sync(grp);
-          }
-          float ov[32];
-          tmem_ld32(tO + cb * 32, ov);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ra = hh * 16 + (wl >> 2), rb = ra + 8;  // the warp's rows this lane stores
+          const float sa = __shfl_sync(0xffffffffu, inv_l, ra), sb = __shfl_sync(0xffffffffu, inv_l, rb);
+          const bool oka = wrow0 + ra < pend.rows, okb = wrow0 + rb < pend.rows;
+          float* ga = a.part_o + (pend.orow0 + wrow0 + ra) * 128 + 2 * (wl & 3);
+          float* gb = ga + 8 * 128;
+          float v0[32], v1[32];
+          tmem_ld16x256b_x8(tO + ((uint32_t)(hh * 16) << 16), v0);
+          tmem_ld16x256b_x8(tO + ((uint32_t)(hh * 16) << 16) + 64, v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            st_shared_v4(stg + (uint32_t)r * 128u + ((uint32_t)(c8 ^ (r & 7)) << 4),
-                         __float_as_uint(ov[4 * c8] * inv_l), __float_as_uint(ov[4 * c8 + 1] * inv_l),
-                         __float_as_uint(ov[4 * c8 + 2] * inv_l), __float_as_uint(ov[4 * c8 + 3] * inv_l));
-          fence_proxy_async_smem();
-          group_sync(grp);
-          if (r == 0) {
-            tma_store_2d(&tmo, stg, cb * 32, (int)pend.orow0, l2_policy);
-            bulk_commit_group();
+          for (int c = 0; c < 8; ++c) {
+            if (oka) st_global_cs_v2f(ga + 8 * c, v0[4 * c] * sa, v0[4 * c + 1] * sa);
+            if (okb) st_global_cs_v2f(gb + 8 * c, v0[4 * c + 2] * sb, v0[4 * c + 3] * sb);
           }
-        }
-        if (r == 0) bulk_wait_group_read<0>();
-        group_sync(grp);  // the buffer is free for the next tile's q rows
-      } else {
-        // partial tile: each 32-column slice goes through the warp's 4 KB of
-        // the group's (free) q/P buffer so that every store instruction
-        // writes four whole 128-byte row segments
-        const uint32_t stg = qp + (uint32_t)(warp & 3) * 4096u;
-        // a warp whose 32 rows are all padding has nothing to store
 #pragma unroll
-        for (int cb = 0; cb < 4 && wrow0 < pend.rows; ++cb) {
-          float ov[32];
-          tmem_ld32(tO + cb * 32, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            st_shared_v4(stg + (uint32_t)wl * 128u + ((uint32_t)(c8 ^ (wl & 7)) << 4),
-                         __float_as_uint(ov[4 * c8] * inv_l), __float_as_uint(ov[4 * c8 + 1] * inv_l),
-                         __float_as_uint(ov[4 * c8 + 2] * inv_l), __float_as_uint(ov[4 * c8 + 3] * inv_l));
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = 4 * i + (wl >> 3), cc = wl & 7;
-            const uint4 val = ld_shared_v4(stg + (uint32_t)rr * 128u + ((uint32_t)(cc ^ (rr & 7)) << 4));
-            if (wrow0 + rr < pend.rows)
-              st_global_cs_v4(a.part_o + (pend.orow0 + wrow0 + rr) * 128 + cb * 32 + cc * 4, val);
+          for (int c = 0; c < 8; ++c) {
+            if (oka) st_global_cs_v2f(ga + 64 + 8 * c, v1[4 * c] * sa, v1[4 * c + 1] * sa);
+            if (okb) st_global_cs_v2f(gb + 64 + 8 * c, v1[4 * c + 2] * sb, v1[4 * c + 3] * sb);
           }
-          __syncwarp();
         }
       }
       if (r < pend.rows)
@@ -482,6 +449,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       group_sync(grp);  // all of the group read the info before the stage may be refilled
       if (r == 0) mbar_arrive(&c.kv_empty[st]);
       const int ntiles = (inf.n + per_tile - 1) / per_tile;
+      bool first = true;  // this group's first tile of the item
       for (int t = 0; t < ntiles && ok; ++t, ++j) {
         if ((j & 1) != grp) continue;
         // ---- gather this tile's q rows: the loads go to registers first
@@ -510,7 +478,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           v[i] = src_row >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.q + (size_t)src_row * 256) + (wl & 15))
                               : make_uint4(0, 0, 0, 0);
         }
-        // this group's buffer (and O) are free once its previous tile's p v is done
+        // this group's buffer (P of its previous tile) and O are free once
+        // that tile's p v is done
         if (pend_j >= 0) {
           ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
                                    kWaitLimitNs),
@@ -518,17 +487,21 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           if (!ok) break;
           tc_fence_after();
         }
-        if (pend_j >= 0) epilogue();
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           st_shared_v4(qp + swz(wrow0 + 2 * i + (wl >> 4), wl & 15), v[i].x, v[i].y, v[i].z, v[i].w);
-        if (t == 0 && !a.kv_fp8 && r >= inf.valid) {
-          // keys past the sequence end must not bring stale values into P V
+        if (first && !a.kv_fp8 && r >= inf.valid) {
+          // keys past the sequence end must not bring stale values (they may
+          // be NaN bit patterns) into P V.  Both groups zero the rows before
+          // their own first p v of the item: zeros written twice are harmless,
+          // and neither group's p v then depends on the other's progress.
           const uint32_t vs = sbase + kOffKV + st * kStageBytes + kTileBytes;
           for (int ch = 0; ch < 16; ++ch) st_shared_v4(vs + swz(r, ch), 0, 0, 0, 0);
         }
+        first = false;
         fence_proxy_async_smem();
         mbar_arrive(&c.q_full[grp]);
+        if (pend_j >= 0) epilogue();
         // ---- softmax of the row
         ok = group_all(mbar_wait(&c.s_full[grp], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
                        grp);
@@ -589,7 +562,6 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         epilogue();
       }
     }
-    if (r == 0) bulk_wait_group_all();  // this group's partial stores are complete
   }
   tc_fence_before();
   __syncthreads();
@@ -601,8 +573,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
 // columns) is allocated once for both phases.
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-          const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo, FwdArgs a,
-          dec::DecArgs d) {
+          const __grid_constant__ CUtensorMap tmq, FwdArgs a, dec::DecArgs d) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint32_t s_tmem;
@@ -626,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   if (has_dec) dec::decode_body<16>(tmk, tmv, tmq, d, sm, tmem);
-  if (has_kvs) kv_stationary_body(tmk, tmv, tmo, a, sm, tmem);
+  if (has_kvs) kv_stationary_body(tmk, tmv, a, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -645,19 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // 3-D view of a cache [pages * Hkv][page_size][128]: box = one page, one
 // 128-byte column slab (64 x 16-bit, swizzled) or the full 128 e4m3 row.
-// 2-D view of the FP32 partial rows [rows][128]: box = 32 columns x 128
-// rows, 128B-swizzled (the epilogue's staging layout).
-bool make_partial_map(CUtensorMap* m, float* part_o, long long n_rows) {
-  auto fn = dec::encode_fn();
-  if (!fn || n_rows < 128) return false;
-  cuuint64_t dims[2] = {128, (cuuint64_t)n_rows};
-  cuuint64_t strides[1] = {512};
-  cuuint32_t box[2] = {32, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
 
 bool make_cache_map(CUtensorMap* m, const void* base, const mxsa_problem& p) {
   auto fn = dec::encode_fn();
@@ -720,12 +678,6 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.sch_hdr_mut = sc.hdr;
   a.claim = sc.hdr + kSchClaim;
   a.part_o = part_o;
-  CUtensorMap tmo;
-  std::memset(&tmo, 0, sizeof(tmo));
-  a.tma_store = make_partial_map(&tmo, part_o,
-                                 (long long)p.total_q * p.num_kv_heads * p.topk * (p.num_q_heads / p.num_kv_heads))
-                    ? 1
-                    : 0;
   a.part_lse = part_lse;
   a.flags = ix.hdr + kHdrFlags;
   a.num_seqs = p.num_seqs;
@@ -742,7 +694,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmo, a, d);
+  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, a, d);
 }
 
 }  // namespace mxsa
