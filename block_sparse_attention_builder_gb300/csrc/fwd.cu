@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -74,6 +75,7 @@ struct FwdArgs {
   float* part_lse;
   int32_t* flags;
   int32_t num_seqs, Hq, Hkv, G, topk, page_size, max_pages, num_pages, causal, kv_fp8, ab_bf16, per_tile;
+  int32_t q_tma;      // q rows of a tile come by TMA (G % 8 == 0; the map tmqs exists)
   int32_t* claim;     // schedule header word: next item to claim
   int32_t* sch_hdr_mut;  // the schedule header (claim and exit counters)
   float scale_log2;
@@ -186,7 +188,8 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
 // Runs the CTA's KV-stationary items (all kThreads threads; 1024-aligned
 // shared memory `sm`; TMEM base `tmem` with 512 columns).
 __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
-                                                   const FwdArgs& a, uint8_t* sm, uint32_t tmem) {
+                                                   const CUtensorMap& tmqs, const FwdArgs& a, uint8_t* sm,
+                                                   uint32_t tmem) {
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Items are claimed dynamically (a global counter), in item order, by the
@@ -201,7 +204,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       // a stage is refilled after both MMA issuers committed it and both
       // softmax groups read its info (so no role lags two phases behind)
       mbar_init(&c.kv_empty[i], 4);
-      mbar_init(&c.q_full[i], 128);
+      mbar_init(&c.q_full[i], a.q_tma ? 1 : 128);  // TMA: one arrival plus the bytes
       mbar_init(&c.s_full[i], 1);
       mbar_init(&c.p_full[i], 128);
       mbar_init(&c.o_full[i], 1);
@@ -370,6 +373,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     const int wl = tid & 31, wrow0 = (warp & 3) * 32;  // lane; the warp's first tile row
     RowState pend{0, -INFINITY, 0.f, 0};
     int pend_j = -1;
+    int jq = -1;  // the group's last tile whose q rows were requested by TMA
     // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l)
     // ln 2.  O is read in the 16x256b shape, in which four consecutive lanes
     // hold 8 consecutive columns of one row, so every store instruction
@@ -452,9 +456,6 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       bool first = true;  // this group's first tile of the item
       for (int t = 0; t < ntiles && ok; ++t, ++j) {
         if ((j & 1) != grp) continue;
-        // ---- gather this tile's q rows: the loads go to registers first
-        // (their latency overlaps the wait for the previous tile's p v), then
-        // the previous tile's epilogue, then the shared-memory stores
         const int et0 = inf.e0 + t * per_tile;
         const int ne = min(per_tile, inf.n - t * per_tile);
         const int rows = ne * a.G;
@@ -469,39 +470,69 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           lim = inf.valid;
           if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
         }
-        // coalesced gather: in round i the two half-warps read whole 256-byte
-        // q rows (the warp's rows 2i and 2i + 1, one 16-byte chunk per lane)
-        uint4 v[16];
+        // ---- this tile's q rows into the group's buffer, which (with O) is
+        // free once the group's previous tile's p v is done
+        if (a.q_tma) {
+          // by TMA: an entry's G rows (its token, this kv head's q heads) are
+          // consecutive q rows, one box per 64-column half, landing at whole
+          // 1024-byte swizzle atoms (G is a multiple of 8).  Rows past the
+          // tile's entries keep stale values: their rows of S, P and O are
+          // never stored.
+          int tok = 0;
+          if ((warp & 3) == 0 && wl < ne) tok = a.entries[et0 + wl] / (a.Hkv * a.topk);
+          if (pend_j >= 0) {
+            ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                     kWaitLimitNs),
+                           grp);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          if ((warp & 3) == 0) {
+            if (wl == 0) mbar_arrive_expect_tx(&c.q_full[grp], (uint32_t)rows * 256u);
+            __syncwarp();
+            if (wl < ne) {
+              uint8_t* dst = sm + kOffQP + grp * kTileBytes + wl * a.G * 128;
+              const int row0 = tok * a.Hq + inf.g * a.G;
+              tma_load_2d(dst, &tmqs, &c.q_full[grp], 0, row0);
+              tma_load_2d(dst + 16384, &tmqs, &c.q_full[grp], 64, row0);
+            }
+          }
+          jq = j;
+        } else {
+          // coalesced gather: in round i the two half-warps read whole
+          // 256-byte q rows (the warp's rows 2i and 2i + 1, one 16-byte chunk
+          // per lane); the loads' latency overlaps the wait for the p v
+          uint4 v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int src_row = __shfl_sync(0xffffffffu, qrow, 2 * i + (wl >> 4));
-          v[i] = src_row >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.q + (size_t)src_row * 256) + (wl & 15))
-                              : make_uint4(0, 0, 0, 0);
-        }
-        // this group's buffer (P of its previous tile) and O are free once
-        // that tile's p v is done
-        if (pend_j >= 0) {
-          ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                                   kWaitLimitNs),
-                         grp);
-          if (!ok) break;
-          tc_fence_after();
-        }
+          for (int i = 0; i < 16; ++i) {
+            const int src_row = __shfl_sync(0xffffffffu, qrow, 2 * i + (wl >> 4));
+            v[i] = src_row >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.q + (size_t)src_row * 256) + (wl & 15))
+                                : make_uint4(0, 0, 0, 0);
+          }
+          if (pend_j >= 0) {
+            ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                     kWaitLimitNs),
+                           grp);
+            if (!ok) break;
+            tc_fence_after();
+          }
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          st_shared_v4(qp + swz(wrow0 + 2 * i + (wl >> 4), wl & 15), v[i].x, v[i].y, v[i].z, v[i].w);
+          for (int i = 0; i < 16; ++i)
+            st_shared_v4(qp + swz(wrow0 + 2 * i + (wl >> 4), wl & 15), v[i].x, v[i].y, v[i].z, v[i].w);
+          fence_proxy_async_smem();
+          mbar_arrive(&c.q_full[grp]);
+        }
+        if (pend_j >= 0) epilogue();
         if (first && !a.kv_fp8 && r >= inf.valid) {
           // keys past the sequence end must not bring stale values (they may
           // be NaN bit patterns) into P V.  Both groups zero the rows before
-          // their own first p v of the item: zeros written twice are harmless,
-          // and neither group's p v then depends on the other's progress.
+          // their own first p v of the item (the fence before p_full orders
+          // the stores): zeros written twice are harmless, and neither
+          // group's p v then depends on the other's progress.
           const uint32_t vs = sbase + kOffKV + st * kStageBytes + kTileBytes;
           for (int ch = 0; ch < 16; ++ch) st_shared_v4(vs + swz(r, ch), 0, 0, 0, 0);
         }
         first = false;
-        fence_proxy_async_smem();
-        mbar_arrive(&c.q_full[grp]);
-        if (pend_j >= 0) epilogue();
         // ---- softmax of the row
         ok = group_all(mbar_wait(&c.s_full[grp], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
                        grp);
@@ -562,6 +593,10 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         epilogue();
       }
     }
+    // q rows requested by TMA have landed before the CTA may exit (after an
+    // abort the issuer may not have waited for them)
+    if (jq >= 0 && (warp & 3) == 0 && wl == 0)
+      mbar_drain(&c.q_full[grp], (jq >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
   }
   tc_fence_before();
   __syncthreads();
@@ -573,7 +608,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
 // columns) is allocated once for both phases.
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-          const __grid_constant__ CUtensorMap tmq, FwdArgs a, dec::DecArgs d) {
+          const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmqs, FwdArgs a,
+          dec::DecArgs d) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint32_t s_tmem;
@@ -597,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   if (has_dec) dec::decode_body<16>(tmk, tmv, tmq, d, sm, tmem);
-  if (has_kvs) kv_stationary_body(tmk, tmv, a, sm, tmem);
+  if (has_kvs) kv_stationary_body(tmk, tmv, tmqs, a, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -680,6 +716,12 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.part_o = part_o;
   a.part_lse = part_lse;
   a.flags = ix.hdr + kHdrFlags;
+  // q rows of the KV-stationary tiles: a box of one entry's G rows when G
+  // is a multiple of 8 (whole swizzle atoms), else the warps' gather
+  const int G = p.num_q_heads / p.num_kv_heads;
+  CUtensorMap tmqs;
+  std::memset(&tmqs, 0, sizeof(tmqs));
+  a.q_tma = (G % 8 == 0 && G <= 128 && dec::make_q_map(&tmqs, q, p, G)) ? 1 : 0;
   a.num_seqs = p.num_seqs;
   a.Hq = p.num_q_heads;
   a.Hkv = p.num_kv_heads;
@@ -694,7 +736,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, a, d);
+  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
 }
 
 }  // namespace mxsa
