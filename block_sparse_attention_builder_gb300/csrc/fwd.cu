@@ -8,10 +8,11 @@
 //   warps 0-3, 4-7  two softmax warpgroups; the CTA's tiles alternate
 //              between them (tile j -> warpgroup j % 2) so that one group's
 //              softmax overlaps the other group's MMAs, loads and stores.
-//              Per tile a group gathers the tile's q rows into its buffer,
-//              turns S = q k^T (TMEM) into P = exp(S - m) written over the q
-//              rows (q is no longer needed once q k^T has run), and after
-//              O = P v writes o = O / l and lse per row.  Row r of a tile is
+//              Per tile a group brings the tile's q rows into its buffer
+//              (TMA boxes, or a warp gather when G is not a multiple of 8),
+//              turns S = q k^T (TMEM) into P = exp(S - m), written back to
+//              TMEM over S as the p v operand, and after O = P v writes
+//              o = O / l and lse per row straight from TMEM.  Row r of a tile is
 //              thread r of its group and TMEM lane r.  For FP8 caches
 //              warpgroup n % 2 widens the staged e4m3 block of the CTA's
 //              n-th item to BF16/FP16 in the stage (exactly), whether or
@@ -24,8 +25,9 @@
 //              accumulate in TMEM: S and O of each group, 512 columns owned
 //              by warp 9): q k^T then p v of each of the group's tiles.
 //
-// Shared-memory operands use the 128-byte swizzled K-major layout (q, K, P)
-// and the 128-byte swizzled MN-major layout (V as the B operand of P V).
+// Shared-memory operands use the 128-byte swizzled K-major layout (q, K)
+// and the 128-byte swizzled MN-major layout (V as the B operand of P V);
+// P is the TMEM (A) operand of P V.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -83,7 +85,7 @@ struct FwdArgs {
 
 // smem offsets from the 1024-aligned base
 constexpr uint32_t kOffKV = 0;                            // 2 stages x (K, V)
-constexpr uint32_t kOffQP = 2 * kStageBytes;              // 2 groups x (q, then p) tile
+constexpr uint32_t kOffQP = 2 * kStageBytes;              // 2 groups x q tile
 constexpr uint32_t kOffStg = kOffQP + 2 * kTileBytes;     // FP8 staging (K, V e4m3), 32 KB
 constexpr uint32_t kCtrlBf16 = kOffStg;
 constexpr uint32_t kCtrlFp8 = kOffStg + kTileBytes;
@@ -148,17 +150,17 @@ struct RowState {
 };
 
 // P = exp2(S * scale_log2 - m2) of one row over 64 of the block's keys
-// (half h: keys 64h .. 64h + 63, S values in sv), packed to the MMA operand
-// type and written to the row's swizzled slots; returns the partial row sum.
+// (half h: keys 64h .. 64h + 63, S values in sv), packed in pairs to the MMA
+// operand type and written to TMEM columns tP + 32h .. + 31 of the row's
+// lane (over S columns already read); returns the partial row sum.
 // kFull: every key is visible (no length or causal limit).
 template <bool kBf16, bool kFull>
 __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float scale_log2, float m2, int lim,
-                                                 uint32_t qp, int r) {
+                                                 uint32_t tP) {
   float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+  uint32_t pk[32];
 #pragma unroll
   for (int cl = 0; cl < 8; ++cl) {
-    const int ch = 8 * h + cl;
-    uint32_t pk[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int kl = cl * 8 + 2 * i, k0 = 64 * h + kl;
@@ -174,14 +176,14 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
       if (i == 3) l3 += p0 + p1;
       if (kBf16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        pk[4 * cl + i] = *reinterpret_cast<uint32_t*>(&h);
       } else {
         __half2 h = __floats2half2_rn(p0, p1);
-        pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        pk[4 * cl + i] = *reinterpret_cast<uint32_t*>(&h);
       }
     }
-    st_shared_v4(qp + swz(r, ch), pk[0], pk[1], pk[2], pk[3]);
   }
+  tmem_st32(tP + 32 * h, pk);
   return (l0 + l1) + (l2 + l3);
 }
 
@@ -309,8 +311,9 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
   } else if (warp >= kMmaWarp) {
     // ---------------------------------------------------------- MMA issuers
     // Warp 9 + g (lane 0) issues the MMAs of softmax group g (its tiles
-    // j = g, g + 2, ...):
-    // q k^T once the group gathered the tile's q, then p v once it wrote P.
+    // j = g, g + 2, ...): q k^T once the tile's q rows are in and the
+    // group's previous p v is done (P is kept in TMEM over S), then p v,
+    // with P as the TMEM operand, once the group wrote P.
     // Each issuer waits only on its own group, so one group's MMAs never
     // queue behind the other group's inputs; a stage is released after both
     // issuers committed it (kv_empty counts two arrivals).
@@ -318,9 +321,9 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       const int g = warp - kMmaWarp;
       const uint32_t id_qk = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 0);
       const uint32_t id_pv = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 1);
-      const uint32_t q_s = sbase + kOffQP + g * kTileBytes;  // q, then P, of group g
+      const uint32_t q_s = sbase + kOffQP + g * kTileBytes;  // q rows of group g
       const uint32_t tS = tmem + g * 256, tO = tS + 128;
-      int n = 0, j = 0;
+      int n = 0, j = 0, jprev = -1;
       bool ok = true;
       for (; ok; ++n) {
         const int st = n & 1, use = n >> 1;
@@ -335,6 +338,10 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           if ((j & 1) != g) continue;
           ok = mbar_wait(&c.q_full[g], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
+          if (jprev >= 0) {  // S is overwritten only after the previous p v read P
+            ok = mbar_wait(&c.o_full[g], (jprev >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (!ok) break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -346,12 +353,10 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
-            mma_f16_ss(tO, smem_desc_sw128(q_s + off, 0, 1024), smem_desc_sw128(v_s + ks * 2048u, 16384, 1024),
-                       id_pv, ks > 0);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(tO, tS + ks * 8, smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), id_pv, ks > 0);
           mma_commit(&c.o_full[g]);
+          jprev = j;
         }
         if (ok) mma_commit(&c.kv_empty[st]);  // this issuer's share of the stage is done
       }
@@ -470,24 +475,17 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           lim = inf.valid;
           if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
         }
-        // ---- this tile's q rows into the group's buffer, which (with O) is
-        // free once the group's previous tile's p v is done
+        // ---- this tile's q rows into the group's buffer, free since the
+        // group's previous q k^T completed (it waited for that S)
         if (a.q_tma) {
           // by TMA: an entry's G rows (its token, this kv head's q heads) are
           // consecutive q rows, one box per 64-column half, landing at whole
           // 1024-byte swizzle atoms (G is a multiple of 8).  Rows past the
           // tile's entries keep stale values: their rows of S, P and O are
           // never stored.
-          int tok = 0;
-          if ((warp & 3) == 0 && wl < ne) tok = a.entries[et0 + wl] / (a.Hkv * a.topk);
-          if (pend_j >= 0) {
-            ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                                     kWaitLimitNs),
-                           grp);
-            if (!ok) break;
-            tc_fence_after();
-          }
           if ((warp & 3) == 0) {
+            int tok = 0;
+            if (wl < ne) tok = a.entries[et0 + wl] / (a.Hkv * a.topk);
             if (wl == 0) mbar_arrive_expect_tx(&c.q_full[grp], (uint32_t)rows * 256u);
             __syncwarp();
             if (wl < ne) {
@@ -501,7 +499,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         } else {
           // coalesced gather: in round i the two half-warps read whole
           // 256-byte q rows (the warp's rows 2i and 2i + 1, one 16-byte chunk
-          // per lane); the loads' latency overlaps the wait for the p v
+          // per lane)
           uint4 v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -509,20 +507,21 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
             v[i] = src_row >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.q + (size_t)src_row * 256) + (wl & 15))
                                 : make_uint4(0, 0, 0, 0);
           }
-          if (pend_j >= 0) {
-            ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                                     kWaitLimitNs),
-                           grp);
-            if (!ok) break;
-            tc_fence_after();
-          }
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             st_shared_v4(qp + swz(wrow0 + 2 * i + (wl >> 4), wl & 15), v[i].x, v[i].y, v[i].z, v[i].w);
           fence_proxy_async_smem();
           mbar_arrive(&c.q_full[grp]);
         }
-        if (pend_j >= 0) epilogue();
+        if (pend_j >= 0) {
+          // the previous tile's O is complete once its p v is done
+          ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                   kWaitLimitNs),
+                         grp);
+          if (!ok) break;
+          tc_fence_after();
+          epilogue();
+        }
         if (first && !a.kv_fp8 && r >= inf.valid) {
           // keys past the sequence end must not bring stale values (they may
           // be NaN bit patterns) into P V.  Both groups zero the rows before
@@ -571,14 +570,15 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
             tmem_ld32(tS + h * 64 + 32, sv + 32);
             tmem_ld_wait();
             if (bf16)
-              l += full ? softmax_store_p<true, true>(sv, h, a.scale_log2, m2, lim, qp, r)
-                        : softmax_store_p<true, false>(sv, h, a.scale_log2, m2, lim, qp, r);
+              l += full ? softmax_store_p<true, true>(sv, h, a.scale_log2, m2, lim, tS)
+                        : softmax_store_p<true, false>(sv, h, a.scale_log2, m2, lim, tS);
             else
-              l += full ? softmax_store_p<false, true>(sv, h, a.scale_log2, m2, lim, qp, r)
-                        : softmax_store_p<false, false>(sv, h, a.scale_log2, m2, lim, qp, r);
+              l += full ? softmax_store_p<false, true>(sv, h, a.scale_log2, m2, lim, tS)
+                        : softmax_store_p<false, false>(sv, h, a.scale_log2, m2, lim, tS);
           }
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();            // P is in TMEM
+        fence_proxy_async_smem();  // the zeroed V rows are visible to the MMA
         tc_fence_before();
         mbar_arrive(&c.p_full[grp]);
         pend = RowState{(size_t)et0 * a.G, m2, l, rows};
