@@ -55,13 +55,19 @@ struct ItemInfo {
   int32_t g, s, b, valid, e0, n, L, tq, q_begin, pad0, pad1, pad2, pad3, pad4, pad5, pad6;
 };
 
+constexpr int kMaxItemEntries = MXSA_ITEM_TILES * (MXSA_TILE_ROWS / 8);
+
 struct Ctrl {
   // stg_full[n % 2]: item n staged.  One barrier per widening group, so
   // that each group waits for every phase of its own barrier in order.
   uint64_t kv_full[2], kv_empty[2], stg_full[2], stg_empty, q_full[2], s_full[2], p_full[2], o_full[2], done;
+  uint64_t epi_turn[2];  // epi_turn[g]: the other group finished an epilogue
   uint32_t tmem_base;
   int32_t abort_flag;
   ItemInfo info[2];
+  // the tokens of each stage's item entries when q comes by TMA (G >= 8:
+  // at most 4 tiles x 16 entries)
+  int32_t tok[2][kMaxItemEntries];
 };
 
 struct FwdArgs {
@@ -123,6 +129,15 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
   __half2 h = *reinterpret_cast<__half2*>(&h2);
   float2 f = __half22float2(h);  // exact
   return pack2(f.x, f.y, 1);     // exact: e4m3 values are representable in bf16
+}
+
+// The tile entry whose q boxes lane `wl` of warp `w` (0..3) of a softmax
+// group issues: warp w holds tile rows 32w .. 32w + 31, and an entry's G rows
+// start at row e * G, so its entries are those starting in that range (for
+// G > 32 some warps have none).  A value past the tile's entries means none.
+__device__ __forceinline__ int qbox_entry(int w, int wl, int G) {
+  const int first = (32 * w + G - 1) / G, last = (32 * w + 32 + G - 1) / G;  // [first, last)
+  return first + wl < last ? first + wl : 1 << 30;
 }
 
 // named barrier (id 1 + group) over the 128 threads of one softmax group
@@ -212,6 +227,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       mbar_init(&c.o_full[i], 1);
       mbar_init(&c.stg_full[i], 1);
     }
+    mbar_init(&c.epi_turn[0], 128);
+    mbar_init(&c.epi_turn[1], 128);
     mbar_init(&c.stg_empty, 128);
     mbar_init(&c.done, 2);
     c.abort_flag = 0;
@@ -224,28 +241,47 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Lane 0 claims, decodes and loads the items; on the TMA q path the warp
+    // first copies the item's entry tokens next to its info, so that the
+    // softmax groups read them from shared memory.
     if (lane == 0) {
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      const int NB = a.idx_hdr[kHdrNB];
-      const int ps = a.page_size;
-      const int npg = ps == 128 ? 1 : 2;
-      int n = 0;
-      bool ok = true, ended = false;
-      int it = atomicAdd(a.claim, 1);
-      for (; ok; ++n) {
-        const int st = n & 1, use = n >> 1;
+      if (a.q_tma) tma_prefetch_desc(&tmqs);
+    }
+    const int NB = a.idx_hdr[kHdrNB];
+    const int ps = a.page_size;
+    const int npg = ps == 128 ? 1 : 2;
+    const int tok_div = a.Hkv * a.topk;
+    int n = 0;
+    bool ok = true, ended = false;
+    int it = 0;
+    if (lane == 0) it = atomicAdd(a.claim, 1);
+    it = __shfl_sync(0xffffffffu, it, 0);
+    for (; ok; ++n) {
+      const int st = n & 1, use = n >> 1;
+      if (lane == 0)
         ok = mbar_wait(&c.kv_empty[st], (use & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        if (!ok) break;
-        if (it >= n_items) {  // no item left: publish the end
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (it >= n_items) {  // no item left: publish the end
+        if (lane == 0) {
           ItemInfo end{};
           c.info[st] = end;
           mbar_arrive(a.kv_fp8 ? &c.stg_full[st] : &c.kv_full[st]);
-          ended = true;
-          break;
         }
-        const int next = atomicAdd(a.claim, 1);  // claimed one item ahead: its latency overlaps this item
-        const int4 itm = a.items[it];
+        ended = true;
+        break;
+      }
+      int next = 0;
+      if (lane == 0) next = atomicAdd(a.claim, 1);  // claimed one item ahead: its latency overlaps this item
+      const int4 itm = a.items[it];
+      if (a.q_tma) {
+        const int ne = min(itm.z, kMaxItemEntries);
+        for (int e = lane; e < ne; e += 32) c.tok[st][e] = __ldg(a.entries + itm.y + e) / tok_div;
+      }
+      __syncwarp();  // the tokens are written before lane 0 publishes the item
+      if (lane == 0) {
         const int key = itm.x;
         const int g = key / NB, r = key - g * NB;
         const int s = seq_of_block(a.seq, a.num_seqs, r);
@@ -285,24 +321,29 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           // FP8: into the staging tile once the previous block was widened
           // out of it (stg_empty); the widening group fills the stage
           ok = mbar_wait(&c.stg_empty, (n & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (!ok) break;
-          uint8_t* stg = sm + kOffStg;
-          uint64_t* sf = &c.stg_full[st];
-          mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
-          for (int pg = 0; pg < npg; ++pg) {
-            if (pages[pg] < 0) continue;
-            const int z = pages[pg] * a.Hkv + g;
-            tma_load_3d(stg + pg * 8192, &tmk, sf, 0, 0, z);
-            tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
+          if (ok) {
+            uint8_t* stg = sm + kOffStg;
+            uint64_t* sf = &c.stg_full[st];
+            mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
+            for (int pg = 0; pg < npg; ++pg) {
+              if (pages[pg] < 0) continue;
+              const int z = pages[pg] * a.Hkv + g;
+              tma_load_3d(stg + pg * 8192, &tmk, sf, 0, 0, z);
+              tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
+            }
           }
         }
-        it = next;
       }
-      // drain: every load this thread issued has landed before the CTA may
-      // exit.  After the end item (published on stage n % 2) item n - 2 has
-      // landed for sure (its stage was released for the end item), and its
-      // barrier has moved on, so only item n - 1 is waited for.  FP8:
-      // staging item n - 1 needed item n - 2 widened, so only n - 1.
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;  // FP8 staging gave up: item n issued no loads
+      it = __shfl_sync(0xffffffffu, next, 0);
+    }
+    // drain: every load lane 0 issued has landed before the CTA may exit.
+    // After the end item (published on stage n % 2) item n - 2 has landed
+    // for sure (its stage was released for the end item), and its barrier
+    // has moved on, so only item n - 1 is waited for.  FP8: staging item
+    // n - 1 needed item n - 2 widened, so only n - 1.
+    if (lane == 0) {
       const int k0 = (ended || a.kv_fp8) ? n - 1 : n - 2;
       for (int k = std::max(0, k0); k < n; ++k)
         mbar_drain(a.kv_fp8 ? &c.stg_full[k & 1] : &c.kv_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT,
@@ -384,7 +425,19 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     // hold 8 consecutive columns of one row, so every store instruction
     // writes eight whole 32-byte sectors (8 rows x 32 B) straight from
     // registers; it runs while the next tile's q k^T is in flight.
-    auto epilogue = [&]() {
+    // The groups take turns at the epilogue, in tile order (tile j's after
+    // tile j - 1's), so that one group's stores run while the other group
+    // computes instead of both groups storing at once at half the rate.
+    int n_epi = 0;  // epilogues this group has run
+    auto epilogue = [&]() -> bool {
+      // this group's epilogue m is tile 2m + grp; it follows tile 2m + grp - 1
+      const int m = n_epi;
+      if (grp == 1 || m > 0) {
+        const int ph = grp == 1 ? m : m - 1;  // the other group's epilogue it waits for
+        if (!group_all(mbar_wait(&c.epi_turn[grp], ph & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
+                       grp))
+          return false;
+      }
       const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
       if (wrow0 < pend.rows) {  // a warp of padding rows has nothing to store
 #pragma unroll
@@ -414,6 +467,9 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         __stcs(&a.part_lse[pend.orow0 + r],
                pend.l > 0.f ? (pend.m2 + lg2_approx(pend.l)) * 0.69314718055994530942f : -INFINITY);
       tc_fence_before();
+      mbar_arrive(&c.epi_turn[grp ^ 1]);  // the other group's turn
+      ++n_epi;
+      return true;
     };
     for (; ok; ++n) {
       const int st = n & 1, use = n >> 1;
@@ -455,48 +511,56 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       if (!ok) break;
       const ItemInfo inf = c.info[st];
       if (inf.n == 0) break;  // the end
+      const int ntiles = (inf.n + per_tile - 1) / per_tile;
+      // TMA q path: the tokens this thread needs for the group's tiles of
+      // the item (at most two: an item has at most 4 tiles), taken from the
+      // producer's copy before the stage is let go: row r's (for its key
+      // limit) and the entry whose q boxes this lane issues
+      const int qe = qbox_entry(warp & 3, wl, a.G);
+      int tk_row0 = -1, tk_row1 = -1, tk_box0 = 0, tk_box1 = 0;
+      if (a.q_tma) {
+        const int t0 = (j & 1) == grp ? 0 : 1;  // the group's first tile of the item
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int t = t0 + 2 * i;
+          if (t >= ntiles) break;
+          const int ne = min(per_tile, inf.n - t * per_tile);
+          const int tr = r < ne * a.G ? c.tok[st][t * per_tile + r / a.G] : -1;
+          const int tb = qe < ne ? c.tok[st][t * per_tile + qe] : 0;
+          if (i == 0) { tk_row0 = tr; tk_box0 = tb; } else { tk_row1 = tr; tk_box1 = tb; }
+        }
+      }
       group_sync(grp);  // all of the group read the info before the stage may be refilled
       if (r == 0) mbar_arrive(&c.kv_empty[st]);
-      const int ntiles = (inf.n + per_tile - 1) / per_tile;
       bool first = true;  // this group's first tile of the item
       for (int t = 0; t < ntiles && ok; ++t, ++j) {
         if ((j & 1) != grp) continue;
         const int et0 = inf.e0 + t * per_tile;
         const int ne = min(per_tile, inf.n - t * per_tile);
         const int rows = ne * a.G;
-        // row r's q row (token, head) and key limit; -1: padding row
-        int lim = 0, qrow = -1;
-        if (r < rows) {
-          const int e = et0 + r / a.G, hh = r % a.G;
-          const int slot = a.entries[e];
-          const int tok = slot / (a.Hkv * a.topk);
-          qrow = tok * a.Hq + inf.g * a.G + hh;
-          const int pos = inf.L - inf.tq + (tok - inf.q_begin);
-          lim = inf.valid;
-          if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
-        }
+        // row r's token (-1: padding row), which gives its q row and key
+        // limit: from the copy above, or (warp gather path) the entry list
+        int tok = (t >> 1) ? tk_row1 : tk_row0;
+        if (!a.q_tma) tok = r < rows ? __ldg(a.entries + et0 + r / a.G) / (a.Hkv * a.topk) : -1;
         // ---- this tile's q rows into the group's buffer, free since the
         // group's previous q k^T completed (it waited for that S)
         if (a.q_tma) {
           // by TMA: an entry's G rows (its token, this kv head's q heads) are
           // consecutive q rows, one box per 64-column half, landing at whole
-          // 1024-byte swizzle atoms (G is a multiple of 8).  Rows past the
-          // tile's entries keep stale values: their rows of S, P and O are
-          // never stored.
-          if ((warp & 3) == 0) {
-            int tok = 0;
-            if (wl < ne) tok = a.entries[et0 + wl] / (a.Hkv * a.topk);
-            if (wl == 0) mbar_arrive_expect_tx(&c.q_full[grp], (uint32_t)rows * 256u);
-            __syncwarp();
-            if (wl < ne) {
-              uint8_t* dst = sm + kOffQP + grp * kTileBytes + wl * a.G * 128;
-              const int row0 = tok * a.Hq + inf.g * a.G;
-              tma_load_2d(dst, &tmqs, &c.q_full[grp], 0, row0);
-              tma_load_2d(dst + 16384, &tmqs, &c.q_full[grp], 64, row0);
-            }
+          // 1024-byte swizzle atoms (G is a multiple of 8).  The warp holding
+          // an entry's first row issues its boxes, so the four warps share
+          // the issue.  Rows past the tile's entries keep stale values: their
+          // rows of S, P and O are never stored.
+          if (r == 0) mbar_arrive_expect_tx(&c.q_full[grp], (uint32_t)rows * 256u);
+          if (qe < ne) {
+            uint8_t* dst = sm + kOffQP + grp * kTileBytes + qe * a.G * 128;
+            const int row0 = ((t >> 1) ? tk_box1 : tk_box0) * a.Hq + inf.g * a.G;
+            tma_load_2d(dst, &tmqs, &c.q_full[grp], 0, row0);
+            tma_load_2d(dst + 16384, &tmqs, &c.q_full[grp], 64, row0);
           }
           jq = j;
         } else {
+          const int qrow = tok >= 0 ? tok * a.Hq + inf.g * a.G + r % a.G : -1;
           // coalesced gather: in round i the two half-warps read whole
           // 256-byte q rows (the warp's rows 2i and 2i + 1, one 16-byte chunk
           // per lane)
@@ -520,7 +584,14 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
                          grp);
           if (!ok) break;
           tc_fence_after();
-          epilogue();
+          ok = epilogue();
+          if (!ok) break;
+        }
+        int lim = 0;
+        if (tok >= 0) {
+          const int pos = inf.L - inf.tq + (tok - inf.q_begin);
+          lim = inf.valid;
+          if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
         }
         if (first && !a.kv_fp8 && r >= inf.valid) {
           // keys past the sequence end must not bring stale values (they may
@@ -590,7 +661,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
       if (ok) {
         tc_fence_after();
-        epilogue();
+        ok = epilogue();
       }
     }
     // q rows requested by TMA have landed before the CTA may exit (after an
