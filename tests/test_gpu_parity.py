@@ -38,6 +38,12 @@ def small_cases():
         "mha_fp16_fp8": W.custom("mha_fp16_fp8", [3, 4], [640, 1111], 4, 4, 128, 4, True, "uniform", 106,
                                  q_dtype="fp16", kv_dtype="fp8"),
         "decode_edges": _decode_edge_workload(),
+        # G = 32 and 64: the KV-stationary q boxes of an entry span one or
+        # two warps' rows (decode rows go through the tile path too: G > 16)
+        "g32_prefill": W.custom("g32_prefill", [1, 37, 90], [700, 1500, 2600], 32, 1, 128, 5, True, "zipf_diag",
+                                110),
+        "g64_mixed": W.custom("g64_mixed", [1, 3, 20], [200, 900, 1300], 64, 1, 64, 4, True, "uniform", 111,
+                              q_dtype="fp16", kv_dtype="fp16"),
     }
 
 
