@@ -8,7 +8,7 @@
 //
 // One warp per row; lane j owns columns 4j..4j+3 (one float4 of every
 // 512-byte partial row, so each partial is read as one coalesced 512-byte
-// transaction).  The row's slot -> entry map and lses are read once per
+// transaction, up to 8 of them in flight per warp).  The row's slot -> entry map and lses are read once per
 // 32 slots with one load per lane.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -21,8 +21,9 @@ namespace mxsa {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kBatch = 8;  // partial rows read ahead per warp
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
     k_combine(const int32_t* slot_entry, const float* part_o, const float* part_lse, uint8_t* out, float* lse_out,
               int total_q, int Hq, int Hkv, int topk, int out_bf16) {
   const int lane = threadIdx.x & 31;
@@ -65,16 +66,31 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         }
         unsigned live = __ballot_sync(0xffffffffu, w > 0.f);
         while (live) {
-          const int src = __ffs(live) - 1;
-          live &= live - 1;
-          const int es = __shfl_sync(0xffffffffu, e, src);
-          const float ws = __shfl_sync(0xffffffffu, w, src);
-          const float4 v = __ldcs(reinterpret_cast<const float4*>(part_o + ((long long)es * G + j) * 128) + lane);
-          acc.x = fmaf(ws, v.x, acc.x);
-          acc.y = fmaf(ws, v.y, acc.y);
-          acc.z = fmaf(ws, v.z, acc.z);
-          acc.w = fmaf(ws, v.w, acc.w);
-          W += ws;
+          // up to kBatch partial rows are requested before any is used, so
+          // that each warp keeps several 512-byte reads in flight; they are
+          // accumulated in slot order (absent ones add exact zeros)
+          float4 v[kBatch];
+          float ws[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            ws[u] = 0.f;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (live) {  // warp-uniform
+              const int src = __ffs(live) - 1;
+              live &= live - 1;
+              const int es = __shfl_sync(0xffffffffu, e, src);
+              ws[u] = __shfl_sync(0xffffffffu, w, src);
+              v[u] = __ldcs(reinterpret_cast<const float4*>(part_o + ((long long)es * G + j) * 128) + lane);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            acc.x = fmaf(ws[u], v[u].x, acc.x);
+            acc.y = fmaf(ws[u], v[u].y, acc.y);
+            acc.z = fmaf(ws[u], v[u].z, acc.z);
+            acc.w = fmaf(ws[u], v[u].w, acc.w);
+            W += ws[u];
+          }
         }
       }
     }
