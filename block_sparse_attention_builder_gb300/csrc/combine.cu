@@ -8,8 +8,8 @@
 //
 // One warp per row; lane j owns columns 4j..4j+3 (one float4 of every
 // 512-byte partial row, so each partial is read as one coalesced 512-byte
-// transaction, up to 8 of them in flight per warp).  The row's slot -> entry map and lses are read once per
-// 32 slots with one load per lane.
+// transaction, up to 8 of them in flight per warp).  The row's slot -> entry
+// map and lses are read once per 32 slots with one load per lane.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
