@@ -140,21 +140,12 @@ __device__ __forceinline__ int qbox_entry(int w, int wl, int G) {
   return first + wl < last ? first + wl : 1 << 30;
 }
 
-// named barrier (id 1 + group) over the 128 threads of one softmax group
-__device__ __forceinline__ void group_sync(int grp) {
-  asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
-}
-
-__device__ __forceinline__ bool group_all(bool v, int grp) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(1 + grp)
-      : "memory");
-  return r != 0;
-}
+// A wait's outcome made uniform across the warp (the TMEM loads and stores
+// that follow are warp-collective).  The warps of a softmax group do not
+// wait for one another: every hand-off between them and the other roles is
+// an mbarrier, and a wait that gives up raises the CTA's abort flag, which
+// ends every other wait.
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 // Per-row state a group keeps from a tile's softmax to its epilogue.  The
 // rows of a tile are consecutive partial rows: row r is orow0 + r.
@@ -218,9 +209,9 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.kv_full[i], a.kv_fp8 ? 128 : 1);  // FP8: the widening group arrives
-      // a stage is refilled after both MMA issuers committed it and both
-      // softmax groups read its info (so no role lags two phases behind)
-      mbar_init(&c.kv_empty[i], 4);
+      // a stage is refilled after both MMA issuers committed it and every
+      // softmax thread read its info (so no role lags two phases behind)
+      mbar_init(&c.kv_empty[i], 2 + 256);
       mbar_init(&c.q_full[i], a.q_tma ? 1 : 128);  // TMA: one arrival plus the bytes
       mbar_init(&c.s_full[i], 1);
       mbar_init(&c.p_full[i], 128);
@@ -434,8 +425,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       const int m = n_epi;
       if (grp == 1 || m > 0) {
         const int ph = grp == 1 ? m : m - 1;  // the other group's epilogue it waits for
-        if (!group_all(mbar_wait(&c.epi_turn[grp], ph & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
-                       grp))
+        if (!warp_all(mbar_wait(&c.epi_turn[grp], ph & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs)))
           return false;
       }
       const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
@@ -477,8 +467,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         // widen the staged e4m3 block (row r of K and V) into the stage;
         // rows past the valid tokens become zero.  The producer staged this
         // block only after kv_empty of the stage, so the stage is free.
-        ok = group_all(mbar_wait(&c.stg_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
-                       grp);
+        ok = warp_all(mbar_wait(&c.stg_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
         const int valid = c.info[st].n > 0 ? c.info[st].valid : 0;  // the end item stages nothing
         const uint8_t* stg = sm + kOffStg;
@@ -507,7 +496,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       }
       // every group reads every item's info (the tile count decides the
       // groups' alternation), then lets the stage go
-      ok = group_all(mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
+      ok = warp_all(mbar_wait(&c.kv_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
       if (!ok) break;
       const ItemInfo inf = c.info[st];
       if (inf.n == 0) break;  // the end
@@ -530,8 +519,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           if (i == 0) { tk_row0 = tr; tk_box0 = tb; } else { tk_row1 = tr; tk_box1 = tb; }
         }
       }
-      group_sync(grp);  // all of the group read the info before the stage may be refilled
-      if (r == 0) mbar_arrive(&c.kv_empty[st]);
+      mbar_arrive(&c.kv_empty[st]);  // this thread read the info and tokens
       bool first = true;  // this group's first tile of the item
       for (int t = 0; t < ntiles && ok; ++t, ++j) {
         if ((j & 1) != grp) continue;
@@ -579,9 +567,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         }
         if (pend_j >= 0) {
           // the previous tile's O is complete once its p v is done
-          ok = group_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
-                                   kWaitLimitNs),
-                         grp);
+          ok = warp_all(mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                   kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           ok = epilogue();
@@ -604,8 +591,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         }
         first = false;
         // ---- softmax of the row
-        ok = group_all(mbar_wait(&c.s_full[grp], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs),
-                       grp);
+        ok = warp_all(mbar_wait(&c.s_full[grp], (j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
         float m2 = -INFINITY, l = 0.f;
@@ -657,8 +643,8 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
       }
     }
     if (ok && pend_j >= 0) {
-      ok = group_all(
-          mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs), grp);
+      ok = warp_all(
+          mbar_wait(&c.o_full[grp], (pend_j >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
       if (ok) {
         tc_fence_after();
         ok = epilogue();
