@@ -44,6 +44,8 @@ def small_cases():
                                 110),
         "g64_mixed": W.custom("g64_mixed", [1, 3, 20], [200, 900, 1300], 64, 1, 64, 4, True, "uniform", 111,
                               q_dtype="fp16", kv_dtype="fp16"),
+        # G = 128 (the largest): one entry per tile, a 128-row q box
+        "g128_tiny": W.custom("g128_tiny", [1, 6], [300, 800], 128, 1, 64, 3, True, "uniform", 112),
     }
 
 
