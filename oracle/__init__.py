@@ -65,6 +65,11 @@ def _load():
         _lib.oracle_combine.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P]
         _lib.oracle_build_index.restype = ctypes.c_int
         _lib.oracle_build_index.argtypes = [P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
+        _lib.oracle_encode_e4m3.restype = ctypes.c_uint32
+        _lib.oracle_encode_e4m3.argtypes = [ctypes.c_double]
+        _lib.oracle_store.restype = ctypes.c_int64
+        _lib.oracle_store.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int64, P, P, P]
         _lib.oracle_schedule.restype = ctypes.c_int
         _lib.oracle_schedule.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int64, P]
@@ -102,6 +107,29 @@ def _bits(x) -> np.ndarray:
 
 def decode(dtype: str, bits: int) -> float:
     return _load().oracle_decode(DTYPE_CODE[dtype], int(bits))
+
+
+def encode_e4m3(x: float) -> int:
+    """The e4m3fn code of x clamped to [-448, 448], nearest value, ties to even."""
+    return int(_load().oracle_encode_e4m3(float(x)))
+
+
+def store(src, loc, cache, page_size: int, src_dtype: str, dst_dtype: str) -> int:
+    """Paged-cache store (the write side of the KV cache): rows of `src`
+    [n, heads, dim] (bf16/fp16, torch tensor or raw bits) into `cache`
+    [num_pages, heads, page_size, dim] (raw bits, numpy, updated in place) at
+    slots loc[t] = page * page_size + offset; loc < 0 stores nothing.  Returns
+    the number of tokens whose slot lies past the cache."""
+    lib = _load()
+    sb = _c(_bits(src), np.uint16)
+    n, heads, dim = (int(v) for v in sb.shape)
+    lo = _c(loc, np.int64)
+    assert cache.flags["C_CONTIGUOUS"] and cache.shape[1:] == (heads, page_size, dim)
+    rc = lib.oracle_store(DTYPE_CODE[src_dtype], DTYPE_CODE[dst_dtype], n, heads, dim, page_size, cache.shape[0],
+                          _ptr(lo), _ptr(sb), _ptr(cache))
+    if rc < 0:
+        raise RuntimeError(f"oracle_store failed: {rc}")
+    return int(rc)
 
 
 def attention_rows(prob: OracleProblem, q, k_cache, v_cache, selected, block_tables, cu_seqlens_q,

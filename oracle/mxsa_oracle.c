@@ -516,3 +516,82 @@ int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t*
   free(active);
   return 0;
 }
+
+/* --------------------------------------------------------------- KV store
+ * The write side of the paged cache: a sglang pull request on the same
+ * pages ("Summary": the fused K/V/index store with an unscaled
+ * bf16-to-fp8_e4m3 cast; "Verification": bit-exact against
+ * x.float().clamp(-448, 448).to(torch.float8_e4m3fn)).
+ *
+ * Row (t, h) of a source [n][heads][dim] goes to cache[page][h][off][:] with
+ * page = loc[t] / page_size and off = loc[t] % page_size, the slot layout of
+ * the paged caches [pages][heads][page_size][dim]; loc[t] < 0 stores nothing
+ * for token t.  Into a cache of the source's own dtype the bits are copied;
+ * into an e4m3 cache each value is clamped to [-448, 448] and rounded to the
+ * nearest e4m3fn value, ties to even (NaN stays NaN with its sign,
+ * S.1111.111). */
+
+/* nearest integer to y >= 0, ties to the even one */
+static double round_half_even(double y) {
+  const double f = floor(y), r = y - f;
+  if (r > 0.5) return f + 1.0;
+  if (r < 0.5) return f;
+  return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* e4m3fn: bias 7; exponent field E in 1..15 gives 2^(E-7) * (1 + m/8),
+ * E = 0 gives m * 2^-9; E = 15 with m = 7 is NaN, so the largest finite
+ * value is 2^8 * 1.75 = 448. */
+static uint8_t encode_e4m3(double x) {
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  if (isnan(x)) return (uint8_t)(sign | 0x7F);
+  double a = fabs(x);
+  if (a > 448.0) a = 448.0;
+  if (a < ldexp(1.0, -6)) {  /* the subnormal range: steps of 2^-9 */
+    const double r = round_half_even(a / ldexp(1.0, -9));  /* 0..8; 8 is the smallest normal */
+    return (uint8_t)(sign | (uint8_t)r);
+  }
+  int e2;
+  frexp(a, &e2);  /* a = f * 2^e2, f in [0.5, 1) */
+  int k = e2 - 1; /* a in [2^k, 2^(k+1)) */
+  double r = round_half_even(a / ldexp(1.0, k - 3));  /* 8..16 */
+  if (r == 16.0) {
+    r = 8.0;
+    ++k;
+  }
+  const int E = k + 7, m = (int)r - 8;
+  return (uint8_t)(sign | (uint8_t)(E << 3) | (uint8_t)m);
+}
+
+uint32_t oracle_encode_e4m3(double x) { return encode_e4m3(x); }
+
+/* Stores n tokens' rows of `src` ([n][heads][dim], dtype src_dtype: bf16 or
+ * fp16) into `cache` ([num_pages][heads][page_size][dim], dtype dst_dtype:
+ * src_dtype or e4m3).  Returns the number of tokens whose loc lies at or
+ * past num_pages * page_size (stored nowhere), or -3 for bad arguments. */
+int64_t oracle_store(int32_t src_dtype, int32_t dst_dtype, int64_t n, int32_t heads, int32_t dim,
+                     int32_t page_size, int64_t num_pages, const int64_t* loc, const void* src, void* cache) {
+  if ((src_dtype != OR_BF16 && src_dtype != OR_FP16) || (dst_dtype != src_dtype && dst_dtype != OR_FP8_E4M3) ||
+      n < 0 || heads <= 0 || dim <= 0 || page_size <= 0 || num_pages < 0)
+    return -3;
+  int64_t bad = 0;
+  for (int64_t t = 0; t < n; ++t) {
+    if (loc[t] < 0) continue;
+    if (loc[t] >= num_pages * page_size) {
+      ++bad;
+      continue;
+    }
+    const int64_t page = loc[t] / page_size, off = loc[t] % page_size;
+    for (int32_t h = 0; h < heads; ++h)
+      for (int32_t d = 0; d < dim; ++d) {
+        const int64_t si = (t * heads + h) * dim + d;
+        const int64_t di = ((page * heads + h) * page_size + off) * dim + d;
+        const uint16_t bits = ((const uint16_t*)src)[si];
+        if (dst_dtype == OR_FP8_E4M3)
+          ((uint8_t*)cache)[di] = encode_e4m3(src_dtype == OR_BF16 ? decode_bf16(bits) : decode_fp16(bits));
+        else
+          ((uint16_t*)cache)[di] = bits;
+      }
+  }
+  return bad;
+}
