@@ -268,6 +268,123 @@ def _stats(w):
 
 
 # ---------------------------------------------------------------- main
+# ----------------------------------------------------------- cache store
+STORE_TOKENS, STORE_HKV, STORE_PS, STORE_IDX_DIM = 32768, 8, 128, 128
+
+
+def run_store(args, rank, world, local_rank):
+    """--workload kv_store: the paged-cache store (mxsa_store_kv) on a long
+    prefill chunk: 32768 new tokens' K and V ([n, 8, 128] bf16) and index keys
+    ([n, 1, 128] bf16) cast to e4m3 into paged caches (page 128, shuffled
+    slots).  HBM-bound: value = tokens/s; roofline = bytes read + written per
+    launch / event-timed launch time, against the measured copy bandwidth."""
+    import block_sparse_attention_builder_gb300 as mx
+    from block_sparse_attention_builder_gb300 import build as B
+    from block_sparse_attention_builder_gb300 import workloads as W
+    B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    n, hkv, ps, idim = STORE_TOKENS, STORE_HKV, STORE_PS, STORE_IDX_DIM
+    pages = n // ps + 8
+    key = W.stream_key(2000 + rank, 0)
+    k = W.generate_values(n * hkv * 128, key, "bf16", dev).view(n, hkv, 128)
+    v = W.generate_values(n * hkv * 128, key + 1, "bf16", dev).view(n, hkv, 128)
+    ik = W.generate_values(n * idim, key + 2, "bf16", dev).view(n, 1, idim)
+    rng = np.random.default_rng(2000 + rank)
+    loc_h = torch.from_numpy(rng.permutation(pages * ps)[:n].astype(np.int64))
+    loc = loc_h.to(dev)
+    prob = mx.make_problem(1, n, hkv, hkv, 1, ps, pages, pages, False, q_dtype=torch.bfloat16,
+                           kv_dtype=torch.float8_e4m3fn)
+    kc = torch.zeros(pages, hkv, ps, 128, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    ic = torch.zeros(pages, 1, ps, idim, dtype=torch.uint8, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    bytes_read = n * (hkv * 128 * 2 * 2 + idim * 2) + n * 8
+    bytes_written = n * (hkv * 128 * 2 + idim)
+
+    def step():
+        mx.store_kv(prob, loc, k, v, kc, vc, idx_k=ik, idx_cache=ic, flags=flags, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
+    ms = total_ms / args.steps
+    if int(flags.item()):
+        raise RuntimeError(f"store flagged {int(flags.item()):#x}")
+    # end to end: this step's new rows and slots from pinned host memory, the
+    # status word back
+    hk, hv, hi = (t.cpu().pin_memory() for t in (k, v, ik))
+    hl = loc_h.pin_memory()
+    hf = torch.zeros(1, dtype=torch.int32).pin_memory()
+    dk, dv, di, dl = torch.empty_like(k), torch.empty_like(v), torch.empty_like(ik), torch.empty_like(loc)
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hi, hl))
+    e2e_ms = 0.0
+    for _ in range(max(3, args.steps // 2)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for d, h in ((dk, hk), (dv, hv), (di, hi), (dl, hl)):
+            d.copy_(h, non_blocking=True)
+        mx.store_kv(prob, dl, dk, dv, kc, vc, idx_k=di, idx_cache=ic, flags=flags, stream=stream)
+        hf.copy_(flags, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= max(3, args.steps // 2)
+    peaks = measured_peaks()
+    gbs = (bytes_read + bytes_written) / (ms / 1e3) / 1e9
+    line = {
+        "metric": "kv-store tokens/s and GB/s vs HBM roofline, 1 GB300", "value": n * world / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
+        "data": "synthetic (seeded counter-based N(0,1) values, shuffled slots)",
+        "config": {"workload": "kv_store", "description": "32768 new tokens, K/V [n,8,128] + index keys [n,1,128] "
+                   "bf16 -> e4m3 paged caches, page 128, shuffled slots", "tokens": n, "num_kv_heads": hkv,
+                   "page_size": ps, "index_dim": idim, "l2": "flushed between timed steps (256 MiB write)"},
+        "bytes": {"read": bytes_read, "written": bytes_written},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "k_store",
+                     "peak_source": peaks["src"]},
+        "e2e": {"value": n / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps, "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        m = 512
+        cache = np.zeros((m // ps + 1, hkv, ps, 128), dtype=np.uint8)
+        src = k[:m].cpu()
+        sl = np.arange(m, dtype=np.int64)
+        t0 = time.time()
+        reps = 0
+        while time.time() - t0 < 10.0:
+            oracle.store(src, sl, cache, ps, "bf16", "fp8")
+            oracle.store(src, sl, cache, ps, "bf16", "fp8")
+            reps += 1
+        dt = time.time() - t0
+        line["cpu_baseline"] = {"value": m * reps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{m} tokens' K and V (8 heads x 128, bf16 -> e4m3), {reps} passes, "
+                                          f"{dt:.1f} s on one thread (the oracle's store is single-threaded)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -292,6 +409,12 @@ def main():
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
+        return
+
+    if args.workload == "kv_store":
+        run_store(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
         return
 
     import block_sparse_attention_builder_gb300 as mx

@@ -36,7 +36,7 @@ STATUS_NAMES = {0: "MXSA_OK", 1: "MXSA_ERR_INVALID_ARG", 2: "MXSA_ERR_UNSUPPORTE
 EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_build_index", "mxsa_schedule",
             "mxsa_plan",
             "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
-            "mxsa_sched_layout_query"]
+            "mxsa_sched_layout_query", "mxsa_store_kv"]
 
 
 class MxsaError(RuntimeError):
@@ -91,6 +91,7 @@ def _load_library() -> ctypes.CDLL:
         "mxsa_read_status": [P, P, P],
         "mxsa_index_layout_query": [P, P],
         "mxsa_sched_layout_query": [P, P],
+        "mxsa_store_kv": [P, ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -190,6 +191,18 @@ def combine(prob, index_ws, partial_ws, out, lse=None, stream=None):
     _check(_lib.mxsa_combine(ctypes.byref(prob), _ptr(index_ws), index_ws.numel() * index_ws.element_size(),
                              _ptr(partial_ws), partial_ws.numel() * partial_ws.element_size(), _ptr(out), _ptr(lse),
                              _stream(stream)), "mxsa_combine")
+
+
+def store_kv(prob, loc, k, v, k_cache, v_cache, idx_k=None, idx_cache=None, flags=None, stream=None):
+    """Paged-cache store: rows of k, v ([n, Hkv, 128], the problem's q dtype)
+    and optionally idx_k ([n, idx_heads, idx_dim]) into the caches at slots
+    loc (int64 [n], page * page_size + offset; < 0: not stored), cast to the
+    caches' dtype (the unscaled e4m3 cast for FP8).  flags: optional int32
+    device tensor that receives MXSA_FLAG_PAGE for slots past the cache."""
+    n = int(loc.numel())
+    ih, idim = (int(idx_k.shape[1]), int(idx_k.shape[2])) if idx_k is not None else (0, 0)
+    _check(_lib.mxsa_store_kv(ctypes.byref(prob), n, _ptr(loc), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(idx_k), _ptr(idx_cache), ih, idim, _ptr(flags), _stream(stream)), "mxsa_store_kv")
 
 
 def read_status(index_ws, stream=None) -> int:

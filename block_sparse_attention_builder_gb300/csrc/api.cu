@@ -335,6 +335,25 @@ mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
 }
 
+mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const int64_t* loc, const void* k,
+                          const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
+                          int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_status s = validate_problem(*problem);
+  if (s != MXSA_OK) return s;
+  const mxsa_problem& p = *problem;
+  if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3) return MXSA_ERR_UNSUPPORTED;
+  if (n_tokens < 0 || (idx_k == nullptr) != (idx_cache == nullptr)) return MXSA_ERR_INVALID_ARG;
+  if (idx_k && (idx_heads <= 0 || idx_dim <= 0 || idx_dim % 8 != 0)) return MXSA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!loc || !k || !v || !k_cache || !v_cache)) return MXSA_ERR_INVALID_ARG;
+  if (!aligned(loc, 8) || !aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(idx_k, 16) || !aligned(idx_cache, 16) || !aligned(device_flags, 4))
+    return MXSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_store(p, n_tokens, loc, k, v, k_cache, v_cache, idx_k, idx_cache, idx_heads, idx_dim,
+                               device_flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
 mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device_flags) {
   if (!index_ws || !device_flags || !aligned(index_ws, 16)) return MXSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

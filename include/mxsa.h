@@ -169,6 +169,29 @@ mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size
  * is set, MXSA_OK otherwise. */
 mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device_flags);
 
+/* Paged-cache store, the write side of the caches the forward reads (a
+ * sglang pull request on these pages, "Summary": the fused K/V/index store
+ * with an unscaled bf16-to-fp8_e4m3 cast).  For each of n_tokens new tokens
+ * with slot loc[t] = page * page_size + offset (device int64; loc[t] < 0:
+ * token t is not stored):
+ *   k_cache[page][h][offset][:] = cast(k[t][h][:]) and likewise v, h < Hkv;
+ *   idx_cache[page][j][offset][:] = cast(idx_k[t][j][:]), j < idx_heads.
+ * k, v: [n_tokens][num_kv_heads][128] in problem->q_dtype (bf16 or fp16);
+ * idx_k: [n_tokens][idx_heads][idx_dim], same dtype, idx_dim a multiple of 8.
+ * Caches: [num_pages][heads][page_size][dim] in problem->kv_dtype, which is
+ * q_dtype (bits copied) or MXSA_FP8_E4M3: each value becomes x clamped to
+ * [-448, 448] rounded to the nearest e4m3fn value, ties to even, NaN keeping
+ * its sign -- bit-identical to x.float().clamp(-448, 448).to(float8_e4m3fn).
+ * idx_k and idx_cache are both NULL (no index keys) or both set.
+ * device_flags (device int32, may be NULL): MXSA_FLAG_PAGE is ORed in when a
+ * slot lies at or past num_pages * page_size (that token is not stored).
+ * Device pointers, 16-byte aligned (loc 8-byte); the caller owns all of them.
+ * One launch, asynchronous on `stream`.  MXSA_ERR_INVALID_ARG /
+ * MXSA_ERR_UNSUPPORTED for bad arguments, before any launch. */
+mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const int64_t* loc, const void* k,
+                          const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
+                          int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream);
+
 /* Byte offsets of the arrays inside the index workspace, for inspection
  * (tests compare them bit-exactly with an independent CPU statement).
  * header: int32[16] = {flags, NB (blocks over all sequences), nnz (entries),

@@ -108,3 +108,22 @@ def test_package_has_no_cpu_fallback():
     for f in os.listdir(os.path.join(ROOT, "block_sparse_attention_builder_gb300", "csrc")):
         text = open(os.path.join(ROOT, "block_sparse_attention_builder_gb300", "csrc", f)).read()
         assert "oracle" not in text.lower() or f.endswith(".md")
+
+
+def test_store_kv_arguments_rejected_before_any_launch(lib):
+    P = ctypes.c_void_p
+    fake, fake8 = P(1 << 20), P((1 << 20) + 8)  # never dereferenced: validation fails first
+    p = _prob(kv_dtype=torch.float8_e4m3fn)
+    ok_args = [fake, fake, fake, fake, fake]
+    # a cache dtype that is neither the source's nor e4m3
+    bad = _prob(q_dtype=torch.float16, kv_dtype=torch.bfloat16)
+    assert lib.mxsa_store_kv(ctypes.byref(bad), 4, *ok_args, None, None, 0, 0, None, None) in (1, 2)
+    assert lib.mxsa_store_kv(ctypes.byref(p), -1, *ok_args, None, None, 0, 0, None, None) == 1
+    # index keys: both pointers or neither; dim a multiple of 8
+    assert lib.mxsa_store_kv(ctypes.byref(p), 4, *ok_args, fake, None, 1, 64, None, None) == 1
+    assert lib.mxsa_store_kv(ctypes.byref(p), 4, *ok_args, fake, fake, 1, 60, None, None) == 1
+    assert lib.mxsa_store_kv(ctypes.byref(p), 4, *ok_args, fake, fake, 0, 64, None, None) == 1
+    # null or misaligned tensors
+    assert lib.mxsa_store_kv(ctypes.byref(p), 4, None, fake, fake, fake, fake, None, None, 0, 0, None, None) == 1
+    assert lib.mxsa_store_kv(ctypes.byref(p), 4, fake, fake8, fake, fake, fake, None, None, 0, 0, None, None) == 1
+    assert lib.mxsa_store_kv(None, 4, *ok_args, None, None, 0, 0, None, None) == 1
