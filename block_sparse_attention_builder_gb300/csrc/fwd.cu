@@ -756,7 +756,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)fwd_smem_bytes(true));
+                                    (int)std::max(fwd_smem_bytes(true), fwd_smem_bytes(false)));
   });
   if (attr_err != cudaSuccess) return attr_err;
   FwdArgs a;
