@@ -341,6 +341,38 @@ __device__ __forceinline__ void emit_row_warp(const IndexPtrs& ix, const uint32_
   }
 }
 
+// The same for one of `wcount` warps sharing a long row: warp `wsub` emits
+// the row's 32-word chunks wsub, wsub + wcount, ...; the entries before each
+// of its chunks are counted from the bitmap words themselves.
+__device__ __forceinline__ void emit_row_shared(const IndexPtrs& ix, const uint32_t* bm, int n_words,
+                                                const uint8_t* km, int q_begin, int g, int Hkv, int topk, int base,
+                                                int wsub, int wcount) {
+  const int lane = threadIdx.x & 31;
+  int run = base, counted = 0;  // entries of words [0, counted)
+  for (int w0 = wsub * 32; w0 < n_words; w0 += wcount * 32) {
+    int skip = 0;
+    for (int w = counted + lane; w < w0; w += 32) skip += __popc(bm[w]);
+    run += __reduce_add_sync(0xffffffffu, skip);
+    const int w = w0 + lane;
+    uint32_t bits = w < n_words ? bm[w] : 0u;
+    const int cnt = __popc(bits);
+    const int inc = warp_inclusive_scan(cnt);
+    int j = run + inc - cnt;
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const int i = w * 32 + bit;
+      const int k = km[i];
+      const int slot = ((q_begin + i) * Hkv + g) * topk + k;
+      ix.entries[j] = slot;
+      ix.slot_entry[slot] = j;
+      ++j;
+    }
+    run += __shfl_sync(0xffffffffu, inc, 31);
+    counted = w0 + 32 < n_words ? w0 + 32 : n_words;
+  }
+}
+
 // scan + emit: each CTA adds the sums of the chunks before its own, scans
 // its chunk in tiles (row_ptr, the list of keys with entries and their valid
 // token counts) and writes the entries of its keys: rows of at most two

@@ -211,15 +211,20 @@ __device__ __forceinline__ void plan_scan_emit(const IndexPtrs& ix, const SchedP
       s_tot_d = (int)(td & kLow);
     }
     __syncthreads();
-    // long bitmap rows: one warp per key
-    for (int i = warp; i < s_n_long; i += n_warps) {
+    // long bitmap rows: one warp per key, or, when the tile has at most half
+    // as many long rows as warps (a few popular keys), several warps per key
+    const int wpr = s_n_long > 0 && 2 * s_n_long <= n_warps ? n_warps / s_n_long : 1;
+    for (int i = warp / wpr; i < s_n_long; i += n_warps / wpr) {
       const int k2 = s_long_key[i];
       const int g = k2 / NB, r = k2 - g * NB;
       const SeqInfo si = tab.get(tab.find(r));
       const int b = r - si.blk_off;
-      ixp::emit_row_warp(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
-                         ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv,
-                         topk, s_long_base[i]);
+      const uint32_t* bm = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
+      const uint8_t* km = ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq;
+      if (wpr == 1)
+        ixp::emit_row_warp(ix, bm, si.words, km, si.q_begin, g, Hkv, topk, s_long_base[i]);
+      else
+        ixp::emit_row_shared(ix, bm, si.words, km, si.q_begin, g, Hkv, topk, s_long_base[i], warp % wpr, wpr);
     }
     const int base_n = (int)(cn & kLow), base_d = (int)(cd & kLow);
     for (int x = threadIdx.x; x < s_tot_n; x += blockDim.x) {
