@@ -6,7 +6,8 @@
 // Row (t, h) of a source [n][heads][dim] goes to cache[page][h][off][:],
 // page = loc[t] / page_size, off = loc[t] % page_size.  K, V and the
 // optional index keys are one launch: one thread per 16-byte source chunk
-// (8 values), so consecutive threads read and write consecutive bytes.  Into
+// (8 values) of K and the same chunk of V, then per index-key chunk, so
+// consecutive threads read and write consecutive bytes.  Into
 // an e4m3 cache the values are converted two at a time with the saturating
 // round-to-nearest-even conversion (448 is the largest finite e4m3fn value,
 // so saturating equals clamping first); NaN keeps the sign of its source.
@@ -64,61 +65,66 @@ __device__ __forceinline__ bool any_nan(const uint4& s, int bf16) {
   return hit != 0;
 }
 
-__global__ void __launch_bounds__(256) k_store(StoreArgs a) {
-  const uint32_t total = a.chunks[0] + a.chunks[1] + a.chunks[2];
-  const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += stride) {
-    int w = 0;
-    uint32_t cc = c;
-    if (cc >= a.chunks[0]) {
-      cc -= a.chunks[0];
-      w = 1;
-      if (cc >= a.chunks[1]) {
-        cc -= a.chunks[1];
-        w = 2;
+// one 16-byte source chunk s (8 values) to its destination: 8 e4m3 bytes or
+// the 16 bytes themselves
+__device__ __forceinline__ void put_chunk(const uint4& s, uint8_t* dst, long long dst_elem, int fp8, int bf16) {
+  if (fp8) {
+    uint32_t o[2];
+    if (!any_nan(s, bf16)) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t x = i ? s.z : s.x, y = i ? s.w : s.y;
+        o[i] = e4m3x2((uint16_t)(x & 0xFFFFu), (uint16_t)(x >> 16), bf16) |
+               (e4m3x2((uint16_t)(y & 0xFFFFu), (uint16_t)(y >> 16), bf16) << 16);
+      }
+    } else {
+      const uint32_t w4[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        o[i] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          o[i] |= e4m3_nan_aware((uint16_t)(w4[2 * i + b / 2] >> (16 * (b & 1))), bf16) << (8 * b);
       }
     }
+    *reinterpret_cast<uint2*>(dst + dst_elem) = make_uint2(o[0], o[1]);
+  } else {
+    *reinterpret_cast<uint4*>(dst + 2 * dst_elem) = s;
+  }
+}
+
+// Units: first the K/V chunks (one thread stores the same chunk of K and of
+// V, which share their token, head and destination offset), then the index
+// keys' chunks.
+__global__ void __launch_bounds__(256) k_store(StoreArgs a) {
+  const uint32_t total = a.chunks[0] + a.chunks[2];
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += stride) {
+    const bool kv = c < a.chunks[0];
+    const uint32_t cc = kv ? c : c - a.chunks[0];
     // per-tensor fields by select (a runtime index would copy the
     // parameters to local memory)
-    const uint32_t rc = (uint32_t)(w == 0 ? a.row_chunks[0] : w == 1 ? a.row_chunks[1] : a.row_chunks[2]);
-    const uint32_t heads = (uint32_t)(w == 0 ? a.heads[0] : w == 1 ? a.heads[1] : a.heads[2]);
-    const int rcs = w == 0 ? a.rc_shift[0] : w == 1 ? a.rc_shift[1] : a.rc_shift[2];
-    const int hs = w == 0 ? a.heads_shift[0] : w == 1 ? a.heads_shift[1] : a.heads_shift[2];
-    const uint16_t* src = w == 0 ? a.src[0] : w == 1 ? a.src[1] : a.src[2];
-    uint8_t* dst = w == 0 ? a.dst[0] : w == 1 ? a.dst[1] : a.dst[2];
+    const uint32_t rc = (uint32_t)(kv ? a.row_chunks[0] : a.row_chunks[2]);
+    const uint32_t heads = (uint32_t)(kv ? a.heads[0] : a.heads[2]);
+    const int rcs = kv ? a.rc_shift[0] : a.rc_shift[2];
+    const int hs = kv ? a.heads_shift[0] : a.heads_shift[2];
     const uint32_t row = rcs >= 0 ? cc >> rcs : cc / rc, part = cc - row * rc;
     const uint32_t t = hs >= 0 ? row >> hs : row / heads, h = row - t * heads;
     const long long l = __ldg(a.loc + t);
     if (l < 0) continue;  // the token is not stored
     if (l >= a.slots) {
-      if (a.flags && w == 0 && h == 0 && part == 0) atomicOr(a.flags, MXSA_FLAG_PAGE);
+      if (a.flags && kv && h == 0 && part == 0) atomicOr(a.flags, MXSA_FLAG_PAGE);
       continue;
     }
     const long long page = l >> a.page_shift, off = l & ((1LL << a.page_shift) - 1);
     const long long dst_elem = ((page * heads + h) << a.page_shift | off) * (8LL * rc) + 8LL * part;
-    const uint4 s = __ldcs(reinterpret_cast<const uint4*>(src) + cc);
-    if (a.fp8) {
-      uint32_t o[2];
-      if (!any_nan(s, a.bf16)) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t x = i ? s.z : s.x, y = i ? s.w : s.y;
-          o[i] = e4m3x2((uint16_t)(x & 0xFFFFu), (uint16_t)(x >> 16), a.bf16) |
-                 (e4m3x2((uint16_t)(y & 0xFFFFu), (uint16_t)(y >> 16), a.bf16) << 16);
-        }
-      } else {
-        const uint32_t w4[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          o[i] = 0;
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            o[i] |= e4m3_nan_aware((uint16_t)(w4[2 * i + b / 2] >> (16 * (b & 1))), a.bf16) << (8 * b);
-        }
-      }
-      *reinterpret_cast<uint2*>(dst + dst_elem) = make_uint2(o[0], o[1]);
+    if (kv) {
+      const uint4 sk = __ldcs(reinterpret_cast<const uint4*>(a.src[0]) + cc);
+      const uint4 sv = __ldcs(reinterpret_cast<const uint4*>(a.src[1]) + cc);
+      put_chunk(sk, a.dst[0], dst_elem, a.fp8, a.bf16);
+      put_chunk(sv, a.dst[1], dst_elem, a.fp8, a.bf16);
     } else {
-      *reinterpret_cast<uint4*>(dst + 2 * dst_elem) = s;
+      put_chunk(__ldcs(reinterpret_cast<const uint4*>(a.src[2]) + cc), a.dst[2], dst_elem, a.fp8, a.bf16);
     }
   }
 }
@@ -168,7 +174,7 @@ cudaError_t launch_store(const mxsa_problem& p, long long n, const int64_t* loc,
     a.fp8 = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 0;
     a.bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
     a.flags = flags;
-    const long long total = (long long)m * per_token;
+    const long long total = (long long)a.chunks[0] + a.chunks[2];  // units: K/V chunk pairs, index chunks
     long long blocks = (total + 255) / 256;
     if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
     k_store<<<(unsigned)blocks, 256, 0, st>>>(a);
