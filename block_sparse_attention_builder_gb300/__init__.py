@@ -2,8 +2,10 @@
 
 Argument marshalling only -- every step runs in the library's CUDA kernels;
 PyTorch provides device memory and streams.  The entry points mirror the C
-ABI in include/mxsa.h (build_index, schedule, kvouter_fwd, combine,
-read_status), plus ``kvouter_attention`` with the call shape of the
+ABI in include/mxsa.h (build_index, schedule, plan, kvouter_fwd, combine,
+read_status, and store_kv, the paged-cache store that writes new tokens'
+K/V and index keys into the caches), plus ``kvouter_attention`` with the
+call shape of the
 fw-ai/minimax-kernels README's Quick start and ``SparseAttention`` which
 keeps the workspaces of one problem shape for repeated calls.
 
