@@ -5,9 +5,9 @@ PyTorch provides device memory and streams.  The entry points mirror the C
 ABI in include/mxsa.h (build_index, schedule, plan, kvouter_fwd, combine,
 read_status, and store_kv, the paged-cache store that writes new tokens'
 K/V and index keys into the caches), plus ``kvouter_attention`` with the
-call shape of the
-fw-ai/minimax-kernels README's Quick start and ``SparseAttention`` which
-keeps the workspaces of one problem shape for repeated calls.
+call shape of the fw-ai/minimax-kernels README's Quick start and
+``SparseAttention`` which keeps the workspaces of one problem shape for
+repeated calls.
 
 There is no fallback: the first call into the library raises ImportError
 when libmxsa.so has not been built, and every library error is raised as
