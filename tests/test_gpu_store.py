@@ -75,6 +75,13 @@ def test_store_with_index_keys_skips_and_flags(src, dst, ps):
     assert bad == 1
 
 
+def test_store_odd_shapes_take_the_division_paths():
+    # 3 kv heads and 24-dim index keys (3 chunks a row): neither is a power
+    # of two, so the row and token indices come from divisions
+    _run("bf16", "fp8", 77, 3, 64, 3, idx=(3, 24), seed=3)
+    _run("fp16", "fp16", 50, 3, 128, 1, idx=(1, 8), seed=4)
+
+
 def test_no_tokens_is_a_no_op():
     prob = mx.make_problem(1, 1, 8, 8, 1, 64, 2, 2, False, q_dtype=torch.bfloat16, kv_dtype=torch.float8_e4m3fn)
     kc = torch.zeros(2, 8, 64, 128, dtype=torch.uint8, device="cuda")
