@@ -385,6 +385,113 @@ def run_store(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ dense path
+def run_dense(args, rank, world, local_rank):
+    """--workload dense_prefill: the dense path (mxsa_dense_fwd: every key,
+    no partials) on the shared-prefill shape (1 sequence, 4096 new tokens on
+    L = 36864, Hq 16 / Hkv 1, page 128, causal).  value = tokens/s; roofline
+    = causal FLOPs (4 * 128 per query head and visible key) per launch / the
+    event-timed launch, against the measured BF16 dense peak."""
+    import block_sparse_attention_builder_gb300 as mx
+    from block_sparse_attention_builder_gb300 import build as B
+    from block_sparse_attention_builder_gb300 import workloads as W
+    B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    tq, L, hq, hkv, ps = 4096, 36864, 16, 1, 128
+    w = W.custom("dense_prefill", [tq], [L], hq, hkv, ps, 1, True, "uniform", 3000 + rank)
+    q, k, v = w.q(dev), w.k_cache(dev), w.v_cache(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
+    lens = torch.from_numpy(w.used_kv_lens).to(dev)
+    prob = mx.make_problem(1, tq, hq, hkv, 1, ps, w.num_pages, w.max_pages_per_seq, True)
+    out = torch.empty_like(q)
+    lse = torch.empty(hq, tq, dtype=torch.float32, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    keys = tq * (L - tq) + tq * (tq + 1) // 2  # visible keys summed over the tokens
+    flops = 4.0 * 128 * hq * keys
+
+    def step():
+        mx.dense_fwd(prob, q, k, v, bt, cu, lens, out, lse, flags=flags, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
+    ms = total_ms / args.steps
+    if int(flags.item()):
+        raise RuntimeError(f"dense path flagged {int(flags.item()):#x}")
+    # end to end: q from pinned host memory, out and lse back to pinned host
+    hq_h = q.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq = torch.empty_like(q)
+    e2e_ms, reps = 0.0, max(3, args.steps // 2)
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dq.copy_(hq_h, non_blocking=True)
+        mx.dense_fwd(prob, dq, k, v, bt, cu, lens, out, lse, flags=flags, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= reps
+    peaks = measured_peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "dense-attn tokens/s and TFLOP/s vs tensor roofline, 1 GB300", "value": tq * world / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based N(0,1) values)",
+        "config": {"workload": "dense_prefill", "description": "1 seq, Tq=4096 on L=36864, Hq16/Hkv1, ps128, causal, "
+                   "every key (no selection)", "num_q_heads": hq, "num_kv_heads": hkv, "page_size": ps,
+                   "l2": "flushed between timed steps (256 MiB write)"},
+        "flops": flops,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"], "traffic": None, "kernel": "k_dense",
+                     "peak_source": peaks["src"]},
+        "e2e": {"value": tq / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": q.numel() * q.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size() + lse.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps, "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        rows = np.arange((tq - 4) * hq, tq * hq, dtype=np.int64)  # the last 4 tokens' rows: the longest
+        t0 = time.time()
+        reps = 0
+        sel = np.arange(w.max_pages_per_seq * ps // 128, dtype=np.int32)[None, None, :].repeat(tq, 0)
+        oprob = oracle.problem(1, tq, hq, hkv, sel.shape[2], ps, w.num_pages, w.max_pages_per_seq, True)
+        qc, kc, vc = w.q(), w.k_cache(), w.v_cache()
+        while time.time() - t0 < 10.0:
+            oracle.attention_rows(oprob, qc, kc, vc, sel, w.block_tables, w.cu_seqlens_q, w.used_kv_lens, rows=rows)
+            reps += 1
+        dt = time.time() - t0
+        line["cpu_baseline"] = {"value": 4 * reps / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1,
+                                "kind": "oracle",
+                                "sample": f"the last 4 tokens (x {hq} heads, ~{L} keys each), {reps} passes, "
+                                          f"{dt:.1f} s; tokens/s = tokens / time"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,8 +518,8 @@ def main():
             dist.destroy_process_group()
         return
 
-    if args.workload == "kv_store":
-        run_store(args, rank, world, local_rank)
+    if args.workload in ("kv_store", "dense_prefill"):
+        (run_store if args.workload == "kv_store" else run_dense)(args, rank, world, local_rank)
         if world > 1:
             torch.distributed.destroy_process_group()
         return

@@ -38,7 +38,7 @@ STATUS_NAMES = {0: "MXSA_OK", 1: "MXSA_ERR_INVALID_ARG", 2: "MXSA_ERR_UNSUPPORTE
 EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_build_index", "mxsa_schedule",
             "mxsa_plan",
             "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
-            "mxsa_sched_layout_query", "mxsa_store_kv"]
+            "mxsa_sched_layout_query", "mxsa_store_kv", "mxsa_dense_fwd"]
 
 
 class MxsaError(RuntimeError):
@@ -94,6 +94,7 @@ def _load_library() -> ctypes.CDLL:
         "mxsa_index_layout_query": [P, P],
         "mxsa_sched_layout_query": [P, P],
         "mxsa_store_kv": [P, ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P],
+        "mxsa_dense_fwd": [P, P, P, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -193,6 +194,15 @@ def combine(prob, index_ws, partial_ws, out, lse=None, stream=None):
     _check(_lib.mxsa_combine(ctypes.byref(prob), _ptr(index_ws), index_ws.numel() * index_ws.element_size(),
                              _ptr(partial_ws), partial_ws.numel() * partial_ws.element_size(), _ptr(out), _ptr(lse),
                              _stream(stream)), "mxsa_combine")
+
+
+def dense_fwd(prob, q, k_cache, v_cache, block_tables, cu_seqlens_q, used_kv_lens, out, lse=None, flags=None,
+              stream=None):
+    """Dense paged attention (every key of each sequence; causal per the
+    problem) straight into out [total_q, Hq, 128] and lse [Hq, total_q]."""
+    _check(_lib.mxsa_dense_fwd(ctypes.byref(prob), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                               _ptr(cu_seqlens_q), _ptr(used_kv_lens), _ptr(out), _ptr(lse), _ptr(flags),
+                               _stream(stream)), "mxsa_dense_fwd")
 
 
 def store_kv(prob, loc, k, v, k_cache, v_cache, idx_k=None, idx_cache=None, flags=None, stream=None):

@@ -335,6 +335,26 @@ mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
 }
 
+mxsa_status mxsa_dense_fwd(const mxsa_problem* problem, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                           void* out, float* lse, int32_t* device_flags, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_status s = validate_problem(*problem);
+  if (s != MXSA_OK) return s;
+  const mxsa_problem& p = *problem;
+  if (p.kv_dtype != p.q_dtype || p.num_seqs > 1024) return MXSA_ERR_UNSUPPORTED;
+  if (!block_tables || !cu_seqlens_q || !used_kv_lens) return MXSA_ERR_INVALID_ARG;
+  if (p.total_q > 0 && (!q || !k_cache || !v_cache || !out)) return MXSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(cu_seqlens_q, 8) || !aligned(used_kv_lens, 4) || !aligned(lse, 4) ||
+      !aligned(device_flags, 4))
+    return MXSA_ERR_INVALID_ARG;
+  if (!kernel_writable(out) || !kernel_writable(lse)) return MXSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_dense(p, q, k_cache, v_cache, block_tables, cu_seqlens_q, used_kv_lens, out, lse,
+                               device_flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
 mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const int64_t* loc, const void* k,
                           const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
                           int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream) {

@@ -119,6 +119,9 @@ cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const Sc
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
                        float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
+cudaError_t launch_dense(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int64_t* cu, const int32_t* lens, void* out, float* lse,
+                         int32_t* flags, cudaStream_t st);
 cudaError_t launch_store(const mxsa_problem& p, long long n, const int64_t* loc, const void* k, const void* v,
                          void* k_cache, void* v_cache, const void* idx_k, void* idx_cache, int idx_heads,
                          int idx_dim, int32_t* flags, cudaStream_t st);

@@ -188,6 +188,26 @@ mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device
  * Device pointers, 16-byte aligned (loc 8-byte); the caller owns all of them.
  * One launch, asynchronous on `stream`.  MXSA_ERR_INVALID_ARG /
  * MXSA_ERR_UNSUPPORTED for bad arguments, before any launch. */
+/* Dense paged attention, the all-blocks-selected case computed directly (no
+ * partials, no combine; the MSA project page lists a dense FMHA path next to
+ * the sparse one): for token t of sequence s and query head h,
+ *   out[t][h][:] = sum_p softmax_p(scale * q[t][h] . k_p) v_p,
+ *   lse[h][t] = log sum_p exp(scale * q[t][h] . k_p)   (natural log),
+ * over keys p < used_kv_lens[s] (and p <= pos(t) = L - Tq_s + i when causal),
+ * k_p / v_p read through block_tables as in mxsa_kvouter_fwd.  No key: out 0,
+ * lse -inf.  Same tensors and layouts as the sparse path (q, caches, out
+ * [total_q][Hq][128] in q_dtype, lse [Hq][total_q] or NULL); topk is unused.
+ * kv_dtype must equal q_dtype (BF16/FP16); num_seqs <= 1024.  Tokens outside
+ * every sequence (cu_seqlens_q out of order or past total_q) are not written.
+ * device_flags (device int32, may be NULL): MXSA_FLAG_PAGE when a needed
+ * block_tables entry lies outside [0, num_pages) (that page is skipped and its
+ * rows' results are undefined), MXSA_FLAG_TIMEOUT.  Device pointers; q, caches
+ * and out 16-byte aligned.  One launch, asynchronous on `stream`;
+ * MXSA_ERR_INVALID_ARG / MXSA_ERR_UNSUPPORTED before any launch. */
+mxsa_status mxsa_dense_fwd(const mxsa_problem* problem, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                           void* out, float* lse, int32_t* device_flags, void* stream);
+
 mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const int64_t* loc, const void* k,
                           const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
                           int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream);
