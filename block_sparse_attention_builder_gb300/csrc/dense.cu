@@ -7,23 +7,27 @@
 // and lse = log sum exp, over keys p < L (and p <= pos(t) when causal,
 // pos(t) = L - Tq + i).
 //
-// Persistent kernel, one CTA per SM, 192 threads:
-//   warps 0-3  softmax: row r of a tile is thread r and TMEM lane r.  A tile
-//              is T = 128 / G tokens x the G query heads of one kv head of
-//              one sequence.  Per 128-key block: S = q k^T (TMEM), a lazily
+// Persistent kernel, one CTA per SM, 352 threads.  A tile is 2T tokens
+// (T = 128 / G) x the G query heads of one kv head of one sequence: two
+// 128-row halves, one per softmax group, that share every K/V block.
+//   warps 0-3, 4-7  softmax groups: row r of a half is thread r of its group
+//              and TMEM lane r.  Per 128-key block: S = q k^T (TMEM), a lazily
 //              raised running maximum (raised only when a score passes it by
 //              2^8; O in TMEM is then rescaled), P = exp2(S - m) written back
 //              to TMEM over S, l += sum P.  After the last block o = O / l
 //              goes straight to the output and lse to its [Hq, Tq] slot.
-//   warp 4     producer: the tile's q rows (one 3-D TMA box per 64-column
+//              While one group runs its softmax, the tensor pipe runs the
+//              other group's products.
+//   warp 8     producer: each half's q rows (one 3-D TMA box per 64-column
 //              half: 64 columns x G heads x T tokens) and each block's K and
 //              V pages (TMA through block_tables) into a 2-stage ring.
-//   warp 5     MMA issuer (tcgen05.mma, cta_group::1, M = N = 128, K = 16,
-//              FP32 accumulate): q k^T into one of two S buffers, then P V
-//              into O with P as the TMEM operand.
-// TMEM: S0, S1 and O (384 of 512 columns).  The tiles are visited in a fixed
-// order (round robin over the CTAs, latest tokens first), so every role
-// walks the same sequence without sharing a queue.
+//   warps 9, 10  MMA issuers, one per group (tcgen05.mma, cta_group::1,
+//              M = N = 128, K = 16, FP32 accumulate): q k^T into the group's
+//              S once its previous p v is done, then P V into its O with P as
+//              the TMEM operand.
+// TMEM: S and O of each group (512 columns).  The tiles are visited in a
+// fixed order (round robin over the CTAs, latest tokens first), so every
+// role walks the same sequence without sharing a queue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -40,19 +44,21 @@ namespace mxsa {
 
 namespace {
 
-constexpr int kDThreads = 192;
-constexpr int kDProducer = 4, kDMma = 5;
+constexpr int kDThreads = 352;
+constexpr int kDProducer = 8, kDMma = 9;  // warps 9, 10: the issuers of groups 0, 1
 constexpr uint32_t kDTile = 32768;        // 128 rows x 128 x 16-bit
 constexpr uint32_t kDStage = 2 * kDTile;  // K and V of one 128-token block
 constexpr int kDMaxSeqs = 1024;           // sequences held in shared memory
 constexpr float kDRescale = 8.f;          // log2 units
 
-constexpr uint32_t kDOffQ = 0;
-constexpr uint32_t kDOffKV = kDTile;
+constexpr uint32_t kDOffQ = 0;            // 2 groups x q half
+constexpr uint32_t kDOffKV = 2 * kDTile;
 constexpr uint32_t kDOffSeq = kDOffKV + 2 * kDStage;
 
 struct DCtrl {
-  uint64_t q_full, q_empty, kv_full[2], kv_empty[2], s_full[2], p_full[2], p_empty[2], o_full, o_empty, done;
+  // q_*, s_full, p_*, o_*: one per softmax group; kv_*: per ring stage
+  uint64_t q_full[2], q_empty[2], kv_full[2], kv_empty[2], s_full[2], p_full[2], p_empty[2], o_full[2], o_empty[2],
+      done;
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t total_tiles, per_head;
@@ -94,7 +100,7 @@ __device__ __forceinline__ bool dwarp_all(bool v) { return __all_sync(0xffffffff
 // (their key ranges are the longest under causal masking), and CTA b takes
 // numbers b, b + gridDim.x, ...  Returns false past the CTA's last tile.
 struct DTile {
-  int s, g, t0, ntok, nb;
+  int s, g, t0, ntok, nb;  // ntok: tokens of both halves (half h holds t0 + hT ..)
 };
 
 __device__ __forceinline__ bool dense_tile(const DSeq* seq, const DCtrl& c, const DenseArgs& a, int n, DTile* d) {
@@ -111,8 +117,8 @@ __device__ __forceinline__ bool dense_tile(const DSeq* seq, const DCtrl& c, cons
   const DSeq sq = seq[lo];
   d->s = lo;
   d->g = g;
-  d->t0 = (rem - sq.tiles_before) * a.T;
-  d->ntok = min(a.T, sq.tq - d->t0);
+  d->t0 = (rem - sq.tiles_before) * 2 * a.T;
+  d->ntok = min(2 * a.T, sq.tq - d->t0);
   const int nblk = (sq.L + 127) >> 7;
   if (a.causal) {
     const int last = sq.L - sq.tq + d->t0 + d->ntok - 1;  // position of the tile's last token
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     d.q_begin = ok ? (int)b0 : 0;
     d.tq = ok ? (int)(b1 - b0) : 0;
     d.L = min(max(a.lens[s], 0), maxL);
-    d.tiles_before = (d.tq + a.T - 1) / a.T;  // this sequence's own tiles for now
+    d.tiles_before = (d.tq + 2 * a.T - 1) / (2 * a.T);  // this sequence's own tiles for now
     seq[s] = d;
   }
   __syncthreads();
@@ -181,18 +187,18 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
     c.per_head = run;
     c.total_tiles = run * a.Hkv;
-    mbar_init(&c.q_full, 1);
-    mbar_init(&c.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.q_full[i], 1);
+      mbar_init(&c.q_empty[i], 1);
       mbar_init(&c.kv_full[i], 1);
-      mbar_init(&c.kv_empty[i], 1);
+      mbar_init(&c.kv_empty[i], 2);  // both issuers' p v of the block
       mbar_init(&c.s_full[i], 1);
       mbar_init(&c.p_full[i], 128);
       mbar_init(&c.p_empty[i], 1);
+      mbar_init(&c.o_full[i], 1);
+      mbar_init(&c.o_empty[i], 128);
     }
-    mbar_init(&c.o_full, 1);
-    mbar_init(&c.o_empty, 128);
-    mbar_init(&c.done, 1);
+    mbar_init(&c.done, 2);
     c.abort_flag = 0;
     c.local_flags = 0;
     fence_mbar_init();
@@ -223,11 +229,17 @@ __global__ void __launch_bounds__(kDThreads, 1)
         DTile d;
         for (; ok && dense_tile(seq, c, a, n, &d); ++n) {
           const DSeq sq = seq[d.s];
-          ok = mbar_wait(&c.q_empty, (n & 1) ^ 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          for (int h = 0; h < 2 && ok; ++h) {
+            // half h's rows (its tokens may run past the sequence: those rows
+            // are padding, never stored)
+            ok = mbar_wait(&c.q_empty[h], (n & 1) ^ 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (!ok) break;
+            uint8_t* qd = sm + kDOffQ + h * kDTile;
+            mbar_arrive_expect_tx(&c.q_full[h], (uint32_t)(G * a.T) * 256u);
+            tma_load_3d(qd, &tmq, &c.q_full[h], 0, d.g * G, sq.q_begin + d.t0 + h * a.T);
+            tma_load_3d(qd + 16384, &tmq, &c.q_full[h], 64, d.g * G, sq.q_begin + d.t0 + h * a.T);
+          }
           if (!ok) break;
-          mbar_arrive_expect_tx(&c.q_full, (uint32_t)(G * a.T) * 256u);
-          tma_load_3d(sm + kDOffQ, &tmq, &c.q_full, 0, d.g * G, sq.q_begin + d.t0);
-          tma_load_3d(sm + kDOffQ + 16384, &tmq, &c.q_full, 64, d.g * G, sq.q_begin + d.t0);
           for (int b = 0; b < d.nb && ok; ++b, ++blk) {
             const int st = blk & 1, us = blk >> 1;
             ok = mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
@@ -261,45 +273,49 @@ __global__ void __launch_bounds__(kDThreads, 1)
         // drain: the copies in flight land before the CTA may exit
         for (int k = std::max(0, blk - 2); k < blk; ++k)
           mbar_drain(&c.kv_full[k & 1], (k >> 1) & 1, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        if (n > 0) mbar_drain(&c.q_full, (n - 1) & 1, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        if (n > 0)
+          for (int h = 0; h < 2; ++h) mbar_drain(&c.q_full[h], (n - 1) & 1, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
       }
-    } else if (warp == kDMma) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == kDMma || warp == kDMma + 1) {
+      // --------------------------------------------------------- MMA issuers
+      // Issuer g serves softmax group g: its S is overwritten only once its
+      // previous p v (which read P from it) is done, so by the time the group
+      // sees S its O is complete too.
       if (lane == 0) {
+        const int gq = warp - kDMma;
         const uint32_t id_qk = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 0);
         const uint32_t id_pv = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 1);
-        const uint32_t q_s = sbase + kDOffQ, tO = tmem + 256;
+        const uint32_t q_s = sbase + kDOffQ + gq * kDTile;
+        const uint32_t tS = tmem + gq * 256, tO = tS + 128;
         int blk = 0, n = 0;
         bool ok = true;
         DTile d;
         for (; ok && dense_tile(seq, c, a, n, &d); ++n) {
-          ok = mbar_wait(&c.q_full, n & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          ok = mbar_wait(&c.q_full[gq], n & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
-          if (d.nb == 0) mma_commit(&c.q_empty);  // q unused: free at once
+          if (d.nb == 0) mma_commit(&c.q_empty[gq]);  // q unused: free at once
           for (int b = 0; b < d.nb && ok; ++b, ++blk) {
-            const int st = blk & 1, sb = blk & 1;
+            const int st = blk & 1;
             ok = mbar_wait(&c.kv_full[st], (blk >> 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
             if (!ok) break;
-            if (blk >= 2) {  // the S/P buffer was read by the p v of block blk - 2
-              ok = mbar_wait(&c.p_empty[sb], ((blk >> 1) - 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT,
-                             kWaitLimitNs);
+            if (blk > 0) {  // the previous p v read P from S
+              ok = mbar_wait(&c.p_empty[gq], (blk - 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
               if (!ok) break;
             }
             tc_fence_after();
             const uint32_t k_s = sbase + kDOffKV + st * kDStage, v_s = k_s + kDTile;
-            const uint32_t tS = tmem + sb * 128;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off = (ks >> 2) * 16384u + (ks & 3) * 32u;
               mma_f16_ss(tS, smem_desc_sw128(q_s + off, 0, 1024), smem_desc_sw128(k_s + off, 0, 1024), id_qk,
                          ks > 0);
             }
-            if (b == d.nb - 1) mma_commit(&c.q_empty);  // the tile's q is read once these complete
-            mma_commit(&c.s_full[sb]);
-            ok = mbar_wait(&c.p_full[sb], (blk >> 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (b == d.nb - 1) mma_commit(&c.q_empty[gq]);  // the half's q is read once these complete
+            mma_commit(&c.s_full[gq]);
+            ok = mbar_wait(&c.p_full[gq], blk & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
             if (!ok) break;
             if (b == 0 && n > 0) {  // O of the previous tile has been read out
-              ok = mbar_wait(&c.o_empty, (n - 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+              ok = mbar_wait(&c.o_empty[gq], (n - 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
               if (!ok) break;
             }
             tc_fence_after();
@@ -307,39 +323,39 @@ __global__ void __launch_bounds__(kDThreads, 1)
             for (int ks = 0; ks < 8; ++ks)
               mma_f16_ts(tO, tS + ks * 8, smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), id_pv,
                          (b > 0 || ks > 0) ? 1u : 0u);
-            mma_commit(&c.p_empty[sb]);
+            mma_commit(&c.p_empty[gq]);
             mma_commit(&c.kv_empty[st]);
           }
-          if (ok) mma_commit(&c.o_full);
+          if (ok) mma_commit(&c.o_full[gq]);
         }
         mma_commit(&c.done);
         mbar_drain(&c.done, 0, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
       }
     } else {
       // ------------------------------------------------------------- softmax
-      const int r = tid;  // tile row == TMEM lane
-      const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-      const uint32_t tO = tmem + 256 + lane_addr;
-      const int tt = r / G, hh = r - tt * G;
+      const int gq = warp >> 2;  // softmax group: the tile's half
+      const int r = tid & 127;   // row of the half == TMEM lane
+      const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tO = tmem + gq * 256 + 128 + lane_addr;
+      const int tt = gq * a.T + r / G, hh = r % G;  // token within the tile, head within the group
       const int bf16 = a.ab_bf16;
       int blk = 0, n = 0;
       bool ok = true;
       DTile d;
       for (; ok && dense_tile(seq, c, a, n, &d); ++n) {
         const DSeq sq = seq[d.s];
-        const bool live = tt < d.ntok;
+        const bool live = r < G * a.T && tt < d.ntok;  // rows past G*T are padding of the half
         const int pos = sq.L - sq.tq + d.t0 + tt;
         float m = -INFINITY, l = 0.f;
         for (int b = 0; b < d.nb && ok; ++b, ++blk) {
-          const int sb = blk & 1, st = blk & 1;
-          ok = dwarp_all(mbar_wait(&c.s_full[sb], (blk >> 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT,
-                                   kWaitLimitNs));
+          const int st = blk & 1;
+          ok = dwarp_all(mbar_wait(&c.s_full[gq], blk & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           const int valid = min(128, sq.L - 128 * b);
           int lim = live ? valid : 0;
           if (a.causal) lim = min(lim, pos - 128 * b + 1);
-          const uint32_t tS = tmem + sb * 128 + lane_addr;
+          const uint32_t tS = tmem + gq * 256 + lane_addr;
           // block maximum (log2 units)
           float bm = -INFINITY;
 #pragma unroll
@@ -356,12 +372,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
           if (__any_sync(0xffffffffu, raise)) {
             const float f = raise ? (m == -INFINITY ? 0.f : ex2_approx(m - bm)) : 1.f;
             if (b > 0) {
-              // O holds this tile's blocks so far: rescale it once the last
-              // p v into it is done
-              ok = dwarp_all(mbar_wait(&c.p_empty[(blk - 1) & 1], ((blk - 1) >> 1) & 1, abort_flag, fl,
-                                       MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-              if (!ok) break;
-              tc_fence_after();
+              // O holds this tile's blocks so far and is complete: the
+              // issuer overwrote S only after the last p v into O was done
 #pragma unroll
               for (int cb = 0; cb < 4; ++cb) {
                 float ov[32];
@@ -396,11 +408,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
           tmem_st_wait();
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(&c.p_full[sb]);
+          mbar_arrive(&c.p_full[gq]);
         }
         if (!ok) break;
         // ---- the tile's output rows
-        ok = dwarp_all(mbar_wait(&c.o_full, n & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        ok = dwarp_all(mbar_wait(&c.o_full[gq], n & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
           a.lse[(size_t)(d.g * G + hh) * a.total_q + sq.q_begin + d.t0 + tt] =
               l > 0.f ? (m + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
         tc_fence_before();
-        mbar_arrive(&c.o_empty);
+        mbar_arrive(&c.o_empty[gq]);
       }
     }
   }
