@@ -130,8 +130,9 @@ __device__ __forceinline__ bool dense_tile(const DSeq* seq, const DCtrl& c, cons
 }
 
 // P = exp2(S * scale_log2 - m) of one row over keys 64h .. 64h + 63 (masked
-// to k < lim), packed in pairs and written to TMEM columns tP + 32h ..;
-// returns the partial row sum.
+// to k < lim unless kFull: every key visible), packed in pairs and written
+// to TMEM columns tP + 32h ..; returns the partial row sum.
+template <bool kFull>
 __device__ __forceinline__ float dense_p(const float* sv, int h, float scale_log2, float m, int lim, uint32_t tP,
                                          int bf16) {
   float l0 = 0.f, l1 = 0.f;
@@ -141,8 +142,10 @@ __device__ __forceinline__ float dense_p(const float* sv, int h, float scale_log
     const int k0 = 64 * h + 2 * i;
     float p0 = ex2_approx(fmaf(sv[2 * i], scale_log2, -m));
     float p1 = ex2_approx(fmaf(sv[2 * i + 1], scale_log2, -m));
-    p0 = k0 < lim ? p0 : 0.f;
-    p1 = k0 + 1 < lim ? p1 : 0.f;
+    if (!kFull) {
+      p0 = k0 < lim ? p0 : 0.f;
+      p1 = k0 + 1 < lim ? p1 : 0.f;
+    }
     if (i & 1) l1 += p0 + p1;
     else l0 += p0 + p1;
     pk[i] = dpack2(p0, p1, bf16);
@@ -356,8 +359,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
           int lim = live ? valid : 0;
           if (a.causal) lim = min(lim, pos - 128 * b + 1);
           const uint32_t tS = tmem + gq * 256 + lane_addr;
-          // block maximum (log2 units)
-          float bm = -INFINITY;
+          // block maximum (log2 units); a warp whose rows all see every key
+          // of the block skips the masking
+          const bool full = __all_sync(0xffffffffu, lim >= 128);
+          float b0 = -INFINITY, b1 = -INFINITY, b2 = -INFINITY, b3 = -INFINITY;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float sv[64];
@@ -365,9 +370,15 @@ __global__ void __launch_bounds__(kDThreads, 1)
             tmem_ld32(tS + h * 64 + 32, sv + 32);
             tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 64; ++k) bm = fmaxf(bm, 64 * h + k < lim ? sv[k] : -INFINITY);
+            for (int k = 0; k < 64; k += 4) {
+              const int kk = 64 * h + k;
+              b0 = fmaxf(b0, full || kk < lim ? sv[k] : -INFINITY);
+              b1 = fmaxf(b1, full || kk + 1 < lim ? sv[k + 1] : -INFINITY);
+              b2 = fmaxf(b2, full || kk + 2 < lim ? sv[k + 2] : -INFINITY);
+              b3 = fmaxf(b3, full || kk + 3 < lim ? sv[k + 3] : -INFINITY);
+            }
           }
-          bm *= a.scale_log2;
+          const float bm = fmaxf(fmaxf(b0, b1), fmaxf(b2, b3)) * a.scale_log2;
           const bool raise = bm > m + kDRescale || (m == -INFINITY && bm > -INFINITY);
           if (__any_sync(0xffffffffu, raise)) {
             const float f = raise ? (m == -INFINITY ? 0.f : ex2_approx(m - bm)) : 1.f;
@@ -397,7 +408,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
             tmem_ld32(tS + h * 64, sv);
             tmem_ld32(tS + h * 64 + 32, sv + 32);
             tmem_ld_wait();
-            l += dense_p(sv, h, a.scale_log2, m == -INFINITY ? 0.f : m, lim, tS, bf16);
+            const float mm = m == -INFINITY ? 0.f : m;
+            l += full ? dense_p<true>(sv, h, a.scale_log2, mm, lim, tS, bf16)
+                      : dense_p<false>(sv, h, a.scale_log2, mm, lim, tS, bf16);
           }
           if (valid < 128 && r >= valid) {
             // keys past the sequence end: zero V rows (stale values may be
