@@ -85,8 +85,9 @@ __device__ __forceinline__ uint32_t dswz(uint32_t row, uint32_t chunk16) {
   return (chunk16 >> 3) * 16384u + row * 128u + (((chunk16 & 7u) ^ (row & 7u)) << 4);
 }
 
-__device__ __forceinline__ uint32_t dpack2(float a, float b, int bf16) {
-  if (bf16) {
+template <bool kBf16>
+__device__ __forceinline__ uint32_t dpack2(float a, float b) {
+  if (kBf16) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
@@ -132,9 +133,8 @@ __device__ __forceinline__ bool dense_tile(const DSeq* seq, const DCtrl& c, cons
 // P = exp2(S * scale_log2 - m) of one row over keys 64h .. 64h + 63 (masked
 // to k < lim unless kFull: every key visible), packed in pairs and written
 // to TMEM columns tP + 32h ..; returns the partial row sum.
-template <bool kFull>
-__device__ __forceinline__ float dense_p(const float* sv, int h, float scale_log2, float m, int lim, uint32_t tP,
-                                         int bf16) {
+template <bool kFull, bool kBf16>
+__device__ __forceinline__ float dense_p(const float* sv, int h, float scale_log2, float m, int lim, uint32_t tP) {
   float l0 = 0.f, l1 = 0.f;
   uint32_t pk[32];
 #pragma unroll
@@ -148,12 +148,13 @@ __device__ __forceinline__ float dense_p(const float* sv, int h, float scale_log
     }
     if (i & 1) l1 += p0 + p1;
     else l0 += p0 + p1;
-    pk[i] = dpack2(p0, p1, bf16);
+    pk[i] = dpack2<kBf16>(p0, p1);
   }
   tmem_st32(tP + 32 * h, pk);
   return l0 + l1;
 }
 
+template <bool kBf16>
 __global__ void __launch_bounds__(kDThreads, 1)
     k_dense(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
             const __grid_constant__ CUtensorMap tmv, DenseArgs a) {
@@ -286,8 +287,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
       // sees S its O is complete too.
       if (lane == 0) {
         const int gq = warp - kDMma;
-        const uint32_t id_qk = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 0);
-        const uint32_t id_pv = idesc_f16(128, 128, (uint32_t)a.ab_bf16, 0, 1);
+        const uint32_t id_qk = idesc_f16(128, 128, kBf16 ? 1u : 0u, 0, 0);
+        const uint32_t id_pv = idesc_f16(128, 128, kBf16 ? 1u : 0u, 0, 1);
         const uint32_t q_s = sbase + kDOffQ + gq * kDTile;
         const uint32_t tS = tmem + gq * 256, tO = tS + 128;
         int blk = 0, n = 0;
@@ -341,7 +342,6 @@ __global__ void __launch_bounds__(kDThreads, 1)
       const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
       const uint32_t tO = tmem + gq * 256 + 128 + lane_addr;
       const int tt = gq * a.T + r / G, hh = r % G;  // token within the tile, head within the group
-      const int bf16 = a.ab_bf16;
       int blk = 0, n = 0;
       bool ok = true;
       DTile d;
@@ -409,17 +409,18 @@ __global__ void __launch_bounds__(kDThreads, 1)
             tmem_ld32(tS + h * 64 + 32, sv + 32);
             tmem_ld_wait();
             const float mm = m == -INFINITY ? 0.f : m;
-            l += full ? dense_p<true>(sv, h, a.scale_log2, mm, lim, tS, bf16)
-                      : dense_p<false>(sv, h, a.scale_log2, mm, lim, tS, bf16);
+            l += full ? dense_p<true, kBf16>(sv, h, a.scale_log2, mm, lim, tS)
+                      : dense_p<false, kBf16>(sv, h, a.scale_log2, mm, lim, tS);
           }
           if (valid < 128 && r >= valid) {
             // keys past the sequence end: zero V rows (stale values may be
-            // NaN bit patterns, and 0 * NaN would reach O)
+            // NaN bit patterns, and 0 * NaN would reach O); the writer's
+            // proxy fence orders them before the p v that reads them
             const uint32_t vs = sbase + kDOffKV + st * kDStage + kDTile;
             for (int ch = 0; ch < 16; ++ch) st_shared_v4(vs + dswz(r, ch), 0, 0, 0, 0);
+            fence_proxy_async_smem();
           }
           tmem_st_wait();
-          fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&c.p_full[gq]);
         }
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              w[i] = d.nb > 0 ? dpack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, bf16) : 0u;
+              w[i] = d.nb > 0 ? dpack2<kBf16>(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l) : 0u;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               *reinterpret_cast<uint4*>(orow + cb * 64 + i * 16) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2],
@@ -528,19 +529,22 @@ cudaError_t launch_dense(const mxsa_problem& p, const void* q, const void* k_cac
   a.num_pages = p.num_pages;
   a.causal = p.causal;
   a.ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
+  auto* kern = a.ab_bf16 ? k_dense<true> : k_dense<false>;
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
   const size_t smem = dense_smem_bytes();
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [smem] {
-    attr_err = cudaFuncSetAttribute(k_dense, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr_err = cudaFuncSetAttribute(k_dense<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(k_dense<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   int sms = 148, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return launch_pdl(k_dense, dim3(sms), dim3(kDThreads), smem, st, tmq, tmk, tmv, a);
+  return launch_pdl(kern, dim3(sms), dim3(kDThreads), smem, st, tmq, tmk, tmv, a);
 }
 
 }  // namespace mxsa
