@@ -58,7 +58,7 @@ constexpr uint32_t kDOffSeq = kDOffKV + 2 * kDStage;
 struct DCtrl {
   // q_*, s_full, p_*, o_*: one per softmax group; kv_*: per ring stage
   uint64_t q_full[2], q_empty[2], kv_full[2], kv_empty[2], s_full[2], p_full[2], p_empty[2], o_full[2], o_empty[2],
-      done;
+      done, go1;
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t total_tiles, per_head;
@@ -93,6 +93,13 @@ __device__ __forceinline__ uint32_t dpack2(float a, float b) {
   }
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// max of three floats in one instruction (NaN operands are ignored, as by fmaxf)
+__device__ __forceinline__ float dmax3(float x, float y, float z) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
 }
 
 __device__ __forceinline__ bool dwarp_all(bool v) { return __all_sync(0xffffffffu, v); }
@@ -203,6 +210,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       mbar_init(&c.o_empty[i], 128);
     }
     mbar_init(&c.done, 2);
+    mbar_init(&c.go1, 1);
     c.abort_flag = 0;
     c.local_flags = 0;
     fence_mbar_init();
@@ -291,13 +299,22 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const uint32_t id_pv = idesc_f16(128, 128, kBf16 ? 1u : 0u, 0, 1);
         const uint32_t q_s = sbase + kDOffQ + gq * kDTile;
         const uint32_t tS = tmem + gq * 256, tO = tS + 128;
-        int blk = 0, n = 0;
+        int blk = 0, n = 0, ng = 0;
         bool ok = true;
         DTile d;
         for (; ok && dense_tile(seq, c, a, n, &d); ++n) {
           ok = mbar_wait(&c.q_full[gq], n & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
           if (d.nb == 0) mma_commit(&c.q_empty[gq]);  // q unused: free at once
+          if (gq == 1 && d.nb > 0) {
+            // group 1 starts a tile once group 0 has its first P, so the two
+            // groups' softmax and MMAs alternate instead of running in step
+            // (go1 completes once per tile with blocks; issuer 0 cannot run a
+            // tile ahead: its next tile needs this issuer's last p v)
+            ok = mbar_wait(&c.go1, ng & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            ++ng;
+            if (!ok) break;
+          }
           for (int b = 0; b < d.nb && ok; ++b, ++blk) {
             const int st = blk & 1;
             ok = mbar_wait(&c.kv_full[st], (blk >> 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
@@ -318,6 +335,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
             mma_commit(&c.s_full[gq]);
             ok = mbar_wait(&c.p_full[gq], blk & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
             if (!ok) break;
+            if (gq == 0 && b == 0) mbar_arrive(&c.go1);
             if (b == 0 && n > 0) {  // O of the previous tile has been read out
               ok = mbar_wait(&c.o_empty[gq], (n - 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
               if (!ok) break;
@@ -369,13 +387,23 @@ __global__ void __launch_bounds__(kDThreads, 1)
             tmem_ld32(tS + h * 64, sv);
             tmem_ld32(tS + h * 64 + 32, sv + 32);
             tmem_ld_wait();
+            if (full) {
 #pragma unroll
-            for (int k = 0; k < 64; k += 4) {
-              const int kk = 64 * h + k;
-              b0 = fmaxf(b0, full || kk < lim ? sv[k] : -INFINITY);
-              b1 = fmaxf(b1, full || kk + 1 < lim ? sv[k + 1] : -INFINITY);
-              b2 = fmaxf(b2, full || kk + 2 < lim ? sv[k + 2] : -INFINITY);
-              b3 = fmaxf(b3, full || kk + 3 < lim ? sv[k + 3] : -INFINITY);
+              for (int k = 0; k < 64; k += 8) {
+                b0 = dmax3(b0, sv[k], sv[k + 1]);
+                b1 = dmax3(b1, sv[k + 2], sv[k + 3]);
+                b2 = dmax3(b2, sv[k + 4], sv[k + 5]);
+                b3 = dmax3(b3, sv[k + 6], sv[k + 7]);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 64; k += 4) {
+                const int kk = 64 * h + k;
+                b0 = fmaxf(b0, kk < lim ? sv[k] : -INFINITY);
+                b1 = fmaxf(b1, kk + 1 < lim ? sv[k + 1] : -INFINITY);
+                b2 = fmaxf(b2, kk + 2 < lim ? sv[k + 2] : -INFINITY);
+                b3 = fmaxf(b3, kk + 3 < lim ? sv[k + 3] : -INFINITY);
+              }
             }
           }
           const float bm = fmaxf(fmaxf(b0, b1), fmaxf(b2, b3)) * a.scale_log2;
