@@ -30,24 +30,34 @@ int64_t max_blocks_per_seq(const mxsa_problem& p) {
   return ((int64_t)p.max_pages_per_seq * p.page_size + 127) / 128;
 }
 
-mxsa_status validate_problem(const mxsa_problem& p) {
-  if (p.num_seqs < 1 || p.total_q < 0 || p.num_q_heads < 1 || p.num_kv_heads < 1 || p.topk < 1 ||
-      p.num_pages < 1 || p.max_pages_per_seq < 1 || (p.causal != 0 && p.causal != 1) ||
-      !(p.softmax_scale >= 0.f) || !std::isfinite(p.softmax_scale))
+// Shape checks every entry point shares; the dense path and the store take
+// the problem without its top-k (they select nothing).
+mxsa_status validate_shape(const mxsa_problem& p) {
+  if (p.num_seqs < 1 || p.total_q < 0 || p.num_q_heads < 1 || p.num_kv_heads < 1 || p.num_pages < 1 ||
+      p.max_pages_per_seq < 1 || (p.causal != 0 && p.causal != 1) || !(p.softmax_scale >= 0.f) ||
+      !std::isfinite(p.softmax_scale))
     return MXSA_ERR_INVALID_ARG;
   if (p.num_q_heads % p.num_kv_heads != 0) return MXSA_ERR_INVALID_ARG;
   if (p.head_dim != 128) return MXSA_ERR_UNSUPPORTED;
   if (p.num_q_heads / p.num_kv_heads > 128) return MXSA_ERR_UNSUPPORTED;
-  if (p.topk > 256) return MXSA_ERR_UNSUPPORTED;
   if (p.page_size != 64 && p.page_size != 128) return MXSA_ERR_UNSUPPORTED;
   if (p.q_dtype != MXSA_BF16 && p.q_dtype != MXSA_FP16) return MXSA_ERR_UNSUPPORTED;
   if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3) return MXSA_ERR_UNSUPPORTED;
+  if ((int64_t)p.num_pages * p.num_kv_heads >= (1ll << 31)) return MXSA_ERR_UNSUPPORTED;
+  if ((int64_t)p.max_pages_per_seq * p.page_size >= (1ll << 30)) return MXSA_ERR_UNSUPPORTED;
+  return MXSA_OK;
+}
+
+// The sparse path: the shape plus the top-k and the index's size limits.
+mxsa_status validate_problem(const mxsa_problem& p) {
+  mxsa_status s = validate_shape(p);
+  if (s != MXSA_OK) return s;
+  if (p.topk < 1) return MXSA_ERR_INVALID_ARG;
+  if (p.topk > 256) return MXSA_ERR_UNSUPPORTED;
   const int64_t nslots = (int64_t)p.total_q * p.num_kv_heads * p.topk;
   if (nslots >= (1ll << 26)) return MXSA_ERR_UNSUPPORTED;  // slot ids and packed scan fields
   const int64_t keys_cap = (int64_t)p.num_kv_heads * p.num_seqs * max_blocks_per_seq(p);
   if (keys_cap >= (1ll << 31) - 1) return MXSA_ERR_UNSUPPORTED;
-  if ((int64_t)p.num_pages * p.num_kv_heads >= (1ll << 31)) return MXSA_ERR_UNSUPPORTED;
-  if ((int64_t)p.max_pages_per_seq * p.page_size >= (1ll << 30)) return MXSA_ERR_UNSUPPORTED;
   return MXSA_OK;
 }
 
@@ -339,7 +349,7 @@ mxsa_status mxsa_dense_fwd(const mxsa_problem* problem, const void* q, const voi
                            const int32_t* block_tables, const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
                            void* out, float* lse, int32_t* device_flags, void* stream) {
   if (!problem) return MXSA_ERR_INVALID_ARG;
-  mxsa_status s = validate_problem(*problem);
+  mxsa_status s = validate_shape(*problem);
   if (s != MXSA_OK) return s;
   const mxsa_problem& p = *problem;
   if (p.kv_dtype != p.q_dtype || p.num_seqs > 1024) return MXSA_ERR_UNSUPPORTED;
@@ -359,7 +369,7 @@ mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const i
                           const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
                           int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream) {
   if (!problem) return MXSA_ERR_INVALID_ARG;
-  mxsa_status s = validate_problem(*problem);
+  mxsa_status s = validate_shape(*problem);
   if (s != MXSA_OK) return s;
   const mxsa_problem& p = *problem;
   if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3) return MXSA_ERR_UNSUPPORTED;

@@ -178,6 +178,8 @@ mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device
  *   idx_cache[page][j][offset][:] = cast(idx_k[t][j][:]), j < idx_heads.
  * k, v: [n_tokens][num_kv_heads][128] in problem->q_dtype (bf16 or fp16);
  * idx_k: [n_tokens][idx_heads][idx_dim], same dtype, idx_dim a multiple of 8.
+ * Of the problem, the store reads the head counts, page size, page count and
+ * dtypes; topk, total_q and the sequence fields are not checked.
  * Caches: [num_pages][heads][page_size][dim] in problem->kv_dtype, which is
  * q_dtype (bits copied) or MXSA_FP8_E4M3: each value becomes x clamped to
  * [-448, 448] rounded to the nearest e4m3fn value, ties to even, NaN keeping
@@ -196,7 +198,8 @@ mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device
  * over keys p < used_kv_lens[s] (and p <= pos(t) = L - Tq_s + i when causal),
  * k_p / v_p read through block_tables as in mxsa_kvouter_fwd.  No key: out 0,
  * lse -inf.  Same tensors and layouts as the sparse path (q, caches, out
- * [total_q][Hq][128] in q_dtype, lse [Hq][total_q] or NULL); topk is unused.
+ * [total_q][Hq][128] in q_dtype, lse [Hq][total_q] or NULL); topk is unused
+ * and not checked, nor are the sparse index's size limits.
  * kv_dtype must equal q_dtype (BF16/FP16); num_seqs <= 1024.  Tokens outside
  * every sequence (cu_seqlens_q out of order or past total_q) are not written.
  * device_flags (device int32, may be NULL): MXSA_FLAG_PAGE when a needed

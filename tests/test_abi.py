@@ -127,3 +127,35 @@ def test_store_kv_arguments_rejected_before_any_launch(lib):
     assert lib.mxsa_store_kv(ctypes.byref(p), 4, None, fake, fake, fake, fake, None, None, 0, 0, None, None) == 1
     assert lib.mxsa_store_kv(ctypes.byref(p), 4, fake, fake8, fake, fake, fake, None, None, 0, 0, None, None) == 1
     assert lib.mxsa_store_kv(None, 4, *ok_args, None, None, 0, 0, None, None) == 1
+
+
+def test_dense_fwd_arguments_rejected_before_any_launch(lib):
+    P = ctypes.c_void_p
+    fake, fake8 = P(1 << 20), P((1 << 20) + 8)  # never dereferenced: validation fails first
+    tabs = [fake, fake, fake]                      # block_tables, cu_seqlens_q, used_kv_lens
+    p = _prob()
+
+    def call(prob, q=fake, k=fake, v=fake, t=tabs, out=fake, lse=None, flags=None):
+        pr = ctypes.byref(prob) if prob is not None else None
+        return lib.mxsa_dense_fwd(pr, q, k, v, *t, out, lse, flags, None)
+
+    assert call(None) == 1
+    # the caches must hold the query's type (no FP8 widening on this path)
+    assert call(_prob(kv_dtype=torch.float8_e4m3fn)) == 2
+    assert call(_prob(num_seqs=1025)) == 2  # the sequence table lives in shared memory
+    assert call(_prob(num_q_heads=12, num_kv_heads=5)) == 1  # an invalid shape stays invalid here
+    # topk is not the dense path's: a problem whose slot count the sparse
+    # index could not hold still passes validation (a null q is the error)
+    big = _prob(total_q=1 << 24, num_kv_heads=2, num_q_heads=16, topk=256)
+    assert lib.mxsa_workspace_size(ctypes.byref(big), None, None, None) in (1, 2)
+    assert call(big, q=None) == 1 and call(_prob(topk=0), q=None) == 1
+    # null tables; null tensors while there are tokens
+    assert call(p, t=[None, fake, fake]) == 1
+    assert call(p, t=[fake, fake, None]) == 1
+    assert call(p, q=None) == 1
+    assert call(p, out=None) == 1
+    # misaligned tensors and tables
+    assert call(p, q=fake8) == 1
+    assert call(p, t=[P((1 << 20) + 2), fake, fake]) == 1
+    assert call(p, t=[fake, P((1 << 20) + 4), fake]) == 1
+    assert call(p, lse=P((1 << 20) + 2)) == 1
