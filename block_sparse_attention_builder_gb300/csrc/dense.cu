@@ -24,7 +24,8 @@
 //   warps 9, 10  MMA issuers, one per group (tcgen05.mma, cta_group::1,
 //              M = N = 128, K = 16, FP32 accumulate): q k^T into the group's
 //              S once its previous p v is done, then P V into its O with P as
-//              the TMEM operand.
+//              the TMEM operand.  Issuer 1 starts each tile only once group
+//              0 has its first P, so the groups work out of step.
 // TMEM: S and O of each group (512 columns).  The tiles are visited in a
 // fixed order (round robin over the CTAs, latest tokens first), so every
 // role walks the same sequence without sharing a queue.
