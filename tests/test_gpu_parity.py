@@ -246,6 +246,49 @@ def test_softmax_scale():
     U.assert_close_lse(lse.cpu().numpy().T.reshape(-1), l_ref, 2e-3, "scale lse")
 
 
+# ------------------------------------------------------- many sequences
+def _many_seq_workload(name, tq, seed):
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(130, 900, len(tq))]
+    return W.custom(name, tq, lens, 8, 1, 64, 3, True, "uniform", seed)
+
+
+@pytest.mark.parametrize("name,tq,seed", [
+    # an all-decode batch past the 512 sequences of the plan's one-barrier
+    # form: the general form indexes it
+    ("decode_600", [1] * 600, 120),
+    # past the 1024 sequences whose scan every CTA repeats: one CTA scans
+    # and a grid barrier publishes the table
+    ("mixed_1100", ([1, 1, 0, 2] * 275), 121),
+])
+def test_many_sequences(name, tq, seed):
+    """Index and schedule bit-exact, the fused plan equal to the separate
+    calls, and the output against the oracle, for batches of many
+    sequences."""
+    import block_sparse_attention_builder_gb300 as mx
+    w = _many_seq_workload(name, tq, seed)
+    attn, out, lse, inp = U.run(w)
+    assert attn.status() == 0
+    got = U.read_index(attn)
+    ref = oracle.build_index(oracle.problem_for(w), w.selected, w.cu_seqlens_q, w.used_kv_lens)
+    assert got["flags"] == ref["flags"] == 0
+    for k in ("row_ptr", "entries", "slot_entry"):
+        assert np.array_equal(got[k], ref[k]), k
+    sch, sref = U.read_sched(attn, NUM_SMS), U.oracle_schedule(w, NUM_SMS)
+    for k in ("items", "cost_prefix", "cta_ptr", "items_dec", "cost_prefix_dec", "cta_ptr_dec"):
+        assert np.array_equal(sch[k], sref[k]), k
+    b = mx.SparseAttention(attn.prob, "cuda")
+    mx.build_index(attn.prob, inp["sel"], inp["cu"], inp["lens"], b.ws.index)
+    mx.schedule(attn.prob, b.ws.index, b.ws.sched)
+    torch.cuda.synchronize()
+    gb = U.read_index(b)
+    for k in got:
+        assert np.array_equal(np.asarray(got[k]), np.asarray(gb[k])), k
+    o_ref, l_ref = U.oracle_full(w)
+    U.assert_close_out(out.float().cpu().numpy().reshape(-1, 128), o_ref, 1e-2, f"{name} out")
+    U.assert_close_lse(lse.cpu().numpy().T.reshape(-1), l_ref, 2e-3, f"{name} lse")
+
+
 # ------------------------------------------------------------------ edges
 def _edge_workload():
     # seq 0: empty (L = 0, no tokens); seq 1: all slots -1 for token 0; seq 2:
