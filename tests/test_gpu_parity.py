@@ -46,6 +46,9 @@ def small_cases():
                               q_dtype="fp16", kv_dtype="fp16"),
         # G = 128 (the largest): one entry per tile, a 128-row q box
         "g128_tiny": W.custom("g128_tiny", [1, 6], [300, 800], 128, 1, 64, 3, True, "uniform", 112),
+        # top-k 256 (the largest): 256 slots per row through the index's
+        # per-row ranking and the combine's slot loop
+        "topk256": W.custom("topk256", [1, 50], [40000, 36000], 8, 1, 128, 256, True, "uniform", 113),
     }
 
 
