@@ -28,6 +28,11 @@ CASES = {
     "g3_causal": _dense_case("dense_g3", [50, 3], [400, 64], 12, 4, 64, True, 204),
     "g128": _dense_case("dense_g128", [3, 1], [500, 130], 128, 1, 128, True, 205),
     "empty_rows": _dense_case("dense_empty", [0, 2, 3], [100, 0, 300], 8, 1, 64, False, 206),
+    # 1024 sequences (the most the kernel's shared-memory table holds),
+    # some without tokens, some shorter than their new tokens
+    "seqs_1024": _dense_case("dense_1024", [1, 2, 0, 3] * 256,
+                             [int(x) for x in np.random.default_rng(207).integers(2, 400, 1024)], 8, 1, 64, True,
+                             207),
 }
 
 
