@@ -17,8 +17,8 @@ any element (or any page of the cache) has the same bits whether it is made
 on the CPU or on the GPU, so the full-size caches are generated directly in
 HBM while the oracle regenerates only the pages it needs.
 
-The five workloads follow the problem statement of the fw-ai/minimax-kernels
-README (section "Quick start": token-major q [Tq, Hq, 128], paged caches
+The five workloads use the tensor layout of the fw-ai/minimax-kernels README
+(section "Quick start": token-major q [Tq, Hq, 128], paged caches
 [pages, Hkv, page_size, 128], int32 selections [Tq, Hkv, topk] with -1 for
 none, int32 block tables, int64 cu_seqlens_q, int32 used_kv_lens).
 """
@@ -177,7 +177,7 @@ WORKLOADS["gqa_decode_p16"] = WorkloadSpec(
     page_size=64, topk=16, causal=False, selection="uniform_last", seed=1012,
     description="profiling copy of gqa_decode with 16 sequences")
 
-# The order of the five workloads as the problem statement lists them.
+# The five workloads, in a fixed order.
 WORKLOAD_ORDER = ["tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode"]
 
 

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
 Index and schedule: bit-exact.  Forward partials and combine: checked in
-isolation and end to end at the tolerances of the problem statement (BF16 /
-FP16 output atol = rtol = 1e-2, FP8 4e-2, lse 2e-3 absolute).  The small
+isolation and end to end at fixed tolerances (BF16 / FP16 output
+atol = rtol = 1e-2, FP8 4e-2, lse 2e-3 absolute).  The small
 cases span several tiles per key and ragged tails; the full-size workloads
 are checked bit-exactly for index and schedule and on sampled rows for the
 output.
