@@ -338,6 +338,28 @@ def _draw_selection(spec: WorkloadSpec, rng: np.random.Generator, lens: np.ndarr
     return sel
 
 
+def _share_prefix_pages(bt: np.ndarray, lens: np.ndarray, ps: int, prefix_blocks: int) -> None:
+    """Shared-prefix page tables (the hot groups of the skewed-decode
+    recipe, read as sequences that share a cached prefix): the hot sequences
+    of group j (sequence s with s % 8 == j and (s // 8) % 2 == 0) point the
+    pages of their first `prefix_blocks` 128-token blocks at the pages of
+    the group's first hot sequence, for every block that is full in both.
+    The pages they no longer reference stay in the cache, unused."""
+    per_blk = BLOCK // ps
+    owner: Dict[int, int] = {}
+    for s in range(len(lens)):
+        if (s // 8) % 2 != 0:
+            continue
+        j = s % 8
+        if j not in owner:
+            owner[j] = s
+            continue
+        o = owner[j]
+        full = min(int(lens[s]), int(lens[o])) // BLOCK
+        for b in range(min(prefix_blocks, full)):
+            bt[s, b * per_blk:(b + 1) * per_blk] = bt[o, b * per_blk:(b + 1) * per_blk]
+
+
 def make_workload(spec: WorkloadSpec, max_pages_per_seq: Optional[int] = None) -> Workload:
     rng = np.random.default_rng(spec.seed)
     B = len(spec.tq)
@@ -354,6 +376,8 @@ def make_workload(spec: WorkloadSpec, max_pages_per_seq: Optional[int] = None) -
     for s, n in enumerate(npages):
         bt[s, :n] = perm[off:off + n]
         off += n
+    if spec.extra.get("shared_prefix_blocks"):
+        _share_prefix_pages(bt, lens, ps, int(spec.extra["shared_prefix_blocks"]))
     sel = _draw_selection(spec, rng, lens, tq)
     cu = np.zeros(B + 1, dtype=np.int64)
     cu[1:] = np.cumsum(tq)
@@ -366,11 +390,12 @@ def workload(name: str) -> Workload:
 
 
 def custom(name: str, tq, kv_lens, num_q_heads, num_kv_heads, page_size, topk, causal, selection, seed,
-           q_dtype="bf16", kv_dtype="bf16") -> Workload:
+           q_dtype="bf16", kv_dtype="bf16", extra=None) -> Workload:
     """A small workload of the same recipe family, for parity and edge-case tests."""
     spec = WorkloadSpec(name=name, tq=list(tq), kv_lens=_fixed(kv_lens), num_q_heads=num_q_heads,
                         num_kv_heads=num_kv_heads, page_size=page_size, topk=topk, causal=causal,
-                        selection=selection, seed=seed, q_dtype=q_dtype, kv_dtype=kv_dtype)
+                        selection=selection, seed=seed, q_dtype=q_dtype, kv_dtype=kv_dtype,
+                        extra=dict(extra or {}))
     return make_workload(spec)
 
 

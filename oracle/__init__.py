@@ -9,8 +9,12 @@ Functions whose parity is pinned by tests/test_oracle_pins.py:
   attention_rows  -- dense-attention / masked-SDPA / closed-form pins
   combine         -- partition-merge identity against a single softmax
   build_index     -- brute-force per-key scan on small inputs
+  build_index_dedup -- brute force over physical block identities; equal to
+                     build_index when no pages are shared
   schedule        -- coverage / ordering / balance invariants
   decode          -- every code against torch's own dtype conversions
+  encode_e4m3, store -- every bf16/fp16 code against torch's clamp-and-cast
+                     (tests/test_store_pins.py)
 """
 from __future__ import annotations
 
@@ -65,6 +69,8 @@ def _load():
         _lib.oracle_combine.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P]
         _lib.oracle_build_index.restype = ctypes.c_int
         _lib.oracle_build_index.argtypes = [P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
+        _lib.oracle_build_index_dedup.restype = ctypes.c_int
+        _lib.oracle_build_index_dedup.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
         _lib.oracle_encode_e4m3.restype = ctypes.c_uint32
         _lib.oracle_encode_e4m3.argtypes = [ctypes.c_double]
         _lib.oracle_store.restype = ctypes.c_int64
@@ -188,6 +194,35 @@ def build_index(prob: OracleProblem, selected, cu_seqlens_q, used_kv_lens):
                                 ctypes.byref(nnz), ctypes.byref(flags))
     if rc != 0:
         raise RuntimeError(f"oracle_build_index failed: {rc}")
+    nkeys = prob.num_kv_heads * nb.value
+    return dict(nb=nb.value, row_ptr=row_ptr[:nkeys + 1].copy(), entries=entries[:nnz.value].copy(),
+                slot_entry=slot_entry[:nslots].copy(), flags=flags.value)
+
+
+def build_index_dedup(prob: OracleProblem, selected, cu_seqlens_q, used_kv_lens, block_tables):
+    """The index keyed by physical block (cross-sequence dedup): a row's
+    selection of a full block whose pages an earlier sequence holds at the
+    same logical block joins that sequence's key.  Same dict as build_index."""
+    lib = _load()
+    sel = _c(selected, np.int32)
+    cu = _c(cu_seqlens_q, np.int64)
+    lens = _c(used_kv_lens, np.int32)
+    bt = _c(block_tables, np.int32)
+    if bt.shape != (prob.num_seqs, prob.max_pages_per_seq):
+        raise ValueError("block_tables must be [num_seqs, max_pages_per_seq]")
+    cap_len = prob.max_pages_per_seq * prob.page_size
+    nb_cap = int(sum((min(max(int(L), 0), cap_len) + 127) // 128 for L in lens))
+    rp_cap = prob.num_kv_heads * nb_cap + 1
+    row_ptr = np.zeros(rp_cap, dtype=np.int32)
+    nslots = prob.total_q * prob.num_kv_heads * prob.topk
+    entries = np.zeros(max(nslots, 1), dtype=np.int32)
+    slot_entry = np.zeros(max(nslots, 1), dtype=np.int32)
+    nb, nnz, flags = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    rc = lib.oracle_build_index_dedup(ctypes.byref(prob), _ptr(sel), _ptr(cu), _ptr(lens), _ptr(bt),
+                                      ctypes.byref(nb), _ptr(row_ptr), ctypes.c_int64(rp_cap), _ptr(entries),
+                                      _ptr(slot_entry), ctypes.byref(nnz), ctypes.byref(flags))
+    if rc != 0:
+        raise RuntimeError(f"oracle_build_index_dedup failed: {rc}")
     nkeys = prob.num_kv_heads * nb.value
     return dict(nb=nb.value, row_ptr=row_ptr[:nkeys + 1].copy(), entries=entries[:nnz.value].copy(),
                 slot_entry=slot_entry[:nslots].copy(), flags=flags.value)

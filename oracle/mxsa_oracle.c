@@ -371,6 +371,151 @@ int oracle_build_index(const oracle_problem* p, const int32_t* sel, const int64_
   return 0;
 }
 
+/* ------------------------------------------- block index, physical dedup
+ * The index of cross-sequence block dedup: sequences that share a cached
+ * prefix point their block tables at the same physical pages, and such a
+ * block should be loaded once for every row of every sequence that selected
+ * it, not once per sequence.  The block identity becomes physical:
+ *
+ *   a block (s, b) is SHAREABLE when it is full (128 b + 128 <= L_s) and
+ *   its pages are valid: for page_size 128 the page block_tables[s][b], for
+ *   64 the pair block_tables[s][2b], [2b+1], each in [0, num_pages);
+ *   owner(s, b) = the smallest s' with (s', b) shareable and the same pages
+ *   at the same logical block b (s itself when none is smaller); a block
+ *   that is not shareable is its own owner;
+ *   key(slot)   = g * NB + blk_off[owner(s, b)] + b.
+ *
+ * Everything else is the plain index's definition above (entries by
+ * (key, slot), flags, capacities).  Two sequences' rows meet in one key only
+ * for the same logical block of the same physical pages, so the keys, the
+ * positions 128 b + i and the valid count 128 agree for every row of the
+ * key; each row keeps its own sequence's causal position.  Keys that lost
+ * their rows to an owner hold no entries. */
+typedef struct {
+  int64_t b, page0, page1;
+  int32_t s;
+} phys_block;
+
+static int cmp_phys_block(const void* a, const void* b) {
+  const phys_block* x = (const phys_block*)a;
+  const phys_block* y = (const phys_block*)b;
+  if (x->b != y->b) return x->b < y->b ? -1 : 1;
+  if (x->page0 != y->page0) return x->page0 < y->page0 ? -1 : 1;
+  if (x->page1 != y->page1) return x->page1 < y->page1 ? -1 : 1;
+  if (x->s != y->s) return x->s < y->s ? -1 : 1;
+  return 0;
+}
+
+int oracle_build_index_dedup(const oracle_problem* p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
+                             const int32_t* block_tables, int32_t* nb_out, int32_t* row_ptr, int64_t row_ptr_cap,
+                             int32_t* entries, int32_t* slot_entry, int32_t* nnz_out, int32_t* flags_out) {
+  const int32_t B = p->num_seqs, Hkv = p->num_kv_heads, K = p->topk, ps = p->page_size;
+  const int64_t cap_len = (int64_t)p->max_pages_per_seq * ps;
+  int32_t flags = 0;
+  int64_t* nblk = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t* blk_off = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t* Lc = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  const int64_t nslots = (int64_t)p->total_q * Hkv * K;
+  key_slot* ks = (key_slot*)malloc(sizeof(key_slot) * (size_t)(nslots > 0 ? nslots : 1));
+  if (!nblk || !blk_off || !Lc || !ks) {
+    free(nblk); free(blk_off); free(Lc); free(ks);
+    return -1;
+  }
+  if (cu[0] != 0 || cu[B] != p->total_q) flags |= OR_FLAG_CU;
+  for (int32_t s = 0; s < B; ++s)
+    if (cu[s + 1] < cu[s]) flags |= OR_FLAG_CU;
+  int64_t NB = 0;
+  for (int32_t s = 0; s < B; ++s) {
+    int64_t L = lens[s];
+    if (L < 0 || L > cap_len) flags |= OR_FLAG_LEN;
+    if (L < 0) L = 0;
+    if (L > cap_len) L = cap_len;
+    if (p->causal && L < cu[s + 1] - cu[s]) flags |= OR_FLAG_CAUSAL_LEN;
+    Lc[s] = L;
+    nblk[s] = (L + 127) / 128;
+    blk_off[s] = NB;
+    NB += nblk[s];
+  }
+  const int64_t nkeys = (int64_t)Hkv * NB;
+  /* owner of every (s, b): shareable blocks sorted by (b, pages, s); the
+   * first of each run of equal (b, pages) owns the run */
+  int32_t* owner = (int32_t*)malloc(sizeof(int32_t) * (size_t)(NB > 0 ? NB : 1));
+  phys_block* pb = (phys_block*)malloc(sizeof(phys_block) * (size_t)(NB > 0 ? NB : 1));
+  if (nkeys + 1 > row_ptr_cap || !owner || !pb) {
+    free(nblk); free(blk_off); free(Lc); free(ks); free(owner); free(pb);
+    return -1;
+  }
+  int64_t npb = 0;
+  for (int32_t s = 0; s < B; ++s) {
+    for (int64_t b = 0; b < nblk[s]; ++b) {
+      owner[blk_off[s] + b] = s;
+      if (128 * b + 128 > Lc[s]) continue; /* partial block: never shared */
+      const int32_t* bt = block_tables + (int64_t)s * p->max_pages_per_seq;
+      int64_t pg0 = ps == 128 ? bt[b] : bt[2 * b];
+      int64_t pg1 = ps == 128 ? -1 : bt[2 * b + 1];
+      if (pg0 < 0 || pg0 >= p->num_pages) continue;
+      if (ps != 128 && (pg1 < 0 || pg1 >= p->num_pages)) continue;
+      pb[npb].b = b;
+      pb[npb].page0 = pg0;
+      pb[npb].page1 = pg1;
+      pb[npb].s = s;
+      ++npb;
+    }
+  }
+  qsort(pb, (size_t)npb, sizeof(phys_block), cmp_phys_block);
+  for (int64_t i = 0; i < npb; ++i) {
+    int64_t first = i;
+    while (first > 0 && pb[first - 1].b == pb[i].b && pb[first - 1].page0 == pb[i].page0 &&
+           pb[first - 1].page1 == pb[i].page1)
+      --first;
+    owner[blk_off[pb[i].s] + pb[i].b] = pb[first].s;
+  }
+  int64_t n = 0;
+  for (int64_t slot = 0; slot < nslots; ++slot) slot_entry[slot] = -1;
+  const int64_t t_end = (flags & OR_FLAG_CU) ? 0 : p->total_q;
+  for (int64_t t = 0; t < t_end; ++t) {
+    int32_t s = seq_of_token(cu, B, t);
+    for (int32_t g = 0; g < Hkv; ++g) {
+      for (int32_t k = 0; k < K; ++k) {
+        int64_t slot = (t * Hkv + g) * K + k;
+        int32_t b = sel[slot];
+        if (b == -1 || s < 0) continue;
+        if (b < -1 || b >= nblk[s]) {
+          flags |= OR_FLAG_SEL_RANGE;
+          continue;
+        }
+        int dup = 0;
+        for (int32_t k2 = 0; k2 < k; ++k2)
+          if (sel[(t * Hkv + g) * K + k2] == b) dup = 1;
+        if (dup) {
+          flags |= OR_FLAG_SEL_DUP;
+          continue;
+        }
+        if (p->causal) {
+          int64_t pos = Lc[s] - (cu[s + 1] - cu[s]) + (t - cu[s]);
+          if (128 * (int64_t)b > pos) continue;
+        }
+        ks[n].key = g * NB + blk_off[owner[blk_off[s] + b]] + b;
+        ks[n].slot = slot;
+        ++n;
+      }
+    }
+  }
+  qsort(ks, (size_t)n, sizeof(key_slot), cmp_key_slot);
+  for (int64_t key = 0; key <= nkeys; ++key) row_ptr[key] = 0;
+  for (int64_t i = 0; i < n; ++i) row_ptr[ks[i].key + 1] += 1;
+  for (int64_t key = 0; key < nkeys; ++key) row_ptr[key + 1] += row_ptr[key];
+  for (int64_t i = 0; i < n; ++i) {
+    entries[i] = (int32_t)ks[i].slot;
+    slot_entry[ks[i].slot] = (int32_t)i;
+  }
+  *nb_out = (int32_t)NB;
+  *nnz_out = (int32_t)n;
+  *flags_out = flags;
+  free(nblk); free(blk_off); free(Lc); free(ks); free(owner); free(pb);
+  return 0;
+}
+
 /* --------------------------------------------------------------- schedule
  * Load-balancing schedule over the index ("load-balancing scheduler" in the
  * README's test list; the splitting rule, the decode merge and the cost

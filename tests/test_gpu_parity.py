@@ -49,6 +49,15 @@ def small_cases():
         # top-k 256 (the largest): 256 slots per row through the index's
         # per-row ranking and the combine's slot loop
         "topk256": W.custom("topk256", [1, 50], [40000, 36000], 8, 1, 128, 256, True, "uniform", 113),
+        # shared-prefix page tables: hot sequences s and s + 16 of a group
+        # point their first 64 blocks at the same pages (the plain index
+        # keeps one key per sequence; the pages are read once per sequence)
+        "shared_prefix_decode": W.custom("shared_prefix_decode", [1] * 24, [9000, 3000, 700, 20000, 129, 8192] * 4,
+                                         16, 2, 64, 16, False, "hot_groups", 114,
+                                         extra={"shared_prefix_blocks": 64}),
+        "shared_prefix_prefill": W.custom("shared_prefix_prefill", [1, 3, 0, 5] * 6, [9000, 4000, 300, 12000] * 6,
+                                          8, 1, 128, 8, True, "hot_groups", 115,
+                                          extra={"shared_prefix_blocks": 64}),
     }
 
 
