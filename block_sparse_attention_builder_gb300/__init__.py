@@ -130,6 +130,39 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_ELEM_BYTES = {BF16: 2, FP16: 2, FP8_E4M3: 1}
+
+
+def _need(what: str, name: str, t: Optional[torch.Tensor], nbytes: int):
+    """The kernels index every buffer by the problem's shape, and a pointer
+    carries no size: a tensor smaller than that shape, or not contiguous,
+    is refused here, before the C call (MXSA_ERR_INVALID_ARG).  Only bytes
+    are compared, so raw views of a cache (uint8, int16) are accepted."""
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise MxsaError(1, f"{what}: {name} is not contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise MxsaError(1, f"{what}: {name} holds {have} bytes, the problem needs {nbytes}")
+
+
+def _need_attention(what: str, prob: Problem, q=None, k_cache=None, v_cache=None, block_tables=None,
+                    cu_seqlens_q=None, used_kv_lens=None, sel=None, out=None, lse=None):
+    qb, kb = _ELEM_BYTES.get(prob.q_dtype, 2), _ELEM_BYTES.get(prob.kv_dtype, 2)
+    rows = max(prob.total_q, 0) * max(prob.num_q_heads, 0)
+    cache = max(prob.num_pages, 0) * max(prob.num_kv_heads, 0) * max(prob.page_size, 0) * 128 * kb
+    _need(what, "q", q, rows * 128 * qb)
+    _need(what, "k_cache", k_cache, cache)
+    _need(what, "v_cache", v_cache, cache)
+    _need(what, "block_tables", block_tables, max(prob.num_seqs, 0) * max(prob.max_pages_per_seq, 0) * 4)
+    _need(what, "cu_seqlens_q", cu_seqlens_q, (max(prob.num_seqs, 0) + 1) * 8)
+    _need(what, "used_kv_lens", used_kv_lens, max(prob.num_seqs, 0) * 4)
+    _need(what, "selected", sel, max(prob.total_q, 0) * max(prob.num_kv_heads, 0) * max(prob.topk, 0) * 4)
+    _need(what, "out", out, rows * 128 * qb)
+    _need(what, "lse", lse, rows * 4)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -164,6 +197,7 @@ def sched_layout(prob: Problem) -> SchedLayout:
 
 
 def build_index(prob, sel, cu_seqlens_q, used_kv_lens, index_ws, stream=None):
+    _need_attention("mxsa_build_index", prob, cu_seqlens_q=cu_seqlens_q, used_kv_lens=used_kv_lens, sel=sel)
     _check(_lib.mxsa_build_index(ctypes.byref(prob), _ptr(sel), _ptr(cu_seqlens_q), _ptr(used_kv_lens),
                                  _ptr(index_ws), index_ws.numel() * index_ws.element_size(), _stream(stream)),
            "mxsa_build_index")
@@ -177,12 +211,14 @@ def schedule(prob, index_ws, sched_ws, num_ctas=0, stream=None):
 
 def plan(prob, sel, cu_seqlens_q, used_kv_lens, index_ws, sched_ws, num_ctas=0, stream=None):
     """build_index + schedule in one launch (identical workspaces)."""
+    _need_attention("mxsa_plan", prob, cu_seqlens_q=cu_seqlens_q, used_kv_lens=used_kv_lens, sel=sel)
     _check(_lib.mxsa_plan(ctypes.byref(prob), _ptr(sel), _ptr(cu_seqlens_q), _ptr(used_kv_lens), _ptr(index_ws),
                           index_ws.numel() * index_ws.element_size(), int(num_ctas), _ptr(sched_ws),
                           sched_ws.numel() * sched_ws.element_size(), _stream(stream)), "mxsa_plan")
 
 
 def kvouter_fwd(prob, q, k_cache, v_cache, block_tables, index_ws, sched_ws, partial_ws, num_ctas=0, stream=None):
+    _need_attention("mxsa_kvouter_fwd", prob, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables)
     _check(_lib.mxsa_kvouter_fwd(ctypes.byref(prob), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                  _ptr(index_ws), index_ws.numel() * index_ws.element_size(), _ptr(sched_ws),
                                  sched_ws.numel() * sched_ws.element_size(), int(num_ctas), _ptr(partial_ws),
@@ -191,6 +227,7 @@ def kvouter_fwd(prob, q, k_cache, v_cache, block_tables, index_ws, sched_ws, par
 
 
 def combine(prob, index_ws, partial_ws, out, lse=None, stream=None):
+    _need_attention("mxsa_combine", prob, out=out, lse=lse)
     _check(_lib.mxsa_combine(ctypes.byref(prob), _ptr(index_ws), index_ws.numel() * index_ws.element_size(),
                              _ptr(partial_ws), partial_ws.numel() * partial_ws.element_size(), _ptr(out), _ptr(lse),
                              _stream(stream)), "mxsa_combine")
@@ -200,6 +237,9 @@ def dense_fwd(prob, q, k_cache, v_cache, block_tables, cu_seqlens_q, used_kv_len
               stream=None):
     """Dense paged attention (every key of each sequence; causal per the
     problem) straight into out [total_q, Hq, 128] and lse [Hq, total_q]."""
+    _need_attention("mxsa_dense_fwd", prob, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                    cu_seqlens_q=cu_seqlens_q, used_kv_lens=used_kv_lens, out=out, lse=lse)
+    _need("mxsa_dense_fwd", "flags", flags, 4)
     _check(_lib.mxsa_dense_fwd(ctypes.byref(prob), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                _ptr(cu_seqlens_q), _ptr(used_kv_lens), _ptr(out), _ptr(lse), _ptr(flags),
                                _stream(stream)), "mxsa_dense_fwd")
@@ -213,6 +253,15 @@ def store_kv(prob, loc, k, v, k_cache, v_cache, idx_k=None, idx_cache=None, flag
     device tensor that receives MXSA_FLAG_PAGE for slots past the cache."""
     n = int(loc.numel())
     ih, idim = (int(idx_k.shape[1]), int(idx_k.shape[2])) if idx_k is not None else (0, 0)
+    what = "mxsa_store_kv"
+    qb, kb = _ELEM_BYTES.get(prob.q_dtype, 2), _ELEM_BYTES.get(prob.kv_dtype, 2)
+    _need(what, "loc", loc, n * 8)
+    _need(what, "k", k, n * prob.num_kv_heads * 128 * qb)
+    _need(what, "v", v, n * prob.num_kv_heads * 128 * qb)
+    _need_attention(what, prob, k_cache=k_cache, v_cache=v_cache)
+    _need(what, "idx_k", idx_k, n * ih * idim * qb)
+    _need(what, "idx_cache", idx_cache, max(prob.num_pages, 0) * ih * max(prob.page_size, 0) * idim * kb)
+    _need(what, "flags", flags, 4)
     _check(_lib.mxsa_store_kv(ctypes.byref(prob), n, _ptr(loc), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                               _ptr(idx_k), _ptr(idx_cache), ih, idim, _ptr(flags), _stream(stream)), "mxsa_store_kv")
 

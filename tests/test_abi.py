@@ -159,3 +159,44 @@ def test_dense_fwd_arguments_rejected_before_any_launch(lib):
     assert call(p, t=[P((1 << 20) + 2), fake, fake]) == 1
     assert call(p, t=[fake, P((1 << 20) + 4), fake]) == 1
     assert call(p, lse=P((1 << 20) + 2)) == 1
+
+
+def test_binding_refuses_buffers_smaller_than_the_problem(lib):
+    """A pointer carries no size, so the binding compares every tensor's
+    bytes with what the problem's shape makes the kernels touch, and refuses
+    short or non-contiguous tensors before the C call (no GPU needed: the
+    refusal comes first)."""
+    p = _prob(num_seqs=2, total_q=4, num_q_heads=16, num_kv_heads=2, topk=8, page_size=64, num_pages=100,
+              max_pages_per_seq=40)
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    q, out = bf(4, 16, 128), bf(4, 16, 128)
+    kc = torch.zeros(100 * 2 * 64 * 128 * 2, dtype=torch.uint8)  # raw bytes are accepted
+    bt = torch.zeros(2, 40, dtype=torch.int32)
+    cu, lens = torch.zeros(3, dtype=torch.int64), torch.zeros(2, dtype=torch.int32)
+    lse = torch.zeros(16, 4, dtype=torch.float32)
+    sel = torch.zeros(4, 2, 8, dtype=torch.int32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+
+    def refused(fn, *a, **k):
+        with pytest.raises(mx.MxsaError) as ei:
+            fn(*a, **k)
+        assert ei.value.status == 1
+
+    refused(mx.dense_fwd, p, q[:3], kc, kc, bt, cu, lens, out, lse)          # q short by one token
+    refused(mx.dense_fwd, p, q, kc[:-1], kc, bt, cu, lens, out, lse)         # cache short by one byte
+    refused(mx.dense_fwd, p, q, kc, kc, bt[:, :39], cu, lens, out, lse)      # table narrower than max_pages
+    refused(mx.dense_fwd, p, q, kc, kc, bt, cu[:2], lens, out, lse)          # cu_seqlens_q needs B + 1
+    refused(mx.dense_fwd, p, q, kc, kc, bt, cu, lens, out, lse[:, :3])       # lse short
+    refused(mx.dense_fwd, p, q, kc, kc, bt, cu, lens, out.transpose(0, 1), lse)  # not contiguous
+    refused(mx.plan, p, sel[:, :, :7].contiguous(), cu, lens, ws, ws)        # topk slots short
+    refused(mx.build_index, p, sel, cu, lens[:1], ws)
+    refused(mx.kvouter_fwd, p, q, kc, kc[:10], bt, ws, ws, ws)
+    refused(mx.combine, p, ws, ws, out[:2])
+    ps = _prob(num_q_heads=2, num_kv_heads=2, page_size=64, num_pages=3, kv_dtype=torch.float8_e4m3fn)
+    loc = torch.zeros(5, dtype=torch.int64)
+    k5 = bf(5, 2, 128)
+    c8 = torch.zeros(3, 2, 64, 128, dtype=torch.uint8)
+    refused(mx.store_kv, ps, loc, k5[:4], k5, c8, c8)                        # k short
+    refused(mx.store_kv, ps, loc, k5, k5, c8[:2], c8)                        # cache short
+    refused(mx.store_kv, ps, loc, k5, k5, c8, c8, idx_k=bf(5, 1, 64),
+            idx_cache=torch.zeros(3, 1, 64, 63, dtype=torch.uint8))          # index cache short
