@@ -34,13 +34,25 @@ DTYPE_CODE = {"bf16": 0, "fp16": 1, "fp8": 2}
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain C11, -O2, pthreads)."""
+    """Compile the oracle with gcc (plain C11, -O2, pthreads).  With
+    MXSA_ORACLE_LIB set, that library is used as it is (the mutant test)."""
+    if os.environ.get("MXSA_ORACLE_LIB"):
+        return os.environ["MXSA_ORACLE_LIB"]
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def build_mutant(n: int, out_dir: str) -> str:
+    """The oracle with planted mistake n (-DORACLE_MUTANT=n), for the test
+    that checks the pins catch it."""
+    path = os.path.join(out_dir, f"liboracle_mutant{n}.so")
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread", f"-DORACLE_MUTANT={int(n)}",
+                           "-o", path, _SRC, "-lm"])
+    return path
 
 
 class OracleProblem(ctypes.Structure):

@@ -42,6 +42,14 @@ enum {
   OR_FLAG_CU = 128         /* cu_seqlens_q not a valid partition of the tokens */
 };
 
+/* Planted mistakes, for the test that checks the pins catch them
+ * (tests/test_oracle_mutants.py): a build with -DORACLE_MUTANT=n makes
+ * mistake n, listed where it is planted; the default build makes none. */
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+#define MUT(n) (ORACLE_MUTANT == (n))
+
 typedef struct {
   int32_t num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, topk, page_size, num_pages,
       max_pages_per_seq, causal;
@@ -54,7 +62,7 @@ typedef struct {
  * definitions (IEEE-754 binary16; bfloat16 = upper half of binary32;
  * OCP FP8 E4M3 "fn": bias 7, no infinities, S.1111.111 is NaN). */
 static double decode_bf16(uint32_t bits) {
-  uint32_t u = (bits & 0xFFFFu) << 16;
+  uint32_t u = (bits & 0xFFFFu) << (MUT(1) ? 15 : 16); /* mutant 1: misplaced bits */
   float f;
   memcpy(&f, &u, 4);
   return (double)f;
@@ -80,7 +88,7 @@ static double decode_e4m3(uint32_t bits) {
   if (e == 0)
     v = ldexp((double)m, -9); /* subnormal: m/8 * 2^-6 */
   else
-    v = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    v = ldexp(1.0 + (double)m / 8.0, (int)e - (MUT(2) ? 8 : 7)); /* mutant 2: wrong exponent bias */
   return s ? -v : v;
 }
 
@@ -125,8 +133,10 @@ typedef struct {
 static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double* lse_out) {
   const oracle_problem* p = J->p;
   const int32_t D = p->head_dim, Hq = p->num_q_heads, Hkv = p->num_kv_heads;
-  const int32_t G = Hq / Hkv, g = h / G, ps = p->page_size;
-  const double scale = p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)D);
+  const int32_t G = Hq / Hkv, ps = p->page_size;
+  const int32_t g = MUT(3) ? h % Hkv : h / G; /* mutant 3: interleaved GQA map */
+  const double scale = MUT(4) ? 1.0 : (p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)D));
+  /* mutant 4: the scale dropped */
   for (int32_t d = 0; d < D; ++d) out[d] = 0.0;
   *lse_out = -INFINITY;
   int32_t s = seq_of_token(J->cu, p->num_seqs, t);
@@ -135,7 +145,7 @@ static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double
   if (L < 0) L = 0;
   if (L > (int64_t)p->max_pages_per_seq * ps) L = (int64_t)p->max_pages_per_seq * ps;
   const int64_t Tq_s = J->cu[s + 1] - J->cu[s];
-  const int64_t pos = L - Tq_s + (t - J->cu[s]);
+  const int64_t pos = L - Tq_s + (t - J->cu[s]) - (MUT(5) ? 1 : 0); /* mutant 5: causal offset */
   const int64_t nblk = (L + 127) / 128;
 
   unsigned char* in_set = (unsigned char*)calloc((size_t)(L > 0 ? L : 1), 1);
@@ -149,6 +159,7 @@ static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double
     int32_t b = J->sel[(t * Hkv + g) * p->topk + k];
     if (b < 0 || b >= nblk) continue;
     int64_t hi = 128 * (int64_t)b + 128 < L ? 128 * (int64_t)b + 128 : L;
+    if (MUT(6) && hi == 128 * (int64_t)b + 128) --hi; /* mutant 6: a block's last key dropped */
     for (int64_t pp = 128 * (int64_t)b; pp < hi; ++pp)
       if (!p->causal || pp <= pos) in_set[pp] = 1;
   }
@@ -158,12 +169,14 @@ static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double
   int64_t count = 0;
   for (int64_t pp = 0; pp < L; ++pp) {
     if (!in_set[pp]) continue;
-    int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + pp / ps];
+    int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + (MUT(7) ? pp / 128 : pp / ps)];
+    /* mutant 7: the page walk steps by block, not by page */
     if (page < 0 || page >= p->num_pages) {
       free(in_set); free(qv); free(sc);
       return -2;
     }
-    int64_t base = (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
+    int64_t base = MUT(8) ? (((int64_t)page * ps + pp % ps) * Hkv + g) * D /* mutant 8: [page][pos][head] */
+                          : (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
     double dot = 0.0;
     for (int32_t d = 0; d < D; ++d) dot += qv[d] * load_elem(J->k, p->kv_dtype, base + d);
     sc[pp] = scale * dot;
@@ -174,14 +187,15 @@ static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double
     double l = 0.0;
     for (int64_t pp = 0; pp < L; ++pp) {
       if (!in_set[pp]) continue;
-      int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + pp / ps];
-      int64_t base = (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
+      int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + (MUT(7) ? pp / 128 : pp / ps)];
+      int64_t base = MUT(8) ? (((int64_t)page * ps + pp % ps) * Hkv + g) * D
+                            : (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
       double w = exp(sc[pp] - m);
       l += w;
       for (int32_t d = 0; d < D; ++d) out[d] += w * load_elem(J->v, p->kv_dtype, base + d);
     }
     for (int32_t d = 0; d < D; ++d) out[d] /= l;
-    *lse_out = m + log(l);
+    *lse_out = m + (MUT(9) ? log2(l) : log(l)); /* mutant 9: lse in base 2 */
   }
   free(in_set); free(qv); free(sc);
   return 0;
@@ -249,7 +263,7 @@ void oracle_combine(int32_t n, int32_t d, const double* o, const double* lse, do
   double W = 0.0;
   for (int32_t k = 0; k < n; ++k) {
     if (lse[k] == -INFINITY) continue;
-    double w = exp(lse[k] - M);
+    double w = MUT(10) ? 1.0 : exp(lse[k] - M); /* mutant 10: parts averaged unweighted */
     W += w;
     for (int32_t j = 0; j < d; ++j) out[j] += w * o[(int64_t)k * d + j];
   }
@@ -286,7 +300,7 @@ static int cmp_key_slot(const void* a, const void* b) {
   const key_slot* x = (const key_slot*)a;
   const key_slot* y = (const key_slot*)b;
   if (x->key != y->key) return x->key < y->key ? -1 : 1;
-  if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;
+  if (x->slot != y->slot) return (x->slot < y->slot) != MUT(12) ? -1 : 1; /* mutant 12: slots descending */
   return 0;
 }
 
@@ -348,7 +362,7 @@ int oracle_build_index(const oracle_problem* p, const int32_t* sel, const int64_
         if (p->causal) {
           int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
           int64_t pos = L - (cu[s + 1] - cu[s]) + (t - cu[s]);
-          if (128 * (int64_t)b > pos) continue;
+          if (128 * (int64_t)b > pos - (MUT(11) ? 1 : 0)) continue; /* mutant 11: causal drop off by one */
         }
         ks[n].key = g * NB + blk_off[s] + b;
         ks[n].slot = slot;
@@ -449,7 +463,7 @@ int oracle_build_index_dedup(const oracle_problem* p, const int32_t* sel, const 
   for (int32_t s = 0; s < B; ++s) {
     for (int64_t b = 0; b < nblk[s]; ++b) {
       owner[blk_off[s] + b] = s;
-      if (128 * b + 128 > Lc[s]) continue; /* partial block: never shared */
+      if (128 * b + 128 > Lc[s] && !MUT(13)) continue; /* partial block: never shared (mutant 13: shared) */
       const int32_t* bt = block_tables + (int64_t)s * p->max_pages_per_seq;
       int64_t pg0 = ps == 128 ? bt[b] : bt[2 * b];
       int64_t pg1 = ps == 128 ? -1 : bt[2 * b + 1];
@@ -468,7 +482,7 @@ int oracle_build_index_dedup(const oracle_problem* p, const int32_t* sel, const 
     while (first > 0 && pb[first - 1].b == pb[i].b && pb[first - 1].page0 == pb[i].page0 &&
            pb[first - 1].page1 == pb[i].page1)
       --first;
-    owner[blk_off[pb[i].s] + pb[i].b] = pb[first].s;
+    owner[blk_off[pb[i].s] + pb[i].b] = MUT(14) ? pb[i].s : pb[first].s; /* mutant 14: nothing merged */
   }
   int64_t n = 0;
   for (int64_t slot = 0; slot < nslots; ++slot) slot_entry[slot] = -1;
@@ -632,7 +646,8 @@ int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t*
       if (g2 != g || s2 != s) break;
       ++len;
     }
-    const int64_t n = (len + decode_blocks - 1) / decode_blocks;
+    const int64_t n = MUT(15) ? len / decode_blocks + 1 : (len + decode_blocks - 1) / decode_blocks;
+    /* mutant 15: one item too many when len is a multiple of decode_blocks */
     for (int64_t i = 0; i < n; ++i) {
       const int64_t k0 = i * len / n, k1 = (i + 1) * len / n;
       if (nd >= items_cap) { free(active); return -1; }
@@ -681,6 +696,7 @@ static double round_half_even(double y) {
   const double f = floor(y), r = y - f;
   if (r > 0.5) return f + 1.0;
   if (r < 0.5) return f;
+  if (MUT(16)) return f + 1.0; /* mutant 16: ties away from zero */
   return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
 }
 

@@ -450,6 +450,16 @@ def test_schedule_decode_run_worked_example():
     assert sch["cost_prefix_dec"].tolist() == [0, first, first + second]
 
 
+def test_schedule_decode_run_of_a_multiple_of_the_item_size():
+    # a run of 16 keys with 8 keys per decode item: exactly 2 items of 8
+    sel = np.arange(16, dtype=np.int32).reshape(1, 1, 16)
+    cu = np.array([0, 1], np.int64)
+    prob = oracle.problem(1, 1, 8, 1, 16, 64, 32, 32, False)
+    idx = oracle.build_index(prob, sel, cu, np.array([2048], np.int32))
+    sch = oracle.schedule(prob, [2048], cu, idx, 4, 8, 2)
+    assert sch["items_dec"][:, 0].tolist() == [0, 8] and sch["items_dec"][:, 3].tolist() == [8, 8]
+
+
 @pytest.mark.parametrize("name", ["tiny_decode", "shared_prefill_small", "varlen_small", "skewed_small"])
 def test_schedule_invariants(name):
     if name == "shared_prefill_small":
@@ -483,6 +493,25 @@ def test_schedule_invariants(name):
                 toks = {int(idx["entries"][rp[k]]) // (w.num_kv_heads * w.topk) for k in keys}
                 assert len(toks) == 1 and tq[np.searchsorted(w.cu_seqlens_q, toks.pop(), side="right") - 1] == 1
             assert sorted(covered) == list(range(len(idx["entries"])))
+            # the fewest items the size limits allow, split evenly: a normal
+            # key of cnt entries gets ceil(cnt / E) items, a decode run of
+            # len keys ceil(len / D), item sizes differing by at most one
+            E = R * max(1, 128 // G)
+            per_key = {}
+            for key, _, n, _ in sch["items"]:
+                per_key.setdefault(int(key), []).append(int(n))
+            for key, sizes in per_key.items():
+                cnt = int(rp[key + 1] - rp[key])
+                assert sum(sizes) == cnt and len(sizes) == -(-cnt // E) and max(sizes) - min(sizes) <= 1
+            per_run = {}
+            for a0, e, _, nk in sch["items_dec"]:
+                g = int(active[a0]) // idx["nb"]
+                tok = int(idx["entries"][e]) // (w.num_kv_heads * w.topk)
+                per_run.setdefault((tok, g), []).append(int(nk))
+            for (tok, g), sizes in per_run.items():
+                run = int(np.count_nonzero(idx["slot_entry"][(tok * w.num_kv_heads + g) * w.topk:
+                                                             (tok * w.num_kv_heads + g + 1) * w.topk] >= 0))
+                assert sum(sizes) == run and len(sizes) == -(-run // D) and max(sizes) - min(sizes) <= 1
             for it, cp, cost in (("items", "cta_ptr", "cost_prefix"), ("items_dec", "cta_ptr_dec", "cost_prefix_dec")):
                 c = sch[cp]
                 assert c[0] == 0 and c[-1] == len(sch[it]) and np.all(np.diff(c) >= 0)
