@@ -167,3 +167,27 @@ def test_partial_and_invalid_blocks_are_never_shared():
     w.block_tables[:, 1] = w.num_pages + 5    # block 0's second page out of range: not shareable
     idx = oracle.build_index_dedup(prob, w.selected, w.cu_seqlens_q, w.used_kv_lens, w.block_tables)
     assert np.diff(idx["row_ptr"]).tolist() == [1, 1, 1, 1]
+
+
+def test_shared_prefix_page_tables_recipe():
+    """The generator's shared-prefix tables: hot sequence s + 16 points the
+    pages of each block that is full in both at sequence s's pages (the
+    group's first hot sequence), for the first 64 blocks, and nothing else
+    changes (the selections and the other rows are those of the plain
+    recipe)."""
+    lens = [9000, 3000, 700, 20000, 129, 8192] * 4
+    plain = W.custom("r0", [1] * 24, lens, 16, 2, 64, 16, False, "hot_groups", 150)
+    shared = W.custom("r0", [1] * 24, lens, 16, 2, 64, 16, False, "hot_groups", 150,
+                      extra={"shared_prefix_blocks": 64})
+    assert np.array_equal(plain.selected, shared.selected)
+    per = BLOCK // 64
+    for s in range(24):
+        hot = (s // 8) % 2 == 0
+        if not hot or s < 8:  # cold sequences and each group's first hot sequence keep their pages
+            assert np.array_equal(plain.block_tables[s], shared.block_tables[s]), s
+            continue
+        o = s - 16
+        full = min(lens[s], lens[o]) // BLOCK
+        n = min(64, full) * per
+        assert np.array_equal(shared.block_tables[s, :n], shared.block_tables[o, :n])
+        assert np.array_equal(shared.block_tables[s, n:], plain.block_tables[s, n:])
