@@ -307,6 +307,13 @@ __global__ void __launch_bounds__(kDThreads, 1)
           ok = mbar_wait(&c.q_full[gq], n & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (!ok) break;
           if (d.nb == 0) mma_commit(&c.q_empty[gq]);  // q unused: free at once
+          if (d.nb == 0 && n > 0) {
+            // no p v of this tile waits for the previous tile's epilogue, so
+            // wait here: o_full must not complete twice before the group has
+            // read the first completion (its parity wait would miss it)
+            ok = mbar_wait(&c.o_empty[gq], (n - 1) & 1, abort_flag, fl, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (!ok) break;
+          }
           if (gq == 1 && d.nb > 0) {
             // group 1 starts a tile once group 0 has its first P, so the two
             // groups' softmax and MMAs alternate instead of running in step
