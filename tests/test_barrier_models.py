@@ -12,7 +12,9 @@ before the next p v overwrites it, epilogues run in tile order, the FP8
 staging tile is widened before it is refilled).  A timeout on the GPU would
 only show such a race as a flag; the model finds it without one.
 
-Covered: k_fwd's KV-stationary phase (BF16 and FP8 staging) and k_dense.
+Covered: k_fwd's decode phase (a 3-stage K/V ring, an MMA issuer polling
+two cursors, BF16 and FP8 staging), its KV-stationary phase (BF16 and FP8)
+and k_dense.
 The dense model without the wait that an empty tile makes before it
 publishes O reproduces the race that wait removes (o_full completing twice
 ahead of the softmax group's parity wait).
@@ -311,12 +313,164 @@ def run_dense(tiles, seed, fix=True):
 
 
 
+NS = 3  # K/V stages of the decode phase
+
+def run_decode(items, seed, fp8=False):
+    """items: key counts (>= 1) of the CTA's decode items, in order."""
+    rnd = random.Random(seed)
+    B = {}
+    def bar(n, c=1): B[n] = Bar(n, c)
+    for i in range(NS):
+        bar(f"kv_full{i}"); bar(f"kv_empty{i}")
+    for i in range(2):
+        for nm in ("q_full", "q_empty", "s_full", "p_full", "p_empty", "o_full", "o_empty"):
+            bar(f"{nm}{i}")
+    bar("stg_full"); bar("stg_empty")
+    pending = {}
+    def later(src, cb): pending.setdefault(src, []).append(cb)
+    stage = {}     # st -> block (landed / widened)
+    staging = [None]
+    Sbuf = {}      # sb -> ('S'|'read', blk)
+    Pbuf = {}      # sb -> ('P'|'used', blk)
+    Obuf = {}      # ib -> ('acc'|'done'|'read', item)
+    pv_done = [-1]
+    nblk = sum(items)
+    def producer():
+        blk = 0
+        for n_it, nk in enumerate(items):
+            ib, ui = n_it & 1, n_it >> 1
+            yield ("wait", B[f"q_empty{ib}"], (ui & 1) ^ 1)
+            later(f"tq{ib}", lambda ib=ib: B[f"q_full{ib}"].arrive())
+            for j in range(nk):
+                st, us = blk % NS, blk // NS
+                yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
+                assert blk < NS or pv_done[0] >= blk - NS, ("stage refilled before its p v", blk)
+                if fp8:
+                    yield ("wait", B["stg_empty"], (blk & 1) ^ 1)
+                    def sl(blk=blk):
+                        staging[0] = blk
+                        B["stg_full"].arrive()
+                    later("tstg", sl)
+                else:
+                    def land(st=st, blk=blk):
+                        stage[st] = blk
+                        B[f"kv_full{st}"].arrive()
+                    later(f"tkv{st}", land)
+                blk += 1
+    def issuer():
+        its, js, ns_it, bs = 0, 0, 0, 0
+        itp, jp, np_it, bp = 0, 0, 0, 0
+        while itp < len(items):
+            def can_qk():
+                if not (its < len(items) and bs <= bp + 1):
+                    return False
+                ib, st = ns_it & 1, bs % NS
+                return (js > 0 or B[f"q_full{ib}"].ready((ns_it >> 1) & 1)) and B[f"kv_full{st}"].ready((bs // NS) & 1)
+            def can_pv():
+                if not bp < bs:
+                    return False
+                ib, sb = np_it & 1, bp & 1
+                return B[f"p_full{sb}"].ready((bp >> 1) & 1) and (jp > 0 or B[f"o_empty{ib}"].ready(((np_it >> 1) & 1) ^ 1))
+            yield ("pred", lambda: can_qk() or can_pv())
+            if can_qk():
+                st, sb = bs % NS, bs & 1
+                assert stage.get(st) == bs, ("S from the wrong K", stage.get(st), bs)
+                assert Sbuf.get(sb) in (None, ("read", bs - 2)), ("S overwritten before read", Sbuf.get(sb), bs)
+                def qk(sb=sb, b=bs):
+                    Sbuf[sb] = ("S", b)
+                    B[f"s_full{sb}"].arrive()
+                later("mma", qk)
+                bs += 1; js += 1
+                if js == items[its]:
+                    later("mma", lambda ib=ns_it & 1: B[f"q_empty{ib}"].arrive())
+                    js = 0; ns_it += 1; its += 1
+            if can_pv():
+                ib, st, sb = np_it & 1, bp % NS, bp & 1
+                assert Pbuf.get(sb) == ("P", bp), (Pbuf.get(sb), bp)
+                assert stage.get(st) == bp
+                if jp == 0:
+                    assert Obuf.get(ib) in (None, ("read", np_it - 2)), ("O overwritten before read", Obuf.get(ib))
+                    Obuf[ib] = ("acc", np_it)
+                def pv(sb=sb, st=st, b=bp):
+                    Pbuf[sb] = ("used", b)
+                    pv_done[0] = b
+                    B[f"p_empty{sb}"].arrive(); B[f"kv_empty{st}"].arrive()
+                later("mma", pv)
+                bp += 1; jp += 1
+                if jp == items[itp]:
+                    def of(ib=ib, it=np_it):
+                        Obuf[ib] = ("done", it)
+                        B[f"o_full{ib}"].arrive()
+                    later("mma", of)
+                    jp = 0; np_it += 1; itp += 1
+    def softmax():
+        blk = 0
+        for n_it, nk in enumerate(items):
+            ib, ui = n_it & 1, n_it >> 1
+            for j in range(nk):
+                st, us, sb, ub = blk % NS, blk // NS, blk & 1, blk >> 1
+                if fp8:
+                    yield ("wait", B["stg_full"], blk & 1)
+                    assert staging[0] == blk
+                    assert blk < NS or pv_done[0] >= blk - NS, ("widening into a busy stage", blk)
+                    stage[st] = blk
+                    B["stg_empty"].arrive(); B[f"kv_full{st}"].arrive()
+                else:
+                    yield ("wait", B[f"kv_full{st}"], us & 1)
+                yield ("wait", B[f"s_full{sb}"], ub & 1)
+                assert Sbuf.get(sb) == ("S", blk)
+                Sbuf[sb] = ("read", blk)
+                yield ("wait", B[f"p_empty{sb}"], (ub & 1) ^ 1)
+                assert blk < 2 or pv_done[0] >= blk - 2
+                if j > 0 and rnd.random() < 0.3:  # raise m: the previous p v must be done
+                    pb = blk - 1
+                    yield ("wait", B[f"p_empty{pb & 1}"], (pb >> 1) & 1)
+                    assert pv_done[0] >= blk - 1 and Obuf.get(ib) == ("acc", n_it)
+                Pbuf[sb] = ("P", blk)
+                B[f"p_full{sb}"].arrive()
+                blk += 1
+                yield None
+            yield ("wait", B[f"o_full{ib}"], ui & 1)
+            assert Obuf.get(ib) == ("done", n_it)
+            Obuf[ib] = ("read", n_it)
+            B[f"o_empty{ib}"].arrive()
+    agents = {"p": producer(), "m": issuer(), "s": softmax()}
+    state = {k: None for k in agents}; done = set(); steps = 0
+    while len(done) < len(agents) or any(pending.values()):
+        steps += 1; assert steps < 500000
+        prog = False
+        srcs = [s for s in pending if pending[s]]
+        if srcs and rnd.random() < 0.5:
+            pending[rnd.choice(srcs)].pop(0)(); prog = True
+        order = list(agents); rnd.shuffle(order)
+        for k in order:
+            if k in done: continue
+            w = state[k]
+            if w is not None:
+                if w[0] == "pred":
+                    if not w[1](): continue
+                elif not w[1].ready(w[2]): continue
+                state[k] = None
+            try: state[k] = next(agents[k])
+            except StopIteration: done.add(k)
+            prog = True; break
+        if not prog and not any(pending.values()):
+            raise AssertionError(f"deadlock {[(k, state[k][0], getattr(state[k][1], 'name', '')) for k in agents if state[k]]}")
+
 @pytest.mark.parametrize("fp8", [False, True])
 def test_fwd_kv_stationary_protocol(fp8):
     rnd = random.Random(11 + fp8)
     for trial in range(400):
         items = [rnd.randint(1, 4) for _ in range(rnd.randint(0, 7))]
         run_fwd_kv_stationary(items, trial, fp8)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_fwd_decode_protocol(fp8):
+    rnd = random.Random(3 + fp8)
+    for trial in range(400):
+        items = [rnd.randint(1, 8) for _ in range(rnd.randint(1, 7))]
+        run_decode(items, trial, fp8)
 
 
 def test_dense_protocol():
