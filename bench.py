@@ -236,8 +236,62 @@ def cpu_baseline(w, budget_s: float = 12.0):
                       f"on {nthreads} threads; tokens/s = rows / Hq / time"}
 
 
+def run_reference_extra(args, world):
+    """The reference arm of the store and dense workloads: the oracle's store
+    of 512 tokens' K and V, or the oracle on the dense workload's last 4
+    tokens, per step, on the host cores."""
+    import oracle
+    from block_sparse_attention_builder_gb300 import workloads as W
+    if args.workload == "kv_store":
+        m, hkv, ps = 512, STORE_HKV, STORE_PS
+        key = W.stream_key(2000, 0)
+        src = W.generate_values(m * hkv * 128, key, "bf16", "cpu").view(m, hkv, 128)
+        cache = np.zeros((m // ps + 1, hkv, ps, 128), dtype=np.uint8)
+        sl = np.arange(m, dtype=np.int64)
+
+        def step():
+            oracle.store(src, sl, cache, ps, "bf16", "fp8")  # K
+            oracle.store(src, sl, cache, ps, "bf16", "fp8")  # V
+        tokens, cores = m, 1
+        metric, dtype = "kv-store tokens/s and GB/s vs HBM roofline, 1 GB300", "bf16->e4m3"
+        config = {"workload": "kv_store", "tokens": STORE_TOKENS, "num_kv_heads": hkv, "page_size": ps,
+                  "index_dim": STORE_IDX_DIM}
+        sample = f"{m} tokens' K and V ({hkv} heads x 128, bf16 -> e4m3) per step, one thread"
+    else:
+        w = dense_workload(0)
+        tq, hq, ps = w.total_q, w.num_q_heads, w.page_size
+        rows = np.arange((tq - 4) * hq, tq * hq, dtype=np.int64)
+        sel = np.arange(w.max_pages_per_seq * ps // 128, dtype=np.int32)[None, None, :].repeat(tq, 0)
+        oprob = oracle.problem(1, tq, hq, w.num_kv_heads, sel.shape[2], ps, w.num_pages, w.max_pages_per_seq, True)
+        qc, kc, vc = w.q(), w.k_cache(), w.v_cache()
+
+        def step():
+            oracle.attention_rows(oprob, qc, kc, vc, sel, w.block_tables, w.cu_seqlens_q, w.used_kv_lens, rows=rows)
+        tokens, cores = 4, os.cpu_count() or 1
+        metric, dtype = "dense-attn tokens/s and TFLOP/s vs tensor roofline, 1 GB300", "f64"
+        config = {"workload": "dense_prefill", "num_q_heads": hq, "num_kv_heads": w.num_kv_heads, "page_size": ps}
+        sample = f"the last 4 tokens (x {hq} heads, every key) per step"
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    total = time.perf_counter() - t0
+    value = tokens * args.steps / total
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
+        return
+    if args.workload in ("kv_store", "dense_prefill"):
+        run_reference_extra(args, world)
         return
     w = load_workload(args.workload, 0)
     nthreads = os.cpu_count() or 1
@@ -366,23 +420,29 @@ def run_store(args, rank, world, local_rank):
         "gpu_launches": args.steps, "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-        m = 512
-        cache = np.zeros((m // ps + 1, hkv, ps, 128), dtype=np.uint8)
-        src = k[:m].cpu()
-        sl = np.arange(m, dtype=np.int64)
-        t0 = time.time()
-        reps = 0
-        while time.time() - t0 < 10.0:
-            oracle.store(src, sl, cache, ps, "bf16", "fp8")
-            oracle.store(src, sl, cache, ps, "bf16", "fp8")
-            reps += 1
-        dt = time.time() - t0
-        line["cpu_baseline"] = {"value": m * reps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{m} tokens' K and V (8 heads x 128, bf16 -> e4m3), {reps} passes, "
-                                          f"{dt:.1f} s on one thread (the oracle's store is single-threaded)"}
+        line["cpu_baseline"] = store_oracle_baseline(k[:512].cpu(), ps, 10.0)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def store_oracle_baseline(src, ps, budget_s):
+    """The oracle's store (single-threaded) of the K and V rows `src`
+    ([m, Hkv, 128] bf16, CPU) into an e4m3 cache, repeated for about
+    `budget_s` seconds."""
+    import oracle
+    m, hkv = int(src.shape[0]), int(src.shape[1])
+    cache = np.zeros((m // ps + 1, hkv, ps, 128), dtype=np.uint8)
+    sl = np.arange(m, dtype=np.int64)
+    t0 = time.time()
+    reps = 0
+    while time.time() - t0 < budget_s or reps == 0:
+        oracle.store(src, sl, cache, ps, "bf16", "fp8")
+        oracle.store(src, sl, cache, ps, "bf16", "fp8")
+        reps += 1
+    dt = time.time() - t0
+    return {"value": m * reps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{m} tokens' K and V ({hkv} heads x 128, bf16 -> e4m3), {reps} passes, "
+                      f"{dt:.1f} s on one thread (the oracle's store is single-threaded)"}
 
 
 # ------------------------------------------------------------ dense path
@@ -399,7 +459,7 @@ def run_dense(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     tq, L, hq, hkv, ps = 4096, 36864, 16, 1, 128
-    w = W.custom("dense_prefill", [tq], [L], hq, hkv, ps, 1, True, "uniform", 3000 + rank)
+    w = dense_workload(rank)
     q, k, v = w.q(dev), w.k_cache(dev), w.v_cache(dev)
     bt = torch.from_numpy(w.block_tables).to(dev)
     cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
@@ -473,23 +533,37 @@ def run_dense(args, rank, world, local_rank):
         "gpu_launches": args.steps, "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-        rows = np.arange((tq - 4) * hq, tq * hq, dtype=np.int64)  # the last 4 tokens' rows: the longest
-        t0 = time.time()
-        reps = 0
-        sel = np.arange(w.max_pages_per_seq * ps // 128, dtype=np.int32)[None, None, :].repeat(tq, 0)
-        oprob = oracle.problem(1, tq, hq, hkv, sel.shape[2], ps, w.num_pages, w.max_pages_per_seq, True)
-        qc, kc, vc = w.q(), w.k_cache(), w.v_cache()
-        while time.time() - t0 < 10.0:
-            oracle.attention_rows(oprob, qc, kc, vc, sel, w.block_tables, w.cu_seqlens_q, w.used_kv_lens, rows=rows)
-            reps += 1
-        dt = time.time() - t0
-        line["cpu_baseline"] = {"value": 4 * reps / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1,
-                                "kind": "oracle",
-                                "sample": f"the last 4 tokens (x {hq} heads, ~{L} keys each), {reps} passes, "
-                                          f"{dt:.1f} s; tokens/s = tokens / time"}
+        line["cpu_baseline"] = dense_oracle_baseline(w, 10.0)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def dense_workload(rank):
+    """The dense path's workload: 1 sequence, 4096 new tokens on L = 36864,
+    Hq 16 / Hkv 1, page 128, causal, every block."""
+    from block_sparse_attention_builder_gb300 import workloads as W
+    return W.custom("dense_prefill", [4096], [36864], 16, 1, 128, 1, True, "uniform", 3000 + rank)
+
+
+def dense_oracle_baseline(w, budget_s):
+    """The oracle on the dense workload's last 4 tokens (the longest rows,
+    every key), repeated for about `budget_s` seconds."""
+    import oracle
+    tq, hq, hkv, ps = w.total_q, w.num_q_heads, w.num_kv_heads, w.page_size
+    L = int(w.used_kv_lens[0])
+    rows = np.arange((tq - 4) * hq, tq * hq, dtype=np.int64)
+    sel = np.arange(w.max_pages_per_seq * ps // 128, dtype=np.int32)[None, None, :].repeat(tq, 0)
+    oprob = oracle.problem(1, tq, hq, hkv, sel.shape[2], ps, w.num_pages, w.max_pages_per_seq, True)
+    qc, kc, vc = w.q(), w.k_cache(), w.v_cache()
+    t0 = time.time()
+    reps = 0
+    while time.time() - t0 < budget_s or reps == 0:
+        oracle.attention_rows(oprob, qc, kc, vc, sel, w.block_tables, w.cu_seqlens_q, w.used_kv_lens, rows=rows)
+        reps += 1
+    dt = time.time() - t0
+    return {"value": 4 * reps / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"the last 4 tokens (x {hq} heads, ~{L} keys each), {reps} passes, "
+                      f"{dt:.1f} s; tokens/s = tokens / time"}
 
 
 def main():

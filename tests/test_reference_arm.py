@@ -7,6 +7,8 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ARGS = ["--impl", "reference", "--workload", "tiny_decode", "--steps", "1", "--warmup", "3"]
 
@@ -44,3 +46,15 @@ def test_reference_arm_under_torchrun_prints_once():
     lines = _lines(r.stdout)
     assert len(lines) == 1
     _check(lines[0], 2)
+
+
+@pytest.mark.parametrize("workload", ["kv_store", "dense_prefill"])
+def test_reference_arm_store_and_dense(workload):
+    args = ["--impl", "reference", "--workload", workload, "--steps", "1", "--warmup", "3"]
+    r = subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _lines(r.stdout)
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["config"]["workload"] == workload and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
