@@ -4,6 +4,7 @@ cpu_baseline and an end-to-end entry, printed by rank 0 alone under
 torchrun (the other rank exits 0 without work)."""
 import json
 import os
+import socket
 import subprocess
 import sys
 
@@ -38,9 +39,15 @@ def test_reference_arm_single_process():
     _check(lines[0], 1)
 
 
+def _free_port():
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
 def test_reference_arm_under_torchrun_prints_once():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
-           "127.0.0.1", "--master-port", "29613", "bench.py", "--gpus", "2", *ARGS]
+           "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--gpus", "2", *ARGS]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _lines(r.stdout)
