@@ -83,6 +83,8 @@ def _load():
         _lib.oracle_build_index.argtypes = [P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
         _lib.oracle_build_index_dedup.restype = ctypes.c_int
         _lib.oracle_build_index_dedup.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, P, P, P, P]
+        _lib.oracle_block_owners.restype = ctypes.c_int64
+        _lib.oracle_block_owners.argtypes = [P, P, P, P, ctypes.c_int64]
         _lib.oracle_encode_e4m3.restype = ctypes.c_uint32
         _lib.oracle_encode_e4m3.argtypes = [ctypes.c_double]
         _lib.oracle_store.restype = ctypes.c_int64
@@ -238,6 +240,21 @@ def build_index_dedup(prob: OracleProblem, selected, cu_seqlens_q, used_kv_lens,
     nkeys = prob.num_kv_heads * nb.value
     return dict(nb=nb.value, row_ptr=row_ptr[:nkeys + 1].copy(), entries=entries[:nnz.value].copy(),
                 slot_entry=slot_entry[:nslots].copy(), flags=flags.value)
+
+
+def block_owners(prob: OracleProblem, used_kv_lens, block_tables) -> np.ndarray:
+    """Owner sequence of every block (cross-sequence dedup), in key order:
+    sequence s's blocks at blk_off[s] .. blk_off[s] + ceil(L_s / 128)."""
+    lib = _load()
+    lens = _c(used_kv_lens, np.int32)
+    bt = _c(block_tables, np.int32)
+    cap_len = prob.max_pages_per_seq * prob.page_size
+    nb_cap = int(sum((min(max(int(L), 0), cap_len) + 127) // 128 for L in lens))
+    out = np.zeros(max(nb_cap, 1), dtype=np.int32)
+    nb = lib.oracle_block_owners(ctypes.byref(prob), _ptr(lens), _ptr(bt), _ptr(out), ctypes.c_int64(len(out)))
+    if nb < 0:
+        raise RuntimeError("oracle_block_owners failed")
+    return out[:nb].copy()
 
 
 def schedule(prob: OracleProblem, used_kv_lens, cu_seqlens_q, index: dict, rows_per_item_tiles: int,

@@ -420,6 +420,43 @@ static int cmp_phys_block(const void* a, const void* b) {
   return 0;
 }
 
+/* owner of every (s, b) at owner[blk_off[s] + b]: the shareable blocks
+ * sorted by (b, pages, s); the first of each run of equal (b, pages) owns
+ * the run; a block that is not shareable owns itself.  Returns 0 or -1. */
+static int fill_owners(const oracle_problem* p, int32_t B, const int64_t* Lc, const int64_t* nblk,
+                       const int64_t* blk_off, int64_t NB, const int32_t* block_tables, int32_t* owner) {
+  const int32_t ps = p->page_size;
+  phys_block* pb = (phys_block*)malloc(sizeof(phys_block) * (size_t)(NB > 0 ? NB : 1));
+  if (!pb) return -1;
+  int64_t npb = 0;
+  for (int32_t s = 0; s < B; ++s) {
+    for (int64_t b = 0; b < nblk[s]; ++b) {
+      owner[blk_off[s] + b] = s;
+      if (128 * b + 128 > Lc[s] && !MUT(13)) continue; /* partial block: never shared (mutant 13: shared) */
+      const int32_t* bt = block_tables + (int64_t)s * p->max_pages_per_seq;
+      int64_t pg0 = ps == 128 ? bt[b] : bt[2 * b];
+      int64_t pg1 = ps == 128 ? -1 : bt[2 * b + 1];
+      if (pg0 < 0 || pg0 >= p->num_pages) continue;
+      if (ps != 128 && (pg1 < 0 || pg1 >= p->num_pages)) continue;
+      pb[npb].b = b;
+      pb[npb].page0 = pg0;
+      pb[npb].page1 = pg1;
+      pb[npb].s = s;
+      ++npb;
+    }
+  }
+  qsort(pb, (size_t)npb, sizeof(phys_block), cmp_phys_block);
+  for (int64_t i = 0; i < npb; ++i) {
+    int64_t first = i;
+    while (first > 0 && pb[first - 1].b == pb[i].b && pb[first - 1].page0 == pb[i].page0 &&
+           pb[first - 1].page1 == pb[i].page1)
+      --first;
+    owner[blk_off[pb[i].s] + pb[i].b] = MUT(14) ? pb[i].s : pb[first].s; /* mutant 14: nothing merged */
+  }
+  free(pb);
+  return 0;
+}
+
 int oracle_build_index_dedup(const oracle_problem* p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
                              const int32_t* block_tables, int32_t* nb_out, int32_t* row_ptr, int64_t row_ptr_cap,
                              int32_t* entries, int32_t* slot_entry, int32_t* nnz_out, int32_t* flags_out) {
@@ -451,38 +488,10 @@ int oracle_build_index_dedup(const oracle_problem* p, const int32_t* sel, const 
     NB += nblk[s];
   }
   const int64_t nkeys = (int64_t)Hkv * NB;
-  /* owner of every (s, b): shareable blocks sorted by (b, pages, s); the
-   * first of each run of equal (b, pages) owns the run */
   int32_t* owner = (int32_t*)malloc(sizeof(int32_t) * (size_t)(NB > 0 ? NB : 1));
-  phys_block* pb = (phys_block*)malloc(sizeof(phys_block) * (size_t)(NB > 0 ? NB : 1));
-  if (nkeys + 1 > row_ptr_cap || !owner || !pb) {
-    free(nblk); free(blk_off); free(Lc); free(ks); free(owner); free(pb);
+  if (nkeys + 1 > row_ptr_cap || !owner || fill_owners(p, B, Lc, nblk, blk_off, NB, block_tables, owner) != 0) {
+    free(nblk); free(blk_off); free(Lc); free(ks); free(owner);
     return -1;
-  }
-  int64_t npb = 0;
-  for (int32_t s = 0; s < B; ++s) {
-    for (int64_t b = 0; b < nblk[s]; ++b) {
-      owner[blk_off[s] + b] = s;
-      if (128 * b + 128 > Lc[s] && !MUT(13)) continue; /* partial block: never shared (mutant 13: shared) */
-      const int32_t* bt = block_tables + (int64_t)s * p->max_pages_per_seq;
-      int64_t pg0 = ps == 128 ? bt[b] : bt[2 * b];
-      int64_t pg1 = ps == 128 ? -1 : bt[2 * b + 1];
-      if (pg0 < 0 || pg0 >= p->num_pages) continue;
-      if (ps != 128 && (pg1 < 0 || pg1 >= p->num_pages)) continue;
-      pb[npb].b = b;
-      pb[npb].page0 = pg0;
-      pb[npb].page1 = pg1;
-      pb[npb].s = s;
-      ++npb;
-    }
-  }
-  qsort(pb, (size_t)npb, sizeof(phys_block), cmp_phys_block);
-  for (int64_t i = 0; i < npb; ++i) {
-    int64_t first = i;
-    while (first > 0 && pb[first - 1].b == pb[i].b && pb[first - 1].page0 == pb[i].page0 &&
-           pb[first - 1].page1 == pb[i].page1)
-      --first;
-    owner[blk_off[pb[i].s] + pb[i].b] = MUT(14) ? pb[i].s : pb[first].s; /* mutant 14: nothing merged */
   }
   int64_t n = 0;
   for (int64_t slot = 0; slot < nslots; ++slot) slot_entry[slot] = -1;
@@ -526,8 +535,36 @@ int oracle_build_index_dedup(const oracle_problem* p, const int32_t* sel, const 
   *nb_out = (int32_t)NB;
   *nnz_out = (int32_t)n;
   *flags_out = flags;
-  free(nblk); free(blk_off); free(Lc); free(ks); free(owner); free(pb);
+  free(nblk); free(blk_off); free(Lc); free(ks); free(owner);
   return 0;
+}
+
+/* The owner of every block, in key order (sequence s's blocks at
+ * blk_off[s] ..): owner_out[NB], NB = sum ceil(L_s / 128) with L_s clamped
+ * as above (capacity owner_cap).  Returns NB, or -1 (capacity / memory). */
+int64_t oracle_block_owners(const oracle_problem* p, const int32_t* lens, const int32_t* block_tables,
+                            int32_t* owner_out, int64_t owner_cap) {
+  const int32_t B = p->num_seqs;
+  const int64_t cap_len = (int64_t)p->max_pages_per_seq * p->page_size;
+  int64_t* nblk = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t* blk_off = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t* Lc = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  if (!nblk || !blk_off || !Lc) {
+    free(nblk); free(blk_off); free(Lc);
+    return -1;
+  }
+  int64_t NB = 0;
+  for (int32_t s = 0; s < B; ++s) {
+    int64_t L = lens[s] < 0 ? 0 : (lens[s] > cap_len ? cap_len : lens[s]);
+    Lc[s] = L;
+    nblk[s] = (L + 127) / 128;
+    blk_off[s] = NB;
+    NB += nblk[s];
+  }
+  int64_t rc = NB;
+  if (NB > owner_cap || fill_owners(p, B, Lc, nblk, blk_off, NB, block_tables, owner_out) != 0) rc = -1;
+  free(nblk); free(blk_off); free(Lc);
+  return rc;
 }
 
 /* --------------------------------------------------------------- schedule

@@ -191,3 +191,29 @@ def test_shared_prefix_page_tables_recipe():
         n = min(64, full) * per
         assert np.array_equal(shared.block_tables[s, :n], shared.block_tables[o, :n])
         assert np.array_equal(shared.block_tables[s, n:], plain.block_tables[s, n:])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_block_owners_equal_brute_force(name):
+    """The owner map on its own (the table the dedup index is keyed by)."""
+    w = CASES[name]
+    ps, per = w.page_size, BLOCK // w.page_size
+    lens = [int(x) for x in w.used_kv_lens]
+    nblk = [(L + BLOCK - 1) // BLOCK for L in lens]
+
+    def pages(s, b):
+        return tuple(int(w.block_tables[s, b * per + j]) for j in range(per))
+
+    def shareable(s, b):
+        return BLOCK * b + BLOCK <= lens[s] and all(0 <= pg < w.num_pages for pg in pages(s, b))
+
+    want = []
+    for s in range(w.num_seqs):
+        for b in range(nblk[s]):
+            o = s
+            if shareable(s, b):
+                o = next(s2 for s2 in range(s + 1) if b < nblk[s2] and shareable(s2, b) and pages(s2, b) == pages(s, b))
+            want.append(o)
+    got = oracle.block_owners(oracle.problem_for(w), w.used_kv_lens, w.block_tables)
+    assert got.tolist() == want
+    assert any(o != s for o, s in zip(got, np.repeat(np.arange(w.num_seqs), nblk)))  # something is shared
