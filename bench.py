@@ -1,20 +1,26 @@
 """Benchmark of block-sparse KV-outer attention on GB300.
 
 One step = the whole hot path (index builder and scheduler in one launch,
-KV-outer forward, combine) over one batch of the synthetic workload, inputs
-resident in HBM.
-Prints ONE JSON line (rank 0).
+KV-outer forward, combine) over one batch of a synthetic workload, inputs
+resident in HBM.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+With no --workload (or --workload all) the line carries all five sparse
+workloads: each is measured in turn (its own warm-up, timed steps, end-to-end
+steps and oracle baseline) and listed under "workloads"; the line's own
+value, roofline, e2e and cpu_baseline are those of skewed_decode, the largest
+workload that fits one GPU.  kv_store and dense_prefill are separate runs.
 
 Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
 on the launching stream with an L2 flush (a 256 MiB write) between steps
 outside the events; device time summed over the K steps; max over ranks.
 Per-kernel durations come from events recorded between the calls (plan =
-index + schedule in one launch, forward, combine) on the same stream.  Multi-GPU (torchrun): every rank runs its own batch of the
-same workload recipe (independent sequences, no collective on the data
-path); value = tokens of all ranks / max-over-ranks time ("weak" scaling).
+index + schedule in one launch, forward, combine) on the same stream.
+Multi-GPU (torchrun): every rank runs its own batch of the same workload
+recipe (independent sequences, no collective on the data path); value =
+tokens of all ranks / max-over-ranks time ("weak" scaling).
 """
 from __future__ import annotations
 
@@ -38,7 +44,10 @@ sys.path.insert(0, ROOT)
 METRIC = "sparse-attn tokens/s, TFLOP/s and unique-KV GB/s vs roofline, 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 3  # k_plan (index + schedule) | k_fwd (decode and KV-stationary items) | k_combine
-DEFAULT_WORKLOAD = "gqa_decode"
+DEFAULT_WORKLOAD = "all"
+# the five sparse workloads, in order; the headline is the largest one that fits one GPU
+SPARSE_WORKLOADS = ("tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode")
+HEADLINE_WORKLOAD = "skewed_decode"
 
 
 def log(*a):
@@ -171,7 +180,11 @@ def algorithmic(w, stats):
     flops = 4 * 128 * stats["visit_keys"] * (w.num_q_heads // w.num_kv_heads)
     io_bytes = (w.total_q * w.num_q_heads * 128 * 2 * 2 + w.total_q * w.num_q_heads * 4 + w.selected.nbytes
                 + w.block_tables.nbytes + w.cu_seqlens_q.nbytes + w.used_kv_lens.nbytes)
-    partial_bytes = stats["block_visits"] * (w.num_q_heads // w.num_kv_heads) * (128 + 1) * 4 * 2
+    # one partial row per (row, block visit): 128 values (FP32 with FP8
+    # caches, else the 16-bit q dtype) and an FP32 lse, written by the
+    # forward and read back by the combine
+    ps = 4 if w.spec.kv_dtype == "fp8" else 2
+    partial_bytes = stats["block_visits"] * (w.num_q_heads // w.num_kv_heads) * (128 * ps + 4) * 2
     return unique_kv_bytes, flops, io_bytes, partial_bytes
 
 
@@ -566,48 +579,17 @@ def dense_oracle_baseline(w, budget_s):
                       f"{dt:.1f} s; tokens/s = tokens / time"}
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if args.impl == "mine" else "gloo")
-
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-
-    if args.workload in ("kv_store", "dense_prefill"):
-        (run_store if args.workload == "kv_store" else run_dense)(args, rank, world, local_rank)
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return
-
+def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
+    """One sparse workload: W warm-up steps, K timed steps (device time per
+    kernel from events on the launching stream, L2 flushed between steps),
+    then the same steps end to end through the public API with host buffers.
+    Returns the workload's JSON entry (rank 0) or None."""
     import block_sparse_attention_builder_gb300 as mx
-    from block_sparse_attention_builder_gb300 import build as B
-    B.build()
-    torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-
-    w = load_workload(args.workload, rank)
+    w = load_workload(name, rank)
     stats = _stats(w)
     unique_kv_bytes, flops, io_bytes, partial_bytes = algorithmic(w, stats)
-    log(f"[bench] {args.workload}: {stats}")
+    log(f"[bench] {name}: {stats}")
 
     # inputs resident in HBM
     q, k, v = w.q(dev), w.k_cache(dev), w.v_cache(dev)
@@ -641,7 +623,7 @@ def main():
     torch.cuda.synchronize()
     flags = mx.read_status(attn.ws.index, stream)
     if flags:
-        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+        raise RuntimeError(f"{name}: device status flags {flags:#x} after warm-up")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
@@ -729,46 +711,106 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e_value = whole_job_value(tokens_per_step, world, args.steps, e2e_ms)
     assert torch.equal(h_out.to(dev), out)
+    del q, k, v, attn, flush, d_q, d_small
+    torch.cuda.empty_cache()
+    if rank != 0:
+        return None
 
+    kv_gbs = unique_kv_bytes / (ms_per_step / 1e3) / 1e9
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    fwd_gbs = unique_kv_bytes / (fwd_ms / 1e3) / 1e9
+    fwd_tflops = flops / (fwd_ms / 1e3) / 1e12
+    bound = "hbm" if "decode" in w.spec.name else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": fwd_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": fwd_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(name),
+                "kernel": "k_fwd (its decode phase; no KV-stationary items here)",
+                "algorithmic_bytes_per_launch": unique_kv_bytes, "peak_source": peaks["src"] + " copy bandwidth"}
+    else:
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": pk, "unit": "TFLOP/s",
+                "frac": fwd_tflops / pk, "traffic": recorded_traffic(name), "kernel": "k_fwd",
+                "algorithmic_flops_per_launch": flops, "peak_source": peaks["src"] + " bf16 burst"}
+    step_roof = {"hbm_frac": kv_gbs / peaks["hbm_gbs"], "tensor_frac": tflops / peaks["bf16_tflops"]}
+    entry = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.spec.kv_dtype if w.spec.kv_dtype != "fp8" else "fp8-e4m3 kv, bf16 q",
+        "data": "synthetic (seeded counter-based N(0,1) values; selections per the workload recipe)",
+        "config": workload_config(w, stats, name),
+        "tflops": tflops, "unique_kv_gbs": kv_gbs, "step_roofline": step_roof,
+        "kernel_ms": {"plan (index + schedule)": float(per[:, 0].mean()), "fwd": fwd_ms,
+                      "combine": float(per[:, 2].mean())},
+        "fwd_unique_kv_gbs": fwd_gbs, "fwd_tflops": fwd_tflops,
+        "bytes": {"unique_kv": unique_kv_bytes, "io": io_bytes, "partials_overhead": partial_bytes},
+        "flops": flops,
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps,
+                "note": "every step: selections, cu_seqlens_q, used_kv_lens copied H2D in one copy from "
+                        "one pinned staging buffer, then the plan while q and block tables copy on a second "
+                        "stream; the combine writes out + lse into pinned host memory directly (counted as "
+                        "D2H bytes); the KV cache is resident model state"},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        entry["cpu_baseline"] = cpu_baseline(w, cpu_budget_s)
+    return entry
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="'all' (default): the five sparse workloads in one line, headline skewed_decode; "
+                         "or one of " + ", ".join(list(SPARSE_WORKLOADS) + ["kv_store", "dense_prefill"]))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "mine" else "gloo")
+
+    if args.impl == "reference":
+        if args.workload == "all":
+            args.workload = HEADLINE_WORKLOAD
+        run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    if args.workload in ("kv_store", "dense_prefill"):
+        (run_store if args.workload == "kv_store" else run_dense)(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    from block_sparse_attention_builder_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(local_rank)
+    if args.workload == "all":
+        names, headline = list(SPARSE_WORKLOADS), HEADLINE_WORKLOAD
+    else:
+        names, headline = [args.workload], args.workload
+    entries = {}
+    for name in names:
+        entries[name] = run_sparse(name, args, rank, world, local_rank, 12.0 if name == headline else 6.0)
     if rank == 0:
-        kv_gbs = unique_kv_bytes / (ms_per_step / 1e3) / 1e9
-        tflops = flops / (ms_per_step / 1e3) / 1e12
-        fwd_gbs = unique_kv_bytes / (fwd_ms / 1e3) / 1e9
-        fwd_tflops = flops / (fwd_ms / 1e3) / 1e12
-        bound = "hbm" if "decode" in w.spec.name else "tensor"
-        if bound == "hbm":
-            roof = {"bound": "hbm", "achieved": fwd_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": fwd_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(args.workload),
-                    "kernel": "k_fwd (its decode phase; no KV-stationary items here)",
-                    "algorithmic_bytes_per_launch": unique_kv_bytes, "peak_source": peaks["src"]}
-        else:
-            pk = peaks["bf16_tflops"]
-            roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": pk, "unit": "TFLOP/s",
-                    "frac": fwd_tflops / pk, "traffic": recorded_traffic(args.workload), "kernel": "k_fwd",
-                    "algorithmic_flops_per_launch": flops, "peak_source": peaks["src"] + " bf16 burst"}
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.spec.kv_dtype if w.spec.kv_dtype != "fp8" else "fp8-e4m3 kv, bf16 q",
-            "data": "synthetic (seeded counter-based N(0,1) values; selections per the workload recipe)",
-            "config": workload_config(w, stats, args.workload),
-            "tflops": tflops, "unique_kv_gbs": kv_gbs,
-            "kernel_ms": {"plan (index + schedule)": float(per[:, 0].mean()), "fwd": fwd_ms,
-                          "combine": float(per[:, 2].mean())},
-            "fwd_unique_kv_gbs": fwd_gbs, "fwd_tflops": fwd_tflops,
-            "bytes": {"unique_kv": unique_kv_bytes, "io": io_bytes, "partials_overhead": partial_bytes},
-            "roofline": roof,
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms / args.steps,
-                    "note": "every step: selections, cu_seqlens_q, used_kv_lens copied H2D in one copy from "
-                            "one pinned staging buffer, then the plan while q and block tables copy on a second "
-                            "stream; the combine writes out + lse into pinned host memory directly (counted as "
-                            "D2H bytes); the KV cache is resident model state"},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
-            "clocks": clk,
-        }
-        if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w)
+        line = dict(entries[headline])
+        if len(names) > 1:
+            line["headline"] = (f"{headline}: the largest single-GPU workload; every workload's own numbers "
+                                f"(value, roofline, e2e, cpu_baseline, clocks) are under 'workloads'")
+            line["workloads"] = entries
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -114,11 +114,15 @@ mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L) {
   return MXSA_OK;
 }
 
+// Partial outputs: one 128-value row per (entry, head), the normalised
+// o = O / l of one block or decode run (its values lie within the range of
+// the V rows it averages), in FP32 or in the 16-bit q dtype
+// (partials_fp32), then one FP32 lse per row.
 static void partial_layout(const mxsa_problem& p, size_t* o_off, size_t* lse_off, size_t* total) {
   const int64_t nslots = (int64_t)p.total_q * p.num_kv_heads * p.topk;
   const int64_t G = p.num_q_heads / p.num_kv_heads;
   *o_off = 0;
-  *lse_off = align_up((size_t)nslots * G * 128 * 4);
+  *lse_off = align_up((size_t)nslots * G * 128 * (partials_fp32(p) ? 4 : 2));
   *total = align_up(*lse_off + (size_t)nslots * G * 4);
   if (*total == 0) *total = kAlign;
 }
@@ -302,7 +306,7 @@ mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const v
   uint8_t* pb = static_cast<uint8_t*>(partial_ws);
   int detail = 0;
   cudaError_t e = launch_fwd(*problem, q, k_cache, v_cache, block_tables, ix, sc, ctas,
-                             reinterpret_cast<float*>(pb + po), reinterpret_cast<float*>(pb + pl),
+                             pb + po, reinterpret_cast<float*>(pb + pl),
                              static_cast<cudaStream_t>(stream), &detail);
   if (e != cudaSuccess) return detail ? MXSA_ERR_INVALID_ARG : MXSA_ERR_CUDA;
   return MXSA_OK;
@@ -339,7 +343,7 @@ mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size
   if (index_bytes < il.total || partial_bytes < pt) return MXSA_ERR_WORKSPACE;
   IndexPtrs ix = index_ptrs(*problem, const_cast<void*>(index_ws));
   const uint8_t* pb = static_cast<const uint8_t*>(partial_ws);
-  cudaError_t e = launch_combine(*problem, ix, reinterpret_cast<const float*>(pb + po),
+  cudaError_t e = launch_combine(*problem, ix, pb + po,
                                  reinterpret_cast<const float*>(pb + pl), out, lse,
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;

@@ -6,10 +6,12 @@
 //   out = sum_k w_k o_k / sum_k w_k   (rounded to nearest-even, q dtype),
 //   lse = M + log(sum_k w_k);  no partial: out = 0, lse = -inf.
 //
-// One warp per row; lane j owns columns 4j..4j+3 (one float4 of every
-// 512-byte partial row, so each partial is read as one coalesced 512-byte
-// transaction, up to 8 of them in flight per warp).  The row's slot -> entry
-// map and lses are read once per 32 slots with one load per lane.
+// Partial rows hold 128 FP32 values, or 128 values of the 16-bit q dtype
+// (widened exactly to FP32 here), and an FP32 lse.  One warp per row; lane
+// j owns columns 4j..4j+3 (16 or 8 bytes of every partial row, so each
+// partial is read as one coalesced transaction of the whole row, up to 8 of
+// them in flight per warp).  The row's slot -> entry map and lses are read
+// once per 32 slots with one load per lane.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -23,9 +25,37 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 constexpr int kBatch = 8;  // partial rows read ahead per warp
 
+// four 16-bit values (bf16 or fp16, low half first) -> FP32, exactly
+__device__ __forceinline__ float4 widen4(uint2 raw, int bf16) {
+  if (bf16)
+    return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// one lane's four columns of a partial row
+template <typename P>
+struct PartialCols;
+template <>
+struct PartialCols<float> {
+  using raw_t = float4;
+  static __device__ __forceinline__ raw_t zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  static __device__ __forceinline__ float4 widen(raw_t v, int) { return v; }
+};
+template <>
+struct PartialCols<uint16_t> {
+  using raw_t = uint2;
+  static __device__ __forceinline__ raw_t zero() { return make_uint2(0u, 0u); }
+  static __device__ __forceinline__ float4 widen(raw_t v, int bf16) { return widen4(v, bf16); }
+};
+
+template <typename P>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
-    k_combine(const int32_t* slot_entry, const float* part_o, const float* part_lse, uint8_t* out, float* lse_out,
+    k_combine(const int32_t* slot_entry, const P* part_o, const float* part_lse, uint8_t* out, float* lse_out,
               int total_q, int Hq, int Hkv, int topk, int out_bf16) {
+  using PC = PartialCols<P>;
   const int lane = threadIdx.x & 31;
   const int G = Hq / Hkv;
   const long long n_rows = (long long)total_q * Hq;
@@ -67,28 +97,29 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
         unsigned live = __ballot_sync(0xffffffffu, w > 0.f);
         while (live) {
           // up to kBatch partial rows are requested before any is used, so
-          // that each warp keeps several 512-byte reads in flight; they are
+          // that each warp keeps several whole-row reads in flight; they are
           // accumulated in slot order (absent ones add exact zeros)
-          float4 v[kBatch];
+          typename PC::raw_t v[kBatch];
           float ws[kBatch];
 #pragma unroll
           for (int u = 0; u < kBatch; ++u) {
             ws[u] = 0.f;
-            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = PC::zero();
             if (live) {  // warp-uniform
               const int src = __ffs(live) - 1;
               live &= live - 1;
               const int es = __shfl_sync(0xffffffffu, e, src);
               ws[u] = __shfl_sync(0xffffffffu, w, src);
-              v[u] = __ldcs(reinterpret_cast<const float4*>(part_o + ((long long)es * G + j) * 128) + lane);
+              v[u] = __ldcs(reinterpret_cast<const typename PC::raw_t*>(part_o + ((long long)es * G + j) * 128) + lane);
             }
           }
 #pragma unroll
           for (int u = 0; u < kBatch; ++u) {
-            acc.x = fmaf(ws[u], v[u].x, acc.x);
-            acc.y = fmaf(ws[u], v[u].y, acc.y);
-            acc.z = fmaf(ws[u], v[u].z, acc.z);
-            acc.w = fmaf(ws[u], v[u].w, acc.w);
+            const float4 f = PC::widen(v[u], out_bf16);
+            acc.x = fmaf(ws[u], f.x, acc.x);
+            acc.y = fmaf(ws[u], f.y, acc.y);
+            acc.z = fmaf(ws[u], f.z, acc.z);
+            acc.w = fmaf(ws[u], f.w, acc.w);
             W += ws[u];
           }
         }
@@ -113,7 +144,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 4)
 
 }  // namespace
 
-cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
+cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const void* part_o,
                            const float* part_lse, void* out, float* lse, cudaStream_t st) {
   const long long rows = (long long)p.total_q * p.num_q_heads;
   if (rows == 0) return cudaSuccess;
@@ -122,9 +153,14 @@ cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const flo
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
-  return launch_pdl(k_combine, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, st,
-                    (const int32_t*)ix.slot_entry, part_o, part_lse, static_cast<uint8_t*>(out), lse, p.total_q,
-                    p.num_q_heads, p.num_kv_heads, p.topk, p.q_dtype == MXSA_BF16 ? 1 : 0);
+  const int out_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
+  if (partials_fp32(p))
+    return launch_pdl(k_combine<float>, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, st,
+                      (const int32_t*)ix.slot_entry, static_cast<const float*>(part_o), part_lse,
+                      static_cast<uint8_t*>(out), lse, p.total_q, p.num_q_heads, p.num_kv_heads, p.topk, out_bf16);
+  return launch_pdl(k_combine<uint16_t>, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, st,
+                    (const int32_t*)ix.slot_entry, static_cast<const uint16_t*>(part_o), part_lse,
+                    static_cast<uint8_t*>(out), lse, p.total_q, p.num_q_heads, p.num_kv_heads, p.topk, out_bf16);
 }
 
 }  // namespace mxsa

@@ -79,10 +79,11 @@ struct FwdArgs {
   const int32_t* cta_ptr;
   const int32_t* idx_hdr;
   const int32_t* sch_hdr;
-  float* part_o;
+  void* part_o;  // partial rows: FP32 when part32, else the 16-bit q dtype
   float* part_lse;
   int32_t* flags;
   int32_t num_seqs, Hq, Hkv, G, topk, page_size, max_pages, num_pages, causal, kv_fp8, ab_bf16, per_tile;
+  int32_t part32;
   int32_t q_tma;      // q rows of a tile come by TMA (G % 8 == 0; the map tmqs exists)
   int32_t* claim;     // schedule header word: next item to claim
   int32_t* sch_hdr_mut;  // the schedule header (claim and exit counters)
@@ -194,7 +195,9 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
 }
 
 // Runs the CTA's KV-stationary items (all kThreads threads; 1024-aligned
-// shared memory `sm`; TMEM base `tmem` with 512 columns).
+// shared memory `sm`; TMEM base `tmem` with 512 columns).  kPart32: FP32
+// partial rows, else the 16-bit q dtype.
+template <bool kPart32>
 __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                                    const CUtensorMap& tmqs, const FwdArgs& a, uint8_t* sm,
                                                    uint32_t tmem) {
@@ -413,9 +416,14 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     int jq = -1;  // the group's last tile whose q rows were requested by TMA
     // epilogue of this group's previous tile: o = O / l, lse = (m2 + log2 l)
     // ln 2.  O is read in the 16x256b shape, in which four consecutive lanes
-    // hold 8 consecutive columns of one row, so every store instruction
-    // writes eight whole 32-byte sectors (8 rows x 32 B) straight from
-    // registers; it runs while the next tile's q k^T is in flight.
+    // hold 8 consecutive columns of one row (two per lane).  FP32 partials:
+    // each lane stores its two values, so each store instruction writes
+    // eight whole 32-byte sectors (8 rows x 8 columns).  16-bit partials:
+    // after packing, one exchange between lane pairs leaves each lane 4
+    // consecutive values of one of two adjacent 8-column chunks, so each
+    // store instruction again writes eight whole sectors (8 rows x 16
+    // columns).  Both straight from registers; the epilogue runs while the
+    // next tile's q k^T is in flight.
     // The groups take turns at the epilogue, in tile order (tile j's after
     // tile j - 1's), so that one group's stores run while the other group
     // computes instead of both groups storing at once at half the rate.
@@ -429,13 +437,13 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           return false;
       }
       const float inv_l = pend.l > 0.f ? 1.f / pend.l : 0.f;
-      if (wrow0 < pend.rows) {  // a warp of padding rows has nothing to store
+      if (kPart32 && wrow0 < pend.rows) {  // a warp of padding rows has nothing to store
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int ra = hh * 16 + (wl >> 2), rb = ra + 8;  // the warp's rows this lane stores
           const float sa = __shfl_sync(0xffffffffu, inv_l, ra), sb = __shfl_sync(0xffffffffu, inv_l, rb);
           const bool oka = wrow0 + ra < pend.rows, okb = wrow0 + rb < pend.rows;
-          float* ga = a.part_o + (pend.orow0 + wrow0 + ra) * 128 + 2 * (wl & 3);
+          float* ga = static_cast<float*>(a.part_o) + (pend.orow0 + wrow0 + ra) * 128 + 2 * (wl & 3);
           float* gb = ga + 8 * 128;
           float v0[32], v1[32];
           tmem_ld16x256b_x8(tO + ((uint32_t)(hh * 16) << 16), v0);
@@ -450,6 +458,41 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           for (int c = 0; c < 8; ++c) {
             if (oka) st_global_cs_v2f(ga + 64 + 8 * c, v1[4 * c] * sa, v1[4 * c + 1] * sa);
             if (okb) st_global_cs_v2f(gb + 64 + 8 * c, v1[4 * c + 2] * sb, v1[4 * c + 3] * sb);
+          }
+        }
+      } else if (!kPart32 && wrow0 < pend.rows) {
+        const int qd = wl & 3, odd = wl & 1;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ra = hh * 16 + (wl >> 2), rb = ra + 8;  // the warp's rows this lane stores
+          const float sa = __shfl_sync(0xffffffffu, inv_l, ra), sb = __shfl_sync(0xffffffffu, inv_l, rb);
+          const bool oka = wrow0 + ra < pend.rows, okb = wrow0 + rb < pend.rows;
+          uint16_t* ga = static_cast<uint16_t*>(a.part_o) + (pend.orow0 + wrow0 + ra) * 128;
+          uint16_t* gb = ga + 8 * 128;
+          float vv[2][32];
+          tmem_ld16x256b_x8(tO + ((uint32_t)(hh * 16) << 16), vv[0]);
+          tmem_ld16x256b_x8(tO + ((uint32_t)(hh * 16) << 16) + 64, vv[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const float* v = vv[half];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              // chunks c0 = 2u, c1 = 2u + 1: this lane holds columns 8c + 2qd, +1
+              // of each; an even lane keeps chunk c0 and takes its odd
+              // neighbour's part of it, an odd lane keeps c1 and takes its even
+              // neighbour's part of c1
+              const int c0 = 2 * u, c1 = 2 * u + 1;
+              const uint32_t a0 = pack2(v[4 * c0] * sa, v[4 * c0 + 1] * sa, bf16);
+              const uint32_t a1 = pack2(v[4 * c1] * sa, v[4 * c1 + 1] * sa, bf16);
+              const uint32_t b0 = pack2(v[4 * c0 + 2] * sb, v[4 * c0 + 3] * sb, bf16);
+              const uint32_t b1 = pack2(v[4 * c1 + 2] * sb, v[4 * c1 + 3] * sb, bf16);
+              const uint32_t ra_x = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+              const uint32_t rb_x = __shfl_xor_sync(0xffffffffu, odd ? b0 : b1, 1);
+              const int col = 64 * half + (odd ? 8 * c1 + 2 * qd - 2 : 8 * c0 + 2 * qd);
+              if (oka) st_global_cs_v2u(ga + col, odd ? ra_x : a0, odd ? a1 : ra_x);
+              if (okb) st_global_cs_v2u(gb + col, odd ? rb_x : b0, odd ? b1 : rb_x);
+            }
           }
         }
       }
@@ -663,6 +706,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
 // The forward: each CTA runs its decode items (decode_body, warps 0-5),
 // then its KV-stationary items (all warps), in one launch.  TMEM (512
 // columns) is allocated once for both phases.
+template <bool kPart32>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
           const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmqs, FwdArgs a,
@@ -689,8 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  if (has_dec) dec::decode_body<16>(tmk, tmv, tmq, d, sm, tmem);
-  if (has_kvs) kv_stationary_body(tmk, tmv, tmqs, a, sm, tmem);
+  if (has_dec) dec::decode_body<16, kPart32>(tmk, tmv, tmq, d, sm, tmem);
+  if (has_kvs) kv_stationary_body<kPart32>(tmk, tmv, tmqs, a, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -737,7 +781,7 @@ size_t fwd_smem_bytes(bool fp8) {
 
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
-                       float* part_o, float* part_lse, cudaStream_t st, int* err_detail) {
+                       void* part_o, float* part_lse, cudaStream_t st, int* err_detail) {
   CUtensorMap tmk, tmv;
   if (!make_cache_map(&tmk, k_cache, p) || !make_cache_map(&tmv, v_cache, p)) {
     *err_detail = 1;
@@ -755,8 +799,10 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)std::max(fwd_smem_bytes(true), fwd_smem_bytes(false)));
+    const int bytes = (int)std::max(fwd_smem_bytes(true), fwd_smem_bytes(false));
+    attr_err = cudaFuncSetAttribute(k_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(k_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   FwdArgs a;
@@ -772,6 +818,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.claim = sc.hdr + kSchClaim;
   a.part_o = part_o;
   a.part_lse = part_lse;
+  a.part32 = partials_fp32(p) ? 1 : 0;
   a.flags = ix.hdr + kHdrFlags;
   // q rows of the KV-stationary tiles: a box of one entry's G rows when G
   // is a multiple of 8 (whole swizzle atoms), else the warps' gather
@@ -793,7 +840,8 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_pdl(k_fwd, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
+  if (a.part32) return launch_pdl(k_fwd<true>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
+  return launch_pdl(k_fwd<false>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
 }
 
 }  // namespace mxsa

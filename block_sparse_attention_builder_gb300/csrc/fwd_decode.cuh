@@ -65,10 +65,10 @@ struct DecArgs {
   const int32_t* cta_ptr;
   const int32_t* idx_hdr;
   const int32_t* sch_hdr;
-  float* part_o;
+  void* part_o;  // partial rows: FP32 when part32, else the 16-bit q dtype
   float* part_lse;
   int32_t* flags;
-  int32_t num_seqs, Hq, Hkv, G, page_size, max_pages, num_pages, kv_fp8, ab_bf16, ns;
+  int32_t num_seqs, Hq, Hkv, G, page_size, max_pages, num_pages, kv_fp8, ab_bf16, ns, part32;
   float scale_log2;
 };
 
@@ -225,7 +225,7 @@ __device__ __forceinline__ void wg_reduce(float* v, float* red) {
 // 1024-aligned shared memory `sm` and the CTA's TMEM base `tmem`).  On
 // return every copy and MMA of the phase has completed and its mbarriers are
 // invalidated, so the shared memory is free for the next phase.
-template <int N>
+template <int N, bool kPart32>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                                             const DecArgs& a, uint8_t* sm, uint32_t tmem) {
   const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
@@ -617,10 +617,21 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       if (!ok) break;
       wg_reduce<N, false>(lsum, red);
       const int e0 = itm.y;
-      float* dst = a.part_o + (size_t)e0 * G * 128 + k;
+      // o = O / l (thread k: head dim k of every row), FP32 or rounded to
+      // the q dtype
+      const size_t o0 = (size_t)e0 * G * 128 + k;
 #pragma unroll
-      for (int r = 0; r < N; ++r)
-        if (r < G) __stcs(&dst[(size_t)r * 128], lsum[r] > 0.f ? o[r] * __frcp_rn(lsum[r]) : 0.f);
+      for (int r = 0; r < N; ++r) {
+        if (r >= G) continue;
+        const float ov = lsum[r] > 0.f ? o[r] * __frcp_rn(lsum[r]) : 0.f;
+        if (kPart32) {
+          __stcs(static_cast<float*>(a.part_o) + o0 + (size_t)r * 128, ov);
+        } else {
+          const unsigned short h =
+              bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(ov)) : __half_as_ushort(__float2half_rn(ov));
+          __stcs(static_cast<unsigned short*>(a.part_o) + o0 + (size_t)r * 128, h);
+        }
+      }
       if (k < G) {
         float lv = -INFINITY, mv = 0.f;
 #pragma unroll
@@ -694,7 +705,7 @@ inline size_t smem_bytes(bool fp8) {
 // Fills the decode phase's arguments and its q tensor map; false when the
 // tensor map cannot be made.
 inline bool make_args(const mxsa_problem& p, const void* q, const int32_t* block_tables, const IndexPtrs& ix,
-                      const SchedPtrs& sc, float* part_o, float* part_lse, DecArgs* a, CUtensorMap* tmq) {
+                      const SchedPtrs& sc, void* part_o, float* part_lse, DecArgs* a, CUtensorMap* tmq) {
   constexpr int N = 16;
   const int G = p.num_q_heads / p.num_kv_heads;
   *a = DecArgs{};
@@ -722,6 +733,7 @@ inline bool make_args(const mxsa_problem& p, const void* q, const int32_t* block
   a->kv_fp8 = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 0;
   a->ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
   a->ns = stages_for<N>(a->kv_fp8);
+  a->part32 = partials_fp32(p) ? 1 : 0;
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a->scale_log2 = scale * 1.4426950408889634f;
   return true;

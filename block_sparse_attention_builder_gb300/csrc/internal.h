@@ -103,6 +103,13 @@ constexpr int kScanTile = kScanThreads * kScanPerThread;  // keys per look-back 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 int64_t max_blocks_per_seq(const mxsa_problem& p);
+
+// Element type of the partial output rows.  With 16-bit caches they are
+// stored in the 16-bit q dtype, which halves the forward's stores and the
+// combine's reads; with FP8 caches they stay FP32 (there the softmax warps
+// also widen the e4m3 blocks, and the packing on their path costs more
+// than the smaller rows save).
+inline bool partials_fp32(const mxsa_problem& p) { return p.kv_dtype == MXSA_FP8_E4M3; }
 mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L);
 mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L);
 IndexPtrs index_ptrs(const mxsa_problem& p, void* ws);
@@ -118,14 +125,14 @@ cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const Sc
                             const mxsa_sched_layout& lay, int num_ctas, cudaStream_t st);
 cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas,
-                       float* part_o, float* part_lse, cudaStream_t st, int* err_detail);
+                       void* part_o, float* part_lse, cudaStream_t st, int* err_detail);
 cudaError_t launch_dense(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* block_tables, const int64_t* cu, const int32_t* lens, void* out, float* lse,
                          int32_t* flags, cudaStream_t st);
 cudaError_t launch_store(const mxsa_problem& p, long long n, const int64_t* loc, const void* k, const void* v,
                          void* k_cache, void* v_cache, const void* idx_k, void* idx_cache, int idx_heads,
                          int idx_dim, int32_t* flags, cudaStream_t st);
-cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const float* part_o,
+cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const void* part_o,
                            const float* part_lse, void* out, float* lse, cudaStream_t st);
 
 

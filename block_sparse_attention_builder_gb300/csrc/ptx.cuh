@@ -281,8 +281,14 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+
 __device__ __forceinline__ void st_global_cs_v2f(float* p, float a, float b) {
   asm volatile("st.global.cs.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
+
+// two 32-bit words to global memory, streaming (evict-first)
+__device__ __forceinline__ void st_global_cs_v2u(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t saddr, uint16_t v) {

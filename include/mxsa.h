@@ -88,17 +88,24 @@ typedef struct {
   int32_t kv_dtype;          /* q_dtype, or MXSA_FP8_E4M3 (unscaled e4m3fn) */
 } mxsa_problem;
 
-/* Library version, (major << 16) | minor. */
+/* Library version, (major << 16) | minor.  (This library's own; the pages
+ * describe no C API.) */
 int32_t mxsa_version(void);
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string).  (This library's
+ * own; no passage.) */
 const char* mxsa_status_string(mxsa_status status);
 
-/* Workspace sizes (bytes) for a problem: upper bounds computed from the
- * shapes alone, so one allocation serves any selections / lengths of that
- * shape.  index: inverted block index + device status word; sched: work
- * items and the per-CTA partition; partial: FP32 partial outputs and lses
- * (one 128-float row + one lse per (selected block, query head) pair).
+/* Workspace sizes (bytes) for a problem.  No passage of the pages defines
+ * this call: the README's Quick-start API allocates internally, and this
+ * caller-owned-workspace design is the library's own.  Upper bounds computed
+ * from the shapes alone (independent of the CTA count: the schedule's
+ * per-CTA arrays are sized for MXSA_MAX_CTAS), so one allocation serves
+ * any selections / lengths of that shape.  index: inverted block index +
+ * device status word; sched: work items and the per-CTA partition; partial:
+ * partial outputs and lses, one row of 128 values plus one FP32 lse per
+ * (selected block, query head) pair; the rows are FP32 when kv_dtype is
+ * MXSA_FP8_E4M3, else in the 16-bit q_dtype.
  * Returns MXSA_ERR_INVALID_ARG / MXSA_ERR_UNSUPPORTED for bad problems. */
 mxsa_status mxsa_workspace_size(const mxsa_problem* problem, size_t* index_bytes, size_t* sched_bytes,
                                 size_t* partial_bytes);
@@ -139,8 +146,11 @@ mxsa_status mxsa_plan(const mxsa_problem* problem, const int32_t* sel, const int
  * its KV block (through block_tables) into shared memory once, gathers the
  * q rows of every (token, head) that selected it, and runs q k^T and p v on
  * the tcgen05 tensor cores with FP32 accumulators in tensor memory and the
- * softmax in registers.  Writes one FP32 partial row o = sum softmax * v
- * over the block's keys and its lse per (entry, head) into partial_ws.
+ * softmax in registers.  Writes one partial row o = sum softmax * v over
+ * the block's keys (accumulated in FP32; stored as FP32 with FP8 caches,
+ * else rounded to nearest-even in q_dtype: o is a convex combination of V
+ * rows, so it stays within their range) and its FP32 lse per (entry, head)
+ * into partial_ws.
  *   q             device [total_q, Hq, 128] of q_dtype
  *   k_cache/v_cache device [num_pages, Hkv, page_size, 128] of kv_dtype
  *   block_tables  device int32 [B, max_pages_per_seq]
@@ -151,8 +161,10 @@ mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const v
                              size_t index_bytes, const void* sched_ws, size_t sched_bytes, int32_t num_ctas,
                              void* partial_ws, size_t partial_bytes, void* stream);
 
-/* Step 4 -- combine: for each (t, h) merges the partials of the row's
- * selected blocks with LSE weights: M = max lse_k, w_k = exp(lse_k - M),
+/* Step 4 -- combine ("combine" kernel in the README's "Tests" list; output
+ * [Tq, Hq, 128] and FP32 lse [Hq, Tq] from its "Quick start"): for each
+ * (t, h) merges the partials of the row's selected blocks with LSE weights,
+ * in FP32: M = max lse_k, w_k = exp(lse_k - M),
  * out = sum w_k o_k / sum w_k (rounded to nearest-even into q_dtype),
  * lse = M + log sum w_k.  A row with no partial gets out 0 and lse -inf.
  *   out   [total_q, Hq, 128] of q_dtype (written): device memory, or pinned
@@ -164,10 +176,33 @@ mxsa_status mxsa_kvouter_fwd(const mxsa_problem* problem, const void* q, const v
 mxsa_status mxsa_combine(const mxsa_problem* problem, const void* index_ws, size_t index_bytes,
                          const void* partial_ws, size_t partial_bytes, void* out, float* lse, void* stream);
 
-/* Synchronises `stream`, then copies the device status word (MXSA_FLAG_*
+/* This library's own (no passage; the README's "Backends" section only
+ * asks that errors are raised rather than hidden).
+ * Synchronises `stream`, then copies the device status word (MXSA_FLAG_*
  * bits) of index_ws into *device_flags.  Returns MXSA_ERR_DATA when any bit
  * is set, MXSA_OK otherwise. */
 mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device_flags);
+
+/* Dense paged attention, the all-blocks-selected case computed directly (no
+ * partials, no combine; the MSA project page lists a dense FMHA path next to
+ * the sparse one): for token t of sequence s and query head h,
+ *   out[t][h][:] = sum_p softmax_p(scale * q[t][h] . k_p) v_p,
+ *   lse[h][t] = log sum_p exp(scale * q[t][h] . k_p)   (natural log),
+ * over keys p < used_kv_lens[s] (and p <= pos(t) = L - Tq_s + i when causal),
+ * k_p / v_p read through block_tables as in mxsa_kvouter_fwd.  No key: out 0,
+ * lse -inf.  Same tensors and layouts as the sparse path (q, caches, out
+ * [total_q][Hq][128] in q_dtype, lse [Hq][total_q] or NULL); topk is unused
+ * and not checked, nor are the sparse index's size limits.
+ * kv_dtype must equal q_dtype (BF16/FP16); num_seqs <= 1024.  Tokens outside
+ * every sequence (cu_seqlens_q out of order or past total_q) are not written.
+ * device_flags (device int32, may be NULL): MXSA_FLAG_PAGE when a needed
+ * block_tables entry lies outside [0, num_pages) (that page is skipped and its
+ * rows' results are undefined), MXSA_FLAG_TIMEOUT.  Device pointers; q, caches
+ * and out 16-byte aligned.  One launch, asynchronous on `stream`;
+ * MXSA_ERR_INVALID_ARG / MXSA_ERR_UNSUPPORTED before any launch. */
+mxsa_status mxsa_dense_fwd(const mxsa_problem* problem, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                           void* out, float* lse, int32_t* device_flags, void* stream);
 
 /* Paged-cache store, the write side of the caches the forward reads (a
  * sglang pull request on these pages, "Summary": the fused K/V/index store
@@ -190,32 +225,12 @@ mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device
  * Device pointers, 16-byte aligned (loc 8-byte); the caller owns all of them.
  * One launch, asynchronous on `stream`.  MXSA_ERR_INVALID_ARG /
  * MXSA_ERR_UNSUPPORTED for bad arguments, before any launch. */
-/* Dense paged attention, the all-blocks-selected case computed directly (no
- * partials, no combine; the MSA project page lists a dense FMHA path next to
- * the sparse one): for token t of sequence s and query head h,
- *   out[t][h][:] = sum_p softmax_p(scale * q[t][h] . k_p) v_p,
- *   lse[h][t] = log sum_p exp(scale * q[t][h] . k_p)   (natural log),
- * over keys p < used_kv_lens[s] (and p <= pos(t) = L - Tq_s + i when causal),
- * k_p / v_p read through block_tables as in mxsa_kvouter_fwd.  No key: out 0,
- * lse -inf.  Same tensors and layouts as the sparse path (q, caches, out
- * [total_q][Hq][128] in q_dtype, lse [Hq][total_q] or NULL); topk is unused
- * and not checked, nor are the sparse index's size limits.
- * kv_dtype must equal q_dtype (BF16/FP16); num_seqs <= 1024.  Tokens outside
- * every sequence (cu_seqlens_q out of order or past total_q) are not written.
- * device_flags (device int32, may be NULL): MXSA_FLAG_PAGE when a needed
- * block_tables entry lies outside [0, num_pages) (that page is skipped and its
- * rows' results are undefined), MXSA_FLAG_TIMEOUT.  Device pointers; q, caches
- * and out 16-byte aligned.  One launch, asynchronous on `stream`;
- * MXSA_ERR_INVALID_ARG / MXSA_ERR_UNSUPPORTED before any launch. */
-mxsa_status mxsa_dense_fwd(const mxsa_problem* problem, const void* q, const void* k_cache, const void* v_cache,
-                           const int32_t* block_tables, const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
-                           void* out, float* lse, int32_t* device_flags, void* stream);
-
 mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const int64_t* loc, const void* k,
                           const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
                           int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream);
 
-/* Byte offsets of the arrays inside the index workspace, for inspection
+/* This library's own (no passage).
+ * Byte offsets of the arrays inside the index workspace, for inspection
  * (tests compare them bit-exactly with an independent CPU statement).
  * header: int32[16] = {flags, NB (blocks over all sequences), nnz (entries),
  *   n_active (keys with entries), n_keys (Hkv * NB), ...};
@@ -229,7 +244,7 @@ typedef struct {
 } mxsa_index_layout;
 mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layout* layout);
 
-/* Byte offsets inside the schedule workspace.  header: int32[16] =
+/* This library's own (no passage).  Byte offsets inside the schedule workspace.  header: int32[16] =
  * {n_items, num_ctas, total cost low, total cost high, (scan counter),
  *  n_dec_items, decode cost low, decode cost high, ...};
  * Two lists, each with int64 exclusive cost prefixes [n + 1] and its own

@@ -66,16 +66,39 @@ def oracle_schedule(w, num_ctas):
     return oracle.schedule(prob, w.used_kv_lens, w.cu_seqlens_q, idx, ITEM_TILES, DECODE_BLOCKS, num_ctas)
 
 
+def partial_elem(prob):
+    """Partial rows are FP32 with FP8 caches, else the 16-bit q dtype."""
+    return (torch.float32, 4) if prob.kv_dtype == mx.FP8_E4M3 else (mx._CODE_DTYPE[prob.q_dtype], 2)
+
+
 def read_partials(attn):
+    """Partial rows (o [nslots * G, 128] as float, lse [nslots * G]) of the
+    partial workspace: the o rows, then the lses at a 256-byte boundary."""
     p = attn.prob
     G = p.num_q_heads // p.num_kv_heads
     nslots = p.total_q * p.num_kv_heads * p.topk
     n_o = nslots * G * 128
-    lse_off = ((n_o * 4 + 255) // 256) * 256
+    dt, es = partial_elem(p)
+    lse_off = ((n_o * es + 255) // 256) * 256
     ws = attn.ws.partial
-    o = ws[:n_o * 4].view(torch.float32).view(nslots * G, 128).cpu().numpy()
+    o = ws[:n_o * es].view(dt).float().view(nslots * G, 128).cpu().numpy()
     lse = ws[lse_off:lse_off + nslots * G * 4].view(torch.float32).cpu().numpy()
     return o, lse
+
+
+def write_partials(attn, o, lse):
+    """Writes partial rows o [nslots * G, 128] (rounded to the partial type)
+    and lse [nslots * G] into the partial workspace, in read_partials' layout."""
+    p = attn.prob
+    G = p.num_q_heads // p.num_kv_heads
+    nslots = p.total_q * p.num_kv_heads * p.topk
+    n_o = nslots * G * 128
+    dt, es = partial_elem(p)
+    lse_off = ((n_o * es + 255) // 256) * 256
+    part = attn.ws.partial
+    ot = torch.from_numpy(np.asarray(o, np.float32).reshape(-1)).to(dt)
+    part[:n_o * es].view(dt).copy_(ot)
+    part[lse_off:lse_off + nslots * G * 4].view(torch.float32).copy_(torch.from_numpy(np.asarray(lse, np.float32)))
 
 
 def oracle_full(w, rows=None):

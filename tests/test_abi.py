@@ -53,7 +53,9 @@ def test_workspace_sizes_are_shape_upper_bounds(lib):
     L = mx.index_layout(p)
     assert ib == L.total and L.nslots == 4 * 2 * 8
     assert L.keys_cap == 2 * 2 * 20  # Hkv * B * ceil(40 * 64 / 128)
-    assert pb >= L.nslots * 8 * 516
+    assert pb >= L.nslots * 8 * (128 * 2 + 4)  # one 16-bit row + an FP32 lse per (slot, head)
+    pf = mx.workspace_size(_prob(kv_dtype=torch.float8_e4m3fn))[2]
+    assert pf >= L.nslots * 8 * (128 * 4 + 4)  # FP8 caches: FP32 rows
     S = mx.sched_layout(p)
     assert sb == S.total and S.items_cap == L.nslots
     offs = [L.header, L.seq_info, L.token_seq, L.slot_entry, L.bitmap, L.kmap, L.counts, L.row_ptr, L.entries,
