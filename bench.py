@@ -608,7 +608,11 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        mx.plan(prob, sel, cu, lens, attn.ws.index, attn.ws.sched, 0, stream)  # index + schedule, one launch
+        if args.plan == "separate":  # the two steps as their own launches (k_index, k_schedule)
+            mx.build_index(prob, sel, cu, lens, attn.ws.index, stream)
+            mx.schedule(prob, attn.ws.index, attn.ws.sched, 0, stream)
+        else:
+            mx.plan(prob, sel, cu, lens, attn.ws.index, attn.ws.sched, 0, stream)  # index + schedule, one launch
         if ev:
             ev[1].record(stream)
         mx.kvouter_fwd(prob, q, k, v, bt, attn.ws.index, attn.ws.sched, attn.ws.partial, 0, stream)
@@ -751,7 +755,7 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
                         "one pinned staging buffer, then the plan while q and block tables copy on a second "
                         "stream; the combine writes out + lse into pinned host memory directly (counted as "
                         "D2H bytes); the KV cache is resident model state"},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (args.plan == "separate")) * args.steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -769,6 +773,9 @@ def main():
                     help="'all' (default): the five sparse workloads in one line, headline skewed_decode; "
                          "or one of " + ", ".join(list(SPARSE_WORKLOADS) + ["kv_store", "dense_prefill"]))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plan", default="fused", choices=["fused", "separate"],
+                    help="index + schedule in one launch (mxsa_plan, default) or as mxsa_build_index then "
+                         "mxsa_schedule")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -74,11 +74,12 @@ class SchedLayout(ctypes.Structure):
                [(n, ctypes.c_int64) for n in ("items_cap", "tiles_cap")]
 
 
-def _load_library() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libmxsa is not built ({LIB_PATH} missing); run __graft_entry__.build() or "
+def _load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"libmxsa is not built ({path} missing); run __graft_entry__.build() or "
                           f"python -m block_sparse_attention_builder_gb300.build")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     P, S = ctypes.c_void_p, ctypes.c_size_t
     lib.mxsa_version.restype = ctypes.c_int32
     lib.mxsa_status_string.restype = ctypes.c_char_p

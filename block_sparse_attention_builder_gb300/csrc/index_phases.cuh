@@ -480,13 +480,13 @@ __device__ __forceinline__ void build_index_phases(const IndexArgs& a, unsigned 
   if (blockIdx.x == 0)
     phase_seq(a.ix, a.cu, a.lens, a.B, a.total_q, a.Hkv, a.cap_len, a.causal, reinterpret_cast<long long*>(tmp));
   phase_token_seq(a.ix, a.cu, a.B, a.total_q);
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   phase_zero(a.ix, a.Hkv, SeqTotals{a.ix.hdr[kHdrNB], a.ix.hdr[kHdrBMW], a.ix.hdr[kHdrKMW]});
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   phase_mark(a.ix, a.sel, a.total_q, a.Hkv, a.topk, a.causal, rowbuf);
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   phase_key_reduce(a.ix, tmp);
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   phase_key_scan_emit(a.ix, a.B, a.Hkv, a.topk, tmp);
 }
 

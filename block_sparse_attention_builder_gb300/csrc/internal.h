@@ -99,8 +99,11 @@ constexpr int kScanThreads = 256;
 constexpr int kScanPerThread = 4;
 constexpr int kScanTile = kScanThreads * kScanPerThread;  // keys per look-back tile
 
-// wall-clock limit of every on-device wait (ns)
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// wall-clock limit of every on-device wait (ns); the test build shortens it
+#ifndef MXSA_WAIT_LIMIT_NS
+#define MXSA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kWaitLimitNs = MXSA_WAIT_LIMIT_NS;
 
 int64_t max_blocks_per_seq(const mxsa_problem& p);
 
@@ -180,6 +183,15 @@ __device__ __forceinline__ unsigned long long dev_globaltimer() {
   return t;
 }
 
+#ifdef MXSA_TEST_HOOKS
+// Test builds only (a separate library): CTA g_skip_cta does not arrive at
+// the g_skip_barrier-th grid barrier of a launch (1 = the first), so that
+// the other CTAs' bounded waits run out.  One copy per translation unit;
+// the setter lives beside the kernel it affects.
+static __device__ int g_skip_cta = -1;
+static __device__ int g_skip_barrier = 0;
+#endif
+
 // Grid-wide barrier for kernels launched cooperatively (all CTAs
 // co-resident).  bar[0] counts arrivals since the launch and must be 0 at
 // launch; the n-th barrier of a launch (n = ++epoch, the same in every CTA)
@@ -187,15 +199,26 @@ __device__ __forceinline__ unsigned long long dev_globaltimer() {
 // needed and the last arrival releases everyone.  bar[1] is the abort word
 // (0 at launch).  The wait is bounded: past the limit it sets
 // MXSA_FLAG_TIMEOUT and the abort word, and every later barrier of the
-// launch returns at once.
-__device__ __forceinline__ void grid_barrier(int* bar, int* flags, unsigned nblocks, int& epoch) {
+// launch returns at once.  Returns false (in every thread of the CTA) when
+// the launch was aborted: the caller must then return instead of starting
+// its next phase on data the other CTAs may not have written.
+__device__ __forceinline__ bool grid_barrier(int* bar, int* flags, unsigned nblocks, int& epoch) {
+  __shared__ int s_ok;
   __syncthreads();
   const int target = ++epoch * (int)nblocks;
   if (threadIdx.x == 0) {
     volatile int* vabort = bar + 1;
     __threadfence();
     int seen;
-    asm volatile("atom.add.release.gpu.global.s32 %0, [%1], 1;" : "=r"(seen) : "l"(bar) : "memory");
+#ifdef MXSA_TEST_HOOKS
+    const bool skip = (int)blockIdx.x == g_skip_cta && epoch == g_skip_barrier;
+#else
+    constexpr bool skip = false;
+#endif
+    if (skip)
+      seen = -1;  // not counted: this CTA's own wait runs out like the others'
+    else
+      asm volatile("atom.add.release.gpu.global.s32 %0, [%1], 1;" : "=r"(seen) : "l"(bar) : "memory");
     if (seen + 1 < target) {
       const unsigned long long t0 = dev_globaltimer();
       while (true) {
@@ -210,8 +233,10 @@ __device__ __forceinline__ void grid_barrier(int* bar, int* flags, unsigned nblo
       }
     }
     __threadfence();
+    s_ok = *vabort == 0;
   }
   __syncthreads();
+  return s_ok != 0;
 }
 
 #endif

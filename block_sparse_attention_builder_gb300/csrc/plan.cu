@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kPlanThreads, 2) k_plan(PlanArgs a) {
     if (blockIdx.x == 0)
       ixp::phase_seq(ia.ix, ia.cu, ia.lens, ia.B, ia.total_q, ia.Hkv, ia.cap_len, ia.causal,
                      reinterpret_cast<long long*>(tmp));
-    grid_barrier(bar, flags, nb, epoch);
+    if (!grid_barrier(bar, flags, nb, epoch)) return;
     tot = ixp::SeqTotals{ia.ix.hdr[kHdrNB], ia.ix.hdr[kHdrBMW], ia.ix.hdr[kHdrKMW]};
   }
   ixp::phase_token_seq(ia.ix, ia.cu, ia.B, ia.total_q);
@@ -571,18 +571,18 @@ __global__ void __launch_bounds__(kPlanThreads, 2) k_plan(PlanArgs a) {
     if (__syncthreads_and(all_decode)) {
       const ixp::SeqTab tab{ia.ix.seq, s_tab, ia.B};
       fast_phase_a(ia.ix, ia.sel, a.P, tab, ia.topk, rowbuf, tmp);
-      grid_barrier(bar, flags, nb, epoch);
+      if (!grid_barrier(bar, flags, nb, epoch)) return;
       fast_phase_b(ia.ix, a.sc, a.P, tab, ia.total_q, ia.topk, rowbuf, tmp);
       return;
     }
   }
   ixp::phase_zero(ia.ix, ia.Hkv, tot, false);
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   ixp::phase_mark(ia.ix, ia.sel, ia.total_q, ia.Hkv, ia.topk, ia.causal, rowbuf, false);
   const ixp::SeqTab tab{ia.ix.seq, ia.B <= ixp::kSeqTab ? s_tab : nullptr, ia.B};
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   plan_reduce(ia.ix, a.P, tab, tmp);
-  grid_barrier(bar, flags, nb, epoch);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
   plan_scan_emit(ia.ix, a.sc, a.P, ia.Hkv, ia.topk, tab, tmp);
 }
 
@@ -614,3 +614,14 @@ cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t
 }
 
 }  // namespace mxsa
+
+#ifdef MXSA_TEST_HOOKS
+// Test builds only: makes CTA `cta` of the next plan launches skip its
+// arrival at grid barrier number `barrier` (1 = the first); cta = -1 turns
+// the switch off.  Synchronous.
+extern "C" mxsa_status mxsa_test_skip_barrier_arrival(int32_t cta, int32_t barrier) {
+  if (cudaMemcpyToSymbol(mxsa::g_skip_cta, &cta, sizeof(cta)) != cudaSuccess) return MXSA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(mxsa::g_skip_barrier, &barrier, sizeof(barrier)) != cudaSuccess) return MXSA_ERR_CUDA;
+  return MXSA_OK;
+}
+#endif

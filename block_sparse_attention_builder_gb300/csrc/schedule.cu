@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
   int epoch = 0;
   int* flags = a.ix.hdr + kHdrFlags;
   phase_reduce(a.ix, a.sc, a.P, tmp);
-  grid_barrier(bar, flags, gridDim.x, epoch);
+  if (!grid_barrier(bar, flags, gridDim.x, epoch)) return;
   phase_scan_emit(a.ix, a.sc, a.P, tmp);
 }
 

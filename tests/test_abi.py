@@ -34,6 +34,14 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= set(mx.EXPORTED) | set(names)
 
 
+def test_test_switch_only_in_the_test_library(lib):
+    """The barrier switch of the wait-limit test exists only in the
+    separate test library, never in libmxsa.so."""
+    assert not hasattr(lib, "mxsa_test_skip_barrier_arrival")
+    test_lib = mx._load_library(B.TEST_LIB)
+    assert hasattr(test_lib, "mxsa_test_skip_barrier_arrival")
+
+
 def test_version_and_status_strings(lib):
     assert lib.mxsa_version() >> 16 == 1
     for code, name in mx.STATUS_NAMES.items():
