@@ -243,6 +243,19 @@ class Workload:
     def v_cache(self, device="cpu") -> torch.Tensor:
         return self._cache(3, device)
 
+    # index tensors of the top-k block selection (one index head per kv head,
+    # in the cache dtype): the query side [Tq, Hkv, dim] and the paged index-K
+    # cache [pages, Hkv, page_size, dim], paged like K
+    def idx_q(self, dim: int, device="cpu") -> torch.Tensor:
+        n = self.total_q * self.num_kv_heads * dim
+        v = generate_values(n, stream_key(self.spec.seed, 4), self.spec.kv_dtype, device)
+        return v.view(self.total_q, self.num_kv_heads, dim)
+
+    def idx_cache(self, dim: int, device="cpu") -> torch.Tensor:
+        n = self.num_pages * self.num_kv_heads * self.page_size * dim
+        v = generate_values(n, stream_key(self.spec.seed, 5), self.spec.kv_dtype, device)
+        return v.view(self.num_pages, self.num_kv_heads, self.page_size, dim)
+
     def cache_pages(self, tensor_id: int, pages: np.ndarray, device="cpu") -> torch.Tensor:
         """Pages `pages` of the K (2) or V (3) cache as a CPU tensor.  The
         values are generated on `device` (identical bits on any device)."""

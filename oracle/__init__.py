@@ -15,6 +15,9 @@ Functions whose parity is pinned by tests/test_oracle_pins.py:
   decode          -- every code against torch's own dtype conversions
   encode_e4m3, store -- every bf16/fp16 code against torch's clamp-and-cast
                      (tests/test_store_pins.py)
+  select_blocks   -- top-k block selection: exact float64 scores and a
+                     brute-force ranking, ties, masks, pages
+                     (tests/test_select_pins.py)
 """
 from __future__ import annotations
 
@@ -90,6 +93,9 @@ def _load():
         _lib.oracle_store.restype = ctypes.c_int64
         _lib.oracle_store.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int64, P, P, P]
+        _lib.oracle_select_blocks.restype = ctypes.c_int
+        _lib.oracle_select_blocks.argtypes = [P, ctypes.c_int32, P, P, P, P, P, P, P, ctypes.c_int64,
+                                              ctypes.c_int32]
         _lib.oracle_schedule.restype = ctypes.c_int
         _lib.oracle_schedule.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int64, P]
@@ -175,6 +181,28 @@ def attention_rows(prob: OracleProblem, q, k_cache, v_cache, selected, block_tab
     if rc != 0:
         raise RuntimeError(f"oracle_attention_rows failed: {rc}")
     return out, lse
+
+
+def select_blocks(prob: OracleProblem, dim: int, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_lens,
+                  with_scores: bool = False, nthreads: Optional[int] = None):
+    """Top-k block selection (see oracle_select_blocks): sel int32 [Tq, Hkv,
+    topk], and with with_scores the block scores float32 [Tq, Hkv, nblk_max]
+    (NaN where a block has none)."""
+    lib = _load()
+    qb, kb = _bits(idx_q), _bits(idx_cache)
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_seqlens_q, np.int64)
+    lens = _c(used_kv_lens, np.int32)
+    T, H, K = prob.total_q, prob.num_kv_heads, prob.topk
+    sel = np.full((T, H, K), -1, dtype=np.int32)
+    nbm = (prob.max_pages_per_seq * prob.page_size + 127) // 128
+    scores = np.full((T, H, nbm), np.nan, dtype=np.float32) if with_scores else None
+    rc = lib.oracle_select_blocks(ctypes.byref(prob), int(dim), _ptr(qb), _ptr(kb), _ptr(bt), _ptr(cu), _ptr(lens),
+                                  _ptr(sel), _ptr(scores) if with_scores else None, ctypes.c_int64(nbm),
+                                  int(nthreads or os.cpu_count() or 1))
+    if rc != 0:
+        raise RuntimeError(f"oracle_select_blocks failed: {rc}")
+    return (sel, scores) if with_scores else sel
 
 
 def combine(o_parts: np.ndarray, lse_parts: np.ndarray):

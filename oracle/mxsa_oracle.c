@@ -567,6 +567,152 @@ int64_t oracle_block_owners(const oracle_problem* p, const int32_t* lens, const 
   return rc;
 }
 
+/* ---------------------------------------------------- top-k block selection
+ * The step before the index: which 128-token blocks each (token, kv head)
+ * row attends to.  The MSA summary page ("How It Works") names "sparse
+ * top-k selection"; the sglang pull request ("Summary") writes an index K
+ * cache beside K and V.  The scoring rule itself is not on the pages; this
+ * is the library's reading (also in the design notes):
+ *   - index query iq[t][g][0..D) and an index key at every cached position p
+ *     of the sequence, ik_cache[block_tables[s][p / ps]][g][p % ps][0..D)
+ *     (one index head per kv head), both in the problem's kv dtype;
+ *   - dot(t, g, p) = the FP32 sum of iq[t][g][d] * ik[p][g][d], accumulated
+ *     by fused multiply-add in the order d = 0, 1, .., D-1 starting from +0:
+ *     the kernel's precision, since the selection is an integer decision
+ *     both sides must take in the same arithmetic;
+ *   - score(t, g, b) = the largest dot(t, g, p) over the block's visible
+ *     positions: 128 b <= p < min(128 b + 128, L), p <= pos(t) when causal,
+ *     and p on a valid page; NaN dots are skipped; a block with no such p
+ *     has no score;
+ *   - sel[t][g][:] = the blocks that have a score, by score descending and
+ *     then block ascending (+0 and -0 are equal), the first topk of them;
+ *     the remaining slots are -1.  Tokens outside every sequence get -1. */
+typedef struct {
+  const oracle_problem* p;
+  int32_t dim;
+  const void *iq, *ik;
+  const int32_t *bt, *lens;
+  const int64_t* cu;
+  int32_t* sel;
+  float* score;
+  int64_t max_blocks;
+  int64_t next;
+  pthread_mutex_t mu;
+  int err;
+} select_job;
+
+typedef struct {
+  float score;
+  int32_t b;
+} block_score;
+
+static int cmp_block_score(const void* a, const void* b) {
+  const block_score* x = (const block_score*)a;
+  const block_score* y = (const block_score*)b;
+  if (x->score > y->score) return -1;
+  if (x->score < y->score) return 1;
+  if (MUT(17)) return x->b > y->b ? -1 : (x->b < y->b ? 1 : 0); /* mutant 17: ties to the larger block */
+  return x->b < y->b ? -1 : (x->b > y->b ? 1 : 0);
+}
+
+static int select_row(const select_job* J, int64_t t, int32_t g) {
+  const oracle_problem* p = J->p;
+  const int32_t Hkv = p->num_kv_heads, K = p->topk, ps = p->page_size, D = J->dim;
+  int32_t* out = J->sel + (t * Hkv + g) * K;
+  for (int32_t k = 0; k < K; ++k) out[k] = -1;
+  const int32_t s = seq_of_token(J->cu, p->num_seqs, t);
+  if (s < 0) return 0;
+  const int64_t cap = (int64_t)p->max_pages_per_seq * ps;
+  int64_t L = J->lens[s];
+  if (L < 0) L = 0;
+  if (L > cap) L = cap;
+  const int64_t tq = J->cu[s + 1] - J->cu[s], pos = L - tq + (t - J->cu[s]);
+  const int64_t nblk = (L + 127) / 128;
+  float* qf = (float*)malloc(sizeof(float) * (size_t)D);
+  block_score* bs = (block_score*)malloc(sizeof(block_score) * (size_t)(nblk > 0 ? nblk : 1));
+  if (!qf || !bs) {
+    free(qf);
+    free(bs);
+    return -1;
+  }
+  for (int32_t d = 0; d < D; ++d) qf[d] = (float)load_elem(J->iq, p->kv_dtype, (t * Hkv + g) * D + d);
+  int64_t n = 0;
+  for (int64_t b = 0; b < nblk; ++b) {
+    int have = 0;
+    float best = 0.f;
+    for (int64_t pp = 128 * b; pp < 128 * b + 128 && pp < L; ++pp) {
+      if (p->causal && pp > pos - (MUT(18) ? 1 : 0)) break; /* mutant 18: the row's own position hidden */
+      const int32_t page = J->bt[(int64_t)s * p->max_pages_per_seq + pp / ps];
+      if (page < 0 || page >= p->num_pages) continue;
+      const int64_t base = (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
+      float acc = 0.f;
+      for (int32_t d = 0; d < D - (MUT(19) ? 1 : 0); ++d) /* mutant 19: the last dimension dropped */
+        acc = fmaf(qf[d], (float)load_elem(J->ik, p->kv_dtype, base + d), acc);
+      if (isnan(acc)) continue;
+      if (!have || (MUT(20) ? acc < best : acc > best)) best = acc; /* mutant 20: the block's minimum */
+      have = 1;
+    }
+    if (J->score && b < J->max_blocks) J->score[(t * Hkv + g) * J->max_blocks + b] = have ? best : NAN;
+    if (!have) continue;
+    bs[n].score = best == 0.f ? 0.f : best; /* -0 ranks as +0 */
+    bs[n].b = (int32_t)b;
+    ++n;
+  }
+  qsort(bs, (size_t)n, sizeof(block_score), cmp_block_score);
+  for (int64_t k = 0; k < n && k < K; ++k) out[k] = bs[k].b;
+  free(qf);
+  free(bs);
+  return 0;
+}
+
+static void* select_worker(void* arg) {
+  select_job* J = (select_job*)arg;
+  const int64_t rows = (int64_t)J->p->total_q * J->p->num_kv_heads;
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    const int64_t r = J->next++;
+    pthread_mutex_unlock(&J->mu);
+    if (r >= rows) break;
+    if (select_row(J, r / J->p->num_kv_heads, (int32_t)(r % J->p->num_kv_heads)) != 0) {
+      pthread_mutex_lock(&J->mu);
+      J->err = 1;
+      pthread_mutex_unlock(&J->mu);
+    }
+  }
+  return NULL;
+}
+
+/* sel_out int32 [total_q][Hkv][topk]; score_out (may be NULL) float
+ * [total_q][Hkv][max_blocks]: each block's score, NaN where it has none.
+ * Returns 0, or -1 (memory). */
+int oracle_select_blocks(const oracle_problem* p, int32_t dim, const void* iq, const void* ik_cache,
+                         const int32_t* block_tables, const int64_t* cu, const int32_t* lens, int32_t* sel_out,
+                         float* score_out, int64_t max_blocks, int32_t nthreads) {
+  select_job J;
+  memset(&J, 0, sizeof(J));
+  J.p = p;
+  J.dim = dim;
+  J.iq = iq;
+  J.ik = ik_cache;
+  J.bt = block_tables;
+  J.lens = lens;
+  J.cu = cu;
+  J.sel = sel_out;
+  J.score = score_out;
+  J.max_blocks = max_blocks;
+  pthread_mutex_init(&J.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int i = 0; i < nthreads; ++i)
+    if (pthread_create(&th[i], NULL, select_worker, &J) == 0) ++started;
+  if (started == 0) select_worker(&J);
+  for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return J.err ? -1 : 0;
+}
+
 /* --------------------------------------------------------------- schedule
  * Load-balancing schedule over the index ("load-balancing scheduler" in the
  * README's test list; the splitting rule, the decode merge and the cost

@@ -11,7 +11,8 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = ["tests/test_oracle_pins.py", "tests/test_store_pins.py", "tests/test_dedup_pins.py"]
+PINS = ["tests/test_oracle_pins.py", "tests/test_store_pins.py", "tests/test_dedup_pins.py",
+        "tests/test_select_pins.py"]
 MUTANTS = {
     1: "bf16 decoding with misplaced bits",
     2: "e4m3 decoding with the wrong exponent bias",
@@ -29,6 +30,10 @@ MUTANTS = {
     14: "dedup merges nothing",
     15: "decode runs split into one item too many",
     16: "e4m3 encoding rounds ties away from zero",
+    17: "selection ties go to the larger block",
+    18: "selection hides the row's own causal position",
+    19: "selection scores drop the last index dimension",
+    20: "selection scores a block by its minimum",
 }
 
 
