@@ -3,8 +3,9 @@
 Argument marshalling only -- every step runs in the library's CUDA kernels;
 PyTorch provides device memory and streams.  The entry points mirror the C
 ABI in include/mxsa.h (build_index, schedule, plan, kvouter_fwd, combine,
-read_status, and store_kv, the paged-cache store that writes new tokens'
-K/V and index keys into the caches), plus ``kvouter_attention`` with the
+read_status, store_kv, the paged-cache store that writes new tokens' K/V
+and index keys into the caches, and select_blocks, the top-k block
+selection over those index keys), plus ``kvouter_attention`` with the
 call shape of the fw-ai/minimax-kernels README's Quick start and
 ``SparseAttention`` which keeps the workspaces of one problem shape for
 repeated calls.
@@ -38,7 +39,8 @@ STATUS_NAMES = {0: "MXSA_OK", 1: "MXSA_ERR_INVALID_ARG", 2: "MXSA_ERR_UNSUPPORTE
 EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_build_index", "mxsa_schedule",
             "mxsa_plan",
             "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
-            "mxsa_sched_layout_query", "mxsa_store_kv", "mxsa_dense_fwd"]
+            "mxsa_sched_layout_query", "mxsa_store_kv", "mxsa_dense_fwd", "mxsa_select_workspace_size",
+            "mxsa_select_blocks"]
 
 
 class MxsaError(RuntimeError):
@@ -96,6 +98,8 @@ def _load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "mxsa_sched_layout_query": [P, P],
         "mxsa_store_kv": [P, ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P],
         "mxsa_dense_fwd": [P, P, P, P, P, P, P, P, P, P, P],
+        "mxsa_select_workspace_size": [P, ctypes.c_int32, P],
+        "mxsa_select_blocks": [P, ctypes.c_int32, P, P, P, P, P, P, S, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -265,6 +269,41 @@ def store_kv(prob, loc, k, v, k_cache, v_cache, idx_k=None, idx_cache=None, flag
     _need(what, "flags", flags, 4)
     _check(_lib.mxsa_store_kv(ctypes.byref(prob), n, _ptr(loc), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                               _ptr(idx_k), _ptr(idx_cache), ih, idim, _ptr(flags), _stream(stream)), "mxsa_store_kv")
+
+
+def select_workspace_size(prob: Problem, idx_dim: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mxsa_select_workspace_size(ctypes.byref(prob), int(idx_dim), ctypes.byref(n)),
+           "mxsa_select_workspace_size")
+    return n.value
+
+
+def select_blocks(prob, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_lens, sel=None, score_ws=None,
+                  flags=None, stream=None):
+    """Top-k block selection (mxsa_select_blocks): sel int32 [total_q, Hkv,
+    topk] from the index queries idx_q [total_q, Hkv, D] and the paged index
+    cache [pages, Hkv, page_size, D] (kv dtype, D = 64 or 128).  Returns
+    (sel, score_ws)."""
+    what = "mxsa_select_blocks"
+    D = int(idx_q.shape[-1])
+    kb = _ELEM_BYTES.get(prob.kv_dtype, 2)
+    nbytes = select_workspace_size(prob, D)
+    if score_ws is None:
+        score_ws = torch.empty(nbytes, dtype=torch.uint8, device=idx_q.device)
+    if sel is None:
+        sel = torch.empty(prob.total_q, prob.num_kv_heads, prob.topk, dtype=torch.int32, device=idx_q.device)
+    _need(what, "idx_q", idx_q, max(prob.total_q, 0) * max(prob.num_kv_heads, 0) * D * kb)
+    _need(what, "idx_cache", idx_cache, max(prob.num_pages, 0) * max(prob.num_kv_heads, 0) *
+          max(prob.page_size, 0) * D * kb)
+    _need_attention(what, prob, block_tables=block_tables, cu_seqlens_q=cu_seqlens_q, used_kv_lens=used_kv_lens,
+                    sel=sel)
+    _need(what, "score_ws", score_ws, nbytes)
+    _need(what, "flags", flags, 4)
+    _check(_lib.mxsa_select_blocks(ctypes.byref(prob), D, _ptr(idx_q), _ptr(idx_cache), _ptr(block_tables),
+                                   _ptr(cu_seqlens_q), _ptr(used_kv_lens), _ptr(score_ws),
+                                   score_ws.numel() * score_ws.element_size(), _ptr(sel), _ptr(flags),
+                                   _stream(stream)), what)
+    return sel, score_ws
 
 
 def read_status(index_ws, stream=None) -> int:

@@ -388,6 +388,44 @@ mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const i
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
 }
 
+// Shape checks of the top-k selection: the sparse problem's (topk, sizes)
+// plus the selection's own limits.
+static mxsa_status validate_select(const mxsa_problem& p, int32_t idx_dim) {
+  mxsa_status s = validate_problem(p);
+  if (s != MXSA_OK) return s;
+  if (idx_dim != 64 && idx_dim != 128) return MXSA_ERR_UNSUPPORTED;
+  if (p.num_seqs > 1024 || max_blocks_per_seq(p) > 4096) return MXSA_ERR_UNSUPPORTED;
+  return MXSA_OK;
+}
+
+mxsa_status mxsa_select_workspace_size(const mxsa_problem* problem, int32_t idx_dim, size_t* score_bytes) {
+  if (!problem || !score_bytes) return MXSA_ERR_INVALID_ARG;
+  mxsa_status s = validate_select(*problem, idx_dim);
+  if (s != MXSA_OK) return s;
+  *score_bytes = align_up(select_score_bytes(*problem));
+  if (*score_bytes == 0) *score_bytes = kAlign;
+  return MXSA_OK;
+}
+
+mxsa_status mxsa_select_blocks(const mxsa_problem* problem, int32_t idx_dim, const void* idx_q,
+                               const void* idx_cache, const int32_t* block_tables, const int64_t* cu_seqlens_q,
+                               const int32_t* used_kv_lens, void* score_ws, size_t score_bytes, int32_t* sel,
+                               int32_t* device_flags, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_status s = validate_select(*problem, idx_dim);
+  if (s != MXSA_OK) return s;
+  const mxsa_problem& p = *problem;
+  if (!block_tables || !cu_seqlens_q || !used_kv_lens || !score_ws) return MXSA_ERR_INVALID_ARG;
+  if (p.total_q > 0 && (!idx_q || !idx_cache || !sel)) return MXSA_ERR_INVALID_ARG;
+  if (!aligned(idx_q, 16) || !aligned(idx_cache, 16) || !aligned(block_tables, 4) || !aligned(cu_seqlens_q, 8) ||
+      !aligned(used_kv_lens, 4) || !aligned(score_ws, 16) || !aligned(sel, 4) || !aligned(device_flags, 4))
+    return MXSA_ERR_INVALID_ARG;
+  if (score_bytes < select_score_bytes(p)) return MXSA_ERR_WORKSPACE;
+  cudaError_t e = launch_select(p, idx_dim, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_lens,
+                                static_cast<float*>(score_ws), sel, device_flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
 mxsa_status mxsa_read_status(const void* index_ws, void* stream, int32_t* device_flags) {
   if (!index_ws || !device_flags || !aligned(index_ws, 16)) return MXSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -256,6 +256,17 @@ class Workload:
         v = generate_values(n, stream_key(self.spec.seed, 5), self.spec.kv_dtype, device)
         return v.view(self.num_pages, self.num_kv_heads, self.page_size, dim)
 
+    def idx_cache_pages(self, dim: int, pages: np.ndarray, device="cpu") -> torch.Tensor:
+        """Pages `pages` of the index-K cache as a CPU tensor [n, Hkv, ps, dim]
+        (the same values as idx_cache's)."""
+        per_page = self.num_kv_heads * self.page_size * dim
+        key = stream_key(self.spec.seed, 5)
+        pages_t = torch.as_tensor(np.asarray(pages, dtype=np.int64)).to(device)
+        ar = torch.arange(per_page, dtype=torch.int64, device=device)
+        idx = (pages_t[:, None] * per_page + ar[None, :]).reshape(-1)
+        raw = generate_at(idx, key, self.spec.kv_dtype).cpu()
+        return raw.view(TORCH_DTYPE[self.spec.kv_dtype]).view(len(pages), self.num_kv_heads, self.page_size, dim)
+
     def cache_pages(self, tensor_id: int, pages: np.ndarray, device="cpu") -> torch.Tensor:
         """Pages `pages` of the K (2) or V (3) cache as a CPU tensor.  The
         values are generated on `device` (identical bits on any device)."""

@@ -229,6 +229,44 @@ mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const i
                           const void* v, void* k_cache, void* v_cache, const void* idx_k, void* idx_cache,
                           int32_t idx_heads, int32_t idx_dim, int32_t* device_flags, void* stream);
 
+/* Top-k block selection, the step before mxsa_build_index: which 128-token
+ * blocks each (token, kv head) row attends to.  The MSA summary page ("How
+ * It Works") names the "sparse top-k selection"; the sglang pull request
+ * ("Summary") writes an index K cache beside K and V (mxsa_store_kv's
+ * idx_cache).  The pages give no scoring rule; this library's reading:
+ *   dot(t, g, p)   = the FP32 sum of idx_q[t][g][d] * ik_p[d] over d,
+ *                    fused multiply-adds in the order d = 0 .. idx_dim-1
+ *                    from +0, where ik_p = idx_cache[block_tables[s][p /
+ *                    page_size]][g][p % page_size][:] (one index head per kv
+ *                    head); a NaN dot counts as no key;
+ *   score(t, g, b) = the largest dot over the block's visible positions:
+ *                    128 b <= p < min(128 b + 128, L), p <= pos(t) when
+ *                    causal, p on a page in [0, num_pages);
+ *   sel[t][g][:]   = the blocks that have a score, by score descending and
+ *                    then block ascending (+0 = -0), the first topk of them;
+ *                    the remaining slots are -1.
+ * The result is exact (bit-identical to a CPU statement of the definition);
+ * its rows are valid input for mxsa_plan / mxsa_build_index.
+ *   idx_q        device [total_q][Hkv][idx_dim] of kv_dtype
+ *   idx_cache    device [num_pages][Hkv][page_size][idx_dim] of kv_dtype
+ *   block_tables, cu_seqlens_q, used_kv_lens as for mxsa_build_index
+ *   score_ws     device, score_bytes from mxsa_select_workspace_size: the
+ *                block scores [total_q][Hkv][ceil(max_pages_per_seq *
+ *                page_size / 128)] FP32 (NaN: no score), kept for
+ *                inspection; entries past a sequence's last block are not
+ *                written
+ *   sel          device int32 [total_q][Hkv][topk] (written)
+ *   device_flags device int32 or NULL: MXSA_FLAG_CU when cu_seqlens_q is not
+ *                a non-decreasing partition of total_q (then every row is -1)
+ * idx_dim is 64 or 128; num_seqs <= 1024; at most 4096 blocks per sequence.
+ * Two launches, asynchronous on `stream`; MXSA_ERR_INVALID_ARG /
+ * MXSA_ERR_UNSUPPORTED / MXSA_ERR_WORKSPACE before any launch. */
+mxsa_status mxsa_select_workspace_size(const mxsa_problem* problem, int32_t idx_dim, size_t* score_bytes);
+mxsa_status mxsa_select_blocks(const mxsa_problem* problem, int32_t idx_dim, const void* idx_q,
+                               const void* idx_cache, const int32_t* block_tables, const int64_t* cu_seqlens_q,
+                               const int32_t* used_kv_lens, void* score_ws, size_t score_bytes, int32_t* sel,
+                               int32_t* device_flags, void* stream);
+
 /* This library's own (no passage).
  * Byte offsets of the arrays inside the index workspace, for inspection
  * (tests compare them bit-exactly with an independent CPU statement).

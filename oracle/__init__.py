@@ -94,8 +94,8 @@ def _load():
         _lib.oracle_store.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int64, P, P, P]
         _lib.oracle_select_blocks.restype = ctypes.c_int
-        _lib.oracle_select_blocks.argtypes = [P, ctypes.c_int32, P, P, P, P, P, P, P, ctypes.c_int64,
-                                              ctypes.c_int32]
+        _lib.oracle_select_blocks.argtypes = [P, ctypes.c_int32, P, P, P, P, P, P, P, ctypes.c_int64, P,
+                                              ctypes.c_int64, ctypes.c_int32]
         _lib.oracle_schedule.restype = ctypes.c_int
         _lib.oracle_schedule.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int64, P]
@@ -184,10 +184,11 @@ def attention_rows(prob: OracleProblem, q, k_cache, v_cache, selected, block_tab
 
 
 def select_blocks(prob: OracleProblem, dim: int, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_lens,
-                  with_scores: bool = False, nthreads: Optional[int] = None):
+                  with_scores: bool = False, nthreads: Optional[int] = None, rows: Optional[np.ndarray] = None):
     """Top-k block selection (see oracle_select_blocks): sel int32 [Tq, Hkv,
     topk], and with with_scores the block scores float32 [Tq, Hkv, nblk_max]
-    (NaN where a block has none)."""
+    (NaN where a block has none).  rows: only these (token * Hkv + kv head)
+    rows are computed (the others stay -1 / NaN)."""
     lib = _load()
     qb, kb = _bits(idx_q), _bits(idx_cache)
     bt = _c(block_tables, np.int32)
@@ -197,8 +198,10 @@ def select_blocks(prob: OracleProblem, dim: int, idx_q, idx_cache, block_tables,
     sel = np.full((T, H, K), -1, dtype=np.int32)
     nbm = (prob.max_pages_per_seq * prob.page_size + 127) // 128
     scores = np.full((T, H, nbm), np.nan, dtype=np.float32) if with_scores else None
+    rws = None if rows is None else _c(rows, np.int64)
     rc = lib.oracle_select_blocks(ctypes.byref(prob), int(dim), _ptr(qb), _ptr(kb), _ptr(bt), _ptr(cu), _ptr(lens),
                                   _ptr(sel), _ptr(scores) if with_scores else None, ctypes.c_int64(nbm),
+                                  _ptr(rws) if rws is not None else None, ctypes.c_int64(0 if rws is None else len(rws)),
                                   int(nthreads or os.cpu_count() or 1))
     if rc != 0:
         raise RuntimeError(f"oracle_select_blocks failed: {rc}")

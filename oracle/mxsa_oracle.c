@@ -596,6 +596,8 @@ typedef struct {
   int32_t* sel;
   float* score;
   int64_t max_blocks;
+  const int64_t* rows; /* (token * Hkv + kv head) rows to compute, or NULL for all */
+  int64_t nrows;
   int64_t next;
   pthread_mutex_t mu;
   int err;
@@ -667,12 +669,13 @@ static int select_row(const select_job* J, int64_t t, int32_t g) {
 
 static void* select_worker(void* arg) {
   select_job* J = (select_job*)arg;
-  const int64_t rows = (int64_t)J->p->total_q * J->p->num_kv_heads;
+  const int64_t rows = J->rows ? J->nrows : (int64_t)J->p->total_q * J->p->num_kv_heads;
   for (;;) {
     pthread_mutex_lock(&J->mu);
-    const int64_t r = J->next++;
+    const int64_t i = J->next++;
     pthread_mutex_unlock(&J->mu);
-    if (r >= rows) break;
+    if (i >= rows) break;
+    const int64_t r = J->rows ? J->rows[i] : i;
     if (select_row(J, r / J->p->num_kv_heads, (int32_t)(r % J->p->num_kv_heads)) != 0) {
       pthread_mutex_lock(&J->mu);
       J->err = 1;
@@ -684,10 +687,12 @@ static void* select_worker(void* arg) {
 
 /* sel_out int32 [total_q][Hkv][topk]; score_out (may be NULL) float
  * [total_q][Hkv][max_blocks]: each block's score, NaN where it has none.
+ * rows (may be NULL): only these (token * Hkv + kv head) rows are computed.
  * Returns 0, or -1 (memory). */
 int oracle_select_blocks(const oracle_problem* p, int32_t dim, const void* iq, const void* ik_cache,
                          const int32_t* block_tables, const int64_t* cu, const int32_t* lens, int32_t* sel_out,
-                         float* score_out, int64_t max_blocks, int32_t nthreads) {
+                         float* score_out, int64_t max_blocks, const int64_t* rows, int64_t nrows,
+                         int32_t nthreads) {
   select_job J;
   memset(&J, 0, sizeof(J));
   J.p = p;
@@ -700,6 +705,8 @@ int oracle_select_blocks(const oracle_problem* p, int32_t dim, const void* iq, c
   J.sel = sel_out;
   J.score = score_out;
   J.max_blocks = max_blocks;
+  J.rows = rows;
+  J.nrows = nrows;
   pthread_mutex_init(&J.mu, NULL);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
