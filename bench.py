@@ -306,6 +306,9 @@ def run_reference(args, rank, world):
     if args.workload in ("kv_store", "dense_prefill"):
         run_reference_extra(args, world)
         return
+    if args.workload in SELECT_WORKLOADS:
+        run_reference_select(args, world)
+        return
     w = load_workload(args.workload, 0)
     nthreads = os.cpu_count() or 1
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
@@ -763,6 +766,188 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     return entry
 
 
+# --------------------------------------------------------- top-k selection
+SELECT_WORKLOADS = {"select_decode": ("gqa_decode", 64), "select_prefill": ("shared_prefill", 128)}
+
+
+def select_visible_keys(w):
+    """Sum over (token, kv head) rows of the positions their blocks are
+    scored over (p < L, and p <= pos(t) when causal): the dot products."""
+    n = 0
+    for s in range(w.num_seqs):
+        L = int(w.used_kv_lens[s])
+        t0, t1 = int(w.cu_seqlens_q[s]), int(w.cu_seqlens_q[s + 1])
+        for i in range(t1 - t0):
+            n += min(L, L - (t1 - t0) + i + 1) if w.causal else L
+    return n * w.num_kv_heads
+
+
+def select_oracle_step(w, dim):
+    """One pass of the oracle's selection over 32 rows of a few sequences (a
+    compact copy of their index pages): (step callable, rows, description)."""
+    import oracle
+    rng = np.random.default_rng(1)
+    seqs = sorted(rng.choice(w.num_seqs, size=min(4, w.num_seqs), replace=False).tolist())
+    pages = sorted({int(p) for s in seqs for p in w.block_tables[s] if p >= 0})
+    remap = {p: i for i, p in enumerate(pages)}
+    bt = np.full_like(w.block_tables, -1)
+    for s in seqs:
+        for j, p in enumerate(w.block_tables[s]):
+            if p >= 0:
+                bt[s, j] = remap[int(p)]
+    ikc = w.idx_cache_pages(dim, np.array(pages), _gen_device())
+    iq = w.idx_q(dim)
+    prob = oracle.problem_for(w)
+    prob.num_pages = len(pages)
+    rows = np.concatenate([np.arange(w.cu_seqlens_q[s] * w.num_kv_heads, w.cu_seqlens_q[s + 1] * w.num_kv_heads)
+                           for s in seqs])
+    rows = np.sort(rng.choice(rows, size=min(len(rows), 32), replace=False))
+    nthreads = os.cpu_count() or 1
+
+    def step():
+        oracle.select_blocks(prob, dim, iq, ikc, bt, w.cu_seqlens_q, w.used_kv_lens, rows=rows, nthreads=nthreads)
+    return step, len(rows), f"{len(rows)} (token, kv head) rows of sequences {seqs} on {nthreads} threads"
+
+
+def select_oracle_sample(w, dim, budget_s):
+    """The oracle's selection sample, repeated for about budget_s seconds."""
+    step, nrows, what = select_oracle_step(w, dim)
+    t0, reps = time.time(), 0
+    while time.time() - t0 < budget_s or reps == 0:
+        step()
+        reps += 1
+    dt = time.time() - t0
+    return {"value": nrows * reps / w.num_kv_heads / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1,
+            "kind": "oracle", "sample": f"{what}, {reps} passes, {dt:.1f} s; tokens/s = rows / Hkv / time"}
+
+
+def run_reference_select(args, world):
+    """The reference arm of the selection workloads: the oracle's selection
+    of 32 rows per step on the host cores."""
+    base, dim = SELECT_WORKLOADS[args.workload]
+    w = load_workload(base, 0)
+    step, nrows, what = select_oracle_step(w, dim)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    total = time.perf_counter() - t0
+    value = nrows / w.num_kv_heads * args.steps / total
+    line = {"impl": "reference", "metric": "top-k block selection tokens/s vs roofline, 1 GB300", "value": value,
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 scores", "data": "synthetic",
+            "config": {"workload": args.workload, "shape_of": base, "index_dim": dim},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+                             "sample": what + " per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_select(args, rank, world, local_rank):
+    """--workload select_decode | select_prefill: the top-k block selection
+    (mxsa_select_blocks) on the gqa_decode shape with 64-dim index keys, or
+    the shared_prefill shape with 128-dim index keys (bf16, one index head
+    per kv head).  value = tokens/s.  select_decode is HBM-bound (the index
+    cache is read once); select_prefill is bound by the CUDA-core FP32 FMAs
+    the exact scores take (alu)."""
+    import block_sparse_attention_builder_gb300 as mx
+    from block_sparse_attention_builder_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    base, dim = SELECT_WORKLOADS[args.workload]
+    w = load_workload(base, rank)
+    iq, ik = w.idx_q(dim, dev), w.idx_cache(dim, dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
+    lens = torch.from_numpy(w.used_kv_lens).to(dev)
+    prob = mx.make_problem(w.num_seqs, w.total_q, w.num_q_heads, w.num_kv_heads, w.topk, w.page_size, w.num_pages,
+                           w.max_pages_per_seq, w.causal, 0.0, torch.bfloat16, torch.bfloat16)
+    sel = torch.empty(w.total_q, w.num_kv_heads, w.topk, dtype=torch.int32, device=dev)
+    ws = torch.empty(mx.select_workspace_size(prob, dim), dtype=torch.uint8, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        mx.select_blocks(prob, iq, ik, bt, cu, lens, sel=sel, score_ws=ws, flags=flags, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
+    ms = total_ms / args.steps
+    if int(flags.item()):
+        raise RuntimeError(f"selection flagged {int(flags.item()):#x}")
+    # end to end: the index queries from pinned host memory, the selections back
+    h_iq = iq.cpu().pin_memory()
+    h_sel = torch.empty(sel.shape, dtype=sel.dtype).pin_memory()
+    d_iq = torch.empty_like(iq)
+    e2e_ms, reps = 0.0, max(3, args.steps // 2)
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        d_iq.copy_(h_iq, non_blocking=True)
+        mx.select_blocks(prob, d_iq, ik, bt, cu, lens, sel=sel, score_ws=ws, flags=flags, stream=stream)
+        h_sel.copy_(sel, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= reps
+    peaks = measured_peaks()
+    visible = select_visible_keys(w)
+    cache_bytes = sum(int(w.used_kv_lens[s]) for s in range(w.num_seqs)) * w.num_kv_heads * dim * 2
+    nbm = (w.max_pages_per_seq * w.page_size + 127) // 128
+    io_bytes = iq.numel() * 2 + sel.numel() * 4 + 2 * w.total_q * w.num_kv_heads * nbm * 4
+    if args.workload == "select_decode":
+        gbs = (cache_bytes + io_bytes) / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "k_select_score + k_select_topk",
+                "algorithmic_bytes_per_launch": cache_bytes + io_bytes,
+                "peak_source": peaks["src"] + " copy bandwidth"}
+    else:
+        fl = 2.0 * visible * dim
+        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 FLOP per FMA x max SM clock
+        tf = fl / (ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                "traffic": None, "kernel": "k_select_score + k_select_topk", "algorithmic_flops_per_launch": fl,
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (FP32 FMA on CUDA cores)"}
+    line = {
+        "metric": "top-k block selection tokens/s vs roofline, 1 GB300", "value": w.total_q * world / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 scores",
+        "data": "synthetic (seeded counter-based N(0,1) index queries and keys)",
+        "config": {"workload": args.workload, "shape_of": base, "index_dim": dim, "num_seqs": w.num_seqs,
+                   "total_q": w.total_q, "num_kv_heads": w.num_kv_heads, "topk": w.topk, "page_size": w.page_size,
+                   "causal": bool(w.causal), "dot_products": visible,
+                   "l2": "flushed between timed steps (256 MiB write)"},
+        "bytes": {"index_cache": cache_bytes, "io": io_bytes}, "roofline": roof,
+        "e2e": {"value": w.total_q / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": iq.numel() * 2,
+                "d2h_bytes_per_step": sel.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = select_oracle_sample(w, dim, 8.0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -771,7 +956,8 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="'all' (default): the five sparse workloads in one line, headline skewed_decode; "
-                         "or one of " + ", ".join(list(SPARSE_WORKLOADS) + ["kv_store", "dense_prefill"]))
+                         "or one of " + ", ".join(list(SPARSE_WORKLOADS) + ["kv_store", "dense_prefill"] +
+                                                  list(SELECT_WORKLOADS)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--plan", default="fused", choices=["fused", "separate"],
                     help="index + schedule in one launch (mxsa_plan, default) or as mxsa_build_index then "
@@ -796,8 +982,9 @@ def main():
             dist.destroy_process_group()
         return
 
-    if args.workload in ("kv_store", "dense_prefill"):
-        (run_store if args.workload == "kv_store" else run_dense)(args, rank, world, local_rank)
+    if args.workload in ("kv_store", "dense_prefill") or args.workload in SELECT_WORKLOADS:
+        run = {"kv_store": run_store, "dense_prefill": run_dense}.get(args.workload, run_select)
+        run(args, rank, world, local_rank)
         if world > 1:
             torch.distributed.destroy_process_group()
         return

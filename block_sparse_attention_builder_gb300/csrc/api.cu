@@ -402,8 +402,7 @@ mxsa_status mxsa_select_workspace_size(const mxsa_problem* problem, int32_t idx_
   if (!problem || !score_bytes) return MXSA_ERR_INVALID_ARG;
   mxsa_status s = validate_select(*problem, idx_dim);
   if (s != MXSA_OK) return s;
-  *score_bytes = align_up(select_score_bytes(*problem));
-  if (*score_bytes == 0) *score_bytes = kAlign;
+  *score_bytes = select_workspace_bytes(*problem);
   return MXSA_OK;
 }
 
@@ -420,9 +419,9 @@ mxsa_status mxsa_select_blocks(const mxsa_problem* problem, int32_t idx_dim, con
   if (!aligned(idx_q, 16) || !aligned(idx_cache, 16) || !aligned(block_tables, 4) || !aligned(cu_seqlens_q, 8) ||
       !aligned(used_kv_lens, 4) || !aligned(score_ws, 16) || !aligned(sel, 4) || !aligned(device_flags, 4))
     return MXSA_ERR_INVALID_ARG;
-  if (score_bytes < select_score_bytes(p)) return MXSA_ERR_WORKSPACE;
-  cudaError_t e = launch_select(p, idx_dim, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_lens,
-                                static_cast<float*>(score_ws), sel, device_flags, static_cast<cudaStream_t>(stream));
+  if (score_bytes < select_workspace_bytes(p)) return MXSA_ERR_WORKSPACE;
+  cudaError_t e = launch_select(p, idx_dim, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_lens, score_ws,
+                                sel, device_flags, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
 }
 

@@ -136,8 +136,9 @@ cudaError_t launch_store(const mxsa_problem& p, long long n, const int64_t* loc,
                          void* k_cache, void* v_cache, const void* idx_k, void* idx_cache, int idx_heads,
                          int idx_dim, int32_t* flags, cudaStream_t st);
 size_t select_score_bytes(const mxsa_problem& p);
+size_t select_workspace_bytes(const mxsa_problem& p);
 cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, const void* ik, const int32_t* bt,
-                          const int64_t* cu, const int32_t* lens, float* score, int32_t* sel, int32_t* flags,
+                          const int64_t* cu, const int32_t* lens, void* ws, int32_t* sel, int32_t* flags,
                           cudaStream_t st);
 cudaError_t launch_combine(const mxsa_problem& p, const IndexPtrs& ix, const void* part_o,
                            const float* part_lse, void* out, float* lse, cudaStream_t st);

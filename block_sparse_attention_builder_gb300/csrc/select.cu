@@ -13,15 +13,21 @@
 // arithmetic (CUDA-core FMAs in dimension order, exact maxima and an exact
 // sort); the result is bit-identical to a plain CPU statement of it.
 //
-// Two launches:
-//   k_select_score  persistent CTAs of 128 threads over work units (sequence,
-//                   block, kv head, query chunk).  A sequence with at most 8
-//                   new tokens: thread p holds key 128 b + p and the block's
-//                   maximum per query comes from a CTA reduction (the index
-//                   keys are read once, the HBM-bound decode case).  Longer
-//                   sequences: the block's keys are staged in shared memory
-//                   as FP32 and thread i owns query i of a 128-query chunk,
-//                   walking the block's keys itself (no reduction).
+// Four launches, chained by programmatic dependent launch:
+//   k_select_prep   one CTA: per sequence its clamped length, first token,
+//                   new tokens and blocks, and the exclusive prefixes of
+//                   the two kinds of work units (below), into the workspace.
+//   k_select_short  units (sequence, block, kv head) of the sequences with at
+//                   most 8 new tokens: the block's key rows are staged in
+//                   shared memory by coalesced 16-byte loads, thread p walks
+//                   row p and the block's maximum per query comes from a CTA
+//                   reduction.  The index keys are read once: this is the
+//                   HBM-bound decode case, so the kernel keeps few registers
+//                   and little shared memory, for many CTAs per SM.
+//   k_select_long   units (sequence, block, kv head, 128-query chunk) of the
+//                   longer sequences: the block's keys are staged as FP32 and
+//                   thread i owns query i of the chunk, walking the keys four
+//                   at a time (four independent FMA chains, no reduction).
 //   k_select_topk   one CTA per (token, kv head) row: the row's block scores
 //                   become 64-bit keys (order-preserving score bits above the
 //                   complemented block index) in shared memory, sorted by a
@@ -39,10 +45,22 @@ namespace mxsa {
 namespace {
 
 constexpr int kSelThreads = 128;
-constexpr int kSelSeqMax = 1024;     // sequences (the per-CTA table)
+constexpr int kPrepThreads = 1024;   // one sequence per thread
 constexpr int kSelMaxBlocks = 4096;  // blocks per sequence (the sort buffer)
-constexpr int kSelSmallTq = 8;       // at most this many new tokens: one thread per key
+constexpr int kSelSmallTq = 8;       // at most this many new tokens: the short form
 constexpr int kTopkThreads = 256;
+
+// The sequence table k_select_prep writes after the scores.
+struct SeqRec {
+  int32_t L, q0, tq, nblk;
+};
+
+struct SelTable {
+  SeqRec* seq;             // [B]
+  long long* unit_short;   // [B + 1] exclusive prefix of short units
+  long long* unit_long;    // [B + 1] exclusive prefix of long units
+  int32_t* bad;            // cu_seqlens_q is not a non-decreasing partition
+};
 
 struct SelArgs {
   const uint8_t* iq;        // [total_q][Hkv][D]
@@ -53,6 +71,7 @@ struct SelArgs {
   float* score;             // [total_q][Hkv][max_blocks]
   int32_t* sel;             // [total_q][Hkv][topk]
   int32_t* flags;           // may be null
+  SelTable tab;
   int32_t B, total_q, Hkv, D, ps, num_pages, max_pages, max_blocks, topk, causal, dtype;
 };
 
@@ -68,101 +87,172 @@ __device__ __forceinline__ float elem(const uint8_t* base, int64_t i, int dtype)
   return __half2float(__ushort_as_half(bits));
 }
 
-// Per-sequence table every CTA builds for itself: L (clamped), first token,
-// new tokens, blocks, and the exclusive prefix of work units.  Returns
-// false (uniform) when cu_seqlens_q is not a non-decreasing partition of
-// [0, total_q].
-struct SeqTable {
-  int32_t* L;
-  int32_t* q0;
-  int32_t* tq;
-  int32_t* nblk;
-  long long* unit0;  // [B + 1]
-};
+// The values of one 16-byte chunk, widened exactly to FP32 in dimension
+// order: 16 e4m3 values, or 8 of a 16-bit type.
+__device__ __forceinline__ void unpack_e4m3x16(uint4 v, float* out) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(w[i] >> (16 * h))));
+      const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h2));
+      out[4 * i + 2 * h] = f.x;
+      out[4 * i + 2 * h + 1] = f.y;
+    }
+  }
+}
 
-__device__ bool build_table(const SelArgs& a, SeqTable T, long long* total_units) {
+__device__ __forceinline__ void unpack_16bitx8(uint4 v, bool bf16, float* out) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (bf16) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      out[2 * i] = f.x;
+      out[2 * i + 1] = f.y;
+    }
+  }
+}
+
+// last s in [0, B) with prefix[s] <= v (prefix non-decreasing, prefix[0] = 0;
+// a sequence without units shares its start with the next one, which wins)
+__device__ __forceinline__ int unit_seq(const long long* prefix, int B, long long v) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) k_select_prep(SelArgs a) {
+  __shared__ long long s_part[2][kPrepThreads / 32];
   __shared__ int s_bad;
-  __shared__ long long s_part[kSelThreads];
-  if (threadIdx.x == 0) s_bad = (a.cu[0] != 0 || a.cu[a.B] != a.total_q) ? 1 : 0;
+  pdl_launch_dependents();
+  pdl_wait();  // the previous user of the workspace is done
+  const int s = threadIdx.x, lane = s & 31, warp = s >> 5;
+  if (s == 0) s_bad = (a.cu[0] != 0 || a.cu[a.B] != a.total_q) ? 1 : 0;
   __syncthreads();
-  const long long cap = (long long)a.max_pages * a.ps;
-  // each thread owns a contiguous run of sequences
-  const int per = (a.B + kSelThreads - 1) / kSelThreads;
-  const int s0 = threadIdx.x * per, s1 = min(a.B, s0 + per);
-  long long run = 0;
-  for (int s = s0; s < s1; ++s) {
+  long long nshort = 0, nlong = 0;
+  if (s < a.B) {
+    const long long cap = (long long)a.max_pages * a.ps;
     const long long c0 = a.cu[s], c1 = a.cu[s + 1];
     if (c1 < c0) s_bad = 1;
     long long L = a.lens[s];
     L = L < 0 ? 0 : (L > cap ? cap : L);
     const int tq = (int)(c1 > c0 ? c1 - c0 : 0);
     const int nb = (int)((L + 127) / 128);
-    T.L[s] = (int)L;
-    T.q0[s] = (int)c0;
-    T.tq[s] = tq;
-    T.nblk[s] = nb;
-    const int chunks = tq == 0 ? 0 : (tq <= kSelSmallTq ? 1 : (tq + kSelThreads - 1) / kSelThreads);
-    run += (long long)nb * chunks;
+    a.tab.seq[s] = SeqRec{(int)L, (int)c0, tq, nb};
+    if (tq >= 1 && tq <= kSelSmallTq) nshort = nb;
+    if (tq > kSelSmallTq) nlong = (long long)nb * ((tq + kSelThreads - 1) / kSelThreads);
   }
-  s_part[threadIdx.x] = run;
-  __syncthreads();
-  if (threadIdx.x == 0) {  // few values: a serial scan is enough
-    long long acc = 0;
-    for (int i = 0; i < kSelThreads; ++i) {
-      const long long v = s_part[i];
-      s_part[i] = acc;
-      acc += v;
+  // block-wide exclusive scans of both unit counts
+  long long is = nshort, il = nlong;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long xs = __shfl_up_sync(0xffffffffu, is, o), xl = __shfl_up_sync(0xffffffffu, il, o);
+    if (lane >= o) {
+      is += xs;
+      il += xl;
     }
-    *total_units = acc;
+  }
+  if (lane == 31) {
+    s_part[0][warp] = is;
+    s_part[1][warp] = il;
   }
   __syncthreads();
-  long long u = s_part[threadIdx.x];
-  for (int s = s0; s < s1; ++s) {
-    T.unit0[s] = u;
-    const int tq = T.tq[s];
-    const int chunks = tq == 0 ? 0 : (tq <= kSelSmallTq ? 1 : (tq + kSelThreads - 1) / kSelThreads);
-    u += (long long)T.nblk[s] * chunks;
+  if (s == 0) {
+    long long as = 0, al = 0;
+    for (int w = 0; w < kPrepThreads / 32; ++w) {
+      const long long vs = s_part[0][w], vl = s_part[1][w];
+      s_part[0][w] = as;
+      s_part[1][w] = al;
+      as += vs;
+      al += vl;
+    }
+    a.tab.unit_short[a.B] = as;
+    a.tab.unit_long[a.B] = al;
   }
-  if (threadIdx.x == kSelThreads - 1) T.unit0[a.B] = *total_units;
   __syncthreads();
-  return s_bad == 0;
+  if (s < a.B) {
+    a.tab.unit_short[s] = s_part[0][warp] + is - nshort;
+    a.tab.unit_long[s] = s_part[1][warp] + il - nlong;
+  }
+  if (s == 0) {
+    *a.tab.bad = s_bad;
+    if (s_bad) {  // nothing is scored: every row will be -1
+      a.tab.unit_short[a.B] = 0;
+      a.tab.unit_long[a.B] = 0;
+      if (a.flags) atomicOr(a.flags, MXSA_FLAG_CU);
+    }
+  }
+}
+
+// Dot products of one staged key row with the first tq (<= NQ) queries,
+// each summed by fused multiply-adds in dimension order.
+template <int NQ, int D>
+__device__ __forceinline__ void short_dots(const uint8_t* row, const float* qs, int dtype, float* acc, int tq = NQ) {
+  if (dtype == MXSA_FP8_E4M3) {
+#pragma unroll 2
+    for (int cc = 0; cc < D / 16; ++cc) {
+      float kd[16];
+      unpack_e4m3x16(*reinterpret_cast<const uint4*>(row + cc * 16), kd);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+#pragma unroll
+        for (int i = 0; i < NQ; ++i)
+          if (i < tq) acc[i] = __fmaf_rn(qs[i * D + cc * 16 + e], kd[e], acc[i]);
+    }
+  } else {
+    const bool bf16 = dtype == MXSA_BF16;
+#pragma unroll 2
+    for (int cc = 0; cc < D / 8; ++cc) {
+      float kd[8];
+      unpack_16bitx8(*reinterpret_cast<const uint4*>(row + cc * 16), bf16, kd);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int i = 0; i < NQ; ++i)
+          if (i < tq) acc[i] = __fmaf_rn(qs[i * D + cc * 8 + e], kd[e], acc[i]);
+    }
+  }
+}
+
+// shared memory of k_select_short: 8 FP32 queries, then 128 raw key rows
+// padded by 16 bytes (each thread reads its own row without bank conflicts)
+__host__ __device__ constexpr size_t short_smem(int D, int esz) {
+  return (size_t)kSelSmallTq * D * sizeof(float) + (size_t)kSelThreads * (D * esz + 16);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kSelThreads)
-    k_select_score(SelArgs a) {
+    k_select_short(SelArgs a) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
-  __shared__ int32_t tL[kSelSeqMax], tq0[kSelSeqMax], ttq[kSelSeqMax], tnb[kSelSeqMax];
-  __shared__ long long tu0[kSelSeqMax + 1];
-  __shared__ long long s_total;
   __shared__ float red_max[kSelSmallTq][kSelThreads / 32];
   __shared__ int red_have[kSelSmallTq][kSelThreads / 32];
+  pdl_wait();  // the sequence table
+  // only now: k_select_long reads the table without a wait of its own
   pdl_launch_dependents();
-  pdl_wait();
-  const SeqTable T{tL, tq0, ttq, tnb, tu0};
-  if (!build_table(a, T, &s_total)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0 && a.flags) atomicOr(a.flags, MXSA_FLAG_CU);
-    return;
-  }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = a.Hkv;
-  float* kf = reinterpret_cast<float*>(sm_raw);              // [128][D] keys (long sequences)
-  float* qs = kf;                                             // [8][D] queries (short sequences)
-  int* kvis = reinterpret_cast<int*>(kf + kSelThreads * D);  // [128]: key p visible (length, page)
-  const long long units = s_total * Hkv;
+  const int esz = a.dtype == MXSA_FP8_E4M3 ? 1 : 2;
+  const int row_bytes = D * esz + 16;
+  float* qs = reinterpret_cast<float*>(sm_raw);                      // [8][D]
+  uint8_t* kst = sm_raw + kSelSmallTq * D * sizeof(float);           // [128][row_bytes]
+  const long long units = a.tab.unit_short[a.B] * Hkv;
   for (long long u = blockIdx.x; u < units; u += gridDim.x) {
     const int g = (int)(u % Hkv);
     const long long v = u / Hkv;
-    int lo = 0, hi = a.B - 1;  // last s with unit0[s] <= v
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (tu0[mid] <= v) lo = mid;
-      else hi = mid - 1;
-    }
-    const int s = lo;
-    const int nb = tnb[s], tq = ttq[s], L = tL[s], q0 = tq0[s];
-    const long long w = v - tu0[s];
-    const int b = (int)(w % nb), chunk = (int)(w / nb);
+    const int s = unit_seq(a.tab.unit_short, a.B, v);
+    const SeqRec r = a.tab.seq[s];
+    const int b = (int)(v - a.tab.unit_short[s]);
+    const int tq = r.tq, L = r.L, q0 = r.q0;
     // this thread's key position and whether it is on a valid page
     const int p = 128 * b + tid;
     int page = -1;
@@ -170,104 +260,171 @@ __global__ void __launch_bounds__(kSelThreads)
       page = a.bt[(long long)s * a.max_pages + p / a.ps];
       if (page < 0 || page >= a.num_pages) page = -1;
     }
-    const long long kbase = (((long long)(page < 0 ? 0 : page) * Hkv + g) * a.ps + p % a.ps) * D;
-    if (tq <= kSelSmallTq) {
-      // ---- one thread per key; the block maximum of each query by reduction
-      __syncthreads();  // the previous unit's shared memory is free
-      for (int i = tid; i < tq * D; i += kSelThreads)
-        qs[i] = elem(a.iq, ((long long)(q0 + i / D) * Hkv + g) * D + i % D, a.dtype);
-      __syncthreads();
-      float best[kSelSmallTq];
-      int have[kSelSmallTq];
+    __syncthreads();  // the previous unit's shared memory is free
+    for (int i = tid; i < tq * D; i += kSelThreads)
+      qs[i] = elem(a.iq, ((long long)(q0 + i / D) * Hkv + g) * D + i % D, a.dtype);
+    const int chunks_row = D * esz / 16;  // 16-byte chunks per key row
+    for (int c = tid; c < kSelThreads * chunks_row; c += kSelThreads) {
+      const int rr = c / chunks_row, cc = c % chunks_row;
+      const int key = 128 * b + rr;
+      if (key >= L) continue;
+      const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
+      if (pg < 0 || pg >= a.num_pages) continue;
+      const uint4 x = __ldcs(
+          reinterpret_cast<const uint4*>(a.ik + ((((long long)pg * Hkv + g) * a.ps + key % a.ps) * D) * esz) + cc);
+      *reinterpret_cast<uint4*>(kst + rr * row_bytes + cc * 16) = x;
+    }
+    __syncthreads();
+    float best[kSelSmallTq];
+    int have[kSelSmallTq];
+#pragma unroll
+    for (int i = 0; i < kSelSmallTq; ++i) {
+      best[i] = -INFINITY;
+      have[i] = 0;
+    }
+    if (page >= 0) {
+      float acc[kSelSmallTq];
+#pragma unroll
+      for (int i = 0; i < kSelSmallTq; ++i) acc[i] = 0.f;
+      const uint8_t* row = kst + tid * row_bytes;
+      if (tq == 1)
+        short_dots<1, D>(row, qs, a.dtype, acc);
+      else
+        short_dots<kSelSmallTq, D>(row, qs, a.dtype, acc, tq);
 #pragma unroll
       for (int i = 0; i < kSelSmallTq; ++i) {
-        best[i] = -INFINITY;
-        have[i] = 0;
-      }
-      if (page >= 0) {
-        float acc[kSelSmallTq];
-#pragma unroll
-        for (int i = 0; i < kSelSmallTq; ++i) acc[i] = 0.f;
-#pragma unroll 4
-        for (int d = 0; d < D; ++d) {
-          const float kd = elem(a.ik, kbase + d, a.dtype);
-#pragma unroll
-          for (int i = 0; i < kSelSmallTq; ++i)
-            if (i < tq) acc[i] = __fmaf_rn(qs[i * D + d], kd, acc[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < kSelSmallTq; ++i) {
-          const int pos = L - tq + i;
-          const bool vis = i < tq && (!a.causal || p <= pos) && !isnan(acc[i]);
-          if (vis) {
-            best[i] = acc[i];
-            have[i] = 1;
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kSelSmallTq; ++i) {
-        if (i >= tq) break;
-        float m = best[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const int h = __any_sync(0xffffffffu, have[i]);
-        if (lane == 0) {
-          red_max[i][warp] = m;
-          red_have[i][warp] = h;
-        }
-      }
-      __syncthreads();
-      if (tid < tq) {
-        float m = -INFINITY;
-        int h = 0;
-        for (int w2 = 0; w2 < kSelThreads / 32; ++w2) {
-          m = fmaxf(m, red_max[tid][w2]);
-          h |= red_have[tid][w2];
-        }
-        a.score[((long long)(q0 + tid) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
-      }
-    } else {
-      // ---- one thread per query of the chunk; the block's keys in shared
-      // memory as FP32 (exact widening), with their visibility
-      __syncthreads();
-      for (int i = tid; i < kSelThreads * D; i += kSelThreads) {
-        const int pp = i / D, d = i % D;
-        const int key = 128 * b + pp;
-        float x = 0.f;
-        if (key < L) {
-          const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
-          if (pg >= 0 && pg < a.num_pages) x = elem(a.ik, (((long long)pg * Hkv + g) * a.ps + key % a.ps) * D + d, a.dtype);
-        }
-        kf[i] = x;
-      }
-      kvis[tid] = page >= 0 ? 1 : 0;
-      __syncthreads();
-      const int i = chunk * kSelThreads + tid;  // this thread's query of the sequence
-      if (i < tq) {
-        float q[D];
-        const long long qb = ((long long)(q0 + i) * Hkv + g) * D;
-#pragma unroll
-        for (int d = 0; d < D; ++d) q[d] = elem(a.iq, qb + d, a.dtype);
         const int pos = L - tq + i;
-        int lim = min(128, L - 128 * b);
-        if (a.causal) lim = min(lim, pos - 128 * b + 1);
-        float m = -INFINITY;
-        int h = 0;
-        for (int pp = 0; pp < lim; ++pp) {
-          if (!kvis[pp]) continue;
-          const float* kr = kf + pp * D;
-          float acc = 0.f;
-#pragma unroll
-          for (int d = 0; d < D; ++d) acc = __fmaf_rn(q[d], kr[d], acc);
-          if (isnan(acc)) continue;
-          if (!h || acc > m) m = acc;
-          h = 1;
+        const bool vis = i < tq && (!a.causal || p <= pos) && !isnan(acc[i]);
+        if (vis) {
+          best[i] = acc[i];
+          have[i] = 1;
         }
-        a.score[((long long)(q0 + i) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
       }
     }
+#pragma unroll
+    for (int i = 0; i < kSelSmallTq; ++i) {
+      if (i >= tq) break;
+      float m = best[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const int h = __any_sync(0xffffffffu, have[i]);
+      if (lane == 0) {
+        red_max[i][warp] = m;
+        red_have[i][warp] = h;
+      }
+    }
+    __syncthreads();
+    if (tid < tq) {
+      float m = -INFINITY;
+      int h = 0;
+      for (int w2 = 0; w2 < kSelThreads / 32; ++w2) {
+        m = fmaxf(m, red_max[tid][w2]);
+        h |= red_have[tid][w2];
+      }
+      a.score[((long long)(q0 + tid) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
+    }
   }
+}
+
+// shared memory of k_select_long: the block's keys as FP32 and their
+// visibility
+__host__ __device__ constexpr size_t long_smem(int D) {
+  return (size_t)kSelThreads * D * sizeof(float) + kSelThreads * sizeof(int);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSelThreads)
+    k_select_long(SelArgs a) {
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  // Let through once every k_select_short CTA has passed its wait for the
+  // table, so the table is complete; this launch waits for k_select_short
+  // itself only at its end (k_select_topk waits on this launch).
+  pdl_launch_dependents();
+  const int tid = threadIdx.x;
+  const int Hkv = a.Hkv;
+  float* kf = reinterpret_cast<float*>(sm_raw);              // [128][D]
+  int* kvis = reinterpret_cast<int*>(kf + kSelThreads * D);  // [128]
+  const long long units = a.tab.unit_long[a.B] * Hkv;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int g = (int)(u % Hkv);
+    const long long v = u / Hkv;
+    const int s = unit_seq(a.tab.unit_long, a.B, v);
+    const SeqRec r = a.tab.seq[s];
+    const long long w = v - a.tab.unit_long[s];
+    const int b = (int)(w % r.nblk), chunk = (int)(w / r.nblk);
+    const int tq = r.tq, L = r.L, q0 = r.q0;
+    __syncthreads();  // the previous unit's shared memory is free
+    for (int i = tid; i < kSelThreads * D; i += kSelThreads) {
+      const int pp = i / D, d = i % D;
+      const int key = 128 * b + pp;
+      float x = 0.f;
+      if (key < L) {
+        const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
+        if (pg >= 0 && pg < a.num_pages) x = elem(a.ik, (((long long)pg * Hkv + g) * a.ps + key % a.ps) * D + d, a.dtype);
+      }
+      kf[i] = x;
+    }
+    {
+      const int key = 128 * b + tid;
+      int ok = 0;
+      if (key < L) {
+        const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
+        ok = pg >= 0 && pg < a.num_pages;
+      }
+      kvis[tid] = ok;
+    }
+    __syncthreads();
+    const int i = chunk * kSelThreads + tid;  // this thread's query of the sequence
+    if (i < tq) {
+      float q[D];
+      const long long qb = ((long long)(q0 + i) * Hkv + g) * D;
+#pragma unroll
+      for (int d = 0; d < D; ++d) q[d] = elem(a.iq, qb + d, a.dtype);
+      const int pos = L - tq + i;
+      int lim = min(128, L - 128 * b);
+      if (a.causal) lim = min(lim, pos - 128 * b + 1);
+      float m = -INFINITY;
+      int h = 0;
+      // four keys per pass: four independent FMA chains, each summed in
+      // dimension order
+      for (int pp = 0; pp < lim; pp += 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4* k0 = reinterpret_cast<const float4*>(kf + (pp + 0) * D);
+        const float4* k1 = reinterpret_cast<const float4*>(kf + min(pp + 1, 127) * D);
+        const float4* k2 = reinterpret_cast<const float4*>(kf + min(pp + 2, 127) * D);
+        const float4* k3 = reinterpret_cast<const float4*>(kf + min(pp + 3, 127) * D);
+#pragma unroll
+        for (int d4 = 0; d4 < D / 4; ++d4) {
+          const float4 a0 = k0[d4], a1 = k1[d4], a2 = k2[d4], a3 = k3[d4];
+          acc[0] = __fmaf_rn(q[4 * d4], a0.x, acc[0]);
+          acc[1] = __fmaf_rn(q[4 * d4], a1.x, acc[1]);
+          acc[2] = __fmaf_rn(q[4 * d4], a2.x, acc[2]);
+          acc[3] = __fmaf_rn(q[4 * d4], a3.x, acc[3]);
+          acc[0] = __fmaf_rn(q[4 * d4 + 1], a0.y, acc[0]);
+          acc[1] = __fmaf_rn(q[4 * d4 + 1], a1.y, acc[1]);
+          acc[2] = __fmaf_rn(q[4 * d4 + 1], a2.y, acc[2]);
+          acc[3] = __fmaf_rn(q[4 * d4 + 1], a3.y, acc[3]);
+          acc[0] = __fmaf_rn(q[4 * d4 + 2], a0.z, acc[0]);
+          acc[1] = __fmaf_rn(q[4 * d4 + 2], a1.z, acc[1]);
+          acc[2] = __fmaf_rn(q[4 * d4 + 2], a2.z, acc[2]);
+          acc[3] = __fmaf_rn(q[4 * d4 + 2], a3.z, acc[3]);
+          acc[0] = __fmaf_rn(q[4 * d4 + 3], a0.w, acc[0]);
+          acc[1] = __fmaf_rn(q[4 * d4 + 3], a1.w, acc[1]);
+          acc[2] = __fmaf_rn(q[4 * d4 + 3], a2.w, acc[2]);
+          acc[3] = __fmaf_rn(q[4 * d4 + 3], a3.w, acc[3]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kp = pp + j;
+          if (kp >= lim || !kvis[kp] || isnan(acc[j])) continue;
+          if (!h || acc[j] > m) m = acc[j];
+          h = 1;
+        }
+      }
+      a.score[((long long)(q0 + i) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
+    }
+  }
+  pdl_wait();  // leave only after k_select_short has completed
 }
 
 // Order-preserving 64-bit key of (score, block): larger = earlier in the
@@ -282,32 +439,23 @@ __device__ __forceinline__ unsigned long long rank_key(float x, int b) {
 __global__ void __launch_bounds__(kTopkThreads)
     k_select_topk(SelArgs a) {
   __shared__ unsigned long long key[kSelMaxBlocks];
-  __shared__ int s_bad;
   pdl_launch_dependents();
   pdl_wait();  // the block scores are complete
-  if (threadIdx.x == 0) s_bad = (a.cu[0] != 0 || a.cu[a.B] != a.total_q) ? 1 : 0;
-  __syncthreads();
-  for (int s = threadIdx.x; s < a.B; s += blockDim.x)
-    if (a.cu[s + 1] < a.cu[s]) s_bad = 1;
-  __syncthreads();
-  const bool bad = s_bad != 0;
+  const bool bad = *a.tab.bad != 0;
   const long long rows = (long long)a.total_q * a.Hkv;
-  const long long cap = (long long)a.max_pages * a.ps;
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const int t = (int)(row / a.Hkv);
     int32_t* out = a.sel + row * a.topk;
     int nb = 0;
     if (!bad) {
-      int lo = 0, hi = a.B - 1;  // the sequence of token t: last s with cu[s] <= t ...
+      int lo = 0, hi = a.B - 1;  // the sequence of token t: the last s with q0 <= t
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.cu[mid] <= t) lo = mid;
+        if (a.tab.seq[mid].q0 <= t) lo = mid;
         else hi = mid - 1;
       }
-      while (lo < a.B - 1 && a.cu[lo + 1] <= t) ++lo;  // ... skipping empty sequences
-      long long L = a.lens[lo];
-      L = L < 0 ? 0 : (L > cap ? cap : L);
-      if (t >= a.cu[lo] && t < a.cu[lo + 1]) nb = (int)((L + 127) / 128);
+      const SeqRec r = a.tab.seq[lo];
+      if (t >= r.q0 && t < r.q0 + r.tq) nb = r.nblk;
     }
     int n2 = 1;
     while (n2 < nb) n2 <<= 1;
@@ -343,17 +491,24 @@ __global__ void __launch_bounds__(kTopkThreads)
       out[k] = kk ? (int32_t)(0xffffffffu - (uint32_t)(kk & 0xffffffffu)) : -1;
     }
   }
-  if (bad && blockIdx.x == 0 && threadIdx.x == 0 && a.flags) atomicOr(a.flags, MXSA_FLAG_CU);
 }
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
+// Workspace: the block scores, then the sequence table.
 size_t select_score_bytes(const mxsa_problem& p) {
   return (size_t)p.total_q * p.num_kv_heads * (size_t)max_blocks_per_seq(p) * sizeof(float);
 }
 
+size_t select_workspace_bytes(const mxsa_problem& p) {
+  const size_t B = (size_t)p.num_seqs;
+  return align256(select_score_bytes(p)) + align256(B * sizeof(SeqRec)) + 2 * align256((B + 1) * 8) + 256;
+}
+
 cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, const void* ik,
-                          const int32_t* bt, const int64_t* cu, const int32_t* lens, float* score, int32_t* sel,
+                          const int32_t* bt, const int64_t* cu, const int32_t* lens, void* ws, int32_t* sel,
                           int32_t* flags, cudaStream_t st) {
   if ((long long)p.total_q * p.num_kv_heads == 0) return cudaSuccess;
   SelArgs a;
@@ -362,7 +517,16 @@ cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, co
   a.bt = bt;
   a.cu = cu;
   a.lens = lens;
-  a.score = score;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.score = reinterpret_cast<float*>(w);
+  size_t o = align256(select_score_bytes(p));
+  a.tab.seq = reinterpret_cast<SeqRec*>(w + o);
+  o += align256((size_t)p.num_seqs * sizeof(SeqRec));
+  a.tab.unit_short = reinterpret_cast<long long*>(w + o);
+  o += align256((size_t)(p.num_seqs + 1) * 8);
+  a.tab.unit_long = reinterpret_cast<long long*>(w + o);
+  o += align256((size_t)(p.num_seqs + 1) * 8);
+  a.tab.bad = reinterpret_cast<int32_t*>(w + o);
   a.sel = sel;
   a.flags = flags;
   a.B = p.num_seqs;
@@ -379,17 +543,39 @@ cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, co
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t smem = (size_t)kSelThreads * idx_dim * sizeof(float) + kSelThreads * sizeof(int);
+  const int esz = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
   static cudaError_t attr_err = [] {
-    const int bytes = (int)((size_t)kSelThreads * 128 * sizeof(float) + kSelThreads * sizeof(int));
-    cudaError_t e = cudaFuncSetAttribute(k_select_score<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_select_score<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = cudaSuccess;
+    const void* k[4] = {(const void*)k_select_short<64>, (const void*)k_select_short<128>,
+                        (const void*)k_select_long<64>, (const void*)k_select_long<128>};
+    const size_t bytes[4] = {short_smem(64, 2), short_smem(128, 2), long_smem(64), long_smem(128)};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = cudaFuncSetAttribute(k[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes[i]);
     return e;
   }();
   if (attr_err != cudaSuccess) return attr_err;
-  cudaError_t e = idx_dim == 64 ? launch_pdl(k_select_score<64>, dim3(sms * 4), dim3(kSelThreads), smem, st, a)
-                                : launch_pdl(k_select_score<128>, dim3(sms * 4), dim3(kSelThreads), smem, st, a);
+  // persistent grids: as many CTAs as fit at once (a second, partial wave
+  // would start only when the first finishes)
+  auto grid_for = [&](const void* kern, size_t smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSelThreads, smem) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    return dim3((unsigned)(sms * per_sm));
+  };
+  cudaError_t e = launch_pdl(k_select_prep, dim3(1), dim3(kPrepThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
+  const size_t ss = short_smem(idx_dim, esz), sl = long_smem(idx_dim);
+  if (idx_dim == 64) {
+    e = launch_pdl(k_select_short<64>, grid_for((const void*)k_select_short<64>, ss), dim3(kSelThreads), ss, st, a);
+    if (e == cudaSuccess)
+      e = launch_pdl(k_select_long<64>, grid_for((const void*)k_select_long<64>, sl), dim3(kSelThreads), sl, st, a);
+  } else {
+    e = launch_pdl(k_select_short<128>, grid_for((const void*)k_select_short<128>, ss), dim3(kSelThreads), ss, st,
+                   a);
+    if (e == cudaSuccess)
+      e = launch_pdl(k_select_long<128>, grid_for((const void*)k_select_long<128>, sl), dim3(kSelThreads), sl, st,
+                     a);
+  }
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.total_q * p.num_kv_heads;
   const long long grid = rows < (long long)sms * 8 ? rows : (long long)sms * 8;

@@ -250,16 +250,16 @@ mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const i
  *   idx_q        device [total_q][Hkv][idx_dim] of kv_dtype
  *   idx_cache    device [num_pages][Hkv][page_size][idx_dim] of kv_dtype
  *   block_tables, cu_seqlens_q, used_kv_lens as for mxsa_build_index
- *   score_ws     device, score_bytes from mxsa_select_workspace_size: the
- *                block scores [total_q][Hkv][ceil(max_pages_per_seq *
+ *   score_ws     device, score_bytes from mxsa_select_workspace_size: first
+ *                the block scores [total_q][Hkv][ceil(max_pages_per_seq *
  *                page_size / 128)] FP32 (NaN: no score), kept for
- *                inspection; entries past a sequence's last block are not
- *                written
+ *                inspection (entries past a sequence's last block are not
+ *                written), then a per-sequence table
  *   sel          device int32 [total_q][Hkv][topk] (written)
  *   device_flags device int32 or NULL: MXSA_FLAG_CU when cu_seqlens_q is not
  *                a non-decreasing partition of total_q (then every row is -1)
  * idx_dim is 64 or 128; num_seqs <= 1024; at most 4096 blocks per sequence.
- * Two launches, asynchronous on `stream`; MXSA_ERR_INVALID_ARG /
+ * Four launches, asynchronous on `stream`; MXSA_ERR_INVALID_ARG /
  * MXSA_ERR_UNSUPPORTED / MXSA_ERR_WORKSPACE before any launch. */
 mxsa_status mxsa_select_workspace_size(const mxsa_problem* problem, int32_t idx_dim, size_t* score_bytes);
 mxsa_status mxsa_select_blocks(const mxsa_problem* problem, int32_t idx_dim, const void* idx_q,
