@@ -97,7 +97,7 @@ def _load():
         _lib.oracle_select_blocks.argtypes = [P, ctypes.c_int32, P, P, P, P, P, P, P, ctypes.c_int64, P,
                                               ctypes.c_int64, ctypes.c_int32]
         _lib.oracle_schedule.restype = ctypes.c_int
-        _lib.oracle_schedule.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32,
+        _lib.oracle_schedule.argtypes = [P, P, P, ctypes.c_int32, P, P, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, P, P, P, P, P, P, ctypes.c_int64, P]
     return _lib
 
@@ -296,6 +296,7 @@ def schedule(prob: OracleProblem, used_kv_lens, cu_seqlens_q, index: dict, rows_
     lens = _c(used_kv_lens, np.int32)
     cu = _c(cu_seqlens_q, np.int64)
     row_ptr = _c(index["row_ptr"], np.int32)
+    entries = _c(index["entries"], np.int32) if len(index["entries"]) else np.zeros(1, np.int32)
     cap = max(int(row_ptr[-1]) + 1, 1)
     items_n = np.zeros((cap, 4), dtype=np.int32)
     cost_n = np.zeros(cap + 1, dtype=np.int64)
@@ -304,7 +305,7 @@ def schedule(prob: OracleProblem, used_kv_lens, cu_seqlens_q, index: dict, rows_
     cost_d = np.zeros(cap + 1, dtype=np.int64)
     cta_d = np.zeros(num_ctas + 1, dtype=np.int32)
     counts = np.zeros(2, dtype=np.int64)
-    rc = lib.oracle_schedule(ctypes.byref(prob), _ptr(lens), _ptr(cu), index["nb"], _ptr(row_ptr),
+    rc = lib.oracle_schedule(ctypes.byref(prob), _ptr(lens), _ptr(cu), index["nb"], _ptr(row_ptr), _ptr(entries),
                              rows_per_item_tiles, decode_blocks, num_ctas, _ptr(items_n), _ptr(cost_n),
                              _ptr(cta_n), _ptr(items_d), _ptr(cost_d), _ptr(cta_d), ctypes.c_int64(cap),
                              _ptr(counts))

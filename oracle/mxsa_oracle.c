@@ -727,15 +727,20 @@ int oracle_select_blocks(const oracle_problem* p, int32_t dim, const void* iq, c
  *
  * Definition (exact, integer), keys with cnt > 0 taken in key order:
  *   G = Hq / Hkv;  a key (g, s, b) is a DECODE key when the sequence has
- *   exactly one new token (Tq_s == 1) and G <= 16; otherwise it is NORMAL.
+ *   exactly one new token (Tq_s == 1), G <= 16, and the key holds exactly
+ *   one entry, whose token is that one token of s; otherwise it is NORMAL.
+ *   (In the plain index every key of such a sequence is a decode key; in
+ *   the deduplicated index a key owned by s may hold other sequences'
+ *   entries, or none of its own, and is then NORMAL.)
  *   NORMAL: E = rows_per_item_tiles * max(1, 128 / G) entries per item;
  *     n = ceil(cnt / E) items, item i covering entries
  *     [row_ptr[key] + i*cnt/n, row_ptr[key] + (i+1)*cnt/n);
  *     cost = 384 + valid_tokens(key) * kv_weight + tiles * 256 + rows * 3
  *     with tiles = ceil(entries / max(1, 128 / G)), rows = entries * G
  *     (the leading 384 is the item's fixed stage turnover).
- *   DECODE: a run is a maximal sequence of consecutive active keys with the
- *     same (g, s) (all hold the same single entry: the one token of s);
+ *   DECODE: a run is a maximal sequence of consecutive active decode keys
+ *     with the same (g, s) (all hold the same single entry: the one token
+ *     of s);
  *     a run of len keys becomes n = ceil(len / decode_blocks) items, item i
  *     covering run positions [i*len/n, (i+1)*len/n);  item = {position of
  *     its first key in the active-key list, entry of that key, 1, nkeys};
@@ -776,8 +781,22 @@ static void partition(int64_t n_items, const int64_t* prefix, int32_t num_ctas, 
   }
 }
 
+/* the decode-key rule above, for the key at active position a */
+static int is_decode_key(const oracle_problem* p, const int32_t* lens, const int64_t* cu, int32_t nb,
+                         const int32_t* row_ptr, const int32_t* entries, int64_t key) {
+  const int32_t G = p->num_q_heads / p->num_kv_heads;
+  int32_t g, s;
+  int64_t b;
+  key_to_gsb(p, lens, nb, key, &g, &s, &b);
+  if (cu[s + 1] - cu[s] != 1 || G > 16) return 0;
+  if (row_ptr[key + 1] - row_ptr[key] != 1 && !MUT(21)) return 0; /* mutant 21: the entry count ignored */
+  const int64_t slot = entries[row_ptr[key]];
+  return slot / ((int64_t)p->num_kv_heads * p->topk) == cu[s];
+}
+
 int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t* cu, int32_t nb,
-                    const int32_t* row_ptr, int32_t rows_per_item_tiles, int32_t decode_blocks, int32_t num_ctas,
+                    const int32_t* row_ptr, const int32_t* entries, int32_t rows_per_item_tiles,
+                    int32_t decode_blocks, int32_t num_ctas,
                     int32_t* items_n, int64_t* cost_n, int32_t* cta_n, int32_t* items_d, int64_t* cost_d,
                     int32_t* cta_d, int64_t items_cap, int64_t* out_counts) {
   const int32_t Hkv = p->num_kv_heads;
@@ -801,8 +820,7 @@ int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t*
     int64_t b;
     key_to_gsb(p, lens, nb, active[a], &g, &s, &b);
     const int64_t L = seq_len_clamped(p, lens, s);
-    const int64_t Tq_s = cu[s + 1] - cu[s];
-    const int dec = Tq_s == 1 && G <= 16;
+    const int dec = is_decode_key(p, lens, cu, nb, row_ptr, entries, active[a]);
     if (!dec) {
       const int64_t key = active[a];
       const int64_t cnt = row_ptr[key + 1] - row_ptr[key];
@@ -821,15 +839,16 @@ int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t*
       }
       continue;
     }
-    /* decode: only the first key of a run emits; the run ends where (g, s) changes */
-    if (a > 0) {
+    /* decode: only the first key of a run emits; the run ends where (g, s)
+       changes or a key that is not a decode key comes */
+    if (a > 0 && is_decode_key(p, lens, cu, nb, row_ptr, entries, active[a - 1])) {
       int32_t g2, s2;
       int64_t b2;
       key_to_gsb(p, lens, nb, active[a - 1], &g2, &s2, &b2);
       if (g2 == g && s2 == s) continue;
     }
     int64_t len = 1;
-    while (a + len < n_active) {
+    while (a + len < n_active && is_decode_key(p, lens, cu, nb, row_ptr, entries, active[a + len])) {
       int32_t g2, s2;
       int64_t b2;
       key_to_gsb(p, lens, nb, active[a + len], &g2, &s2, &b2);

@@ -217,3 +217,31 @@ def test_block_owners_equal_brute_force(name):
     got = oracle.block_owners(oracle.problem_for(w), w.used_kv_lens, w.block_tables)
     assert got.tolist() == want
     assert any(o != s for o, s in zip(got, np.repeat(np.arange(w.num_seqs), nblk)))  # something is shared
+
+
+def test_schedule_of_a_dedup_index_worked_example():
+    """Hand-worked schedule of a deduplicated decode batch.  Two sequences of
+    one new token each, L = 512 (4 blocks), Hkv 1, G 16, page 128; sequence
+    1's blocks 0 and 1 sit on sequence 0's pages; both select blocks 0..3.
+    Dedup index (key = g*NB + blk_off[owner] + b, NB = 8):
+      key 0 (s0 b0): 2 entries (both tokens), key 1 (s0 b1): 2 entries,
+      key 2 (s0 b2): token 0, key 3 (s0 b3): token 0,
+      keys 4, 5 (s1 b0, b1): none, key 6 (s1 b2): token 1, key 7 (s1 b3): token 1.
+    Keys 0 and 1 hold two entries, so they are NORMAL (one item each);
+    keys 2, 3 and 6, 7 are decode keys forming two runs of two."""
+    prob = oracle.problem(2, 2, 16, 1, 4, 128, 8, 4, False)
+    bt = np.array([[0, 1, 2, 3], [0, 1, 6, 7]], dtype=np.int32)
+    lens = np.array([512, 512], dtype=np.int32)
+    cu = np.array([0, 1, 2], dtype=np.int64)
+    sel = np.array([[[0, 1, 2, 3]], [[3, 2, 1, 0]]], dtype=np.int32)
+    idx = oracle.build_index_dedup(prob, sel, cu, lens, bt)
+    # slots: token t, slot k -> t * 4 + k
+    assert list(idx["row_ptr"]) == [0, 2, 4, 5, 6, 6, 6, 7, 8]
+    assert list(idx["entries"]) == [0, 7, 1, 6, 2, 3, 5, 4]
+    sch = oracle.schedule(prob, lens, cu, idx, 4, 8, 2)
+    # normal: cost 384 + 128 * 2 (bf16) + 1 tile * 256 + 2 rows-of-16 * 3 = 992
+    assert sch["items"].tolist() == [[0, 0, 2, 0], [1, 2, 2, 0]]
+    assert sch["cost_prefix"].tolist() == [0, 992, 1984]
+    # decode: {active position, entry, 1, keys}; cost 2 * 64 + 256 + 2 * 128 * 2 = 896
+    assert sch["items_dec"].tolist() == [[2, 4, 1, 2], [4, 6, 1, 2]]
+    assert sch["cost_prefix_dec"].tolist() == [0, 896, 1792]

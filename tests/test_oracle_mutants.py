@@ -34,6 +34,7 @@ MUTANTS = {
     18: "selection hides the row's own causal position",
     19: "selection scores drop the last index dimension",
     20: "selection scores a block by its minimum",
+    21: "schedule treats a shared key of several entries as a decode key",
 }
 
 
