@@ -40,7 +40,7 @@ EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_b
             "mxsa_plan",
             "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
             "mxsa_sched_layout_query", "mxsa_store_kv", "mxsa_dense_fwd", "mxsa_select_workspace_size",
-            "mxsa_select_blocks"]
+            "mxsa_select_blocks", "mxsa_dedup_workspace_size", "mxsa_build_index_dedup"]
 
 
 class MxsaError(RuntimeError):
@@ -72,7 +72,8 @@ class IndexLayout(ctypes.Structure):
 
 class SchedLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("header", "items", "cost_prefix", "cta_ptr", "items_dec",
-                                               "cost_prefix_dec", "cta_ptr_dec", "cta_sums", "total")] + \
+                                               "cost_prefix_dec", "cta_ptr_dec", "cta_sums", "decode_bits",
+                                               "total")] + \
                [(n, ctypes.c_int64) for n in ("items_cap", "tiles_cap")]
 
 
@@ -100,6 +101,8 @@ def _load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "mxsa_dense_fwd": [P, P, P, P, P, P, P, P, P, P, P],
         "mxsa_select_workspace_size": [P, ctypes.c_int32, P],
         "mxsa_select_blocks": [P, ctypes.c_int32, P, P, P, P, P, P, S, P, P, P],
+        "mxsa_dedup_workspace_size": [P, P],
+        "mxsa_build_index_dedup": [P, P, P, P, P, P, S, P, S, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -206,6 +209,24 @@ def build_index(prob, sel, cu_seqlens_q, used_kv_lens, index_ws, stream=None):
     _check(_lib.mxsa_build_index(ctypes.byref(prob), _ptr(sel), _ptr(cu_seqlens_q), _ptr(used_kv_lens),
                                  _ptr(index_ws), index_ws.numel() * index_ws.element_size(), _stream(stream)),
            "mxsa_build_index")
+
+
+def dedup_workspace_size(prob: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mxsa_dedup_workspace_size(ctypes.byref(prob), ctypes.byref(n)), "mxsa_dedup_workspace_size")
+    return n.value
+
+
+def build_index_dedup(prob, sel, cu_seqlens_q, used_kv_lens, block_tables, index_ws, dedup_ws, stream=None):
+    """The index keyed by physical block: rows of sequences whose block
+    tables share a full block's pages at the same logical block meet in the
+    smallest such sequence's key (same workspace as build_index)."""
+    _need_attention("mxsa_build_index_dedup", prob, cu_seqlens_q=cu_seqlens_q, used_kv_lens=used_kv_lens, sel=sel,
+                    block_tables=block_tables)
+    _check(_lib.mxsa_build_index_dedup(ctypes.byref(prob), _ptr(sel), _ptr(cu_seqlens_q), _ptr(used_kv_lens),
+                                       _ptr(block_tables), _ptr(index_ws), index_ws.numel() * index_ws.element_size(),
+                                       _ptr(dedup_ws), dedup_ws.numel() * dedup_ws.element_size(), _stream(stream)),
+           "mxsa_build_index_dedup")
 
 
 def schedule(prob, index_ws, sched_ws, num_ctas=0, stream=None):
@@ -331,23 +352,37 @@ def allocate_workspaces(prob: Problem, device) -> Workspaces:
 class SparseAttention:
     """The four steps for one problem shape, with workspaces kept across calls."""
 
-    def __init__(self, prob: Problem, device="cuda", num_ctas: int = 0):
+    def __init__(self, prob: Problem, device="cuda", num_ctas: int = 0, dedup: bool = False):
         self.prob = prob
         self.device = torch.device(device)
         self.ws = allocate_workspaces(prob, self.device)
         self.num_ctas = num_ctas
+        # dedup: key the index by physical block (sequences sharing cached
+        # prefix pages load each shared block once); needs block_tables
+        self.dedup_ws = (torch.empty(dedup_workspace_size(prob), dtype=torch.uint8, device=self.device)
+                         if dedup else None)
 
     def __call__(self, q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, out=None,
                  lse=None, return_lse=True, stream=None):
         """All four steps.  out / lse may be pinned host tensors: the combine
         kernel then writes them directly (valid once the stream is synced)."""
-        self.prepare(selected, cu_seqlens_q, used_kv_lens, stream)
+        self.prepare(selected, cu_seqlens_q, used_kv_lens, stream, block_tables=block_tables)
         return self.attend(q, k_cache, v_cache, block_tables, out, lse, return_lse, stream)
 
-    def prepare(self, selected, cu_seqlens_q, used_kv_lens, stream=None):
-        """Index + schedule (one launch).  Needs only the selections and the
-        sequence lengths, so q and block_tables may still be in flight."""
-        plan(self.prob, selected, cu_seqlens_q, used_kv_lens, self.ws.index, self.ws.sched, self.num_ctas, stream)
+    def prepare(self, selected, cu_seqlens_q, used_kv_lens, stream=None, block_tables=None):
+        """Index + schedule.  The plain index needs only the selections and
+        the sequence lengths (one launch), so q and block_tables may still
+        be in flight; the dedup index also reads block_tables (two
+        launches: the dedup build, then the scheduler)."""
+        if self.dedup_ws is None:
+            plan(self.prob, selected, cu_seqlens_q, used_kv_lens, self.ws.index, self.ws.sched, self.num_ctas,
+                 stream)
+            return
+        if block_tables is None:
+            raise ValueError("the dedup index needs block_tables")
+        build_index_dedup(self.prob, selected, cu_seqlens_q, used_kv_lens, block_tables, self.ws.index,
+                          self.dedup_ws, stream)
+        schedule(self.prob, self.ws.index, self.ws.sched, self.num_ctas, stream)
 
     def attend(self, q, k_cache, v_cache, block_tables, out=None, lse=None, return_lse=True, stream=None):
         """Forward + combine over the last prepare()'s index and schedule."""
@@ -369,7 +404,7 @@ class SparseAttention:
 
 
 def kvouter_attention(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, page_size,
-                      causal=False, softmax_scale=None, return_lse=False, num_ctas=0, check=True):
+                      causal=False, softmax_scale=None, return_lse=False, num_ctas=0, check=True, dedup=False):
     """Block-sparse KV-outer attention with the README Quick-start call shape.
 
     q [Tq, Hq, 128] bf16/fp16; k_cache/v_cache [pages, Hkv, page_size, 128]
@@ -377,7 +412,8 @@ def kvouter_attention(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q,
     int32 [B, max_pages]; cu_seqlens_q int64 [B+1]; used_kv_lens int32 [B].
     Returns (output [Tq, Hq, 128], lse [Hq, Tq] float32 or None).  With
     check=True the device status word is read (one stream sync) and data
-    errors are raised.
+    errors are raised.  dedup=True keys the index by physical block, so
+    blocks shared through the block tables load once for all sequences.
     """
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("selected", selected),
                     ("block_tables", block_tables), ("cu_seqlens_q", cu_seqlens_q), ("used_kv_lens", used_kv_lens)):
@@ -395,7 +431,7 @@ def kvouter_attention(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q,
         raise ValueError("k_cache / v_cache shapes disagree with q or page_size")
     prob = make_problem(len(used_kv_lens), Tq, Hq, Hkv, selected.shape[2], page_size, pages,
                         block_tables.shape[1], causal, softmax_scale or 0.0, q.dtype, k_cache.dtype, head_dim=D)
-    attn = SparseAttention(prob, q.device, num_ctas)
+    attn = SparseAttention(prob, q.device, num_ctas, dedup=dedup)
     out, lse = attn(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, return_lse=return_lse)
     if check:
         flags = attn.status()

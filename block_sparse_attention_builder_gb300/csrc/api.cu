@@ -110,6 +110,7 @@ mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L) {
   L->cost_prefix_dec = o; o = align_up(o + (size_t)(L->items_cap + 1) * 8);
   L->cta_ptr_dec = o;     o = align_up(o + (size_t)(MXSA_MAX_CTAS + 1) * 4);
   L->cta_sums = o;        o = align_up(o + (size_t)kMaxCoopCtas * 16);
+  L->decode_bits = o;     o = align_up(o + (size_t)((act + 31) / 32) * 4);
   L->total = o;
   return MXSA_OK;
 }
@@ -163,7 +164,30 @@ SchedPtrs sched_ptrs(const mxsa_problem& p, void* ws) {
   x.cost_prefix_dec = reinterpret_cast<long long*>(b + L.cost_prefix_dec);
   x.cta_ptr_dec = reinterpret_cast<int32_t*>(b + L.cta_ptr_dec);
   x.cta_sums = reinterpret_cast<unsigned long long*>(b + L.cta_sums);
+  x.dk = reinterpret_cast<uint32_t*>(b + L.decode_bits);
   return x;
+}
+
+// Dedup scratch: the page array first (8-byte words), then the two block
+// arrays and the per-key counts.
+size_t dedup_workspace_bytes(const mxsa_problem& p) {
+  const int64_t nb_cap = (int64_t)p.num_seqs * max_blocks_per_seq(p);
+  return align_up((size_t)p.num_pages * 8) + 2 * align_up((size_t)nb_cap * 4) +
+         align_up((size_t)nb_cap * p.num_kv_heads * 4);
+}
+
+DedupPtrs dedup_ptrs(const mxsa_problem& p, void* ws) {
+  const int64_t nb_cap = (int64_t)p.num_seqs * max_blocks_per_seq(p);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  DedupPtrs d;
+  d.page_min = reinterpret_cast<unsigned long long*>(b);
+  b += align_up((size_t)p.num_pages * 8);
+  d.owner = reinterpret_cast<int32_t*>(b);
+  b += align_up((size_t)nb_cap * 4);
+  d.gsize = reinterpret_cast<int32_t*>(b);
+  b += align_up((size_t)nb_cap * 4);
+  d.own_count = reinterpret_cast<int32_t*>(b);
+  return d;
 }
 
 static mxsa_status resolve_ctas(int32_t num_ctas, int* out) {
@@ -233,6 +257,34 @@ mxsa_status mxsa_build_index(const mxsa_problem* problem, const int32_t* sel, co
   IndexPtrs ix = index_ptrs(*problem, index_ws);
   cudaError_t e = launch_build_index(*problem, sel, cu_seqlens_q, used_kv_lens, ix, L,
                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
+}
+
+mxsa_status mxsa_dedup_workspace_size(const mxsa_problem* problem, size_t* dedup_bytes) {
+  if (!problem || !dedup_bytes) return MXSA_ERR_INVALID_ARG;
+  mxsa_status s = validate_problem(*problem);
+  if (s != MXSA_OK) return s;
+  *dedup_bytes = dedup_workspace_bytes(*problem);
+  return MXSA_OK;
+}
+
+mxsa_status mxsa_build_index_dedup(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
+                                   const int32_t* used_kv_lens, const int32_t* block_tables, void* index_ws,
+                                   size_t index_bytes, void* dedup_ws, size_t dedup_bytes, void* stream) {
+  if (!problem) return MXSA_ERR_INVALID_ARG;
+  mxsa_index_layout L;
+  mxsa_status s = index_layout(*problem, &L);
+  if (s != MXSA_OK) return s;
+  if (!cu_seqlens_q || !used_kv_lens || !block_tables || !index_ws || !dedup_ws || (problem->total_q > 0 && !sel))
+    return MXSA_ERR_INVALID_ARG;
+  if (!aligned(sel, 4) || !aligned(cu_seqlens_q, 8) || !aligned(used_kv_lens, 4) || !aligned(block_tables, 4) ||
+      !aligned(index_ws, 16) || !aligned(dedup_ws, 16))
+    return MXSA_ERR_INVALID_ARG;
+  if (index_bytes < L.total || dedup_bytes < dedup_workspace_bytes(*problem)) return MXSA_ERR_WORKSPACE;
+  IndexPtrs ix = index_ptrs(*problem, index_ws);
+  DedupPtrs d = dedup_ptrs(*problem, dedup_ws);
+  cudaError_t e = launch_build_index_dedup(*problem, sel, cu_seqlens_q, used_kv_lens, block_tables, ix, d,
+                                           static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXSA_OK : MXSA_ERR_CUDA;
 }
 

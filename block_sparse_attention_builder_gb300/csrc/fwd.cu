@@ -74,6 +74,7 @@ struct FwdArgs {
   const uint8_t* q;
   const int32_t* block_tables;
   const SeqInfo* seq;
+  const int32_t* token_seq;
   const int32_t* entries;
   const int4* items;
   const int32_t* cta_ptr;
@@ -404,6 +405,10 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     // ------------------------------------------------------ softmax groups
     const int grp = warp >> 2;     // 0 or 1
     const int r = tid & 127;       // tile row == TMEM lane
+    // With the dedup index a key's rows may come from several sequences
+    // (the same physical block at the same logical position): each row then
+    // takes its causal position from its own token's sequence.
+    const bool row_seq = a.causal && a.idx_hdr[kHdrDedup] != 0;
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + grp * 256 + lane_addr, tO = tS + 128;
     const uint32_t qp = sbase + kOffQP + grp * kTileBytes;
@@ -573,6 +578,16 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         // limit: from the copy above, or (warp gather path) the entry list
         int tok = (t >> 1) ? tk_row1 : tk_row0;
         if (!a.q_tma) tok = r < rows ? __ldg(a.entries + et0 + r / a.G) / (a.Hkv * a.topk) : -1;
+        // the token's causal position (loaded here, used after the epilogue)
+        int pos = 0;
+        if (tok >= 0) {
+          if (row_seq) {
+            const SeqInfo* ts = a.seq + __ldg(a.token_seq + tok);
+            pos = __ldg(&ts->L) - __ldg(&ts->tq) + (tok - __ldg(&ts->q_begin));
+          } else {
+            pos = inf.L - inf.tq + (tok - inf.q_begin);
+          }
+        }
         // ---- this tile's q rows into the group's buffer, free since the
         // group's previous q k^T completed (it waited for that S)
         if (a.q_tma) {
@@ -619,7 +634,6 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         }
         int lim = 0;
         if (tok >= 0) {
-          const int pos = inf.L - inf.tq + (tok - inf.q_begin);
           lim = inf.valid;
           if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
         }
@@ -809,6 +823,7 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.q = static_cast<const uint8_t*>(q);
   a.block_tables = block_tables;
   a.seq = ix.seq;
+  a.token_seq = ix.token_seq;
   a.entries = ix.entries;
   a.items = sc.items;
   a.cta_ptr = sc.cta_ptr;

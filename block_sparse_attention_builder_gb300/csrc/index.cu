@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kIndexThreads) k_index(IndexArgs a) {
 // CTAs of a cooperative launch: at most 2 per SM (all must be resident at
 // once); 0 when the device cannot launch cooperatively.  Cached per device.
 int coop_grid(const void* kernel, int threads) {
-  constexpr int kMaxDev = 64, kMaxKernels = 4;
+  constexpr int kMaxDev = 64, kMaxKernels = 8;
   static std::mutex mu;
   static const void* keys[kMaxDev][kMaxKernels] = {};
   static int vals[kMaxDev][kMaxKernels] = {};

@@ -23,7 +23,7 @@ enum : int {
   kHdrTileCtr = 7,   // dynamic tile counter of the key scan
   kHdrBarCount = 8,  // grid barrier: arrivals (cleared before each launch)
   kHdrAbort = 9,     // grid barrier: set when a barrier wait gave up
-  kHdrReserved10 = 10,
+  kHdrDedup = 10,    // 1: keys are physical blocks (built by the dedup index build)
   kHdrInts = 16
 };
 
@@ -93,6 +93,18 @@ struct SchedPtrs {
   long long* cost_prefix_dec;
   int32_t* cta_ptr_dec;
   unsigned long long* cta_sums;  // 2 words per CTA: normal, decode
+  uint32_t* dk;             // bit a: active key a is a decode key
+};
+
+// Scratch of the dedup index build (its own workspace): the smallest packed
+// (block, sequence) per physical page, each block's owner sequence, the
+// number of blocks each owner block stands for, and each (kv head, block)
+// row's own entry count before the rows join their owner's key.
+struct DedupPtrs {
+  unsigned long long* page_min;  // [num_pages]
+  int32_t* owner;                // [blocks]
+  int32_t* gsize;                // [blocks]
+  int32_t* own_count;            // [Hkv * blocks], key order
 };
 
 constexpr int kScanThreads = 256;
@@ -122,6 +134,11 @@ mxsa_status validate_problem(const mxsa_problem& p);
 // launchers (return cudaGetLastError())
 cudaError_t launch_build_index(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
                                const IndexPtrs& ix, const mxsa_index_layout& lay, cudaStream_t st);
+size_t dedup_workspace_bytes(const mxsa_problem& p);
+DedupPtrs dedup_ptrs(const mxsa_problem& p, void* ws);
+cudaError_t launch_build_index_dedup(const mxsa_problem& p, const int32_t* sel, const int64_t* cu,
+                                     const int32_t* lens, const int32_t* block_tables, const IndexPtrs& ix,
+                                     const DedupPtrs& d, cudaStream_t st);
 cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
                         const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas, cudaStream_t st);
 cudaError_t launch_schedule(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc,

@@ -604,6 +604,7 @@ cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t
   a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
   a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
   a.P.num_ctas = num_ctas;
+  a.P.topk = p.topk;
   const int grid = coop_grid(reinterpret_cast<const void*>(k_plan), kPlanThreads);
   if (grid <= 0) return cudaErrorNotSupported;
   cudaError_t e = cudaMemsetAsync(ix.hdr, 0, kHdrInts * sizeof(int32_t), st);

@@ -97,7 +97,7 @@ __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
 }
 
 struct Params {
-  int B, Hkv, G, kvw, per_tile, E, num_ctas;
+  int B, Hkv, G, kvw, per_tile, E, num_ctas, topk;
 };
 
 // What one active key contributes.  kind 0: nothing (inside a decode run),

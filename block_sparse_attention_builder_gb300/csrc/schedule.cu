@@ -4,15 +4,19 @@
 //
 // Active keys (keys with entries) are taken in key order and produce two
 // work lists:
-//  * normal keys (sequences with several new tokens): n = ceil(cnt / E)
-//    items of <= E = MXSA_ITEM_TILES * (128 / G) entries, item i covering
-//    entries [i*cnt/n, (i+1)*cnt/n) of the key; cost =
-//    valid_tokens * kv_weight + tiles * 256 + rows * 2;
-//  * decode keys (sequences with one new token, G <= 16): every key of one
-//    (kv head, sequence) holds the same single entry, so the run of such
-//    keys is cut into ceil(len / 8) items of consecutive keys that the
-//    decode forward processes with one online softmax; cost =
-//    sum(valid_tokens * kv_weight) + keys * 64 + 256.
+//  * decode keys: a key of a sequence with one new token (G <= 16) that
+//    holds exactly one entry, of that token.  A maximal run of consecutive
+//    active decode keys of one (kv head, sequence) is cut into
+//    ceil(len / 8) items of consecutive keys that the decode forward
+//    processes with one online softmax; cost =
+//    sum(valid_tokens * kv_weight) + keys * 64 + 256.  With the plain index
+//    every key of such a sequence is a decode key; with the dedup index a
+//    key of a shared block holds several sequences' entries and is a normal
+//    key;
+//  * normal keys (every other key): n = ceil(cnt / E) items of
+//    <= E = MXSA_ITEM_TILES * (128 / G) entries, item i covering entries
+//    [i*cnt/n, (i+1)*cnt/n) of the key; cost =
+//    valid_tokens * kv_weight + tiles * 256 + rows * 2.
 // kv_weight = 2 for 16-bit caches and 1 for FP8.  Each list is laid out in
 // key order and cut into num_ctas contiguous ranges at the cost targets
 // floor(c * C / num_ctas): CTA c takes the items whose exclusive cost prefix
@@ -21,10 +25,12 @@
 //
 // Every per-key and per-item quantity has a closed form (item sizes take
 // two values, q = cnt / n and q + 1, and the first i items hold
-// floor(i * cnt / n) entries), so the work per key and per item is O(1).
-// One cooperative launch, two phases separated by a bounded grid barrier
-// (the fused plan kernel in plan.cu computes the same schedule inside the
-// index build):
+// floor(i * cnt / n) entries), so the work per key and per item is O(1);
+// a decode run's length is found from a bit per active key (is it a decode
+// key) and the run's (kv head, sequence) key range.  One cooperative launch,
+// three phases separated by bounded grid barriers (the fused plan kernel in
+// plan.cu computes the same schedule of a plain index inside its build):
+//   flags   one warp per 32 active keys writes their decode-key bits
 //   reduce  the active keys are cut into one contiguous chunk per CTA; each
 //           CTA sums the item counts and costs of its chunk (both lists)
 //   scan    each CTA adds the sums of the chunks before it, scans its chunk
@@ -43,18 +49,70 @@ namespace {
 
 using namespace sch;
 
-__device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const Params& P, int NB, int n_active, int a) {
+__device__ __forceinline__ bool dk_bit(const uint32_t* dk, int a) { return (dk[a >> 5] >> (a & 31)) & 1u; }
+
+// flags: bit a of sc.dk = active key a is a decode key
+__device__ void phase_flags(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P) {
+  const int n_active = ix.hdr[kHdrActive], NB = ix.hdr[kHdrNB];
+  const int lane = threadIdx.x & 31;
+  const long long n_words = ((long long)n_active + 31) / 32;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n_words; w += warps) {
+    const int a = (int)(w * 32) + lane;
+    bool d = false;
+    if (a < n_active && P.G <= kDecodeMaxG) {
+      const int key = ix.active[a];
+      const int g = key / NB, r = key - g * NB;
+      const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+      if (si.tq == 1) {
+        const int beg = ix.row_ptr[key];
+        if (ix.row_ptr[key + 1] - beg == 1) d = ix.entries[beg] / (P.Hkv * P.topk) == si.q_begin;
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, d);
+    if (lane == 0) sc.dk[w] = m;
+  }
+}
+
+// first active position after a (< n_active) that is not a decode key, or
+// n_active
+__device__ __forceinline__ int next_non_decode(const uint32_t* dk, int a, int n_active) {
+  int e = a + 1;
+  while (e < n_active) {
+    const int sh = e & 31;
+    const uint32_t inv = ~(dk[e >> 5] >> sh);  // bit j: key e + j is not a decode key (or lies past the word)
+    const int z = __ffs(inv) - 1;
+    if (z >= 0 && z < 32 - sh) {
+      e += z;
+      break;
+    }
+    e += 32 - sh;
+  }
+  return e < n_active ? e : n_active;
+}
+
+// chunk_end: keys from chunk_end on belong to the next CTA (nothing to do)
+__device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const SchedPtrs& sc, const Params& P, int NB,
+                                            int chunk_end, int n_active, int a) {
   KeyWork w{};
   w.a = a;
-  if (a >= n_active) return w;
+  if (a >= chunk_end) return w;
   const int key = ix.active[a];
-  const int g = key / NB, r = key - g * NB;
-  const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
-  if (P.G <= kDecodeMaxG && si.tq == 1) {
-    const int lo = g * NB + si.blk_off;
-    if (a > 0 && ix.active[a - 1] >= lo) return w;  // inside a run
-    const int len = ix.row_nnz[si.q_begin * P.Hkv + g];  // entries of the token's row = keys of the run
-    const int b_last = ix.active[a + len - 1] - lo;
+  if (dk_bit(sc.dk, a)) {
+    const int g = key / NB, r = key - g * NB;
+    const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
+    const int lo = g * NB + si.blk_off, hi = lo + si.nblk;
+    if (a > 0 && dk_bit(sc.dk, a - 1) && ix.active[a - 1] >= lo) return w;  // inside a run
+    // the run: decode keys from a on, up to the first that leaves (g, s)
+    int e = next_non_decode(sc.dk, a, n_active);
+    int l = a + 1;
+    while (l < e) {
+      const int mid = (l + e) >> 1;
+      if (ix.active[mid] >= hi) e = mid;
+      else l = mid + 1;
+    }
+    const int len = e - a;
+    const int b_last = ix.active[e - 1] - lo;
     const int v_last = si.L - 128 * b_last;
     w.kind = 2;
     w.cnt = len;
@@ -82,7 +140,7 @@ __device__ void phase_reduce(const IndexPtrs& ix, const SchedPtrs& sc, const Par
   active_chunk(n_active, &lo, &hi);
   unsigned long long vn = 0, vd = 0;
   for (int a = lo + threadIdx.x; a < hi; a += blockDim.x) {
-    const KeyWork w = key_work(ix, P, NB, hi, a);
+    const KeyWork w = key_work(ix, sc, P, NB, hi, n_active, a);
     if (w.kind == 1) vn += pack(w.cost, w.n);
     if (w.kind == 2) vd += pack(w.cost, w.n);
   }
@@ -145,7 +203,7 @@ __device__ void phase_scan_emit(const IndexPtrs& ix, const SchedPtrs& sc, const 
 #pragma unroll
     for (int j = 0; j < kSchPerThread; ++j) {
       const int a = t0 + threadIdx.x * kSchPerThread + j;
-      w[j] = key_work(ix, P, NB, hi, a);
+      w[j] = key_work(ix, sc, P, NB, hi, n_active, a);
       if (w[j].kind == 1) vn += pack(w[j].cost, w[j].n);
       if (w[j].kind == 2) vd += pack(w[j].cost, w[j].n);
     }
@@ -231,6 +289,8 @@ __global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
   int* bar = a.sc.hdr + kSchBarCount;
   int epoch = 0;
   int* flags = a.ix.hdr + kHdrFlags;
+  phase_flags(a.ix, a.sc, a.P);
+  if (!grid_barrier(bar, flags, gridDim.x, epoch)) return;
   phase_reduce(a.ix, a.sc, a.P, tmp);
   if (!grid_barrier(bar, flags, gridDim.x, epoch)) return;
   phase_scan_emit(a.ix, a.sc, a.P, tmp);
@@ -254,6 +314,7 @@ static SchedArgs sched_args(const mxsa_problem& p, const IndexPtrs& ix, const Sc
   a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
   a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
   a.P.num_ctas = num_ctas;
+  a.P.topk = p.topk;
   return a;
 }
 

@@ -123,6 +123,34 @@ mxsa_status mxsa_workspace_size(const mxsa_problem* problem, size_t* index_bytes
 mxsa_status mxsa_build_index(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
                              const int32_t* used_kv_lens, void* index_ws, size_t index_bytes, void* stream);
 
+/* Step 1, cross-sequence variant.  The README's intro (fw-ai/minimax-kernels)
+ * makes the KV block the unit that is loaded once for every query that
+ * selected it; with a paged cache, sequences that share a cached prefix
+ * point their block_tables at the same physical pages, and this build
+ * keys such blocks by the pages, not by the sequence (the rule is this
+ * library's reading of that passage):
+ *   a block (s, b) is shareable when it is full (128 b + 128 <= L_s) and
+ *   its pages (block_tables[s][b] for page_size 128, [2b] and [2b + 1] for
+ *   64) lie in [0, num_pages); owner(s, b) = the smallest sequence s' whose
+ *   block b is shareable with the same pages (s itself when none is
+ *   smaller; a block that is not shareable owns itself); a selection of
+ *   (s, b) becomes an entry of key g * NB + blk_off[owner] + b.
+ * Everything else is mxsa_build_index's definition: keys (g, s, b) in that
+ * order (a key whose rows moved to an owner holds no entries), entries by
+ * slot within a key, the same flags and workspace.  A key then holds rows
+ * of several sequences; each keeps its own causal position, which the
+ * forward reads per row.  mxsa_schedule and mxsa_kvouter_fwd take the
+ * result as they take the plain index; mxsa_plan builds the plain index
+ * only.
+ *   block_tables  device int32 [B, max_pages_per_seq]
+ *   dedup_ws      device scratch, dedup_bytes from mxsa_dedup_workspace_size
+ *                 (its contents need no initialisation and are not kept)
+ * Other arguments as for mxsa_build_index.  Asynchronous on `stream`. */
+mxsa_status mxsa_dedup_workspace_size(const mxsa_problem* problem, size_t* dedup_bytes);
+mxsa_status mxsa_build_index_dedup(const mxsa_problem* problem, const int32_t* sel, const int64_t* cu_seqlens_q,
+                                   const int32_t* used_kv_lens, const int32_t* block_tables, void* index_ws,
+                                   size_t index_bytes, void* dedup_ws, size_t dedup_bytes, void* stream);
+
 /* Step 2 -- load-balancing scheduler ("load-balancing scheduler" in the
  * README's test list; the split rule and cost model are this library's):
  * splits each key's entries into work items of at most 4 tiles of 128
@@ -290,10 +318,15 @@ mxsa_status mxsa_index_layout_query(const mxsa_problem* problem, mxsa_index_layo
  *   items:     int32[4] = {key, entry_begin, n_entries, 0}, keys of
  *              sequences with several new tokens (KV-stationary tiles);
  *   items_dec: int32[4] = {position in active_keys, entry, 1, n_keys}, runs
- *              of up to 8 keys of one single-token sequence and kv head
- *              (every one of those keys holds that token's one entry). */
+ *              of up to 8 consecutive decode keys of one sequence and kv
+ *              head.  A decode key belongs to a sequence with one new token
+ *              (G <= 16) and holds exactly one entry, of that token.  With
+ *              the plain index every key of such a sequence is one; with the
+ *              dedup index a shared block's key holds several sequences'
+ *              entries and goes to the first list.
+ * decode_bits: uint32 words, bit a set when active key a is a decode key. */
 typedef struct {
-  size_t header, items, cost_prefix, cta_ptr, items_dec, cost_prefix_dec, cta_ptr_dec, cta_sums, total;
+  size_t header, items, cost_prefix, cta_ptr, items_dec, cost_prefix_dec, cta_ptr_dec, cta_sums, decode_bits, total;
   int64_t items_cap, tiles_cap;
 } mxsa_sched_layout;
 mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layout* layout);
