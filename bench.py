@@ -8,10 +8,13 @@ resident in HBM.  Prints ONE JSON line (rank 0).
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
 With no --workload (or --workload all) the line carries all five sparse
-workloads: each is measured in turn (its own warm-up, timed steps, end-to-end
-steps and oracle baseline) and listed under "workloads"; the line's own
-value, roofline, e2e and cpu_baseline are those of skewed_decode, the largest
-workload that fits one GPU.  kv_store and dense_prefill are separate runs.
+workloads and skewed_decode_shared (skewed_decode on shared prefix pages,
+run through the dedup index: dedup build + scheduler + forward + combine):
+each is measured in turn (its own warm-up, timed steps, end-to-end steps and
+oracle baseline) and listed under "workloads"; the line's own value,
+roofline, e2e and cpu_baseline are those of skewed_decode, the largest
+workload that fits one GPU.  kv_store, dense_prefill and the top-k
+selection workloads are separate runs.
 
 Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
 on the launching stream with an L2 flush (a 256 MiB write) between steps
@@ -47,6 +50,8 @@ KERNELS_PER_STEP = 3  # k_plan (index + schedule) | k_fwd (decode and KV-station
 DEFAULT_WORKLOAD = "all"
 # the five sparse workloads, in order; the headline is the largest one that fits one GPU
 SPARSE_WORKLOADS = ("tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode")
+# run with the dedup index (mxsa_build_index_dedup + mxsa_schedule: 4 launches a step)
+DEDUP_WORKLOADS = ("skewed_decode_shared",)
 HEADLINE_WORKLOAD = "skewed_decode"
 
 
@@ -589,8 +594,14 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     Returns the workload's JSON entry (rank 0) or None."""
     import block_sparse_attention_builder_gb300 as mx
     dev = torch.device("cuda", local_rank)
+    from block_sparse_attention_builder_gb300 import workloads as W
+    dedup = name in DEDUP_WORKLOADS
     w = load_workload(name, rank)
     stats = _stats(w)
+    if dedup:  # a shared block is loaded once for every sequence that holds it
+        phys = W.physical_blocks_tokens(w)
+        stats["unique_blocks_per_sequence"] = stats["unique_blocks"]
+        stats["unique_blocks"], stats["unique_tokens"] = phys["unique_blocks"], phys["unique_tokens"]
     unique_kv_bytes, flops, io_bytes, partial_bytes = algorithmic(w, stats)
     log(f"[bench] {name}: {stats}")
 
@@ -602,7 +613,7 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     lens = torch.from_numpy(w.used_kv_lens).to(dev)
     prob = mx.make_problem(w.num_seqs, w.total_q, w.num_q_heads, w.num_kv_heads, w.topk, w.page_size,
                            w.num_pages, w.max_pages_per_seq, w.causal, 0.0, q.dtype, k.dtype)
-    attn = mx.SparseAttention(prob, dev)
+    attn = mx.SparseAttention(prob, dev, dedup=dedup)
     out = torch.empty_like(q)
     lse = torch.empty(w.num_q_heads, w.total_q, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -611,7 +622,10 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        if args.plan == "separate":  # the two steps as their own launches (k_index, k_schedule)
+        if dedup:  # the index keyed by physical block, then the scheduler
+            mx.build_index_dedup(prob, sel, cu, lens, bt, attn.ws.index, attn.dedup_ws, stream)
+            mx.schedule(prob, attn.ws.index, attn.ws.sched, 0, stream)
+        elif args.plan == "separate":  # the two steps as their own launches (k_index, k_schedule)
             mx.build_index(prob, sel, cu, lens, attn.ws.index, stream)
             mx.schedule(prob, attn.ws.index, attn.ws.sched, 0, stream)
         else:
@@ -698,7 +712,9 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
             ev_in.record(side)
         with torch.cuda.stream(e2e_stream):
             d_small.copy_(h_small, non_blocking=True)
-        attn.prepare(d_sel, d_cu, d_lens, stream=e2e_stream)
+        if dedup:  # the dedup index reads the block tables too
+            e2e_stream.wait_event(ev_in)
+        attn.prepare(d_sel, d_cu, d_lens, stream=e2e_stream, block_tables=d_bt)
         e2e_stream.wait_event(ev_in)
         attn.attend(d_q, k, v, d_bt, out=h_out, lse=h_lse, stream=e2e_stream)
 
@@ -746,7 +762,8 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
         "data": "synthetic (seeded counter-based N(0,1) values; selections per the workload recipe)",
         "config": workload_config(w, stats, name),
         "tflops": tflops, "unique_kv_gbs": kv_gbs, "step_roofline": step_roof,
-        "kernel_ms": {"plan (index + schedule)": float(per[:, 0].mean()), "fwd": fwd_ms,
+        "kernel_ms": {("dedup index + schedule" if dedup else "plan (index + schedule)"): float(per[:, 0].mean()),
+                      "fwd": fwd_ms,
                       "combine": float(per[:, 2].mean())},
         "fwd_unique_kv_gbs": fwd_gbs, "fwd_tflops": fwd_tflops,
         "bytes": {"unique_kv": unique_kv_bytes, "io": io_bytes, "partials_overhead": partial_bytes},
@@ -758,7 +775,7 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
                         "one pinned staging buffer, then the plan while q and block tables copy on a second "
                         "stream; the combine writes out + lse into pinned host memory directly (counted as "
                         "D2H bytes); the KV cache is resident model state"},
-        "gpu_launches": (KERNELS_PER_STEP + (args.plan == "separate")) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (dedup or args.plan == "separate")) * args.steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -955,8 +972,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    help="'all' (default): the five sparse workloads in one line, headline skewed_decode; "
-                         "or one of " + ", ".join(list(SPARSE_WORKLOADS) + ["kv_store", "dense_prefill"] +
+                    help="'all' (default): the five sparse workloads and the dedup one in one line, headline "
+                         "skewed_decode; "
+                         "or one of " + ", ".join(list(SPARSE_WORKLOADS) + list(DEDUP_WORKLOADS) +
+                                                  ["kv_store", "dense_prefill"] +
                                                   list(SELECT_WORKLOADS)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--plan", default="fused", choices=["fused", "separate"],
@@ -993,7 +1012,7 @@ def main():
     B.build()
     torch.cuda.set_device(local_rank)
     if args.workload == "all":
-        names, headline = list(SPARSE_WORKLOADS), HEADLINE_WORKLOAD
+        names, headline = list(SPARSE_WORKLOADS) + list(DEDUP_WORKLOADS), HEADLINE_WORKLOAD
     else:
         names, headline = [args.workload], args.workload
     entries = {}

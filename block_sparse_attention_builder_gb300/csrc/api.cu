@@ -168,25 +168,44 @@ SchedPtrs sched_ptrs(const mxsa_problem& p, void* ws) {
   return x;
 }
 
-// Dedup scratch: the page array first (8-byte words), then the two block
-// arrays and the per-key counts.
-size_t dedup_workspace_bytes(const mxsa_problem& p) {
+// Dedup scratch: the page array first (8-byte words), then the block
+// arrays and the per-key arrays.
+namespace {
+struct DedupLayout {
+  size_t page_min, owner, gsize, own_count, mbeg, mlist, glist, gkeys, total;
+};
+DedupLayout dedup_layout(const mxsa_problem& p) {
   const int64_t nb_cap = (int64_t)p.num_seqs * max_blocks_per_seq(p);
-  return align_up((size_t)p.num_pages * 8) + 2 * align_up((size_t)nb_cap * 4) +
-         align_up((size_t)nb_cap * p.num_kv_heads * 4);
+  const size_t blk = align_up((size_t)nb_cap * 4), key = align_up((size_t)nb_cap * p.num_kv_heads * 4);
+  DedupLayout L;
+  size_t o = 0;
+  L.page_min = o;  o += align_up((size_t)p.num_pages * 8);
+  L.owner = o;     o += blk;
+  L.gsize = o;     o += blk;
+  L.own_count = o; o += key;
+  L.mbeg = o;      o += blk;
+  L.mlist = o;     o += blk;
+  L.glist = o;     o += blk;
+  L.gkeys = o;     o += 2 * key;
+  L.total = o;
+  return L;
 }
+}  // namespace
+
+size_t dedup_workspace_bytes(const mxsa_problem& p) { return dedup_layout(p).total; }
 
 DedupPtrs dedup_ptrs(const mxsa_problem& p, void* ws) {
-  const int64_t nb_cap = (int64_t)p.num_seqs * max_blocks_per_seq(p);
+  const DedupLayout L = dedup_layout(p);
   uint8_t* b = static_cast<uint8_t*>(ws);
   DedupPtrs d;
-  d.page_min = reinterpret_cast<unsigned long long*>(b);
-  b += align_up((size_t)p.num_pages * 8);
-  d.owner = reinterpret_cast<int32_t*>(b);
-  b += align_up((size_t)nb_cap * 4);
-  d.gsize = reinterpret_cast<int32_t*>(b);
-  b += align_up((size_t)nb_cap * 4);
-  d.own_count = reinterpret_cast<int32_t*>(b);
+  d.page_min = reinterpret_cast<unsigned long long*>(b + L.page_min);
+  d.owner = reinterpret_cast<int32_t*>(b + L.owner);
+  d.gsize = reinterpret_cast<int32_t*>(b + L.gsize);
+  d.own_count = reinterpret_cast<int32_t*>(b + L.own_count);
+  d.mbeg = reinterpret_cast<int32_t*>(b + L.mbeg);
+  d.mlist = reinterpret_cast<int32_t*>(b + L.mlist);
+  d.glist = reinterpret_cast<int32_t*>(b + L.glist);
+  d.gkeys = reinterpret_cast<int2*>(b + L.gkeys);
   return d;
 }
 

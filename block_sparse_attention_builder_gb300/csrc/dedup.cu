@@ -15,7 +15,7 @@
 // are its member blocks' own rows (bitmap walks, as in the plain build)
 // taken in sequence order.
 //
-// One cooperative launch, six phases separated by bounded grid barriers:
+// One cooperative launch, seven phases separated by bounded grid barriers:
 //   seq     CTA 0: per-sequence scan; every CTA: token -> sequence map and
 //           the page array set to "none"
 //   zero    counters and bitmaps cleared; every shareable block offers its
@@ -26,12 +26,20 @@
 //           search over the smaller sequences (pages reused at another
 //           logical block, or 64-token page pairs that share only one page);
 //           each owner block counts its members
-//   fold    each (g, s, b) row's population is kept as its own count and
-//           added to its owner's key
-//   reduce  per-CTA sums of the key counts (the plain build's phase)
-//   scan    row_ptr, active keys and entries; a key whose owner block has
-//           other members is emitted by one warp that walks the sequences
-//           from the owner up, 32 at a time, finding the members in order
+//   fold    per block, each head's row population is kept as its own count
+//           and added to its owner's key; owner blocks with other members
+//           are listed and given room for their member list
+//   reduce  per-CTA sums of the key counts (the plain build's phase); one
+//           warp per listed owner block walks the sequences from the owner
+//           up (32 lanes x 4 at a time) and writes its members in order
+//   scan    row_ptr, active keys and the entries of keys that are their
+//           block's only member (as in the plain build); keys of listed
+//           owner blocks are queued with their first entry
+//   group   one warp per queued key writes its entries: its members' own
+//           bitmap rows in member order
+// The last two phases spread the shared blocks' work over the whole grid:
+// their keys lie in a few sequences' key ranges, which the scan's chunks
+// would otherwise leave to a few CTAs.
 #include "index_phases.cuh"
 
 namespace mxsa {
@@ -114,42 +122,80 @@ __device__ void phase_owner(const DedupArgs& a) {
 __device__ void phase_fold(const DedupArgs& a) {
   const IndexPtrs& ix = a.ia.ix;
   const int NB = ix.hdr[kHdrNB];
-  const long long n_keys = (long long)ix.hdr[kHdrKeys];
   const size_t BMW = (size_t)ix.hdr[kHdrBMW];
-  for (long long k = grid_tid(); k < n_keys; k += grid_threads()) {
-    const int g = (int)(k / NB), r = (int)(k - (long long)g * NB);
-    const int s = ixp::seq_of_block(ix.seq, a.ia.B, r);
+  for (long long r = grid_tid(); r < NB; r += grid_threads()) {
+    const int s = ixp::seq_of_block(ix.seq, a.ia.B, (int)r);
     const SeqInfo si = ix.seq[s];
-    const int b = r - si.blk_off;
-    const uint32_t* row = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
-    int c = 0;
-    for (int w = 0; w < si.words; ++w) c += __popc(row[w]);
-    a.d.own_count[k] = c;
-    if (c > 0) atomicAdd(&ix.counts[(long long)g * NB + ix.seq[a.d.owner[r]].blk_off + b], c);
+    const int b = (int)r - si.blk_off;
+    const int orow = ix.seq[a.d.owner[r]].blk_off + b;
+    for (int g = 0; g < a.ia.Hkv; ++g) {
+      const uint32_t* row = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
+      int c = 0;
+      for (int w = 0; w < si.words; ++w) c += __popc(row[w]);
+      a.d.own_count[(long long)g * NB + r] = c;
+      if (c > 0) atomicAdd(&ix.counts[(long long)g * NB + orow], c);
+    }
+    const int m = a.d.gsize[r];
+    if (m > 1) {
+      a.d.glist[atomicAdd(&ix.hdr[kHdrGroups], 1)] = (int)r;
+      a.d.mbeg[r] = atomicAdd(&ix.hdr[kHdrMembers], m);
+    }
   }
 }
 
-// One warp emits the entries of key (g, owner sequence o, block b) from
-// `base`: the member sequences s >= o (owner(s, b) == o) in increasing
-// order, each member's own bitmap row in token order.  `members` is the
-// owner block's member count (the walk stops once all are found).
-__device__ void emit_group(const DedupArgs& a, int g, int o, int b, int base, int members) {
+// One warp writes the member sequences of owner block R (sequence o, block
+// b) in increasing order: the sequences s >= o with owner(s, b) == o.
+constexpr int kWalkUnroll = 4;
+__device__ void walk_members(const DedupArgs& a, int R) {
+  const IndexPtrs& ix = a.ia.ix;
+  const int lane = threadIdx.x & 31;
+  const int o = ixp::seq_of_block(ix.seq, a.ia.B, R);
+  const int b = R - ix.seq[o].blk_off;
+  const int m = a.d.gsize[R];
+  int32_t* out = a.d.mlist + a.d.mbeg[R];
+  int found = 0;
+  for (int s0 = o; s0 < a.ia.B && found < m; s0 += 32 * kWalkUnroll) {
+    bool mem[kWalkUnroll];
+#pragma unroll
+    for (int u = 0; u < kWalkUnroll; ++u) {
+      const int s = s0 + 32 * u + lane;
+      mem[u] = false;
+      if (s < a.ia.B) {
+        const int nblk = ix.seq[s].nblk, boff = ix.seq[s].blk_off;
+        mem[u] = b < nblk && a.d.owner[boff + b] == o;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kWalkUnroll; ++u) {
+      const unsigned bal = __ballot_sync(0xffffffffu, mem[u]);
+      if (mem[u]) out[found + __popc(bal & ((1u << lane) - 1u))] = s0 + 32 * u + lane;
+      found += __popc(bal);
+    }
+  }
+}
+
+// One warp writes the entries of key (g, owner block R) from `base`: the
+// members' own bitmap rows in member order.
+__device__ void emit_group_key(const DedupArgs& a, int key, int base) {
   const IndexPtrs& ix = a.ia.ix;
   const int lane = threadIdx.x & 31;
   const int NB = ix.hdr[kHdrNB];
   const size_t BMW = (size_t)ix.hdr[kHdrBMW], KMW = (size_t)ix.hdr[kHdrKMW];
   const int Hkv = a.ia.Hkv, topk = a.ia.topk;
-  int found = 0, run = base;
-  for (int s0 = o; s0 < a.ia.B && found < members; s0 += 32) {
-    const int s = s0 + lane;
-    bool mem = false;
+  const int g = key / NB, R = key - g * NB;
+  const int o = ixp::seq_of_block(ix.seq, a.ia.B, R);
+  const int b = R - ix.seq[o].blk_off;
+  const int m = a.d.gsize[R];
+  const int32_t* mem = a.d.mlist + a.d.mbeg[R];
+  int run = base;
+  for (int i0 = 0; i0 < m; i0 += 32) {
+    const int i = i0 + lane;
     SeqInfo si{};
-    if (s < a.ia.B) {
-      si = ix.seq[s];
-      mem = b < si.nblk && a.d.owner[si.blk_off + b] == o;
+    int cnt = 0;
+    if (i < m) {
+      si = ix.seq[mem[i]];
+      cnt = a.d.own_count[(long long)g * NB + si.blk_off + b];
     }
-    found += __popc(__ballot_sync(0xffffffffu, mem));
-    const int cnt = mem ? a.d.own_count[(long long)g * NB + si.blk_off + b] : 0;
     const int inc = ixp::warp_inclusive_scan(cnt);
     const int my_base = run + inc - cnt;
     const uint32_t* bm = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
@@ -172,8 +218,11 @@ __device__ void emit_group(const DedupArgs& a, int g, int o, int b, int base, in
   }
 }
 
-// scan + emit: the plain build's phase, with keys of shared owner blocks
-// emitted by emit_group
+__device__ __forceinline__ long long grid_warp() { return ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; }
+__device__ __forceinline__ long long grid_warps() { return ((long long)gridDim.x * blockDim.x) >> 5; }
+
+// scan + emit: the plain build's phase; keys of shared owner blocks are
+// queued for the group phase instead of emitted
 __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tmp) {
   __shared__ int long_key[kScanTile];
   __shared__ int long_base[kScanTile];
@@ -227,7 +276,9 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
           const int b = r - si.blk_off;
           const int valid = si.L - 128 * b;
           ix.active_valid[pos] = valid < 128 ? valid : 128;
-          if (a.d.gsize[r] <= 1 && si.words <= 2) {
+          if (a.d.gsize[r] > 1) {
+            a.d.gkeys[atomicAdd(&ix.hdr[kHdrGroupKeys], 1)] = make_int2(key, base);
+          } else if (si.words <= 2) {
             ixp::emit_row_serial(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words,
                                  si.words, ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq,
                                  si.q_begin, g, Hkv, topk, base);
@@ -244,16 +295,11 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
     for (int i = warp; i < n_long; i += n_warps) {
       const int key = long_key[i];
       const int g = key / NB, r = key - g * NB;
-      const int s = ixp::seq_of_block(ix.seq, B, r);
-      const SeqInfo si = ix.seq[s];
+      const SeqInfo si = ix.seq[ixp::seq_of_block(ix.seq, B, r)];
       const int b = r - si.blk_off;
-      const int members = a.d.gsize[r];
-      if (members <= 1)
-        ixp::emit_row_warp(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
-                           ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv,
-                           topk, long_base[i]);
-      else
-        emit_group(a, g, s, b, long_base[i], members);
+      ixp::emit_row_warp(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words, si.words,
+                         ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq, si.q_begin, g, Hkv,
+                         topk, long_base[i]);
     }
     __syncthreads();
     carry += tot;
@@ -285,8 +331,14 @@ __global__ void __launch_bounds__(kIndexThreads) k_index_dedup(DedupArgs a) {
   phase_fold(a);
   if (!grid_barrier(bar, flags, nb, epoch)) return;
   ixp::phase_key_reduce(ix, tmp);
+  for (long long i = grid_warp(); i < ix.hdr[kHdrGroups]; i += grid_warps()) walk_members(a, a.d.glist[i]);
   if (!grid_barrier(bar, flags, nb, epoch)) return;
   phase_scan_emit_dedup(a, tmp);
+  if (!grid_barrier(bar, flags, nb, epoch)) return;
+  for (long long i = grid_warp(); i < ix.hdr[kHdrGroupKeys]; i += grid_warps()) {
+    const int2 gk = a.d.gkeys[i];
+    emit_group_key(a, gk.x, gk.y);
+  }
 }
 
 }  // namespace

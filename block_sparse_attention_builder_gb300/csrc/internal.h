@@ -24,6 +24,9 @@ enum : int {
   kHdrBarCount = 8,  // grid barrier: arrivals (cleared before each launch)
   kHdrAbort = 9,     // grid barrier: set when a barrier wait gave up
   kHdrDedup = 10,    // 1: keys are physical blocks (built by the dedup index build)
+  kHdrGroups = 11,   // dedup build: owner blocks with other members (glist)
+  kHdrMembers = 12,  // dedup build: member slots handed out (mlist)
+  kHdrGroupKeys = 13,  // dedup build: keys of shared owner blocks with entries (gkeys)
   kHdrInts = 16
 };
 
@@ -105,6 +108,10 @@ struct DedupPtrs {
   int32_t* owner;                // [blocks]
   int32_t* gsize;                // [blocks]
   int32_t* own_count;            // [Hkv * blocks], key order
+  int32_t* mbeg;                 // [blocks]: an owner block's first member in mlist
+  int32_t* mlist;                // [blocks]: member sequences of each shared owner block, in order
+  int32_t* glist;                // [blocks]: the owner blocks with other members
+  int2* gkeys;                   // [Hkv * blocks]: keys of those blocks with entries {key, first entry}
 };
 
 constexpr int kScanThreads = 256;

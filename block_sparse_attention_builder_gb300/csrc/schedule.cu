@@ -74,11 +74,10 @@ __device__ void phase_flags(const IndexPtrs& ix, const SchedPtrs& sc, const Para
   }
 }
 
-// first active position after a (< n_active) that is not a decode key, or
-// n_active
-__device__ __forceinline__ int next_non_decode(const uint32_t* dk, int a, int n_active) {
+// first active position in (a, limit) that is not a decode key, or limit
+__device__ __forceinline__ int next_non_decode(const uint32_t* dk, int a, int limit) {
   int e = a + 1;
-  while (e < n_active) {
+  while (e < limit) {
     const int sh = e & 31;
     const uint32_t inv = ~(dk[e >> 5] >> sh);  // bit j: key e + j is not a decode key (or lies past the word)
     const int z = __ffs(inv) - 1;
@@ -88,7 +87,7 @@ __device__ __forceinline__ int next_non_decode(const uint32_t* dk, int a, int n_
     }
     e += 32 - sh;
   }
-  return e < n_active ? e : n_active;
+  return e < limit ? e : limit;
 }
 
 // chunk_end: keys from chunk_end on belong to the next CTA (nothing to do)
@@ -103,8 +102,10 @@ __device__ __forceinline__ KeyWork key_work(const IndexPtrs& ix, const SchedPtrs
     const SeqInfo si = ix.seq[seq_of_block(ix.seq, P.B, r)];
     const int lo = g * NB + si.blk_off, hi = lo + si.nblk;
     if (a > 0 && dk_bit(sc.dk, a - 1) && ix.active[a - 1] >= lo) return w;  // inside a run
-    // the run: decode keys from a on, up to the first that leaves (g, s)
-    int e = next_non_decode(sc.dk, a, n_active);
+    // the run: decode keys from a on, up to the first that leaves (g, s).
+    // Its keys hold entries of one (token, kv head) row, so it has at most
+    // topk keys (the decode keys of the next sequence follow directly).
+    int e = next_non_decode(sc.dk, a, min(n_active, a + P.topk));
     int l = a + 1;
     while (l < e) {
       const int mid = (l + e) >> 1;

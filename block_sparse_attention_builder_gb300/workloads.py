@@ -24,6 +24,7 @@ none, int32 block tables, int64 cu_seqlens_q, int32 used_kv_lens).
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 from dataclasses import dataclass, field
 from typing import Callable, Dict, List, Optional, Sequence
@@ -139,6 +140,36 @@ def _uniform_int(lo: int, hi: int):
     return lambda rng, b: rng.integers(lo, hi, size=b, endpoint=True).astype(np.int64)
 
 
+def physical_blocks_tokens(w: Workload) -> Dict[str, float]:
+    """Unique selected blocks counted by physical identity, as the dedup
+    index keys them: a block that is full and whose pages are valid is
+    (kv head, logical block, its pages); any other block stays
+    (kv head, sequence, block).  Plain bookkeeping over the selection
+    array and the block tables."""
+    Hkv, ps = w.num_kv_heads, w.page_size
+    per_blk = BLOCK // ps
+    uniq = set()
+    tokens_unique = 0
+    for s in range(w.num_seqs):
+        L = int(w.used_kv_lens[s])
+        nblk = (L + BLOCK - 1) // BLOCK
+        t0, t1 = int(w.cu_seqlens_q[s]), int(w.cu_seqlens_q[s + 1])
+        for t in range(t0, t1):
+            pos = L - (t1 - t0) + (t - t0)
+            for g in range(Hkv):
+                for b in w.selected[t, g]:
+                    b = int(b)
+                    if not 0 <= b < nblk or (w.causal and BLOCK * b > pos):
+                        continue
+                    pages = tuple(int(x) for x in w.block_tables[s, b * per_blk:(b + 1) * per_blk])
+                    full = BLOCK * b + BLOCK <= L and all(0 <= x < w.num_pages for x in pages)
+                    key = (g, b, pages) if full else (g, b, ("seq", s))
+                    if key not in uniq:
+                        uniq.add(key)
+                        tokens_unique += min(BLOCK, L - BLOCK * b)
+    return {"unique_blocks": len(uniq), "unique_tokens": tokens_unique}
+
+
 def _log_uniform_int(lo: int, hi: int):
     def f(rng, b):
         x = rng.uniform(math.log(lo), math.log(hi), size=b)
@@ -176,6 +207,13 @@ WORKLOADS["gqa_decode_p16"] = WorkloadSpec(
     name="gqa_decode_p16", tq=[1] * 16, kv_lens=_uniform_int(4096, 32768), num_q_heads=64, num_kv_heads=8,
     page_size=64, topk=16, causal=False, selection="uniform_last", seed=1012,
     description="profiling copy of gqa_decode with 16 sequences")
+
+# The skewed decode batch read as sequences that share cached prefixes: the
+# hot sequences of each group point their first 64 blocks at the group's
+# first hot sequence's pages (the cross-sequence dedup case).
+WORKLOADS["skewed_decode_shared"] = dataclasses.replace(
+    WORKLOADS["skewed_decode"], name="skewed_decode_shared", extra={"shared_prefix_blocks": 64},
+    description="skewed_decode with each hot group's first 64 blocks on shared prefix pages")
 
 # The five workloads, in a fixed order.
 WORKLOAD_ORDER = ["tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode"]
