@@ -51,7 +51,7 @@ DEFAULT_WORKLOAD = "all"
 # the five sparse workloads, in order; the headline is the largest one that fits one GPU
 SPARSE_WORKLOADS = ("tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode")
 # run with the dedup index (mxsa_build_index_dedup + mxsa_schedule: 4 launches a step)
-DEDUP_WORKLOADS = ("skewed_decode_shared",)
+DEDUP_WORKLOADS = ("skewed_decode_shared", "skewed_decode_shared_p64")
 HEADLINE_WORKLOAD = "skewed_decode"
 
 
@@ -595,7 +595,7 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     import block_sparse_attention_builder_gb300 as mx
     dev = torch.device("cuda", local_rank)
     from block_sparse_attention_builder_gb300 import workloads as W
-    dedup = name in DEDUP_WORKLOADS
+    dedup = name in DEDUP_WORKLOADS if args.index == "auto" else args.index == "dedup"
     w = load_workload(name, rank)
     stats = _stats(w)
     if dedup:  # a shared block is loaded once for every sequence that holds it
@@ -981,6 +981,9 @@ def main():
     ap.add_argument("--plan", default="fused", choices=["fused", "separate"],
                     help="index + schedule in one launch (mxsa_plan, default) or as mxsa_build_index then "
                          "mxsa_schedule")
+    ap.add_argument("--index", default="auto", choices=["auto", "plain", "dedup"],
+                    help="the index a sparse workload runs on: auto = dedup for " + ", ".join(DEDUP_WORKLOADS) +
+                         ", plain for the others")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

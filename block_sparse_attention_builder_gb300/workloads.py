@@ -215,6 +215,13 @@ WORKLOADS["skewed_decode_shared"] = dataclasses.replace(
     WORKLOADS["skewed_decode"], name="skewed_decode_shared", extra={"shared_prefix_blocks": 64},
     description="skewed_decode with each hot group's first 64 blocks on shared prefix pages")
 
+# Profiling copy of skewed_decode_shared with 64 sequences (4 hot sequences
+# per group share their prefix pages).
+WORKLOADS["skewed_decode_shared_p64"] = dataclasses.replace(
+    WORKLOADS["skewed_decode_shared"], name="skewed_decode_shared_p64", tq=[1] * 64,
+    kv_lens=_log_uniform_int(1024, 32768), seed=1015,
+    description="profiling copy of skewed_decode_shared: 64 sequences, L log-U[1K, 32K]")
+
 # The five workloads, in a fixed order.
 WORKLOAD_ORDER = ["tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode"]
 
