@@ -85,7 +85,12 @@ def _quantile_table(dtype: str) -> torch.Tensor:
     return _TABLES[dtype]
 
 
-TORCH_DTYPE = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8": torch.float8_e4m3fn}
+TORCH_DTYPE = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8": torch.float8_e4m3fn, "nvfp4": torch.uint8}
+
+# NVFP4 cache slabs: per (page, kv head), page_size rows of 64 code bytes then
+# page_size rows of 8 scale bytes (72 bytes per position)
+NVFP4_ROW_BYTES = HEAD_DIM // 2 + HEAD_DIM // 16
+NVFP4_SCALE_BASE = 0x18  # e4m3 codes 0x18 .. 0x37: scales 2^-4 .. 15/32
 
 
 def stream_key(seed: int, tensor_id: int) -> int:
@@ -103,6 +108,28 @@ def generate_values(numel: int, key: int, dtype: str, device, start: int = 0, ch
         out[c0:c0 + n] = table[(h >> 16) & 0xFFFF]
         del idx, h
     return out.view(TORCH_DTYPE[dtype])
+
+
+def nvfp4_bytes_at(idx: torch.Tensor, key: int, page_size: int) -> torch.Tensor:
+    """Bytes at the int64 flat indices `idx` of an NVFP4 cache drawn from the
+    stream `key`: code bytes uniform over all 256 values (two uniform E2M1
+    codes), scale bytes uniform over the 32 E4M3 codes from NVFP4_SCALE_BASE
+    (2^-4 up to 15/32).  Raw draws only: no value is quantised."""
+    h = (_hash_index(idx, key) >> 16) & 0xFFFF
+    in_slab = idx % (page_size * NVFP4_ROW_BYTES)
+    scale = in_slab >= page_size * (HEAD_DIM // 2)
+    return torch.where(scale, NVFP4_SCALE_BASE + (h & 31), h & 0xFF).to(torch.uint8)
+
+
+def generate_nvfp4(numel: int, key: int, page_size: int, device, chunk: int = 1 << 25) -> torch.Tensor:
+    """The first `numel` bytes of an NVFP4 cache (see nvfp4_bytes_at)."""
+    out = torch.empty(numel, dtype=torch.uint8, device=device)
+    for c0 in range(0, numel, chunk):
+        n = min(chunk, numel - c0)
+        idx = torch.arange(c0, c0 + n, dtype=torch.int64, device=device)
+        out[c0:c0 + n] = nvfp4_bytes_at(idx, key, page_size)
+        del idx
+    return out
 
 
 def generate_at(idx: torch.Tensor, key: int, dtype: str) -> torch.Tensor:
@@ -278,6 +305,10 @@ class Workload:
         return v.view(self.total_q, self.num_q_heads, HEAD_DIM)
 
     def _cache(self, tensor_id: int, device) -> torch.Tensor:
+        if self.spec.kv_dtype == "nvfp4":
+            n = self.num_pages * self.num_kv_heads * self.page_size * NVFP4_ROW_BYTES
+            v = generate_nvfp4(n, stream_key(self.spec.seed, tensor_id), self.page_size, device)
+            return v.view(self.num_pages, self.num_kv_heads, self.page_size * NVFP4_ROW_BYTES)
         n = self.num_pages * self.num_kv_heads * self.page_size * HEAD_DIM
         v = generate_values(n, stream_key(self.spec.seed, tensor_id), self.spec.kv_dtype, device)
         return v.view(self.num_pages, self.num_kv_heads, self.page_size, HEAD_DIM)
@@ -315,8 +346,15 @@ class Workload:
     def cache_pages(self, tensor_id: int, pages: np.ndarray, device="cpu") -> torch.Tensor:
         """Pages `pages` of the K (2) or V (3) cache as a CPU tensor.  The
         values are generated on `device` (identical bits on any device)."""
-        per_page = self.num_kv_heads * self.page_size * HEAD_DIM
         key = stream_key(self.spec.seed, tensor_id)
+        if self.spec.kv_dtype == "nvfp4":
+            per_page = self.num_kv_heads * self.page_size * NVFP4_ROW_BYTES
+            pg = torch.as_tensor(np.asarray(pages, dtype=np.int64)).to(device)
+            ar = torch.arange(per_page, dtype=torch.int64, device=device)
+            idx = (pg[:, None] * per_page + ar[None, :]).reshape(-1)
+            out = nvfp4_bytes_at(idx, key, self.page_size).cpu()
+            return out.view(len(pages), self.num_kv_heads, self.page_size * NVFP4_ROW_BYTES)
+        per_page = self.num_kv_heads * self.page_size * HEAD_DIM
         pages = torch.as_tensor(np.asarray(pages, dtype=np.int64)).to(device)
         raw = _quantile_table(self.spec.kv_dtype)
         out = torch.empty(len(pages) * per_page, dtype=raw.dtype)

@@ -15,6 +15,10 @@ Functions whose parity is pinned by tests/test_oracle_pins.py:
   decode          -- every code against torch's own dtype conversions
   encode_e4m3, store -- every bf16/fp16 code against torch's clamp-and-cast
                      (tests/test_store_pins.py)
+  encode_e2m1, NVFP4 store and attention -- E2M1 / E4M3 conversions against
+                     ml_dtypes, a hand-made layout fixture, attention on
+                     NVFP4 caches against the same values in a BF16 cache
+                     (tests/test_nvfp4_pins.py)
   select_blocks   -- top-k block selection: exact float64 scores and a
                      brute-force ranking, ties, masks, pages
                      (tests/test_select_pins.py)
@@ -33,7 +37,7 @@ _SRC = os.path.join(_HERE, "mxsa_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-DTYPE_CODE = {"bf16": 0, "fp16": 1, "fp8": 2}
+DTYPE_CODE = {"bf16": 0, "fp16": 1, "fp8": 2, "nvfp4": 3}
 
 
 def build(force: bool = False) -> str:
@@ -90,6 +94,8 @@ def _load():
         _lib.oracle_block_owners.argtypes = [P, P, P, P, ctypes.c_int64]
         _lib.oracle_encode_e4m3.restype = ctypes.c_uint32
         _lib.oracle_encode_e4m3.argtypes = [ctypes.c_double]
+        _lib.oracle_encode_e2m1.restype = ctypes.c_uint32
+        _lib.oracle_encode_e2m1.argtypes = [ctypes.c_float]
         _lib.oracle_store.restype = ctypes.c_int64
         _lib.oracle_store.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int64, P, P, P]
@@ -140,17 +146,29 @@ def encode_e4m3(x: float) -> int:
     return int(_load().oracle_encode_e4m3(float(x)))
 
 
+def encode_e2m1(y: float) -> int:
+    """The E2M1 code of the single-precision y: nearest value, ties to even,
+    saturating at 6, with y's sign."""
+    return int(_load().oracle_encode_e2m1(float(y)))
+
+
 def store(src, loc, cache, page_size: int, src_dtype: str, dst_dtype: str) -> int:
     """Paged-cache store (the write side of the KV cache): rows of `src`
-    [n, heads, dim] (bf16/fp16, torch tensor or raw bits) into `cache`
-    [num_pages, heads, page_size, dim] (raw bits, numpy, updated in place) at
-    slots loc[t] = page * page_size + offset; loc < 0 stores nothing.  Returns
-    the number of tokens whose slot lies past the cache."""
+    [n, heads, dim] (bf16/fp16, torch tensor or raw bits) into `cache` (raw
+    bits, numpy, updated in place) at slots loc[t] = page * page_size +
+    offset; loc < 0 stores nothing.  `cache` is [num_pages, heads,
+    page_size, dim], or for dst_dtype "nvfp4" the byte slabs [num_pages,
+    heads, page_size * (dim / 2 + dim / 16)].  Returns the number of tokens
+    whose slot lies past the cache."""
     lib = _load()
     sb = _c(_bits(src), np.uint16)
     n, heads, dim = (int(v) for v in sb.shape)
     lo = _c(loc, np.int64)
-    assert cache.flags["C_CONTIGUOUS"] and cache.shape[1:] == (heads, page_size, dim)
+    if dst_dtype == "nvfp4":
+        assert cache.flags["C_CONTIGUOUS"] and cache.dtype == np.uint8
+        assert cache.shape[1:] == (heads, page_size * (dim // 2 + dim // 16))
+    else:
+        assert cache.flags["C_CONTIGUOUS"] and cache.shape[1:] == (heads, page_size, dim)
     rc = lib.oracle_store(DTYPE_CODE[src_dtype], DTYPE_CODE[dst_dtype], n, heads, dim, page_size, cache.shape[0],
                           _ptr(lo), _ptr(sb), _ptr(cache))
     if rc < 0:

@@ -31,7 +31,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_BF16 = 0, OR_FP16 = 1, OR_FP8_E4M3 = 2 };
+enum { OR_BF16 = 0, OR_FP16 = 1, OR_FP8_E4M3 = 2, OR_NVFP4 = 3 };
 
 /* status bits shared in meaning (not in code) with the GPU library */
 enum {
@@ -92,11 +92,21 @@ static double decode_e4m3(uint32_t bits) {
   return s ? -v : v;
 }
 
+/* OCP MX FP4 E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit; no
+ * infinities or NaN.  E = 0: m * 0.5; E > 0: 2^(E-1) * (1 + m/2); so the
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+static double decode_e2m1(uint32_t bits) {
+  uint32_t s = (bits >> 3) & 1u, e = (bits >> 1) & 3u, m = bits & 1u;
+  double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, (int)e - (MUT(23) ? 2 : 1)); /* mutant 23: bias 2 */
+  return s ? -v : v;
+}
+
 double oracle_decode(int32_t dtype, uint32_t bits) {
   switch (dtype) {
     case OR_BF16: return decode_bf16(bits);
     case OR_FP16: return decode_fp16(bits);
     case OR_FP8_E4M3: return decode_e4m3(bits);
+    case OR_NVFP4: return decode_e2m1(bits);
     default: return NAN;
   }
 }
@@ -104,6 +114,34 @@ double oracle_decode(int32_t dtype, uint32_t bits) {
 static double load_elem(const void* base, int32_t dtype, int64_t idx) {
   if (dtype == OR_FP8_E4M3) return decode_e4m3(((const uint8_t*)base)[idx]);
   return oracle_decode(dtype, ((const uint16_t*)base)[idx]);
+}
+
+/* NVFP4 KV cache (the MSA summary page, "Highlighted Details", lists NVFP4
+ * among the formats of its sparse attention and decoding; the layout and
+ * the scaling below are this library's reading):
+ *   - each 16 consecutive elements of a row (one position of one kv head)
+ *     share an E4M3 scale; element value = e2m1(code) * e4m3(scale), with
+ *     no per-tensor scale;
+ *   - a (page, kv head) slab of ps positions holds ps rows of D/2 bytes of
+ *     codes (element 2i in the low nibble of byte i, 2i + 1 in the high
+ *     nibble), then ps rows of D/16 scale bytes (scale j covers elements
+ *     16 j .. 16 j + 15); slabs follow each other as [page][kv head].
+ * Element `idx` of the row-major view [page][kv head][ps][D] used for the
+ * other dtypes: */
+static double load_nvfp4(const void* base, int32_t ps, int32_t D, int64_t idx) {
+  const int64_t row = idx / D, d = idx % D;
+  const int64_t slab = row / ps, pos = row % ps;
+  const uint8_t* sb = (const uint8_t*)base + slab * ps * (D / 2 + D / 16);
+  const uint8_t byte = sb[pos * (D / 2) + d / 2];
+  const uint32_t code = (MUT(22) ? !(d & 1) : (d & 1)) ? (byte >> 4) : (byte & 0xFu); /* mutant 22: nibbles swapped */
+  const uint8_t scale = sb[(int64_t)ps * (D / 2) + pos * (D / 16) + d / 16];
+  return decode_e2m1(code) * decode_e4m3(scale);
+}
+
+/* a K or V element of the paged cache, element idx of [page][kv head][ps][D] */
+static double load_kv(const void* base, const oracle_problem* p, int64_t idx) {
+  if (p->kv_dtype == OR_NVFP4) return load_nvfp4(base, p->page_size, p->head_dim, idx);
+  return load_elem(base, p->kv_dtype, idx);
 }
 
 /* sequence of token t: the s with cu[s] <= t < cu[s+1] (linear scan) */
@@ -178,7 +216,7 @@ static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double
     int64_t base = MUT(8) ? (((int64_t)page * ps + pp % ps) * Hkv + g) * D /* mutant 8: [page][pos][head] */
                           : (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
     double dot = 0.0;
-    for (int32_t d = 0; d < D; ++d) dot += qv[d] * load_elem(J->k, p->kv_dtype, base + d);
+    for (int32_t d = 0; d < D; ++d) dot += qv[d] * load_kv(J->k, p, base + d);
     sc[pp] = scale * dot;
     if (sc[pp] > m) m = sc[pp];
     ++count;
@@ -192,7 +230,7 @@ static int attn_row(const attn_job* J, int64_t t, int32_t h, double* out, double
                             : (((int64_t)page * Hkv + g) * ps + pp % ps) * D;
       double w = exp(sc[pp] - m);
       l += w;
-      for (int32_t d = 0; d < D; ++d) out[d] += w * load_elem(J->v, p->kv_dtype, base + d);
+      for (int32_t d = 0; d < D; ++d) out[d] += w * load_kv(J->v, p, base + d);
     }
     for (int32_t d = 0; d < D; ++d) out[d] /= l;
     *lse_out = m + (MUT(9) ? log2(l) : log(l)); /* mutant 9: lse in base 2 */
@@ -693,6 +731,7 @@ int oracle_select_blocks(const oracle_problem* p, int32_t dim, const void* iq, c
                          const int32_t* block_tables, const int64_t* cu, const int32_t* lens, int32_t* sel_out,
                          float* score_out, int64_t max_blocks, const int64_t* rows, int64_t nrows,
                          int32_t nthreads) {
+  if (p->kv_dtype == OR_NVFP4) return -2; /* index keys are 16-bit or FP8 */
   select_job J;
   memset(&J, 0, sizeof(J));
   J.p = p;
@@ -745,7 +784,8 @@ int oracle_select_blocks(const oracle_problem* p, int32_t dim, const void* iq, c
  *     covering run positions [i*len/n, (i+1)*len/n);  item = {position of
  *     its first key in the active-key list, entry of that key, 1, nkeys};
  *     cost = sum over its keys of valid_tokens * kv_weight + nkeys * 64 + 256.
- *   valid_tokens = min(128, L_s - 128 b); kv_weight = 2 (16-bit) or 1 (FP8).
+ *   valid_tokens = min(128, L_s - 128 b); kv_weight = 2 (16-bit caches) or 1
+ *   (FP8 and NVFP4, whose blocks are widened before the MMAs).
  *   Each list (normal, decode) gets its own exclusive cost prefix (total C)
  *   and its own partition: cta_ptr[c] = #{items i : prefix[i] < floor(c*C/P)}.
  * items rows: {key, entry_begin, n_entries, 0} (normal);
@@ -803,7 +843,7 @@ int oracle_schedule(const oracle_problem* p, const int32_t* lens, const int64_t*
   const int32_t G = p->num_q_heads / Hkv;
   const int32_t per_tile = 128 / G > 0 ? 128 / G : 1;
   const int64_t E = (int64_t)rows_per_item_tiles * per_tile;
-  const int32_t kvw = p->kv_dtype == OR_FP8_E4M3 ? 1 : 2;
+  const int32_t kvw = (p->kv_dtype == OR_BF16 || p->kv_dtype == OR_FP16) ? 2 : 1;
   const int64_t nkeys = (int64_t)Hkv * nb;
   /* the active keys, in key order */
   int64_t n_active = 0;
@@ -935,14 +975,53 @@ static uint8_t encode_e4m3(double x) {
 
 uint32_t oracle_encode_e4m3(double x) { return encode_e4m3(x); }
 
+/* NVFP4 store of one 16-element group (the NVFP4 reading above; the
+ * scaling rule is the library's):
+ *   amax = the largest |x| over the group's non-NaN elements (0 if none);
+ *   scale code = e4m3(amax / 6): the division in IEEE single precision,
+ *   then the FP8 store's rounding (clamp to 448, nearest, ties to even);
+ *   with sd = the scale's value, an element's code is 0 when sd is 0 or x is
+ *   NaN; otherwise the E2M1 value nearest to y = x / sd (single-precision
+ *   division), ties to the even mantissa, magnitudes above 6 saturating to
+ *   6, with the sign of y. */
+static uint8_t encode_e2m1(float y) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const uint8_t sign = signbit(y) ? 8 : 0;
+  const double a = fabs((double)y);
+  int i = 0;
+  while (i < 7) {
+    const double mid = 0.5 * (mag[i] + mag[i + 1]);
+    if (a < mid) break;
+    if (a == mid) {
+      if ((i % 2 != 0) != MUT(24)) ++i; /* a tie goes to the even index (mutant 24: to the odd one) */
+      break;
+    }
+    ++i;
+  }
+  return (uint8_t)(sign | i);
+}
+
+static void encode_nvfp4_group(const float* x, uint8_t* codes, uint8_t* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i)
+    if (!isnan(x[i]) && fabsf(x[i]) > amax) amax = fabsf(x[i]);
+  const float s = amax / (MUT(25) ? 4.0f : 6.0f); /* mutant 25: scaled to 4, not 6 */
+  *scale = encode_e4m3((double)s);
+  const float sd = (float)decode_e4m3(*scale);
+  for (int i = 0; i < 16; ++i) codes[i] = (sd == 0.0f || isnan(x[i])) ? 0 : encode_e2m1(x[i] / sd);
+}
+
+uint32_t oracle_encode_e2m1(float y) { return encode_e2m1(y); }
+
 /* Stores n tokens' rows of `src` ([n][heads][dim], dtype src_dtype: bf16 or
  * fp16) into `cache` ([num_pages][heads][page_size][dim], dtype dst_dtype:
  * src_dtype or e4m3).  Returns the number of tokens whose loc lies at or
  * past num_pages * page_size (stored nowhere), or -3 for bad arguments. */
 int64_t oracle_store(int32_t src_dtype, int32_t dst_dtype, int64_t n, int32_t heads, int32_t dim,
                      int32_t page_size, int64_t num_pages, const int64_t* loc, const void* src, void* cache) {
-  if ((src_dtype != OR_BF16 && src_dtype != OR_FP16) || (dst_dtype != src_dtype && dst_dtype != OR_FP8_E4M3) ||
-      n < 0 || heads <= 0 || dim <= 0 || page_size <= 0 || num_pages < 0)
+  if ((src_dtype != OR_BF16 && src_dtype != OR_FP16) ||
+      (dst_dtype != src_dtype && dst_dtype != OR_FP8_E4M3 && dst_dtype != OR_NVFP4) || n < 0 || heads <= 0 ||
+      dim <= 0 || page_size <= 0 || num_pages < 0 || (dst_dtype == OR_NVFP4 && dim % 16 != 0))
     return -3;
   int64_t bad = 0;
   for (int64_t t = 0; t < n; ++t) {
@@ -952,6 +1031,25 @@ int64_t oracle_store(int32_t src_dtype, int32_t dst_dtype, int64_t n, int32_t he
       continue;
     }
     const int64_t page = loc[t] / page_size, off = loc[t] % page_size;
+    if (dst_dtype == OR_NVFP4) {
+      /* the slab layout of the NVFP4 reading above */
+      for (int32_t h = 0; h < heads; ++h) {
+        uint8_t* sb = (uint8_t*)cache + (page * heads + h) * (int64_t)page_size * (dim / 2 + dim / 16);
+        for (int32_t j = 0; j < dim / 16; ++j) {
+          float x[16];
+          uint8_t codes[16], scale;
+          for (int i = 0; i < 16; ++i) {
+            const uint16_t bits = ((const uint16_t*)src)[(t * heads + h) * dim + 16 * j + i];
+            x[i] = (float)(src_dtype == OR_BF16 ? decode_bf16(bits) : decode_fp16(bits));
+          }
+          encode_nvfp4_group(x, codes, &scale);
+          for (int i = 0; i < 16; i += 2)
+            sb[off * (dim / 2) + (16 * j + i) / 2] = (uint8_t)(codes[i] | (codes[i + 1] << 4));
+          sb[(int64_t)page_size * (dim / 2) + off * (dim / 16) + j] = scale;
+        }
+      }
+      continue;
+    }
     for (int32_t h = 0; h < heads; ++h)
       for (int32_t d = 0; d < dim; ++d) {
         const int64_t si = (t * heads + h) * dim + d;

@@ -12,7 +12,7 @@ import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PINS = ["tests/test_oracle_pins.py", "tests/test_store_pins.py", "tests/test_dedup_pins.py",
-        "tests/test_select_pins.py"]
+        "tests/test_select_pins.py", "tests/test_nvfp4_pins.py"]
 MUTANTS = {
     1: "bf16 decoding with misplaced bits",
     2: "e4m3 decoding with the wrong exponent bias",
@@ -35,6 +35,10 @@ MUTANTS = {
     19: "selection scores drop the last index dimension",
     20: "selection scores a block by its minimum",
     21: "schedule treats a shared key of several entries as a decode key",
+    22: "NVFP4 nibbles read in the swapped order",
+    23: "E2M1 decoding with exponent bias 2",
+    24: "E2M1 encoding rounds ties to the odd code",
+    25: "NVFP4 group scale amax / 4 instead of amax / 6",
 }
 
 
