@@ -8,8 +8,9 @@ resident in HBM.  Prints ONE JSON line (rank 0).
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
 With no --workload (or --workload all) the line carries all five sparse
-workloads and skewed_decode_shared (skewed_decode on shared prefix pages,
-run through the dedup index: dedup build + scheduler + forward + combine):
+workloads, skewed_decode_shared (skewed_decode on shared prefix pages,
+run through the dedup index: dedup build + scheduler + forward + combine)
+and gqa_decode_nvfp4 (gqa_decode on an NVFP4 cache):
 each is measured in turn (its own warm-up, timed steps, end-to-end steps and
 oracle baseline) and listed under "workloads"; the line's own value,
 roofline, e2e and cpu_baseline are those of skewed_decode, the largest
@@ -52,6 +53,8 @@ DEFAULT_WORKLOAD = "all"
 SPARSE_WORKLOADS = ("tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode")
 # run with the dedup index (mxsa_build_index_dedup + mxsa_schedule: 4 launches a step)
 DEDUP_WORKLOADS = ("skewed_decode_shared", "skewed_decode_shared_p64")
+# the "next" rows' variants measured in the default run besides the five
+EXTRA_WORKLOADS = ("skewed_decode_shared", "gqa_decode_nvfp4")
 HEADLINE_WORKLOAD = "skewed_decode"
 
 
@@ -179,16 +182,19 @@ def workload_config(w, stats, name):
             "the step's unique KV also exceeds L2", "kv_cache": "resident in HBM (model state)"}
 
 
+# bytes of one cached position of one kv head (K or V)
+KV_ROW_BYTES = {"bf16": 256, "fp16": 256, "fp8": 128, "nvfp4": 72}
+
+
 def algorithmic(w, stats):
-    kv_elem = 1 if w.spec.kv_dtype == "fp8" else 2
-    unique_kv_bytes = stats["unique_tokens"] * 128 * 2 * kv_elem
+    unique_kv_bytes = stats["unique_tokens"] * KV_ROW_BYTES[w.spec.kv_dtype] * 2
     flops = 4 * 128 * stats["visit_keys"] * (w.num_q_heads // w.num_kv_heads)
     io_bytes = (w.total_q * w.num_q_heads * 128 * 2 * 2 + w.total_q * w.num_q_heads * 4 + w.selected.nbytes
                 + w.block_tables.nbytes + w.cu_seqlens_q.nbytes + w.used_kv_lens.nbytes)
     # one partial row per (row, block visit): 128 values (FP32 with FP8
     # caches, else the 16-bit q dtype) and an FP32 lse, written by the
     # forward and read back by the combine
-    ps = 4 if w.spec.kv_dtype == "fp8" else 2
+    ps = 4 if w.spec.kv_dtype in ("fp8", "nvfp4") else 2
     partial_bytes = stats["block_visits"] * (w.num_q_heads // w.num_kv_heads) * (128 * ps + 4) * 2
     return unique_kv_bytes, flops, io_bytes, partial_bytes
 
@@ -612,7 +618,8 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
     lens = torch.from_numpy(w.used_kv_lens).to(dev)
     prob = mx.make_problem(w.num_seqs, w.total_q, w.num_q_heads, w.num_kv_heads, w.topk, w.page_size,
-                           w.num_pages, w.max_pages_per_seq, w.causal, 0.0, q.dtype, k.dtype)
+                           w.num_pages, w.max_pages_per_seq, w.causal, 0.0, q.dtype,
+                           "nvfp4" if w.spec.kv_dtype == "nvfp4" else k.dtype)
     attn = mx.SparseAttention(prob, dev, dedup=dedup)
     out = torch.empty_like(q)
     lse = torch.empty(w.num_q_heads, w.total_q, dtype=torch.float32, device=dev)
@@ -758,7 +765,9 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     entry = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.spec.kv_dtype if w.spec.kv_dtype != "fp8" else "fp8-e4m3 kv, bf16 q",
+        "vs_baseline": None,
+        "dtype": {"fp8": "fp8-e4m3 kv, bf16 q", "nvfp4": "nvfp4 kv (e2m1 + e4m3 scale per 16), bf16 q"}.get(
+            w.spec.kv_dtype, w.spec.kv_dtype),
         "data": "synthetic (seeded counter-based N(0,1) values; selections per the workload recipe)",
         "config": workload_config(w, stats, name),
         "tflops": tflops, "unique_kv_gbs": kv_gbs, "step_roofline": step_roof,
@@ -972,9 +981,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    help="'all' (default): the five sparse workloads and the dedup one in one line, headline "
+                    help="'all' (default): the five sparse workloads, the dedup one and the NVFP4 one in one line, headline "
                          "skewed_decode; "
                          "or one of " + ", ".join(list(SPARSE_WORKLOADS) + list(DEDUP_WORKLOADS) +
+                                                  ["gqa_decode_nvfp4", "gqa_decode_p16"] +
                                                   ["kv_store", "dense_prefill"] +
                                                   list(SELECT_WORKLOADS)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1015,7 +1025,7 @@ def main():
     B.build()
     torch.cuda.set_device(local_rank)
     if args.workload == "all":
-        names, headline = list(SPARSE_WORKLOADS) + list(DEDUP_WORKLOADS), HEADLINE_WORKLOAD
+        names, headline = list(SPARSE_WORKLOADS) + list(EXTRA_WORKLOADS), HEADLINE_WORKLOAD
     else:
         names, headline = [args.workload], args.workload
     entries = {}

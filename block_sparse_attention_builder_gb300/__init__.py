@@ -28,9 +28,13 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libmxsa.so")
 
-BF16, FP16, FP8_E4M3 = 0, 1, 2
-_DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16, torch.float8_e4m3fn: FP8_E4M3}
-_CODE_DTYPE = {v: k for k, v in _DTYPE_CODE.items()}
+BF16, FP16, FP8_E4M3, NVFP4 = 0, 1, 2, 3
+_DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: FP16, torch.float8_e4m3fn: FP8_E4M3, "nvfp4": NVFP4}
+_CODE_DTYPE = {BF16: torch.bfloat16, FP16: torch.float16, FP8_E4M3: torch.float8_e4m3fn, NVFP4: torch.uint8}
+# NVFP4 caches are bytes [pages, Hkv, page_size * NVFP4_ROW_BYTES]: per (page,
+# kv head), page_size rows of 64 E2M1 code bytes, then page_size rows of 8
+# E4M3 scale bytes (one per 16 elements)
+NVFP4_ROW_BYTES = 72
 
 FLAG_NAMES = {1: "SEL_RANGE", 2: "SEL_DUP", 4: "PAGE", 8: "CAUSAL_LEN", 16: "LEN", 32: "TIMEOUT",
               64: "SCHEDULE", 128: "CU"}
@@ -139,6 +143,7 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 _ELEM_BYTES = {BF16: 2, FP16: 2, FP8_E4M3: 1}
+_ROW_BYTES = {BF16: 256, FP16: 256, FP8_E4M3: 128, NVFP4: NVFP4_ROW_BYTES}  # per (position, kv head)
 
 
 def _need(what: str, name: str, t: Optional[torch.Tensor], nbytes: int):
@@ -159,7 +164,8 @@ def _need_attention(what: str, prob: Problem, q=None, k_cache=None, v_cache=None
                     cu_seqlens_q=None, used_kv_lens=None, sel=None, out=None, lse=None):
     qb, kb = _ELEM_BYTES.get(prob.q_dtype, 2), _ELEM_BYTES.get(prob.kv_dtype, 2)
     rows = max(prob.total_q, 0) * max(prob.num_q_heads, 0)
-    cache = max(prob.num_pages, 0) * max(prob.num_kv_heads, 0) * max(prob.page_size, 0) * 128 * kb
+    cache = max(prob.num_pages, 0) * max(prob.num_kv_heads, 0) * max(prob.page_size, 0) * \
+        _ROW_BYTES.get(prob.kv_dtype, 256)
     _need(what, "q", q, rows * 128 * qb)
     _need(what, "k_cache", k_cache, cache)
     _need(what, "v_cache", v_cache, cache)
@@ -179,6 +185,8 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def make_problem(num_seqs, total_q, num_q_heads, num_kv_heads, topk, page_size, num_pages, max_pages_per_seq,
                  causal=False, softmax_scale=0.0, q_dtype=torch.bfloat16, kv_dtype=None, head_dim=128) -> Problem:
+    """kv_dtype: q_dtype (None), torch.float8_e4m3fn, or "nvfp4" (byte caches
+    in the NVFP4_ROW_BYTES layout)."""
     kv_dtype = q_dtype if kv_dtype is None else kv_dtype
     return Problem(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, topk, page_size, num_pages,
                    max_pages_per_seq, int(bool(causal)), float(softmax_scale or 0.0), _DTYPE_CODE[q_dtype],
@@ -408,7 +416,7 @@ def kvouter_attention(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q,
     """Block-sparse KV-outer attention with the README Quick-start call shape.
 
     q [Tq, Hq, 128] bf16/fp16; k_cache/v_cache [pages, Hkv, page_size, 128]
-    (q's dtype or float8_e4m3fn); selected int32 [Tq, Hkv, topk]; block_tables
+    (q's dtype or float8_e4m3fn), or NVFP4 uint8 [pages, Hkv, page_size * 72]; selected int32 [Tq, Hkv, topk]; block_tables
     int32 [B, max_pages]; cu_seqlens_q int64 [B+1]; used_kv_lens int32 [B].
     Returns (output [Tq, Hq, 128], lse [Hq, Tq] float32 or None).  With
     check=True the device status word is read (one stream sync) and data
@@ -426,11 +434,18 @@ def kvouter_attention(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q,
     if cu_seqlens_q.dtype != torch.int64:
         raise ValueError("cu_seqlens_q must be int64")
     Tq, Hq, D = q.shape
-    pages, Hkv, ps, D2 = k_cache.shape
-    if k_cache.shape != v_cache.shape or D2 != D or ps != page_size:
-        raise ValueError("k_cache / v_cache shapes disagree with q or page_size")
+    if k_cache.dtype == torch.uint8:  # NVFP4 byte slabs [pages, Hkv, page_size * 72]
+        pages, Hkv, row = k_cache.shape
+        if k_cache.shape != v_cache.shape or D != 128 or row != page_size * NVFP4_ROW_BYTES:
+            raise ValueError("NVFP4 k_cache / v_cache must be [pages, Hkv, page_size * 72] bytes")
+        kv_dtype = "nvfp4"
+    else:
+        pages, Hkv, ps, D2 = k_cache.shape
+        if k_cache.shape != v_cache.shape or D2 != D or ps != page_size:
+            raise ValueError("k_cache / v_cache shapes disagree with q or page_size")
+        kv_dtype = k_cache.dtype
     prob = make_problem(len(used_kv_lens), Tq, Hq, Hkv, selected.shape[2], page_size, pages,
-                        block_tables.shape[1], causal, softmax_scale or 0.0, q.dtype, k_cache.dtype, head_dim=D)
+                        block_tables.shape[1], causal, softmax_scale or 0.0, q.dtype, kv_dtype, head_dim=D)
     attn = SparseAttention(prob, q.device, num_ctas, dedup=dedup)
     out, lse = attn(q, k_cache, v_cache, selected, block_tables, cu_seqlens_q, used_kv_lens, return_lse=return_lse)
     if check:

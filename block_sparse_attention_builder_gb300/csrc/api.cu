@@ -42,7 +42,8 @@ mxsa_status validate_shape(const mxsa_problem& p) {
   if (p.num_q_heads / p.num_kv_heads > 128) return MXSA_ERR_UNSUPPORTED;
   if (p.page_size != 64 && p.page_size != 128) return MXSA_ERR_UNSUPPORTED;
   if (p.q_dtype != MXSA_BF16 && p.q_dtype != MXSA_FP16) return MXSA_ERR_UNSUPPORTED;
-  if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3) return MXSA_ERR_UNSUPPORTED;
+  if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3 && p.kv_dtype != MXSA_NVFP4)
+    return MXSA_ERR_UNSUPPORTED;
   if ((int64_t)p.num_pages * p.num_kv_heads >= (1ll << 31)) return MXSA_ERR_UNSUPPORTED;
   if ((int64_t)p.max_pages_per_seq * p.page_size >= (1ll << 30)) return MXSA_ERR_UNSUPPORTED;
   return MXSA_OK;
@@ -447,8 +448,8 @@ mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const i
   mxsa_status s = validate_shape(*problem);
   if (s != MXSA_OK) return s;
   const mxsa_problem& p = *problem;
-  if (p.kv_dtype != p.q_dtype && p.kv_dtype != MXSA_FP8_E4M3) return MXSA_ERR_UNSUPPORTED;
   if (n_tokens < 0 || (idx_k == nullptr) != (idx_cache == nullptr)) return MXSA_ERR_INVALID_ARG;
+  if (p.kv_dtype == MXSA_NVFP4 && idx_k) return MXSA_ERR_UNSUPPORTED;  // index keys stay 16-bit or FP8
   if (idx_k && (idx_heads <= 0 || idx_dim <= 0 || idx_dim % 8 != 0)) return MXSA_ERR_INVALID_ARG;
   if (n_tokens > 0 && (!loc || !k || !v || !k_cache || !v_cache)) return MXSA_ERR_INVALID_ARG;
   if (!aligned(loc, 8) || !aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
@@ -465,6 +466,7 @@ static mxsa_status validate_select(const mxsa_problem& p, int32_t idx_dim) {
   mxsa_status s = validate_problem(p);
   if (s != MXSA_OK) return s;
   if (idx_dim != 64 && idx_dim != 128) return MXSA_ERR_UNSUPPORTED;
+  if (p.kv_dtype == MXSA_NVFP4) return MXSA_ERR_UNSUPPORTED;  // index keys are 16-bit or FP8
   if (p.num_seqs > 1024 || max_blocks_per_seq(p) > 4096) return MXSA_ERR_UNSUPPORTED;
   return MXSA_OK;
 }

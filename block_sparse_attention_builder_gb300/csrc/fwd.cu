@@ -85,6 +85,9 @@ struct FwdArgs {
   int32_t* flags;
   int32_t num_seqs, Hq, Hkv, G, topk, page_size, max_pages, num_pages, causal, kv_fp8, ab_bf16, per_tile;
   int32_t part32;
+  int32_t kv_fp4;     // NVFP4 (kv_fp8 is set too: staged and widened); scale rows from kbase / vbase
+  const uint8_t* kbase;
+  const uint8_t* vbase;
   int32_t q_tma;      // q rows of a tile come by TMA (G % 8 == 0; the map tmqs exists)
   int32_t* claim;     // schedule header word: next item to claim
   int32_t* sch_hdr_mut;  // the schedule header (claim and exit counters)
@@ -196,12 +199,14 @@ __device__ __forceinline__ float softmax_store_p(const float* sv, int h, float s
 }
 
 // Runs the CTA's KV-stationary items (all kThreads threads; 1024-aligned
-// shared memory `sm`; TMEM base `tmem` with 512 columns).  kPart32: FP32
-// partial rows, else the 16-bit q dtype.
-template <bool kPart32>
+// shared memory `sm`; TMEM base `tmem` with 512 columns).  kKV: the cache
+// kind (kKv16, kKvFp8, kKvFp4); widened caches write FP32 partial rows,
+// 16-bit ones rows in the q dtype.
+template <int kKV>
 __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                                    const CUtensorMap& tmqs, const FwdArgs& a, uint8_t* sm,
                                                    uint32_t tmem) {
+  constexpr bool kPart32 = kKV != dec::kKv16;
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Items are claimed dynamically (a global counter), in item order, by the
@@ -316,7 +321,22 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           // FP8: into the staging tile once the previous block was widened
           // out of it (stg_empty); the widening group fills the stage
           ok = mbar_wait(&c.stg_empty, (n & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (ok) {
+          if (ok && a.kv_fp4) {
+            // NVFP4: code rows by TMA, scale rows by bulk copy (K at 0, V
+            // at 16 KB of the staging tile; codes, then scales at 8 KB)
+            uint8_t* stg = sm + kOffStg;
+            uint64_t* sf = &c.stg_full[st];
+            mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 144u);
+            for (int pg = 0; pg < npg; ++pg) {
+              if (pages[pg] < 0) continue;
+              const int z = pages[pg] * a.Hkv + g;
+              const size_t so = (size_t)z * ps * 72 + (size_t)ps * 64;
+              tma_load_3d(stg + pg * ps * 64, &tmk, sf, 0, 0, z);
+              tma_load_3d(stg + 16384 + pg * ps * 64, &tmv, sf, 0, 0, z);
+              bulk_load(stg + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, sf);
+              bulk_load(stg + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, sf);
+            }
+          } else if (ok) {
             uint8_t* stg = sm + kOffStg;
             uint64_t* sf = &c.stg_full[st];
             mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
@@ -511,7 +531,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     };
     for (; ok; ++n) {
       const int st = n & 1, use = n >> 1;
-      if (a.kv_fp8 && st == grp) {
+      if (kKV != dec::kKv16 && st == grp) {
         // widen the staged e4m3 block (row r of K and V) into the stage;
         // rows past the valid tokens become zero.  The producer staged this
         // block only after kv_empty of the stage, so the stage is free.
@@ -519,7 +539,14 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         if (!ok) break;
         const int valid = c.info[st].n > 0 ? c.info[st].valid : 0;  // the end item stages nothing
         const uint8_t* stg = sm + kOffStg;
-        for (int kv = 0; kv < 2; ++kv) {
+        for (int kv = 0; kv < 2 && kKV == dec::kKvFp4; ++kv) {
+          const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
+          if (r < valid)
+            dec::widen_fp4_row(stg + kv * 16384 + r * 64, stg + kv * 16384 + 8192 + r * 8, dst, r, bf16);
+          else
+            for (int ch = 0; ch < 16; ++ch) st_shared_v4(dst + swz(r, ch), 0, 0, 0, 0);
+        }
+        for (int kv = 0; kv < 2 && kKV == dec::kKvFp8; ++kv) {
           const uint8_t* src = stg + kv * 16384 + r * 128;
           const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
 #pragma unroll
@@ -637,7 +664,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           lim = inf.valid;
           if (a.causal) lim = min(lim, pos - 128 * inf.b + 1);
         }
-        if (first && !a.kv_fp8 && r >= inf.valid) {
+        if (first && kKV == dec::kKv16 && r >= inf.valid) {
           // keys past the sequence end must not bring stale values (they may
           // be NaN bit patterns) into P V.  Both groups zero the rows before
           // their own first p v of the item (the fence before p_full orders
@@ -720,7 +747,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
 // The forward: each CTA runs its decode items (decode_body, warps 0-5),
 // then its KV-stationary items (all warps), in one launch.  TMEM (512
 // columns) is allocated once for both phases.
-template <bool kPart32>
+template <int kKV>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
           const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmqs, FwdArgs a,
@@ -747,8 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  if (has_dec) dec::decode_body<16, kPart32>(tmk, tmv, tmq, d, sm, tmem);
-  if (has_kvs) kv_stationary_body<kPart32>(tmk, tmv, tmqs, a, sm, tmem);
+  if (has_dec) dec::decode_body<16, kKV>(tmk, tmv, tmq, d, sm, tmem);
+  if (has_kvs) kv_stationary_body<kKV>(tmk, tmv, tmqs, a, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -771,6 +798,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool make_cache_map(CUtensorMap* m, const void* base, const mxsa_problem& p) {
   auto fn = dec::encode_fn();
   if (!fn) return false;
+  if (p.kv_dtype == MXSA_NVFP4) {
+    // the code rows of the NVFP4 slabs [pages * Hkv][page_size * 72 bytes]:
+    // box = one page's page_size rows of 64 bytes (the scale rows after
+    // them come by bulk copy)
+    cuuint64_t dims[3] = {64, (cuuint64_t)p.page_size, (cuuint64_t)p.num_pages * p.num_kv_heads};
+    cuuint64_t strides[2] = {64, 72 * (cuuint64_t)p.page_size};
+    cuuint32_t box[3] = {64u, (cuuint32_t)p.page_size, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  }
   const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
   const cuuint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {128, (cuuint64_t)p.page_size, (cuuint64_t)p.num_pages * p.num_kv_heads};
@@ -804,19 +844,21 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   // one launch for both work lists (decode runs, KV-stationary tiles)
   dec::DecArgs d;
   CUtensorMap tmq;
-  if (!dec::make_args(p, q, block_tables, ix, sc, part_o, part_lse, &d, &tmq)) {
+  if (!dec::make_args(p, q, k_cache, v_cache, block_tables, ix, sc, part_o, part_lse, &d, &tmq)) {
     *err_detail = 1;
     return cudaErrorInvalidValue;
   }
-  const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
+  const bool fp8 = kv_widened(p);  // FP8 or NVFP4: staged and widened
   const size_t smem = fwd_smem_bytes(fp8);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     const int bytes = (int)std::max(fwd_smem_bytes(true), fwd_smem_bytes(false));
-    attr_err = cudaFuncSetAttribute(k_fwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    attr_err = cudaFuncSetAttribute(k_fwd<dec::kKv16>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(k_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      attr_err = cudaFuncSetAttribute(k_fwd<dec::kKvFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(k_fwd<dec::kKvFp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   FwdArgs a;
@@ -851,12 +893,18 @@ cudaError_t launch_fwd(const mxsa_problem& p, const void* q, const void* k_cache
   a.num_pages = p.num_pages;
   a.causal = p.causal;
   a.kv_fp8 = fp8 ? 1 : 0;
+  a.kv_fp4 = p.kv_dtype == MXSA_NVFP4 ? 1 : 0;
+  a.kbase = static_cast<const uint8_t*>(k_cache);
+  a.vbase = static_cast<const uint8_t*>(v_cache);
   a.ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
   a.per_tile = std::max(1, MXSA_TILE_ROWS / a.G);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 0.08838834764831845f;  // 1/sqrt(128)
   a.scale_log2 = scale * 1.4426950408889634f;
-  if (a.part32) return launch_pdl(k_fwd<true>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
-  return launch_pdl(k_fwd<false>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
+  if (p.kv_dtype == MXSA_NVFP4)
+    return launch_pdl(k_fwd<dec::kKvFp4>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
+  if (p.kv_dtype == MXSA_FP8_E4M3)
+    return launch_pdl(k_fwd<dec::kKvFp8>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
+  return launch_pdl(k_fwd<dec::kKv16>, dim3(num_ctas), dim3(kThreads), smem, st, tmk, tmv, tmq, tmqs, a, d);
 }
 
 }  // namespace mxsa

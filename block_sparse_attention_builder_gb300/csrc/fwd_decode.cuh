@@ -56,6 +56,10 @@ struct Ctrl {
   BlockInfo info[kMaxStages];
 };
 
+// cache kinds, the forward's template parameter: 16-bit (the q dtype), and
+// the two that are staged and widened, FP8 and NVFP4
+constexpr int kKv16 = 0, kKvFp8 = 1, kKvFp4 = 2;
+
 struct DecArgs {
   const int32_t* block_tables;
   const SeqInfo* seq;
@@ -68,7 +72,11 @@ struct DecArgs {
   void* part_o;  // partial rows: FP32 when part32, else the 16-bit q dtype
   float* part_lse;
   int32_t* flags;
-  int32_t num_seqs, Hq, Hkv, G, page_size, max_pages, num_pages, kv_fp8, ab_bf16, ns, part32;
+  // kv_fp8: blocks are staged and widened (FP8 or NVFP4); kv_fp4: NVFP4,
+  // whose scale rows come from kbase / vbase by bulk copies
+  int32_t num_seqs, Hq, Hkv, G, page_size, max_pages, num_pages, kv_fp8, ab_bf16, ns, part32, kv_fp4;
+  const uint8_t* kbase;
+  const uint8_t* vbase;
   float scale_log2;
 };
 
@@ -136,6 +144,49 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
   __half2 h = *reinterpret_cast<__half2*>(&h2);
   float2 f = __half22float2(h);
   return pack2(f.x, f.y, 1);
+}
+
+// NVFP4 rows (E2M1 codes, one E4M3 scale per 16 elements) widened to the
+// q dtype: every code times its scale is exact in FP16 (|values| within
+// [2^-10, 2688]) and in BF16.  Row `row` of a [128][128] tile at `dst` (the
+// swz_kv layout) from its 64 code bytes and 8 scale bytes in shared memory.
+__device__ __forceinline__ void widen_fp4_row(const uint8_t* codes, const uint8_t* scales, uint32_t dst, int row,
+                                              int bf16) {
+  const uint2 sc = *reinterpret_cast<const uint2*>(scales);
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c4 = (cc + row) & 3;  // 32 elements: groups 2 c4 and 2 c4 + 1 (rotated to spread banks)
+    const uint4 raw = *reinterpret_cast<const uint4*>(codes + c4 * 16);
+    const uint32_t sw = ((c4 < 2 ? sc.x : sc.y) >> (16 * (c4 & 1))) & 0xFFFFu;
+    uint32_t s2[2];
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const uint16_t b = (uint16_t)((sw >> (8 * gi)) & 0xFFu);
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2[gi]) : "h"((uint16_t)(b | (b << 8))));
+    }
+    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t h[4];
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+          : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+          : "r"(words[w]));
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[i]), *reinterpret_cast<const __half2*>(&s2[w >> 1]));
+        if (bf16) {
+          const float2 f = __half22float2(v);
+          o[i] = pack2(f.x, f.y, 1);
+        } else {
+          o[i] = *reinterpret_cast<uint32_t*>(&v);
+        }
+      }
+      st_shared_v4(dst + swz_kv(row, 4 * c4 + w), o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 // named barrier 1 over the 128 softmax threads
@@ -225,9 +276,10 @@ __device__ __forceinline__ void wg_reduce(float* v, float* red) {
 // 1024-aligned shared memory `sm` and the CTA's TMEM base `tmem`).  On
 // return every copy and MMA of the phase has completed and its mbarriers are
 // invalidated, so the shared memory is free for the next phase.
-template <int N, bool kPart32>
+template <int N, int kKV>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                                             const DecArgs& a, uint8_t* sm, uint32_t tmem) {
+  constexpr bool kPart32 = kKV != kKv16;
   const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + L.ctrl);
   float* red = reinterpret_cast<float*>(sm + L.red);
@@ -348,6 +400,20 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
                 tma_load_3d(kdst + h * 16384 + pg * 8192, &tmk, &c.kv_full[st], h * 64, 0, z);
                 tma_load_3d(vdst + h * 16384 + pg * 8192, &tmv, &c.kv_full[st], h * 64, 0, z);
               }
+            }
+          } else if (a.kv_fp4) {
+            // NVFP4: code rows by TMA, scale rows by bulk copy, K at 0 and
+            // V at 16 KB of the staging tile (codes, then scales at 8 KB)
+            uint8_t* stg = sm + L.stg;
+            mbar_arrive_expect_tx(&c.stg_full, (uint32_t)present * (uint32_t)ps * 144u);
+            for (int pg = 0; pg < npg; ++pg) {
+              if (pages[pg] < 0) continue;
+              const int z = pages[pg] * a.Hkv + cur.g;
+              const size_t so = (size_t)z * ps * 72 + (size_t)ps * 64;
+              tma_load_3d(stg + pg * ps * 64, &tmk, &c.stg_full, 0, 0, z);
+              tma_load_3d(stg + 16384 + pg * ps * 64, &tmv, &c.stg_full, 0, 0, z);
+              bulk_load(stg + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, &c.stg_full);
+              bulk_load(stg + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, &c.stg_full);
             }
           } else {
             uint8_t* stg = sm + L.stg;
@@ -494,12 +560,19 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
         uint8_t* vst = kst + kKVTile;
         int valid = 0;
         bool okb;
-        if (a.kv_fp8) {
+        if (kKV != kKv16) {
           okb = mbar_wait(&c.stg_full, blk & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
           if (okb) {
             valid = c.info[st].valid;
             const uint8_t* stg = sm + L.stg;
-            for (int kv = 0; kv < 2; ++kv) {
+            for (int kv = 0; kv < 2 && kKV == kKvFp4; ++kv) {
+              const uint32_t dst = smem_u32(kv ? vst : kst);
+              if (k < valid)
+                widen_fp4_row(stg + kv * 16384 + k * 64, stg + kv * 16384 + 8192 + k * 8, dst, k, bf16);
+              else
+                for (int ch = 0; ch < 16; ++ch) st_shared_v4(dst + swz_kv(k, ch), 0, 0, 0, 0);
+            }
+            for (int kv = 0; kv < 2 && kKV == kKvFp8; ++kv) {
               const uint8_t* src = stg + kv * 16384 + k * 128;
               const uint32_t dst = smem_u32(kv ? vst : kst);
               for (int cc = 0; cc < 8; ++cc) {
@@ -704,8 +777,9 @@ inline size_t smem_bytes(bool fp8) {
 
 // Fills the decode phase's arguments and its q tensor map; false when the
 // tensor map cannot be made.
-inline bool make_args(const mxsa_problem& p, const void* q, const int32_t* block_tables, const IndexPtrs& ix,
-                      const SchedPtrs& sc, void* part_o, float* part_lse, DecArgs* a, CUtensorMap* tmq) {
+inline bool make_args(const mxsa_problem& p, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const IndexPtrs& ix, const SchedPtrs& sc, void* part_o,
+                      float* part_lse, DecArgs* a, CUtensorMap* tmq) {
   constexpr int N = 16;
   const int G = p.num_q_heads / p.num_kv_heads;
   *a = DecArgs{};
@@ -730,7 +804,10 @@ inline bool make_args(const mxsa_problem& p, const void* q, const int32_t* block
   a->page_size = p.page_size;
   a->max_pages = p.max_pages_per_seq;
   a->num_pages = p.num_pages;
-  a->kv_fp8 = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 0;
+  a->kv_fp8 = kv_widened(p) ? 1 : 0;
+  a->kv_fp4 = p.kv_dtype == MXSA_NVFP4 ? 1 : 0;
+  a->kbase = static_cast<const uint8_t*>(k_cache);
+  a->vbase = static_cast<const uint8_t*>(v_cache);
   a->ab_bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
   a->ns = stages_for<N>(a->kv_fp8);
   a->part32 = partials_fp32(p) ? 1 : 0;

@@ -126,12 +126,16 @@ constexpr unsigned long long kWaitLimitNs = MXSA_WAIT_LIMIT_NS;
 
 int64_t max_blocks_per_seq(const mxsa_problem& p);
 
+// KV blocks stored narrower than q (FP8, NVFP4) are staged and widened to
+// q's 16-bit type by the softmax warps before the MMAs.
+inline bool kv_widened(const mxsa_problem& p) { return p.kv_dtype == MXSA_FP8_E4M3 || p.kv_dtype == MXSA_NVFP4; }
+
 // Element type of the partial output rows.  With 16-bit caches they are
 // stored in the 16-bit q dtype, which halves the forward's stores and the
-// combine's reads; with FP8 caches they stay FP32 (there the softmax warps
-// also widen the e4m3 blocks, and the packing on their path costs more
+// combine's reads; with widened caches they stay FP32 (there the softmax
+// warps also widen the blocks, and the packing on their path costs more
 // than the smaller rows save).
-inline bool partials_fp32(const mxsa_problem& p) { return p.kv_dtype == MXSA_FP8_E4M3; }
+inline bool partials_fp32(const mxsa_problem& p) { return kv_widened(p); }
 mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L);
 mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L);
 IndexPtrs index_ptrs(const mxsa_problem& p, void* ws);

@@ -600,7 +600,7 @@ cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t
   a.P.B = p.num_seqs;
   a.P.Hkv = p.num_kv_heads;
   a.P.G = G;
-  a.P.kvw = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
+  a.P.kvw = kv_widened(p) ? 1 : 2;
   a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
   a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
   a.P.num_ctas = num_ctas;

@@ -311,7 +311,7 @@ static SchedArgs sched_args(const mxsa_problem& p, const IndexPtrs& ix, const Sc
   a.P.B = p.num_seqs;
   a.P.Hkv = p.num_kv_heads;
   a.P.G = G;
-  a.P.kvw = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
+  a.P.kvw = kv_widened(p) ? 1 : 2;
   a.P.per_tile = std::max(1, MXSA_TILE_ROWS / G);
   a.P.E = MXSA_ITEM_TILES * a.P.per_tile;
   a.P.num_ctas = num_ctas;

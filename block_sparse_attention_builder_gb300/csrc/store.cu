@@ -129,6 +129,97 @@ __global__ void __launch_bounds__(256) k_store(StoreArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ NVFP4
+// The NVFP4 cache (E2M1 codes, one E4M3 scale per 16 elements; the MSA
+// summary page lists the format, the layout and scaling are this library's):
+// a (page, head) slab holds page_size rows of 64 code bytes (element 2i in
+// the low nibble of byte i) and then page_size rows of 8 scale bytes.  A
+// group of 16 values x stores scale = e4m3(amax / 6) (single-precision
+// division, the FP8 cast above) and, with sd the scale's value, codes
+// nearest(x / sd) over the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}, ties
+// to the even code, saturating at 6, with the quotient's sign; NaN elements
+// (which amax ignores) and groups whose scale is 0 store code 0.
+
+// E2M1 code of y: the comparisons put each tie on the even magnitude index
+// (0.25 -> 0, 0.75 and 1.25 -> 1.0, 1.75 and 2.5 -> 2, 3.5 and 5 -> 4)
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const uint32_t sign = (__float_as_uint(y) >> 31) << 3;
+  const float a = fabsf(y);
+  uint32_t i;
+  if (a <= 0.25f) i = 0;
+  else if (a < 0.75f) i = 1;
+  else if (a <= 1.25f) i = 2;
+  else if (a < 1.75f) i = 3;
+  else if (a <= 2.5f) i = 4;
+  else if (a < 3.5f) i = 5;
+  else if (a <= 5.0f) i = 6;
+  else i = 7;
+  return sign | i;
+}
+
+struct StoreFp4Args {
+  const int64_t* loc;
+  const uint16_t* src[2];  // K, V of this launch's first token
+  uint8_t* dst[2];
+  int32_t heads, heads_shift, page_shift, bf16;
+  uint32_t groups;         // tokens * heads * 8
+  long long slots;
+  int32_t* flags;
+};
+
+// one group: its 8 code bytes and its scale byte
+__device__ __forceinline__ void put_group_fp4(const uint16_t* src, uint8_t* codes, uint8_t* scale, int bf16) {
+  const uint4 s0 = __ldcs(reinterpret_cast<const uint4*>(src));
+  const uint4 s1 = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
+  const uint32_t w[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  float x[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = to_f32((uint16_t)(w[i] & 0xFFFFu), bf16);
+    x[2 * i + 1] = to_f32((uint16_t)(w[i] >> 16), bf16);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));  // fmaxf drops a NaN operand
+  uint16_t sc;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(sc) : "f"(0.f), "f"(__fdiv_rn(amax, 6.f)));
+  sc &= 0xFFu;
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(sc));
+  const float sd = __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t c = (sd == 0.f || isnan(x[i])) ? 0u : e2m1_code(__fdiv_rn(x[i], sd));
+    if (i < 8) lo |= c << (4 * i);
+    else hi |= c << (4 * (i - 8));
+  }
+  *reinterpret_cast<uint2*>(codes) = make_uint2(lo, hi);
+  *scale = (uint8_t)sc;
+}
+
+__global__ void __launch_bounds__(256) k_store_fp4(StoreFp4Args a) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const int ps = 1 << a.page_shift;
+  for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < a.groups; g += stride) {
+    const uint32_t row = g >> 3, j = g & 7;  // row = t * heads + h
+    const uint32_t t = a.heads_shift >= 0 ? row >> a.heads_shift : row / (uint32_t)a.heads;
+    const uint32_t h = row - t * (uint32_t)a.heads;
+    const long long l = __ldg(a.loc + t);
+    if (l < 0) continue;
+    if (l >= a.slots) {
+      if (a.flags && h == 0 && j == 0) atomicOr(a.flags, MXSA_FLAG_PAGE);
+      continue;
+    }
+    const long long page = l >> a.page_shift, off = l & (ps - 1);
+    const long long slab = (page * a.heads + h) * (long long)ps * 72;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv)
+      put_group_fp4(a.src[kv] + (size_t)g * 16, a.dst[kv] + slab + off * 64 + 8 * j,
+                    a.dst[kv] + slab + (long long)ps * 64 + off * 8 + j, a.bf16);
+  }
+}
+
 }  // namespace
 
 // log2(x) when x is a power of two, else -1
@@ -148,6 +239,31 @@ cudaError_t launch_store(const mxsa_problem& p, long long n, const int64_t* loc,
   int sms = 148, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (p.kv_dtype == MXSA_NVFP4) {  // (no index keys: the caller checked)
+    const long long max_tokens = std::max(1LL, (long long)INT32_MAX / (8LL * p.num_kv_heads));
+    for (long long t0 = 0; t0 < n; t0 += max_tokens) {
+      const long long m = std::min(max_tokens, n - t0);
+      StoreFp4Args a{};
+      a.loc = loc + t0;
+      a.src[0] = static_cast<const uint16_t*>(k) + t0 * p.num_kv_heads * 128;
+      a.src[1] = static_cast<const uint16_t*>(v) + t0 * p.num_kv_heads * 128;
+      a.dst[0] = static_cast<uint8_t*>(k_cache);
+      a.dst[1] = static_cast<uint8_t*>(v_cache);
+      a.heads = p.num_kv_heads;
+      a.heads_shift = log2_exact(p.num_kv_heads);
+      a.page_shift = p.page_size == 128 ? 7 : 6;
+      a.bf16 = p.q_dtype == MXSA_BF16 ? 1 : 0;
+      a.groups = (uint32_t)(m * p.num_kv_heads * 8);
+      a.slots = (long long)p.num_pages * p.page_size;
+      a.flags = flags;
+      long long blocks = ((long long)a.groups + 255) / 256;
+      if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+      k_store_fp4<<<(unsigned)blocks, 256, 0, st>>>(a);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   const long long max_tokens = std::max(1LL, (long long)INT32_MAX / per_token);  // 32-bit chunk indices
   for (long long t0 = 0; t0 < n; t0 += max_tokens) {
     const long long m = std::min(max_tokens, n - t0);

@@ -249,6 +249,12 @@ WORKLOADS["skewed_decode_shared_p64"] = dataclasses.replace(
     kv_lens=_log_uniform_int(1024, 32768), seed=1015,
     description="profiling copy of skewed_decode_shared: 64 sequences, L log-U[1K, 32K]")
 
+# The GQA decode batch on an NVFP4 cache (E2M1 codes, one E4M3 scale per 16
+# elements): 72 bytes per position and kv head against 256 for BF16.
+WORKLOADS["gqa_decode_nvfp4"] = dataclasses.replace(
+    WORKLOADS["gqa_decode"], name="gqa_decode_nvfp4", kv_dtype="nvfp4",
+    description="gqa_decode with NVFP4 K/V (E2M1 + one E4M3 scale per 16 elements)")
+
 # The five workloads, in a fixed order.
 WORKLOAD_ORDER = ["tiny_decode", "gqa_decode", "shared_prefill", "fp8_varlen", "skewed_decode"]
 

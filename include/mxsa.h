@@ -57,7 +57,16 @@ typedef enum {
   MXSA_ERR_DATA = 5         /* mxsa_read_status: the device flagged bad input data */
 } mxsa_status;
 
-typedef enum { MXSA_BF16 = 0, MXSA_FP16 = 1, MXSA_FP8_E4M3 = 2 } mxsa_dtype;
+typedef enum { MXSA_BF16 = 0, MXSA_FP16 = 1, MXSA_FP8_E4M3 = 2, MXSA_NVFP4 = 3 } mxsa_dtype;
+
+/* MXSA_NVFP4 caches (the MSA summary page, "Highlighted Details", lists
+ * NVFP4 among the formats of sparse attention and decoding; the layout and
+ * the scaling are this library's): OCP MX FP4 E2M1 codes, each 16
+ * consecutive elements of a row sharing one E4M3 scale (value = e2m1 *
+ * scale, no per-tensor scale).  A cache is bytes [num_pages][Hkv][page_size
+ * * 72]: per (page, kv head) slab, page_size rows of 64 code bytes (element
+ * 2i in the low nibble of byte i, 2i + 1 in the high one) and then
+ * page_size rows of 8 scale bytes (scale j for elements 16 j .. 16 j + 15). */
 
 /* Bits of the device status word (mxsa_read_status). */
 #define MXSA_FLAG_SEL_RANGE 1   /* selected block outside [-1, ceil(L/128)) : slot ignored */
@@ -85,7 +94,7 @@ typedef struct {
   int32_t causal;            /* 0 or 1 (bottom-right aligned: pos(t) = L - Tq_s + i) */
   float softmax_scale;       /* 0 means 1/sqrt(128) */
   int32_t q_dtype;           /* MXSA_BF16 or MXSA_FP16; the output has this dtype */
-  int32_t kv_dtype;          /* q_dtype, or MXSA_FP8_E4M3 (unscaled e4m3fn) */
+  int32_t kv_dtype;          /* q_dtype, MXSA_FP8_E4M3 (unscaled e4m3fn) or MXSA_NVFP4 */
 } mxsa_problem;
 
 /* Library version, (major << 16) | minor.  (This library's own; the pages
@@ -105,7 +114,7 @@ const char* mxsa_status_string(mxsa_status status);
  * device status word; sched: work items and the per-CTA partition; partial:
  * partial outputs and lses, one row of 128 values plus one FP32 lse per
  * (selected block, query head) pair; the rows are FP32 when kv_dtype is
- * MXSA_FP8_E4M3, else in the 16-bit q_dtype.
+ * MXSA_FP8_E4M3 or MXSA_NVFP4, else in the 16-bit q_dtype.
  * Returns MXSA_ERR_INVALID_ARG / MXSA_ERR_UNSUPPORTED for bad problems. */
 mxsa_status mxsa_workspace_size(const mxsa_problem* problem, size_t* index_bytes, size_t* sched_bytes,
                                 size_t* partial_bytes);
@@ -181,6 +190,9 @@ mxsa_status mxsa_plan(const mxsa_problem* problem, const int32_t* sel, const int
  * into partial_ws.
  *   q             device [total_q, Hq, 128] of q_dtype
  *   k_cache/v_cache device [num_pages, Hkv, page_size, 128] of kv_dtype
+ *                 (MXSA_NVFP4: the byte slabs described at mxsa_dtype; FP8
+ *                 and NVFP4 blocks are widened exactly to q_dtype before
+ *                 the MMAs)
  *   block_tables  device int32 [B, max_pages_per_seq]
  *   num_ctas      must equal the value given to mxsa_schedule (0 = #SMs)
  *   partial_ws    device, partial_bytes from mxsa_workspace_size (written) */
@@ -244,7 +256,13 @@ mxsa_status mxsa_dense_fwd(const mxsa_problem* problem, const void* q, const voi
  * Of the problem, the store reads the head counts, page size, page count and
  * dtypes; topk, total_q and the sequence fields are not checked.
  * Caches: [num_pages][heads][page_size][dim] in problem->kv_dtype, which is
- * q_dtype (bits copied) or MXSA_FP8_E4M3: each value becomes x clamped to
+ * q_dtype (bits copied), MXSA_NVFP4 or MXSA_FP8_E4M3.  MXSA_NVFP4 (the slab
+ * layout at mxsa_dtype; no index keys): a group of 16 values stores the
+ * scale e4m3(amax / 6) (amax over its non-NaN |x|, single-precision
+ * division, rounded as below) and, with sd that scale's value, the E2M1
+ * code nearest to x / sd (single precision), ties to even, saturating at
+ * 6, with the quotient's sign; NaN elements and groups whose scale is 0
+ * store code 0.  MXSA_FP8_E4M3: each value becomes x clamped to
  * [-448, 448] rounded to the nearest e4m3fn value, ties to even, NaN keeping
  * its sign -- bit-identical to x.float().clamp(-448, 448).to(float8_e4m3fn).
  * idx_k and idx_cache are both NULL (no index keys) or both set.
@@ -275,7 +293,8 @@ mxsa_status mxsa_store_kv(const mxsa_problem* problem, int64_t n_tokens, const i
  *                    the remaining slots are -1.
  * The result is exact (bit-identical to a CPU statement of the definition);
  * its rows are valid input for mxsa_plan / mxsa_build_index.
- *   idx_q        device [total_q][Hkv][idx_dim] of kv_dtype
+ *   idx_q        device [total_q][Hkv][idx_dim] of kv_dtype (BF16, FP16 or
+ *                FP8: an MXSA_NVFP4 problem is MXSA_ERR_UNSUPPORTED)
  *   idx_cache    device [num_pages][Hkv][page_size][idx_dim] of kv_dtype
  *   block_tables, cu_seqlens_q, used_kv_lens as for mxsa_build_index
  *   score_ws     device, score_bytes from mxsa_select_workspace_size: first

@@ -21,8 +21,9 @@ def device_inputs(w, device="cuda"):
 
 
 def problem(w, scale=0.0):
+    kv = "nvfp4" if w.spec.kv_dtype == "nvfp4" else TORCH[w.spec.kv_dtype]
     return mx.make_problem(w.num_seqs, w.total_q, w.num_q_heads, w.num_kv_heads, w.topk, w.page_size, w.num_pages,
-                           w.max_pages_per_seq, w.causal, scale, TORCH[w.spec.q_dtype], TORCH[w.spec.kv_dtype])
+                           w.max_pages_per_seq, w.causal, scale, TORCH[w.spec.q_dtype], kv)
 
 
 def run(w, inp=None, num_ctas=0, scale=0.0):
@@ -67,8 +68,8 @@ def oracle_schedule(w, num_ctas):
 
 
 def partial_elem(prob):
-    """Partial rows are FP32 with FP8 caches, else the 16-bit q dtype."""
-    return (torch.float32, 4) if prob.kv_dtype == mx.FP8_E4M3 else (mx._CODE_DTYPE[prob.q_dtype], 2)
+    """Partial rows are FP32 with FP8 and NVFP4 caches, else the 16-bit q dtype."""
+    return (torch.float32, 4) if prob.kv_dtype in (mx.FP8_E4M3, mx.NVFP4) else (mx._CODE_DTYPE[prob.q_dtype], 2)
 
 
 def read_partials(attn):
