@@ -16,10 +16,11 @@
 // rescaled), so most blocks need no cross-thread reduction.
 //
 // The decode phase of the forward kernel (fwd.cu), run by each CTA on its
-// decode items before its KV-stationary items: warps 0-3 softmax/epilogue
-// (and FP8 widening), warp 4 TMA producer (q rows of the item; K and V pages
-// of each block into a 2-3 stage ring), warp 5 MMA issuer; the kernel's
-// other warps idle through this phase.  TMEM columns [0, 64) of the CTA's
+// decode items before its KV-stationary items: warps 0-3 softmax/epilogue,
+// warp 4 TMA producer (q rows of the item; K and V pages of each block into
+// a 2-3 stage ring, or for FP8 / NVFP4 caches into two staging tiles), warp
+// 5 MMA issuer, warps 6-9 widening (FP8 / NVFP4: each staged block into the
+// q dtype in its stage); the kernel's other warps idle through this phase.  TMEM columns [0, 64) of the CTA's
 // allocation hold S^T and O^T.
 #pragma once
 #include <cuda.h>
@@ -50,10 +51,11 @@ struct BlockInfo {
 struct Ctrl {
   uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
-  uint64_t stg_full, stg_empty, done;
+  uint64_t stg_full[2], stg_empty[2], done;  // two staging tiles (widened caches)
   uint32_t tmem_base;
   int32_t abort_flag;
   BlockInfo info[kMaxStages];
+  int32_t stg_valid[2];  // widened caches: valid keys of the block in each staging tile
 };
 
 // cache kinds, the forward's template parameter: 16-bit (the q dtype), and
@@ -90,7 +92,7 @@ __host__ __device__ constexpr Layout smem_layout(int ns, int fp8) {
   L.q = (uint32_t)ns * kStage;
   L.p = L.q + 2u * N * 256u;
   L.stg = L.p + 2u * N * 256u;
-  L.red = L.stg + (fp8 ? kKVTile : 0u);
+  L.red = L.stg + (fp8 ? 2u * kKVTile : 0u);  // widened caches: two staging tiles
   L.ctrl = L.red + 4u * N * 4u;
   L.total = L.ctrl + (uint32_t)sizeof(Ctrl);
   return L;
@@ -302,8 +304,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       mbar_init(&c.o_full[i], 1);
       mbar_init(&c.o_empty[i], 128);
     }
-    mbar_init(&c.stg_full, 1);
-    mbar_init(&c.stg_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.stg_full[i], 1);
+      mbar_init(&c.stg_empty[i], 128);
+    }
     mbar_init(&c.done, 1);
     c.abort_flag = 0;
     fence_mbar_init();
@@ -376,17 +380,24 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       BlockDesc nxt = cur;
       for (int j = 0; j < cur.nk && ok; ++j, ++blk) {
         const int st = blk % ns, us = blk / ns;
-        ok = __all_sync(0xffffffffu, mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags,
-                                               MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-        if (ok && a.kv_fp8)
-          ok = __all_sync(0xffffffffu, mbar_wait(&c.stg_empty, (blk & 1) ^ 1, abort_flag, a.flags,
+        // 16-bit caches: block blk lands in stage st once the stage's
+        // previous block was consumed.  Widened caches: it stages into
+        // tile blk % 2 once block blk - 2 was widened out of it (the
+        // widening warps wait for the stage), so the copies run ahead of
+        // the MMAs.
+        if (!a.kv_fp8)
+          ok = __all_sync(0xffffffffu, mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags,
+                                                 MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        else
+          ok = __all_sync(0xffffffffu, mbar_wait(&c.stg_empty[blk & 1], ((blk >> 1) & 1) ^ 1, abort_flag, a.flags,
                                                  MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
         const int valid = __shfl_sync(0xffffffffu, cur.valid, j);
         const int pg0 = __shfl_sync(0xffffffffu, cur.page0, j);
         const int pg1 = __shfl_sync(0xffffffffu, cur.page1, j);
         if (lane == 0) {
-          c.info[st].valid = valid;
+          if (!a.kv_fp8) c.info[st].valid = valid;
+          else c.stg_valid[blk & 1] = valid;
           const int pages[2] = {pg0, pg1};
           const int present = (pg0 >= 0) + (pg1 >= 0);
           if (!a.kv_fp8) {
@@ -404,25 +415,27 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
           } else if (a.kv_fp4) {
             // NVFP4: code rows by TMA, scale rows by bulk copy, K at 0 and
             // V at 16 KB of the staging tile (codes, then scales at 8 KB)
-            uint8_t* stg = sm + L.stg;
-            mbar_arrive_expect_tx(&c.stg_full, (uint32_t)present * (uint32_t)ps * 144u);
+            uint8_t* stg = sm + L.stg + (blk & 1) * kKVTile;
+            uint64_t* sf = &c.stg_full[blk & 1];
+            mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 144u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
               const int z = pages[pg] * a.Hkv + cur.g;
               const size_t so = (size_t)z * ps * 72 + (size_t)ps * 64;
-              tma_load_3d(stg + pg * ps * 64, &tmk, &c.stg_full, 0, 0, z);
-              tma_load_3d(stg + 16384 + pg * ps * 64, &tmv, &c.stg_full, 0, 0, z);
-              bulk_load(stg + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, &c.stg_full);
-              bulk_load(stg + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, &c.stg_full);
+              tma_load_3d(stg + pg * ps * 64, &tmk, sf, 0, 0, z);
+              tma_load_3d(stg + 16384 + pg * ps * 64, &tmv, sf, 0, 0, z);
+              bulk_load(stg + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, sf);
+              bulk_load(stg + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, sf);
             }
           } else {
-            uint8_t* stg = sm + L.stg;
-            mbar_arrive_expect_tx(&c.stg_full, (uint32_t)present * (uint32_t)ps * 256u);
+            uint8_t* stg = sm + L.stg + (blk & 1) * kKVTile;
+            uint64_t* sf = &c.stg_full[blk & 1];
+            mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
               const int z = pages[pg] * a.Hkv + cur.g;
-              tma_load_3d(stg + pg * 8192, &tmk, &c.stg_full, 0, 0, z);
-              tma_load_3d(stg + 16384 + pg * 8192, &tmv, &c.stg_full, 0, 0, z);
+              tma_load_3d(stg + pg * 8192, &tmk, sf, 0, 0, z);
+              tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
             }
           }
         }
@@ -441,7 +454,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       // drain the loads in flight before the CTA may exit
       for (int k = std::max(0, blk - ns); k < blk; ++k) {
         if (a.kv_fp8) {
-          if (k == blk - 1) mbar_drain(&c.stg_full, k & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+          // staging tile k % 2 was refilled only after block k - 2 was
+          // widened: the last two blocks' copies may still be in flight
+          if (k >= blk - 2) mbar_drain(&c.stg_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         } else {
           mbar_drain(&c.kv_full[k % ns], (k / ns) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
         }
@@ -530,6 +545,55 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       mma_commit(&c.done);
       mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
+  } else if (kKV != kKv16 && warp >= 6 && warp < 10) {
+    // ------------------------------------------------------ widening warps
+    // Widened caches (FP8, NVFP4): thread k turns row k of each staged
+    // block's K and V into the q dtype in the block's stage, zero past the
+    // valid keys, while the softmax warps work on the previous block.
+    const int k = tid - 192;
+    const int bf16 = a.ab_bf16;
+    int blk = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it) {
+      const int nk = a.items[it].w;
+      for (int j = 0; j < nk; ++j, ++blk) {
+        const int st = blk % ns, us = blk / ns;
+        ok = mbar_wait(&c.stg_full[blk & 1], (blk >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        // the stage's previous block (blk - ns) was consumed by its p v
+        ok = ok && mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        if (!ok) break;
+        const int valid = c.stg_valid[blk & 1];
+        if (k == 0) c.info[st].valid = valid;  // for the softmax warps, published by kv_full
+        const uint8_t* stg = sm + L.stg + (blk & 1) * kKVTile;
+        uint8_t* kst = sm + st * kStage;
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t dst = smem_u32(kv ? kst + kKVTile : kst);
+          if (k >= valid) {
+            for (int ch = 0; ch < 16; ++ch) st_shared_v4(dst + swz_kv(k, ch), 0, 0, 0, 0);
+          } else if (kKV == kKvFp4) {
+            widen_fp4_row(stg + kv * 16384 + k * 64, stg + kv * 16384 + 8192 + k * 8, dst, k, bf16);
+          } else {
+            const uint8_t* src = stg + kv * 16384 + k * 128;
+            for (int cc = 0; cc < 8; ++cc) {
+              const int c8 = (cc + k) & 7;
+              const uint4 raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
+              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                o[2 * i] = widen_e4m3x2((uint16_t)(w[i] & 0xffffu), bf16);
+                o[2 * i + 1] = widen_e4m3x2((uint16_t)(w[i] >> 16), bf16);
+              }
+              st_shared_v4(dst + swz_kv(k, 2 * c8), o[0], o[1], o[2], o[3]);
+              st_shared_v4(dst + swz_kv(k, 2 * c8 + 1), o[4], o[5], o[6], o[7]);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&c.stg_empty[blk & 1]);
+        mbar_arrive(&c.kv_full[st]);
+      }
+    }
   } else if (warp < 4) {
     // ------------------------------------------------------ softmax group
     // Each thread waits on the barriers itself; the four warps vote once per
@@ -560,48 +624,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
         uint8_t* vst = kst + kKVTile;
         int valid = 0;
         bool okb;
-        if (kKV != kKv16) {
-          okb = mbar_wait(&c.stg_full, blk & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (okb) {
-            valid = c.info[st].valid;
-            const uint8_t* stg = sm + L.stg;
-            for (int kv = 0; kv < 2 && kKV == kKvFp4; ++kv) {
-              const uint32_t dst = smem_u32(kv ? vst : kst);
-              if (k < valid)
-                widen_fp4_row(stg + kv * 16384 + k * 64, stg + kv * 16384 + 8192 + k * 8, dst, k, bf16);
-              else
-                for (int ch = 0; ch < 16; ++ch) st_shared_v4(dst + swz_kv(k, ch), 0, 0, 0, 0);
-            }
-            for (int kv = 0; kv < 2 && kKV == kKvFp8; ++kv) {
-              const uint8_t* src = stg + kv * 16384 + k * 128;
-              const uint32_t dst = smem_u32(kv ? vst : kst);
-              for (int cc = 0; cc < 8; ++cc) {
-                const int c8 = (cc + k) & 7;
-                uint4 raw = make_uint4(0, 0, 0, 0);
-                if (k < valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t o[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  o[2 * i] = widen_e4m3x2((uint16_t)(w[i] & 0xffffu), bf16);
-                  o[2 * i + 1] = widen_e4m3x2((uint16_t)(w[i] >> 16), bf16);
-                }
-                st_shared_v4(dst + swz_kv(k, 2 * c8), o[0], o[1], o[2], o[3]);
-                st_shared_v4(dst + swz_kv(k, 2 * c8 + 1), o[4], o[5], o[6], o[7]);
-              }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&c.stg_empty);
-            mbar_arrive(&c.kv_full[st]);
-          }
-        } else {
-          okb = mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (okb) {
-            valid = c.info[st].valid;
-            if (k >= valid) {
-              // keys past the sequence end must not bring stale values into P V
-              for (int ch = 0; ch < 16; ++ch) st_shared_v4(smem_u32(vst) + swz_kv(k, ch), 0, 0, 0, 0);
-            }
+        // the block's K and V in stage st (widened caches: written by the
+        // widening warps, which zero the rows past the valid keys)
+        okb = mbar_wait(&c.kv_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        if (okb) {
+          valid = c.info[st].valid;
+          if (kKV == kKv16 && k >= valid) {
+            // keys past the sequence end must not bring stale values into P V
+            for (int ch = 0; ch < 16; ++ch) st_shared_v4(smem_u32(vst) + swz_kv(k, ch), 0, 0, 0, 0);
           }
         }
         // ---- scores of key k for every row (tcgen05.ld is warp-collective)
@@ -734,8 +764,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       mbar_inval(&c.o_full[i]);
       mbar_inval(&c.o_empty[i]);
     }
-    mbar_inval(&c.stg_full);
-    mbar_inval(&c.stg_empty);
+    for (int i = 0; i < 2; ++i) {
+      mbar_inval(&c.stg_full[i]);
+      mbar_inval(&c.stg_empty[i]);
+    }
     mbar_inval(&c.done);
   }
   __syncthreads();

@@ -313,10 +313,11 @@ def run_dense(tiles, seed, fix=True):
 
 
 
-NS = 3  # K/V stages of the decode phase
-
 def run_decode(items, seed, fp8=False):
-    """items: key counts (>= 1) of the CTA's decode items, in order."""
+    """items: key counts (>= 1) of the CTA's decode items, in order.  K/V
+    stages: 3 for 16-bit caches, 2 for widened ones (FP8, NVFP4), whose
+    blocks land in two staging tiles in turn."""
+    NS = 2 if fp8 else 3
     rnd = random.Random(seed)
     B = {}
     def bar(n, c=1): B[n] = Bar(n, c)
@@ -325,11 +326,12 @@ def run_decode(items, seed, fp8=False):
     for i in range(2):
         for nm in ("q_full", "q_empty", "s_full", "p_full", "p_empty", "o_full", "o_empty"):
             bar(f"{nm}{i}")
-    bar("stg_full"); bar("stg_empty")
+    for i in range(2):
+        bar(f"stg_full{i}"); bar(f"stg_empty{i}")
     pending = {}
     def later(src, cb): pending.setdefault(src, []).append(cb)
     stage = {}     # st -> block (landed / widened)
-    staging = [None]
+    staging = [None, None]
     Sbuf = {}      # sb -> ('S'|'read', blk)
     Pbuf = {}      # sb -> ('P'|'used', blk)
     Obuf = {}      # ib -> ('acc'|'done'|'read', item)
@@ -343,14 +345,16 @@ def run_decode(items, seed, fp8=False):
             later(f"tq{ib}", lambda ib=ib: B[f"q_full{ib}"].arrive())
             for j in range(nk):
                 st, us = blk % NS, blk // NS
-                yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
-                assert blk < NS or pv_done[0] >= blk - NS, ("stage refilled before its p v", blk)
+                if not fp8:  # widened caches: the widening warps wait for the stage
+                    yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
+                    assert blk < NS or pv_done[0] >= blk - NS, ("stage refilled before its p v", blk)
                 if fp8:
-                    yield ("wait", B["stg_empty"], (blk & 1) ^ 1)
+                    yield ("wait", B[f"stg_empty{blk & 1}"], ((blk >> 1) & 1) ^ 1)
+                    assert staging[blk & 1] in (None, ("widened", blk - 2)), ("staging refilled early", blk)
                     def sl(blk=blk):
-                        staging[0] = blk
-                        B["stg_full"].arrive()
-                    later("tstg", sl)
+                        staging[blk & 1] = ("landed", blk)
+                        B[f"stg_full{blk & 1}"].arrive()
+                    later(f"tstg{blk & 1}", sl)
                 else:
                     def land(st=st, blk=blk):
                         stage[st] = blk
@@ -409,14 +413,8 @@ def run_decode(items, seed, fp8=False):
             ib, ui = n_it & 1, n_it >> 1
             for j in range(nk):
                 st, us, sb, ub = blk % NS, blk // NS, blk & 1, blk >> 1
-                if fp8:
-                    yield ("wait", B["stg_full"], blk & 1)
-                    assert staging[0] == blk
-                    assert blk < NS or pv_done[0] >= blk - NS, ("widening into a busy stage", blk)
-                    stage[st] = blk
-                    B["stg_empty"].arrive(); B[f"kv_full{st}"].arrive()
-                else:
-                    yield ("wait", B[f"kv_full{st}"], us & 1)
+                yield ("wait", B[f"kv_full{st}"], us & 1)
+                assert stage.get(st) == blk, ("softmax on the wrong block", stage.get(st), blk)
                 yield ("wait", B[f"s_full{sb}"], ub & 1)
                 assert Sbuf.get(sb) == ("S", blk)
                 Sbuf[sb] = ("read", blk)
@@ -434,7 +432,21 @@ def run_decode(items, seed, fp8=False):
             assert Obuf.get(ib) == ("done", n_it)
             Obuf[ib] = ("read", n_it)
             B[f"o_empty{ib}"].arrive()
+    def widen():
+        # widened caches: warps 6-9 turn each staged block into its stage
+        for blk in range(nblk):
+            st, us = blk % NS, blk // NS
+            yield ("wait", B[f"stg_full{blk & 1}"], (blk >> 1) & 1)
+            yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
+            assert staging[blk & 1] == ("landed", blk)
+            assert blk < NS or pv_done[0] >= blk - NS, ("widening into a busy stage", blk)
+            stage[st] = blk
+            staging[blk & 1] = ("widened", blk)
+            B[f"stg_empty{blk & 1}"].arrive(); B[f"kv_full{st}"].arrive()
+            yield None
     agents = {"p": producer(), "m": issuer(), "s": softmax()}
+    if fp8:
+        agents["w"] = widen()
     state = {k: None for k in agents}; done = set(); steps = 0
     while len(done) < len(agents) or any(pending.values()):
         steps += 1; assert steps < 500000
