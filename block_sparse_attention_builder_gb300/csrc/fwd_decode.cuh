@@ -477,7 +477,11 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       // so a stage is released as soon as its block is consumed.
       int its = it_begin, js = 0, ns_it = 0, nks = a.items[it_begin].w, bs = 0;
       int itp = it_begin, jp = 0, np_it = 0, nkp = nks, bp = 0;
-      uint64_t t_last = globaltimer_ns();
+      // the wait limit runs from the first pass that found nothing to issue;
+      // the timer is read once every 64 such passes (a read costs more than
+      // a pass, and it would delay the issuer's reaction to the barriers)
+      uint64_t t_idle = 0;
+      uint32_t idle = 0;
       while (itp < it_end) {
         bool progressed = false;
         if (its < it_end && bs <= bp + 1) {
@@ -532,14 +536,20 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
           }
         }
         if (progressed) {
-          t_last = globaltimer_ns();
+          idle = 0;
         } else {
           if (*abort_flag) break;
-          if (globaltimer_ns() - t_last > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(a.flags, MXSA_FLAG_TIMEOUT);
-            break;
+          if ((idle & 63u) == 0u) {
+            const uint64_t now = globaltimer_ns();
+            if (idle == 0u) {
+              t_idle = now;
+            } else if (now - t_idle > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(a.flags, MXSA_FLAG_TIMEOUT);
+              break;
+            }
           }
+          ++idle;
         }
       }
       mma_commit(&c.done);
