@@ -56,6 +56,8 @@ struct Ctrl {
   int32_t abort_flag;
   BlockInfo info[kMaxStages];
   int32_t stg_valid[2];  // widened caches: valid keys of the block in each staging tile
+  float inv_l[2][16];    // 1 / l per row of an item whose epilogue is pending, by O buffer
+  float lse[2][16];      // and its lse per row
 };
 
 // cache kinds, the forward's template parameter: 16-bit (the q dtype), and
@@ -621,12 +623,52 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
     int blk = 0, n_it = 0;
     bool ok = true;
     float m[N], lsum[N];
+    // The epilogue of an item (o = O / l into its partial rows) waits for
+    // the item's last p v, so it runs at the end of the next item (the O
+    // accumulators alternate between items; the next-but-one item's first
+    // p v needs it, and comes after it); the CTA's last item finishes at
+    // once.  An item's sums wait in shared memory, ordered by the named
+    // barriers in between.
+    static_assert(N <= 16, "inv_l holds 16 rows");
+    int prev_e0 = 0;
+    auto finish = [&](int pn, int pend_e0) -> bool {
+      const int pend_ib = pn & 1, pend_ui = pn >> 1;
+      const uint32_t tOp = tmem + lane_addr + 2 * N + pend_ib * N;
+      const bool oko = __all_sync(
+          0xffffffffu, mbar_wait(&c.o_full[pend_ib], pend_ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+      float o[N];
+      if (oko) {
+        tc_fence_after();
+        tmem_ld_n<N>(tOp, o);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&c.o_empty[pend_ib]);
+      }
+      if (!wg_all(oko)) return false;
+      // o = O / l (thread k: head dim k of every row), FP32 or rounded to
+      // the q dtype
+      const size_t o0 = (size_t)pend_e0 * G * 128 + k;
+#pragma unroll
+      for (int r = 0; r < N; ++r) {
+        if (r >= G) continue;
+        const float ov = o[r] * c.inv_l[pend_ib][r];
+        if (kPart32) {
+          __stcs(static_cast<float*>(a.part_o) + o0 + (size_t)r * 128, ov);
+        } else {
+          const unsigned short h =
+              bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(ov)) : __half_as_ushort(__float2half_rn(ov));
+          __stcs(static_cast<unsigned short*>(a.part_o) + o0 + (size_t)r * 128, h);
+        }
+      }
+      if (k < G) a.part_lse[(size_t)pend_e0 * G + k] = c.lse[pend_ib][k];
+      return true;
+    };
     int4 itm_next = a.items[it_begin];
     for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
       const int4 itm = itm_next;
       if (it + 1 < it_end) itm_next = a.items[it + 1];  // its latency hides behind this item
       const int nk = itm.w;
-      const int ib = n_it & 1, ui = n_it >> 1;
+      const int ib = n_it & 1;
       const uint32_t tO = tmem + lane_addr + 2 * N + ib * N;
       for (int j = 0; j < nk; ++j, ++blk) {
         const int st = blk % ns, us = blk / ns, sb = blk & 1, ub = blk >> 1;
@@ -715,35 +757,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
         mbar_arrive(&c.p_full[sb]);
       }
       if (!ok) break;
-      // ---- epilogue of the item: o = O / l, lse = (m + log2 l) ln 2
-      bool oko = __all_sync(0xffffffffu,
-                            mbar_wait(&c.o_full[ib], ui & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-      float o[N];
-      if (oko) {
-        tc_fence_after();
-        tmem_ld_n<N>(tO, o);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&c.o_empty[ib]);
-      }
-      ok = wg_all(oko);
-      if (!ok) break;
+      // ---- the item's sums: l over the four warps, 1 / l per row and
+      // lse = (m + log2 l) ln 2; its epilogue follows the next item's first
+      // softmax, or now for the last item
       wg_reduce<N, false>(lsum, red);
-      const int e0 = itm.y;
-      // o = O / l (thread k: head dim k of every row), FP32 or rounded to
-      // the q dtype
-      const size_t o0 = (size_t)e0 * G * 128 + k;
+      if (k == 0) {  // every thread holds the same sums; read after the next named barrier
 #pragma unroll
-      for (int r = 0; r < N; ++r) {
-        if (r >= G) continue;
-        const float ov = lsum[r] > 0.f ? o[r] * __frcp_rn(lsum[r]) : 0.f;
-        if (kPart32) {
-          __stcs(static_cast<float*>(a.part_o) + o0 + (size_t)r * 128, ov);
-        } else {
-          const unsigned short h =
-              bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(ov)) : __half_as_ushort(__float2half_rn(ov));
-          __stcs(static_cast<unsigned short*>(a.part_o) + o0 + (size_t)r * 128, h);
-        }
+        for (int r = 0; r < N; ++r) c.inv_l[ib][r] = lsum[r] > 0.f ? __frcp_rn(lsum[r]) : 0.f;
       }
       if (k < G) {
         float lv = -INFINITY, mv = 0.f;
@@ -753,8 +773,13 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
             lv = lsum[r];
             mv = m[r];
           }
-        a.part_lse[(size_t)e0 * G + k] = lv > 0.f ? (mv + lg2_approx(lv)) * 0.69314718055994530942f : -INFINITY;
+        c.lse[ib][k] = lv > 0.f ? (mv + lg2_approx(lv)) * 0.69314718055994530942f : -INFINITY;
       }
+      // the previous item's epilogue (its last p v finished long ago), and
+      // this one's when it is the CTA's last item
+      for (int q = n_it > 0 ? n_it - 1 : 0; q <= (it + 1 == it_end ? n_it : n_it - 1) && ok; ++q)
+        ok = finish(q, q == n_it ? itm.y : prev_e0);
+      prev_e0 = itm.y;
     }
   }
   tc_fence_before();

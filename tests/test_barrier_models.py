@@ -428,10 +428,15 @@ def run_decode(items, seed, fp8=False):
                 B[f"p_full{sb}"].arrive()
                 blk += 1
                 yield None
-            yield ("wait", B[f"o_full{ib}"], ui & 1)
-            assert Obuf.get(ib) == ("done", n_it)
-            Obuf[ib] = ("read", n_it)
-            B[f"o_empty{ib}"].arrive()
+            # the previous item's epilogue at this item's end; the last
+            # item's own epilogue follows at once
+            last = n_it == len(items) - 1
+            for q in range(max(0, n_it - 1), n_it + 1 if last else n_it):
+                qb = q & 1
+                yield ("wait", B[f"o_full{qb}"], (q >> 1) & 1)
+                assert Obuf.get(qb) == ("done", q)
+                Obuf[qb] = ("read", q)
+                B[f"o_empty{qb}"].arrive()
     def widen():
         # widened caches: warps 6-9 turn each staged block into its stage
         for blk in range(nblk):
