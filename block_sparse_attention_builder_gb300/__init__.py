@@ -44,7 +44,8 @@ EXPORTED = ["mxsa_version", "mxsa_status_string", "mxsa_workspace_size", "mxsa_b
             "mxsa_plan",
             "mxsa_kvouter_fwd", "mxsa_combine", "mxsa_read_status", "mxsa_index_layout_query",
             "mxsa_sched_layout_query", "mxsa_store_kv", "mxsa_dense_fwd", "mxsa_select_workspace_size",
-            "mxsa_select_blocks", "mxsa_dedup_workspace_size", "mxsa_build_index_dedup"]
+            "mxsa_select_blocks", "mxsa_dedup_workspace_size", "mxsa_build_index_dedup",
+            "mxsa_attention_noalloc", "mxsa_noalloc_read_status"]
 
 
 class MxsaError(RuntimeError):
@@ -107,6 +108,8 @@ def _load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "mxsa_select_blocks": [P, ctypes.c_int32, P, P, P, P, P, P, S, P, P, P],
         "mxsa_dedup_workspace_size": [P, P],
         "mxsa_build_index_dedup": [P, P, P, P, P, P, S, P, S, P],
+        "mxsa_attention_noalloc": [P] * 11,
+        "mxsa_noalloc_read_status": [P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -333,6 +336,26 @@ def select_blocks(prob, idx_q, idx_cache, block_tables, cu_seqlens_q, used_kv_le
                                    score_ws.numel() * score_ws.element_size(), _ptr(sel), _ptr(flags),
                                    _stream(stream)), what)
     return sel, score_ws
+
+
+def attention_noalloc(prob, q, k_cache, v_cache, sel, block_tables, cu_seqlens_q, used_kv_lens, out, lse=None,
+                      stream=None):
+    """All four steps with the library's own fixed scratch array (no
+    workspace from the caller); the status word is read with
+    noalloc_read_status."""
+    _need_attention("mxsa_attention_noalloc", prob, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                    cu_seqlens_q=cu_seqlens_q, used_kv_lens=used_kv_lens, sel=sel, out=out, lse=lse)
+    _check(_lib.mxsa_attention_noalloc(ctypes.byref(prob), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sel),
+                                       _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(used_kv_lens), _ptr(out),
+                                       _ptr(lse), _stream(stream)), "mxsa_attention_noalloc")
+
+
+def noalloc_read_status(stream=None) -> int:
+    flags = ctypes.c_int32(0)
+    st = _lib.mxsa_noalloc_read_status(_stream(stream), ctypes.byref(flags))
+    if st not in (0, 5):
+        raise MxsaError(st, "mxsa_noalloc_read_status")
+    return flags.value
 
 
 def read_status(index_ws, stream=None) -> int:

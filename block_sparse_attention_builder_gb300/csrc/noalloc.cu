@@ -34,17 +34,34 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (looked up once
-// per device); nullptr on failure.
-void* noalloc_scratch_address() {
+// per device).  The stream must belong to the current device, and the first
+// look-up on a device may not happen while the stream is being captured (it
+// is a runtime call a capture does not record): both return
+// MXSA_ERR_INVALID_ARG before anything runs.
+mxsa_status noalloc_scratch_address(cudaStream_t stream, void** out) {
+  *out = nullptr;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXSA_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MXSA_ERR_INVALID_ARG;
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
+  // the stream's device, outside a capture only (a query a capture in its
+  // global mode does not allow; a stream being captured was checked when
+  // the calls before the capture ran)
+  if (stream && !capturing) {
+    int sdev = -1;
+    if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return MXSA_ERR_INVALID_ARG;
+    if (sdev != dev) return MXSA_ERR_INVALID_ARG;  // the array of another device
+  }
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_addr[dev]) {
+    if (capturing) return MXSA_ERR_INVALID_ARG;  // make the first call on a device outside any capture
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return MXSA_ERR_CUDA;
     g_noalloc_addr[dev] = p;
   }
-  return g_noalloc_addr[dev];
+  *out = g_noalloc_addr[dev];
+  return MXSA_OK;
 }
 
 }  // namespace
@@ -58,8 +75,10 @@ extern "C" mxsa_status mxsa_attention_noalloc(const mxsa_problem* problem, const
   mxsa_status s = mxsa_workspace_size(problem, &ib, &sb, &pb);
   if (s != MXSA_OK) return s;
   if (ib + sb + pb > kNoAllocScratchBytes) return MXSA_ERR_WORKSPACE;  // problem too large for the fixed array
-  uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address());
-  if (!base) return MXSA_ERR_CUDA;
+  void* addr = nullptr;
+  s = noalloc_scratch_address(static_cast<cudaStream_t>(stream), &addr);
+  if (s != MXSA_OK) return s;
+  uint8_t* base = static_cast<uint8_t*>(addr);
   void* index_ws = base;
   void* sched_ws = base + ib;  // ib and sb are multiples of 256 bytes
   void* partial_ws = base + ib + sb;
@@ -71,4 +90,16 @@ extern "C" mxsa_status mxsa_attention_noalloc(const mxsa_problem* problem, const
                        stream);
   if (s != MXSA_OK) return s;
   return mxsa_combine(problem, index_ws, ib, partial_ws, pb, out, lse, stream);
+}
+
+// The device status word of the last call's index (at the array's start,
+// where that call's index workspace begins), as mxsa_read_status reads it
+// from a caller's workspace: synchronises `stream` first.
+extern "C" mxsa_status mxsa_noalloc_read_status(void* stream, int32_t* device_flags) {
+  if (!device_flags) return MXSA_ERR_INVALID_ARG;
+  *device_flags = 0;
+  void* addr = nullptr;
+  const mxsa_status s = noalloc_scratch_address(static_cast<cudaStream_t>(stream), &addr);
+  if (s != MXSA_OK) return s;
+  return mxsa_read_status(addr, stream, device_flags);
 }

@@ -361,16 +361,24 @@ mxsa_status mxsa_sched_layout_query(const mxsa_problem* problem, mxsa_sched_layo
  * the library keeps reserved until the process exits.  Problems whose three
  * workspaces (mxsa_workspace_size) add up to more than 16 MiB are rejected
  * with MXSA_ERR_WORKSPACE before anything runs.  Nothing is allocated.
- * The first call on a device looks up the array's device address (make that
- * first call before any stream capture).  Calls share the array: calls that
- * overlap on the GPU race and must be serialised by the caller.  Device-side
- * data errors are not reported by this entry point (the status word lives
- * in the shared array); use the four steps to read them.  Asynchronous on
- * `stream`. */
+ * The first call on a device looks up the array's device address: made
+ * while `stream` is being captured it returns MXSA_ERR_INVALID_ARG, as does
+ * a stream of another device than the current one (nothing runs).  Calls
+ * share the array: calls that overlap on the GPU race and must be
+ * serialised by the caller.  Asynchronous on `stream`; the device status
+ * word of the last call (data errors, MXSA_FLAG_TIMEOUT) is read with
+ * mxsa_noalloc_read_status. */
 mxsa_status mxsa_attention_noalloc(const mxsa_problem* problem, const void* q, const void* k_cache,
                                    const void* v_cache, const int32_t* sel, const int32_t* block_tables,
                                    const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, void* out, float* lse,
                                    void* stream);
+
+/* This library's own (no passage), the companion of mxsa_attention_noalloc:
+ * synchronises `stream`, then copies the status word (MXSA_FLAG_* bits) that
+ * the last mxsa_attention_noalloc call on the current device left in the
+ * library's array into *device_flags.  Returns MXSA_ERR_DATA when any bit
+ * is set, MXSA_OK otherwise (MXSA_ERR_INVALID_ARG as for that call). */
+mxsa_status mxsa_noalloc_read_status(void* stream, int32_t* device_flags);
 
 /* Rows per tile, tiles per normal work item and blocks per decode work item
  * used by the scheduler. */
