@@ -25,9 +25,10 @@
 //                   HBM-bound decode case, so the kernel keeps few registers
 //                   and little shared memory, for many CTAs per SM.
 //   k_select_long   units (sequence, block, kv head, 128-query chunk) of the
-//                   longer sequences: the block's keys are staged as FP32 and
-//                   thread i owns query i of the chunk, walking the keys four
-//                   at a time (four independent FMA chains, no reduction).
+//                   longer sequences: the chunk's queries and the block's keys
+//                   staged as FP32, 32 dimensions at a time, and multiplied
+//                   like a matrix product (8 x 8 accumulators per thread),
+//                   then a maximum over each query's visible keys.
 //   k_select_topk   one CTA per (token, kv head) row: the row's block scores
 //                   become 64-bit keys (order-preserving score bits above the
 //                   complemented block index) in shared memory, sorted by a
@@ -326,24 +327,50 @@ __global__ void __launch_bounds__(kSelThreads)
   }
 }
 
-// shared memory of k_select_long: the block's keys as FP32 and their
-// visibility
-__host__ __device__ constexpr size_t long_smem(int D) {
-  return (size_t)kSelThreads * D * sizeof(float) + kSelThreads * sizeof(int);
+// k_select_long: a unit's 128 queries x 128 keys of dot products, blocked
+// like a matrix product.  The dimensions pass in chunks of 32: each chunk of
+// the queries and of the keys is staged in shared memory as FP32, transposed
+// ([dimension][query or key]); thread (qg, kg) keeps an 8 x 8 tile of
+// accumulators (queries 8 qg .. 8 qg + 7, keys 4 kg .. 4 kg + 3 and
+// 64 + 4 kg .. 64 + 4 kg + 3) and adds one FMA per dimension to each, in
+// dimension order from +0, so every dot is the reading's exact sum.  Four
+// 16-byte shared-memory reads feed 64 FMAs.
+constexpr int kLongThreads = 256;
+constexpr int kLongChunk = 32;  // dimensions staged at a time
+struct LongSmem {
+  float q[kLongChunk][128];
+  float k[kLongChunk][128];
+  int kvis[128];  // key on a valid page inside the sequence
+  int qlim[128];  // keys a query sees (0: no query)
+};
+
+__host__ __device__ constexpr size_t long_smem(int) { return sizeof(LongSmem); }
+
+// 16 consecutive values from `base` (16-byte aligned), widened to FP32
+__device__ __forceinline__ void load16(const uint8_t* base, int dtype, float* out) {
+  if (dtype == MXSA_FP8_E4M3) {
+    unpack_e4m3x16(__ldg(reinterpret_cast<const uint4*>(base)), out);
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(base);
+    unpack_16bitx8(__ldg(p), dtype == MXSA_BF16, out);
+    unpack_16bitx8(__ldg(p + 1), dtype == MXSA_BF16, out + 8);
+  }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kLongThreads, 2)
     k_select_long(SelArgs a) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
+  LongSmem& sm = *reinterpret_cast<LongSmem*>(sm_raw);
   // Let through once every k_select_short CTA has passed its wait for the
   // table, so the table is complete; this launch waits for k_select_short
   // itself only at its end (k_select_topk waits on this launch).
   pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int Hkv = a.Hkv;
-  float* kf = reinterpret_cast<float*>(sm_raw);              // [128][D]
-  int* kvis = reinterpret_cast<int*>(kf + kSelThreads * D);  // [128]
+  const int esz = a.dtype == MXSA_FP8_E4M3 ? 1 : 2;
+  const int qg = tid >> 4, kg = tid & 15;
+  const int row = tid & 127, half = tid >> 7;  // staging: row, 16 dimensions of the chunk
   const long long units = a.tab.unit_long[a.B] * Hkv;
   for (long long u = blockIdx.x; u < units; u += gridDim.x) {
     const int g = (int)(u % Hkv);
@@ -353,75 +380,88 @@ __global__ void __launch_bounds__(kSelThreads)
     const long long w = v - a.tab.unit_long[s];
     const int b = (int)(w % r.nblk), chunk = (int)(w / r.nblk);
     const int tq = r.tq, L = r.L, q0 = r.q0;
-    __syncthreads();  // the previous unit's shared memory is free
-    for (int i = tid; i < kSelThreads * D; i += kSelThreads) {
-      const int pp = i / D, d = i % D;
-      const int key = 128 * b + pp;
-      float x = 0.f;
-      if (key < L) {
-        const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
-        if (pg >= 0 && pg < a.num_pages) x = elem(a.ik, (((long long)pg * Hkv + g) * a.ps + key % a.ps) * D + d, a.dtype);
-      }
-      kf[i] = x;
+    // this thread's staging rows: key 128 b + row and query chunk * 128 + row
+    const int key = 128 * b + row;
+    int page = -1;
+    if (key < L) {
+      page = a.bt[(long long)s * a.max_pages + key / a.ps];
+      if (page < 0 || page >= a.num_pages) page = -1;
     }
-    {
-      const int key = 128 * b + tid;
-      int ok = 0;
-      if (key < L) {
-        const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
-        ok = pg >= 0 && pg < a.num_pages;
+    const int qi = chunk * 128 + row;
+    __syncthreads();  // the previous unit is done with the shared memory
+    if (half == 0) {
+      sm.kvis[row] = page >= 0;
+      int lim = 0;
+      if (qi < tq) {
+        lim = min(128, L - 128 * b);
+        if (a.causal) lim = min(lim, L - tq + qi - 128 * b + 1);
       }
-      kvis[tid] = ok;
+      sm.qlim[row] = lim;
     }
-    __syncthreads();
-    const int i = chunk * kSelThreads + tid;  // this thread's query of the sequence
-    if (i < tq) {
-      float q[D];
-      const long long qb = ((long long)(q0 + i) * Hkv + g) * D;
+    const uint8_t* krow =
+        page >= 0 ? a.ik + ((((long long)page * Hkv + g) * a.ps + key % a.ps) * D) * esz : nullptr;
+    const uint8_t* qrow = qi < tq ? a.iq + (((long long)(q0 + qi) * Hkv + g) * D) * esz : nullptr;
+    float acc[8][8];
 #pragma unroll
-      for (int d = 0; d < D; ++d) q[d] = elem(a.iq, qb + d, a.dtype);
-      const int pos = L - tq + i;
-      int lim = min(128, L - 128 * b);
-      if (a.causal) lim = min(lim, pos - 128 * b + 1);
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 1
+    for (int d0 = 0; d0 < D; d0 += kLongChunk) {
+      float x[16];
+      if (krow) load16(krow + (size_t)(d0 + 16 * half) * esz, a.dtype, x);
+      else
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sm.k[16 * half + j][row] = x[j];
+      if (qrow) load16(qrow + (size_t)(d0 + 16 * half) * esz, a.dtype, x);
+      else
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sm.q[16 * half + j][row] = x[j];
+      __syncthreads();
+#pragma unroll 4
+      for (int dl = 0; dl < kLongChunk; ++dl) {
+        const float4 qa = *reinterpret_cast<const float4*>(&sm.q[dl][8 * qg]);
+        const float4 qb = *reinterpret_cast<const float4*>(&sm.q[dl][8 * qg + 4]);
+        const float4 ka = *reinterpret_cast<const float4*>(&sm.k[dl][4 * kg]);
+        const float4 kb = *reinterpret_cast<const float4*>(&sm.k[dl][64 + 4 * kg]);
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const float kv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(qv[i], kv[j], acc[i][j]);
+      }
+      __syncthreads();  // the chunk is read before the next one is staged
+    }
+    // block maximum per query over its visible keys (NaN dots skipped),
+    // then over the 16 threads that share the query
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int qr = 8 * qg + i;
+      const int lim = sm.qlim[qr];
       float m = -INFINITY;
       int h = 0;
-      // four keys per pass: four independent FMA chains, each summed in
-      // dimension order
-      for (int pp = 0; pp < lim; pp += 4) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const float4* k0 = reinterpret_cast<const float4*>(kf + (pp + 0) * D);
-        const float4* k1 = reinterpret_cast<const float4*>(kf + min(pp + 1, 127) * D);
-        const float4* k2 = reinterpret_cast<const float4*>(kf + min(pp + 2, 127) * D);
-        const float4* k3 = reinterpret_cast<const float4*>(kf + min(pp + 3, 127) * D);
 #pragma unroll
-        for (int d4 = 0; d4 < D / 4; ++d4) {
-          const float4 a0 = k0[d4], a1 = k1[d4], a2 = k2[d4], a3 = k3[d4];
-          acc[0] = __fmaf_rn(q[4 * d4], a0.x, acc[0]);
-          acc[1] = __fmaf_rn(q[4 * d4], a1.x, acc[1]);
-          acc[2] = __fmaf_rn(q[4 * d4], a2.x, acc[2]);
-          acc[3] = __fmaf_rn(q[4 * d4], a3.x, acc[3]);
-          acc[0] = __fmaf_rn(q[4 * d4 + 1], a0.y, acc[0]);
-          acc[1] = __fmaf_rn(q[4 * d4 + 1], a1.y, acc[1]);
-          acc[2] = __fmaf_rn(q[4 * d4 + 1], a2.y, acc[2]);
-          acc[3] = __fmaf_rn(q[4 * d4 + 1], a3.y, acc[3]);
-          acc[0] = __fmaf_rn(q[4 * d4 + 2], a0.z, acc[0]);
-          acc[1] = __fmaf_rn(q[4 * d4 + 2], a1.z, acc[1]);
-          acc[2] = __fmaf_rn(q[4 * d4 + 2], a2.z, acc[2]);
-          acc[3] = __fmaf_rn(q[4 * d4 + 2], a3.z, acc[3]);
-          acc[0] = __fmaf_rn(q[4 * d4 + 3], a0.w, acc[0]);
-          acc[1] = __fmaf_rn(q[4 * d4 + 3], a1.w, acc[1]);
-          acc[2] = __fmaf_rn(q[4 * d4 + 3], a2.w, acc[2]);
-          acc[3] = __fmaf_rn(q[4 * d4 + 3], a3.w, acc[3]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int kp = pp + j;
-          if (kp >= lim || !kvis[kp] || isnan(acc[j])) continue;
-          if (!h || acc[j] > m) m = acc[j];
-          h = 1;
-        }
+      for (int j = 0; j < 8; ++j) {
+        const int kp = j < 4 ? 4 * kg + j : 64 + 4 * kg + (j - 4);
+        const float x = acc[i][j];
+        if (kp >= lim || !sm.kvis[kp] || isnan(x)) continue;
+        if (!h || x > m) m = x;
+        h = 1;
       }
-      a.score[((long long)(q0 + i) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, off);
+        const int oh = __shfl_xor_sync(0xffffffffu, h, off);
+        if (oh && (!h || om > m)) m = om;
+        h |= oh;
+      }
+      const int qq = chunk * 128 + qr;
+      if (kg == 0 && qq < tq) a.score[((long long)(q0 + qq) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
     }
   }
   pdl_wait();  // leave only after k_select_short has completed
@@ -556,9 +596,9 @@ cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, co
   if (attr_err != cudaSuccess) return attr_err;
   // persistent grids: as many CTAs as fit at once (a second, partial wave
   // would start only when the first finishes)
-  auto grid_for = [&](const void* kern, size_t smem) {
+  auto grid_for = [&](const void* kern, size_t smem, int threads) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSelThreads, smem) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
       per_sm = 1;
     return dim3((unsigned)(sms * per_sm));
   };
@@ -566,15 +606,17 @@ cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, co
   if (e != cudaSuccess) return e;
   const size_t ss = short_smem(idx_dim, esz), sl = long_smem(idx_dim);
   if (idx_dim == 64) {
-    e = launch_pdl(k_select_short<64>, grid_for((const void*)k_select_short<64>, ss), dim3(kSelThreads), ss, st, a);
+    e = launch_pdl(k_select_short<64>, grid_for((const void*)k_select_short<64>, ss, kSelThreads), dim3(kSelThreads),
+                   ss, st, a);
     if (e == cudaSuccess)
-      e = launch_pdl(k_select_long<64>, grid_for((const void*)k_select_long<64>, sl), dim3(kSelThreads), sl, st, a);
+      e = launch_pdl(k_select_long<64>, grid_for((const void*)k_select_long<64>, sl, kLongThreads),
+                     dim3(kLongThreads), sl, st, a);
   } else {
-    e = launch_pdl(k_select_short<128>, grid_for((const void*)k_select_short<128>, ss), dim3(kSelThreads), ss, st,
-                   a);
+    e = launch_pdl(k_select_short<128>, grid_for((const void*)k_select_short<128>, ss, kSelThreads),
+                   dim3(kSelThreads), ss, st, a);
     if (e == cudaSuccess)
-      e = launch_pdl(k_select_long<128>, grid_for((const void*)k_select_long<128>, sl), dim3(kSelThreads), sl, st,
-                     a);
+      e = launch_pdl(k_select_long<128>, grid_for((const void*)k_select_long<128>, sl, kLongThreads),
+                     dim3(kLongThreads), sl, st, a);
   }
   if (e != cudaSuccess) return e;
   const long long rows = (long long)p.total_q * p.num_kv_heads;
