@@ -264,16 +264,42 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();  // the previous unit's shared memory is free
     for (int i = tid; i < tq * D; i += kSelThreads)
       qs[i] = elem(a.iq, ((long long)(q0 + i / D) * Hkv + g) * D + i % D, a.dtype);
-    const int chunks_row = D * esz / 16;  // 16-byte chunks per key row
-    for (int c = tid; c < kSelThreads * chunks_row; c += kSelThreads) {
+    // the block's pages (one for 128-token pages, two for 64), read once;
+    // then every 16-byte chunk of the thread's share issued before any is
+    // stored, so the copies overlap (consecutive threads: consecutive
+    // chunks of a row)
+    const int chunks_row = D * esz / 16;  // 16-byte chunks per key row: 4, 8 or 16
+    int pg_lo = -1, pg_hi = -1;  // the pages of rows 0-63 and 64-127
+    if (128 * b < L) {
+      const int pg = a.bt[(long long)s * a.max_pages + (128 * b) / a.ps];
+      pg_lo = (pg >= 0 && pg < a.num_pages) ? pg : -1;
+    }
+    if (a.ps == 128) {
+      pg_hi = pg_lo;
+    } else if (128 * b + 64 < L) {
+      const int pg = a.bt[(long long)s * a.max_pages + (128 * b + 64) / a.ps];
+      pg_hi = (pg >= 0 && pg < a.num_pages) ? pg : -1;
+    }
+    uint4 xs[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i >= chunks_row) break;
+      const int c = i * kSelThreads + tid;
       const int rr = c / chunks_row, cc = c % chunks_row;
       const int key = 128 * b + rr;
-      if (key >= L) continue;
-      const int pg = a.bt[(long long)s * a.max_pages + key / a.ps];
-      if (pg < 0 || pg >= a.num_pages) continue;
-      const uint4 x = __ldcs(
-          reinterpret_cast<const uint4*>(a.ik + ((((long long)pg * Hkv + g) * a.ps + key % a.ps) * D) * esz) + cc);
-      *reinterpret_cast<uint4*>(kst + rr * row_bytes + cc * 16) = x;
+      const int pg = rr < 64 ? pg_lo : pg_hi;
+      xs[i] = make_uint4(0, 0, 0, 0);
+      if (key < L && pg >= 0)
+        xs[i] = __ldcs(reinterpret_cast<const uint4*>(
+                           a.ik + ((((long long)pg * Hkv + g) * a.ps + key % a.ps) * D) * esz) +
+                       cc);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i >= chunks_row) break;
+      const int c = i * kSelThreads + tid;
+      const int rr = c / chunks_row, cc = c % chunks_row;
+      *reinterpret_cast<uint4*>(kst + rr * row_bytes + cc * 16) = xs[i];
     }
     __syncthreads();
     float best[kSelSmallTq];
