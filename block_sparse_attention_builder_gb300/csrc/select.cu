@@ -33,6 +33,8 @@
 //                   become 64-bit keys (order-preserving score bits above the
 //                   complemented block index) in shared memory, sorted by a
 //                   bitonic network, and the first topk blocks are written.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,6 +42,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mxsa {
 
@@ -75,18 +78,6 @@ struct SelArgs {
   SelTable tab;
   int32_t B, total_q, Hkv, D, ps, num_pages, max_pages, max_blocks, topk, causal, dtype;
 };
-
-__device__ __forceinline__ float elem(const uint8_t* base, int64_t i, int dtype) {
-  if (dtype == MXSA_FP8_E4M3) {
-    const uint16_t two = base[i];
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-  }
-  const uint16_t bits = reinterpret_cast<const uint16_t*>(base)[i];
-  if (dtype == MXSA_BF16) return __uint_as_float((uint32_t)bits << 16);
-  return __half2float(__ushort_as_half(bits));
-}
 
 // The values of one 16-byte chunk, widened exactly to FP32 in dimension
 // order: 16 e4m3 values, or 8 of a 16-bit type.
@@ -195,162 +186,266 @@ __global__ void __launch_bounds__(kPrepThreads) k_select_prep(SelArgs a) {
   }
 }
 
-// Dot products of one staged key row with the first tq (<= NQ) queries,
-// each summed by fused multiply-adds in dimension order.
-template <int NQ, int D>
-__device__ __forceinline__ void short_dots(const uint8_t* row, const float* qs, int dtype, float* acc, int tq = NQ) {
-  if (dtype == MXSA_FP8_E4M3) {
-#pragma unroll 2
-    for (int cc = 0; cc < D / 16; ++cc) {
+// k_select_short: each unit's key rows come into a ring of kShortStages
+// shared-memory stages by TMA tiled copies (one box per page slice and
+// 128-byte column segment, swizzled: 16-byte chunk c of row r of a
+// segment lands at chunk c ^ (r & 7) for 128-byte rows, c ^ ((r >> 1) & 3)
+// for 64-byte ones), and the unit's query rows by bulk copies.  Thread 0
+// issues them kShortStages - 1 units ahead, so later units' copies overlap
+// this unit's scoring.  Thread r reads row r chunk by chunk in dimension
+// order; the swizzle spreads any 8 consecutive rows' same chunk over all
+// banks.
+constexpr int kShortStages = 3;
+
+// bytes of one row segment in shared memory (the swizzle span) and stage size
+__host__ __device__ constexpr int short_span(int D, int esz) { return D * esz < 128 ? D * esz : 128; }
+__host__ __device__ constexpr size_t short_stage_bytes(int D, int esz) {
+  return ((size_t)(kSelThreads + kSelSmallTq) * D * esz + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr size_t short_smem(int D, int esz) {
+  return kShortStages * short_stage_bytes(D, esz) + 1024;  // + alignment of the base to 1024
+}
+
+// What a short unit is: its sequence record, block and kv head.
+struct ShortUnit {
+  SeqRec r;
+  int s, b, g;
+};
+
+// A staged unit as the producer warp describes it to the scoring warps.
+struct ShortInfo {
+  int b, g, tq, L, q0, pg_lo, pg_hi;  // pages of key rows 0-63 and 64-127 (-1: none)
+  int pad;
+};
+
+// Page of the unit block's key row rr (0..127), or -1 (past the sequence or
+// outside [0, num_pages)).
+__device__ __forceinline__ int short_page(const SelArgs& a, const ShortUnit& x, int rr) {
+  const int key = 128 * x.b + rr;
+  if (key >= x.r.L) return -1;
+  const int pg = a.bt[(long long)x.s * a.max_pages + key / a.ps];
+  return (pg >= 0 && pg < a.num_pages) ? pg : -1;
+}
+
+// The producer's look-ups for unit u: the sequence (advanced from *s_cur,
+// the previous unit's: a CTA's units come in increasing order), the
+// block's pages and the bytes its copies will bring.
+struct ShortPlan {
+  ShortInfo in;
+  int s;
+  uint32_t bytes;
+};
+
+__device__ __forceinline__ ShortPlan short_plan(const SelArgs& a, long long u, int* s_cur, int D, int esz) {
+  ShortPlan pl;
+  const int g = (int)(u % a.Hkv);
+  const long long v = u / a.Hkv;
+  int s = *s_cur;
+  while (s + 1 < a.B && a.tab.unit_short[s + 1] <= v) ++s;  // the last s with prefix[s] <= v
+  *s_cur = s;
+  const SeqRec r = a.tab.seq[s];
+  ShortUnit x;
+  x.r = r;
+  x.s = s;
+  x.g = g;
+  x.b = (int)(v - a.tab.unit_short[s]);
+  const uint32_t row = (uint32_t)D * esz, span = (uint32_t)short_span(D, esz), nseg = row / span;
+  const int n_slices = a.ps == 128 ? 1 : 2, per = a.ps == 128 ? 128 : 64;
+  int pgs[2] = {-1, -1};
+  uint32_t bytes = (uint32_t)r.tq * row;
+  for (int h = 0; h < n_slices; ++h) {
+    pgs[h] = short_page(a, x, per * h);
+    if (pgs[h] >= 0) bytes += nseg * (uint32_t)per * span;
+  }
+  pl.in.b = x.b;
+  pl.in.g = g;
+  pl.in.tq = r.tq;
+  pl.in.L = r.L;
+  pl.in.q0 = r.q0;
+  pl.in.pg_lo = pgs[0];
+  pl.in.pg_hi = a.ps == 128 ? pgs[0] : pgs[1];
+  pl.in.pad = 0;
+  pl.s = s;
+  pl.bytes = bytes;
+  return pl;
+}
+
+// The copies of a planned unit into stage `st` on barrier `full`: per page
+// slice of the block (one for 128-token pages, two for 64) on a valid page,
+// one TMA box per column segment (segment sg of rows at sg * 128 * span +
+// row * span); then the query rows after the 128 key rows.
+__device__ __forceinline__ void short_issue(const SelArgs& a, const CUtensorMap* tmk, const ShortPlan& pl,
+                                            uint8_t* st, uint64_t* full, ShortInfo* info, int D, int esz) {
+  const uint32_t row = (uint32_t)D * esz, span = (uint32_t)short_span(D, esz), nseg = row / span;
+  const int n_slices = a.ps == 128 ? 1 : 2, per = a.ps == 128 ? 128 : 64;
+  *info = pl.in;  // published by the arrival below
+  mbar_arrive_expect_tx(full, pl.bytes);
+  for (int h = 0; h < n_slices; ++h) {
+    const int pg = h == 0 ? pl.in.pg_lo : pl.in.pg_hi;
+    if (pg < 0) continue;
+    for (uint32_t sg = 0; sg < nseg; ++sg)
+      tma_load_3d(st + (size_t)sg * kSelThreads * span + (size_t)per * h * span, tmk, full,
+                  (int)(sg * span / esz), 0, pg * a.Hkv + pl.in.g);
+  }
+  for (int i = 0; i < pl.in.tq; ++i)
+    bulk_load(st + (size_t)kSelThreads * row + (size_t)i * row,
+              a.iq + ((long long)(pl.in.q0 + i) * a.Hkv + pl.in.g) * row, row, full);
+}
+
+// Dot products of key row t (swizzled segments in `keys`) with the first
+// tq (<= NQ) query rows (plain rows in `qrows`), each summed by fused
+// multiply-adds in dimension order.
+template <int D, bool kFp8, int NQ>
+__device__ __forceinline__ void short_dots(const uint8_t* keys, const uint8_t* qrows, int t, int tq, bool bf16,
+                                           float* acc) {
+  constexpr int esz = kFp8 ? 1 : 2, span = short_span(D, esz), nseg = D * esz / span, cps = span / 16;
+  constexpr int epc = 16 / esz;  // elements per 16-byte chunk
+#pragma unroll
+  for (int sg = 0; sg < nseg; ++sg) {
+#pragma unroll
+    for (int c = 0; c < cps; ++c) {
+      const int sw = span == 128 ? (c ^ (t & 7)) : (c ^ ((t >> 1) & 3));
+      const uint4 kv = *reinterpret_cast<const uint4*>(keys + (size_t)sg * kSelThreads * span + (size_t)t * span + sw * 16);
       float kd[16];
-      unpack_e4m3x16(*reinterpret_cast<const uint4*>(row + cc * 16), kd);
+      if (kFp8) unpack_e4m3x16(kv, kd);
+      else unpack_16bitx8(kv, bf16, kd);
+      const int dchunk = sg * cps + c;  // the chunk's place in the row
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
+      for (int i = 0; i < NQ; ++i) {
+        if (i >= tq) break;
+        const uint4 qv = *reinterpret_cast<const uint4*>(qrows + (size_t)i * D * esz + dchunk * 16);
+        float qd[16];
+        if (kFp8) unpack_e4m3x16(qv, qd);
+        else unpack_16bitx8(qv, bf16, qd);
 #pragma unroll
-        for (int i = 0; i < NQ; ++i)
-          if (i < tq) acc[i] = __fmaf_rn(qs[i * D + cc * 16 + e], kd[e], acc[i]);
-    }
-  } else {
-    const bool bf16 = dtype == MXSA_BF16;
-#pragma unroll 2
-    for (int cc = 0; cc < D / 8; ++cc) {
-      float kd[8];
-      unpack_16bitx8(*reinterpret_cast<const uint4*>(row + cc * 16), bf16, kd);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int i = 0; i < NQ; ++i)
-          if (i < tq) acc[i] = __fmaf_rn(qs[i * D + cc * 8 + e], kd[e], acc[i]);
+        for (int e = 0; e < epc; ++e) acc[i] = __fmaf_rn(qd[e], kd[e], acc[i]);
+      }
     }
   }
 }
 
-// shared memory of k_select_short: 8 FP32 queries, then 128 raw key rows
-// padded by 16 bytes (each thread reads its own row without bank conflicts)
-__host__ __device__ constexpr size_t short_smem(int D, int esz) {
-  return (size_t)kSelSmallTq * D * sizeof(float) + (size_t)kSelThreads * (D * esz + 16);
-}
+// 160 threads: warps 0-3 score (thread r: key row r), warp 4 issues the
+// copies kShortStages units ahead.
+constexpr int kShortThreads = kSelThreads + 32;
 
-template <int D>
-__global__ void __launch_bounds__(kSelThreads)
-    k_select_short(SelArgs a) {
-  extern __shared__ __align__(16) uint8_t sm_raw[];
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(kShortThreads)
+    k_select_short(const __grid_constant__ CUtensorMap tmk, SelArgs a) {
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kShortStages], empty[kShortStages];
+  __shared__ ShortInfo info[kShortStages];
   __shared__ float red_max[kSelSmallTq][kSelThreads / 32];
   __shared__ int red_have[kSelSmallTq][kSelThreads / 32];
+  __shared__ int abort_flag, sink;
   pdl_wait();  // the sequence table
   // only now: k_select_long reads the table without a wait of its own
   pdl_launch_dependents();
+  constexpr int esz = kFp8 ? 1 : 2;
+  constexpr size_t stage = short_stage_bytes(D, esz);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int Hkv = a.Hkv;
-  const int esz = a.dtype == MXSA_FP8_E4M3 ? 1 : 2;
-  const int row_bytes = D * esz + 16;
-  float* qs = reinterpret_cast<float*>(sm_raw);                      // [8][D]
-  uint8_t* kst = sm_raw + kSelSmallTq * D * sizeof(float);           // [128][row_bytes]
-  const long long units = a.tab.unit_short[a.B] * Hkv;
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int g = (int)(u % Hkv);
-    const long long v = u / Hkv;
-    const int s = unit_seq(a.tab.unit_short, a.B, v);
-    const SeqRec r = a.tab.seq[s];
-    const int b = (int)(v - a.tab.unit_short[s]);
-    const int tq = r.tq, L = r.L, q0 = r.q0;
-    // this thread's key position and whether it is on a valid page
-    const int p = 128 * b + tid;
-    int page = -1;
-    if (p < L) {
-      page = a.bt[(long long)s * a.max_pages + p / a.ps];
-      if (page < 0 || page >= a.num_pages) page = -1;
+  const bool bf16 = a.dtype == MXSA_BF16;
+  const long long units = a.tab.unit_short[a.B] * a.Hkv;
+  const long long first = blockIdx.x, stride = gridDim.x;
+  if (first >= units) return;  // uniform
+  const long long n_mine = (units - first + stride - 1) / stride;
+  if (tid == 0) {
+    for (int i = 0; i < kShortStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kSelThreads);
     }
-    __syncthreads();  // the previous unit's shared memory is free
-    for (int i = tid; i < tq * D; i += kSelThreads)
-      qs[i] = elem(a.iq, ((long long)(q0 + i / D) * Hkv + g) * D + i % D, a.dtype);
-    // the block's pages (one for 128-token pages, two for 64), read once;
-    // then every 16-byte chunk of the thread's share issued before any is
-    // stored, so the copies overlap (consecutive threads: consecutive
-    // chunks of a row)
-    const int chunks_row = D * esz / 16;  // 16-byte chunks per key row: 4, 8 or 16
-    int pg_lo = -1, pg_hi = -1;  // the pages of rows 0-63 and 64-127
-    if (128 * b < L) {
-      const int pg = a.bt[(long long)s * a.max_pages + (128 * b) / a.ps];
-      pg_lo = (pg >= 0 && pg < a.num_pages) ? pg : -1;
+    abort_flag = 0;
+    sink = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  int* status = a.flags ? a.flags : &sink;
+  if (warp == kSelThreads / 32) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmk);
+      int s_cur = 0;
+      for (long long j = 0; j < n_mine; ++j) {
+        const int st = (int)(j % kShortStages);
+        // the look-ups first: their latency overlaps the wait for the stage
+        const ShortPlan pl = short_plan(a, first + j * stride, &s_cur, D, esz);
+        // the stage's previous unit (j - kShortStages) was scored
+        if (!mbar_wait(&empty[st], (uint32_t)(((j / kShortStages) & 1) ^ 1), &abort_flag, status, MXSA_FLAG_TIMEOUT,
+                       kWaitLimitNs))
+          break;
+        short_issue(a, &tmk, pl, sm + st * stage, &full[st], &info[st], D, esz);
+      }
+      // copies of the last units may still be in flight if a wait gave up
+      for (long long i = n_mine > kShortStages ? n_mine - kShortStages : 0; i < n_mine; ++i)
+        mbar_drain(&full[i % kShortStages], (uint32_t)((i / kShortStages) & 1), status, MXSA_FLAG_TIMEOUT,
+                   kWaitLimitNs);
     }
-    if (a.ps == 128) {
-      pg_hi = pg_lo;
-    } else if (128 * b + 64 < L) {
-      const int pg = a.bt[(long long)s * a.max_pages + (128 * b + 64) / a.ps];
-      pg_hi = (pg >= 0 && pg < a.num_pages) ? pg : -1;
-    }
-    uint4 xs[16];
+  } else {
+    // ------------------------------------------------------------- scoring
+    for (long long i = 0; i < n_mine; ++i) {
+      const int st = (int)(i % kShortStages);
+      const bool ok = mbar_wait(&full[st], (uint32_t)((i / kShortStages) & 1), &abort_flag, status,
+                                MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+      const ShortInfo x = info[st];
+      const int tq = ok ? x.tq : 0, L = x.L, q0 = x.q0, b = x.b;
+      const int page = 128 * b + tid < L ? (tid < 64 ? x.pg_lo : x.pg_hi) : -1;
+      float best[kSelSmallTq];
+      int have[kSelSmallTq];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i >= chunks_row) break;
-      const int c = i * kSelThreads + tid;
-      const int rr = c / chunks_row, cc = c % chunks_row;
-      const int key = 128 * b + rr;
-      const int pg = rr < 64 ? pg_lo : pg_hi;
-      xs[i] = make_uint4(0, 0, 0, 0);
-      if (key < L && pg >= 0)
-        xs[i] = __ldcs(reinterpret_cast<const uint4*>(
-                           a.ik + ((((long long)pg * Hkv + g) * a.ps + key % a.ps) * D) * esz) +
-                       cc);
-    }
+      for (int q = 0; q < kSelSmallTq; ++q) {
+        best[q] = -INFINITY;
+        have[q] = 0;
+      }
+      if (ok && page >= 0) {
+        float acc[kSelSmallTq];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i >= chunks_row) break;
-      const int c = i * kSelThreads + tid;
-      const int rr = c / chunks_row, cc = c % chunks_row;
-      *reinterpret_cast<uint4*>(kst + rr * row_bytes + cc * 16) = xs[i];
-    }
-    __syncthreads();
-    float best[kSelSmallTq];
-    int have[kSelSmallTq];
+        for (int q = 0; q < kSelSmallTq; ++q) acc[q] = 0.f;
+        const uint8_t* keys = sm + st * stage;
+        const uint8_t* qrows = keys + (size_t)kSelThreads * D * esz;
+        if (tq == 1) short_dots<D, kFp8, 1>(keys, qrows, tid, 1, bf16, acc);
+        else short_dots<D, kFp8, kSelSmallTq>(keys, qrows, tid, tq, bf16, acc);
+        const int p = 128 * b + tid;
 #pragma unroll
-    for (int i = 0; i < kSelSmallTq; ++i) {
-      best[i] = -INFINITY;
-      have[i] = 0;
-    }
-    if (page >= 0) {
-      float acc[kSelSmallTq];
-#pragma unroll
-      for (int i = 0; i < kSelSmallTq; ++i) acc[i] = 0.f;
-      const uint8_t* row = kst + tid * row_bytes;
-      if (tq == 1)
-        short_dots<1, D>(row, qs, a.dtype, acc);
-      else
-        short_dots<kSelSmallTq, D>(row, qs, a.dtype, acc, tq);
-#pragma unroll
-      for (int i = 0; i < kSelSmallTq; ++i) {
-        const int pos = L - tq + i;
-        const bool vis = i < tq && (!a.causal || p <= pos) && !isnan(acc[i]);
-        if (vis) {
-          best[i] = acc[i];
-          have[i] = 1;
+        for (int q = 0; q < kSelSmallTq; ++q) {
+          const int pos = L - tq + q;
+          if (q < tq && (!a.causal || p <= pos) && !isnan(acc[q])) {
+            best[q] = acc[q];
+            have[q] = 1;
+          }
         }
       }
-    }
+      mbar_arrive(&empty[st]);  // this thread is done with the stage
 #pragma unroll
-    for (int i = 0; i < kSelSmallTq; ++i) {
-      if (i >= tq) break;
-      float m = best[i];
+      for (int q = 0; q < kSelSmallTq; ++q) {
+        if (q >= tq) break;
+        float m = best[q];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const int h = __any_sync(0xffffffffu, have[i]);
-      if (lane == 0) {
-        red_max[i][warp] = m;
-        red_have[i][warp] = h;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int h = __any_sync(0xffffffffu, have[q]);
+        if (lane == 0) {
+          red_max[q][warp] = m;
+          red_have[q][warp] = h;
+        }
       }
-    }
-    __syncthreads();
-    if (tid < tq) {
-      float m = -INFINITY;
-      int h = 0;
-      for (int w2 = 0; w2 < kSelThreads / 32; ++w2) {
-        m = fmaxf(m, red_max[tid][w2]);
-        h |= red_have[tid][w2];
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid < tq) {
+        float m = -INFINITY;
+        int h = 0;
+        for (int w2 = 0; w2 < kSelThreads / 32; ++w2) {
+          m = fmaxf(m, red_max[tid][w2]);
+          h |= red_have[tid][w2];
+        }
+        a.score[((long long)(q0 + tid) * a.Hkv + x.g) * a.max_blocks + b] = h ? m : NAN;
       }
-      a.score[((long long)(q0 + tid) * Hkv + g) * a.max_blocks + b] = h ? m : NAN;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the sums are read before the next unit writes them
     }
   }
+  __syncthreads();
+  if (tid == 0)
+    for (int i = 0; i < kShortStages; ++i) {
+      mbar_inval(&full[i]);
+      mbar_inval(&empty[i]);
+    }
 }
 
 // k_select_long: a unit's 128 queries x 128 keys of dot products, blocked
@@ -573,6 +668,34 @@ size_t select_workspace_bytes(const mxsa_problem& p) {
   return align256(select_score_bytes(p)) + align256(B * sizeof(SeqRec)) + 2 * align256((B + 1) * 8) + 256;
 }
 
+// 3-D map of the index-key cache [pages * Hkv][page_size][idx_dim] for the
+// short scorer: box = one page's rows x one segment of at most 128 bytes,
+// 128-byte swizzle (64-byte for the 64-byte rows of FP8 64-dim keys).
+static bool make_idx_map(CUtensorMap* m, const void* ik, const mxsa_problem& p, int D) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  if (!fn) return false;
+  const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
+  const cuuint64_t esz = fp8 ? 1 : 2;
+  const int span = short_span(D, (int)esz);
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.page_size, (cuuint64_t)p.num_pages * p.num_kv_heads};
+  cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)D * esz * p.page_size};
+  cuuint32_t box[3] = {(cuuint32_t)(span / esz), (cuuint32_t)(p.page_size == 128 ? 128 : 64), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const CUresult r = fn(m, dt, 3, const_cast<void*>(ik), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, const void* ik,
                           const int32_t* bt, const int64_t* cu, const int32_t* lens, void* ws, int32_t* sel,
                           int32_t* flags, cudaStream_t st) {
@@ -612,14 +735,18 @@ cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, co
   const int esz = p.kv_dtype == MXSA_FP8_E4M3 ? 1 : 2;
   static cudaError_t attr_err = [] {
     cudaError_t e = cudaSuccess;
-    const void* k[4] = {(const void*)k_select_short<64>, (const void*)k_select_short<128>,
-                        (const void*)k_select_long<64>, (const void*)k_select_long<128>};
-    const size_t bytes[4] = {short_smem(64, 2), short_smem(128, 2), long_smem(64), long_smem(128)};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    const void* k[6] = {(const void*)k_select_short<64, false>, (const void*)k_select_short<128, false>,
+                        (const void*)k_select_short<64, true>,  (const void*)k_select_short<128, true>,
+                        (const void*)k_select_long<64>,         (const void*)k_select_long<128>};
+    const size_t bytes[6] = {short_smem(64, 2), short_smem(128, 2), short_smem(64, 1),
+                             short_smem(128, 1), long_smem(64),     long_smem(128)};
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
       e = cudaFuncSetAttribute(k[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes[i]);
     return e;
   }();
   if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap tmk;
+  if (!make_idx_map(&tmk, ik, p, idx_dim)) return cudaErrorInvalidValue;
   // persistent grids: as many CTAs as fit at once (a second, partial wave
   // would start only when the first finishes)
   auto grid_for = [&](const void* kern, size_t smem, int threads) {
@@ -631,15 +758,17 @@ cudaError_t launch_select(const mxsa_problem& p, int idx_dim, const void* iq, co
   cudaError_t e = launch_pdl(k_select_prep, dim3(1), dim3(kPrepThreads), 0, st, a);
   if (e != cudaSuccess) return e;
   const size_t ss = short_smem(idx_dim, esz), sl = long_smem(idx_dim);
+  auto short_kernel = [&](auto kern) {
+    return launch_pdl(kern, grid_for((const void*)kern, ss, kShortThreads), dim3(kShortThreads), ss, st, tmk, a);
+  };
+  const bool fp8 = p.kv_dtype == MXSA_FP8_E4M3;
   if (idx_dim == 64) {
-    e = launch_pdl(k_select_short<64>, grid_for((const void*)k_select_short<64>, ss, kSelThreads), dim3(kSelThreads),
-                   ss, st, a);
+    e = fp8 ? short_kernel(k_select_short<64, true>) : short_kernel(k_select_short<64, false>);
     if (e == cudaSuccess)
       e = launch_pdl(k_select_long<64>, grid_for((const void*)k_select_long<64>, sl, kLongThreads),
                      dim3(kLongThreads), sl, st, a);
   } else {
-    e = launch_pdl(k_select_short<128>, grid_for((const void*)k_select_short<128>, ss, kSelThreads),
-                   dim3(kSelThreads), ss, st, a);
+    e = fp8 ? short_kernel(k_select_short<128, true>) : short_kernel(k_select_short<128, false>);
     if (e == cudaSuccess)
       e = launch_pdl(k_select_long<128>, grid_for((const void*)k_select_long<128>, sl, kLongThreads),
                      dim3(kLongThreads), sl, st, a);
