@@ -307,7 +307,7 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
 }
 
 __global__ void __launch_bounds__(kIndexThreads) k_index_dedup(DedupArgs a) {
-  __shared__ unsigned long long tmp[33];
+  __shared__ unsigned long long tmp[3 * 33];
   __shared__ int32_t rowbuf[ixp::kMarkWarps][256];
   const IndexPtrs& ix = a.ia.ix;
   int* bar = ix.hdr + kHdrBarCount;

@@ -33,7 +33,7 @@ using ixp::IndexArgs;
 using ixp::kIndexThreads;
 
 __global__ void __launch_bounds__(kIndexThreads) k_index(IndexArgs a) {
-  __shared__ unsigned long long tmp[33];
+  __shared__ unsigned long long tmp[3 * 33];
   __shared__ int32_t rowbuf[ixp::kMarkWarps][256];
   ixp::build_index_phases(a, tmp, rowbuf);
 }

@@ -40,6 +40,36 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* tmp, T* total) {
   return r;
 }
 
+// Three exclusive scans across the CTA at once (one round of barriers).
+// `tmp` holds 3 * 33 elements of shared memory.
+struct L3 {
+  long long a, b, c;
+};
+__device__ __forceinline__ L3 block_exclusive_scan3(L3 v, long long* tmp, L3* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const L3 inc{warp_inclusive_scan(v.a), warp_inclusive_scan(v.b), warp_inclusive_scan(v.c)};
+  if (lane == 31) {
+    tmp[warp] = inc.a;
+    tmp[33 + warp] = inc.b;
+    tmp[66 + warp] = inc.c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const long long x = lane < nw ? tmp[33 * j + lane] : 0;
+      const long long xi = warp_inclusive_scan(x);
+      if (lane < nw) tmp[33 * j + lane] = xi - x;
+      if (lane == nw - 1) tmp[33 * j + 32] = xi;
+    }
+  }
+  __syncthreads();
+  const L3 r{tmp[warp] + inc.a - v.a, tmp[33 + warp] + inc.b - v.b, tmp[66 + warp] + inc.c - v.c};
+  *total = L3{tmp[32], tmp[65], tmp[98]};
+  __syncthreads();
+  return r;
+}
+
 // Totals of the sequence scan (blocks, bitmap words and kmap bytes per kv head).
 struct SeqTotals {
   long long nb, bmw, kmw;
@@ -87,18 +117,16 @@ struct SeqTab {
 __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_t* cu, const int32_t* lens, int B,
                                                int total_q, int Hkv, int cap_len, int causal, long long* tmp,
                                                bool writer = true, int (*tab)[kSeqTab] = nullptr) {
-  __shared__ int cu_bad;
   long long carry_blk = 0, carry_bm = 0, carry_km = 0;
   int flags = 0;
   // cu_seqlens_q must be a non-decreasing partition of [0, total_q]; if it is
   // not, every sequence is treated as having no new tokens (nothing indexed),
-  // which keeps all per-sequence regions inside their shape-derived bounds
-  if (threadIdx.x == 0) cu_bad = (cu[0] != 0 || cu[B] != (int64_t)total_q) ? 1 : 0;
-  __syncthreads();
-  for (int s = threadIdx.x; s < B; s += blockDim.x)
-    if (cu[s + 1] < cu[s]) cu_bad = 1;
-  __syncthreads();
-  const bool cu_ok = cu_bad == 0;
+  // which keeps all per-sequence regions inside their shape-derived bounds.
+  // The first chunk's lengths load in the same round trip as the check.
+  bool bad = threadIdx.x == 0 && (cu[0] != 0 || cu[B] != (int64_t)total_q);
+  for (int s = threadIdx.x; s < B; s += blockDim.x) bad |= cu[s + 1] < cu[s];
+  const int len0 = (int)threadIdx.x < B ? lens[threadIdx.x] : 0;
+  const bool cu_ok = !__syncthreads_or(bad);
   if (!cu_ok) flags |= MXSA_FLAG_CU;
   for (int base = 0; base < B; base += blockDim.x) {
     const int s = base + threadIdx.x;
@@ -108,7 +136,7 @@ __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_
       const int64_t c0 = cu[s], c1 = cu[s + 1];
       tq = cu_ok ? (int)(c1 - c0) : 0;
       q0 = cu_ok ? (int)c0 : 0;
-      int Lr = lens[s];
+      const int Lr = base == 0 ? len0 : lens[s];
       if (Lr < 0 || Lr > cap_len) flags |= MXSA_FLAG_LEN;
       L = Lr < 0 ? 0 : (Lr > cap_len ? cap_len : Lr);
       if (causal && L < tq) flags |= MXSA_FLAG_CAUSAL_LEN;
@@ -117,14 +145,12 @@ __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_
       bmw = nblk * words;
       kmw = nblk * tq;
     }
-    long long tb, tbm, tkm;
-    long long eb = block_exclusive_scan(nblk, tmp, &tb);
-    long long ebm = block_exclusive_scan(bmw, tmp, &tbm);
-    long long ekm = block_exclusive_scan(kmw, tmp, &tkm);
+    L3 t3;
+    const L3 e3 = block_exclusive_scan3(L3{nblk, bmw, kmw}, tmp, &t3);
     if (tab != nullptr && s < B && B <= kSeqTab) {
-      tab[0][s] = (int)(carry_blk + eb);
-      tab[1][s] = (int)(carry_bm + ebm);
-      tab[2][s] = (int)(carry_km + ekm);
+      tab[0][s] = (int)(carry_blk + e3.a);
+      tab[1][s] = (int)(carry_bm + e3.b);
+      tab[2][s] = (int)(carry_km + e3.c);
       tab[3][s] = q0;
       tab[4][s] = L;
       tab[5][s] = tq;
@@ -133,17 +159,17 @@ __device__ __forceinline__ SeqTotals phase_seq(const IndexPtrs& ix, const int64_
       SeqInfo si;
       si.L = L;
       si.nblk = (int)nblk;
-      si.blk_off = (int)(carry_blk + eb);
+      si.blk_off = (int)(carry_blk + e3.a);
       si.tq = tq;
       si.q_begin = q0;
-      si.bm_off = (int)(carry_bm + ebm);
-      si.km_off = (int)(carry_km + ekm);
+      si.bm_off = (int)(carry_bm + e3.b);
+      si.km_off = (int)(carry_km + e3.c);
       si.words = words;
       ix.seq[s] = si;
     }
-    carry_blk += tb;
-    carry_bm += tbm;
-    carry_km += tkm;
+    carry_blk += t3.a;
+    carry_bm += t3.b;
+    carry_km += t3.c;
   }
   // OR the per-thread flags together
   int f = __reduce_or_sync(0xffffffffu, flags);
@@ -177,15 +203,20 @@ __device__ __forceinline__ void phase_zero(const IndexPtrs& ix, int Hkv, const S
   for (long long i = tid; i < n_bm; i += stride) ix.bitmap[i] = 0u;
 }
 
-__device__ __forceinline__ void phase_token_seq(const IndexPtrs& ix, const int64_t* cu, int B, int total_q) {
+// token -> sequence: the last s with cu[s] <= t (sequences of zero tokens
+// are skipped naturally).  With `first` (the table's first tokens, B <=
+// kSeqTab) the search runs in shared memory; those are cu[s] when
+// cu_seqlens_q is valid and all 0 otherwise, when no token has a sequence
+// and any s in range will do.
+__device__ __forceinline__ void phase_token_seq(const IndexPtrs& ix, const int64_t* cu, int B, int total_q,
+                                                const int* first = nullptr) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   for (long long t = tid; t < total_q; t += stride) {
-    // last s with cu[s] <= t (sequences of zero tokens are skipped naturally)
     int lo = 0, hi = B - 1;
     while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (cu[mid] <= t) lo = mid;
+      const int mid = (lo + hi + 1) >> 1;
+      if ((first ? (long long)first[mid] : (long long)cu[mid]) <= t) lo = mid;
       else hi = mid - 1;
     }
     ix.token_seq[t] = lo;
@@ -193,61 +224,111 @@ __device__ __forceinline__ void phase_token_seq(const IndexPtrs& ix, const int64
 }
 
 constexpr int kMarkWarps = 8;
+constexpr int kMarkRows = 8;  // most (token, kv head) rows one warp marks per pass
 
-// count = false leaves counts alone (the caller derives them from the
-// bitmap rows), so popular blocks cost no contended atomics.
-__device__ __forceinline__ void phase_mark(const IndexPtrs& ix, const int32_t* sel, int total_q, int Hkv, int topk, int causal,
-                           int32_t (*rowbuf)[256], bool count = true) {
+// One warp marks up to kMarkRows consecutive (token, kv head) rows per pass
+// (as many as fit 256 selection slots), so the loads of several rows are in
+// flight together: the selections of all of them in one coalesced read, the
+// sequence facts of row r by lane r.  Lanes then take the pass's slots in
+// order; each row's entry count and smallest / largest block are summed over
+// the lanes holding its slots.  count = false leaves counts alone (the caller
+// derives them from the bitmap rows), so popular blocks cost no contended
+// atomics.
+__device__ __forceinline__ void phase_mark(const IndexPtrs& ix, const int32_t* sel, int total_q, int Hkv, int topk,
+                                           int causal, int32_t (*rowbuf)[256], bool count = true) {
+  // per row of the pass: nblk, token index in its sequence (-1: none),
+  // causal position, bitmap offset, kmap offset, words, tq, block offset,
+  // kv head, then the row's entry count, smallest and largest block
+  __shared__ int s_row[kMarkWarps][kMarkRows][12];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int NB = ix.hdr[kHdrNB];
   const size_t BMW = (size_t)ix.hdr[kHdrBMW], KMW = (size_t)ix.hdr[kHdrKMW];
   const long long n_rows = (long long)total_q * Hkv;
-  int flags = 0, made = 0, bmin = 0x7fffffff, bmax = -1;
-  for (long long row = (long long)blockIdx.x * kMarkWarps + w; row < n_rows; row += (long long)gridDim.x * kMarkWarps) {
-    const int t = (int)(row / Hkv), g = (int)(row % Hkv);
-    const int32_t* srow = sel + row * topk;
-    for (int k = lane; k < topk; k += 32) rowbuf[w][k] = srow[k];
+  // rows per pass: enough to give every warp of the grid work, at most
+  // kMarkRows and 256 slots (1 <= topk <= 256)
+  const long long warps = (long long)gridDim.x * kMarkWarps;
+  const int rp = (int)max(1ll, min((long long)min(kMarkRows, 256 / topk), (n_rows + warps - 1) / warps));
+  const long long stride = warps * rp;
+  int flags = 0;
+  for (long long r0 = ((long long)blockIdx.x * kMarkWarps + w) * rp; r0 < n_rows; r0 += stride) {
+    const int nr = (int)min((long long)rp, n_rows - r0);
+    const int ns = nr * topk;
+    const int32_t* srow = sel + r0 * topk;
+    for (int x = lane; x < ns; x += 32) rowbuf[w][x] = srow[x];
+    if (lane < nr) {
+      const long long row = r0 + lane;
+      const int t = (int)(row / Hkv), g = (int)(row - (long long)t * Hkv);
+      const SeqInfo si = ix.seq[ix.token_seq[t]];
+      const int i = t - si.q_begin;
+      int* f = s_row[w][lane];
+      f[0] = si.nblk;
+      f[1] = (i >= 0 && i < si.tq) ? i : -1;
+      f[2] = si.L - si.tq + i;
+      f[3] = si.bm_off;
+      f[4] = si.km_off;
+      f[5] = si.words;
+      f[6] = si.tq;
+      f[7] = si.blk_off;
+      f[8] = g;
+      f[9] = 0;
+      f[10] = 0x7fffffff;
+      f[11] = -1;
+    }
     __syncwarp();
-    const int s = ix.token_seq[t];
-    const SeqInfo si = ix.seq[s];
-    const int i = t - si.q_begin;
-    const bool in_seq = i >= 0 && i < si.tq;
-    const int pos = si.L - si.tq + i;
-    for (int k = lane; k < topk; k += 32) {
-      const long long slot = row * topk + k;
-      ix.slot_entry[slot] = -1;
-      const int b = rowbuf[w][k];
-      if (b == -1 || !in_seq) continue;
-      if (b < -1 || b >= si.nblk) {
-        flags |= MXSA_FLAG_SEL_RANGE;
-        continue;
+    for (int x0 = 0; x0 < ns; x0 += 32) {
+      const int x = x0 + lane;
+      const int r = x < ns ? x / topk : nr;  // nr: past the pass
+      const int* f = s_row[w][r < nr ? r : 0];
+      const int i = f[1];
+      bool cand = false;  // a block of the sequence, for a token of the sequence
+      int b = 0;
+      if (x < ns) {
+        ix.slot_entry[r0 * topk + x] = -1;
+        b = rowbuf[w][x];
+        if (b != -1 && i >= 0) {
+          if (b < -1 || b >= f[0]) flags |= MXSA_FLAG_SEL_RANGE;
+          else cand = true;
+        }
       }
-      bool dup = false;
-      for (int k2 = 0; k2 < k; ++k2) dup |= rowbuf[w][k2] == b;
-      if (dup) {
-        flags |= MXSA_FLAG_SEL_DUP;
-        continue;
+      // repeated earlier in its row: at a lower lane of this 32-slot step
+      // (the lanes with the same row and block), or in an earlier step
+      const unsigned long long tag = cand ? ((unsigned long long)r << 32) | (unsigned)b
+                                          : (~0ull << 32) | (unsigned)lane;
+      const unsigned same = __match_any_sync(0xffffffffu, tag);
+      bool ok = false;
+      if (cand) {
+        bool dup = (same & ((1u << lane) - 1)) != 0;
+        for (int k2 = r * topk; k2 < x0; ++k2) dup |= rowbuf[w][k2] == b;
+        if (dup) flags |= MXSA_FLAG_SEL_DUP;
+        else ok = !(causal && 128 * b > f[2]);  // a block entirely after the token: no entry
       }
-      if (causal && 128 * b > pos) continue;  // block entirely after the token
-      const size_t word = (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words + (i >> 5);
-      atomicOr(&ix.bitmap[word], 1u << (i & 31));
-      ix.kmap[(size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq + i] = (uint8_t)k;
-      if (count) atomicAdd(&ix.counts[(long long)g * NB + si.blk_off + b], 1);
-      ++made;
-      bmin = min(bmin, b);
-      bmax = max(bmax, b);
+      if (ok) {
+        const int g = f[8], k = x - r * topk;
+        const size_t word = (size_t)g * BMW + (size_t)f[3] + (size_t)b * f[5] + (i >> 5);
+        atomicOr(&ix.bitmap[word], 1u << (i & 31));
+        ix.kmap[(size_t)g * KMW + (size_t)f[4] + (size_t)b * f[6] + i] = (uint8_t)k;
+        if (count) atomicAdd(&ix.counts[(long long)g * NB + f[7] + b], 1);
+      }
+      // the lanes of each row (the same r) sum their share; the lowest adds it
+      const unsigned grp = __match_any_sync(0xffffffffu, r);
+      const int made = __reduce_add_sync(grp, ok ? 1 : 0);
+      const int bmin = __reduce_min_sync(grp, ok ? b : 0x7fffffff);
+      const int bmax = __reduce_max_sync(grp, ok ? b : -1);
+      if (r < nr && lane == __ffs(grp) - 1) {
+        int* fr = s_row[w][r];
+        fr[9] += made;
+        fr[10] = min(fr[10], bmin);
+        fr[11] = max(fr[11], bmax);
+      }
+      __syncwarp();
     }
-    made = __reduce_add_sync(0xffffffffu, made);
-    bmin = __reduce_min_sync(0xffffffffu, bmin);
-    bmax = __reduce_max_sync(0xffffffffu, bmax);
-    if (lane == 0) {
-      ix.row_nnz[row] = made;
-      ix.row_minb[row] = bmin;
-      ix.row_maxb[row] = bmax;
+    if (lane < nr) {
+      const long long row = r0 + lane;
+      const int* f = s_row[w][lane];
+      ix.row_nnz[row] = f[9];
+      ix.row_minb[row] = f[10];
+      ix.row_maxb[row] = f[11];
     }
-    made = 0;
-    bmin = 0x7fffffff;
-    bmax = -1;
     __syncwarp();
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
@@ -294,25 +375,42 @@ __device__ __forceinline__ void phase_key_reduce(const IndexPtrs& ix, unsigned l
   if (threadIdx.x == 0) ix.cta_sums[blockIdx.x] = v;
 }
 
+// Writes the entries of the set bits of one bitmap word (word `w` of its
+// row: tokens 32 w + bit), starting at entry j; returns the next entry.  The
+// bits go in batches of kEmitBatch so that their kmap loads are in flight
+// together instead of one dependent load per entry.
+constexpr int kEmitBatch = 8;
+__device__ __forceinline__ int emit_word(const IndexPtrs& ix, uint32_t bits, int w, const uint8_t* km, int q_begin,
+                                         int g, int Hkv, int topk, int j) {
+  while (bits) {
+    int i[kEmitBatch], k[kEmitBatch];
+#pragma unroll
+    for (int u = 0; u < kEmitBatch; ++u) {
+      i[u] = bits ? w * 32 + __ffs(bits) - 1 : -1;
+      bits &= bits - 1;
+    }
+#pragma unroll
+    for (int u = 0; u < kEmitBatch; ++u) k[u] = i[u] >= 0 ? km[i[u]] : 0;
+#pragma unroll
+    for (int u = 0; u < kEmitBatch; ++u) {
+      if (i[u] >= 0) {
+        const int slot = ((q_begin + i[u]) * Hkv + g) * topk + k[u];
+        ix.entries[j] = slot;
+        ix.slot_entry[slot] = j;
+        ++j;
+      }
+    }
+  }
+  return j;
+}
+
 // Writes the entries of one bitmap row: `n_words` words starting at `bm`,
 // for tokens q_begin + 32 w + bit.  Serial over the row (one lane).
 __device__ __forceinline__ void emit_row_serial(const IndexPtrs& ix, const uint32_t* bm, int n_words,
                                                 const uint8_t* km, int q_begin, int g, int Hkv, int topk,
                                                 int base) {
   int j = base;
-  for (int w = 0; w < n_words; ++w) {
-    uint32_t bits = bm[w];
-    while (bits) {
-      const int bit = __ffs(bits) - 1;
-      bits &= bits - 1;
-      const int i = w * 32 + bit;
-      const int k = km[i];
-      const int slot = ((q_begin + i) * Hkv + g) * topk + k;
-      ix.entries[j] = slot;
-      ix.slot_entry[slot] = j;
-      ++j;
-    }
-  }
+  for (int w = 0; w < n_words; ++w) j = emit_word(ix, bm[w], w, km, q_begin, g, Hkv, topk, j);
 }
 
 // One warp writes the entries of a long bitmap row, 32 words at a time
@@ -323,20 +421,10 @@ __device__ __forceinline__ void emit_row_warp(const IndexPtrs& ix, const uint32_
   int run = base;
   for (int w0 = 0; w0 < n_words; w0 += 32) {
     const int w = w0 + lane;
-    uint32_t bits = w < n_words ? bm[w] : 0u;
+    const uint32_t bits = w < n_words ? bm[w] : 0u;
     const int cnt = __popc(bits);
     const int inc = warp_inclusive_scan(cnt);
-    int j = run + inc - cnt;
-    while (bits) {
-      const int bit = __ffs(bits) - 1;
-      bits &= bits - 1;
-      const int i = w * 32 + bit;
-      const int k = km[i];
-      const int slot = ((q_begin + i) * Hkv + g) * topk + k;
-      ix.entries[j] = slot;
-      ix.slot_entry[slot] = j;
-      ++j;
-    }
+    emit_word(ix, bits, w, km, q_begin, g, Hkv, topk, run + inc - cnt);
     run += __shfl_sync(0xffffffffu, inc, 31);
   }
 }
@@ -354,20 +442,10 @@ __device__ __forceinline__ void emit_row_shared(const IndexPtrs& ix, const uint3
     for (int w = counted + lane; w < w0; w += 32) skip += __popc(bm[w]);
     run += __reduce_add_sync(0xffffffffu, skip);
     const int w = w0 + lane;
-    uint32_t bits = w < n_words ? bm[w] : 0u;
+    const uint32_t bits = w < n_words ? bm[w] : 0u;
     const int cnt = __popc(bits);
     const int inc = warp_inclusive_scan(cnt);
-    int j = run + inc - cnt;
-    while (bits) {
-      const int bit = __ffs(bits) - 1;
-      bits &= bits - 1;
-      const int i = w * 32 + bit;
-      const int k = km[i];
-      const int slot = ((q_begin + i) * Hkv + g) * topk + k;
-      ix.entries[j] = slot;
-      ix.slot_entry[slot] = j;
-      ++j;
-    }
+    emit_word(ix, bits, w, km, q_begin, g, Hkv, topk, run + inc - cnt);
     run += __shfl_sync(0xffffffffu, inc, 31);
     counted = w0 + 32 < n_words ? w0 + 32 : n_words;
   }

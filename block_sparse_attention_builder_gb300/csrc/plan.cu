@@ -499,15 +499,17 @@ __device__ __forceinline__ void fast_phase_b(const IndexPtrs& ix, const SchedPtr
         }
       }
       __syncwarp();
-      // row_ptr of every key of the row: entries before it
-      for (int b = lane; b < si.nblk; b += 32) {
-        int lo = 0, hi = nnz;  // ranked blocks below b
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if ((rowbuf[w][mid] >> 8) < b) lo = mid + 1;
-          else hi = mid;
-        }
-        ix.row_ptr[key0 + b] = base_e + lo;
+      // row_ptr of every key of the row: entries before it.  Windows of 32
+      // blocks: `cur` ranked blocks lie below the window, and those inside
+      // it (at most 32) are the ranks that follow, so one look at ranks
+      // cur .. cur + 31 gives the window's bit mask.
+      for (int b0 = 0, cur = 0; b0 < si.nblk; b0 += 32) {
+        const int jr = cur + lane;
+        const int bj = jr < nnz ? (rowbuf[w][jr] >> 8) : 0x7fffffff;
+        const bool in = bj < b0 + 32;
+        const unsigned mask = __reduce_or_sync(0xffffffffu, in ? 1u << (bj - b0) : 0u);
+        if (b0 + lane < si.nblk) ix.row_ptr[key0 + b0 + lane] = base_e + cur + __popc(mask & ((1u << lane) - 1));
+        cur += __popc(__ballot_sync(0xffffffffu, in));
       }
       // the row's decode items
       if (nnz > 0) {
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(kPlanThreads, 2) k_plan(PlanArgs a) {
     if (!grid_barrier(bar, flags, nb, epoch)) return;
     tot = ixp::SeqTotals{ia.ix.hdr[kHdrNB], ia.ix.hdr[kHdrBMW], ia.ix.hdr[kHdrKMW]};
   }
-  ixp::phase_token_seq(ia.ix, ia.cu, ia.B, ia.total_q);
+  ixp::phase_token_seq(ia.ix, ia.cu, ia.B, ia.total_q, ia.B <= ixp::kSeqTab ? s_tab[3] : nullptr);
   // (block << 8 | slot) of the ranked rows must fit an int: blocks < 2^23
   if (ia.B <= ixp::kSeqTab && a.P.G <= kDecodeMaxG && ia.cap_len < (1 << 30)) {
     // all-decode batch (every sequence at most one new token): one barrier
