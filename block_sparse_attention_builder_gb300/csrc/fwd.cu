@@ -13,13 +13,15 @@
 //              turns S = q k^T (TMEM) into P = exp(S - m), written back to
 //              TMEM over S as the p v operand, and after O = P v writes
 //              o = O / l and lse per row straight from TMEM.  Row r of a tile is
-//              thread r of its group and TMEM lane r.  For FP8 caches
-//              warpgroup n % 2 widens the staged e4m3 block of the CTA's
-//              n-th item to BF16/FP16 in the stage (exactly), whether or
-//              not it owns a tile of that item.
+//              thread r of its group and TMEM lane r.  For FP8 and NVFP4
+//              caches warpgroup n % 2 widens the CTA's n-th block to
+//              BF16/FP16 in the stage (exactly), whether or not it owns a
+//              tile of that item.
 //   warp 8     producer: decodes items (key -> kv head, sequence, block),
 //              walks the block table and TMA-loads the block's K and V pages
-//              into a double-buffered stage (FP8: into a staging tile).
+//              into a double-buffered stage (FP8: e4m3 rows into the
+//              stage's V half, widened in place; NVFP4: into a staging
+//              tile).
 //   warps 9, 10  MMA issuers, one per softmax group (tcgen05.mma,
 //              cta_group::1, M = N = 128, K = 16 per instruction, FP32
 //              accumulate in TMEM: S and O of each group, 512 columns owned
@@ -206,7 +208,7 @@ template <int kKV>
 __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                                    const CUtensorMap& tmqs, const FwdArgs& a, uint8_t* sm,
                                                    uint32_t tmem) {
-  constexpr bool kPart32 = kKV != dec::kKv16;
+  constexpr bool kPart32 = kind_partials_fp32(kKV);
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + (a.kv_fp8 ? kCtrlFp8 : kCtrlBf16));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Items are claimed dynamically (a global counter), in item order, by the
@@ -317,13 +319,26 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
               tma_load_3d(vdst + h * 16384 + pg * 8192, &tmv, &c.kv_full[st], h * 64, 0, z);
             }
           }
+        } else if (!a.kv_fp4) {
+          // FP8: the e4m3 rows land in the stage's V half (K rows at 0, V
+          // rows at 16 KB, 128 bytes each), where the widening group widens
+          // them in place
+          uint8_t* vhalf = sm + kOffKV + st * kStageBytes + kTileBytes;
+          uint64_t* sf = &c.stg_full[st];
+          mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
+          for (int pg = 0; pg < npg; ++pg) {
+            if (pages[pg] < 0) continue;
+            const int z = pages[pg] * a.Hkv + g;
+            tma_load_3d(vhalf + pg * 8192, &tmk, sf, 0, 0, z);
+            tma_load_3d(vhalf + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
+          }
         } else {
-          // FP8: into the staging tile once the previous block was widened
-          // out of it (stg_empty); the widening group fills the stage
+          // NVFP4: into the staging tile once the previous block was widened
+          // out of it (stg_empty): code rows by TMA, scale rows by bulk copy
+          // (K at 0, V at 16 KB of the staging tile; codes, then scales at
+          // 8 KB); the widening group fills the stage
           ok = mbar_wait(&c.stg_empty, (n & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-          if (ok && a.kv_fp4) {
-            // NVFP4: code rows by TMA, scale rows by bulk copy (K at 0, V
-            // at 16 KB of the staging tile; codes, then scales at 8 KB)
+          if (ok) {
             uint8_t* stg = sm + kOffStg;
             uint64_t* sf = &c.stg_full[st];
             mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 144u);
@@ -336,30 +351,20 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
               bulk_load(stg + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, sf);
               bulk_load(stg + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, sf);
             }
-          } else if (ok) {
-            uint8_t* stg = sm + kOffStg;
-            uint64_t* sf = &c.stg_full[st];
-            mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
-            for (int pg = 0; pg < npg; ++pg) {
-              if (pages[pg] < 0) continue;
-              const int z = pages[pg] * a.Hkv + g;
-              tma_load_3d(stg + pg * 8192, &tmk, sf, 0, 0, z);
-              tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
-            }
           }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;  // FP8 staging gave up: item n issued no loads
+      if (!ok) break;  // NVFP4 staging gave up: item n issued no loads
       it = __shfl_sync(0xffffffffu, next, 0);
     }
     // drain: every load lane 0 issued has landed before the CTA may exit.
     // After the end item (published on stage n % 2) item n - 2 has landed
     // for sure (its stage was released for the end item), and its barrier
-    // has moved on, so only item n - 1 is waited for.  FP8: staging item
+    // has moved on, so only item n - 1 is waited for.  NVFP4: staging item
     // n - 1 needed item n - 2 widened, so only n - 1.
     if (lane == 0) {
-      const int k0 = (ended || a.kv_fp8) ? n - 1 : n - 2;
+      const int k0 = (ended || a.kv_fp4) ? n - 1 : n - 2;
       for (int k = std::max(0, k0); k < n; ++k)
         mbar_drain(a.kv_fp8 ? &c.stg_full[k & 1] : &c.kv_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT,
                    kWaitLimitNs);
@@ -532,29 +537,39 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
     for (; ok; ++n) {
       const int st = n & 1, use = n >> 1;
       if (kKV != dec::kKv16 && st == grp) {
-        // widen the staged e4m3 block (row r of K and V) into the stage;
-        // rows past the valid tokens become zero.  The producer staged this
-        // block only after kv_empty of the stage, so the stage is free.
+        // widen the staged block (row r of K and V) into the stage; rows
+        // past the valid tokens become zero.  The producer loaded this block
+        // only after kv_empty of the stage, so the stage is free.
         ok = warp_all(mbar_wait(&c.stg_full[st], use & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
         const int valid = c.info[st].n > 0 ? c.info[st].valid : 0;  // the end item stages nothing
-        const uint8_t* stg = sm + kOffStg;
         for (int kv = 0; kv < 2 && kKV == dec::kKvFp4; ++kv) {
+          const uint8_t* stg = sm + kOffStg;
           const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
           if (r < valid)
             dec::widen_fp4_row(stg + kv * 16384 + r * 64, stg + kv * 16384 + 8192 + r * 8, dst, r, bf16);
           else
             for (int ch = 0; ch < 16; ++ch) st_shared_v4(dst + swz(r, ch), 0, 0, 0, 0);
         }
+        // FP8, in place: the e4m3 rows sit in the stage's V half (K row r at
+        // r * 128, V row r at 16 KB + r * 128).  K widens into the K half.
+        // Widened V row r covers bytes r * 128 of both 16 KB halves of the V
+        // half: e4m3 K row r (already widened) and e4m3 V row r, which this
+        // thread reads whole before writing, so no thread touches another
+        // thread's row.
         for (int kv = 0; kv < 2 && kKV == dec::kKvFp8; ++kv) {
-          const uint8_t* src = stg + kv * 16384 + r * 128;
+          const uint8_t* src = sm + kOffKV + st * kStageBytes + kTileBytes + kv * 16384 + r * 128;
           const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
+          uint4 raw[8];
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const int c8 = (cc + r) & 7;  // rotate to spread banks
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (r < valid) raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+            raw[cc] = r < valid ? *reinterpret_cast<const uint4*>(src + c8 * 16) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const int c8 = (cc + r) & 7;
+            const uint32_t w4[4] = {raw[cc].x, raw[cc].y, raw[cc].z, raw[cc].w};
             uint32_t o8[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -566,7 +581,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
           }
         }
         fence_proxy_async_smem();
-        if (c.info[st].n > 0) mbar_arrive(&c.stg_empty);
+        if (kKV == dec::kKvFp4 && c.info[st].n > 0) mbar_arrive(&c.stg_empty);
         mbar_arrive(&c.kv_full[st]);
       }
       // every group reads every item's info (the tile count decides the

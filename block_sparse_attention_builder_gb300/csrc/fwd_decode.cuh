@@ -62,7 +62,7 @@ struct Ctrl {
 
 // cache kinds, the forward's template parameter: 16-bit (the q dtype), and
 // the two that are staged and widened, FP8 and NVFP4
-constexpr int kKv16 = 0, kKvFp8 = 1, kKvFp4 = 2;
+constexpr int kKv16 = kKind16, kKvFp8 = kKindFp8, kKvFp4 = kKindFp4;
 
 struct DecArgs {
   const int32_t* block_tables;
@@ -283,7 +283,7 @@ __device__ __forceinline__ void wg_reduce(float* v, float* red) {
 template <int N, int kKV>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                                             const DecArgs& a, uint8_t* sm, uint32_t tmem) {
-  constexpr bool kPart32 = kKV != kKv16;
+  constexpr bool kPart32 = kind_partials_fp32(kKV);
   const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + L.ctrl);
   float* red = reinterpret_cast<float*>(sm + L.red);

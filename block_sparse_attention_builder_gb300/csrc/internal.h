@@ -130,12 +130,21 @@ int64_t max_blocks_per_seq(const mxsa_problem& p);
 // q's 16-bit type by the softmax warps before the MMAs.
 inline bool kv_widened(const mxsa_problem& p) { return p.kv_dtype == MXSA_FP8_E4M3 || p.kv_dtype == MXSA_NVFP4; }
 
-// Element type of the partial output rows.  With 16-bit caches they are
-// stored in the 16-bit q dtype, which halves the forward's stores and the
-// combine's reads; with widened caches they stay FP32 (there the softmax
-// warps also widen the blocks, and the packing on their path costs more
-// than the smaller rows save).
-inline bool partials_fp32(const mxsa_problem& p) { return kv_widened(p); }
+// Cache kinds: the forward kernels' template parameter.
+constexpr int kKind16 = 0, kKindFp8 = 1, kKindFp4 = 2;
+inline int cache_kind(const mxsa_problem& p) {
+  return p.kv_dtype == MXSA_NVFP4 ? kKindFp4 : (p.kv_dtype == MXSA_FP8_E4M3 ? kKindFp8 : kKind16);
+}
+
+// Element type of the partial output rows, per cache kind: the one
+// definition behind the kernels' stores, the workspace size and the
+// combine's reads.  With 16-bit caches they are stored in the 16-bit q
+// dtype, which halves the forward's stores and the combine's reads; with
+// widened caches they stay FP32 (there the softmax warps also widen the
+// blocks, and the packing on their path costs more than the smaller rows
+// save).
+__host__ __device__ constexpr bool kind_partials_fp32(int kind) { return kind != kKind16; }
+inline bool partials_fp32(const mxsa_problem& p) { return kind_partials_fp32(cache_kind(p)); }
 mxsa_status index_layout(const mxsa_problem& p, mxsa_index_layout* L);
 mxsa_status sched_layout(const mxsa_problem& p, mxsa_sched_layout* L);
 IndexPtrs index_ptrs(const mxsa_problem& p, void* ws);
