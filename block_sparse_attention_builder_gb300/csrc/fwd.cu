@@ -544,7 +544,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         if (!ok) break;
         const int valid = c.info[st].n > 0 ? c.info[st].valid : 0;  // the end item stages nothing
         for (int kv = 0; kv < 2 && kKV == dec::kKvFp4; ++kv) {
-          const uint8_t* stg = sm + kOffStg;
+          const uint32_t stg = sbase + kOffStg;
           const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
           if (r < valid)
             dec::widen_fp4_row(stg + kv * 16384 + r * 64, stg + kv * 16384 + 8192 + r * 8, dst, r, bf16);
@@ -558,13 +558,13 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
         // thread reads whole before writing, so no thread touches another
         // thread's row.
         for (int kv = 0; kv < 2 && kKV == dec::kKvFp8; ++kv) {
-          const uint8_t* src = sm + kOffKV + st * kStageBytes + kTileBytes + kv * 16384 + r * 128;
+          const uint32_t src = sbase + kOffKV + st * kStageBytes + kTileBytes + kv * 16384 + r * 128;
           const uint32_t dst = sbase + kOffKV + st * kStageBytes + kv * kTileBytes;
           uint4 raw[8];
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             const int c8 = (cc + r) & 7;  // rotate to spread banks
-            raw[cc] = r < valid ? *reinterpret_cast<const uint4*>(src + c8 * 16) : make_uint4(0, 0, 0, 0);
+            raw[cc] = r < valid ? ld_shared_v4(src + c8 * 16) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {

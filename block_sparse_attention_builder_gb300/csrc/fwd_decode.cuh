@@ -153,14 +153,14 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
 // NVFP4 rows (E2M1 codes, one E4M3 scale per 16 elements) widened to the
 // q dtype: every code times its scale is exact in FP16 (|values| within
 // [2^-10, 2688]) and in BF16.  Row `row` of a [128][128] tile at `dst` (the
-// swz_kv layout) from its 64 code bytes and 8 scale bytes in shared memory.
-__device__ __forceinline__ void widen_fp4_row(const uint8_t* codes, const uint8_t* scales, uint32_t dst, int row,
-                                              int bf16) {
-  const uint2 sc = *reinterpret_cast<const uint2*>(scales);
+// swz_kv layout) from its 64 code bytes and 8 scale bytes in shared memory
+// (shared addresses `codes`, `scales`).
+__device__ __forceinline__ void widen_fp4_row(uint32_t codes, uint32_t scales, uint32_t dst, int row, int bf16) {
+  const uint2 sc = ld_shared_v2(scales);
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
     const int c4 = (cc + row) & 3;  // 32 elements: groups 2 c4 and 2 c4 + 1 (rotated to spread banks)
-    const uint4 raw = *reinterpret_cast<const uint4*>(codes + c4 * 16);
+    const uint4 raw = ld_shared_v4(codes + c4 * 16);
     const uint32_t sw = ((c4 < 2 ? sc.x : sc.y) >> (16 * (c4 & 1))) & 0xFFFFu;
     uint32_t s2[2];
 #pragma unroll
@@ -576,7 +576,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
         if (!ok) break;
         const int valid = c.stg_valid[blk & 1];
         if (k == 0) c.info[st].valid = valid;  // for the softmax warps, published by kv_full
-        const uint8_t* stg = sm + L.stg + (blk & 1) * kKVTile;
+        const uint32_t stg = smem_u32(sm + L.stg + (blk & 1) * kKVTile);
         uint8_t* kst = sm + st * kStage;
         for (int kv = 0; kv < 2; ++kv) {
           const uint32_t dst = smem_u32(kv ? kst + kKVTile : kst);
@@ -585,10 +585,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
           } else if (kKV == kKvFp4) {
             widen_fp4_row(stg + kv * 16384 + k * 64, stg + kv * 16384 + 8192 + k * 8, dst, k, bf16);
           } else {
-            const uint8_t* src = stg + kv * 16384 + k * 128;
+            const uint32_t src = stg + kv * 16384 + k * 128;
             for (int cc = 0; cc < 8; ++cc) {
               const int c8 = (cc + k) & 7;
-              const uint4 raw = *reinterpret_cast<const uint4*>(src + c8 * 16);
+              const uint4 raw = ld_shared_v4(src + c8 * 16);
               const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
               uint32_t o[8];
 #pragma unroll
