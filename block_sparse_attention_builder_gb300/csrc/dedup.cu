@@ -119,6 +119,7 @@ __device__ void phase_owner(const DedupArgs& a) {
   }
 }
 
+constexpr int kFoldHeads = 8;
 __device__ void phase_fold(const DedupArgs& a) {
   const IndexPtrs& ix = a.ia.ix;
   const int NB = ix.hdr[kHdrNB];
@@ -128,12 +129,29 @@ __device__ void phase_fold(const DedupArgs& a) {
     const SeqInfo si = ix.seq[s];
     const int b = (int)r - si.blk_off;
     const int orow = ix.seq[a.d.owner[r]].blk_off + b;
-    for (int g = 0; g < a.ia.Hkv; ++g) {
-      const uint32_t* row = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
-      int c = 0;
-      for (int w = 0; w < si.words; ++w) c += __popc(row[w]);
-      a.d.own_count[(long long)g * NB + r] = c;
-      if (c > 0) atomicAdd(&ix.counts[(long long)g * NB + orow], c);
+    // the heads' rows kFoldHeads at a time: their bitmap reads are issued
+    // together, then the counts are stored
+    for (int g0 = 0; g0 < a.ia.Hkv; g0 += kFoldHeads) {
+      int c[kFoldHeads];
+#pragma unroll
+      for (int u = 0; u < kFoldHeads; ++u) {
+        const int g = g0 + u;
+        c[u] = 0;
+        if (g < a.ia.Hkv) {
+          const uint32_t* row = ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words;
+          if (si.words == 1) c[u] = __popc(row[0]);
+          else
+            for (int w = 0; w < si.words; ++w) c[u] += __popc(row[w]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kFoldHeads; ++u) {
+        const int g = g0 + u;
+        if (g < a.ia.Hkv) {
+          a.d.own_count[(long long)g * NB + r] = c[u];
+          if (c[u] > 0) atomicAdd(&ix.counts[(long long)g * NB + orow], c[u]);
+        }
+      }
     }
     const int m = a.d.gsize[r];
     if (m > 1) {
@@ -226,7 +244,8 @@ __device__ __forceinline__ long long grid_warps() { return ((long long)gridDim.x
 __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tmp) {
   __shared__ int long_key[kScanTile];
   __shared__ int long_base[kScanTile];
-  __shared__ int n_long;
+  __shared__ int n_long, n_grp, grp_at;
+  __shared__ int2 grp_key[kScanTile];
   const IndexPtrs& ix = a.ia.ix;
   const int B = a.ia.B, Hkv = a.ia.Hkv, topk = a.ia.topk;
   const int n_keys = ix.hdr[kHdrKeys];
@@ -259,9 +278,25 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
       c[j] = (k0 + j < hi) ? ix.counts[k0 + j] : 0;
       local += ixp::key_payload(c[j]);
     }
-    if (threadIdx.x == 0) n_long = 0;
+    if (threadIdx.x == 0) {
+      n_long = 0;
+      n_grp = 0;
+    }
     unsigned long long tot;
     unsigned long long run = carry + ixp::block_exclusive_scan(local, tmp, &tot);
+    // the member counts of the thread's keys' blocks, read together
+    int gs[kScanPerThread];
+#pragma unroll
+    for (int j = 0; j < kScanPerThread; ++j) gs[j] = (k0 + j < hi && c[j] > 0) ? a.d.gsize[(k0 + j) % NB] : 0;
+    // keys of single-token sequences (one entry each, token 0's): their
+    // kmap bytes are read together after the loop
+    size_t d_km[kScanPerThread];
+    int d_slot[kScanPerThread], d_base[kScanPerThread];
+    unsigned deferred = 0;
+    // the thread's keys are consecutive: one sequence look-up serves them
+    // while their blocks stay in its range
+    SeqInfo si{};
+    int s_lo = 1, s_hi = 0;
 #pragma unroll
     for (int j = 0; j < kScanPerThread; ++j) {
       const int key = k0 + j;
@@ -272,12 +307,21 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
           const int pos = (int)(run & kLow);
           ix.active[pos] = key;
           const int g = key / NB, r = key - g * NB;
-          const SeqInfo si = ix.seq[ixp::seq_of_block(ix.seq, B, r)];
+          if (r < s_lo || r >= s_hi) {
+            si = ix.seq[ixp::seq_of_block(ix.seq, B, r)];
+            s_lo = si.blk_off;
+            s_hi = si.blk_off + si.nblk;
+          }
           const int b = r - si.blk_off;
           const int valid = si.L - 128 * b;
           ix.active_valid[pos] = valid < 128 ? valid : 128;
-          if (a.d.gsize[r] > 1) {
-            a.d.gkeys[atomicAdd(&ix.hdr[kHdrGroupKeys], 1)] = make_int2(key, base);
+          if (gs[j] > 1) {
+            grp_key[atomicAdd(&n_grp, 1)] = make_int2(key, base);  // queued below, one global add per tile
+          } else if (si.tq == 1) {
+            d_km[j] = (size_t)g * KMW + (size_t)si.km_off + (size_t)b;
+            d_slot[j] = (si.q_begin * Hkv + g) * topk;
+            d_base[j] = base;
+            deferred |= 1u << j;
           } else if (si.words <= 2) {
             ixp::emit_row_serial(ix, ix.bitmap + (size_t)g * BMW + (size_t)si.bm_off + (size_t)b * si.words,
                                  si.words, ix.kmap + (size_t)g * KMW + (size_t)si.km_off + (size_t)b * si.tq,
@@ -291,7 +335,21 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
       }
       run += ixp::key_payload(c[j]);
     }
+    int d_k[kScanPerThread];
+#pragma unroll
+    for (int j = 0; j < kScanPerThread; ++j) d_k[j] = (deferred >> j) & 1u ? ix.kmap[d_km[j]] : 0;
+#pragma unroll
+    for (int j = 0; j < kScanPerThread; ++j) {
+      if ((deferred >> j) & 1u) {
+        const int slot = d_slot[j] + d_k[j];
+        ix.entries[d_base[j]] = slot;
+        ix.slot_entry[slot] = d_base[j];
+      }
+    }
     __syncthreads();
+    if (threadIdx.x == 0 && n_grp > 0) grp_at = atomicAdd(&ix.hdr[kHdrGroupKeys], n_grp);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_grp; i += blockDim.x) a.d.gkeys[grp_at + i] = grp_key[i];
     for (int i = warp; i < n_long; i += n_warps) {
       const int key = long_key[i];
       const int g = key / NB, r = key - g * NB;
@@ -306,7 +364,11 @@ __device__ void phase_scan_emit_dedup(const DedupArgs& a, unsigned long long* tm
   }
 }
 
-__global__ void __launch_bounds__(kIndexThreads) k_index_dedup(DedupArgs a) {
+// Four CTAs per SM (64 registers): the phases are chains of dependent
+// reads, and twice the warps of the other index kernels keep twice the reads
+// in flight.
+constexpr int kDedupCtasPerSm = 3;
+__global__ void __launch_bounds__(kIndexThreads, kDedupCtasPerSm) k_index_dedup(DedupArgs a) {
   __shared__ unsigned long long tmp[3 * 33];
   __shared__ int32_t rowbuf[ixp::kMarkWarps][256];
   const IndexPtrs& ix = a.ia.ix;
@@ -343,7 +405,6 @@ __global__ void __launch_bounds__(kIndexThreads) k_index_dedup(DedupArgs a) {
 
 }  // namespace
 
-int coop_grid(const void* kernel, int threads);
 
 cudaError_t launch_build_index_dedup(const mxsa_problem& p, const int32_t* sel, const int64_t* cu,
                                      const int32_t* lens, const int32_t* block_tables, const IndexPtrs& ix,
@@ -356,7 +417,7 @@ cudaError_t launch_build_index_dedup(const mxsa_problem& p, const int32_t* sel, 
   a.max_pages = p.max_pages_per_seq;
   a.num_pages = p.num_pages;
   a.ps = p.page_size;
-  const int grid = coop_grid(reinterpret_cast<const void*>(k_index_dedup), kIndexThreads);
+  const int grid = coop_grid(reinterpret_cast<const void*>(k_index_dedup), kIndexThreads, kDedupCtasPerSm);
   if (grid <= 0) return cudaErrorNotSupported;
   cudaError_t e = cudaMemsetAsync(ix.hdr, 0, kHdrInts * sizeof(int32_t), st);
   if (e != cudaSuccess) return e;

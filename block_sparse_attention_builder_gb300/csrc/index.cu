@@ -42,7 +42,10 @@ __global__ void __launch_bounds__(kIndexThreads) k_index(IndexArgs a) {
 
 // CTAs of a cooperative launch: at most 2 per SM (all must be resident at
 // once); 0 when the device cannot launch cooperatively.  Cached per device.
-int coop_grid(const void* kernel, int threads) {
+// Co-resident CTAs of a cooperative launch: the SM count times the CTAs an
+// SM holds, at most max_per_sm (more CTAs, more arrivals at each grid
+// barrier).  Cached per device and kernel.
+int coop_grid(const void* kernel, int threads, int max_per_sm) {
   constexpr int kMaxDev = 64, kMaxKernels = 8;
   static std::mutex mu;
   static const void* keys[kMaxDev][kMaxKernels] = {};
@@ -56,7 +59,7 @@ int coop_grid(const void* kernel, int threads) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess) per_sm = 0;
-  int g = (coop && sms > 0 && per_sm > 0) ? sms * (per_sm < 2 ? per_sm : 2) : 0;
+  int g = (coop && sms > 0 && per_sm > 0) ? sms * (per_sm < max_per_sm ? per_sm : max_per_sm) : 0;
   if (g > kMaxCoopCtas) g = kMaxCoopCtas;
   for (int i = 0; i < kMaxKernels; ++i)
     if (!keys[dev][i]) {

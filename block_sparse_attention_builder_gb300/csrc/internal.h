@@ -86,6 +86,8 @@ struct IndexPtrs {
 
 // CTAs of the cooperative launches (index, schedule) never exceed this
 constexpr int kMaxCoopCtas = 1024;
+// CTAs of a cooperative launch of `kernel` (index.cu).
+int coop_grid(const void* kernel, int threads, int max_per_sm = 2);
 
 struct SchedPtrs {
   int32_t* hdr;

@@ -590,7 +590,6 @@ __global__ void __launch_bounds__(kPlanThreads, 2) k_plan(PlanArgs a) {
 
 }  // namespace
 
-int coop_grid(const void* kernel, int threads);
 
 cudaError_t launch_plan(const mxsa_problem& p, const int32_t* sel, const int64_t* cu, const int32_t* lens,
                         const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas, cudaStream_t st) {

@@ -301,7 +301,6 @@ __global__ void __launch_bounds__(kSchThreads) k_schedule(SchedArgs a) {
 
 }  // namespace
 
-int coop_grid(const void* kernel, int threads);
 
 static SchedArgs sched_args(const mxsa_problem& p, const IndexPtrs& ix, const SchedPtrs& sc, int num_ctas) {
   const int G = p.num_q_heads / p.num_kv_heads;
