@@ -51,11 +51,11 @@ struct BlockInfo {
 struct Ctrl {
   uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
-  uint64_t stg_full[2], stg_empty[2], done;  // two staging tiles (widened caches)
+  // widened caches: stg_full[st], the block's narrow rows landed in stage st
+  uint64_t stg_full[kMaxStages], done;
   uint32_t tmem_base;
   int32_t abort_flag;
   BlockInfo info[kMaxStages];
-  int32_t stg_valid[2];  // widened caches: valid keys of the block in each staging tile
   float inv_l[2][16];    // 1 / l per row of an item whose epilogue is pending, by O buffer
   float lse[2][16];      // and its lse per row
 };
@@ -85,16 +85,17 @@ struct DecArgs {
 };
 
 struct Layout {
-  uint32_t q, p, stg, red, ctrl, total;
+  uint32_t q, p, red, ctrl, total;
 };
 
+// Widened caches need no room of their own: a block's narrow rows land in
+// the V half of its own stage and are widened in place.
 template <int N>
-__host__ __device__ constexpr Layout smem_layout(int ns, int fp8) {
+__host__ __device__ constexpr Layout smem_layout(int ns) {
   Layout L{};
   L.q = (uint32_t)ns * kStage;
   L.p = L.q + 2u * N * 256u;
-  L.stg = L.p + 2u * N * 256u;
-  L.red = L.stg + (fp8 ? 2u * kKVTile : 0u);  // widened caches: two staging tiles
+  L.red = L.p + 2u * N * 256u;
   L.ctrl = L.red + 4u * N * 4u;
   L.total = L.ctrl + (uint32_t)sizeof(Ctrl);
   return L;
@@ -102,7 +103,8 @@ __host__ __device__ constexpr Layout smem_layout(int ns, int fp8) {
 
 template <int N>
 constexpr int stages_for(int fp8) {
-  return fp8 ? 2 : (N <= 32 ? 3 : 2);
+  (void)fp8;  // widened caches widen in their stage: the same ring
+  return N <= 32 ? 3 : 2;
 }
 
 // One item's look-ups as the producer warp holds them: uniform fields, and
@@ -152,45 +154,65 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint16_t v, int bf16) {
 
 // NVFP4 rows (E2M1 codes, one E4M3 scale per 16 elements) widened to the
 // q dtype: every code times its scale is exact in FP16 (|values| within
-// [2^-10, 2688]) and in BF16.  Row `row` of a [128][128] tile at `dst` (the
-// swz_kv layout) from its 64 code bytes and 8 scale bytes in shared memory
-// (shared addresses `codes`, `scales`).
+// [2^-10, 2688]) and in BF16.  One 32-element chunk c4 of row `row` of a
+// [128][128] tile at `dst` (the swz_kv layout) from its 16 code bytes and
+// the row's 8 scale bytes.
+__device__ __forceinline__ void widen_fp4_chunk(uint4 raw, uint2 sc, uint32_t dst, int row, int c4, int bf16) {
+  const uint32_t sw = ((c4 < 2 ? sc.x : sc.y) >> (16 * (c4 & 1))) & 0xFFFFu;
+  uint32_t s2[2];
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi) {
+    const uint16_t b = (uint16_t)((sw >> (8 * gi)) & 0xFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2[gi]) : "h"((uint16_t)(b | (b << 8))));
+  }
+  const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(words[w]));
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[i]), *reinterpret_cast<const __half2*>(&s2[w >> 1]));
+      if (bf16) {
+        const float2 f = __half22float2(v);
+        o[i] = pack2(f.x, f.y, 1);
+      } else {
+        o[i] = *reinterpret_cast<uint32_t*>(&v);
+      }
+    }
+    st_shared_v4(dst + swz_kv(row, 4 * c4 + w), o[0], o[1], o[2], o[3]);
+  }
+}
+
+// A whole row from its 64 code bytes and 8 scale bytes in shared memory
+// (shared addresses `codes`, `scales`), the chunks in an order rotated by
+// the row to spread the code reads over the banks.
 __device__ __forceinline__ void widen_fp4_row(uint32_t codes, uint32_t scales, uint32_t dst, int row, int bf16) {
   const uint2 sc = ld_shared_v2(scales);
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
-    const int c4 = (cc + row) & 3;  // 32 elements: groups 2 c4 and 2 c4 + 1 (rotated to spread banks)
-    const uint4 raw = ld_shared_v4(codes + c4 * 16);
-    const uint32_t sw = ((c4 < 2 ? sc.x : sc.y) >> (16 * (c4 & 1))) & 0xFFFFu;
-    uint32_t s2[2];
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const uint16_t b = (uint16_t)((sw >> (8 * gi)) & 0xFFu);
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2[gi]) : "h"((uint16_t)(b | (b << 8))));
-    }
-    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t h[4];
-      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-          "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-          "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-          : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-          : "r"(words[w]));
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h[i]), *reinterpret_cast<const __half2*>(&s2[w >> 1]));
-        if (bf16) {
-          const float2 f = __half22float2(v);
-          o[i] = pack2(f.x, f.y, 1);
-        } else {
-          o[i] = *reinterpret_cast<uint32_t*>(&v);
-        }
-      }
-      st_shared_v4(dst + swz_kv(row, 4 * c4 + w), o[0], o[1], o[2], o[3]);
-    }
+    const int c4 = (cc + row) & 3;
+    widen_fp4_chunk(ld_shared_v4(codes + c4 * 16), sc, dst, row, c4, bf16);
   }
+}
+
+// named barrier 2 over the 128 widening threads (warps 6-9), and the same
+// barrier as an and-vote
+__device__ __forceinline__ void widen_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ bool widen_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
 }
 
 // named barrier 1 over the 128 softmax threads
@@ -284,7 +306,7 @@ template <int N, int kKV>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                                             const DecArgs& a, uint8_t* sm, uint32_t tmem) {
   constexpr bool kPart32 = kind_partials_fp32(kKV);
-  const Layout L = smem_layout<N>(a.ns, a.kv_fp8);
+  const Layout L = smem_layout<N>(a.ns);
   Ctrl& c = *reinterpret_cast<Ctrl*>(sm + L.ctrl);
   float* red = reinterpret_cast<float*>(sm + L.red);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -306,10 +328,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       mbar_init(&c.o_full[i], 1);
       mbar_init(&c.o_empty[i], 128);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&c.stg_full[i], 1);
-      mbar_init(&c.stg_empty[i], 128);
-    }
+    for (int i = 0; i < ns; ++i) mbar_init(&c.stg_full[i], 1);
     mbar_init(&c.done, 1);
     c.abort_flag = 0;
     fence_mbar_init();
@@ -382,29 +401,22 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       BlockDesc nxt = cur;
       for (int j = 0; j < cur.nk && ok; ++j, ++blk) {
         const int st = blk % ns, us = blk / ns;
-        // 16-bit caches: block blk lands in stage st once the stage's
-        // previous block was consumed.  Widened caches: it stages into
-        // tile blk % 2 once block blk - 2 was widened out of it (the
-        // widening warps wait for the stage), so the copies run ahead of
-        // the MMAs.
-        if (!a.kv_fp8)
-          ok = __all_sync(0xffffffffu, mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags,
-                                                 MXSA_FLAG_TIMEOUT, kWaitLimitNs));
-        else
-          ok = __all_sync(0xffffffffu, mbar_wait(&c.stg_empty[blk & 1], ((blk >> 1) & 1) ^ 1, abort_flag, a.flags,
-                                                 MXSA_FLAG_TIMEOUT, kWaitLimitNs));
+        // block blk lands in stage st once the stage's previous block was
+        // consumed (its p v); widened caches land their narrow rows in the
+        // stage's V half, where the widening warps widen them in place
+        ok = __all_sync(0xffffffffu, mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags,
+                                               MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
         const int valid = __shfl_sync(0xffffffffu, cur.valid, j);
         const int pg0 = __shfl_sync(0xffffffffu, cur.page0, j);
         const int pg1 = __shfl_sync(0xffffffffu, cur.page1, j);
         if (lane == 0) {
-          if (!a.kv_fp8) c.info[st].valid = valid;
-          else c.stg_valid[blk & 1] = valid;
+          c.info[st].valid = valid;  // read after kv_full (softmax) or stg_full (widening)
           const int pages[2] = {pg0, pg1};
           const int present = (pg0 >= 0) + (pg1 >= 0);
+          uint8_t* kdst = sm + st * kStage;
+          uint8_t* vdst = kdst + kKVTile;
           if (!a.kv_fp8) {
-            uint8_t* kdst = sm + st * kStage;
-            uint8_t* vdst = kdst + kKVTile;
             mbar_arrive_expect_tx(&c.kv_full[st], (uint32_t)present * (uint32_t)ps * 512u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
@@ -415,29 +427,28 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
               }
             }
           } else if (a.kv_fp4) {
-            // NVFP4: code rows by TMA, scale rows by bulk copy, K at 0 and
-            // V at 16 KB of the staging tile (codes, then scales at 8 KB)
-            uint8_t* stg = sm + L.stg + (blk & 1) * kKVTile;
-            uint64_t* sf = &c.stg_full[blk & 1];
+            // NVFP4: code rows by TMA, scale rows by bulk copy; K at 0 and
+            // V at 16 KB of the V half (codes, then scales at 8 KB)
+            uint64_t* sf = &c.stg_full[st];
             mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 144u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
               const int z = pages[pg] * a.Hkv + cur.g;
               const size_t so = (size_t)z * ps * 72 + (size_t)ps * 64;
-              tma_load_3d(stg + pg * ps * 64, &tmk, sf, 0, 0, z);
-              tma_load_3d(stg + 16384 + pg * ps * 64, &tmv, sf, 0, 0, z);
-              bulk_load(stg + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, sf);
-              bulk_load(stg + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, sf);
+              tma_load_3d(vdst + pg * ps * 64, &tmk, sf, 0, 0, z);
+              tma_load_3d(vdst + 16384 + pg * ps * 64, &tmv, sf, 0, 0, z);
+              bulk_load(vdst + 8192 + pg * ps * 8, a.kbase + so, (uint32_t)ps * 8u, sf);
+              bulk_load(vdst + 16384 + 8192 + pg * ps * 8, a.vbase + so, (uint32_t)ps * 8u, sf);
             }
           } else {
-            uint8_t* stg = sm + L.stg + (blk & 1) * kKVTile;
-            uint64_t* sf = &c.stg_full[blk & 1];
+            // FP8: e4m3 rows of 128 bytes, K at 0 and V at 16 KB of the V half
+            uint64_t* sf = &c.stg_full[st];
             mbar_arrive_expect_tx(sf, (uint32_t)present * (uint32_t)ps * 256u);
             for (int pg = 0; pg < npg; ++pg) {
               if (pages[pg] < 0) continue;
               const int z = pages[pg] * a.Hkv + cur.g;
-              tma_load_3d(stg + pg * 8192, &tmk, sf, 0, 0, z);
-              tma_load_3d(stg + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
+              tma_load_3d(vdst + pg * 8192, &tmk, sf, 0, 0, z);
+              tma_load_3d(vdst + 16384 + pg * 8192, &tmv, sf, 0, 0, z);
             }
           }
         }
@@ -454,15 +465,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
     }
     if (lane == 0) {
       // drain the loads in flight before the CTA may exit
-      for (int k = std::max(0, blk - ns); k < blk; ++k) {
-        if (a.kv_fp8) {
-          // staging tile k % 2 was refilled only after block k - 2 was
-          // widened: the last two blocks' copies may still be in flight
-          if (k >= blk - 2) mbar_drain(&c.stg_full[k & 1], (k >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        } else {
-          mbar_drain(&c.kv_full[k % ns], (k / ns) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        }
-      }
+      for (int k = std::max(0, blk - ns); k < blk; ++k)
+        mbar_drain(a.kv_fp8 ? &c.stg_full[k % ns] : &c.kv_full[k % ns], (k / ns) & 1, a.flags, MXSA_FLAG_TIMEOUT,
+                   kWaitLimitNs);
       if (n_it > 0)
         mbar_drain(&c.q_full[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
@@ -559,9 +564,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
     }
   } else if (kKV != kKv16 && warp >= 6 && warp < 10) {
     // ------------------------------------------------------ widening warps
-    // Widened caches (FP8, NVFP4): thread k turns row k of each staged
-    // block's K and V into the q dtype in the block's stage, zero past the
-    // valid keys, while the softmax warps work on the previous block.
+    // Widened caches (FP8, NVFP4): thread k turns row k of each block's K
+    // and V into the q dtype, zero past the valid keys, while the softmax
+    // warps work on the previous block.  The narrow rows sit in the V half
+    // of the block's own stage (K rows at 0, V rows at 16 KB).  K widens
+    // into the K half.  V widens over itself: widened V row k covers bytes
+    // k * 128 of both 16 KB halves of the V half.  For FP8 those are e4m3 K
+    // row k (already widened) and e4m3 V row k (read whole first), so each
+    // thread only touches its own row.  NVFP4 rows are 64 code bytes and 8
+    // scale bytes, so a widened row covers other rows' codes and scales:
+    // every thread reads its V row first, and the 128 threads meet at a
+    // named barrier before any V byte is written.
     const int k = tid - 192;
     const int bf16 = a.ab_bf16;
     int blk = 0;
@@ -570,26 +583,45 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       const int nk = a.items[it].w;
       for (int j = 0; j < nk; ++j, ++blk) {
         const int st = blk % ns, us = blk / ns;
-        ok = mbar_wait(&c.stg_full[blk & 1], (blk >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
-        // the stage's previous block (blk - ns) was consumed by its p v
-        ok = ok && mbar_wait(&c.kv_empty[st], (us & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+        // the four warps agree on the outcome, so that all 128 threads or
+        // none reach the NVFP4 barrier below
+        ok = widen_all(mbar_wait(&c.stg_full[st], us & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs));
         if (!ok) break;
-        const int valid = c.stg_valid[blk & 1];
-        if (k == 0) c.info[st].valid = valid;  // for the softmax warps, published by kv_full
-        const uint32_t stg = smem_u32(sm + L.stg + (blk & 1) * kKVTile);
-        uint8_t* kst = sm + st * kStage;
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t dst = smem_u32(kv ? kst + kKVTile : kst);
-          if (k >= valid) {
-            for (int ch = 0; ch < 16; ++ch) st_shared_v4(dst + swz_kv(k, ch), 0, 0, 0, 0);
-          } else if (kKV == kKvFp4) {
-            widen_fp4_row(stg + kv * 16384 + k * 64, stg + kv * 16384 + 8192 + k * 8, dst, k, bf16);
+        const int valid = c.info[st].valid;
+        const uint32_t kst = sbase + st * kStage, vst = kst + kKVTile;
+        if (kKV == kKvFp4) {
+          if (k < valid) {
+            widen_fp4_row(vst + k * 64, vst + 8192 + k * 8, kst, k, bf16);
           } else {
-            const uint32_t src = stg + kv * 16384 + k * 128;
+            for (int ch = 0; ch < 16; ++ch) st_shared_v4(kst + swz_kv(k, ch), 0, 0, 0, 0);
+          }
+          uint4 vc[4];
+          uint2 vs = make_uint2(0u, 0u);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c4 = (cc + k) & 3;  // rotated to spread banks
+            vc[cc] = k < valid ? ld_shared_v4(vst + 16384 + k * 64 + c4 * 16) : make_uint4(0, 0, 0, 0);
+          }
+          if (k < valid) vs = ld_shared_v2(vst + 16384 + 8192 + k * 8);
+          widen_sync();  // every V row read before any is written
+          if (k < valid) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) widen_fp4_chunk(vc[cc], vs, vst, k, (cc + k) & 3, bf16);
+          } else {
+            for (int ch = 0; ch < 16; ++ch) st_shared_v4(vst + swz_kv(k, ch), 0, 0, 0, 0);
+          }
+        } else {
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t src = vst + kv * 16384 + k * 128;
+            const uint32_t dst = kv ? vst : kst;
+            uint4 raw[8];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)  // rotated to spread banks
+              raw[cc] = k < valid ? ld_shared_v4(src + ((cc + k) & 7) * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
               const int c8 = (cc + k) & 7;
-              const uint4 raw = ld_shared_v4(src + c8 * 16);
-              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+              const uint32_t w[4] = {raw[cc].x, raw[cc].y, raw[cc].z, raw[cc].w};
               uint32_t o[8];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -602,7 +634,6 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&c.stg_empty[blk & 1]);
         mbar_arrive(&c.kv_full[st]);
       }
     }
@@ -799,10 +830,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       mbar_inval(&c.o_full[i]);
       mbar_inval(&c.o_empty[i]);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_inval(&c.stg_full[i]);
-      mbar_inval(&c.stg_empty[i]);
-    }
+    for (int i = 0; i < ns; ++i) mbar_inval(&c.stg_full[i]);
     mbar_inval(&c.done);
   }
   __syncthreads();
@@ -839,7 +867,7 @@ inline bool make_q_map(CUtensorMap* m, const void* q, const mxsa_problem& p, int
 // phase needs for the cache dtype.
 inline size_t smem_bytes(bool fp8) {
   constexpr int N = 16;
-  return smem_layout<N>(stages_for<N>(fp8 ? 1 : 0), fp8 ? 1 : 0).total + 1024;
+  return smem_layout<N>(stages_for<N>(fp8 ? 1 : 0)).total + 1024;
 }
 
 // Fills the decode phase's arguments and its q tensor map; false when the

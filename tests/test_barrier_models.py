@@ -8,13 +8,16 @@ mbarrier keeps the hardware's phase/parity rule (a parity wait is satisfied
 once the barrier's phase parity differs from the one asked for).  A run
 checks that no schedule deadlocks and that the facts the kernels rely on
 hold (a stage is refilled only after every reader released it, O is read
-before the next p v overwrites it, epilogues run in tile order, the FP8
-staging tile is widened before it is refilled).  A timeout on the GPU would
-only show such a race as a flag; the model finds it without one.
+before the next p v overwrites it, epilogues run in tile order, narrow rows
+are widened from the copy that landed for that block, in place in its
+stage or from the NVFP4 staging tile before it is refilled).  A timeout on
+the GPU would only show such a race as a flag; the model finds it without
+one.
 
 Covered: k_fwd's decode phase (a 3-stage K/V ring, an MMA issuer polling
-two cursors, BF16 and FP8 staging), its KV-stationary phase (BF16 and FP8)
-and k_dense.
+two cursors, 16-bit caches and widened ones, whose narrow rows land in the
+stage and are widened in place), its KV-stationary phase (16-bit, FP8
+widened in place, NVFP4 through a staging tile) and k_dense.
 The dense model without the wait that an empty tile makes before it
 publishes O reproduces the race that wait removes (o_full completing twice
 ahead of the softmax group's parity wait).
@@ -37,8 +40,12 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def run_fwd_kv_stationary(items, seed, fp8=False):
-    """items: list of tile counts (1..4) of the items this CTA claims."""
+def run_fwd_kv_stationary(items, seed, kind="16"):
+    """items: list of tile counts (1..4) of the items this CTA claims.
+    kind: "16" (16-bit caches), "fp8" (e4m3 rows land in the item's own
+    stage and are widened in place) or "fp4" (NVFP4 rows land in one
+    staging tile, widened into the stage)."""
+    widened_kind = kind != "16"
     rnd = random.Random(seed)
     B = {}
     def bar(n, c=1): B[n] = Bar(n, c)
@@ -51,6 +58,7 @@ def run_fwd_kv_stationary(items, seed, fp8=False):
     widened = {}
     info = [None, None]
     stage_item = [None, None]
+    stage_raw = [None, None]        # the item whose narrow rows landed in the stage (fp8)
     stage_readers = {}
     pending = {}
     def later(src, cb): pending.setdefault(src, []).append(cb)
@@ -71,11 +79,16 @@ def run_fwd_kv_stationary(items, seed, fp8=False):
                 assert stage_readers.get(n - 2, 0) == 4, ("stage reused early", n)
             if it >= len(items):
                 info[st] = (0, n)
-                B[f"stg_full{st}" if fp8 else f"kv_full{st}"].arrive()
+                B[f"stg_full{st}" if widened_kind else f"kv_full{st}"].arrive()
                 return
             nxt = claim[0]; claim[0] += 1
             info[st] = (items[it], n)
-            if fp8:
+            if kind == "fp8":
+                def raw_land(st=st, n=n):
+                    stage_raw[st] = n
+                    B[f"stg_full{st}"].arrive()
+                later(f"tma_kv{st}", raw_land)
+            elif kind == "fp4":
                 yield ("wait", B["stg_empty"], (n & 1) ^ 1)
                 assert n == 0 or widened.get(n - 1), ("staging overwritten before widening", n)
                 def stg_land(st=st, n=n):
@@ -147,15 +160,19 @@ def run_fwd_kv_stationary(items, seed, fp8=False):
             n_epi += 1
         while True:
             st, use = n & 1, n >> 1
-            if fp8 and st == g:
+            if widened_kind and st == g:
                 yield ("wait", B[f"stg_full{st}"], use & 1)
                 nt0, item0 = info[st]
                 if nt0 > 0:
-                    assert staging[0] == item0, ("widening the wrong staged block", staging[0], item0)
+                    if kind == "fp8":
+                        assert stage_raw[st] == item0, ("widening rows of another item", stage_raw[st], item0)
+                    else:
+                        assert staging[0] == item0, ("widening the wrong staged block", staging[0], item0)
                     assert item0 < 2 or stage_readers.get(item0 - 2, 0) == 4, ("stage not free for widening", item0)
                     stage_item[st] = item0
                     widened[item0] = True
-                    B["stg_empty"].arrive()
+                    if kind == "fp4":
+                        B["stg_empty"].arrive()
                 B[f"kv_full{st}"].arrive()
             yield ("wait", B[f"kv_full{st}"], use & 1)
             nt, item_n = info[st]
@@ -314,10 +331,10 @@ def run_dense(tiles, seed, fix=True):
 
 
 def run_decode(items, seed, fp8=False):
-    """items: key counts (>= 1) of the CTA's decode items, in order.  K/V
-    stages: 3 for 16-bit caches, 2 for widened ones (FP8, NVFP4), whose
-    blocks land in two staging tiles in turn."""
-    NS = 2 if fp8 else 3
+    """items: key counts (>= 1) of the CTA's decode items, in order.  Three
+    K/V stages; widened caches (FP8, NVFP4) land a block's narrow rows in
+    its own stage, where the widening warps widen them in place."""
+    NS = 3
     rnd = random.Random(seed)
     B = {}
     def bar(n, c=1): B[n] = Bar(n, c)
@@ -326,12 +343,12 @@ def run_decode(items, seed, fp8=False):
     for i in range(2):
         for nm in ("q_full", "q_empty", "s_full", "p_full", "p_empty", "o_full", "o_empty"):
             bar(f"{nm}{i}")
-    for i in range(2):
-        bar(f"stg_full{i}"); bar(f"stg_empty{i}")
+    for i in range(NS):
+        bar(f"stg_full{i}")
     pending = {}
     def later(src, cb): pending.setdefault(src, []).append(cb)
     stage = {}     # st -> block (landed / widened)
-    staging = [None, None]
+    stage_raw = {}  # st -> block whose narrow rows landed there
     Sbuf = {}      # sb -> ('S'|'read', blk)
     Pbuf = {}      # sb -> ('P'|'used', blk)
     Obuf = {}      # ib -> ('acc'|'done'|'read', item)
@@ -345,16 +362,14 @@ def run_decode(items, seed, fp8=False):
             later(f"tq{ib}", lambda ib=ib: B[f"q_full{ib}"].arrive())
             for j in range(nk):
                 st, us = blk % NS, blk // NS
-                if not fp8:  # widened caches: the widening warps wait for the stage
-                    yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
-                    assert blk < NS or pv_done[0] >= blk - NS, ("stage refilled before its p v", blk)
+                yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
+                assert blk < NS or pv_done[0] >= blk - NS, ("stage refilled before its p v", blk)
                 if fp8:
-                    yield ("wait", B[f"stg_empty{blk & 1}"], ((blk >> 1) & 1) ^ 1)
-                    assert staging[blk & 1] in (None, ("widened", blk - 2)), ("staging refilled early", blk)
-                    def sl(blk=blk):
-                        staging[blk & 1] = ("landed", blk)
-                        B[f"stg_full{blk & 1}"].arrive()
-                    later(f"tstg{blk & 1}", sl)
+                    assert blk < NS or stage.get(st) == blk - NS, ("narrow rows over an unwidened block", blk)
+                    def sl(st=st, blk=blk):
+                        stage_raw[st] = blk
+                        B[f"stg_full{st}"].arrive()
+                    later(f"tkv{st}", sl)
                 else:
                     def land(st=st, blk=blk):
                         stage[st] = blk
@@ -438,16 +453,14 @@ def run_decode(items, seed, fp8=False):
                 Obuf[qb] = ("read", q)
                 B[f"o_empty{qb}"].arrive()
     def widen():
-        # widened caches: warps 6-9 turn each staged block into its stage
+        # widened caches: warps 6-9 widen each block's narrow rows in place
         for blk in range(nblk):
             st, us = blk % NS, blk // NS
-            yield ("wait", B[f"stg_full{blk & 1}"], (blk >> 1) & 1)
-            yield ("wait", B[f"kv_empty{st}"], (us & 1) ^ 1)
-            assert staging[blk & 1] == ("landed", blk)
+            yield ("wait", B[f"stg_full{st}"], us & 1)
+            assert stage_raw.get(st) == blk, ("widening rows of another block", stage_raw.get(st), blk)
             assert blk < NS or pv_done[0] >= blk - NS, ("widening into a busy stage", blk)
             stage[st] = blk
-            staging[blk & 1] = ("widened", blk)
-            B[f"stg_empty{blk & 1}"].arrive(); B[f"kv_full{st}"].arrive()
+            B[f"kv_full{st}"].arrive()
             yield None
     agents = {"p": producer(), "m": issuer(), "s": softmax()}
     if fp8:
@@ -474,12 +487,12 @@ def run_decode(items, seed, fp8=False):
         if not prog and not any(pending.values()):
             raise AssertionError(f"deadlock {[(k, state[k][0], getattr(state[k][1], 'name', '')) for k in agents if state[k]]}")
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_fwd_kv_stationary_protocol(fp8):
-    rnd = random.Random(11 + fp8)
+@pytest.mark.parametrize("kind", ["16", "fp8", "fp4"])
+def test_fwd_kv_stationary_protocol(kind):
+    rnd = random.Random(11 + ["16", "fp8", "fp4"].index(kind))
     for trial in range(400):
         items = [rnd.randint(1, 4) for _ in range(rnd.randint(0, 7))]
-        run_fwd_kv_stationary(items, trial, fp8)
+        run_fwd_kv_stationary(items, trial, kind)
 
 
 @pytest.mark.parametrize("fp8", [False, True])
