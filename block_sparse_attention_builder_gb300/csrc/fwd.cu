@@ -759,7 +759,7 @@ __device__ __forceinline__ void kv_stationary_body(const CUtensorMap& tmk, const
   tc_fence_after();
 }
 
-// The forward: each CTA runs its decode items (decode_body, warps 0-5),
+// The forward: each CTA runs its decode items (decode_body),
 // then its KV-stationary items (all warps), in one launch.  TMEM (512
 // columns) is allocated once for both phases.
 template <int kKV>

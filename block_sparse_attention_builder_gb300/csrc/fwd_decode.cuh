@@ -18,10 +18,11 @@
 // The decode phase of the forward kernel (fwd.cu), run by each CTA on its
 // decode items before its KV-stationary items: warps 0-3 softmax/epilogue,
 // warp 4 TMA producer (q rows of the item; K and V pages of each block into
-// a 2-3 stage ring, or for FP8 / NVFP4 caches into two staging tiles), warp
-// 5 MMA issuer, warps 6-9 widening (FP8 / NVFP4: each staged block into the
-// q dtype in its stage); the kernel's other warps idle through this phase.  TMEM columns [0, 64) of the CTA's
-// allocation hold S^T and O^T.
+// a 3-stage ring; FP8 / NVFP4 rows into the V half of the block's stage),
+// warp 5 issues the S^T MMAs and warp 10 the O^T MMAs, warps 6-9 widen (FP8
+// / NVFP4: each block's narrow rows into the q dtype, in place); the
+// kernel's other warps idle through this phase.  TMEM columns [0, 64) of
+// the CTA's allocation hold S^T and O^T.
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -329,7 +330,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       mbar_init(&c.o_empty[i], 128);
     }
     for (int i = 0; i < ns; ++i) mbar_init(&c.stg_full[i], 1);
-    mbar_init(&c.done, 1);
+    mbar_init(&c.done, 2);  // one commit from each MMA issuer
     c.abort_flag = 0;
     fence_mbar_init();
   }
@@ -471,55 +472,52 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
       if (n_it > 0)
         mbar_drain(&c.q_full[(n_it - 1) & 1], ((n_it - 1) >> 1) & 1, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }
-  } else if (warp == 5) {
-    // ----------------------------------------------------------- MMA issuer
+  } else if (warp == 5 || warp == 10) {
+    // ---------------------------------------------------------- MMA issuers
+    // Warp 5 issues S^T = K Q^T of each block, warp 10 O^T += V^T P^T (one
+    // thread each, blocking waits on exactly the barriers it needs): issuing
+    // one block's eight MMAs takes hundreds of cycles, and with two issuers
+    // neither waits behind the other's issue.  S^T of block b needs its K,
+    // at an item start its q, and the S buffer it reuses read out (P of
+    // block b - 2 written).  P V of block b needs its P, and at an item
+    // start the O buffer it reuses read out; it never waits for the next
+    // block's load, so a stage is released as soon as its block is consumed.
     if (lane == 0) {
-      const uint32_t id_s = idesc_f16(128, N, (uint32_t)a.ab_bf16, 0, 0);
-      const uint32_t id_o = idesc_f16(128, N, (uint32_t)a.ab_bf16, 1, 0);
-      // Two cursors over the CTA's blocks, each issued as soon as its inputs
-      // are there: S^T of block bs (its K landed; at an item start its q;
-      // the S buffer it reuses was read, i.e. bs <= bp + 1) and O^T += V^T P^T
-      // of block bp (its P written; at an item start the O buffer it reuses
-      // was read out).  P V of a block never waits for the next block's load,
-      // so a stage is released as soon as its block is consumed.
-      int its = it_begin, js = 0, ns_it = 0, nks = a.items[it_begin].w, bs = 0;
-      int itp = it_begin, jp = 0, np_it = 0, nkp = nks, bp = 0;
-      // the wait limit runs from the first pass that found nothing to issue;
-      // the timer is read once every 64 such passes (a read costs more than
-      // a pass, and it would delay the issuer's reaction to the barriers)
-      uint64_t t_idle = 0;
-      uint32_t idle = 0;
-      while (itp < it_end) {
-        bool progressed = false;
-        if (its < it_end && bs <= bp + 1) {
-          const int ib = ns_it & 1, st = bs % ns;
-          if ((js > 0 || mbar_test(&c.q_full[ib], (ns_it >> 1) & 1)) && mbar_test(&c.kv_full[st], (bs / ns) & 1)) {
+      const bool qk = warp == 5;
+      const uint32_t id = idesc_f16(128, N, (uint32_t)a.ab_bf16, qk ? 0 : 1, 0);
+      int b = 0, n_it = 0;
+      bool ok = true;
+      for (int it = it_begin; it < it_end && ok; ++it, ++n_it) {
+        const int nk = a.items[it].w;
+        const int ib = n_it & 1;
+        for (int j = 0; j < nk; ++j, ++b) {
+          const int st = b % ns, sb = b & 1;
+          if (qk) {
+            if (j == 0)
+              ok = mbar_wait(&c.q_full[ib], (n_it >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            ok = ok && mbar_wait(&c.kv_full[st], (b / ns) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            ok = ok && (b < 2 || mbar_wait(&c.p_full[sb], ((b - 2) >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                           kWaitLimitNs));
+            if (!ok) break;
             tc_fence_after();
             const uint32_t k_s = sbase + st * kStage;
             const uint32_t q_s = sbase + L.q + ib * (N * 256);
-            const uint32_t tS = tmem + (bs & 1) * N;
+            const uint32_t tS = tmem + sb * N;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off_k = (ks >> 2) * 16384u + (ks & 3) * 32u;
               const uint32_t off_q = (ks >> 2) * (uint32_t)(N * 128) + (ks & 3) * 32u;
-              mma_f16_ss(tS, smem_desc_sw128(k_s + off_k, 0, 1024), smem_desc_sw128(q_s + off_q, 0, 1024), id_s,
+              mma_f16_ss(tS, smem_desc_sw128(k_s + off_k, 0, 1024), smem_desc_sw128(q_s + off_q, 0, 1024), id,
                          ks > 0);
             }
-            mma_commit(&c.s_full[bs & 1]);
-            ++bs;
-            if (++js == nks) {
-              mma_commit(&c.q_empty[ib]);
-              js = 0;
-              ++ns_it;
-              if (++its < it_end) nks = a.items[its].w;
-            }
-            progressed = true;
-          }
-        }
-        if (bp < bs) {
-          const int ib = np_it & 1, st = bp % ns, sb = bp & 1;
-          if (mbar_test(&c.p_full[sb], (bp >> 1) & 1) &&
-              (jp > 0 || mbar_test(&c.o_empty[ib], ((np_it >> 1) & 1) ^ 1))) {
+            mma_commit(&c.s_full[sb]);
+            if (j == nk - 1) mma_commit(&c.q_empty[ib]);
+          } else {
+            ok = mbar_wait(&c.p_full[sb], (b >> 1) & 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
+            if (j == 0)
+              ok = ok && mbar_wait(&c.o_empty[ib], ((n_it >> 1) & 1) ^ 1, abort_flag, a.flags, MXSA_FLAG_TIMEOUT,
+                                   kWaitLimitNs);
+            if (!ok) break;
             tc_fence_after();
             const uint32_t v_s = sbase + st * kStage + kKVTile;
             const uint32_t p_s = sbase + L.p + sb * (N * 256);
@@ -528,37 +526,16 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmk, const CUtens
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off_p = (ks >> 2) * (uint32_t)(N * 128) + (ks & 3) * 32u;
               mma_f16_ss(tO, smem_desc_sw128(v_s + ks * 2048u, 16384, 1024), smem_desc_sw128(p_s + off_p, 0, 1024),
-                         id_o, (jp > 0 || ks > 0) ? 1u : 0u);
+                         id, (j > 0 || ks > 0) ? 1u : 0u);
             }
             mma_commit(&c.p_empty[sb]);
             mma_commit(&c.kv_empty[st]);
-            ++bp;
-            if (++jp == nkp) {
-              mma_commit(&c.o_full[ib]);
-              jp = 0;
-              ++np_it;
-              if (++itp < it_end) nkp = a.items[itp].w;
-            }
-            progressed = true;
+            if (j == nk - 1) mma_commit(&c.o_full[ib]);
           }
-        }
-        if (progressed) {
-          idle = 0;
-        } else {
-          if (*abort_flag) break;
-          if ((idle & 63u) == 0u) {
-            const uint64_t now = globaltimer_ns();
-            if (idle == 0u) {
-              t_idle = now;
-            } else if (now - t_idle > kWaitLimitNs) {
-              *abort_flag = 1;
-              atomicOr(a.flags, MXSA_FLAG_TIMEOUT);
-              break;
-            }
-          }
-          ++idle;
         }
       }
+      // both issuers' MMAs complete before the CTA moves on (c.done takes
+      // one commit from each)
       mma_commit(&c.done);
       mbar_drain(&c.done, 0, a.flags, MXSA_FLAG_TIMEOUT, kWaitLimitNs);
     }

@@ -14,8 +14,8 @@ stage or from the NVFP4 staging tile before it is refilled).  A timeout on
 the GPU would only show such a race as a flag; the model finds it without
 one.
 
-Covered: k_fwd's decode phase (a 3-stage K/V ring, an MMA issuer polling
-two cursors, 16-bit caches and widened ones, whose narrow rows land in the
+Covered: k_fwd's decode phase (a 3-stage K/V ring, two MMA issuers, one
+for S^T and one for O^T, 16-bit caches and widened ones, whose narrow rows land in the
 stage and are widened in place), its KV-stationary phase (16-bit, FP8
 widened in place, NVFP4 through a staging tile) and k_dense.
 The dense model without the wait that an empty tile makes before it
@@ -376,52 +376,57 @@ def run_decode(items, seed, fp8=False):
                         B[f"kv_full{st}"].arrive()
                     later(f"tkv{st}", land)
                 blk += 1
-    def issuer():
-        its, js, ns_it, bs = 0, 0, 0, 0
-        itp, jp, np_it, bp = 0, 0, 0, 0
-        while itp < len(items):
-            def can_qk():
-                if not (its < len(items) and bs <= bp + 1):
-                    return False
-                ib, st = ns_it & 1, bs % NS
-                return (js > 0 or B[f"q_full{ib}"].ready((ns_it >> 1) & 1)) and B[f"kv_full{st}"].ready((bs // NS) & 1)
-            def can_pv():
-                if not bp < bs:
-                    return False
-                ib, sb = np_it & 1, bp & 1
-                return B[f"p_full{sb}"].ready((bp >> 1) & 1) and (jp > 0 or B[f"o_empty{ib}"].ready(((np_it >> 1) & 1) ^ 1))
-            yield ("pred", lambda: can_qk() or can_pv())
-            if can_qk():
-                st, sb = bs % NS, bs & 1
-                assert stage.get(st) == bs, ("S from the wrong K", stage.get(st), bs)
-                assert Sbuf.get(sb) in (None, ("read", bs - 2)), ("S overwritten before read", Sbuf.get(sb), bs)
-                def qk(sb=sb, b=bs):
+    def issuer_qk():
+        # S^T of block b: its q (item start), its K, and the S buffer it
+        # reuses read out (P of block b - 2 written)
+        b = 0
+        for n_it, nk in enumerate(items):
+            ib = n_it & 1
+            for j in range(nk):
+                st, sb = b % NS, b & 1
+                if j == 0:
+                    yield ("wait", B[f"q_full{ib}"], (n_it >> 1) & 1)
+                yield ("wait", B[f"kv_full{st}"], (b // NS) & 1)
+                if b >= 2:
+                    yield ("wait", B[f"p_full{sb}"], ((b - 2) >> 1) & 1)
+                assert stage.get(st) == b, ("S from the wrong K", stage.get(st), b)
+                assert Sbuf.get(sb) in (None, ("read", b - 2)), ("S overwritten before read", Sbuf.get(sb), b)
+                def qk(sb=sb, b=b):
                     Sbuf[sb] = ("S", b)
                     B[f"s_full{sb}"].arrive()
-                later("mma", qk)
-                bs += 1; js += 1
-                if js == items[its]:
-                    later("mma", lambda ib=ns_it & 1: B[f"q_empty{ib}"].arrive())
-                    js = 0; ns_it += 1; its += 1
-            if can_pv():
-                ib, st, sb = np_it & 1, bp % NS, bp & 1
-                assert Pbuf.get(sb) == ("P", bp), (Pbuf.get(sb), bp)
-                assert stage.get(st) == bp
-                if jp == 0:
-                    assert Obuf.get(ib) in (None, ("read", np_it - 2)), ("O overwritten before read", Obuf.get(ib))
-                    Obuf[ib] = ("acc", np_it)
-                def pv(sb=sb, st=st, b=bp):
+                later("mma_qk", qk)
+                if j == nk - 1:
+                    later("mma_qk", lambda ib=ib: B[f"q_empty{ib}"].arrive())
+                b += 1
+                yield None
+    def issuer_pv():
+        # O^T += V^T P^T of block b: its P, and at an item start the O
+        # buffer it reuses read out
+        b = 0
+        for n_it, nk in enumerate(items):
+            ib = n_it & 1
+            for j in range(nk):
+                st, sb = b % NS, b & 1
+                yield ("wait", B[f"p_full{sb}"], (b >> 1) & 1)
+                if j == 0:
+                    yield ("wait", B[f"o_empty{ib}"], ((n_it >> 1) & 1) ^ 1)
+                assert Pbuf.get(sb) == ("P", b), (Pbuf.get(sb), b)
+                assert stage.get(st) == b
+                if j == 0:
+                    assert Obuf.get(ib) in (None, ("read", n_it - 2)), ("O overwritten before read", Obuf.get(ib))
+                    Obuf[ib] = ("acc", n_it)
+                def pv(sb=sb, st=st, b=b):
                     Pbuf[sb] = ("used", b)
                     pv_done[0] = b
                     B[f"p_empty{sb}"].arrive(); B[f"kv_empty{st}"].arrive()
-                later("mma", pv)
-                bp += 1; jp += 1
-                if jp == items[itp]:
-                    def of(ib=ib, it=np_it):
+                later("mma_pv", pv)
+                if j == nk - 1:
+                    def of(ib=ib, it=n_it):
                         Obuf[ib] = ("done", it)
                         B[f"o_full{ib}"].arrive()
-                    later("mma", of)
-                    jp = 0; np_it += 1; itp += 1
+                    later("mma_pv", of)
+                b += 1
+                yield None
     def softmax():
         blk = 0
         for n_it, nk in enumerate(items):
@@ -462,7 +467,7 @@ def run_decode(items, seed, fp8=False):
             stage[st] = blk
             B[f"kv_full{st}"].arrive()
             yield None
-    agents = {"p": producer(), "m": issuer(), "s": softmax()}
+    agents = {"p": producer(), "mq": issuer_qk(), "mp": issuer_pv(), "s": softmax()}
     if fp8:
         agents["w"] = widen()
     state = {k: None for k in agents}; done = set(); steps = 0
