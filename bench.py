@@ -81,6 +81,16 @@ def fwd_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def fwd_phases_label(n_dec_items: int, n_kvs_items: int) -> str:
+    """k_fwd and the phases its schedule uses, from the schedule header's
+    item counts."""
+    if n_kvs_items == 0:
+        return f"k_fwd (its decode phase: {n_dec_items} items; no KV-stationary items here)"
+    if n_dec_items == 0:
+        return f"k_fwd (its KV-stationary phase: {n_kvs_items} items; no decode items here)"
+    return f"k_fwd (decode phase: {n_dec_items} items, KV-stationary phase: {n_kvs_items} items)"
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per forward launch from a committed ncu summary, if it was
     taken on the current forward-kernel source; else None."""
@@ -652,6 +662,11 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     flags = mx.read_status(attn.ws.index, stream)
     if flags:
         raise RuntimeError(f"{name}: device status flags {flags:#x} after warm-up")
+    # which of the forward's phases this schedule uses (the schedule
+    # header's item counts: KV-stationary items, decode items)
+    hdr_off = mx.sched_layout(prob).header
+    sch_hdr = attn.ws.sched[hdr_off:hdr_off + 64].view(torch.int32).cpu()
+    n_kvs_items, n_dec_items = int(sch_hdr[0]), int(sch_hdr[5])
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
@@ -754,12 +769,13 @@ def run_sparse(name, args, rank, world, local_rank, cpu_budget_s):
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": fwd_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": fwd_gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(name),
-                "kernel": "k_fwd (its decode phase; no KV-stationary items here)",
+                "kernel": fwd_phases_label(n_dec_items, n_kvs_items),
                 "algorithmic_bytes_per_launch": unique_kv_bytes, "peak_source": peaks["src"] + " copy bandwidth"}
     else:
         pk = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": pk, "unit": "TFLOP/s",
-                "frac": fwd_tflops / pk, "traffic": recorded_traffic(name), "kernel": "k_fwd",
+                "frac": fwd_tflops / pk, "traffic": recorded_traffic(name),
+                "kernel": fwd_phases_label(n_dec_items, n_kvs_items),
                 "algorithmic_flops_per_launch": flops, "peak_source": peaks["src"] + " bf16 burst"}
     step_roof = {"hbm_frac": kv_gbs / peaks["hbm_gbs"], "tensor_frac": tflops / peaks["bf16_tflops"]}
     entry = {
