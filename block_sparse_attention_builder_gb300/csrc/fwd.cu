@@ -99,9 +99,9 @@ struct FwdArgs {
 // smem offsets from the 1024-aligned base
 constexpr uint32_t kOffKV = 0;                            // 2 stages x (K, V)
 constexpr uint32_t kOffQP = 2 * kStageBytes;              // 2 groups x q tile
-constexpr uint32_t kOffStg = kOffQP + 2 * kTileBytes;     // FP8 staging (K, V e4m3), 32 KB
+constexpr uint32_t kOffStg = kOffQP + 2 * kTileBytes;     // NVFP4 staging (K, V code and scale rows), 32 KB
 constexpr uint32_t kCtrlBf16 = kOffStg;
-constexpr uint32_t kCtrlFp8 = kOffStg + kTileBytes;
+constexpr uint32_t kCtrlFp8 = kOffStg + kTileBytes;  // widened caches (FP8 widens in place and leaves the staging tile unused)
 
 __device__ __forceinline__ int seq_of_block(const SeqInfo* seq, int B, int r) {
   int lo = 0, hi = B - 1;
